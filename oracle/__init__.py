@@ -1,0 +1,33 @@
+"""CPU oracle for lightning-indexer sparse attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or run
+anything in this package.  The product path (the CUDA library and its Python
+binding) never imports it and shares no code with it.
+
+Everything here is plain numpy in float64, written from the method's
+definition on the source pages, with no blocking, fusion or reordering beyond
+what that definition states.  Each function names the passage it follows.
+
+Pins (tests that tie this code to something other than itself) live in
+``tests/test_oracle_*.py``.  Every function below is pinned; none is
+"parity unpinned".
+"""
+
+from .lidx_oracle import (  # noqa: F401
+    round_to_storage,
+    hadamard_matrix,
+    hadamard_rotate,
+    visible_count,
+    indexer_scores,
+    topk_select,
+    block_pool,
+    block_select,
+    block_select_expanded,
+    attention_over,
+    sparse_attention_mla,
+    sparse_attention_gqa,
+    dense_attention_gqa,
+    dense_attention_mla,
+    decode_pipeline_mla,
+)
