@@ -1,0 +1,339 @@
+#!/usr/bin/env python3
+"""Throughput of one decode step of lightning-indexer sparse attention.
+
+Workload (one step): 64 decode queries, each over n_kv = 131072 cached tokens:
+score every key with the 64-head x 128-dim indexer (F16 key cache), select
+top_k = 2048 keys per query, and run MLA attention (128 heads, 576-wide bf16
+latent, 512-wide value) over the selected keys.  Synthetic, seeded data.
+
+Prints ONE JSON line (rank 0):
+  value       queries/s, device-resident inputs, CUDA events over K steps
+  e2e         the same metric through the public API with pinned host buffers:
+              per step H2D of the step's query inputs and D2H of its output
+  roofline    the dominant kernel (the indexer key-cache scan) against the
+              measured HBM copy bandwidth
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+
+`--impl reference` times the CPU oracle instead (the reference arm).
+Multi-GPU (torchrun): each rank runs its own 64-query batch (weak scaling),
+no data-path collective; the step time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn decode queries/s at n_kv=128K,top_k=2048; key-cache GB/s vs HBM peak"
+UNIT = "queries/s"
+WORKLOAD = "decode_mla_64x131072"
+
+# DRAM bytes per launch of the scorer from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by the SHA-256 of the kernel source it was taken on.
+# A source change makes the figure stale and the bench reports traffic = null.
+NCU_TRAFFIC = {}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def _threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_oracle_queries(wl, rows):
+    """Run the CPU oracle (score -> select -> attend) for the given decode rows; return (seconds, selections)."""
+    import numpy as np
+    import torch
+    import oracle as O
+    sels = {}
+    inputs = []
+    for r in rows:
+        row0, n = wl.row0(r), wl.n_kv_host[r]
+        inputs.append((r, wl.q_idx[r].to("cpu", torch.float64).numpy(), wl.w[r].to("cpu", torch.float64).numpy(),
+                       wl.k_idx[row0:row0 + n].to("cpu", torch.float64).numpy(),
+                       wl.q_attn[r].to("cpu", torch.float64).numpy(),
+                       wl.k_attn[row0:row0 + n].to("cpu", torch.float64).numpy(), n))
+    t0 = time.perf_counter()
+    for r, q, w, k, qa, lat, n in inputs:
+        s, sel, out = O.decode_pipeline_mla(q, w, k, n, wl.top_k, qa, lat, wl.scale, wl.dv)
+        sels[r] = (s, sel)
+    return time.perf_counter() - t0, sels
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle, as it stands, on bounded samples of the workload."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import torch
+    from lightning_indexer_top_gb300 import workloads
+    wl = workloads.make("headline", device="cpu", batch_override=1)
+    for _ in range(args.warmup):
+        cpu_oracle_queries(wl, [0])
+    t = 0.0
+    for _ in range(args.steps):
+        dt, _ = cpu_oracle_queries(wl, [0])
+        t += dt
+    v = args.steps / t
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) inputs)",
+            "config": {"workload": WORKLOAD, "sample": "1 query of the workload per step",
+                       "top_k": 2048, "n_kv": 131072},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": _threads(), "kind": "oracle",
+                             "sample": "1 decode query (n_kv=131072) per step: score, top-k, MLA attention"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-sample", type=int, default=4, help="decode queries the CPU baseline runs")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import lightning_indexer_top_gb300 as L
+    from lightning_indexer_top_gb300 import workloads
+    from lightning_indexer_top_gb300.pipeline import SparseAttentionStep
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    L.build() if rank == 0 else None
+    if dist:
+        dist.barrier()
+    L.load()
+
+    wl = workloads.make("headline", device=f"cuda:{local}")
+    step = SparseAttentionStep(wl, out_dtype=torch.bfloat16)
+    stream = torch.cuda.current_stream()
+
+    # per-kernel events: score / select / attend of every timed step
+    def timed_step(ev):
+        ev[0].record(stream)
+        step.score()
+        ev[1].record(stream)
+        step.select()
+        ev[2].record(stream)
+        step.attend()
+        ev[3].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step.run()
+    torch.cuda.synchronize()
+    L.idx_device_status(reset=True)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        timed_step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    status = L.idx_device_status(reset=True)
+    if status != 0:
+        raise RuntimeError(f"device status {status} during the timed region")
+
+    ms_total = t_start.elapsed_time(t_end)
+    ms_score = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ms_select = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    ms_attend = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    ms_step = ms_total / args.steps
+    if dist:
+        t = torch.tensor([ms_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t)
+
+    # ---- end to end through the public API with pinned host buffers
+    host_in = [wl.q_idx.cpu().pin_memory(), wl.w.cpu().pin_memory(), wl.q_attn.cpu().pin_memory()]
+    dev_in = [wl.q_idx, wl.w, wl.q_attn]
+    host_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        step.run()
+        host_out.copy_(step.out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    if dist:
+        t = torch.tensor([ms_e2e], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t)
+
+    if rank != 0:
+        dist.destroy_process_group() if dist else None
+        return
+
+    B = wl.B
+    n_kv_total = sum(wl.n_kv_host)
+    key_bytes = n_kv_total * wl.d * 2
+    # scorer's algorithmic bytes per launch: every key row read once, one f32 score written per
+    # key, the queries and weights read once
+    score_bytes = key_bytes + n_kv_total * 4 + B * wl.H * wl.d * 2 + B * wl.H * 4
+    hbm, bf16, peak_kind = _peaks()
+    achieved = score_bytes / (ms_score * 1e-3) / 1e9
+    src = os.path.join(ROOT, "lightning_indexer_top_gb300", "csrc", "k_score_tc.cu")
+    tr = NCU_TRAFFIC.get(_sha(src))
+    value = ws * B / (ms_step * 1e-3)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16/bf16 (f32 accumulate)",
+        "data": "synthetic (seeded N(0,1) q/k/latent, w ~ N(0,1/64))",
+        "config": {"workload": WORKLOAD, "queries_per_gpu": B, "n_kv": 131072, "top_k": 2048,
+                   "indexer": "64 heads x 128, F16 cache", "attention": "MLA 128 heads, 576/512 bf16",
+                   "l2": "inputs larger than L2 (2.1 GB key cache, 9.7 GB latent), no flush"},
+        "key_cache_gbs": key_bytes / ((ms_score + ms_select) * 1e-3) / 1e9,
+        "ms_per_kernel": {"score": ms_score, "topk": ms_select, "attention": ms_attend},
+        "roofline": {"bound": "hbm", "kernel": "idx_score (key-cache scan)", "achieved": achieved, "peak": hbm,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": tr, "algorithmic_bytes_per_launch": score_bytes},
+        "e2e": {"value": ws * B / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        rows = list(range(min(args.cpu_sample, B)))
+        dt, sels = cpu_oracle_queries(wl, rows)
+        same = []
+        for r in rows:
+            ns = int(step.n_sel[r])
+            same.append(sorted(step.idx[r, :ns].tolist()) == sels[r][1].tolist())
+        line["cpu_baseline"] = {"value": len(rows) / dt, "unit": UNIT, "cores": _threads(), "kind": "oracle",
+                                "sample": f"{len(rows)} of the {B} decode queries (n_kv=131072 each), "
+                                          "float64 score, top-k and MLA attention"}
+        line["parity_sample"] = {"rows": len(rows), "identical_sets": int(sum(same))}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,235 @@
+/*
+ * lidx.h -- C ABI of the lightning-indexer sparse-attention library (liblidx.so).
+ *
+ * The path: score every visible cached key with the lightning indexer, select
+ * the top_k keys per query row, and run softmax attention over only those
+ * keys.  Also the block-pooled variant: one mean-pooled key per block of C
+ * positions, whole blocks plus the incomplete tail.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Pointers named in the argument lists are DEVICE pointers unless said
+ *    otherwise.  The caller owns every buffer; the library allocates nothing,
+ *    synchronises nothing and only enqueues kernels on `stream` (NULL = the
+ *    legacy default stream).  Calls are asynchronous.
+ *  - Arguments are validated on the host before anything is launched.  A bad
+ *    argument returns IDX_ERR_INVALID_ARG (or IDX_ERR_UNSUPPORTED for a valid
+ *    but unimplemented shape/dtype) and launches nothing; idx_last_error()
+ *    then returns a message for the calling thread.  Nothing aborts.
+ *  - A failed launch returns IDX_ERR_CUDA.  Data-dependent faults the host
+ *    cannot see (an index outside its sequence, a key row outside the
+ *    allocation, a bounded wait that ran out) are never followed: the kernel
+ *    skips the access and records the fault in a device status word, read by
+ *    idx_device_status().
+ *  - Element strides and row strides are in ELEMENTS of the named dtype.
+ *  - Query rows: a batch has n_seq sequences of n_q_per_seq query rows each;
+ *    query row r = b * n_q_per_seq + t belongs to sequence b.
+ *  - Key positions are relative to the sequence: position j of sequence b is
+ *    cache row kv_start[b] + j (or b * kv_seq_stride + j).  Indices returned
+ *    by idx_topk are such positions.
+ */
+#ifndef LIDX_H
+#define LIDX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, without requiring the CUDA headers. */
+typedef struct CUstream_st* idx_stream_t;
+
+typedef enum idx_status {
+    IDX_OK = 0,
+    IDX_ERR_INVALID_ARG = 1,
+    IDX_ERR_UNSUPPORTED = 2,
+    IDX_ERR_CUDA = 3,
+    IDX_ERR_TIMEOUT = 4,      /* device status only: a bounded wait ran out */
+    IDX_ERR_DEVICE_BOUNDS = 5 /* device status only: an out-of-range index or row was skipped */
+} idx_status;
+
+typedef enum idx_dtype {
+    IDX_F32 = 0,
+    IDX_F16 = 1,
+    IDX_BF16 = 2
+} idx_dtype;
+
+/*
+ * Batch geometry shared by the calls below.
+ *   n_seq          B >= 0 sequences.
+ *   n_q_per_seq    T >= 1 query rows per sequence (decode: 1).
+ *   n_kv           device int32[B]: cached tokens of sequence b.  A decode
+ *                  query's own key is written to the cache before scoring, so
+ *                  n_kv counts it (ik_llama.cpp PR #2058, commit
+ *                  "decode-correct via persistent indexer-K cache").
+ *   kv_start       device int32[B] or NULL: cache row of position 0 of
+ *                  sequence b.  NULL means b * kv_seq_stride.
+ *   kv_seq_stride  rows between sequences when kv_start is NULL.
+ *   q_pos          device int32[B*T] or NULL: position of each query row.
+ *                  Key j is visible to row r iff j < n_kv[b] and, when q_pos
+ *                  is given, j <= q_pos[r] (the causal mask, ik_llama.cpp PR
+ *                  #2058, commit "Add GLM-5.2/DeepSeek-V3.2 DSA lightning
+ *                  indexer").  n_vis(r) = min(q_pos[r] + 1, n_kv[b]), >= 0.
+ *   max_n_kv       host-side bound: every n_kv[b] <= max_n_kv.  It sizes the
+ *                  grids; a larger n_kv[b] is clamped to it and flagged.
+ */
+typedef struct idx_batch {
+    int32_t n_seq;
+    int32_t n_q_per_seq;
+    const int32_t* n_kv;
+    const int32_t* kv_start;
+    int64_t kv_seq_stride;
+    const int32_t* q_pos;
+    int32_t max_n_kv;
+} idx_batch;
+
+/*
+ * idx_hadamard -- rotate rows by the orthonormal Sylvester Walsh-Hadamard
+ * matrix H_d (natural order, entries (-1)^popcount(i&j)/sqrt(d)): y = H_d x.
+ * Score preserving: (Hq).(Hk) = q.k (ik_llama.cpp PR #2058, commit "Add
+ * GLM-5.2/DeepSeek-V3.2 DSA lightning indexer"; applied to cached keys and to
+ * queries in commit "decode-correct via persistent indexer-K cache").
+ *   x, y       device [n_rows] rows of d elements, row r at x + r*row_stride
+ *              (y likewise).  y may equal x (in place); other overlap is
+ *              not allowed.
+ *   dtype      storage type of x and y; the rotation runs in f32 and is
+ *              rounded once (nearest even) to dtype.
+ *   d          32, 64, 128 or 256.
+ * Errors: INVALID_ARG for x or y NULL with n_rows > 0, n_rows < 0,
+ * unsupported d, row_stride < d, or x, y not 16-byte aligned or
+ * row_stride*size not a multiple of 16 bytes.
+ */
+idx_status idx_hadamard(const void* x, void* y, idx_dtype dtype, int64_t n_rows, int32_t d,
+                        int64_t row_stride, idx_stream_t stream);
+
+/*
+ * idx_score -- lightning-indexer scores
+ *     s[r, j] = sum_h w[r, h] * max(0, q[r, h, :] . k[j, :])      (f32 out)
+ * for every visible key j of every query row r, accumulated in f32 (ik_llama_opt
+ * commit log, "openpangu: DSA lightning indexer + SWA schedule"; ReLU per head
+ * before the head sum: llama.cpp commit c88c916636, QSA commit message).
+ *   q          [B*T, H, d] contiguous, q_dtype.
+ *   w          f32 [B*T, H]: per-row, per-head weights (the indexer projection
+ *              of the token; it carries every scale).
+ *   k          one shared (MQA) key row of d elements per cached token, row i
+ *              at k + i*k_row_stride; k_rows = rows in the allocation.
+ *   block_size 0 or 1: token keys, row r sees n_vis(r) keys.  C > 1: k holds
+ *              pooled block keys (idx_block_pool) addressed by kv_start /
+ *              kv_seq_stride in BLOCK rows, and row r sees floor(n_vis(r)/C)
+ *              blocks (only complete blocks are scored).
+ *   scores     f32, row r at scores + r*score_row_stride; entries j of
+ *              visible keys are written, the rest of the row is untouched.
+ *   workspace  may be NULL when idx_workspace_size(IDX_OP_SCORE, ...) is 0.
+ * Supported: q_dtype, k_dtype in {F32, F16, BF16}, H <= 128, d <= 256 and
+ * H*d <= 16384.  H = 64, d = 128 with F16/BF16 keys runs on the tensor cores.
+ */
+idx_status idx_score(const void* q, idx_dtype q_dtype, const float* w, int32_t n_heads,
+                     int32_t head_dim, const void* k, idx_dtype k_dtype, int64_t k_row_stride,
+                     int64_t k_rows, idx_batch batch, int32_t block_size, float* scores,
+                     int64_t score_row_stride, void* workspace, size_t workspace_bytes,
+                     idx_stream_t stream);
+
+/*
+ * idx_block_pool -- mean-pooled raw key of every complete block
+ *     p[b, beta, :] = (1/C) * sum_{t=beta*C}^{beta*C+C-1} k_raw[row(b, t), :]
+ * for beta < floor(n_kv[b] / C).  Blocks are cuts of the position line from
+ * the sequence's first position, and pooling takes the raw key, before any
+ * norm or rotation (llama.cpp commit c88c916636, QSA commit message;
+ * llama-memory-hybrid-idx.h, kpool_layout).  Sums in f32.
+ *   k_raw      rows addressed by batch.kv_start / kv_seq_stride, k_dtype.
+ *   pooled     f32, block beta of sequence b at
+ *              pooled + (b*pool_seq_stride + beta)*head_dim.
+ * Errors: INVALID_ARG for block_size < 1, pool_seq_stride < max_n_kv/C.
+ */
+idx_status idx_block_pool(const void* k_raw, idx_dtype k_dtype, int64_t k_row_stride,
+                          int64_t k_rows, idx_batch batch, int32_t block_size, int32_t head_dim,
+                          float* pooled, int64_t pool_seq_stride, idx_stream_t stream);
+
+/*
+ * idx_topk -- per-row selection, positions ascending.
+ * Token mode (block_size 0 or 1): K = min(top_k, n_vis(r)) positions with
+ *   the largest scores; equal scores: the lower position wins; -0 == +0.
+ *   ("ggml_top_k(min(top_k, n_tokens))", ik_llama.cpp PR #2058.)
+ * Block mode (block_size C > 1; scores are block scores from idx_score in
+ *   block mode): the best min(floor(top_k/C), n_cb) complete blocks (lower
+ *   block index wins ties), every token of those blocks, plus every tail
+ *   token [n_cb*C, n_vis) -- exactly dense when n_vis <= top_k + C - 1
+ *   (llama.cpp commit c88c916636, QSA commit message).
+ *   idx        int32, row r at idx + r*idx_row_stride.  Capacity: top_k in
+ *              token mode, floor(top_k/C)*C + C - 1 in block mode; entries
+ *              past the selection up to that capacity are set to -1.
+ *   n_sel      int32[B*T] or NULL: number of positions selected per row.
+ * Scores must be finite (a NaN is ordered like a value, never trusted).
+ */
+idx_status idx_topk(const float* scores, int64_t score_row_stride, idx_batch batch,
+                    int32_t top_k, int32_t block_size, int32_t* idx, int64_t idx_row_stride,
+                    int32_t* n_sel, void* workspace, size_t workspace_bytes,
+                    idx_stream_t stream);
+
+/*
+ * sparse_attn_decode / sparse_attn_prefill -- softmax attention of each
+ * query row over only its selected keys:
+ *     l[h, j] = scale * q[r, h, :] . K[j, g(h), :],  p = softmax_j(l),
+ *     out[r, h, :] = sum_j p[h, j] * V[j, g(h), :],   g(h) = h / (Hq / Hkv)
+ * for j in idx[r, 0 : n_sel[r]] ("Gather OpenPangu DSA decode reads" and
+ * "Gather OpenPangu sparse prefill attention", ik_llama_opt commit log).
+ *   q          [B*T, Hq, dk] contiguous, dtype.
+ *   k          row i at k + i*kv_row_stride holds [Hkv, dk] contiguous.
+ *   v          row i at v + i*v_row_stride holds [Hkv, dv]; NULL selects the
+ *              MLA latent form: Hkv must be 1 and V = the first dv columns
+ *              of the same K row ("openpangu: MLA-latent KV cache").
+ *   kv_rows    rows in the K (and V) allocation.
+ *   idx/n_sel  as written by idx_topk (positions of sequence b, -1 padding
+ *              ignored); n_sel[r] in [1, idx_row_stride].  A row with
+ *              n_sel[r] == 0 gets zeros.
+ *   out        [B*T, Hq, dv] contiguous, out_dtype (F32 or BF16).
+ *   workspace  idx_workspace_size(IDX_OP_ATTN, ...) bytes (16-byte aligned)
+ *              or NULL when that is 0; used for split-key partial results.
+ * dtype in {F32, F16, BF16}; dk <= 576, dv <= 512, Hq % Hkv == 0.  The two
+ * entry points compute the same function; decode is tuned for few rows with
+ * long selections, prefill for many rows.
+ */
+idx_status sparse_attn_decode(const void* q, idx_dtype dtype, int32_t n_q_heads, int32_t n_kv_heads,
+                              int32_t dk, int32_t dv, const void* k, const void* v,
+                              int64_t kv_row_stride, int64_t v_row_stride, int64_t kv_rows,
+                              idx_batch batch, const int32_t* idx, int64_t idx_row_stride,
+                              const int32_t* n_sel, float scale, void* out, idx_dtype out_dtype,
+                              void* workspace, size_t workspace_bytes, idx_stream_t stream);
+
+idx_status sparse_attn_prefill(const void* q, idx_dtype dtype, int32_t n_q_heads, int32_t n_kv_heads,
+                               int32_t dk, int32_t dv, const void* k, const void* v,
+                               int64_t kv_row_stride, int64_t v_row_stride, int64_t kv_rows,
+                               idx_batch batch, const int32_t* idx, int64_t idx_row_stride,
+                               const int32_t* n_sel, float scale, void* out, idx_dtype out_dtype,
+                               void* workspace, size_t workspace_bytes, idx_stream_t stream);
+
+/* Operation selectors for idx_workspace_size. */
+enum { IDX_OP_SCORE = 0, IDX_OP_TOPK = 1, IDX_OP_ATTN_DECODE = 2, IDX_OP_ATTN_PREFILL = 3 };
+
+/*
+ * idx_workspace_size -- bytes of device workspace an operation needs for the
+ * given sizes (0 when none).  n_rows = B*T query rows; the other arguments are
+ * the same as the call's.  Pure host arithmetic; never fails (returns 0 for
+ * nonsense sizes, which the call itself then rejects).
+ */
+size_t idx_workspace_size(int32_t op, int64_t n_rows, int32_t max_n_kv, int32_t top_k,
+                          int32_t n_q_heads, int32_t dv);
+
+/* Message for the last non-OK status returned on the calling thread. */
+const char* idx_last_error(void);
+
+/*
+ * idx_device_status -- synchronise the current device and return the first
+ * data-dependent fault recorded by a kernel since the last reset
+ * (IDX_ERR_DEVICE_BOUNDS, IDX_ERR_TIMEOUT) or IDX_OK; reset != 0 clears it.
+ * Returns IDX_ERR_CUDA if the synchronisation itself fails.
+ */
+idx_status idx_device_status(int32_t reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIDX_H */

@@ -1,0 +1,265 @@
+"""lightning_indexer_top_gb300 -- lightning-indexer sparse attention on GB300.
+
+A thin ctypes binding over ``liblidx.so`` (C ABI in ``include/lidx.h``).  The
+functions here only marshal torch tensors into pointers, sizes and the current
+CUDA stream; every step of the computation runs in the library's kernels.
+There is no CPU fallback: if the library is missing or fails to load, every
+call raises.
+
+Build with ``lightning_indexer_top_gb300.build()`` (nvcc, sm_103a).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from ._build import LIB as _LIB_PATH
+from ._build import build  # noqa: F401
+
+__all__ = [
+    "Batch", "LidxError", "build", "load", "idx_hadamard", "idx_score", "idx_block_pool",
+    "idx_topk", "sparse_attn_decode", "sparse_attn_prefill", "idx_workspace_size",
+    "idx_device_status", "topk_capacity",
+]
+
+IDX_OK, IDX_ERR_INVALID_ARG, IDX_ERR_UNSUPPORTED, IDX_ERR_CUDA, IDX_ERR_TIMEOUT, IDX_ERR_DEVICE_BOUNDS = range(6)
+IDX_F32, IDX_F16, IDX_BF16 = 0, 1, 2
+IDX_OP_SCORE, IDX_OP_TOPK, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL = 0, 1, 2, 3
+
+_DTYPES = {torch.float32: IDX_F32, torch.float16: IDX_F16, torch.bfloat16: IDX_BF16}
+
+
+class LidxError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"lidx status {status}: {msg}")
+        self.status = status
+
+
+class _Batch(ctypes.Structure):
+    _fields_ = [
+        ("n_seq", ctypes.c_int32),
+        ("n_q_per_seq", ctypes.c_int32),
+        ("n_kv", ctypes.c_void_p),
+        ("kv_start", ctypes.c_void_p),
+        ("kv_seq_stride", ctypes.c_int64),
+        ("q_pos", ctypes.c_void_p),
+        ("max_n_kv", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load liblidx.so (once) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run lightning_indexer_top_gb300.build() first")
+    lib = ctypes.CDLL(path)
+    P, I32, I64, F, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    sigs = {
+        "idx_hadamard": [P, P, I32, I64, I32, I64, P],
+        "idx_score": [P, I32, P, I32, I32, P, I32, I64, I64, _Batch, I32, P, I64, P, SZ, P],
+        "idx_block_pool": [P, I32, I64, I64, _Batch, I32, I32, P, I64, P],
+        "idx_topk": [P, I64, _Batch, I32, I32, P, I64, P, P, SZ, P],
+        "sparse_attn_decode": [P, I32, I32, I32, I32, I32, P, P, I64, I64, I64, _Batch, P, I64, P, F,
+                               P, I32, P, SZ, P],
+        "sparse_attn_prefill": [P, I32, I32, I32, I32, I32, P, P, I64, I64, I64, _Batch, P, I64, P, F,
+                                P, I32, P, SZ, P],
+        "idx_workspace_size": [I32, I64, I32, I32, I32, I32],
+        "idx_last_error": [],
+        "idx_device_status": [I32],
+    }
+    for name, args in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.idx_workspace_size.restype = ctypes.c_size_t
+    lib.idx_last_error.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != IDX_OK:
+        raise LidxError(status, load().idx_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}") from None
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("lidx operates on CUDA tensors only")
+
+
+@dataclass
+class Batch:
+    """Batch geometry (see idx_batch in include/lidx.h).
+
+    n_kv:      int32 CUDA tensor [B], cached tokens per sequence.
+    n_q_per_seq: query rows per sequence (decode: 1).
+    max_n_kv:  host bound on every n_kv[b].
+    kv_start:  optional int32 CUDA tensor [B]: cache row of position 0.
+    kv_seq_stride: rows between sequences when kv_start is None.
+    q_pos:     optional int32 CUDA tensor [B*T]: causal position per query row.
+    """
+
+    n_kv: torch.Tensor
+    n_q_per_seq: int
+    max_n_kv: int
+    kv_start: Optional[torch.Tensor] = None
+    kv_seq_stride: int = 0
+    q_pos: Optional[torch.Tensor] = None
+
+    @property
+    def n_seq(self) -> int:
+        return int(self.n_kv.numel())
+
+    @property
+    def n_rows(self) -> int:
+        return self.n_seq * self.n_q_per_seq
+
+    def c(self) -> _Batch:
+        for t in (self.n_kv, self.kv_start, self.q_pos):
+            if t is not None and (t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous()):
+                raise ValueError("batch arrays must be contiguous int32 CUDA tensors")
+        return _Batch(self.n_seq, self.n_q_per_seq, _ptr(self.n_kv), _ptr(self.kv_start),
+                      self.kv_seq_stride, _ptr(self.q_pos), self.max_n_kv)
+
+
+def topk_capacity(top_k: int, block_size: int = 0) -> int:
+    """Row capacity idx_topk writes: top_k, or floor(top_k/C)*C + C - 1 in block mode."""
+    if block_size > 1:
+        return (top_k // block_size) * block_size + block_size - 1
+    return top_k
+
+
+def idx_hadamard(x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Rotate the rows (last dim) of x by the orthonormal Hadamard matrix into `out`
+    (in place when out is None or is x)."""
+    out = x if out is None else out
+    _need_cuda(x, out)
+    if not x.is_contiguous() or not out.is_contiguous() or out.shape != x.shape or out.dtype != x.dtype:
+        raise ValueError("x and out must be contiguous tensors of the same shape and dtype")
+    d = x.shape[-1]
+    rows = x.numel() // d
+    _check(load().idx_hadamard(_ptr(x), _ptr(out), _dtype(x), rows, d, d, _stream(x.device)))
+    return out
+
+
+def idx_workspace_size(op: int, n_rows: int, max_n_kv: int, top_k: int, n_q_heads: int = 0, dv: int = 0) -> int:
+    return int(load().idx_workspace_size(op, n_rows, max_n_kv, top_k, n_q_heads, dv))
+
+
+def idx_score(q: torch.Tensor, w: torch.Tensor, k: torch.Tensor, batch: Batch, *, block_size: int = 0,
+              scores: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Indexer scores [B*T, keys] f32.  q [B*T, H, d]; w [B*T, H] f32; k [rows, d] (key cache
+    or pooled keys when block_size > 1)."""
+    _need_cuda(q, w, k, scores, workspace)
+    rows, H, d = q.shape
+    assert rows == batch.n_rows and w.shape == (rows, H) and w.dtype == torch.float32
+    assert q.is_contiguous() and w.is_contiguous() and k.stride(-1) == 1
+    keys = batch.max_n_kv // block_size if block_size > 1 else batch.max_n_kv
+    if scores is None:
+        scores = torch.empty(rows, max(keys, 1), device=q.device, dtype=torch.float32)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().idx_score(_ptr(q), _dtype(q), _ptr(w), H, d, _ptr(k), _dtype(k), k.stride(0),
+                            k.shape[0], batch.c(), block_size, _ptr(scores), scores.stride(0),
+                            _ptr(workspace), ws_bytes, _stream(q.device)))
+    return scores
+
+
+def idx_block_pool(k_raw: torch.Tensor, batch: Batch, block_size: int, *, pool_seq_stride: Optional[int] = None,
+                   pooled: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Mean-pooled complete blocks, f32 [B, pool_seq_stride, d]."""
+    _need_cuda(k_raw, pooled)
+    d = k_raw.shape[-1]
+    if pool_seq_stride is None:
+        pool_seq_stride = max(batch.max_n_kv // block_size, 1)
+    if pooled is None:
+        pooled = torch.zeros(batch.n_seq, pool_seq_stride, d, device=k_raw.device, dtype=torch.float32)
+    _check(load().idx_block_pool(_ptr(k_raw), _dtype(k_raw), k_raw.stride(0), k_raw.shape[0], batch.c(),
+                                 block_size, d, _ptr(pooled), pool_seq_stride, _stream(k_raw.device)))
+    return pooled
+
+
+def idx_topk(scores: torch.Tensor, batch: Batch, top_k: int, *, block_size: int = 0,
+             idx: Optional[torch.Tensor] = None, n_sel: Optional[torch.Tensor] = None,
+             workspace: Optional[torch.Tensor] = None):
+    """Selected positions (ascending, -1 padded) and their count per row."""
+    _need_cuda(scores, idx, n_sel, workspace)
+    rows = batch.n_rows
+    cap = topk_capacity(top_k, block_size)
+    if idx is None:
+        idx = torch.empty(rows, cap, device=scores.device, dtype=torch.int32)
+    if n_sel is None:
+        n_sel = torch.empty(rows, device=scores.device, dtype=torch.int32)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().idx_topk(_ptr(scores), scores.stride(0), batch.c(), top_k, block_size, _ptr(idx),
+                           idx.stride(0), _ptr(n_sel), _ptr(workspace), ws_bytes, _stream(scores.device)))
+    return idx, n_sel
+
+
+def _attn(fn_name, q, k, v, batch, idx, n_sel, scale, out, out_dtype, workspace, n_kv_heads, dv):
+    _need_cuda(q, k, v, idx, n_sel, out, workspace)
+    rows, Hq, dk = q.shape
+    assert rows == batch.n_rows and q.is_contiguous()
+    if v is None:
+        hkv, dv = 1, (dv if dv is not None else 512)
+        kv_row_stride = k.stride(0)
+        v_row_stride = 0
+    else:
+        hkv = n_kv_heads if n_kv_heads is not None else k.shape[1]
+        dv = v.shape[-1]
+        kv_row_stride = k.stride(0)
+        v_row_stride = v.stride(0)
+    if out is None:
+        out = torch.empty(rows, Hq, dv, device=q.device, dtype=out_dtype)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    fn = getattr(load(), fn_name)
+    _check(fn(_ptr(q), _dtype(q), Hq, hkv, dk, dv, _ptr(k), _ptr(v), kv_row_stride, v_row_stride,
+              k.shape[0], batch.c(), _ptr(idx), idx.stride(0), _ptr(n_sel), float(scale), _ptr(out),
+              _dtype(out), _ptr(workspace), ws_bytes, _stream(q.device)))
+    return out
+
+
+def sparse_attn_decode(q, k, v, batch, idx, n_sel, scale, *, out=None, out_dtype=torch.float32,
+                       workspace=None, n_kv_heads=None, dv=None):
+    """Attention over the selected keys.  q [B*T, Hq, dk]; k [rows, Hkv, dk] (or the MLA latent
+    [rows, 576] with v=None and dv=512); v [rows, Hkv, dv] or None."""
+    return _attn("sparse_attn_decode", q, k, v, batch, idx, n_sel, scale, out, out_dtype, workspace,
+                 n_kv_heads, dv)
+
+
+def sparse_attn_prefill(q, k, v, batch, idx, n_sel, scale, *, out=None, out_dtype=torch.float32,
+                        workspace=None, n_kv_heads=None, dv=None):
+    """Same function as sparse_attn_decode, tuned for many query rows."""
+    return _attn("sparse_attn_prefill", q, k, v, batch, idx, n_sel, scale, out, out_dtype, workspace,
+                 n_kv_heads, dv)
+
+
+def idx_device_status(reset: bool = True) -> int:
+    """Synchronise and return the device fault word (0 = none)."""
+    return int(load().idx_device_status(1 if reset else 0))

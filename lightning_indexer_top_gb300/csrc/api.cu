@@ -1,0 +1,301 @@
+// C-ABI entry points of liblidx: host-side argument validation, kernel
+// dispatch and error reporting.  Nothing here allocates device memory or
+// synchronises, except idx_device_status(), which is documented to.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <cmath>
+#include <mutex>
+#include <string>
+
+#include "lidx_internal.cuh"
+
+namespace lidx {
+namespace {
+
+thread_local std::string t_last_error;
+
+idx_status fail(idx_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return s;
+}
+
+idx_status from_cuda(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return IDX_OK;
+    if (e == cudaErrorNotSupported) return fail(IDX_ERR_UNSUPPORTED, "%s: unsupported shape", what);
+    return fail(IDX_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// device status word: first data-dependent fault any kernel recorded
+__device__ int g_device_status = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+// device address of g_device_status on the current device (looked up once per device)
+int* status_ptr() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+bool valid_dtype(int t) { return t == IDX_F32 || t == IDX_F16 || t == IDX_BF16; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+idx_status check_batch(const idx_batch& b, const char* what) {
+    if (b.n_seq < 0) return fail(IDX_ERR_INVALID_ARG, "%s: n_seq < 0", what);
+    if (b.n_q_per_seq < 1) return fail(IDX_ERR_INVALID_ARG, "%s: n_q_per_seq < 1", what);
+    if (b.max_n_kv < 0) return fail(IDX_ERR_INVALID_ARG, "%s: max_n_kv < 0", what);
+    if (b.n_seq > 0 && !b.n_kv) return fail(IDX_ERR_INVALID_ARG, "%s: n_kv is NULL", what);
+    if (!b.kv_start && b.kv_seq_stride < 0)
+        return fail(IDX_ERR_INVALID_ARG, "%s: kv_seq_stride < 0", what);
+    if ((int64_t)b.n_seq * b.n_q_per_seq > (int64_t)INT32_MAX)
+        return fail(IDX_ERR_INVALID_ARG, "%s: more than 2^31-1 query rows", what);
+    return IDX_OK;
+}
+
+Geom make_geom(const idx_batch& b) {
+    Geom g;
+    g.B = b.n_seq;
+    g.T = b.n_q_per_seq;
+    g.n_kv = b.n_kv;
+    g.kv_start = b.kv_start;
+    g.kv_seq_stride = b.kv_seq_stride;
+    g.q_pos = b.q_pos;
+    g.max_n_kv = b.max_n_kv;
+    g.status = status_ptr();
+    return g;
+}
+
+idx_status attn_common(const char* what, const void* q, idx_dtype dtype, int32_t Hq, int32_t Hkv,
+                       int32_t dk, int32_t dv, const void* k, const void* v, int64_t kv_row_stride,
+                       int64_t v_row_stride, int64_t kv_rows, idx_batch batch, const int32_t* idx,
+                       int64_t idx_row_stride, const int32_t* n_sel, float scale, void* out,
+                       idx_dtype out_dtype, void* ws, size_t ws_bytes, cudaStream_t st) {
+    (void)ws;
+    (void)ws_bytes;
+    idx_status s = check_batch(batch, what);
+    if (s != IDX_OK) return s;
+    const int64_t rows = (int64_t)batch.n_seq * batch.n_q_per_seq;
+    if (!valid_dtype(dtype)) return fail(IDX_ERR_INVALID_ARG, "%s: bad dtype", what);
+    if (out_dtype != IDX_F32 && out_dtype != IDX_BF16)
+        return fail(IDX_ERR_INVALID_ARG, "%s: out_dtype must be F32 or BF16", what);
+    if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+        return fail(IDX_ERR_INVALID_ARG, "%s: need Hq, Hkv >= 1 and Hq %% Hkv == 0", what);
+    if (dk < 1 || dk > 576 || dv < 1 || dv > 512)
+        return fail(IDX_ERR_INVALID_ARG, "%s: need 1 <= dk <= 576 and 1 <= dv <= 512", what);
+    if (!v && (Hkv != 1 || dv > dk))
+        return fail(IDX_ERR_INVALID_ARG, "%s: latent form (v == NULL) needs Hkv == 1, dv <= dk", what);
+    if (kv_row_stride < (int64_t)Hkv * dk)
+        return fail(IDX_ERR_INVALID_ARG, "%s: kv_row_stride < Hkv*dk", what);
+    if (v && v_row_stride < (int64_t)Hkv * dv)
+        return fail(IDX_ERR_INVALID_ARG, "%s: v_row_stride < Hkv*dv", what);
+    if (kv_rows < 0) return fail(IDX_ERR_INVALID_ARG, "%s: kv_rows < 0", what);
+    if (idx_row_stride < 1) return fail(IDX_ERR_INVALID_ARG, "%s: idx_row_stride < 1", what);
+    if (!std::isfinite(scale)) return fail(IDX_ERR_INVALID_ARG, "%s: scale not finite", what);
+    if (rows == 0) return IDX_OK;
+    if (!q || !k || !idx || !n_sel || !out)
+        return fail(IDX_ERR_INVALID_ARG, "%s: NULL q/k/idx/n_sel/out", what);
+    const Geom g = make_geom(batch);
+    return from_cuda(launch_attn_generic(q, dtype, Hq, Hkv, dk, dv, k, v, kv_row_stride,
+                                         v_row_stride, kv_rows, g, idx, idx_row_stride, n_sel,
+                                         scale, out, out_dtype, st),
+                     what);
+}
+
+}  // namespace
+
+int sm_count() {
+    const int dev = current_device();
+    if (dev < 0) return 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+            n = 1;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+}  // namespace lidx
+
+using namespace lidx;
+
+extern "C" {
+
+idx_status idx_hadamard(const void* x, void* y, idx_dtype dtype, int64_t n_rows, int32_t d,
+                        int64_t row_stride, idx_stream_t stream) {
+    const char* what = "idx_hadamard";
+    if (!valid_dtype(dtype)) return fail(IDX_ERR_INVALID_ARG, "%s: bad dtype", what);
+    if (n_rows < 0) return fail(IDX_ERR_INVALID_ARG, "%s: n_rows < 0", what);
+    if (d != 32 && d != 64 && d != 128 && d != 256)
+        return fail(IDX_ERR_INVALID_ARG, "%s: d must be 32, 64, 128 or 256", what);
+    if (row_stride < d) return fail(IDX_ERR_INVALID_ARG, "%s: row_stride < d", what);
+    if (n_rows == 0) return IDX_OK;
+    if (!x || !y) return fail(IDX_ERR_INVALID_ARG, "%s: x or y is NULL", what);
+    if (!aligned16(x) || !aligned16(y) || (row_stride * (int64_t)dtype_size(dtype)) % 16 != 0)
+        return fail(IDX_ERR_INVALID_ARG, "%s: x, y and rows must be 16-byte aligned", what);
+    return from_cuda(launch_hadamard(x, y, dtype, n_rows, d, row_stride, (cudaStream_t)stream), what);
+}
+
+idx_status idx_score(const void* q, idx_dtype q_dtype, const float* w, int32_t n_heads,
+                     int32_t head_dim, const void* k, idx_dtype k_dtype, int64_t k_row_stride,
+                     int64_t k_rows, idx_batch batch, int32_t block_size, float* scores,
+                     int64_t score_row_stride, void* workspace, size_t workspace_bytes,
+                     idx_stream_t stream) {
+    const char* what = "idx_score";
+    (void)workspace;
+    (void)workspace_bytes;
+    idx_status s = check_batch(batch, what);
+    if (s != IDX_OK) return s;
+    if (!valid_dtype(q_dtype) || !valid_dtype(k_dtype))
+        return fail(IDX_ERR_INVALID_ARG, "%s: bad dtype", what);
+    if (n_heads < 1 || n_heads > 64)
+        return fail(IDX_ERR_UNSUPPORTED, "%s: n_heads must be in [1, 64]", what);
+    if (head_dim < 1 || head_dim > 256)
+        return fail(IDX_ERR_UNSUPPORTED, "%s: head_dim must be in [1, 256]", what);
+    if (block_size < 0) return fail(IDX_ERR_INVALID_ARG, "%s: block_size < 0", what);
+    if (k_row_stride < head_dim) return fail(IDX_ERR_INVALID_ARG, "%s: k_row_stride < head_dim", what);
+    if (k_rows < 0) return fail(IDX_ERR_INVALID_ARG, "%s: k_rows < 0", what);
+    const int32_t max_keys = block_size > 1 ? batch.max_n_kv / block_size : batch.max_n_kv;
+    if (score_row_stride < max_keys)
+        return fail(IDX_ERR_INVALID_ARG, "%s: score_row_stride < keys per row", what);
+    const int64_t rows = (int64_t)batch.n_seq * batch.n_q_per_seq;
+    if (rows == 0 || max_keys == 0) return IDX_OK;
+    if (!q || !w || !k || !scores) return fail(IDX_ERR_INVALID_ARG, "%s: NULL q/w/k/scores", what);
+    const Geom g = make_geom(batch);
+    const cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaErrorNotSupported;
+    // tensor cores when q converts exactly to the key type (same type, or bf16 q with F16
+    // keys: bf16's 8-bit significand fits f16's 11 bits inside f16's normal range)
+    const bool q_exact = q_dtype == k_dtype || (q_dtype == IDX_BF16 && k_dtype == IDX_F16);
+    if (n_heads == 64 && head_dim == 128 && k_dtype != IDX_F32 && block_size <= 1 && q_exact)
+        e = launch_score_tc(q, q_dtype, w, n_heads, head_dim, k, k_dtype, k_row_stride, k_rows, g,
+                            block_size, scores, score_row_stride, st);
+    if (e == cudaErrorNotSupported)
+        e = launch_score_generic(q, q_dtype, w, n_heads, head_dim, k, k_dtype, k_row_stride, k_rows,
+                                 g, block_size, scores, score_row_stride, st);
+    return from_cuda(e, what);
+}
+
+idx_status idx_block_pool(const void* k_raw, idx_dtype k_dtype, int64_t k_row_stride,
+                          int64_t k_rows, idx_batch batch, int32_t block_size, int32_t head_dim,
+                          float* pooled, int64_t pool_seq_stride, idx_stream_t stream) {
+    const char* what = "idx_block_pool";
+    idx_status s = check_batch(batch, what);
+    if (s != IDX_OK) return s;
+    if (!valid_dtype(k_dtype)) return fail(IDX_ERR_INVALID_ARG, "%s: bad dtype", what);
+    if (block_size < 1) return fail(IDX_ERR_INVALID_ARG, "%s: block_size < 1", what);
+    const int64_t row_bytes = (int64_t)head_dim * dtype_size(k_dtype);
+    if (head_dim < 1 || row_bytes % 16 != 0 || row_bytes > 2048)
+        return fail(IDX_ERR_UNSUPPORTED, "%s: head_dim*size must be a multiple of 16 bytes, <= 2048", what);
+    if (k_row_stride < head_dim || (k_row_stride * (int64_t)dtype_size(k_dtype)) % 16 != 0)
+        return fail(IDX_ERR_INVALID_ARG, "%s: k_row_stride < head_dim or not 16-byte aligned", what);
+    if (pool_seq_stride < batch.max_n_kv / block_size)
+        return fail(IDX_ERR_INVALID_ARG, "%s: pool_seq_stride < max_n_kv / block_size", what);
+    if (k_rows < 0) return fail(IDX_ERR_INVALID_ARG, "%s: k_rows < 0", what);
+    if (batch.n_seq == 0 || batch.max_n_kv / block_size == 0) return IDX_OK;
+    if (!k_raw || !pooled) return fail(IDX_ERR_INVALID_ARG, "%s: NULL k_raw/pooled", what);
+    if (!aligned16(k_raw)) return fail(IDX_ERR_INVALID_ARG, "%s: k_raw not 16-byte aligned", what);
+    const Geom g = make_geom(batch);
+    return from_cuda(launch_block_pool(k_raw, k_dtype, k_row_stride, k_rows, g, block_size, head_dim,
+                                       pooled, pool_seq_stride, (cudaStream_t)stream),
+                     what);
+}
+
+idx_status idx_topk(const float* scores, int64_t score_row_stride, idx_batch batch, int32_t top_k,
+                    int32_t block_size, int32_t* idx, int64_t idx_row_stride, int32_t* n_sel,
+                    void* workspace, size_t workspace_bytes, idx_stream_t stream) {
+    const char* what = "idx_topk";
+    (void)workspace;
+    (void)workspace_bytes;
+    idx_status s = check_batch(batch, what);
+    if (s != IDX_OK) return s;
+    if (top_k < 1) return fail(IDX_ERR_INVALID_ARG, "%s: top_k < 1", what);
+    if (block_size < 0) return fail(IDX_ERR_INVALID_ARG, "%s: block_size < 0", what);
+    const bool blocks = block_size > 1;
+    const int64_t cap = blocks ? (int64_t)(top_k / block_size) * block_size + block_size - 1 : top_k;
+    if (idx_row_stride < cap)
+        return fail(IDX_ERR_INVALID_ARG, "%s: idx_row_stride < output capacity %lld", what,
+                    (long long)cap);
+    const int32_t max_keys = blocks ? batch.max_n_kv / block_size : batch.max_n_kv;
+    if (score_row_stride < max_keys)
+        return fail(IDX_ERR_INVALID_ARG, "%s: score_row_stride < candidates per row", what);
+    const int64_t rows = (int64_t)batch.n_seq * batch.n_q_per_seq;
+    if (rows == 0) return IDX_OK;
+    if (!idx || (!scores && max_keys > 0)) return fail(IDX_ERR_INVALID_ARG, "%s: NULL scores/idx", what);
+    const Geom g = make_geom(batch);
+    return from_cuda(launch_topk(scores, score_row_stride, g, top_k, block_size, idx, idx_row_stride,
+                                 n_sel, (cudaStream_t)stream),
+                     what);
+}
+
+idx_status sparse_attn_decode(const void* q, idx_dtype dtype, int32_t n_q_heads, int32_t n_kv_heads,
+                              int32_t dk, int32_t dv, const void* k, const void* v,
+                              int64_t kv_row_stride, int64_t v_row_stride, int64_t kv_rows,
+                              idx_batch batch, const int32_t* idx, int64_t idx_row_stride,
+                              const int32_t* n_sel, float scale, void* out, idx_dtype out_dtype,
+                              void* workspace, size_t workspace_bytes, idx_stream_t stream) {
+    return attn_common("sparse_attn_decode", q, dtype, n_q_heads, n_kv_heads, dk, dv, k, v,
+                       kv_row_stride, v_row_stride, kv_rows, batch, idx, idx_row_stride, n_sel,
+                       scale, out, out_dtype, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+idx_status sparse_attn_prefill(const void* q, idx_dtype dtype, int32_t n_q_heads, int32_t n_kv_heads,
+                               int32_t dk, int32_t dv, const void* k, const void* v,
+                               int64_t kv_row_stride, int64_t v_row_stride, int64_t kv_rows,
+                               idx_batch batch, const int32_t* idx, int64_t idx_row_stride,
+                               const int32_t* n_sel, float scale, void* out, idx_dtype out_dtype,
+                               void* workspace, size_t workspace_bytes, idx_stream_t stream) {
+    return attn_common("sparse_attn_prefill", q, dtype, n_q_heads, n_kv_heads, dk, dv, k, v,
+                       kv_row_stride, v_row_stride, kv_rows, batch, idx, idx_row_stride, n_sel,
+                       scale, out, out_dtype, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+size_t idx_workspace_size(int32_t op, int64_t n_rows, int32_t max_n_kv, int32_t top_k,
+                          int32_t n_q_heads, int32_t dv) {
+    (void)op;
+    (void)n_rows;
+    (void)max_n_kv;
+    (void)top_k;
+    (void)n_q_heads;
+    (void)dv;
+    return 0;
+}
+
+const char* idx_last_error(void) { return t_last_error.c_str(); }
+
+idx_status idx_device_status(int32_t reset) {
+    int* p = status_ptr();
+    if (!p) return fail(IDX_ERR_CUDA, "idx_device_status: no device status word");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "idx_device_status: %s", cudaGetErrorString(e));
+    int v = 0;
+    e = cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && reset) e = cudaMemset(p, 0, sizeof(int));
+    if (e != cudaSuccess) return fail(IDX_ERR_CUDA, "idx_device_status: %s", cudaGetErrorString(e));
+    if (v != 0) fail((idx_status)v, "a kernel recorded device fault code %d", v);
+    return (idx_status)v;
+}
+
+}  // extern "C"

@@ -1,0 +1,95 @@
+// Block mean-pool of raw indexer keys:
+//     p[b, beta, :] = (1/C) * sum_{t < C} k_raw[row(b, beta*C + t), :]
+// for every complete block beta < floor(n_kv[b] / C).  Blocks are cuts of the
+// position line measured from the sequence's first position, and the pooled
+// key is the raw key's mean, before any norm or rotation (llama.cpp commit
+// c88c916636, QSA commit message; llama-memory-hybrid-idx.h, kpool_layout).
+//
+// One CTA of 128 threads per (block, sequence).  With 16-byte vector loads a
+// row of d elements takes TPR = d*size/16 threads, so the CTA reads
+// RP = 128/TPR rows at once; each thread sums its rows in f32 and the RP
+// partial sums are added in shared memory.  A pure HBM stream: each raw key
+// byte is read once and 1/C of it is written (as f32).
+#include "lidx_internal.cuh"
+
+namespace lidx {
+namespace {
+
+constexpr int kThreads = 128;
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) pool_kernel(const T* __restrict__ k, int64_t k_row_stride,
+                                                        int64_t k_rows, Geom g, int C, int d,
+                                                        float* __restrict__ pooled,
+                                                        int64_t pool_seq_stride) {
+    extern __shared__ float part[];  // [RP][d]
+    const int b = blockIdx.y;
+    const int n_cb = seq_n_kv(g, b) / C;
+    constexpr int V = 16 / sizeof(T);
+    const int tpr = d / V;              // threads per row
+    const int rp = kThreads / tpr;      // rows per pass
+    const int64_t row0 = seq_row0(g, b);
+    for (int beta = blockIdx.x; beta < n_cb; beta += gridDim.x) {
+        const int rg = threadIdx.x / tpr, cv = threadIdx.x % tpr;
+        float acc[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = 0.f;
+        if (rg < rp) {
+            for (int t = rg; t < C; t += rp) {
+                const int64_t row = row0 + (int64_t)beta * C + t;
+                if (row < 0 || row >= k_rows) {
+                    flag(g.status, IDX_ERR_DEVICE_BOUNDS);
+                    continue;
+                }
+                const uint4 raw = *reinterpret_cast<const uint4*>(k + row * k_row_stride + cv * V);
+                const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+                for (int i = 0; i < V; ++i) acc[i] += to_f32(e[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < V; ++i) part[rg * d + cv * V + i] = acc[i];
+        }
+        __syncthreads();
+        for (int c = threadIdx.x; c < d; c += kThreads) {
+            float sum = 0.f;
+            for (int i = 0; i < rp; ++i) sum += part[i * d + c];
+            pooled[((int64_t)b * pool_seq_stride + beta) * d + c] = sum / (float)C;
+        }
+        __syncthreads();
+    }
+}
+
+template <typename T>
+cudaError_t run(const T* k, int64_t k_row_stride, int64_t k_rows, const Geom& g, int C, int d,
+                float* pooled, int64_t pool_seq_stride, cudaStream_t st) {
+    const int max_blocks = g.max_n_kv / C;
+    if (max_blocks == 0 || g.B == 0) return cudaSuccess;
+    constexpr int V = 16 / sizeof(T);
+    const int tpr = d / V;
+    const int rp = kThreads / tpr;
+    const size_t sm = (size_t)rp * d * sizeof(float);
+    dim3 grid((unsigned)(max_blocks < 65535 ? max_blocks : 65535), (unsigned)g.B);
+    pool_kernel<T><<<grid, kThreads, sm, st>>>(k, k_row_stride, k_rows, g, C, d, pooled,
+                                               pool_seq_stride);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_block_pool(const void* k_raw, int k_dtype, int64_t k_row_stride, int64_t k_rows,
+                              const Geom& g, int C, int d, float* pooled, int64_t pool_seq_stride,
+                              cudaStream_t st) {
+    switch (k_dtype) {
+        case IDX_F16:
+            return run(static_cast<const __half*>(k_raw), k_row_stride, k_rows, g, C, d, pooled,
+                       pool_seq_stride, st);
+        case IDX_BF16:
+            return run(static_cast<const __nv_bfloat16*>(k_raw), k_row_stride, k_rows, g, C, d,
+                       pooled, pool_seq_stride, st);
+        default:
+            return run(static_cast<const float*>(k_raw), k_row_stride, k_rows, g, C, d, pooled,
+                       pool_seq_stride, st);
+    }
+}
+
+}  // namespace lidx

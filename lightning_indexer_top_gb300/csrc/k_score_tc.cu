@@ -1,0 +1,392 @@
+// Lightning-indexer scores of decode query rows on the 5th-generation tensor
+// cores (H = 64 indexer heads, d = 128, 16-bit key cache):
+//     s[r, j] = sum_h w[r, h] * max(0, q[r, h, :] . k[j, :])
+// (ik_llama_opt commit log, "openpangu: DSA lightning indexer + SWA schedule";
+// ReLU per head before the head sum, llama.cpp commit c88c916636, QSA commit
+// message).  The pages' fused indexer ("Route DSA indexer selection through
+// ggml_indexer_topk", same log) avoids a per-head score tensor; here the
+// per-head dot products live only in TMEM.
+//
+// Why tensor cores for decode: a 256-byte F16 key row costs 64*128 MACs, 64
+// flop/byte; streaming keys at HBM speed needs ~430 TFLOP/s, several times
+// what the CUDA cores deliver.  Per tile of 128 keys one MMA chain
+//     D[128 keys x 64 heads] = K_tile[128 x 128] . Q^T[128 x 64]
+// (M = 128, N = 64, K = 128 as 8 steps of 16) puts one key per TMEM lane, so
+// the epilogue thread that owns a lane applies ReLU, weights and sums its 64
+// head columns with no cross-thread reduction.
+//
+// Persistent CTAs (one per SM).  The (row, 128-key tile) pairs of all query
+// rows form one flat list, split evenly over the CTAs, so ragged n_kv is
+// balanced.  Warp roles:
+//   warp 0      producer: TMA loads of key tiles (two 64-column boxes, 128-byte
+//               swizzle) into a 6-stage ring; at each new query row it also
+//               converts that row's q to the key dtype and writes it, swizzled,
+//               into one of two q buffers (the MMA's B operand).
+//   warp 1      TMEM owner and MMA issuer (one lane): 8 tcgen05.mma per tile
+//               into one of 4 TMEM accumulators of 64 columns.
+//   warps 2-5   epilogue: tcgen05.ld of the tile's [128 x 64] accumulator, one
+//               key per thread, then sum_h w_h*relu(d_h) and a coalesced store.
+// Every wait is bounded; a timeout records IDX_ERR_TIMEOUT and the CTA winds
+// down (drains its TMA loads and MMAs, frees TMEM) instead of hanging.
+#include <mutex>
+
+#include "lidx_internal.cuh"
+#include "sm100_ptx.cuh"
+
+namespace lidx {
+namespace {
+using namespace sm100;
+
+constexpr int kTileKeys = 128;
+constexpr int kH = 64;
+constexpr int kD = 128;
+constexpr int kStages = 6;
+constexpr int kAcc = 4;
+constexpr int kTmemCols = kAcc * kH;                 // 256
+constexpr int kTileBytes = kTileKeys * kD * 2;       // 32 KB
+constexpr int kHalfBytes = kTileBytes / 2;           // one 64-column box
+constexpr int kQBytes = kH * kD * 2;                 // 16 KB
+constexpr int kQHalfBytes = kQBytes / 2;
+constexpr int kThreads = 192;
+
+struct Ctl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[kAcc];
+    uint64_t tempty[kAcc];
+    uint64_t qfull[2];
+    uint64_t qempty[2];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+    int64_t r_begin;     // first query row of this CTA's range
+    int t_begin;         // tile index inside that row
+    int64_t count;       // tiles in this CTA's range
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kTileBytes + 2 * kQBytes + sizeof(Ctl);
+
+template <typename T> constexpr bool kIsBF16 = false;
+template <> constexpr bool kIsBF16<__nv_bfloat16> = true;
+
+__device__ __forceinline__ int row_tiles(int n_keys) { return (n_keys + kTileKeys - 1) / kTileKeys; }
+
+// Walks the flat (row, tile) list in order, skipping rows without keys.
+struct TileCursor {
+    int64_t r;
+    int t;
+    int n_keys;
+    int n_tiles;
+    __device__ void start(const Geom& g, int64_t r0, int t0, int64_t n_rows) {
+        r = r0;
+        t = t0;
+        n_keys = r < n_rows ? row_n_vis(g, r) : 0;   // an empty share may start past the last row
+        n_tiles = row_tiles(n_keys);
+    }
+    // advance one tile; returns true when the next tile starts a new row
+    __device__ bool next(const Geom& g, int64_t n_rows) {
+        if (++t < n_tiles) return false;
+        t = 0;
+        do {
+            ++r;
+            if (r >= n_rows) break;
+            n_keys = row_n_vis(g, r);
+            n_tiles = row_tiles(n_keys);
+        } while (n_tiles == 0);
+        return true;
+    }
+};
+
+__device__ __forceinline__ void abort_cta(Ctl& c, const Geom& g) {
+    *(volatile int*)&c.abort = 1;
+    flag(g.status, IDX_ERR_TIMEOUT);
+}
+
+template <typename TK>
+__global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
+    const __grid_constant__ CUtensorMap kmap, const void* __restrict__ q, int q_dtype,
+    const float* __restrict__ w, Geom g, float* __restrict__ scores, int64_t score_row_stride) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* tiles = smem;                                   // kStages x 32 KB, 1024-aligned
+    uint8_t* qbuf = smem + (size_t)kStages * kTileBytes;     // 2 x 16 KB, 1024-aligned
+    Ctl& c = *reinterpret_cast<Ctl*>(qbuf + 2 * kQBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n_rows = (int64_t)g.B * g.T;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&c.full[i], 1);
+            mbar_init(&c.empty[i], 1);
+        }
+        for (int i = 0; i < kAcc; ++i) {
+            mbar_init(&c.tfull[i], 1);
+            mbar_init(&c.tempty[i], 4);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&c.qfull[i], 1);
+            mbar_init(&c.qempty[i], 1);
+        }
+        mbar_init(&c.done, 1);
+        c.abort = 0;
+        fence_mbar_init();
+        // this CTA's share of the flat tile list
+        int64_t total = 0;
+        for (int64_t r = 0; r < n_rows; ++r) total += row_tiles(row_n_vis(g, r));
+        const int64_t b0 = (int64_t)blockIdx.x * total / gridDim.x;
+        const int64_t b1 = (int64_t)(blockIdx.x + 1) * total / gridDim.x;
+        int64_t acc = 0, r = 0;
+        while (r < n_rows) {
+            const int nt = row_tiles(row_n_vis(g, r));
+            if (acc + nt > b0) break;
+            acc += nt;
+            ++r;
+        }
+        c.r_begin = r;
+        c.t_begin = (int)(b0 - acc);
+        c.count = b1 - b0;
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&kmap);
+    if (warp == 1) {
+        tmem_alloc(&c.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = c.tmem_base;
+    const int64_t count = c.count;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        TileCursor cur;
+        cur.start(g, c.r_begin, c.t_begin, n_rows);
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t seg = -1;
+        int64_t issued = 0;
+        for (int64_t i = 0; i < count; ++i) {
+            if (*(volatile int*)&c.abort) break;
+            if (i == 0 || cur.t == 0) {
+                // new query row: stage its q (converted, swizzled) as the MMA B operand
+                ++seg;
+                const int qb = (int)(seg & 1);
+                const uint32_t qph = (uint32_t)((seg >> 1) & 1);
+                if (!mbar_wait(&c.qempty[qb], qph ^ 1)) {
+                    abort_cta(c, g);
+                    break;
+                }
+                uint8_t* qdst = qbuf + qb * kQBytes;
+                const int64_t qrow = cur.r * (int64_t)kH * kD;
+                for (int ch = lane; ch < kH * kD / 8; ch += 32) {
+                    const int h = ch >> 4, cc = ch & 15;
+                    const int half = cc >> 3, c8 = cc & 7;
+                    TK vals[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) vals[e] = from_f32<TK>(load_any(q, qrow + h * kD + cc * 8 + e, q_dtype));
+                    uint8_t* dst = qdst + half * kQHalfBytes + h * 128 + ((c8 ^ (h & 7)) << 4);
+                    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(vals);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c.qfull[qb]);
+            }
+            if (lane == 0) {
+                if (!mbar_wait(&c.empty[stage], phase ^ 1)) {
+                    abort_cta(c, g);
+                } else {
+                    const int64_t krow = seq_row0(g, (int)(cur.r / g.T)) + (int64_t)cur.t * kTileKeys;
+                    uint8_t* dst = tiles + (size_t)stage * kTileBytes;
+                    mbar_arrive_expect_tx(&c.full[stage], kTileBytes);
+                    tma_load_2d(dst, &kmap, &c.full[stage], 0, (int32_t)krow);
+                    tma_load_2d(dst + kHalfBytes, &kmap, &c.full[stage], 64, (int32_t)krow);
+                    ++issued;
+                }
+            }
+            __syncwarp();
+            if (*(volatile int*)&c.abort) break;
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1;
+            }
+            cur.next(g, n_rows);
+        }
+        // never leave the CTA with TMA writes in flight
+        if (lane == 0) {
+            const int64_t n = issued < kStages ? issued : kStages;
+            for (int64_t i = issued - n; i < issued; ++i)
+                mbar_wait(&c.full[i % kStages], (uint32_t)((i / kStages) & 1));
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(kTileKeys, kH, kIsBF16<TK> ? 1 : 0);
+            TileCursor cur;
+            cur.start(g, c.r_begin, c.t_begin, n_rows);
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, aphase = 0;
+            int64_t seg = -1;
+            for (int64_t i = 0; i < count; ++i) {
+                if (*(volatile int*)&c.abort) break;
+                if (i == 0 || cur.t == 0) {
+                    ++seg;
+                    if (!mbar_wait(&c.qfull[seg & 1], (uint32_t)((seg >> 1) & 1))) {
+                        abort_cta(c, g);
+                        break;
+                    }
+                }
+                if (!mbar_wait(&c.tempty[acc], aphase ^ 1) || !mbar_wait(&c.full[stage], phase)) {
+                    abort_cta(c, g);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(tiles + (size_t)stage * kTileBytes);
+                const uint32_t b0 = smem_u32(qbuf + (seg & 1) * kQBytes);
+                const uint32_t d = tmem + acc * kH;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;   // K offset inside the 128-byte row
+                    const uint64_t ad = desc_sw128_kmajor(a0 + (kk >> 2) * kHalfBytes + off, 1024);
+                    const uint64_t bd = desc_sw128_kmajor(b0 + (kk >> 2) * kQHalfBytes + off, 1024);
+                    mma_f16_ss(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&c.empty[stage]);
+                mma_commit(&c.tfull[acc]);
+                const bool last_of_row = (cur.t == cur.n_tiles - 1) || (i == count - 1);
+                if (last_of_row) mma_commit(&c.qempty[seg & 1]);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+                if (++acc == kAcc) {
+                    acc = 0;
+                    aphase ^= 1;
+                }
+                cur.next(g, n_rows);
+            }
+            // every MMA issued by this thread has completed before TMEM is freed
+            mma_commit(&c.done);
+            mbar_wait(&c.done, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quad = warp & 3;                 // TMEM lane quarter this warp may access
+        TileCursor cur;
+        cur.start(g, c.r_begin, c.t_begin, n_rows);
+        int acc = 0;
+        uint32_t aphase = 0;
+        float wv[kH];
+        for (int64_t i = 0; i < count; ++i) {
+            if (*(volatile int*)&c.abort) break;
+            if (i == 0 || cur.t == 0) {
+                const float4* wr = reinterpret_cast<const float4*>(w + cur.r * kH);
+#pragma unroll
+                for (int h4 = 0; h4 < kH / 4; ++h4) {
+                    const float4 x = wr[h4];
+                    wv[4 * h4] = x.x;
+                    wv[4 * h4 + 1] = x.y;
+                    wv[4 * h4 + 2] = x.z;
+                    wv[4 * h4 + 3] = x.w;
+                }
+            }
+            if (!mbar_wait(&c.tfull[acc], aphase)) {
+                abort_cta(c, g);
+                break;
+            }
+            tc_fence_after();
+            float v0[32], v1[32];
+            const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + acc * kH;
+            tmem_ld_32x32b_x32(ta, v0);
+            tmem_ld_32x32b_x32(ta + 32, v1);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c.tempty[acc]);
+            float s = 0.f;
+#pragma unroll
+            for (int h = 0; h < 32; ++h) s = fmaf(wv[h], fmaxf(v0[h], 0.f), s);
+#pragma unroll
+            for (int h = 0; h < 32; ++h) s = fmaf(wv[32 + h], fmaxf(v1[h], 0.f), s);
+            const int j = cur.t * kTileKeys + quad * 32 + lane;
+            if (j < cur.n_keys) scores[cur.r * score_row_stride + j] = s + 0.0f;
+            if (++acc == kAcc) {
+                acc = 0;
+                aphase ^= 1;
+            }
+            cur.next(g, n_rows);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+    static std::once_flag once;
+    static EncodeFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeFn>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+// 2-D tensor map over a [rows, 128] 16-bit key cache: boxes of 64 columns x
+// 128 rows with the 128-byte swizzle the MMA descriptors expect.
+bool make_key_tmap(CUtensorMap* m, const void* k, bool bf16, int64_t k_row_stride, int64_t k_rows,
+                   int box_rows) {
+    EncodeFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)k_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)k_row_stride * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+              const_cast<void*>(k), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, int d, const void* k,
+                            int k_dtype, int64_t k_row_stride, int64_t k_rows, const Geom& g, int block_size,
+                            float* scores, int64_t score_row_stride, cudaStream_t st) {
+    if (H != kH || d != kD || k_dtype == IDX_F32 || block_size > 1 || g.T != 1) return cudaErrorNotSupported;
+    if ((reinterpret_cast<uintptr_t>(k) & 15u) || (k_row_stride % 8) || k_rows < 1 || k_rows > INT32_MAX ||
+        (reinterpret_cast<uintptr_t>(w) & 15u))
+        return cudaErrorNotSupported;
+    const int64_t n_rows = (int64_t)g.B * g.T;
+    if (n_rows == 0 || g.max_n_kv == 0) return cudaSuccess;
+    CUtensorMap map;
+    const bool bf16 = k_dtype == IDX_BF16;
+    if (!make_key_tmap(&map, k, bf16, k_row_stride, k_rows, kTileKeys)) return cudaErrorNotSupported;
+    const int64_t max_tiles = n_rows * ((g.max_n_kv + kTileKeys - 1) / kTileKeys);
+    const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
+    if (bf16) {
+        auto kern = score_tc_decode_kernel<__nv_bfloat16>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        kern<<<grid, kThreads, kSmemBytes, st>>>(map, q, q_dtype, w, g, scores, score_row_stride);
+    } else {
+        auto kern = score_tc_decode_kernel<__half>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        kern<<<grid, kThreads, kSmemBytes, st>>>(map, q, q_dtype, w, g, scores, score_row_stride);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace lidx

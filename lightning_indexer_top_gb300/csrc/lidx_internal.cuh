@@ -1,0 +1,126 @@
+// Internal declarations shared by the kernels and the C-ABI layer of liblidx.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lidx.h"
+
+namespace lidx {
+
+// ---------------------------------------------------------------------------
+// batch geometry as the kernels see it (a by-value copy of idx_batch plus the
+// device status word every kernel reports data-dependent faults to)
+// ---------------------------------------------------------------------------
+struct Geom {
+    int32_t B;
+    int32_t T;
+    const int32_t* n_kv;
+    const int32_t* kv_start;
+    int64_t kv_seq_stride;
+    const int32_t* q_pos;
+    int32_t max_n_kv;
+    int* status;  // device int: first fault code recorded, 0 = none
+};
+
+__device__ __forceinline__ void flag(int* status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// cached tokens of sequence b, clamped to [0, max_n_kv] (a violation is flagged)
+__device__ __forceinline__ int seq_n_kv(const Geom& g, int b) {
+    int n = g.n_kv[b];
+    if (n < 0 || n > g.max_n_kv) {
+        flag(g.status, IDX_ERR_DEVICE_BOUNDS);
+        n = n < 0 ? 0 : g.max_n_kv;
+    }
+    return n;
+}
+
+// keys visible to query row r: min(q_pos + 1, n_kv) under the causal mask, else n_kv
+__device__ __forceinline__ int row_n_vis(const Geom& g, int64_t r) {
+    int b = (int)(r / g.T);
+    int n = seq_n_kv(g, b);
+    if (g.q_pos) {
+        int p = g.q_pos[r];
+        int lim = p < 0 ? 0 : (p >= n ? n : p + 1);
+        n = lim;
+    }
+    return n;
+}
+
+// cache row of position 0 of sequence b
+__device__ __forceinline__ int64_t seq_row0(const Geom& g, int b) {
+    return g.kv_start ? (int64_t)g.kv_start[b] : (int64_t)b * g.kv_seq_stride;
+}
+
+// ---------------------------------------------------------------------------
+// element conversions
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float load_any(const void* p, int64_t i, int dtype) {
+    switch (dtype) {
+        case IDX_F16: return __half2float(static_cast<const __half*>(p)[i]);
+        case IDX_BF16: return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+        default: return static_cast<const float*>(p)[i];
+    }
+}
+
+// order-preserving map of an f32 score to uint32 (larger score -> larger key);
+// -0 is folded onto +0 first so that equal scores have equal keys
+__device__ __forceinline__ uint32_t order_key(float s) {
+    uint32_t u = __float_as_uint(s);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+inline size_t dtype_size(int t) { return t == IDX_F32 ? 4 : 2; }
+
+// ---------------------------------------------------------------------------
+// launchers (one per kernel family); each returns cudaGetLastError()
+// ---------------------------------------------------------------------------
+cudaError_t launch_hadamard(const void* x, void* y, int dtype, int64_t n_rows, int d,
+                            int64_t row_stride, cudaStream_t st);
+
+cudaError_t launch_score_generic(const void* q, int q_dtype, const float* w, int H, int d,
+                                 const void* k, int k_dtype, int64_t k_row_stride, int64_t k_rows,
+                                 const Geom& g, int block_size, float* scores,
+                                 int64_t score_row_stride, cudaStream_t st);
+
+// tensor-core scorer for H = 64, d = 128, 16-bit keys; returns cudaErrorNotSupported
+// when the shape is not one it handles (the caller then uses the generic scorer)
+cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, int d,
+                            const void* k, int k_dtype, int64_t k_row_stride, int64_t k_rows,
+                            const Geom& g, int block_size, float* scores, int64_t score_row_stride,
+                            cudaStream_t st);
+
+cudaError_t launch_block_pool(const void* k_raw, int k_dtype, int64_t k_row_stride, int64_t k_rows,
+                              const Geom& g, int C, int d, float* pooled, int64_t pool_seq_stride,
+                              cudaStream_t st);
+
+cudaError_t launch_topk(const float* scores, int64_t score_row_stride, const Geom& g, int top_k,
+                        int block_size, int32_t* idx, int64_t idx_row_stride, int32_t* n_sel,
+                        cudaStream_t st);
+
+cudaError_t launch_attn_generic(const void* q, int dtype, int Hq, int Hkv, int dk, int dv,
+                                const void* k, const void* v, int64_t kv_row_stride,
+                                int64_t v_row_stride, int64_t kv_rows, const Geom& g,
+                                const int32_t* idx, int64_t idx_row_stride, const int32_t* n_sel,
+                                float scale, void* out, int out_dtype, cudaStream_t st);
+
+// number of SMs of the current device (cached per device)
+int sm_count();
+
+}  // namespace lidx

@@ -1,0 +1,94 @@
+"""One pass of the hot path over a workload: (Hadamard) -> score -> select -> attend.
+
+Buffers are allocated once at construction; ``run()`` only enqueues the
+library's kernels on the current stream, so a step can be timed, repeated or
+captured in a CUDA graph.  This is orchestration only: every arithmetic step
+is a call into liblidx.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import Batch, idx_block_pool, idx_hadamard, idx_score, idx_topk, idx_workspace_size, topk_capacity
+from . import sparse_attn_decode, sparse_attn_prefill, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL
+from .workloads import Workload
+
+
+class SparseAttentionStep:
+    def __init__(self, wl: Workload, out_dtype=None):
+        self.wl = wl
+        dev = wl.q_idx.device
+        self.batch = Batch(wl.n_kv, wl.T, wl.max_n_kv, kv_start=wl.kv_start, kv_seq_stride=wl.kv_seq_stride,
+                           q_pos=wl.q_pos)
+        rows = wl.B * wl.T
+        C = wl.block_size
+        if C > 1:
+            self.pool_stride = max(wl.max_n_kv // C, 1)
+            self.pooled = torch.zeros(wl.B, self.pool_stride, wl.d, device=dev, dtype=torch.float32)
+            self.pool_batch = Batch(wl.n_kv, wl.T, wl.max_n_kv, kv_seq_stride=self.pool_stride, q_pos=wl.q_pos)
+            n_keys = self.pool_stride
+        else:
+            n_keys = max(wl.max_n_kv, 1)
+        self.scores = torch.empty(rows, n_keys, device=dev, dtype=torch.float32)
+        cap = topk_capacity(wl.top_k, C)
+        self.idx = torch.empty(rows, cap, device=dev, dtype=torch.int32)
+        self.n_sel = torch.empty(rows, device=dev, dtype=torch.int32)
+        if out_dtype is None:   # f32 in -> f32 out, 16-bit in -> bf16 out
+            out_dtype = torch.float32 if wl.q_attn.dtype == torch.float32 else torch.bfloat16
+        self.out = torch.empty(rows, wl.q_attn.shape[1], wl.dv, device=dev, dtype=out_dtype)
+        op = IDX_OP_ATTN_PREFILL if wl.kind == "prefill" else IDX_OP_ATTN_DECODE
+        ws = idx_workspace_size(op, rows, wl.max_n_kv, cap, wl.q_attn.shape[1], wl.dv)
+        self.attn_ws = torch.empty(max(ws, 16), device=dev, dtype=torch.uint8) if ws else None
+        self.attn = sparse_attn_prefill if wl.kind == "prefill" else sparse_attn_decode
+        self.q_rot = None
+        self.k_rot = None
+        if wl.hadamard:
+            self.q_rot = torch.empty_like(wl.q_idx)
+            self.k_rot = torch.empty_like(wl.k_idx)
+
+    def rotate(self):
+        """Hadamard-rotate q and k into separate buffers (the cache holds rotated keys)."""
+        idx_hadamard(self.wl.q_idx, self.q_rot)
+        idx_hadamard(self.wl.k_idx, self.k_rot)
+
+    def score(self):
+        wl = self.wl
+        q = wl.q_idx if self.q_rot is None else self.q_rot
+        k = wl.k_idx if self.k_rot is None else self.k_rot
+        if wl.block_size > 1:
+            idx_block_pool(k, self.batch, wl.block_size, pool_seq_stride=self.pool_stride, pooled=self.pooled)
+            kp = self.pooled.view(-1, wl.d)
+            idx_score(q, wl.w, kp, self.pool_batch, block_size=wl.block_size, scores=self.scores)
+        else:
+            idx_score(q, wl.w, k, self.batch, scores=self.scores)
+
+    def select(self):
+        idx_topk(self.scores, self.batch, self.wl.top_k, block_size=self.wl.block_size, idx=self.idx,
+                 n_sel=self.n_sel)
+
+    def attend(self):
+        wl = self.wl
+        if wl.v_attn is None:
+            self.attn(wl.q_attn, wl.k_attn, None, self.batch, self.idx, self.n_sel, wl.scale, out=self.out,
+                      workspace=self.attn_ws, dv=wl.dv)
+        else:
+            self.attn(wl.q_attn, wl.k_attn, wl.v_attn, self.batch, self.idx, self.n_sel, wl.scale,
+                      out=self.out, workspace=self.attn_ws)
+
+    def run(self):
+        if self.q_rot is not None:
+            self.rotate()
+        self.score()
+        self.select()
+        self.attend()
+        return self.out
+
+    def launches_per_step(self) -> int:
+        """Kernels one run() enqueues (library launches only)."""
+        n = 3                                   # score, select, attend
+        if self.q_rot is not None:
+            n += 2                              # two Hadamard rotations
+        if self.wl.block_size > 1:
+            n += 1                              # block pool
+        return n

@@ -18,6 +18,7 @@ from .lidx_oracle import (  # noqa: F401
     round_to_storage,
     hadamard_matrix,
     hadamard_rotate,
+    hadamard_store,
     visible_count,
     indexer_scores,
     topk_select,

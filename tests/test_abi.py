@@ -1,0 +1,84 @@
+"""CPU-side tests of the C ABI: the library builds for sm_103a, loads without a
+GPU, exports every function include/lidx.h declares, and rejects bad
+arguments on the host before anything is launched."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import lightning_indexer_top_gb300 as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    L.build()
+    return L.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "lidx.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:idx_status|size_t|const char\*)\s+(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("idx_score", "idx_block_pool", "idx_topk", "sparse_attn_decode", "sparse_attn_prefill",
+              "idx_hadamard", "idx_workspace_size", "idx_last_error", "idx_device_status"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_library_is_built_for_sm103a():
+    log = open(os.path.join(ROOT, "lightning_indexer_top_gb300", "_build", "api.cu.log")).read()
+    assert "arch=compute_103a,code=sm_103a" in log
+
+
+def _batch(n_seq=1, T=1, max_n_kv=16):
+    return L._Batch(n_seq, T, ctypes.c_void_p(16), None, max_n_kv, None, max_n_kv)
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    # each call fails validation before any CUDA call is made
+    assert lib.idx_hadamard(ctypes.c_void_p(16), ctypes.c_void_p(16), L.IDX_BF16, 4, 100, 100, None) == L.IDX_ERR_INVALID_ARG
+    assert b"d must be" in lib.idx_last_error()
+    assert lib.idx_hadamard(None, None, L.IDX_BF16, 4, 128, 128, None) == L.IDX_ERR_INVALID_ARG
+    assert lib.idx_hadamard(ctypes.c_void_p(16), ctypes.c_void_p(16), 7, 4, 128, 128, None) == L.IDX_ERR_INVALID_ARG
+    b = _batch()
+    assert lib.idx_topk(None, 16, b, 0, 0, None, 16, None, None, 0, None) == L.IDX_ERR_INVALID_ARG
+    assert b"top_k" in lib.idx_last_error()
+    assert lib.idx_topk(None, 16, b, 32, 0, None, 16, None, None, 0, None) == L.IDX_ERR_INVALID_ARG
+    assert b"capacity" in lib.idx_last_error()
+    # block mode capacity = floor(top_k/C)*C + C - 1
+    assert lib.idx_topk(None, 16, b, 8, 4, None, 10, None, None, 0, None) == L.IDX_ERR_INVALID_ARG
+    bad = L._Batch(-1, 1, None, None, 0, None, 0)
+    assert lib.idx_score(None, 0, None, 4, 32, None, 0, 32, 0, bad, 0, None, 0, None, 0, None) == L.IDX_ERR_INVALID_ARG
+    assert lib.idx_score(None, 0, None, 65, 32, None, 0, 32, 0, b, 0, None, 16, None, 0, None) == L.IDX_ERR_UNSUPPORTED
+    assert lib.idx_block_pool(None, L.IDX_BF16, 128, 0, b, 0, 128, None, 16, None) == L.IDX_ERR_INVALID_ARG
+    assert lib.sparse_attn_decode(None, L.IDX_BF16, 6, 4, 128, 128, None, None, 512, 512, 0, b, None, 16, None,
+                                  1.0, None, L.IDX_F32, None, 0, None) == L.IDX_ERR_INVALID_ARG
+    assert b"Hq % Hkv" in lib.idx_last_error() or b"Hq" in lib.idx_last_error()
+    # latent form requires one kv head
+    assert lib.sparse_attn_decode(None, L.IDX_BF16, 8, 2, 576, 512, None, None, 1152, 0, 0, b, None, 16, None,
+                                  1.0, None, L.IDX_F32, None, 0, None) == L.IDX_ERR_INVALID_ARG
+    assert lib.sparse_attn_decode(None, L.IDX_BF16, 8, 1, 576, 512, None, None, 576, 0, 0, b, None, 16, None,
+                                  float("nan"), None, L.IDX_F32, None, 0, None) == L.IDX_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(lib):
+    empty = L._Batch(0, 1, None, None, 0, None, 0)
+    assert lib.idx_topk(None, 0, empty, 4, 0, None, 4, None, None, 0, None) == L.IDX_OK
+    assert lib.sparse_attn_decode(None, L.IDX_BF16, 8, 1, 576, 512, None, None, 576, 0, 0, empty, None, 16,
+                                  None, 1.0, None, L.IDX_F32, None, 0, None) == L.IDX_OK
+
+
+def test_workspace_size_is_pure_host(lib):
+    assert lib.idx_workspace_size(99, -5, -1, 0, 0, 0) == 0

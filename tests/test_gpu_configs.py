@@ -1,0 +1,223 @@
+"""End-to-end parity on the five synthetic configurations and the headline
+decode workload: the whole path (Hadamard -> score -> select -> attend) runs
+on the GPU exactly as the bench launches it; the oracle recomputes sampled
+rows from the same inputs.  Reports the identical-set rate and the mean
+Jaccard of the selections (the pages' comparison metric)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import lightning_indexer_top_gb300 as L
+from lightning_indexer_top_gb300 import workloads
+from lightning_indexer_top_gb300.pipeline import SparseAttentionStep
+from _helpers import assert_scores_close, check_selection, np64, sorted_unique
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    L.build()
+    L.load()
+    L.idx_device_status(reset=True)
+    yield
+    torch.cuda.empty_cache()
+
+
+def _run(wl):
+    step = SparseAttentionStep(wl)
+    step.run()
+    torch.cuda.synchronize()
+    assert L.idx_device_status(reset=True) == 0
+    return step
+
+
+def _report(name, ident):
+    rate = float(np.mean([i for i, _ in ident]))
+    jac = float(np.mean([j for _, j in ident]))
+    print(f"\n[{name}] identical-set rate {rate:.3f}  mean Jaccard {jac:.5f}  over {len(ident)} rows")
+    return rate
+
+
+def _check_mla_rows(wl, step, rows, k_rot=None, q_rot=None):
+    """Verify sampled rows of an MLA workload (decode or causal prefill)."""
+    ident = []
+    kh = np64(wl.k_idx) if k_rot is None else k_rot
+    lat = wl.k_attn
+    s_gpu = step.scores
+    for r in rows:
+        b = r // wl.T
+        row0 = wl.row0(b)
+        n_kv = wl.n_kv_host[b]
+        nv = O.visible_count(n_kv, None if wl.q_pos is None else r % wl.T)
+        q = np64(wl.q_idx[r]) if q_rot is None else q_rot(r)
+        s_ref = O.indexer_scores(q, np64(wl.w[r]), kh[row0:row0 + nv])
+        assert_scores_close(s_gpu[r, :nv].cpu().numpy(), s_ref, f"{wl.name} row {r}")
+        sel_ref = O.topk_select(s_ref, nv, wl.top_k)
+        ns = int(step.n_sel[r])
+        sel_gpu = sorted_unique(step.idx[r].cpu().numpy(), ns)
+        assert all(x == -1 for x in step.idx[r, ns:].tolist())
+        same, jac = check_selection(sel_gpu, sel_ref, s_ref, f"{wl.name} row {r}")
+        ident.append((same, jac))
+        if same:
+            lat_rows = np64(lat[row0:row0 + nv])
+            ref = O.sparse_attention_mla(np64(wl.q_attn[r]), lat_rows, sel_ref, wl.scale, wl.dv)
+            err = np.max(np.abs(np64(step.out[r]) - ref))
+            assert err <= 2e-2, f"{wl.name} row {r}: attention max-abs {err}"
+    return ident
+
+
+def test_config1_tiny_prefill_fp32_all_rows():
+    wl = workloads.make(1)
+    step = _run(wl)
+    ident = []
+    qh, wh, kh = np64(wl.q_idx), np64(wl.w), np64(wl.k_idx)
+    Kh, Vh = np64(wl.k_attn), np64(wl.v_attn)
+    for t in range(wl.T):
+        nv = t + 1
+        s_ref = O.indexer_scores(qh[t], wh[t], kh[:nv])
+        assert_scores_close(step.scores[t, :nv].cpu().numpy(), s_ref, f"row {t}")
+        sel_ref = O.topk_select(s_ref, nv, wl.top_k)
+        ns = int(step.n_sel[t])
+        sel_gpu = sorted_unique(step.idx[t].cpu().numpy(), ns)
+        same, jac = check_selection(sel_gpu, sel_ref, s_ref, f"row {t}")
+        ident.append((same, jac))
+        if nv <= wl.top_k:
+            assert sel_gpu == list(range(nv))          # exactly dense below the budget
+            dense = O.dense_attention_gqa(np64(wl.q_attn[t]), Kh, Vh, nv, wl.scale)
+            assert np.max(np.abs(np64(step.out[t]) - dense)) <= 1e-4
+        if same:
+            ref = O.sparse_attention_gqa(np64(wl.q_attn[t]), Kh, Vh, sel_ref, wl.scale)
+            assert np.max(np.abs(np64(step.out[t]) - ref)) <= 1e-4, t
+    assert _report(wl.name, ident) > 0.9
+
+
+def test_config2_decode_mla_all_rows():
+    wl = workloads.make(2)
+    step = _run(wl)
+    ident = _check_mla_rows(wl, step, range(wl.B))
+    assert _report(wl.name, ident) >= 0.5
+
+
+def test_config2_batched_equals_each_sequence_alone():
+    # "n_seq=4 == n_seq=1 chunk-for-chunk" (ik_llama.cpp PR #2058): a batched call is bit-identical
+    wl = workloads.make(2)
+    full = _run(wl)
+    for b in (0, 5):
+        one = workloads.make(2)
+        one.B = 1
+        one.q_idx, one.w, one.q_attn = wl.q_idx[b:b + 1], wl.w[b:b + 1], wl.q_attn[b:b + 1]
+        one.k_idx, one.k_attn = wl.k_idx, wl.k_attn
+        one.n_kv = wl.n_kv[b:b + 1].contiguous()
+        one.n_kv_host = [wl.n_kv_host[b]]
+        one.kv_start = torch.tensor([b * wl.kv_seq_stride], dtype=torch.int32, device="cuda")
+        one.kv_start_host = [b * wl.kv_seq_stride]
+        st = _run(one)
+        assert torch.equal(st.scores[0], full.scores[b])
+        assert torch.equal(st.idx[0], full.idx[b])
+        assert torch.equal(st.out[0], full.out[b])
+
+
+def test_config3_prefill_sampled_rows():
+    wl = workloads.make(3)
+    step = _run(wl)
+    # the oracle rotates the keys once (the cache holds rotated keys) and each sampled q row
+    k_rot = O.hadamard_store(np64(wl.k_idx), "bf16")
+    rows = [0, 1, 777, 2046, 2047, 2048, 2049, 5000, 9999, 16383]
+    ident = _check_mla_rows(wl, step, rows, k_rot=k_rot,
+                            q_rot=lambda r: O.hadamard_store(np64(wl.q_idx[r]), "bf16"))
+    for r in rows[:5]:   # rows below the budget are exactly dense
+        assert int(step.n_sel[r]) == r + 1
+    _report(wl.name, ident)
+
+
+def test_prefill_chunking_over_query_rows_is_bit_identical():
+    # chunked prefill scoring/selection is numerically identical to one call ("Subchunk OpenPangu DSA
+    # prefill gather", ik_llama_opt log): rows are independent
+    wl = workloads.make(3, n_tokens_override=6000)
+    step = _run(wl)
+    n = wl.T
+    for a, z in ((0, 2500), (2500, 6000)):
+        b = L.Batch(wl.n_kv, z - a, wl.max_n_kv, kv_seq_stride=wl.kv_seq_stride, q_pos=wl.q_pos[a:z])
+        s = L.idx_score(step.q_rot[a:z], wl.w[a:z], step.k_rot, b)
+        idx, ns = L.idx_topk(s, b, wl.top_k)
+        out = L.sparse_attn_prefill(wl.q_attn[a:z], wl.k_attn, None, b, idx, ns, wl.scale, dv=wl.dv,
+                                    out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        for r in range(z - a):
+            nv = a + r + 1
+            assert torch.equal(s[r, :nv], step.scores[a + r, :nv])
+        assert torch.equal(idx, step.idx[a:z])
+        assert torch.equal(out, step.out[a:z])
+    assert n == 6000
+
+
+def test_config4_block_decode_all_rows_with_tails():
+    wl = workloads.make(4, parity_tails=True)
+    step = _run(wl)
+    C = wl.block_size
+    ident = []
+    kh = np64(wl.k_idx)
+    Kh, Vh = wl.k_attn, wl.v_attn
+    for b in range(wl.B):
+        n = wl.n_kv_host[b]
+        row0 = wl.row0(b)
+        pooled = O.block_pool(kh[row0:row0 + n], C, n)
+        np.testing.assert_allclose(step.pooled[b, :n // C].cpu().numpy(), pooled, rtol=1e-5, atol=1e-6)
+        bs_ref = O.indexer_scores(np64(wl.q_idx[b]), np64(wl.w[b]), pooled)
+        assert_scores_close(step.scores[b, :n // C].cpu().numpy(), bs_ref, f"seq {b}")
+        sel_ref = O.block_select(bs_ref, n, wl.top_k, C)
+        assert np.array_equal(sel_ref, O.block_select_expanded(bs_ref, n, wl.top_k, C))
+        ns = int(step.n_sel[b])
+        sel_gpu = sorted_unique(step.idx[b].cpu().numpy(), ns)
+        n_cb = n // C
+        tail = list(range(n_cb * C, n))
+        assert sel_gpu[len(sel_gpu) - len(tail):] == tail          # the tail is always kept
+        gb = sorted(set(t // C for t in sel_gpu if t < n_cb * C))
+        rb = sorted(set(t // C for t in sel_ref if t < n_cb * C))
+        assert len([t for t in sel_gpu if t < n_cb * C]) == len(gb) * C      # whole blocks
+        same, jac = check_selection(gb, rb, bs_ref, f"seq {b}")
+        ident.append((same, jac))
+        if same:
+            ref = O.sparse_attention_gqa(np64(wl.q_attn[b]), np64(Kh[row0:row0 + n]), np64(Vh[row0:row0 + n]),
+                                         sel_ref, wl.scale)
+            assert np.max(np.abs(np64(step.out[b]) - ref)) <= 2e-2, b
+    _report(wl.name, ident)
+
+
+def test_config4_dense_threshold():
+    # exactly dense at n_vis = top_k + C - 1; one more token and a block is dropped
+    wl = workloads.make(4, batch_override=2, n_kv_override=2048 + 63)
+    wl.n_kv = torch.tensor([2048 + 63, 2048 + 64], dtype=torch.int32, device="cuda")
+    wl.n_kv_host = [2048 + 63, 2048 + 64]
+    wl.max_n_kv = 2048 + 64
+    wl.kv_seq_stride = 2048 + 64
+    wl.k_idx = torch.randn(2 * (2048 + 64), 128, device="cuda").to(torch.bfloat16)
+    wl.k_attn = torch.randn(2 * (2048 + 64), 4, 128, device="cuda").to(torch.bfloat16)
+    wl.v_attn = torch.randn(2 * (2048 + 64), 4, 128, device="cuda").to(torch.bfloat16)
+    step = _run(wl)
+    assert int(step.n_sel[0]) == 2048 + 63
+    assert step.idx[0, :2048 + 63].tolist() == list(range(2048 + 63))
+    assert int(step.n_sel[1]) == 2048
+    dense = O.dense_attention_gqa(np64(wl.q_attn[0]), np64(wl.k_attn[:2111]), np64(wl.v_attn[:2111]), 2111, wl.scale)
+    assert np.max(np.abs(np64(step.out[0]) - dense)) <= 2e-2
+
+
+def test_config5_long_ragged_decode_sampled_rows():
+    wl = workloads.make(5)
+    step = _run(wl)
+    order = np.argsort(wl.n_kv_host)
+    rows = [int(order[0]), int(order[len(order) // 2]), int(order[-1]), 7]
+    ident = _check_mla_rows(wl, step, rows)
+    _report(wl.name, ident)
+
+
+def test_headline_decode_64x131072_sampled_rows():
+    wl = workloads.make("headline")
+    step = _run(wl)
+    ident = _check_mla_rows(wl, step, [0, 31, 63])
+    _report(wl.name, ident)

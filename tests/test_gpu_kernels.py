@@ -1,0 +1,286 @@
+"""Per-kernel parity: each CUDA entry point against the CPU oracle on the same
+seeded inputs, at sizes that span several tiles plus a ragged tail."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import lightning_indexer_top_gb300 as L
+from _helpers import assert_scores_close, np64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+FMT = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    L.build()
+    L.load()
+    L.idx_device_status(reset=True)
+    yield
+    assert L.idx_device_status(reset=True) == 0
+
+
+def _i32(x):
+    return torch.tensor(x, dtype=torch.int32, device=DEV)
+
+
+# ------------------------------------------------------------------ Hadamard
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
+def test_hadamard_matches_oracle(dtype, d):
+    # the stored rotation is decided in f32 on both sides: bit-exact
+    g = torch.Generator(device=DEV).manual_seed(11 + d)
+    x = torch.randn(1003, d, generator=g, device=DEV).to(dtype)
+    y = L.idx_hadamard(x, torch.empty_like(x))
+    ref = O.hadamard_store(np64(x), FMT[dtype])
+    np.testing.assert_array_equal(np64(y), ref)
+    # in place gives the same bits
+    x2 = x.clone()
+    L.idx_hadamard(x2)
+    assert torch.equal(x2, y)
+
+
+# ------------------------------------------------------------------ score (CUDA-core scorer)
+
+@pytest.mark.parametrize("H,d,qt,kt", [(4, 32, torch.float32, torch.float32), (3, 40, torch.bfloat16, torch.float32),
+                                       (32, 128, torch.bfloat16, torch.float32), (8, 64, torch.float16, torch.bfloat16)])
+def test_score_generic_matches_oracle(H, d, qt, kt):
+    g = torch.Generator(device=DEV).manual_seed(21 + H)
+    B, T = 3, 5
+    n_kv = [300, 129, 1]
+    max_n = 300
+    starts = [7, 400, 1000]
+    rows = 1024
+    q = torch.randn(B * T, H, d, generator=g, device=DEV).to(qt)
+    w = torch.randn(B * T, H, generator=g, device=DEV) / math.sqrt(H)
+    k = torch.randn(rows, d, generator=g, device=DEV).to(kt)
+    q_pos = _i32([p for n in n_kv for p in (n - 1, 0, n // 2, n + 5, -1)])
+    batch = L.Batch(_i32(n_kv), T, max_n, kv_start=_i32(starts), q_pos=q_pos)
+    s = torch.full((B * T, max_n), 12345.0, device=DEV)
+    L.idx_score(q, w, k, batch, scores=s)
+    torch.cuda.synchronize()
+    qh, wh, kh, sh, qp = np64(q), np64(w), np64(k), s.cpu().numpy(), q_pos.cpu().numpy()
+    for r in range(B * T):
+        b = r // T
+        nv = O.visible_count(n_kv[b], int(qp[r]))
+        ref = O.indexer_scores(qh[r], wh[r], kh[starts[b]:starts[b] + nv])
+        assert_scores_close(sh[r, :nv], ref, f"row {r}")
+        assert np.all(sh[r, nv:] == 12345.0), "entries past the visible keys must be untouched"
+
+
+def test_score_block_mode_counts_complete_blocks():
+    g = torch.Generator(device=DEV).manual_seed(31)
+    C, H, d = 4, 8, 128
+    n_kv = [37, 4, 3, 64]
+    B = len(n_kv)
+    stride = 16
+    pooled = torch.randn(B * stride, d, generator=g, device=DEV)
+    q = torch.randn(B, H, d, generator=g, device=DEV).to(torch.bfloat16)
+    w = torch.randn(B, H, generator=g, device=DEV)
+    batch = L.Batch(_i32(n_kv), 1, 64, kv_seq_stride=stride)
+    s = torch.full((B, stride), -7.0, device=DEV)
+    L.idx_score(q, w, pooled, batch, block_size=C, scores=s)
+    torch.cuda.synchronize()
+    for b, n in enumerate(n_kv):
+        nb = n // C
+        ref = O.indexer_scores(np64(q[b]), np64(w[b]), np64(pooled[b * stride:b * stride + nb]))
+        assert_scores_close(s[b, :nb].cpu().numpy(), ref, f"seq {b}")
+        assert torch.all(s[b, nb:] == -7.0)
+
+
+# ------------------------------------------------------------------ top-k (bit-exact: same f32 scores on both sides)
+
+def _scores_cases():
+    g = torch.Generator().manual_seed(41)
+    yield "ties_small_ints", torch.randint(-3, 4, (6, 5000), generator=g).float()
+    yield "normal", torch.randn(6, 5000, generator=g)
+    yield "constant", torch.zeros(3, 3000)
+    z = torch.randint(0, 2, (3, 4000), generator=g).float()
+    z[z == 0] = -0.0
+    z[:, ::7] = 0.0
+    yield "signed_zero_ties", z
+    yield "one_long_row", torch.randn(1, 131072, generator=g) * 8 + 3
+    x = torch.randn(2, 70000, generator=g)
+    x[:, 1000:1100] = x.max() + 1.0  # exact ties straddling the threshold
+    yield "tie_block_at_top", x
+
+
+@pytest.mark.parametrize("case", [c for c, _ in _scores_cases()])
+@pytest.mark.parametrize("top_k", [1, 64, 2048])
+def test_topk_bit_exact(case, top_k):
+    scores = dict(_scores_cases())[case]
+    rows, n = scores.shape
+    n_kv = [n - 37 * r for r in range(rows)]
+    s = scores.to(DEV)
+    batch = L.Batch(_i32(n_kv), 1, n, kv_seq_stride=0)
+    idx, n_sel = L.idx_topk(s, batch, top_k)
+    torch.cuda.synchronize()
+    idx_h, ns_h = idx.cpu().numpy(), n_sel.cpu().numpy()
+    for r in range(rows):
+        ref = O.topk_select(scores[r].numpy(), n_kv[r], top_k)
+        assert ns_h[r] == len(ref)
+        assert idx_h[r, :len(ref)].tolist() == ref.tolist(), f"row {r}"
+        assert np.all(idx_h[r, len(ref):] == -1)
+
+
+def test_topk_causal_rows_and_dense_short_rows():
+    g = torch.Generator().manual_seed(42)
+    T, n, top_k = 300, 3000, 100
+    scores = torch.randint(-5, 6, (T, n), generator=g).float()
+    q_pos = [int(x) for x in torch.randint(-2, n + 3, (T,), generator=g)]
+    batch = L.Batch(_i32([n]), T, n, kv_seq_stride=0, q_pos=_i32(q_pos))
+    idx, n_sel = L.idx_topk(scores.to(DEV), batch, top_k)
+    idx_h, ns_h = idx.cpu().numpy(), n_sel.cpu().numpy()
+    for t in range(T):
+        nv = O.visible_count(n, q_pos[t])
+        ref = O.topk_select(scores[t].numpy(), nv, top_k)
+        assert ns_h[t] == len(ref) and idx_h[t, :len(ref)].tolist() == ref.tolist(), t
+
+
+@pytest.mark.parametrize("C,top_k", [(64, 2048), (4, 10), (3, 2), (8, 8)])
+def test_topk_block_mode_bit_exact(C, top_k):
+    g = torch.Generator().manual_seed(43 + C)
+    n_vis = [top_k + C - 1, top_k + C, 0, 1, C - 1, 5 * top_k + 3, 40 * C + 17, 2 * C]
+    B = len(n_vis)
+    nb_max = max(n_vis) // C + 1
+    bscores = torch.randint(-2, 3, (B, nb_max), generator=g).float()
+    batch = L.Batch(_i32(n_vis), 1, max(n_vis), kv_seq_stride=0)
+    idx, n_sel = L.idx_topk(bscores.to(DEV), batch, top_k, block_size=C)
+    idx_h, ns_h = idx.cpu().numpy(), n_sel.cpu().numpy()
+    cap = L.topk_capacity(top_k, C)
+    assert idx_h.shape[1] == cap
+    for b, nv in enumerate(n_vis):
+        ref = O.block_select(bscores[b].numpy(), nv, top_k, C)
+        assert ns_h[b] == len(ref), b
+        assert idx_h[b, :len(ref)].tolist() == ref.tolist(), b
+        assert np.all(idx_h[b, len(ref):] == -1)
+
+
+# ------------------------------------------------------------------ block pool
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float16, 64), (torch.float32, 128)])
+def test_block_pool_matches_oracle(dtype, d):
+    g = torch.Generator(device=DEV).manual_seed(51)
+    C = 64
+    n_kv = [32768 - 4 * s for s in range(3)] + [63, 64, 0]
+    B = len(n_kv)
+    stride_rows = 32768
+    k = torch.randn(B * stride_rows, d, generator=g, device=DEV).to(dtype)
+    batch = L.Batch(_i32(n_kv), 1, 32768, kv_seq_stride=stride_rows)
+    pooled = L.idx_block_pool(k, batch, C, pool_seq_stride=512)
+    torch.cuda.synchronize()
+    kh = np64(k)
+    for b, n in enumerate(n_kv):
+        ref = O.block_pool(kh[b * stride_rows:b * stride_rows + n], C, n)
+        got = pooled[b, :n // C].cpu().numpy()
+        np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-6)
+
+
+# ------------------------------------------------------------------ attention over generator-drawn index sets
+
+def _random_sel(g, n_kv, sizes, rows):
+    idx = torch.full((rows, max(sizes)), -1, dtype=torch.int32)
+    for r in range(rows):
+        perm = torch.randperm(n_kv, generator=g)[:sizes[r]]     # unsorted on purpose
+        idx[r, :sizes[r]] = perm.to(torch.int32)
+    return idx
+
+
+@pytest.mark.parametrize("dtype,out_dtype", [(torch.bfloat16, torch.bfloat16), (torch.bfloat16, torch.float32),
+                                             (torch.float32, torch.float32)])
+def test_attention_gqa_matches_oracle(dtype, out_dtype):
+    g = torch.Generator().manual_seed(61)
+    B, Hq, Hkv, dh, n_kv = 5, 32, 4, 128, 3000
+    sizes = [1, 31, 33, 2048, 2111]
+    q = torch.randn(B, Hq, dh, generator=g).to(dtype)
+    K = torch.randn(B * n_kv, Hkv, dh, generator=g).to(dtype)
+    V = torch.randn(B * n_kv, Hkv, dh, generator=g).to(dtype)
+    idx = _random_sel(g, n_kv, sizes, B)
+    batch = L.Batch(_i32([n_kv] * B), 1, n_kv, kv_seq_stride=n_kv)
+    out = L.sparse_attn_decode(q.to(DEV), K.to(DEV), V.to(DEV), batch, idx.to(DEV), _i32(sizes), 1 / math.sqrt(dh),
+                               out_dtype=out_dtype)
+    got = np64(out)
+    tol = 1e-4 if (dtype == torch.float32 and out_dtype == torch.float32) else 2e-2
+    Kh, Vh = np64(K), np64(V)
+    for r in range(B):
+        sel = idx[r, :sizes[r]].numpy()
+        ref = O.sparse_attention_gqa(np64(q[r]), Kh[r * n_kv:(r + 1) * n_kv], Vh[r * n_kv:(r + 1) * n_kv], sel,
+                                     1 / math.sqrt(dh))
+        assert np.max(np.abs(got[r] - ref)) <= tol, r
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_attention_mla_matches_oracle(out_dtype):
+    g = torch.Generator().manual_seed(62)
+    B, Hq, dk, dv, n_kv = 3, 128, 576, 512, 4096
+    sizes = [2048, 1, 700]
+    q = torch.randn(B, Hq, dk, generator=g).to(torch.bfloat16)
+    lat = torch.randn(B * n_kv, dk, generator=g).to(torch.bfloat16)
+    idx = _random_sel(g, n_kv, sizes, B)
+    batch = L.Batch(_i32([n_kv] * B), 1, n_kv, kv_seq_stride=n_kv)
+    scale = 1 / math.sqrt(192)
+    out = L.sparse_attn_decode(q.to(DEV), lat.to(DEV), None, batch, idx.to(DEV), _i32(sizes), scale,
+                               out_dtype=out_dtype, dv=dv)
+    got = np64(out)
+    lh = np64(lat)
+    for r in range(B):
+        ref = O.sparse_attention_mla(np64(q[r]), lh[r * n_kv:(r + 1) * n_kv], idx[r, :sizes[r]].numpy(), scale, dv)
+        assert np.max(np.abs(got[r] - ref)) <= 2e-2, r
+
+
+def test_attention_empty_selection_gives_zeros_and_bad_index_is_flagged():
+    B, Hq, dh, n_kv = 2, 4, 32, 64
+    q = torch.randn(B, Hq, dh, device=DEV)
+    K = torch.randn(B * n_kv, 1, dh, device=DEV)
+    V = torch.randn(B * n_kv, 1, dh, device=DEV)
+    idx = _i32([[3, 5, 7], [1, 999, 2]])              # 999 is outside sequence 1
+    n_sel = _i32([0, 3])
+    batch = L.Batch(_i32([n_kv] * B), 1, n_kv, kv_seq_stride=n_kv)
+    assert L.idx_device_status(reset=True) == 0
+    out = L.sparse_attn_decode(q, K, V, batch, idx, n_sel, 0.5)
+    assert L.idx_device_status(reset=True) == L.IDX_ERR_DEVICE_BOUNDS
+    assert torch.all(out[0] == 0)
+    ref = O.sparse_attention_gqa(np64(q[1]), np64(K[n_kv:]), np64(V[n_kv:]), [1, 2], 0.5)
+    assert np.max(np.abs(np64(out[1]) - ref)) <= 1e-4
+
+
+# ------------------------------------------------------------------ score (tensor-core decode scorer: H=64, d=128)
+
+@pytest.mark.parametrize("qt,kt", [(torch.bfloat16, torch.float16), (torch.float16, torch.bfloat16),
+                                   (torch.float32, torch.float16)])
+def test_score_tensor_core_decode_matches_oracle(qt, kt):
+    g = torch.Generator(device=DEV).manual_seed(71)
+    n_kv = [0, 1, 129, 8192, 300, 128, 5000]
+    starts = [0, 3, 100, 500, 9000, 9400, 9600]
+    B, H, d, rows = len(n_kv), 64, 128, 14700
+    q = torch.randn(B, H, d, generator=g, device=DEV).to(qt)
+    w = torch.randn(B, H, generator=g, device=DEV) / 8
+    k = torch.randn(rows, d, generator=g, device=DEV).to(kt)
+    batch = L.Batch(_i32(n_kv), 1, 8192, kv_start=_i32(starts))
+    s = torch.full((B, 8192), 777.0, device=DEV)
+    L.idx_score(q, w, k, batch, scores=s)
+    torch.cuda.synchronize()
+    sh, kh = s.cpu().numpy(), np64(k)
+    for b, n in enumerate(n_kv):
+        ref = O.indexer_scores(np64(q[b]), np64(w[b]), kh[starts[b]:starts[b] + n])
+        assert_scores_close(sh[b, :n], ref, f"seq {b}")
+        assert np.all(sh[b, n:] == 777.0)
+
+
+def test_score_tensor_core_one_short_row_many_idle_ctas():
+    # far fewer tiles than SMs: most CTAs get an empty share
+    g = torch.Generator(device=DEV).manual_seed(72)
+    q = torch.randn(1, 64, 128, generator=g, device=DEV).to(torch.bfloat16)
+    w = torch.randn(1, 64, generator=g, device=DEV)
+    k = torch.randn(300, 128, generator=g, device=DEV).to(torch.float16)
+    batch = L.Batch(_i32([300]), 1, 300, kv_seq_stride=0)
+    s = L.idx_score(q, w, k, batch)
+    ref = O.indexer_scores(np64(q[0]), np64(w[0]), np64(k))
+    assert_scores_close(s[0].cpu().numpy(), ref)

@@ -344,3 +344,33 @@ def test_attention_large_logits_limit():
     best = [0, 2, 3, 5][int(np.argmax(K[[0, 2, 3, 5], 0] @ q[0]))]
     assert np.all(np.isfinite(out))
     np.testing.assert_allclose(out[0], V[best, 0], rtol=1e-9, atol=1e-12)
+
+
+def test_hadamard_store_close_to_exact_rotation():
+    # the f32 butterflies land within one storage ulp (+ the f32 error bound) of the exact
+    # rotation rounded once, and agree with it on almost every element
+    rng = np.random.default_rng(18)
+    for fmt, p in (("bf16", 8), ("f16", 11)):
+        x = O.round_to_storage(rng.standard_normal((400, 128)), fmt)
+        got = O.hadamard_store(x, fmt)
+        exact = O.hadamard_rotate(x)
+        ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(exact), 1e-30))) - (p - 1))
+        f32_bound = 8 * 2.0 ** -24 * np.abs(x).sum(axis=1, keepdims=True) / math.sqrt(128)
+        assert np.all(np.abs(got - exact) <= ulp + f32_bound)
+        assert np.mean(got == O.round_to_storage(exact, fmt)) > 0.995
+    # f32 storage: the f32 result itself, close to the exact rotation
+    x = rng.standard_normal((10, 64))
+    np.testing.assert_allclose(O.hadamard_store(x, "f32"), O.hadamard_rotate(x.astype(np.float32)), rtol=0, atol=1e-5)
+
+
+def test_hadamard_store_exact_on_integer_inputs():
+    # small integers: every butterfly is exact in f32, so only the final scale and rounding remain
+    rng = np.random.default_rng(19)
+    x = rng.integers(-8, 9, (20, 32)).astype(float)
+    sums = O.hadamard_rotate(x) * math.sqrt(32)          # integer Walsh sums
+    np.testing.assert_allclose(sums, np.round(sums), atol=1e-9)
+    expect = O.round_to_storage((np.round(sums).astype(np.float32) * np.float32(1 / math.sqrt(32))).astype(np.float64), "bf16")
+    np.testing.assert_array_equal(O.hadamard_store(x, "bf16"), expect)
+    # an involution up to rounding: applying it twice returns the input
+    y = O.hadamard_store(O.hadamard_store(x, "f32"), "f32")
+    np.testing.assert_allclose(y, x, atol=1e-5)
