@@ -237,6 +237,11 @@ def _attn(fn_name, q, k, v, batch, idx, n_sel, scale, out, out_dtype, workspace,
         v_row_stride = v.stride(0)
     if out is None:
         out = torch.empty(rows, Hq, dv, device=q.device, dtype=out_dtype)
+    if workspace is None:
+        op = IDX_OP_ATTN_PREFILL if fn_name == "sparse_attn_prefill" else IDX_OP_ATTN_DECODE
+        need = idx_workspace_size(op, rows, batch.max_n_kv, idx.stride(0), Hq, dv)
+        if need:
+            workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     fn = getattr(load(), fn_name)
     _check(fn(_ptr(q), _dtype(q), Hq, hkv, dk, dv, _ptr(k), _ptr(v), kv_row_stride, v_row_stride,

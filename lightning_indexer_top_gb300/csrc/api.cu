@@ -91,8 +91,6 @@ idx_status attn_common(const char* what, const void* q, idx_dtype dtype, int32_t
                        int64_t v_row_stride, int64_t kv_rows, idx_batch batch, const int32_t* idx,
                        int64_t idx_row_stride, const int32_t* n_sel, float scale, void* out,
                        idx_dtype out_dtype, void* ws, size_t ws_bytes, cudaStream_t st) {
-    (void)ws;
-    (void)ws_bytes;
     idx_status s = check_batch(batch, what);
     if (s != IDX_OK) return s;
     const int64_t rows = (int64_t)batch.n_seq * batch.n_q_per_seq;
@@ -116,6 +114,15 @@ idx_status attn_common(const char* what, const void* q, idx_dtype dtype, int32_t
     if (!q || !k || !idx || !n_sel || !out)
         return fail(IDX_ERR_INVALID_ARG, "%s: NULL q/k/idx/n_sel/out", what);
     const Geom g = make_geom(batch);
+    if (mla_tc_supported(dtype, Hq, Hkv, dk, dv, k, v, kv_row_stride, kv_rows, q, out)) {
+        const size_t need = mla_workspace_bytes(rows, idx_row_stride);
+        if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws)))
+            return fail(IDX_ERR_INVALID_ARG,
+                        "%s: needs a 16-byte aligned workspace of %zu bytes (idx_workspace_size)", what, need);
+        return from_cuda(launch_attn_mla_tc(q, k, kv_row_stride, kv_rows, g, idx, idx_row_stride, n_sel, scale,
+                                            out, out_dtype, ws, ws_bytes, st),
+                         what);
+    }
     return from_cuda(launch_attn_generic(q, dtype, Hq, Hkv, dk, dv, k, v, kv_row_stride,
                                          v_row_stride, kv_rows, g, idx, idx_row_stride, n_sel,
                                          scale, out, out_dtype, st),
@@ -274,12 +281,10 @@ idx_status sparse_attn_prefill(const void* q, idx_dtype dtype, int32_t n_q_heads
 
 size_t idx_workspace_size(int32_t op, int64_t n_rows, int32_t max_n_kv, int32_t top_k,
                           int32_t n_q_heads, int32_t dv) {
-    (void)op;
-    (void)n_rows;
     (void)max_n_kv;
-    (void)top_k;
-    (void)n_q_heads;
-    (void)dv;
+    if (n_rows <= 0 || top_k <= 0) return 0;
+    if ((op == IDX_OP_ATTN_DECODE || op == IDX_OP_ATTN_PREFILL) && n_q_heads == 128 && dv == 512)
+        return mla_workspace_bytes(n_rows, top_k);
     return 0;
 }
 

@@ -1,0 +1,643 @@
+// Sparse MLA attention on the 5th-generation tensor cores: 128 query heads
+// over the selected rows of a 576-wide bf16 latent cache, value = the first
+// 512 columns of the same row ("Gather OpenPangu DSA decode reads" and
+// "openpangu: MLA-latent KV cache", ik_llama_opt commit log):
+//     l[h, j] = scale * q[h] . c_j,   o[h] = sum_j softmax_j(l)[h, j] * c_j[0:512]
+// over j in the row's selected positions.
+//
+// The output accumulator O [128 heads x 512] f32 fills all 512 TMEM columns,
+// so one work unit (query row, key split) runs on a CLUSTER OF TWO CTAs:
+//   rank 0: Q [128 x 576] bf16 lives in TMEM (288 columns) as the MMA A
+//           operand; key tiles of 64 selected rows x 576 are gathered by TMA
+//           (tile::gather4, 128-byte swizzle) into a 2-stage ring;
+//           S = Q K^T (M=128 heads, N=64 keys, K=576) goes to one of two TMEM
+//           buffers; four softmax warps (thread = head) turn S into
+//           P = exp2(S*scale*log2e - m) as bf16 and bulk-copy P, the
+//           per-head rescale factor, row sum and max to rank 1 over DSMEM.
+//   rank 1: O lives in TMEM (512 columns); value tiles (the same rows, first
+//           512 columns) are gathered into its own ring; O += P V with P as a
+//           K-major and V as an MN-major shared-memory operand (M=128,
+//           N=256 x 2, K=16 x 4).  Four correction warps rescale O when
+//           rank 0 raised a row maximum by more than 2^8 (rare after the
+//           first tiles, so P stays <= 2^8 otherwise) and finally write
+//           O / l, or the unnormalised partial (O, m, l) of a key split.
+// Key splits (few query rows) are merged by a small combine kernel.
+// Padding and invalid indices gather a valid row and get p = 0.  Every wait
+// is bounded; a timeout records IDX_ERR_TIMEOUT and the cluster winds down.
+#include "lidx_internal.cuh"
+#include "sm100_ptx.cuh"
+
+namespace lidx {
+namespace {
+using namespace sm100;
+
+constexpr int kHq = 128;
+constexpr int kDk = 576;
+constexpr int kDv = 512;
+constexpr int kKeys = 64;                               // keys per tile
+constexpr int kDkBlocks = kDk / 64;                     // 9 column blocks of 128 bytes
+constexpr int kDvBlocks = kDv / 64;                     // 8
+constexpr int kBlockBytes = kKeys * 128;                // one column block of a tile
+constexpr int kKTileBytes = kDkBlocks * kBlockBytes;    // 73728
+constexpr int kVTileBytes = kDvBlocks * kBlockBytes;    // 65536
+constexpr int kStages = 2;
+constexpr int kPBytes = kHq * kKeys * 2;                // P tile, bf16, 128-byte swizzle K-major
+constexpr int kPktBytes = kPBytes + 3 * kHq * 4 + 16;   // P + alpha + l + m + flag
+constexpr int kPktStride = 18432;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kSCol0 = 320;                             // rank 0: S buffers at 320 and 384 (Q at 0..287)
+constexpr float kRescaleLog2 = 8.f;
+
+struct PktTail {
+    float alpha[kHq];
+    float l[kHq];
+    float m[kHq];
+    int flag;
+    int pad[3];
+};
+static_assert(kPBytes + sizeof(PktTail) == kPktBytes, "packet layout");
+
+struct Ctl {
+    uint64_t xfull[kStages];
+    uint64_t xempty[kStages];
+    uint64_t sfull[2];
+    uint64_t sempty[2];
+    uint64_t pfree[2];
+    uint64_t pfull[2];
+    uint64_t cdone[2];
+    uint64_t pvdone[2];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+    uint32_t warp_flags[4];
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kKTileBytes + 2 * kPktStride + sizeof(Ctl);
+
+__device__ __forceinline__ void abort_cta(Ctl& c, int* status) {
+    *(volatile int*)&c.abort = 1;
+    flag(status, IDX_ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ bool aborted(Ctl& c) { return *(volatile int*)&c.abort != 0; }
+
+// the whole warp sees the same answer
+__device__ __forceinline__ bool warp_aborted(Ctl& c) { return __any_sync(0xffffffffu, aborted(c)); }
+
+struct Unit {
+    int64_t r;        // query row
+    int k0, k1;       // selected-key range [k0, k1) of this split
+    int n_tiles;
+    int64_t row0;     // cache row of position 0 of the row's sequence
+    int n_kv;         // keys of the sequence
+    int64_t fallback; // an in-bounds cache row for padding keys
+};
+
+__device__ __forceinline__ Unit make_unit(const Geom& g, const int32_t* n_sel, int64_t idx_row_stride,
+                                          int64_t kv_rows, int splits, int kps) {
+    Unit u;
+    const int64_t unit = blockIdx.x >> 1;
+    u.r = unit / splits;
+    const int s = (int)(unit % splits);
+    int ns = n_sel[u.r];
+    if (ns < 0 || ns > idx_row_stride) ns = ns < 0 ? 0 : (int)idx_row_stride;
+    u.k0 = s * kps;
+    u.k1 = min(ns, u.k0 + kps);
+    u.n_tiles = u.k1 > u.k0 ? (u.k1 - u.k0 + kKeys - 1) / kKeys : 0;
+    const int b = (int)(u.r / g.T);
+    u.n_kv = seq_n_kv(g, b);
+    u.row0 = seq_row0(g, b);
+    int64_t fb = u.row0;
+    if (fb < 0) fb = 0;
+    if (fb >= kv_rows) fb = kv_rows - 1;
+    u.fallback = fb;
+    return u;
+}
+
+// cache row of selected key j (padding and invalid indices -> the fallback row)
+__device__ __forceinline__ int32_t key_row(const Unit& u, const int32_t* idx, int64_t idx_row_stride,
+                                           int64_t kv_rows, int j, bool& valid) {
+    valid = false;
+    if (j >= u.k1) return (int32_t)u.fallback;
+    const int pos = idx[u.r * idx_row_stride + j];
+    const int64_t row = u.row0 + pos;
+    if (pos >= 0 && pos < u.n_kv && row >= 0 && row < kv_rows) {
+        valid = true;
+        return (int32_t)row;
+    }
+    return (int32_t)u.fallback;
+}
+
+// producer: gather the tile's 64 rows, `nblocks` column blocks of 64 elements each
+__device__ __forceinline__ void gather_tiles(Ctl& c, uint8_t* xtiles, const CUtensorMap* map, const Unit& u,
+                                             const int32_t* idx, int64_t idx_row_stride, int64_t kv_rows,
+                                             int nblocks, int* status, bool report) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t tile_bytes = (uint32_t)nblocks * kBlockBytes;
+    for (int t = 0; t < u.n_tiles; ++t) {
+        const int stage = t & 1;
+        const uint32_t ph = (uint32_t)((t >> 1) & 1);
+        const int j0 = u.k0 + t * kKeys;
+        bool va, vb;
+        const int32_t ra = key_row(u, idx, idx_row_stride, kv_rows, j0 + lane, va);
+        const int32_t rb = key_row(u, idx, idx_row_stride, kv_rows, j0 + 32 + lane, vb);
+        if (report && ((j0 + lane < u.k1 && !va) || (j0 + 32 + lane < u.k1 && !vb)))
+            flag(status, IDX_ERR_DEVICE_BOUNDS);
+        if (lane == 0) {
+            if (!mbar_wait(&c.xempty[stage], ph ^ 1)) {
+                abort_cta(c, status);
+            } else {
+                mbar_arrive_expect_tx(&c.xfull[stage], tile_bytes);
+            }
+        }
+        if (warp_aborted(c)) break;
+        // lane g < 16 issues the gathers of keys 4g .. 4g+3
+        int32_t rows[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int key = 4 * (lane & 15) + i;
+            const int32_t xa = __shfl_sync(0xffffffffu, ra, key & 31);
+            const int32_t xb = __shfl_sync(0xffffffffu, rb, key & 31);
+            rows[i] = key < 32 ? xa : xb;
+        }
+        if (lane < 16) {
+            uint8_t* dst = xtiles + (size_t)stage * kKTileBytes + lane * 4 * 128;
+            for (int db = 0; db < nblocks; ++db)
+                tma_gather4(dst + db * kBlockBytes, map, &c.xfull[stage], db * 64, rows[0], rows[1], rows[2],
+                            rows[3]);
+        }
+        __syncwarp();
+    }
+    // no TMA writes may be in flight when the CTA leaves
+    if (lane == 0) {
+        const int n = min(u.n_tiles, kStages);
+        for (int t = u.n_tiles - n; t < u.n_tiles; ++t) mbar_wait(&c.xfull[t & 1], (uint32_t)((t >> 1) & 1));
+    }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_attn_tc_kernel(const __grid_constant__ CUtensorMap lat_map, const __nv_bfloat16* __restrict__ q, Geom g,
+                       const int32_t* __restrict__ idx, int64_t idx_row_stride,
+                       const int32_t* __restrict__ n_sel, int64_t kv_rows, float scale_log2, int splits,
+                       int kps, void* __restrict__ out, int out_dtype, float* __restrict__ part_o,
+                       float* __restrict__ part_ml) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* xtiles = smem;                                         // K tiles (rank 0) / V tiles (rank 1)
+    uint8_t* pkts = smem + (size_t)kStages * kKTileBytes;           // P staging (rank 0) / P received (rank 1)
+    Ctl& c = *reinterpret_cast<Ctl*>(pkts + 2 * kPktStride);
+
+    const uint32_t rank = cluster_ctarank();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Unit u = make_unit(g, n_sel, idx_row_stride, kv_rows, splits, kps);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&c.xfull[i], 1);
+            mbar_init(&c.xempty[i], 1);
+            mbar_init(&c.sfull[i], 1);
+            mbar_init(&c.sempty[i], 4);
+            mbar_init(&c.pfree[i], 1);
+            mbar_init(&c.pfull[i], 1);
+            mbar_init(&c.cdone[i], 4);
+            mbar_init(&c.pvdone[i], 1);
+        }
+        mbar_init(&c.done, 1);
+        c.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&lat_map);
+    if (warp == 1) {
+        tmem_alloc(&c.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = c.tmem_base;
+    const int quad = warp & 3;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+
+    // rank 0: load this row's Q into TMEM columns [0, 288), thread = head
+    if (rank == 0 && warp >= 2 && u.n_tiles > 0) {
+        const int h = quad * 32 + lane;
+        const uint4* src = reinterpret_cast<const uint4*>(q + (u.r * kHq + h) * (int64_t)kDk);
+        for (int cb = 0; cb < kDkBlocks; ++cb) {
+            uint32_t regs[32];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint4 x = src[cb * 8 + i];
+                regs[4 * i] = x.x;
+                regs[4 * i + 1] = x.y;
+                regs[4 * i + 2] = x.z;
+                regs[4 * i + 3] = x.w;
+            }
+            tmem_st_32x32b_x32(tmem + lane_off + cb * 32, regs);
+        }
+        tmem_st_wait();
+    }
+    tc_fence_before();
+    cluster_sync();  // barriers of both CTAs initialised, Q in TMEM
+    tc_fence_after();
+
+    if (rank == 0) {
+        if (warp == 0) {
+            gather_tiles(c, xtiles, &lat_map, u, idx, idx_row_stride, kv_rows, kDkBlocks, g.status, true);
+        } else if (warp == 1) {
+            if (lane == 0) {
+                const uint32_t idesc = idesc_f16_f32_major(kHq, kKeys, 1, 0, 0);
+                for (int t = 0; t < u.n_tiles; ++t) {
+                    const int stage = t & 1, sb = t & 1;
+                    const uint32_t ph = (uint32_t)((t >> 1) & 1);
+                    if (aborted(c)) break;
+                    if (!mbar_wait(&c.xfull[stage], ph) || !mbar_wait(&c.sempty[sb], ph ^ 1)) {
+                        abort_cta(c, g.status);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kb = smem_u32(xtiles + (size_t)stage * kKTileBytes);
+                    const uint32_t d = tmem + kSCol0 + sb * kKeys;
+#pragma unroll 4
+                    for (int ks = 0; ks < kDk / 16; ++ks) {
+                        const uint64_t bd = desc_sw128_kmajor(kb + (ks >> 2) * kBlockBytes + (ks & 3) * 32, 1024);
+                        mma_f16_ts(d, tmem + ks * 8, bd, idesc, ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&c.xempty[stage]);
+                    mma_commit(&c.sfull[sb]);
+                }
+                mma_commit(&c.done);
+                mbar_wait(&c.done, 0);
+            }
+            __syncwarp();
+        } else {
+            // ---------------------------------------------------------- softmax (thread = head)
+            const int h = quad * 32 + lane;
+            const bool leader = (warp == 2 && lane == 0);
+            float m_used = 0.f, lsum = 0.f;
+            bool has_m = false;
+            for (int t = 0; t < u.n_tiles; ++t) {
+                const int sb = t & 1, j = t & 1;
+                const uint32_t ph = (uint32_t)((t >> 1) & 1);
+                const int j0 = u.k0 + t * kKeys;
+                bool va, vb;
+                key_row(u, idx, idx_row_stride, kv_rows, j0 + lane, va);
+                key_row(u, idx, idx_row_stride, kv_rows, j0 + 32 + lane, vb);
+                const uint32_t ma = __ballot_sync(0xffffffffu, va);
+                const uint32_t mb = __ballot_sync(0xffffffffu, vb);
+                // every softmax warp runs both named barriers of every tile, also after an
+                // abort (then with zero scores and no waits), so none can be left behind
+                bool live = !warp_aborted(c);
+                if (live && !warp_wait(&c.sfull[sb], ph)) {
+                    abort_cta(c, g.status);
+                    live = false;
+                }
+                float s0[32], s1[32];
+                if (live) {
+                    tc_fence_after();
+                    tmem_ld_32x32b_x32(tmem + lane_off + kSCol0 + sb * kKeys, s0);
+                    tmem_ld_32x32b_x32(tmem + lane_off + kSCol0 + sb * kKeys + 32, s1);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&c.sempty[sb]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s0[i] = s1[i] = 0.f;
+                }
+
+                float mt = -3.0e38f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    s0[i] *= scale_log2;
+                    s1[i] *= scale_log2;
+                    if ((ma >> i) & 1u) mt = fmaxf(mt, s0[i]);
+                    if ((mb >> i) & 1u) mt = fmaxf(mt, s1[i]);
+                }
+                float alpha = 1.f;
+                if ((ma | mb) != 0u) {
+                    if (!has_m) {
+                        m_used = mt;
+                        has_m = true;
+                    } else if (mt > m_used + kRescaleLog2) {
+                        alpha = exp2f(m_used - mt);
+                        lsum *= alpha;
+                        m_used = mt;
+                    }
+                }
+                uint32_t pk[32];
+                float psum = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ((ma >> (2 * i)) & 1u) ? exp2f(s0[2 * i] - m_used) : 0.f;
+                    const float p1 = ((ma >> (2 * i + 1)) & 1u) ? exp2f(s0[2 * i + 1] - m_used) : 0.f;
+                    const float p2 = ((mb >> (2 * i)) & 1u) ? exp2f(s1[2 * i] - m_used) : 0.f;
+                    const float p3 = ((mb >> (2 * i + 1)) & 1u) ? exp2f(s1[2 * i + 1] - m_used) : 0.f;
+                    psum += (p0 + p1) + (p2 + p3);
+                    const __nv_bfloat162 a = __floats2bfloat162_rn(p0, p1);
+                    const __nv_bfloat162 bb = __floats2bfloat162_rn(p2, p3);
+                    pk[i] = *reinterpret_cast<const uint32_t*>(&a);
+                    pk[16 + i] = *reinterpret_cast<const uint32_t*>(&bb);
+                }
+                lsum += psum;
+                const uint32_t resc = __ballot_sync(0xffffffffu, alpha != 1.f);
+
+                // staging buffer j is free once the copy of tile t-2 has read it
+                if (leader) bulk_wait_read<1>();
+                named_bar_sync(1, 128);
+                uint8_t* stage_p = pkts + j * kPktStride;
+                uint8_t* rowp = stage_p + (h >> 3) * 1024 + (h & 7) * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint4 v;
+                    v.x = pk[4 * ch];
+                    v.y = pk[4 * ch + 1];
+                    v.z = pk[4 * ch + 2];
+                    v.w = pk[4 * ch + 3];
+                    *reinterpret_cast<uint4*>(rowp + ((ch ^ (h & 7)) << 4)) = v;
+                }
+                PktTail& tail = *reinterpret_cast<PktTail*>(stage_p + kPBytes);
+                tail.alpha[h] = alpha;
+                tail.l[h] = lsum;
+                tail.m[h] = m_used;
+                if (lane == 0) c.warp_flags[quad] = resc;
+                fence_proxy_async_smem();
+                named_bar_sync(1, 128);
+                if (leader && !aborted(c)) {
+                    tail.flag = (c.warp_flags[0] | c.warp_flags[1] | c.warp_flags[2] | c.warp_flags[3]) ? 1 : 0;
+                    fence_proxy_async_smem();
+                    if (!mbar_wait(&c.pfree[j], ph ^ 1)) {
+                        abort_cta(c, g.status);
+                    } else {
+                        const uint32_t rbar = mapa(&c.pfull[j], 1);
+                        mbar_arrive_expect_tx_remote(rbar, kPktBytes);
+                        bulk_copy_s2cluster(mapa(stage_p, 1), stage_p, kPktBytes, rbar);
+                        bulk_commit();
+                    }
+                }
+            }
+            if (leader) {
+                bulk_wait_read<0>();
+                // rank 1's last arrivals on pfree land before this CTA may leave
+                const int n = min(u.n_tiles, 2);
+                for (int t = u.n_tiles - n; t < u.n_tiles; ++t)
+                    if (!aborted(c)) mbar_wait(&c.pfree[t & 1], (uint32_t)((t >> 1) & 1));
+            }
+        }
+    } else {
+        if (warp == 0) {
+            gather_tiles(c, xtiles, &lat_map, u, idx, idx_row_stride, kv_rows, kDvBlocks, g.status, false);
+        } else if (warp == 1) {
+            if (lane == 0) {
+                const uint32_t idesc = idesc_f16_f32_major(kHq, 256, 1, 0, 1);
+                for (int t = 0; t < u.n_tiles; ++t) {
+                    const int stage = t & 1, j = t & 1;
+                    const uint32_t ph = (uint32_t)((t >> 1) & 1);
+                    if (aborted(c)) break;
+                    if (!mbar_wait(&c.xfull[stage], ph) || !mbar_wait(&c.cdone[j], ph)) {
+                        abort_cta(c, g.status);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t pb = smem_u32(pkts + j * kPktStride);
+                    const uint32_t vb = smem_u32(xtiles + (size_t)stage * kKTileBytes);
+#pragma unroll
+                    for (int ks = 0; ks < kKeys / 16; ++ks) {
+                        const uint64_t ad = desc_sw128_kmajor(pb + ks * 32, 1024);
+#pragma unroll
+                        for (int nh = 0; nh < 2; ++nh) {
+                            const uint64_t bd = desc_sw128_mnmajor(vb + nh * 4 * kBlockBytes + ks * 2 * 1024,
+                                                                   kBlockBytes, 1024);
+                            mma_f16_ss(tmem + nh * 256, ad, bd, idesc, (t > 0 || ks > 0) ? 1u : 0u);
+                        }
+                    }
+                    mma_commit(&c.xempty[stage]);
+                    mma_commit(&c.pvdone[j]);
+                    mma_commit_multicast(&c.pfree[j], (uint16_t)0x1);
+                }
+                mma_commit(&c.done);
+                mbar_wait(&c.done, 0);
+            }
+            __syncwarp();
+        } else {
+            // ---------------------------------------------------------- correction + output (thread = head)
+            const int h = quad * 32 + lane;
+            bool ok = true;
+            for (int t = 0; t < u.n_tiles; ++t) {
+                const int j = t & 1;
+                const uint32_t ph = (uint32_t)((t >> 1) & 1);
+                if (warp_aborted(c) || !warp_wait(&c.pfull[j], ph)) {
+                    abort_cta(c, g.status);
+                    ok = false;
+                    break;
+                }
+                const PktTail& tail = *reinterpret_cast<const PktTail*>(pkts + j * kPktStride + kPBytes);
+                if (tail.flag && t > 0) {
+                    const int tp = t - 1;
+                    if (!warp_wait(&c.pvdone[tp & 1], (uint32_t)((tp >> 1) & 1))) {
+                        abort_cta(c, g.status);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const float a = tail.alpha[h];
+                    for (int cb = 0; cb < kDv / 32; ++cb) {
+                        float v[32];
+                        tmem_ld_32x32b_x32(tmem + lane_off + cb * 32, v);
+                        tmem_ld_wait();
+                        uint32_t w[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(v[i] * a);
+                        tmem_st_32x32b_x32(tmem + lane_off + cb * 32, w);
+                    }
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c.cdone[j]);
+            }
+            float lsum = 0.f, mrow = 0.f;
+            const bool have = ok && u.n_tiles > 0;
+            if (have) {
+                const int tl = u.n_tiles - 1;
+                if (!warp_wait(&c.pvdone[tl & 1], (uint32_t)((tl >> 1) & 1))) {
+                    abort_cta(c, g.status);
+                } else {
+                    tc_fence_after();
+                    const PktTail& tail = *reinterpret_cast<const PktTail*>(pkts + (tl & 1) * kPktStride + kPBytes);
+                    lsum = tail.l[h];
+                    mrow = tail.m[h];
+                }
+            }
+            const bool read_o = have && !warp_aborted(c);
+            const int64_t unit = blockIdx.x >> 1;
+            if (splits == 1) {
+                const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                const int64_t base = (u.r * kHq + h) * (int64_t)kDv;
+                for (int cb = 0; cb < kDv / 32; ++cb) {
+                    float v[32];
+                    if (read_o) {
+                        tmem_ld_32x32b_x32(tmem + lane_off + cb * 32, v);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    }
+                    if (out_dtype == IDX_BF16) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + base + cb * 32);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 pk;
+                            __nv_bfloat162 a0 = __floats2bfloat162_rn(v[8 * q4] * inv, v[8 * q4 + 1] * inv);
+                            __nv_bfloat162 a1 = __floats2bfloat162_rn(v[8 * q4 + 2] * inv, v[8 * q4 + 3] * inv);
+                            __nv_bfloat162 a2 = __floats2bfloat162_rn(v[8 * q4 + 4] * inv, v[8 * q4 + 5] * inv);
+                            __nv_bfloat162 a3 = __floats2bfloat162_rn(v[8 * q4 + 6] * inv, v[8 * q4 + 7] * inv);
+                            pk.x = *reinterpret_cast<uint32_t*>(&a0);
+                            pk.y = *reinterpret_cast<uint32_t*>(&a1);
+                            pk.z = *reinterpret_cast<uint32_t*>(&a2);
+                            pk.w = *reinterpret_cast<uint32_t*>(&a3);
+                            dst[q4] = pk;
+                        }
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + base + cb * 32);
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            dst[q4] = make_float4(v[4 * q4] * inv, v[4 * q4 + 1] * inv, v[4 * q4 + 2] * inv,
+                                                  v[4 * q4 + 3] * inv);
+                    }
+                }
+            } else {
+                float* po = part_o + (unit * kHq + h) * (int64_t)kDv;
+                for (int cb = 0; cb < kDv / 32; ++cb) {
+                    float v[32];
+                    if (read_o) {
+                        tmem_ld_32x32b_x32(tmem + lane_off + cb * 32, v);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    }
+                    float4* dst = reinterpret_cast<float4*>(po + cb * 32);
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        dst[q4] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+                }
+                part_ml[(unit * kHq + h) * 2] = mrow;
+                part_ml[(unit * kHq + h) * 2 + 1] = read_o ? lsum : 0.f;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // no cross-CTA traffic may target a CTA that has left
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Merge key splits: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s over splits with l_s > 0.
+__global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restrict__ part_o,
+                                                          const float* __restrict__ part_ml, int splits,
+                                                          void* __restrict__ out, int out_dtype) {
+    const int64_t r = blockIdx.x;
+    const int h = blockIdx.y;
+    const int c0 = threadIdx.x * 4;
+    float M = -3.0e38f;
+    bool any = false;
+    for (int s = 0; s < splits; ++s) {
+        const int64_t u = r * splits + s;
+        const float l = part_ml[(u * kHq + h) * 2 + 1];
+        if (l > 0.f) {
+            M = fmaxf(M, part_ml[(u * kHq + h) * 2]);
+            any = true;
+        }
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float den = 0.f;
+    if (any) {
+        for (int s = 0; s < splits; ++s) {
+            const int64_t u = r * splits + s;
+            const float l = part_ml[(u * kHq + h) * 2 + 1];
+            if (!(l > 0.f)) continue;
+            const float wgt = exp2f(part_ml[(u * kHq + h) * 2] - M);
+            den += wgt * l;
+            const float4 o = *reinterpret_cast<const float4*>(part_o + (u * kHq + h) * (int64_t)kDv + c0);
+            acc[0] += wgt * o.x;
+            acc[1] += wgt * o.y;
+            acc[2] += wgt * o.z;
+            acc[3] += wgt * o.w;
+        }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const int64_t base = (r * kHq + h) * (int64_t)kDv + c0;
+    if (out_dtype == IDX_BF16) {
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + base;
+        *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+        *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+    } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(out) + base) =
+            make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    }
+}
+
+}  // namespace
+
+// key splits per query row: enough clusters to cover the SMs when rows are few
+int mla_splits(int64_t n_rows, int64_t cap) {
+    if (n_rows <= 0) return 1;
+    int sms = sm_count();
+    if (sms < 2) sms = 152;
+    const int64_t clusters = sms / 2;
+    if (n_rows >= clusters) return 1;
+    const int64_t by_sm = clusters / n_rows;
+    const int64_t by_keys = (cap + 255) / 256;
+    int64_t s = by_sm < by_keys ? by_sm : by_keys;
+    return (int)(s < 1 ? 1 : s);
+}
+
+size_t mla_workspace_bytes(int64_t n_rows, int64_t cap) {
+    const int s = mla_splits(n_rows, cap);
+    if (s <= 1) return 0;
+    return (size_t)n_rows * s * kHq * (kDv + 2) * sizeof(float);
+}
+
+bool mla_tc_supported(int dtype, int Hq, int Hkv, int dk, int dv, const void* k, const void* v,
+                      int64_t kv_row_stride, int64_t kv_rows, const void* q, const void* out) {
+    return dtype == IDX_BF16 && !v && Hq == kHq && Hkv == 1 && dk == kDk && dv == kDv &&
+           kv_row_stride % 8 == 0 && kv_rows >= 1 && kv_rows <= INT32_MAX &&
+           !(reinterpret_cast<uintptr_t>(k) & 15u) && !(reinterpret_cast<uintptr_t>(q) & 15u) &&
+           !(reinterpret_cast<uintptr_t>(out) & 15u);
+}
+
+cudaError_t launch_attn_mla_tc(const void* q, const void* lat, int64_t kv_row_stride, int64_t kv_rows,
+                               const Geom& g, const int32_t* idx, int64_t idx_row_stride, const int32_t* n_sel,
+                               float scale, void* out, int out_dtype, void* ws, size_t ws_bytes,
+                               cudaStream_t st) {
+    const int64_t n_rows = (int64_t)g.B * g.T;
+    if (n_rows == 0) return cudaSuccess;
+    const int splits = mla_splits(n_rows, idx_row_stride);
+    const int64_t kps64 = ((idx_row_stride + splits - 1) / splits + kKeys - 1) / kKeys * kKeys;
+    float* part_o = nullptr;
+    float* part_ml = nullptr;
+    if (splits > 1) {
+        const size_t need = mla_workspace_bytes(n_rows, idx_row_stride);
+        if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 15u)) return cudaErrorInvalidValue;
+        part_o = static_cast<float*>(ws);
+        part_ml = part_o + (size_t)n_rows * splits * kHq * kDv;
+    }
+    CUtensorMap map;
+    if (!make_latent_tmap(&map, lat, kv_row_stride, kv_rows)) return cudaErrorNotSupported;
+    const int64_t grid = 2 * n_rows * splits;
+    if (grid > INT32_MAX) return cudaErrorNotSupported;
+    cudaFuncSetAttribute(mla_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    const float scale_log2 = scale * 1.4426950408889634f;
+    mla_attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(
+        map, static_cast<const __nv_bfloat16*>(q), g, idx, idx_row_stride, n_sel, kv_rows, scale_log2, splits,
+        (int)kps64, out, out_dtype, part_o, part_ml);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || splits == 1) return e;
+    mla_combine_kernel<<<dim3((unsigned)n_rows, kHq), 128, 0, st>>>(part_o, part_ml, splits, out, out_dtype);
+    return cudaGetLastError();
+}
+
+}  // namespace lidx

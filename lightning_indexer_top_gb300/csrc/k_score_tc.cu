@@ -28,8 +28,6 @@
 //               key per thread, then sum_h w_h*relu(d_h) and a coalesced store.
 // Every wait is bounded; a timeout records IDX_ERR_TIMEOUT and the CTA winds
 // down (drains its TMA loads and MMAs, frees TMEM) instead of hanging.
-#include <mutex>
-
 #include "lidx_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -102,6 +100,9 @@ __device__ __forceinline__ void abort_cta(Ctl& c, const Geom& g) {
     flag(g.status, IDX_ERR_TIMEOUT);
 }
 
+// the whole warp sees the same answer
+__device__ __forceinline__ bool warp_aborted(Ctl& c) { return __any_sync(0xffffffffu, *(volatile int*)&c.abort != 0); }
+
 template <typename TK>
 __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
     const __grid_constant__ CUtensorMap kmap, const void* __restrict__ q, int q_dtype,
@@ -167,13 +168,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
         int64_t seg = -1;
         int64_t issued = 0;
         for (int64_t i = 0; i < count; ++i) {
-            if (*(volatile int*)&c.abort) break;
+            if (warp_aborted(c)) break;
             if (i == 0 || cur.t == 0) {
                 // new query row: stage its q (converted, swizzled) as the MMA B operand
                 ++seg;
                 const int qb = (int)(seg & 1);
                 const uint32_t qph = (uint32_t)((seg >> 1) & 1);
-                if (!mbar_wait(&c.qempty[qb], qph ^ 1)) {
+                if (!warp_wait(&c.qempty[qb], qph ^ 1)) {
                     abort_cta(c, g);
                     break;
                 }
@@ -204,8 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
                     ++issued;
                 }
             }
-            __syncwarp();
-            if (*(volatile int*)&c.abort) break;
+            if (warp_aborted(c)) break;
             if (++stage == kStages) {
                 stage = 0;
                 phase ^= 1;
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
         uint32_t aphase = 0;
         float wv[kH];
         for (int64_t i = 0; i < count; ++i) {
-            if (*(volatile int*)&c.abort) break;
+            if (warp_aborted(c)) break;
             if (i == 0 || cur.t == 0) {
                 const float4* wr = reinterpret_cast<const float4*>(w + cur.r * kH);
 #pragma unroll
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
                     wv[4 * h4 + 3] = x.w;
                 }
             }
-            if (!mbar_wait(&c.tfull[acc], aphase)) {
+            if (!warp_wait(&c.tfull[acc], aphase)) {
                 abort_cta(c, g);
                 break;
             }
@@ -325,43 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ------------------------------------------------------------------ host side
-
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn encode_fn() {
-    static std::once_flag once;
-    static EncodeFn fn = nullptr;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeFn>(p);
-    });
-    return fn;
-}
-
 }  // namespace
-
-// 2-D tensor map over a [rows, 128] 16-bit key cache: boxes of 64 columns x
-// 128 rows with the 128-byte swizzle the MMA descriptors expect.
-bool make_key_tmap(CUtensorMap* m, const void* k, bool bf16, int64_t k_row_stride, int64_t k_rows,
-                   int box_rows) {
-    EncodeFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)k_rows};
-    cuuint64_t strides[1] = {(cuuint64_t)k_row_stride * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-              const_cast<void*>(k), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, int d, const void* k,
                             int k_dtype, int64_t k_row_stride, int64_t k_rows, const Geom& g, int block_size,

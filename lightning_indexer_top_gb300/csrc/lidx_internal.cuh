@@ -1,6 +1,7 @@
 // Internal declarations shared by the kernels and the C-ABI layer of liblidx.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -119,6 +120,21 @@ cudaError_t launch_attn_generic(const void* q, int dtype, int Hq, int Hkv, int d
                                 int64_t v_row_stride, int64_t kv_rows, const Geom& g,
                                 const int32_t* idx, int64_t idx_row_stride, const int32_t* n_sel,
                                 float scale, void* out, int out_dtype, cudaStream_t st);
+
+// tcgen05 sparse MLA attention (128 heads, 576/512 bf16 latent); the caller
+// checks mla_tc_supported() first; splits > 1 needs mla_workspace_bytes()
+bool mla_tc_supported(int dtype, int Hq, int Hkv, int dk, int dv, const void* k, const void* v,
+                      int64_t kv_row_stride, int64_t kv_rows, const void* q, const void* out);
+int mla_splits(int64_t n_rows, int64_t cap);
+size_t mla_workspace_bytes(int64_t n_rows, int64_t cap);
+cudaError_t launch_attn_mla_tc(const void* q, const void* lat, int64_t kv_row_stride, int64_t kv_rows,
+                               const Geom& g, const int32_t* idx, int64_t idx_row_stride, const int32_t* n_sel,
+                               float scale, void* out, int out_dtype, void* ws, size_t ws_bytes,
+                               cudaStream_t st);
+
+// TMA tensor maps over 16-bit caches (128-byte swizzle); false if encoding fails
+bool make_key_tmap(CUtensorMap* m, const void* k, bool bf16, int64_t k_row_stride, int64_t k_rows, int box_rows);
+bool make_latent_tmap(CUtensorMap* m, const void* lat, int64_t row_stride, int64_t rows);
 
 // number of SMs of the current device (cached per device)
 int sm_count();

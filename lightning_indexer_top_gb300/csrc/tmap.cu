@@ -1,0 +1,53 @@
+// TMA tensor maps (cuTensorMapEncodeTiled, reached through the runtime's
+// driver entry point so the library does not link libcuda directly).
+#include <mutex>
+
+#include "lidx_internal.cuh"
+
+namespace lidx {
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+    static std::once_flag once;
+    static EncodeFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeFn>(p);
+    });
+    return fn;
+}
+
+bool encode_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+               uint32_t box_cols, uint32_t box_rows) {
+    EncodeFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// [rows, 128] 16-bit key cache: boxes of 64 columns x box_rows rows, 128-byte swizzle
+bool make_key_tmap(CUtensorMap* m, const void* k, bool bf16, int64_t k_row_stride, int64_t k_rows, int box_rows) {
+    return encode_2d(m, k, bf16, 128, (uint64_t)k_rows, (uint64_t)k_row_stride * 2, 64, (uint32_t)box_rows);
+}
+
+// [rows, 576] bf16 latent cache for row gathers: boxes of 64 columns x 1 row, 128-byte swizzle
+bool make_latent_tmap(CUtensorMap* m, const void* lat, int64_t row_stride, int64_t rows) {
+    return encode_2d(m, lat, true, 576, (uint64_t)rows, (uint64_t)row_stride * 2, 64, 1);
+}
+
+}  // namespace lidx

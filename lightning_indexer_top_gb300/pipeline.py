@@ -86,7 +86,7 @@ class SparseAttentionStep:
 
     def launches_per_step(self) -> int:
         """Kernels one run() enqueues (library launches only)."""
-        n = 3                                   # score, select, attend
+        n = 3 + (1 if self.attn_ws is not None else 0)   # score, select, attend (+ split combine)
         if self.q_rot is not None:
             n += 2                              # two Hadamard rotations
         if self.wl.block_size > 1:

@@ -284,3 +284,99 @@ def test_score_tensor_core_one_short_row_many_idle_ctas():
     s = L.idx_score(q, w, k, batch)
     ref = O.indexer_scores(np64(q[0]), np64(w[0]), np64(k))
     assert_scores_close(s[0].cpu().numpy(), ref)
+
+
+# ------------------------------------------------------------------ MLA attention on the tensor cores
+
+def _mla_case(seed, B, n_kv, sizes, q_scale=1.0, sorted_sel=False):
+    g = torch.Generator().manual_seed(seed)
+    q = (torch.randn(B, 128, 576, generator=g) * q_scale).to(torch.bfloat16)
+    lat = torch.randn(B * n_kv, 576, generator=g).to(torch.bfloat16)
+    idx = _random_sel(g, n_kv, [max(s, 1) for s in sizes], B)
+    if sorted_sel:
+        idx = torch.sort(torch.where(idx < 0, torch.iinfo(torch.int32).max, idx), dim=1).values
+        idx[idx == torch.iinfo(torch.int32).max] = -1
+    return q, lat, idx
+
+
+def _mla_check(q, lat, idx, sizes, n_kv, out, scale, tol=2e-2):
+    got, lh = np64(out), np64(lat)
+    for r, ns in enumerate(sizes):
+        if ns == 0:
+            assert np.all(got[r] == 0)
+            continue
+        ref = O.sparse_attention_mla(np64(q[r]), lh[r * n_kv:(r + 1) * n_kv], idx[r, :ns].numpy(), scale, 512)
+        err = np.max(np.abs(got[r] - ref))
+        assert err <= tol, (r, ns, err)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_attention_mla_tc_one_split_many_rows(out_dtype):
+    # >= 76 rows: one cluster per row, no key split
+    B, n_kv = 80, 700
+    sizes = [(37 * r) % 700 for r in range(B)]
+    sizes[3], sizes[4] = 1, 64
+    q, lat, idx = _mla_case(81, B, n_kv, sizes)
+    batch = L.Batch(_i32([n_kv] * B), 1, n_kv, kv_seq_stride=n_kv)
+    scale = 1 / math.sqrt(192)
+    assert L.idx_workspace_size(L.IDX_OP_ATTN_DECODE, B, n_kv, idx.shape[1], 128, 512) == 0
+    out = L.sparse_attn_decode(q.to(DEV), lat.to(DEV), None, batch, idx.to(DEV), _i32(sizes), scale,
+                               out_dtype=out_dtype, dv=512)
+    torch.cuda.synchronize()
+    _mla_check(q, lat, idx, sizes, n_kv, out, scale)
+
+
+def test_attention_mla_tc_split_keys_and_combine():
+    # few rows: each row's keys are split over several clusters and merged
+    B, n_kv = 3, 5000
+    sizes = [2048, 2047, 129]
+    q, lat, idx = _mla_case(82, B, n_kv, sizes)
+    batch = L.Batch(_i32([n_kv] * B), 1, n_kv, kv_seq_stride=n_kv)
+    assert L.idx_workspace_size(L.IDX_OP_ATTN_DECODE, B, n_kv, idx.shape[1], 128, 512) > 0
+    scale = 1 / math.sqrt(192)
+    out = L.sparse_attn_decode(q.to(DEV), lat.to(DEV), None, batch, idx.to(DEV), _i32(sizes), scale, dv=512,
+                               out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    _mla_check(q, lat, idx, sizes, n_kv, out, scale)
+
+
+def test_attention_mla_tc_growing_maxima_rescale():
+    # large logits with keys visited in ascending-logit order: the running maximum
+    # jumps by far more than 2^8 between tiles, exercising the O rescale path
+    B, n_kv = 2, 4096
+    g = torch.Generator().manual_seed(83)
+    q = (torch.randn(B, 128, 576, generator=g) * 4).to(torch.bfloat16)
+    lat = torch.randn(B * n_kv, 576, generator=g)
+    # later positions -> larger logits, through the 64 rope columns only, so the value
+    # part (first 512 columns) stays N(0, 1)
+    lat[:, 512:] *= torch.linspace(0.1, 12.0, n_kv).repeat(B)[:, None]
+    lat = lat.to(torch.bfloat16)
+    sizes = [2048, 1500]
+    idx = torch.full((B, 2048), -1, dtype=torch.int32)
+    for r in range(B):
+        idx[r, :sizes[r]] = torch.arange(0, 2 * sizes[r], 2, dtype=torch.int32)
+    batch = L.Batch(_i32([n_kv] * B), 1, n_kv, kv_seq_stride=n_kv)
+    scale = 1 / math.sqrt(192)
+    out = L.sparse_attn_decode(q.to(DEV), lat.to(DEV), None, batch, idx.to(DEV), _i32(sizes), scale, dv=512,
+                               out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    _mla_check(q, lat, idx, sizes, n_kv, out, scale)
+
+
+def test_attention_mla_tc_empty_rows_and_invalid_index():
+    B, n_kv = 80, 300
+    sizes = [0 if r % 5 == 0 else 70 for r in range(B)]
+    q, lat, idx = _mla_case(84, B, n_kv, sizes)
+    idx[1, 5] = 5000                                           # outside the sequence
+    batch = L.Batch(_i32([n_kv] * B), 1, n_kv, kv_seq_stride=n_kv)
+    scale = 1 / math.sqrt(192)
+    assert L.idx_device_status(reset=True) == 0
+    out = L.sparse_attn_decode(q.to(DEV), lat.to(DEV), None, batch, idx.to(DEV), _i32(sizes), scale, dv=512,
+                               out_dtype=torch.float32)
+    assert L.idx_device_status(reset=True) == L.IDX_ERR_DEVICE_BOUNDS
+    keep = [j for j in range(70) if j != 5]
+    ref = O.sparse_attention_mla(np64(q[1]), np64(lat[n_kv:2 * n_kv]), idx[1, keep].numpy(), scale, 512)
+    assert np.max(np.abs(np64(out[1]) - ref)) <= 2e-2
+    rest = [r for r in range(B) if r != 1]
+    _mla_check(q[rest], lat.view(B, n_kv, 576)[rest].reshape(-1, 576), idx[rest], [sizes[r] for r in rest], n_kv,
+               out[rest], scale)
