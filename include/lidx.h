@@ -205,6 +205,32 @@ idx_status sparse_attn_prefill(const void* q, idx_dtype dtype, int32_t n_q_heads
                                const int32_t* n_sel, float scale, void* out, idx_dtype out_dtype,
                                void* workspace, size_t workspace_bytes, idx_stream_t stream);
 
+/*
+ * sparse_attn_decode_noalloc -- sparse_attn_decode's 128-head MLA latent
+ * attention for callers that cannot allocate device memory: programs that
+ * own all device memory through their own pool or arena (serving engines,
+ * frameworks embedding this library), for which a cudaMalloc would fall
+ * outside their accounting and could block or synchronise the device.
+ * The source pages have no counterpart to this entry point.
+ *   Same arguments and result as sparse_attn_decode with v == NULL, minus
+ *   the workspace: the key-split partials go to a static device array of
+ *   20,000,768 bytes that belongs to the library (held by every GPU that
+ *   loads it until the process exits).
+ *   Supported: dtype BF16, n_q_heads 128, n_kv_heads 1, dk 576, dv 512,
+ *   16-byte aligned q/k/out, kv_row_stride % 8 == 0 (else UNSUPPORTED).
+ *   A call whose partials would not fit the array returns INVALID_ARG
+ *   without launching anything.  The array is shared by all calls and keeps
+ *   the last call's contents (nothing in it must start at zero); calls whose
+ *   work overlaps on the GPU race on it and must be serialised by the caller.
+ *   The first call on each device, with that device current, looks up the
+ *   array's device address; make that call before any stream capture.
+ */
+idx_status sparse_attn_decode_noalloc(const void* q, idx_dtype dtype, int32_t n_q_heads, int32_t n_kv_heads,
+                                      int32_t dk, int32_t dv, const void* k, int64_t kv_row_stride,
+                                      int64_t kv_rows, idx_batch batch, const int32_t* idx,
+                                      int64_t idx_row_stride, const int32_t* n_sel, float scale, void* out,
+                                      idx_dtype out_dtype, idx_stream_t stream);
+
 /* Operation selectors for idx_workspace_size. */
 enum { IDX_OP_SCORE = 0, IDX_OP_TOPK = 1, IDX_OP_ATTN_DECODE = 2, IDX_OP_ATTN_PREFILL = 3 };
 

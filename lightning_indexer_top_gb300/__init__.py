@@ -24,7 +24,7 @@ from ._build import build  # noqa: F401
 __all__ = [
     "Batch", "LidxError", "build", "load", "idx_hadamard", "idx_score", "idx_block_pool",
     "idx_topk", "sparse_attn_decode", "sparse_attn_prefill", "idx_workspace_size",
-    "idx_device_status", "topk_capacity",
+    "idx_device_status", "topk_capacity", "sparse_attn_decode_noalloc",
 ]
 
 IDX_OK, IDX_ERR_INVALID_ARG, IDX_ERR_UNSUPPORTED, IDX_ERR_CUDA, IDX_ERR_TIMEOUT, IDX_ERR_DEVICE_BOUNDS = range(6)
@@ -74,6 +74,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                P, I32, P, SZ, P],
         "sparse_attn_prefill": [P, I32, I32, I32, I32, I32, P, P, I64, I64, I64, _Batch, P, I64, P, F,
                                 P, I32, P, SZ, P],
+        "sparse_attn_decode_noalloc": [P, I32, I32, I32, I32, I32, P, I64, I64, _Batch, P, I64, P, F, P, I32, P],
         "idx_workspace_size": [I32, I64, I32, I32, I32, I32],
         "idx_last_error": [],
         "idx_device_status": [I32],
@@ -263,6 +264,21 @@ def sparse_attn_prefill(q, k, v, batch, idx, n_sel, scale, *, out=None, out_dtyp
     """Same function as sparse_attn_decode, tuned for many query rows."""
     return _attn("sparse_attn_prefill", q, k, v, batch, idx, n_sel, scale, out, out_dtype, workspace,
                  n_kv_heads, dv)
+
+
+def sparse_attn_decode_noalloc(q, latent, batch, idx, n_sel, scale, *, out=None, out_dtype=torch.bfloat16):
+    """The 128-head MLA decode attention without a workspace, for callers that cannot
+    allocate device memory: its key-split scratch is a static array inside the library
+    (see include/lidx.h).  Calls that overlap on the GPU must be serialised."""
+    _need_cuda(q, latent, idx, n_sel, out)
+    rows, Hq, dk = q.shape
+    assert rows == batch.n_rows and q.is_contiguous()
+    if out is None:
+        out = torch.empty(rows, Hq, 512, device=q.device, dtype=out_dtype)
+    _check(load().sparse_attn_decode_noalloc(_ptr(q), _dtype(q), Hq, 1, dk, 512, _ptr(latent), latent.stride(0),
+                                             latent.shape[0], batch.c(), _ptr(idx), idx.stride(0), _ptr(n_sel),
+                                             float(scale), _ptr(out), _dtype(out), _stream(q.device)))
+    return out
 
 
 def idx_device_status(reset: bool = True) -> int:

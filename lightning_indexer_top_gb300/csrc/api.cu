@@ -131,6 +131,12 @@ idx_status attn_common(const char* what, const void* q, idx_dtype dtype, int32_t
 
 }  // namespace
 
+// for entry points defined in other files: record the calling thread's message
+idx_status record_error(idx_status s, const char* msg) { return fail(s, "%s", msg); }
+
+// for entry points defined in other files: the kernels' view of a validated batch
+Geom geom_of(const idx_batch& b) { return make_geom(b); }
+
 int sm_count() {
     const int dev = current_device();
     if (dev < 0) return 1;

@@ -139,4 +139,10 @@ bool make_latent_tmap(CUtensorMap* m, const void* lat, int64_t row_stride, int64
 // number of SMs of the current device (cached per device)
 int sm_count();
 
+// set idx_last_error() for the calling thread and return s
+idx_status record_error(idx_status s, const char* msg);
+
+// kernel geometry of a batch (with the device status word of the current device)
+Geom geom_of(const idx_batch& b);
+
 }  // namespace lidx
