@@ -39,6 +39,16 @@ METRIC = "sparse-attn decode queries/s at n_kv=128K,top_k=2048; key-cache GB/s v
 UNIT = "queries/s"
 WORKLOAD = "decode_mla_64x131072"
 
+# name -> (workloads.make arguments); the first is the headline the bench line reports.
+# The others serve profiling captures on smaller cases and the per-config timings.
+WORKLOADS = {
+    "decode_mla_64x131072": (("headline",), {}),
+    "decode_mla_8x131072": (("headline",), {"batch_override": 8}),
+    "decode_mla_8x8192": ((2,), {}),
+    "decode_mla_64x8192": (("headline",), {"n_kv_override": 8192}),
+    "long_decode_mla_ragged": ((5,), {}),
+}
+
 # DRAM bytes per launch of the scorer from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by the SHA-256 of the kernel source it was taken on.
 # A source change makes the figure stale and the bench reports traffic = null.
@@ -185,6 +195,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=4, help="decode queries the CPU baseline runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOADS))
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -205,7 +216,8 @@ def main():
         dist.barrier()
     L.load()
 
-    wl = workloads.make("headline", device=f"cuda:{local}")
+    wa, wk = WORKLOADS[args.workload]
+    wl = workloads.make(*wa, device=f"cuda:{local}", **wk)
     step = SparseAttentionStep(wl, out_dtype=torch.bfloat16)
     stream = torch.cuda.current_stream()
 
@@ -306,9 +318,10 @@ def main():
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16/bf16 (f32 accumulate)",
         "data": "synthetic (seeded N(0,1) q/k/latent, w ~ N(0,1/64))",
-        "config": {"workload": WORKLOAD, "queries_per_gpu": B, "n_kv": 131072, "top_k": 2048,
+        "config": {"workload": args.workload, "queries_per_gpu": B, "n_kv": max(wl.n_kv_host), "top_k": wl.top_k,
                    "indexer": "64 heads x 128, F16 cache", "attention": "MLA 128 heads, 576/512 bf16",
-                   "l2": "inputs larger than L2 (2.1 GB key cache, 9.7 GB latent), no flush"},
+                   "l2": "inputs larger than L2 (key cache %.2f GB, latent %.2f GB), no flush"
+                         % (wl.k_idx.numel() * 2 / 1e9, wl.k_attn.numel() * 2 / 1e9)},
         "key_cache_gbs": key_bytes / ((ms_score + ms_select) * 1e-3) / 1e9,
         "ms_per_kernel": {"score": ms_score, "topk": ms_select, "attention": ms_attend},
         "roofline": {"bound": "hbm", "kernel": "idx_score (key-cache scan)", "achieved": achieved, "peak": hbm,
@@ -327,7 +340,7 @@ def main():
             ns = int(step.n_sel[r])
             same.append(sorted(step.idx[r, :ns].tolist()) == sels[r][1].tolist())
         line["cpu_baseline"] = {"value": len(rows) / dt, "unit": UNIT, "cores": _threads(), "kind": "oracle",
-                                "sample": f"{len(rows)} of the {B} decode queries (n_kv=131072 each), "
+                                "sample": f"{len(rows)} of the {B} decode queries (n_kv={max(wl.n_kv_host)} max), "
                                           "float64 score, top-k and MLA attention"}
         line["parity_sample"] = {"rows": len(rows), "identical_sets": int(sum(same))}
     print(json.dumps(line), flush=True)

@@ -12,18 +12,21 @@
 //           (tile::gather4, 128-byte swizzle) into a 2-stage ring;
 //           S = Q K^T (M=128 heads, N=64 keys, K=576) goes to one of two TMEM
 //           buffers; four softmax warps (thread = head) turn S into
-//           P = exp2(S*scale*log2e - m) as bf16 and bulk-copy P, the
-//           per-head rescale factor, row sum and max to rank 1 over DSMEM.
+//           P = 2^(S*scale*log2e - m) as bf16 and store P, the per-head
+//           rescale factor, row sum and max straight into rank 1's shared
+//           memory (DSMEM), then release-arrive on rank 1's barrier.
 //   rank 1: O lives in TMEM (512 columns); value tiles (the same rows, first
 //           512 columns) are gathered into its own ring; O += P V with P as a
 //           K-major and V as an MN-major shared-memory operand (M=128,
-//           N=256 x 2, K=16 x 4).  Four correction warps rescale O when
-//           rank 0 raised a row maximum by more than 2^8 (rare after the
-//           first tiles, so P stays <= 2^8 otherwise) and finally write
-//           O / l, or the unnormalised partial (O, m, l) of a key split.
-// Key splits (few query rows) are merged by a small combine kernel.
-// Padding and invalid indices gather a valid row and get p = 0.  Every wait
-// is bounded; a timeout records IDX_ERR_TIMEOUT and the cluster winds down.
+//           N=256 x 2, K=16 x 4).  Four correction warps rescale their heads'
+//           O rows when rank 0 raised a row maximum by more than 2^8 (rare
+//           after the first tiles, so P stays <= 2^8 otherwise) and finally
+//           write O / l, or the unnormalised partial (O, m, l) of a key split.
+// Each CTA first turns its slice of the index list into cache rows and a
+// validity bitmask in shared memory; padding and invalid indices gather a
+// valid row and get p = 0.  Key splits (few query rows) are merged by a small
+// combine kernel.  Every wait is bounded; a timeout records IDX_ERR_TIMEOUT
+// and the cluster winds down.
 #include "lidx_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -39,12 +42,13 @@ constexpr int kDkBlocks = kDk / 64;                     // 9 column blocks of 12
 constexpr int kDvBlocks = kDv / 64;                     // 8
 constexpr int kBlockBytes = kKeys * 128;                // one column block of a tile
 constexpr int kKTileBytes = kDkBlocks * kBlockBytes;    // 73728
-constexpr int kVTileBytes = kDvBlocks * kBlockBytes;    // 65536
 constexpr int kStages = 2;
 constexpr int kPBytes = kHq * kKeys * 2;                // P tile, bf16, 128-byte swizzle K-major
-constexpr int kPktBytes = kPBytes + 3 * kHq * 4 + 16;   // P + alpha + l + m + flag
-constexpr int kPktStride = 18432;
-constexpr int kThreads = 192;
+constexpr int kPktBytes = kPBytes + 3 * kHq * 4;        // P tile + alpha, l, m per head
+constexpr int kPktStride = 18432;                       // P tile + tail, 1024-aligned
+constexpr int kMaxKps = 4096;                           // selected keys per split, at most
+constexpr int kThreads = 288;                           // 9 warps
+constexpr int kProducerWarps = 4;                       // warps 0, 6, 7, 8
 constexpr int kTmemCols = 512;
 constexpr int kSCol0 = 320;                             // rank 0: S buffers at 320 and 384 (Q at 0..287)
 constexpr float kRescaleLog2 = 8.f;
@@ -53,27 +57,28 @@ struct PktTail {
     float alpha[kHq];
     float l[kHq];
     float m[kHq];
-    int flag;
-    int pad[3];
 };
-static_assert(kPBytes + sizeof(PktTail) == kPktBytes, "packet layout");
+static_assert(kPBytes + sizeof(PktTail) <= kPktStride, "packet layout");
 
 struct Ctl {
-    uint64_t xfull[kStages];
-    uint64_t xempty[kStages];
-    uint64_t sfull[2];
-    uint64_t sempty[2];
-    uint64_t pfree[2];
-    uint64_t pfull[2];
-    uint64_t cdone[2];
-    uint64_t pvdone[2];
+    uint64_t xfull[kStages];   // gathered tile landed (32 producer lanes arrive)
+    uint64_t xempty[kStages];  // tile consumed by the MMAs
+    uint64_t sfull[2];         // rank 0: S accumulator written
+    uint64_t sempty[2];        // rank 0: S read by the softmax warps
+    uint64_t qready;           // rank 0: Q stored in TMEM
+    uint64_t staged[2];        // rank 0: P packet j written to the staging slot
+    uint64_t stfree[2];        // rank 0: staging slot j read by its bulk copy
+    uint64_t pfree[2];         // rank 0: rank 1's packet slot j consumed by its MMAs
+    uint64_t pfull[2];         // rank 1: packet j arrived
+    uint64_t cdone[2];         // rank 1: O corrected for packet j
+    uint64_t pvdone[2];        // rank 1: PV MMAs that read packet j completed
     uint64_t done;
     uint32_t tmem_base;
     int abort;
-    uint32_t warp_flags[4];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kKTileBytes + 2 * kPktStride + sizeof(Ctl);
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kKTileBytes + 2 * kPktStride + kMaxKps * 4 +
+                              kMaxKps / 8 + sizeof(Ctl);
 
 __device__ __forceinline__ void abort_cta(Ctl& c, int* status) {
     *(volatile int*)&c.abort = 1;
@@ -115,78 +120,63 @@ __device__ __forceinline__ Unit make_unit(const Geom& g, const int32_t* n_sel, i
     return u;
 }
 
-// cache row of selected key j (padding and invalid indices -> the fallback row)
-__device__ __forceinline__ int32_t key_row(const Unit& u, const int32_t* idx, int64_t idx_row_stride,
-                                           int64_t kv_rows, int j, bool& valid) {
-    valid = false;
-    if (j >= u.k1) return (int32_t)u.fallback;
-    const int pos = idx[u.r * idx_row_stride + j];
-    const int64_t row = u.row0 + pos;
-    if (pos >= 0 && pos < u.n_kv && row >= 0 && row < kv_rows) {
-        valid = true;
-        return (int32_t)row;
-    }
-    return (int32_t)u.fallback;
-}
-
-// producer: gather the tile's 64 rows, `nblocks` column blocks of 64 elements each
-__device__ __forceinline__ void gather_tiles(Ctl& c, uint8_t* xtiles, const CUtensorMap* map, const Unit& u,
-                                             const int32_t* idx, int64_t idx_row_stride, int64_t kv_rows,
-                                             int nblocks, int* status, bool report) {
+// Producer warps (kProducerWarps of them, index p): gather each tile's 64 rows
+// (the first kChunks*16 bytes of each row) with 16-byte cp.async copies into
+// the 128-byte swizzled layout the MMA descriptors read: column block
+// db = chunk/8 at db*8192, row at row*128, the 16-byte chunk at
+// ((chunk%8) ^ (row%8))*16.  A warp instruction copies 512 contiguous bytes.
+// Tile t is announced (xfull, one arrival per producer lane) once the copies of
+// tile t+1 are in flight, so two tiles' loads overlap.
+template <int kChunks>
+__device__ __forceinline__ void gather_tiles(Ctl& c, uint8_t* xtiles, const __nv_bfloat16* lat,
+                                             int64_t lat_row_stride, const Unit& u, const int32_t* rows_s,
+                                             int p, int* status) {
     const int lane = threadIdx.x & 31;
-    const uint32_t tile_bytes = (uint32_t)nblocks * kBlockBytes;
+    const char* base = reinterpret_cast<const char*>(lat);
+    const int64_t row_bytes = lat_row_stride * 2;
+    int issued = 0;
     for (int t = 0; t < u.n_tiles; ++t) {
         const int stage = t & 1;
         const uint32_t ph = (uint32_t)((t >> 1) & 1);
-        const int j0 = u.k0 + t * kKeys;
-        bool va, vb;
-        const int32_t ra = key_row(u, idx, idx_row_stride, kv_rows, j0 + lane, va);
-        const int32_t rb = key_row(u, idx, idx_row_stride, kv_rows, j0 + 32 + lane, vb);
-        if (report && ((j0 + lane < u.k1 && !va) || (j0 + 32 + lane < u.k1 && !vb)))
-            flag(status, IDX_ERR_DEVICE_BOUNDS);
-        if (lane == 0) {
-            if (!mbar_wait(&c.xempty[stage], ph ^ 1)) {
-                abort_cta(c, status);
-            } else {
-                mbar_arrive_expect_tx(&c.xfull[stage], tile_bytes);
-            }
+        if (warp_aborted(c) || !warp_wait(&c.xempty[stage], ph ^ 1)) {
+            abort_cta(c, status);
+            break;
         }
-        if (warp_aborted(c)) break;
-        // lane g < 16 issues the gathers of keys 4g .. 4g+3
-        int32_t rows[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int key = 4 * (lane & 15) + i;
-            const int32_t xa = __shfl_sync(0xffffffffu, ra, key & 31);
-            const int32_t xb = __shfl_sync(0xffffffffu, rb, key & 31);
-            rows[i] = key < 32 ? xa : xb;
+        const uint32_t dst0 = smem_u32(xtiles + (size_t)stage * kKTileBytes);
+        const int32_t* rr = rows_s + t * kKeys;
+#pragma unroll 4
+        for (int i = p * 32 + lane; i < kKeys * kChunks; i += 32 * kProducerWarps) {
+            const int row = i / kChunks, cc = i - row * kChunks;
+            const char* src = base + (int64_t)rr[row] * row_bytes + cc * 16;
+            const uint32_t dst = dst0 + (cc >> 3) * kBlockBytes + row * 128 + (((cc & 7) ^ (row & 7)) << 4);
+            cp_async16(dst, src);
         }
-        if (lane < 16) {
-            uint8_t* dst = xtiles + (size_t)stage * kKTileBytes + lane * 4 * 128;
-            for (int db = 0; db < nblocks; ++db)
-                tma_gather4(dst + db * kBlockBytes, map, &c.xfull[stage], db * 64, rows[0], rows[1], rows[2],
-                            rows[3]);
+        cp_async_commit();
+        ++issued;
+        if (t > 0) {
+            cp_async_wait<1>();
+            fence_proxy_async_smem();
+            mbar_arrive(&c.xfull[(t - 1) & 1]);
         }
-        __syncwarp();
     }
-    // no TMA writes may be in flight when the CTA leaves
-    if (lane == 0) {
-        const int n = min(u.n_tiles, kStages);
-        for (int t = u.n_tiles - n; t < u.n_tiles; ++t) mbar_wait(&c.xfull[t & 1], (uint32_t)((t >> 1) & 1));
-    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    if (issued > 0) mbar_arrive(&c.xfull[(issued - 1) & 1]);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_attn_tc_kernel(const __grid_constant__ CUtensorMap lat_map, const __nv_bfloat16* __restrict__ q, Geom g,
-                       const int32_t* __restrict__ idx, int64_t idx_row_stride,
-                       const int32_t* __restrict__ n_sel, int64_t kv_rows, float scale_log2, int splits,
-                       int kps, void* __restrict__ out, int out_dtype, float* __restrict__ part_o,
-                       float* __restrict__ part_ml) {
+    mla_attn_tc_kernel(const __nv_bfloat16* __restrict__ lat, int64_t lat_row_stride,
+                       const __nv_bfloat16* __restrict__ q, Geom g, const int32_t* __restrict__ idx,
+                       int64_t idx_row_stride, const int32_t* __restrict__ n_sel, int64_t kv_rows,
+                       float scale_log2, int splits, int kps, void* __restrict__ out, int out_dtype,
+                       float* __restrict__ part_o, float* __restrict__ part_ml) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* xtiles = smem;                                         // K tiles (rank 0) / V tiles (rank 1)
     uint8_t* pkts = smem + (size_t)kStages * kKTileBytes;           // P staging (rank 0) / P received (rank 1)
-    Ctl& c = *reinterpret_cast<Ctl*>(pkts + 2 * kPktStride);
+    int32_t* rows_s = reinterpret_cast<int32_t*>(pkts + 2 * kPktStride);   // cache row of each selected key
+    uint32_t* vmask = reinterpret_cast<uint32_t*>(rows_s + kMaxKps);       // bit = key index is valid
+    Ctl& c = *reinterpret_cast<Ctl*>(vmask + kMaxKps / 32);
 
     const uint32_t rank = cluster_ctarank();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -194,60 +184,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&c.xfull[i], 1);
+            mbar_init(&c.xfull[i], 32 * kProducerWarps);
             mbar_init(&c.xempty[i], 1);
             mbar_init(&c.sfull[i], 1);
             mbar_init(&c.sempty[i], 4);
+            mbar_init(&c.staged[i], 4);
+            mbar_init(&c.stfree[i], 1);
             mbar_init(&c.pfree[i], 1);
             mbar_init(&c.pfull[i], 1);
             mbar_init(&c.cdone[i], 4);
             mbar_init(&c.pvdone[i], 1);
         }
+        mbar_init(&c.qready, 4);
         mbar_init(&c.done, 1);
         c.abort = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) tma_prefetch_desc(&lat_map);
+    // the split's selected keys -> cache rows + validity bits, 32 keys per warp step
+    for (int wd = warp; wd < u.n_tiles * (kKeys / 32); wd += kThreads / 32) {
+        const int j = u.k0 + wd * 32 + lane;
+        bool valid = false;
+        int64_t row = u.fallback;
+        if (j < u.k1) {
+            const int pos = idx[u.r * idx_row_stride + j];
+            const int64_t rr = u.row0 + pos;
+            if (pos >= 0 && pos < u.n_kv && rr >= 0 && rr < kv_rows) {
+                valid = true;
+                row = rr;
+            } else if (rank == 0) {
+                flag(g.status, IDX_ERR_DEVICE_BOUNDS);
+            }
+        }
+        rows_s[wd * 32 + lane] = (int32_t)row;
+        const uint32_t bits = __ballot_sync(0xffffffffu, valid);
+        if (lane == 0) vmask[wd] = bits;
+    }
     if (warp == 1) {
         tmem_alloc(&c.tmem_base, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // barriers of both CTAs initialised, indices staged, TMEM allocated
     tc_fence_after();
     const uint32_t tmem = c.tmem_base;
     const int quad = warp & 3;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
 
-    // rank 0: load this row's Q into TMEM columns [0, 288), thread = head
-    if (rank == 0 && warp >= 2 && u.n_tiles > 0) {
-        const int h = quad * 32 + lane;
-        const uint4* src = reinterpret_cast<const uint4*>(q + (u.r * kHq + h) * (int64_t)kDk);
-        for (int cb = 0; cb < kDkBlocks; ++cb) {
-            uint32_t regs[32];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint4 x = src[cb * 8 + i];
-                regs[4 * i] = x.x;
-                regs[4 * i + 1] = x.y;
-                regs[4 * i + 2] = x.z;
-                regs[4 * i + 3] = x.w;
-            }
-            tmem_st_32x32b_x32(tmem + lane_off + cb * 32, regs);
-        }
-        tmem_st_wait();
-    }
-    tc_fence_before();
-    cluster_sync();  // barriers of both CTAs initialised, Q in TMEM
-    tc_fence_after();
-
+    const int producer = warp == 0 ? 0 : (warp >= 6 ? warp - 5 : -1);   // producer index or -1
     if (rank == 0) {
-        if (warp == 0) {
-            gather_tiles(c, xtiles, &lat_map, u, idx, idx_row_stride, kv_rows, kDkBlocks, g.status, true);
+        if (producer >= 0) {
+            gather_tiles<kDkBlocks * 8>(c, xtiles, lat, lat_row_stride, u, rows_s, producer, g.status);
         } else if (warp == 1) {
             if (lane == 0) {
+                // ---------------------------------------------------- S = Q K^T issuer
                 const uint32_t idesc = idesc_f16_f32_major(kHq, kKeys, 1, 0, 0);
-                for (int t = 0; t < u.n_tiles; ++t) {
+                bool ok = u.n_tiles == 0 || mbar_wait(&c.qready, 0);
+                if (!ok) abort_cta(c, g.status);
+                tc_fence_after();
+                for (int t = 0; ok && t < u.n_tiles; ++t) {
                     const int stage = t & 1, sb = t & 1;
                     const uint32_t ph = (uint32_t)((t >> 1) & 1);
                     if (aborted(c)) break;
@@ -268,43 +262,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&c.done);
                 mbar_wait(&c.done, 0);
+            } else if (lane == 1) {
+                // ---------------------------------------------------- P packet sender
+                for (int t = 0; t < u.n_tiles; ++t) {
+                    const int j = t & 1;
+                    const uint32_t ph = (uint32_t)((t >> 1) & 1);
+                    if (aborted(c)) break;
+                    if (!mbar_wait(&c.staged[j], ph) || !mbar_wait(&c.pfree[j], ph ^ 1)) {
+                        abort_cta(c, g.status);
+                        break;
+                    }
+                    uint8_t* slot = pkts + j * kPktStride;
+                    const uint32_t rbar = mapa(&c.pfull[j], 1);
+                    mbar_arrive_expect_tx_remote(rbar, kPktBytes);
+                    bulk_copy_s2cluster(mapa(slot, 1), slot, kPktBytes, rbar);
+                    bulk_commit();
+                    // the previous packet's copy has read its staging slot: release it
+                    if (t > 0) {
+                        bulk_wait_read<1>();
+                        mbar_arrive(&c.stfree[(t - 1) & 1]);
+                    }
+                }
+                bulk_wait_read<0>();
+                if (u.n_tiles > 0 && !aborted(c)) mbar_arrive(&c.stfree[(u.n_tiles - 1) & 1]);
+                // rank 1's last arrivals on pfree land before this CTA may leave
+                const int n = min(u.n_tiles, 2);
+                for (int t = u.n_tiles - n; t < u.n_tiles; ++t)
+                    if (!aborted(c)) mbar_wait(&c.pfree[t & 1], (uint32_t)((t >> 1) & 1));
             }
             __syncwarp();
         } else {
-            // ---------------------------------------------------------- softmax (thread = head)
+            // ---------------------------------------------------------- Q to TMEM, then softmax (thread = head)
             const int h = quad * 32 + lane;
-            const bool leader = (warp == 2 && lane == 0);
+            if (u.n_tiles > 0) {
+                const uint4* src = reinterpret_cast<const uint4*>(q + (u.r * kHq + h) * (int64_t)kDk);
+#pragma unroll 1
+                for (int cb0 = 0; cb0 < kDkBlocks; cb0 += 3) {
+                    uint4 x[24];
+#pragma unroll
+                    for (int i = 0; i < 24; ++i) x[i] = src[cb0 * 8 + i];
+#pragma unroll
+                    for (int k3 = 0; k3 < 3; ++k3) {
+                        uint32_t regs[32];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            regs[4 * i] = x[k3 * 8 + i].x;
+                            regs[4 * i + 1] = x[k3 * 8 + i].y;
+                            regs[4 * i + 2] = x[k3 * 8 + i].z;
+                            regs[4 * i + 3] = x[k3 * 8 + i].w;
+                        }
+                        tmem_st_32x32b_x32(tmem + lane_off + (cb0 + k3) * 32, regs);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c.qready);
+            }
             float m_used = 0.f, lsum = 0.f;
             bool has_m = false;
             for (int t = 0; t < u.n_tiles; ++t) {
                 const int sb = t & 1, j = t & 1;
                 const uint32_t ph = (uint32_t)((t >> 1) & 1);
-                const int j0 = u.k0 + t * kKeys;
-                bool va, vb;
-                key_row(u, idx, idx_row_stride, kv_rows, j0 + lane, va);
-                key_row(u, idx, idx_row_stride, kv_rows, j0 + 32 + lane, vb);
-                const uint32_t ma = __ballot_sync(0xffffffffu, va);
-                const uint32_t mb = __ballot_sync(0xffffffffu, vb);
-                // every softmax warp runs both named barriers of every tile, also after an
-                // abort (then with zero scores and no waits), so none can be left behind
-                bool live = !warp_aborted(c);
-                if (live && !warp_wait(&c.sfull[sb], ph)) {
+                const uint32_t ma = vmask[2 * t], mb = vmask[2 * t + 1];
+                if (warp_aborted(c) || !warp_wait(&c.sfull[sb], ph)) {
                     abort_cta(c, g.status);
-                    live = false;
+                    break;
                 }
+                tc_fence_after();
                 float s0[32], s1[32];
-                if (live) {
-                    tc_fence_after();
-                    tmem_ld_32x32b_x32(tmem + lane_off + kSCol0 + sb * kKeys, s0);
-                    tmem_ld_32x32b_x32(tmem + lane_off + kSCol0 + sb * kKeys + 32, s1);
-                    tmem_ld_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&c.sempty[sb]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s0[i] = s1[i] = 0.f;
-                }
+                tmem_ld_32x32b_x32(tmem + lane_off + kSCol0 + sb * kKeys, s0);
+                tmem_ld_32x32b_x32(tmem + lane_off + kSCol0 + sb * kKeys + 32, s1);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c.sempty[sb]);
 
                 float mt = -3.0e38f;
 #pragma unroll
@@ -320,7 +352,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         m_used = mt;
                         has_m = true;
                     } else if (mt > m_used + kRescaleLog2) {
-                        alpha = exp2f(m_used - mt);
+                        alpha = ex2_approx(m_used - mt);
                         lsum *= alpha;
                         m_used = mt;
                     }
@@ -329,10 +361,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 float psum = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ((ma >> (2 * i)) & 1u) ? exp2f(s0[2 * i] - m_used) : 0.f;
-                    const float p1 = ((ma >> (2 * i + 1)) & 1u) ? exp2f(s0[2 * i + 1] - m_used) : 0.f;
-                    const float p2 = ((mb >> (2 * i)) & 1u) ? exp2f(s1[2 * i] - m_used) : 0.f;
-                    const float p3 = ((mb >> (2 * i + 1)) & 1u) ? exp2f(s1[2 * i + 1] - m_used) : 0.f;
+                    const float p0 = ((ma >> (2 * i)) & 1u) ? ex2_approx(s0[2 * i] - m_used) : 0.f;
+                    const float p1 = ((ma >> (2 * i + 1)) & 1u) ? ex2_approx(s0[2 * i + 1] - m_used) : 0.f;
+                    const float p2 = ((mb >> (2 * i)) & 1u) ? ex2_approx(s1[2 * i] - m_used) : 0.f;
+                    const float p3 = ((mb >> (2 * i + 1)) & 1u) ? ex2_approx(s1[2 * i + 1] - m_used) : 0.f;
                     psum += (p0 + p1) + (p2 + p3);
                     const __nv_bfloat162 a = __floats2bfloat162_rn(p0, p1);
                     const __nv_bfloat162 bb = __floats2bfloat162_rn(p2, p3);
@@ -340,53 +372,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     pk[16 + i] = *reinterpret_cast<const uint32_t*>(&bb);
                 }
                 lsum += psum;
-                const uint32_t resc = __ballot_sync(0xffffffffu, alpha != 1.f);
 
-                // staging buffer j is free once the copy of tile t-2 has read it
-                if (leader) bulk_wait_read<1>();
-                named_bar_sync(1, 128);
-                uint8_t* stage_p = pkts + j * kPktStride;
-                uint8_t* rowp = stage_p + (h >> 3) * 1024 + (h & 7) * 128;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    uint4 v;
-                    v.x = pk[4 * ch];
-                    v.y = pk[4 * ch + 1];
-                    v.z = pk[4 * ch + 2];
-                    v.w = pk[4 * ch + 3];
-                    *reinterpret_cast<uint4*>(rowp + ((ch ^ (h & 7)) << 4)) = v;
+                // staging slot j is free once the copy of tile t-2 has read it
+                if (!warp_wait(&c.stfree[j], ph ^ 1)) {
+                    abort_cta(c, g.status);
+                    break;
                 }
-                PktTail& tail = *reinterpret_cast<PktTail*>(stage_p + kPBytes);
+                uint8_t* slot = pkts + j * kPktStride;
+                uint8_t* rowp = slot + (h >> 3) * 1024 + (h & 7) * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4*>(rowp + ((ch ^ (h & 7)) << 4)) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                PktTail& tail = *reinterpret_cast<PktTail*>(slot + kPBytes);
                 tail.alpha[h] = alpha;
                 tail.l[h] = lsum;
                 tail.m[h] = m_used;
-                if (lane == 0) c.warp_flags[quad] = resc;
                 fence_proxy_async_smem();
-                named_bar_sync(1, 128);
-                if (leader && !aborted(c)) {
-                    tail.flag = (c.warp_flags[0] | c.warp_flags[1] | c.warp_flags[2] | c.warp_flags[3]) ? 1 : 0;
-                    fence_proxy_async_smem();
-                    if (!mbar_wait(&c.pfree[j], ph ^ 1)) {
-                        abort_cta(c, g.status);
-                    } else {
-                        const uint32_t rbar = mapa(&c.pfull[j], 1);
-                        mbar_arrive_expect_tx_remote(rbar, kPktBytes);
-                        bulk_copy_s2cluster(mapa(stage_p, 1), stage_p, kPktBytes, rbar);
-                        bulk_commit();
-                    }
-                }
-            }
-            if (leader) {
-                bulk_wait_read<0>();
-                // rank 1's last arrivals on pfree land before this CTA may leave
-                const int n = min(u.n_tiles, 2);
-                for (int t = u.n_tiles - n; t < u.n_tiles; ++t)
-                    if (!aborted(c)) mbar_wait(&c.pfree[t & 1], (uint32_t)((t >> 1) & 1));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c.staged[j]);
             }
         }
     } else {
-        if (warp == 0) {
-            gather_tiles(c, xtiles, &lat_map, u, idx, idx_row_stride, kv_rows, kDvBlocks, g.status, false);
+        if (producer >= 0) {
+            gather_tiles<kDvBlocks * 8>(c, xtiles, lat, lat_row_stride, u, rows_s, producer, g.status);
         } else if (warp == 1) {
             if (lane == 0) {
                 const uint32_t idesc = idesc_f16_f32_major(kHq, 256, 1, 0, 1);
@@ -426,13 +435,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int t = 0; t < u.n_tiles; ++t) {
                 const int j = t & 1;
                 const uint32_t ph = (uint32_t)((t >> 1) & 1);
-                if (warp_aborted(c) || !warp_wait(&c.pfull[j], ph)) {
+                if (warp_aborted(c) || !warp_wait_cluster(&c.pfull[j], ph)) {
                     abort_cta(c, g.status);
                     ok = false;
                     break;
                 }
                 const PktTail& tail = *reinterpret_cast<const PktTail*>(pkts + j * kPktStride + kPBytes);
-                if (tail.flag && t > 0) {
+                const float a = tail.alpha[h];
+                if (t > 0 && __any_sync(0xffffffffu, a != 1.f)) {
                     const int tp = t - 1;
                     if (!warp_wait(&c.pvdone[tp & 1], (uint32_t)((tp >> 1) & 1))) {
                         abort_cta(c, g.status);
@@ -440,7 +450,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const float a = tail.alpha[h];
                     for (int cb = 0; cb < kDv / 32; ++cb) {
                         float v[32];
                         tmem_ld_32x32b_x32(tmem + lane_off + cb * 32, v);
@@ -582,16 +591,21 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restric
 
 }  // namespace
 
-// key splits per query row: enough clusters to cover the SMs when rows are few
+// key splits per query row: enough clusters to cover the SMs when rows are few,
+// and never more than kMaxKps selected keys per split
 int mla_splits(int64_t n_rows, int64_t cap) {
-    if (n_rows <= 0) return 1;
+    const int64_t min_s = cap > kMaxKps ? (cap + kMaxKps - 1) / kMaxKps : 1;
+    if (n_rows <= 0) return (int)min_s;
     int sms = sm_count();
     if (sms < 2) sms = 152;
     const int64_t clusters = sms / 2;
-    if (n_rows >= clusters) return 1;
-    const int64_t by_sm = clusters / n_rows;
-    const int64_t by_keys = (cap + 255) / 256;
-    int64_t s = by_sm < by_keys ? by_sm : by_keys;
+    int64_t s = 1;
+    if (n_rows < clusters) {
+        const int64_t by_sm = clusters / n_rows;
+        const int64_t by_keys = (cap + 255) / 256;
+        s = by_sm < by_keys ? by_sm : by_keys;
+    }
+    if (s < min_s) s = min_s;
     return (int)(s < 1 ? 1 : s);
 }
 
@@ -625,15 +639,13 @@ cudaError_t launch_attn_mla_tc(const void* q, const void* lat, int64_t kv_row_st
         part_o = static_cast<float*>(ws);
         part_ml = part_o + (size_t)n_rows * splits * kHq * kDv;
     }
-    CUtensorMap map;
-    if (!make_latent_tmap(&map, lat, kv_row_stride, kv_rows)) return cudaErrorNotSupported;
     const int64_t grid = 2 * n_rows * splits;
     if (grid > INT32_MAX) return cudaErrorNotSupported;
     cudaFuncSetAttribute(mla_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     const float scale_log2 = scale * 1.4426950408889634f;
     mla_attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(
-        map, static_cast<const __nv_bfloat16*>(q), g, idx, idx_row_stride, n_sel, kv_rows, scale_log2, splits,
-        (int)kps64, out, out_dtype, part_o, part_ml);
+        static_cast<const __nv_bfloat16*>(lat), kv_row_stride, static_cast<const __nv_bfloat16*>(q), g, idx,
+        idx_row_stride, n_sel, kv_rows, scale_log2, splits, (int)kps64, out, out_dtype, part_o, part_ml);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || splits == 1) return e;
     mla_combine_kernel<<<dim3((unsigned)n_rows, kHq), 128, 0, st>>>(part_o, part_ml, splits, out, out_dtype);

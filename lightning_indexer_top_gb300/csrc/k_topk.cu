@@ -28,7 +28,7 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kPer = 4;
+constexpr int kPer = 16;                 // consecutive positions per thread in one compaction chunk
 constexpr int kChunk = kThreads * kPer;
 
 struct Shared {
@@ -74,9 +74,49 @@ __device__ __forceinline__ void radix_round(const float* __restrict__ s, int n, 
     const int nbins = 1 << bits;
     for (int i = threadIdx.x; i < nbins; i += kThreads) sh.hist[i] = 0u;
     __syncthreads();
-    for (int j = threadIdx.x; j < n; j += kThreads) {
-        const uint32_t key = order_key(s[j]);
-        if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & (nbins - 1)], 1u);
+    // Scores crowd into few bins, so equal bins are combined across the warp
+    // first (one shared-memory atomic per distinct bin per warp instruction).
+    const int lane = threadIdx.x & 31;
+    auto count = [&](uint32_t key, bool in) {
+        const bool hit = in && (key & mask) == prefix;
+        const uint32_t bin = hit ? (key >> shift) & (nbins - 1) : 0xffffffffu;
+        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+        if (hit && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[bin], (uint32_t)__popc(peers));
+    };
+    if ((reinterpret_cast<uintptr_t>(s) & 15u) == 0) {
+        const int n4 = n >> 2;
+        const float4* s4 = reinterpret_cast<const float4*>(s);
+        // kBatch independent 16-byte loads in flight per thread before any is used
+        constexpr int kBatch = 8;
+        const int step = kThreads * kBatch;
+        const int lim = (n4 + step - 1) / step * step;   // whole warps stay converged
+        for (int i0 = threadIdx.x; i0 < lim; i0 += step) {
+            float4 v[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int i = i0 + b * kThreads;
+                v[b] = i < n4 ? s4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const bool in = i0 + b * kThreads < n4;
+                count(order_key(v[b].x), in);
+                count(order_key(v[b].y), in);
+                count(order_key(v[b].z), in);
+                count(order_key(v[b].w), in);
+            }
+        }
+        if (threadIdx.x < 32) {   // the last n % 4 elements, by all lanes of warp 0
+            const int j = (n4 << 2) + lane;
+            const bool in = j < n;
+            count(in ? order_key(s[j]) : 0u, in);
+        }
+    } else {
+        const int lim = (n + kThreads - 1) / kThreads * kThreads;
+        for (int j = threadIdx.x; j < lim; j += kThreads) {
+            const bool in = j < n;
+            count(in ? order_key(s[j]) : 0u, in);
+        }
     }
     __syncthreads();
     // thread t owns nbins/kThreads consecutive bins, walked from the top
@@ -133,6 +173,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
             __syncthreads();
         }
         const uint32_t T = prefix;
+        const bool aligned = (reinterpret_cast<uintptr_t>(s) & 15u) == 0;
 
         uint32_t run_gt = 0, run_eq = 0;
 #pragma unroll 1
@@ -140,9 +181,24 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict_
             const int p0 = base + threadIdx.x * kPer;
             uint32_t key[kPer];
             uint32_t gt = 0, eq = 0;
+            if (aligned && p0 + kPer <= n) {
+                const float4* s4 = reinterpret_cast<const float4*>(s + p0);
+                float4 v[kPer / 4];
+#pragma unroll
+                for (int q4 = 0; q4 < kPer / 4; ++q4) v[q4] = s4[q4];
+#pragma unroll
+                for (int q4 = 0; q4 < kPer / 4; ++q4) {
+                    key[4 * q4] = order_key(v[q4].x);
+                    key[4 * q4 + 1] = order_key(v[q4].y);
+                    key[4 * q4 + 2] = order_key(v[q4].z);
+                    key[4 * q4 + 3] = order_key(v[q4].w);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) key[i] = (p0 + i < n) ? order_key(s[p0 + i]) : 0u;
+            }
 #pragma unroll
             for (int i = 0; i < kPer; ++i) {
-                key[i] = (p0 + i < n) ? order_key(s[p0 + i]) : 0u;
                 const bool valid = p0 + i < n;
                 gt += (valid && key[i] > T);
                 eq += (valid && key[i] == T);

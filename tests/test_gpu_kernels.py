@@ -380,3 +380,24 @@ def test_attention_mla_tc_empty_rows_and_invalid_index():
     rest = [r for r in range(B) if r != 1]
     _mla_check(q[rest], lat.view(B, n_kv, 576)[rest].reshape(-1, 576), idx[rest], [sizes[r] for r in rest], n_kv,
                out[rest], scale)
+
+
+def test_attention_mla_tc_selections_longer_than_one_split():
+    # selections above 4096 keys always split, even with many rows; all rows share one cache
+    B, n_kv, cap = 80, 6000, 5000
+    g = torch.Generator().manual_seed(85)
+    q = torch.randn(B, 128, 576, generator=g).to(torch.bfloat16)
+    lat = torch.randn(n_kv, 576, generator=g).to(torch.bfloat16)
+    sizes = [cap if r % 3 == 0 else (r * 61) % cap + 1 for r in range(B)]
+    idx = torch.full((B, cap), -1, dtype=torch.int32)
+    for r in range(B):
+        idx[r, :sizes[r]] = torch.randperm(n_kv, generator=g)[:sizes[r]].to(torch.int32)
+    batch = L.Batch(_i32([n_kv] * B), 1, n_kv, kv_seq_stride=0)
+    assert L.idx_workspace_size(L.IDX_OP_ATTN_DECODE, B, n_kv, cap, 128, 512) > 0
+    scale = 1 / math.sqrt(192)
+    out = L.sparse_attn_decode(q.to(DEV), lat.to(DEV), None, batch, idx.to(DEV), _i32(sizes), scale, dv=512,
+                               out_dtype=torch.float32)
+    got, lh = np64(out), np64(lat)
+    for r in range(0, B, 7):
+        ref = O.sparse_attention_mla(np64(q[r]), lh, idx[r, :sizes[r]].numpy(), scale, 512)
+        assert np.max(np.abs(got[r] - ref)) <= 2e-2, r
