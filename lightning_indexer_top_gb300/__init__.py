@@ -217,6 +217,10 @@ def idx_topk(scores: torch.Tensor, batch: Batch, top_k: int, *, block_size: int 
         idx = torch.empty(rows, cap, device=scores.device, dtype=torch.int32)
     if n_sel is None:
         n_sel = torch.empty(rows, device=scores.device, dtype=torch.int32)
+    if workspace is None and block_size <= 1:
+        need = idx_workspace_size(IDX_OP_TOPK, rows, batch.max_n_kv, top_k)
+        if need:
+            workspace = torch.empty(need, device=scores.device, dtype=torch.uint8)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().idx_topk(_ptr(scores), scores.stride(0), batch.c(), top_k, block_size, _ptr(idx),
                            idx.stride(0), _ptr(n_sel), _ptr(workspace), ws_bytes, _stream(scores.device)))

@@ -240,8 +240,6 @@ idx_status idx_topk(const float* scores, int64_t score_row_stride, idx_batch bat
                     int32_t block_size, int32_t* idx, int64_t idx_row_stride, int32_t* n_sel,
                     void* workspace, size_t workspace_bytes, idx_stream_t stream) {
     const char* what = "idx_topk";
-    (void)workspace;
-    (void)workspace_bytes;
     idx_status s = check_batch(batch, what);
     if (s != IDX_OK) return s;
     if (top_k < 1) return fail(IDX_ERR_INVALID_ARG, "%s: top_k < 1", what);
@@ -258,8 +256,10 @@ idx_status idx_topk(const float* scores, int64_t score_row_stride, idx_batch bat
     if (rows == 0) return IDX_OK;
     if (!idx || (!scores && max_keys > 0)) return fail(IDX_ERR_INVALID_ARG, "%s: NULL scores/idx", what);
     const Geom g = make_geom(batch);
+    if (workspace && !aligned16(workspace))
+        return fail(IDX_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", what);
     return from_cuda(launch_topk(scores, score_row_stride, g, top_k, block_size, idx, idx_row_stride,
-                                 n_sel, (cudaStream_t)stream),
+                                 n_sel, workspace, workspace ? workspace_bytes : 0, (cudaStream_t)stream),
                      what);
 }
 
@@ -291,6 +291,7 @@ size_t idx_workspace_size(int32_t op, int64_t n_rows, int32_t max_n_kv, int32_t 
     if (n_rows <= 0 || top_k <= 0) return 0;
     if ((op == IDX_OP_ATTN_DECODE || op == IDX_OP_ATTN_PREFILL) && n_q_heads == 128 && dv == 512)
         return mla_workspace_bytes(n_rows, top_k);
+    if (op == IDX_OP_TOPK) return topk_workspace_bytes(n_rows, top_k);
     return 0;
 }
 

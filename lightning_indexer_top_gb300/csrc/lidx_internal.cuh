@@ -111,9 +111,11 @@ cudaError_t launch_block_pool(const void* k_raw, int k_dtype, int64_t k_row_stri
                               const Geom& g, int C, int d, float* pooled, int64_t pool_seq_stride,
                               cudaStream_t st);
 
+// few rows with a workspace of topk_workspace_bytes(): multi-CTA passes; else one CTA per row
 cudaError_t launch_topk(const float* scores, int64_t score_row_stride, const Geom& g, int top_k,
-                        int block_size, int32_t* idx, int64_t idx_row_stride, int32_t* n_sel,
-                        cudaStream_t st);
+                        int block_size, int32_t* idx, int64_t idx_row_stride, int32_t* n_sel, void* ws,
+                        size_t ws_bytes, cudaStream_t st);
+size_t topk_workspace_bytes(int64_t n_rows, int top_k);
 
 cudaError_t launch_attn_generic(const void* q, int dtype, int Hq, int Hkv, int dk, int dv,
                                 const void* k, const void* v, int64_t kv_row_stride,

@@ -11,7 +11,7 @@ from __future__ import annotations
 import torch
 
 from . import Batch, idx_block_pool, idx_hadamard, idx_score, idx_topk, idx_workspace_size, topk_capacity
-from . import sparse_attn_decode, sparse_attn_prefill, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL
+from . import sparse_attn_decode, sparse_attn_prefill, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL, IDX_OP_TOPK
 from .workloads import Workload
 
 
@@ -34,6 +34,8 @@ class SparseAttentionStep:
         cap = topk_capacity(wl.top_k, C)
         self.idx = torch.empty(rows, cap, device=dev, dtype=torch.int32)
         self.n_sel = torch.empty(rows, device=dev, dtype=torch.int32)
+        tws = idx_workspace_size(IDX_OP_TOPK, rows, wl.max_n_kv, wl.top_k) if C <= 1 else 0
+        self.topk_ws = torch.empty(tws, device=dev, dtype=torch.uint8) if tws else None
         if out_dtype is None:   # f32 in -> f32 out, 16-bit in -> bf16 out
             out_dtype = torch.float32 if wl.q_attn.dtype == torch.float32 else torch.bfloat16
         self.out = torch.empty(rows, wl.q_attn.shape[1], wl.dv, device=dev, dtype=out_dtype)
@@ -65,7 +67,7 @@ class SparseAttentionStep:
 
     def select(self):
         idx_topk(self.scores, self.batch, self.wl.top_k, block_size=self.wl.block_size, idx=self.idx,
-                 n_sel=self.n_sel)
+                 n_sel=self.n_sel, workspace=self.topk_ws)
 
     def attend(self):
         wl = self.wl
@@ -87,6 +89,8 @@ class SparseAttentionStep:
     def launches_per_step(self) -> int:
         """Kernels one run() enqueues (library launches only)."""
         n = 3 + (1 if self.attn_ws is not None else 0)   # score, select, attend (+ split combine)
+        if self.topk_ws is not None:
+            n += 2                              # multi-CTA select: histogram, filter, finish
         if self.q_rot is not None:
             n += 2                              # two Hadamard rotations
         if self.wl.block_size > 1:

@@ -110,17 +110,27 @@ def _scores_cases():
     x = torch.randn(2, 70000, generator=g)
     x[:, 1000:1100] = x.max() + 1.0  # exact ties straddling the threshold
     yield "tie_block_at_top", x
+    # more keys in the threshold bin than the candidate list holds
+    yield "mass_ties", torch.randint(0, 2, (2, 30000), generator=g).float()
+    yield "long_row_beyond_bitmap", torch.randn(1, 300000, generator=g)
 
 
+def _topk_ws(path):
+    # "multi": the binding sizes the workspace (several CTAs per row for few rows);
+    # "single": a workspace too small for that, so one CTA handles each row
+    return None if path == "multi" else torch.empty(16, device=DEV, dtype=torch.uint8)
+
+
+@pytest.mark.parametrize("path", ["multi", "single"])
 @pytest.mark.parametrize("case", [c for c, _ in _scores_cases()])
 @pytest.mark.parametrize("top_k", [1, 64, 2048])
-def test_topk_bit_exact(case, top_k):
+def test_topk_bit_exact(case, top_k, path):
     scores = dict(_scores_cases())[case]
     rows, n = scores.shape
     n_kv = [n - 37 * r for r in range(rows)]
     s = scores.to(DEV)
     batch = L.Batch(_i32(n_kv), 1, n, kv_seq_stride=0)
-    idx, n_sel = L.idx_topk(s, batch, top_k)
+    idx, n_sel = L.idx_topk(s, batch, top_k, workspace=_topk_ws(path))
     torch.cuda.synchronize()
     idx_h, ns_h = idx.cpu().numpy(), n_sel.cpu().numpy()
     for r in range(rows):
@@ -130,13 +140,14 @@ def test_topk_bit_exact(case, top_k):
         assert np.all(idx_h[r, len(ref):] == -1)
 
 
-def test_topk_causal_rows_and_dense_short_rows():
+@pytest.mark.parametrize("path", ["multi", "single"])
+def test_topk_causal_rows_and_dense_short_rows(path):
     g = torch.Generator().manual_seed(42)
     T, n, top_k = 300, 3000, 100
     scores = torch.randint(-5, 6, (T, n), generator=g).float()
     q_pos = [int(x) for x in torch.randint(-2, n + 3, (T,), generator=g)]
     batch = L.Batch(_i32([n]), T, n, kv_seq_stride=0, q_pos=_i32(q_pos))
-    idx, n_sel = L.idx_topk(scores.to(DEV), batch, top_k)
+    idx, n_sel = L.idx_topk(scores.to(DEV), batch, top_k, workspace=_topk_ws(path))
     idx_h, ns_h = idx.cpu().numpy(), n_sel.cpu().numpy()
     for t in range(T):
         nv = O.visible_count(n, q_pos[t])
