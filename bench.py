@@ -49,10 +49,13 @@ WORKLOADS = {
     "long_decode_mla_ragged": ((5,), {}),
 }
 
-# DRAM bytes per launch of the scorer from an ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed by the SHA-256 of the kernel source it was taken on.
-# A source change makes the figure stale and the bench reports traffic = null.
-NCU_TRAFFIC = {}
+# DRAM bytes of the scorer per key from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum of one launch over 8 rows x 131072 keys, scaled to a launch by
+# the keys it scans), keyed by the SHA-256 of the kernel source it was taken on.  A
+# source change makes the figure stale and the bench reports traffic = null.
+NCU_TRAFFIC = {
+    "ef2cc3e0db8e589da31ef8ccf25fbc38673093269e125f20cf074f67cb2d183e": (268642816 + 6057728) / (8 * 131072),
+}
 
 
 def _dist():
@@ -122,6 +125,21 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The slowest rank's value (step times are reported as the max over ranks)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world_size: int, units_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's step time."""
+    return world_size * units_per_rank / (ms_per_step * 1e-3)
 
 
 def _sha(path):
@@ -261,11 +279,7 @@ def main():
     ms_score = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     ms_select = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     ms_attend = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    ms_step = ms_total / args.steps
-    if dist:
-        t = torch.tensor([ms_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t)
+    ms_step = max_over_ranks(ms_total / args.steps, dist, torch.device("cuda", local))
 
     # ---- end to end through the public API with pinned host buffers
     host_in = [wl.q_idx.cpu().pin_memory(), wl.w.cpu().pin_memory(), wl.q_attn.cpu().pin_memory()]
@@ -291,11 +305,7 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1) / args.steps
-    if dist:
-        t = torch.tensor([ms_e2e], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, torch.device("cuda", local))
 
     if rank != 0:
         dist.destroy_process_group() if dist else None
@@ -310,8 +320,9 @@ def main():
     hbm, bf16, peak_kind = _peaks()
     achieved = score_bytes / (ms_score * 1e-3) / 1e9
     src = os.path.join(ROOT, "lightning_indexer_top_gb300", "csrc", "k_score_tc.cu")
-    tr = NCU_TRAFFIC.get(_sha(src))
-    value = ws * B / (ms_step * 1e-3)
+    per_key = NCU_TRAFFIC.get(_sha(src))
+    tr = per_key * n_kv_total if per_key is not None else None
+    value = job_value(ws, B, ms_step)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -327,7 +338,7 @@ def main():
         "roofline": {"bound": "hbm", "kernel": "idx_score (key-cache scan)", "achieved": achieved, "peak": hbm,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": tr, "algorithmic_bytes_per_launch": score_bytes},
-        "e2e": {"value": ws * B / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_value(ws, B, ms_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clocks,
