@@ -327,10 +327,314 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Prefill (many query rows per sequence, causal): tiles of 128 query rows x
+// 256 keys of one sequence, persistent CTAs taking tiles round-robin.  Per tile
+// the key tile [256 x 128] is loaded once and stays in shared memory; for each
+// of the 64 heads the head's query tile Q_h [128 x 128] is loaded by TMA (a 3-D
+// tensor map over [rows, heads, d], so head h's rows are strided) and
+//     D_h[128 queries x 256 keys] = Q_h . K^T     (M=128, N=256, K=128)
+// goes to one of two 256-column TMEM buffers while eight epilogue warps (two per
+// TMEM lane quarter, one per 128-key half) add w[q, h] * relu(D_h) into f32
+// registers.  After the 64 heads the visible scores (key < n_vis of the row)
+// are written.  Tiles whose keys all lie beyond every row's causal bound are
+// skipped.
+// ---------------------------------------------------------------------------
+constexpr int kPQ = 128;                          // query rows per tile
+constexpr int kPK = 256;                          // keys per tile
+constexpr int kPStages = 3;                       // Q_h stages
+constexpr int kPQBytes = kPQ * kD * 2;            // 32 KB
+constexpr int kPKBytes = kPK * kD * 2;            // 64 KB
+constexpr int kPWBytes = kPQ * kH * 4;            // 32 KB
+constexpr int kPThreads = 320;                    // 10 warps
+constexpr int kPTmemCols = 512;
+
+struct PCtl {
+    uint64_t qfull[kPStages];
+    uint64_t qempty[kPStages];
+    uint64_t kfull, kempty;
+    uint64_t wfull, wempty;
+    uint64_t dfull[2], dempty[2];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t kPSmemBytes = 1024 + kPKBytes + (size_t)kPStages * kPQBytes + kPWBytes + sizeof(PCtl);
+
+struct PTile {
+    int b, qt, kt;      // sequence, query tile, key tile
+    bool live;          // some key of the tile is visible to some row of it
+};
+
+__device__ __forceinline__ PTile ptile_of(const Geom& g, int64_t tile, int q_tiles, int k_tiles) {
+    PTile p;
+    p.kt = (int)(tile % k_tiles);
+    const int64_t bq = tile / k_tiles;
+    p.qt = (int)(bq % q_tiles);
+    p.b = (int)(bq / q_tiles);
+    // visible keys of the tile's last row bound every row of it (q_pos grows along the rows)
+    int nv = 0;
+    for (int t = p.qt * kPQ; t < min(g.T, p.qt * kPQ + kPQ); ++t) nv = max(nv, row_n_vis(g, (int64_t)p.b * g.T + t));
+    p.live = p.kt * kPK < nv;
+    return p;
+}
+
+__device__ __forceinline__ bool pc_aborted(PCtl& c) { return __any_sync(0xffffffffu, *(volatile int*)&c.abort != 0); }
+__device__ __forceinline__ void pc_abort(PCtl& c, const Geom& g) {
+    *(volatile int*)&c.abort = 1;
+    flag(g.status, IDX_ERR_TIMEOUT);
+}
+
+template <int kBF16>
+__global__ void __launch_bounds__(kPThreads, 1) score_tc_prefill_kernel(
+    const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+    const __grid_constant__ CUtensorMap wmap, Geom g, float* __restrict__ scores, int64_t score_row_stride,
+    int q_tiles, int k_tiles) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ktile = smem;                                  // 2 x [256 rows x 128 B]
+    uint8_t* qst = ktile + kPKBytes;                        // kPStages x 2 x [128 rows x 128 B]
+    float* wt = reinterpret_cast<float*>(qst + (size_t)kPStages * kPQBytes);   // [128 rows][64 heads]
+    PCtl& c = *reinterpret_cast<PCtl*>(reinterpret_cast<uint8_t*>(wt) + kPWBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n_tiles = (int64_t)g.B * q_tiles * k_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kPStages; ++i) {
+            mbar_init(&c.qfull[i], 1);
+            mbar_init(&c.qempty[i], 1);
+        }
+        mbar_init(&c.kfull, 1);
+        mbar_init(&c.kempty, 1);
+        mbar_init(&c.wfull, 1);
+        mbar_init(&c.wempty, 8);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&c.dfull[i], 1);
+            mbar_init(&c.dempty[i], 8);
+        }
+        mbar_init(&c.done, 1);
+        c.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&wmap);
+    }
+    if (warp == 1) {
+        tmem_alloc(&c.tmem_base, kPTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = c.tmem_base;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer (one lane)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, tph = 0;
+            for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+                const PTile p = ptile_of(g, tile, q_tiles, k_tiles);
+                if (!p.live) continue;
+                const int32_t row0 = (int32_t)((int64_t)p.b * g.T + p.qt * kPQ);
+                const int32_t key0 = (int32_t)(seq_row0(g, p.b) + (int64_t)p.kt * kPK);
+                if (!mbar_wait(&c.kempty, tph ^ 1) || !mbar_wait(&c.wempty, tph ^ 1)) {
+                    pc_abort(c, g);
+                    break;
+                }
+                mbar_arrive_expect_tx(&c.kfull, kPKBytes);
+                tma_load_2d(ktile, &kmap, &c.kfull, 0, key0);
+                tma_load_2d(ktile + kPKBytes / 2, &kmap, &c.kfull, 64, key0);
+                mbar_arrive_expect_tx(&c.wfull, kPWBytes);
+                tma_load_2d(wt, &wmap, &c.wfull, 0, row0);
+                for (int h = 0; h < kH; ++h) {
+                    if (!mbar_wait(&c.qempty[stage], phase ^ 1)) {
+                        pc_abort(c, g);
+                        break;
+                    }
+                    uint8_t* dst = qst + (size_t)stage * kPQBytes;
+                    mbar_arrive_expect_tx(&c.qfull[stage], kPQBytes);
+                    tma_load_3d(dst, &qmap, &c.qfull[stage], 0, h, row0);
+                    tma_load_3d(dst + kPQBytes / 2, &qmap, &c.qfull[stage], 64, h, row0);
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (*(volatile int*)&c.abort) break;
+                tph ^= 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer (one lane)
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(kPQ, kPK, kBF16);
+            int stage = 0, buf = 0;
+            uint32_t phase = 0, bph = 0, tph = 0;
+            for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+                const PTile p = ptile_of(g, tile, q_tiles, k_tiles);
+                if (!p.live) continue;
+                if (!mbar_wait(&c.kfull, tph)) {
+                    pc_abort(c, g);
+                    break;
+                }
+                const uint32_t kb = smem_u32(ktile);
+                bool ok = true;
+                for (int h = 0; h < kH && ok; ++h) {
+                    if (!mbar_wait(&c.qfull[stage], phase) || !mbar_wait(&c.dempty[buf], bph ^ 1)) {
+                        pc_abort(c, g);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t qb = smem_u32(qst + (size_t)stage * kPQBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t off = (kk & 3) * 32;
+                        const uint64_t ad = desc_sw128_kmajor(qb + (kk >> 2) * (kPQBytes / 2) + off, 1024);
+                        const uint64_t bd = desc_sw128_kmajor(kb + (kk >> 2) * (kPKBytes / 2) + off, 1024);
+                        mma_f16_ss(tmem + buf * kPK, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&c.qempty[stage]);
+                    mma_commit(&c.dfull[buf]);
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                    if (++buf == 2) {
+                        buf = 0;
+                        bph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&c.kempty);
+                tph ^= 1;
+            }
+            mma_commit(&c.done);
+            mbar_wait(&c.done, 0);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- epilogue: 8 warps, thread = query row
+        const int ew = warp - 2;                  // 0..7
+        const int quad = warp & 3;                // TMEM lane quarter this warp may access
+        const int half = ew >> 2;                 // which 128 keys of the tile
+        const int ql = quad * 32 + lane;          // query row within the tile
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        int buf = 0;
+        uint32_t bph = 0, tph = 0;
+        for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            const PTile p = ptile_of(g, tile, q_tiles, k_tiles);
+            if (!p.live) continue;
+            if (pc_aborted(c) || !warp_wait(&c.wfull, tph)) {
+                pc_abort(c, g);
+                break;
+            }
+            float acc[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+            const float* wrow = wt + ql * kH;
+            bool ok = true;
+            for (int h = 0; h < kH; ++h) {
+                const float wv = wrow[h];
+                if (!warp_wait(&c.dfull[buf], bph)) {
+                    pc_abort(c, g);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ta = tmem + lane_off + buf * kPK + half * 128;
+#pragma unroll
+                for (int cb = 0; cb < 4; ++cb) {
+                    float v[32];
+                    tmem_ld_32x32b_x32(ta + cb * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[cb * 32 + i] = fmaf(wv, fmaxf(v[i], 0.f), acc[cb * 32 + i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c.dempty[buf]);
+                if (++buf == 2) {
+                    buf = 0;
+                    bph ^= 1;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c.wempty);
+            if (!ok) break;
+            const int t = p.qt * kPQ + ql;
+            if (t < g.T) {
+                const int64_t r = (int64_t)p.b * g.T + t;
+                const int nv = row_n_vis(g, r);
+                const int j0 = p.kt * kPK + half * 128;
+                float* dst = scores + r * score_row_stride + j0;
+                const int nw = min(128, nv - j0);
+                if (nw == 128 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+#pragma unroll
+                    for (int j = 0; j < 128; j += 4)
+                        *reinterpret_cast<float4*>(dst + j) =
+                            make_float4(acc[j] + 0.f, acc[j + 1] + 0.f, acc[j + 2] + 0.f, acc[j + 3] + 0.f);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 128; ++j)
+                        if (j < nw) dst[j] = acc[j] + 0.f;
+                }
+            }
+            tph ^= 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kPTmemCols);
+}
+
+cudaError_t launch_score_tc_prefill(const void* q, int q_dtype, const float* w, const void* k, int k_dtype,
+                                    int64_t k_row_stride, int64_t k_rows, const Geom& g, float* scores,
+                                    int64_t score_row_stride, cudaStream_t st) {
+    const int64_t n_rows = (int64_t)g.B * g.T;
+    if (n_rows == 0 || g.max_n_kv == 0) return cudaSuccess;
+    if (n_rows > INT32_MAX || k_rows > INT32_MAX) return cudaErrorNotSupported;
+    const bool bf16 = k_dtype == IDX_BF16;
+    CUtensorMap qm, km, wm;
+    if (!make_q3d_tmap(&qm, q, bf16, n_rows) || !make_key_tmap(&km, k, bf16, k_row_stride, k_rows, kPK) ||
+        !make_w_tmap(&wm, w, n_rows))
+        return cudaErrorNotSupported;
+    const int q_tiles = (g.T + kPQ - 1) / kPQ;
+    const int k_tiles = (g.max_n_kv + kPK - 1) / kPK;
+    const int64_t n_tiles = (int64_t)g.B * q_tiles * k_tiles;
+    const int grid = (int)(n_tiles < sm_count() ? n_tiles : sm_count());
+    if (bf16) {
+        auto kern = score_tc_prefill_kernel<1>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
+        kern<<<grid, kPThreads, kPSmemBytes, st>>>(qm, km, wm, g, scores, score_row_stride, q_tiles, k_tiles);
+    } else {
+        auto kern = score_tc_prefill_kernel<0>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
+        kern<<<grid, kPThreads, kPSmemBytes, st>>>(qm, km, wm, g, scores, score_row_stride, q_tiles, k_tiles);
+    }
+    (void)q_dtype;
+    return cudaGetLastError();
+}
+
 cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, int d, const void* k,
                             int k_dtype, int64_t k_row_stride, int64_t k_rows, const Geom& g, int block_size,
                             float* scores, int64_t score_row_stride, cudaStream_t st) {
-    if (H != kH || d != kD || k_dtype == IDX_F32 || block_size > 1 || g.T != 1) return cudaErrorNotSupported;
+    if (H != kH || d != kD || k_dtype == IDX_F32 || block_size > 1) return cudaErrorNotSupported;
+    if (g.T >= 64) {
+        // many query rows per sequence: query tiles on the tensor cores (same-type operands)
+        if (q_dtype != k_dtype || (reinterpret_cast<uintptr_t>(q) & 15u) || (k_row_stride % 8)) return cudaErrorNotSupported;
+        return launch_score_tc_prefill(q, q_dtype, w, k, k_dtype, k_row_stride, k_rows, g, scores, score_row_stride,
+                                       st);
+    }
+    if (g.T != 1) return cudaErrorNotSupported;
     if ((reinterpret_cast<uintptr_t>(k) & 15u) || (k_row_stride % 8) || k_rows < 1 || k_rows > INT32_MAX ||
         (reinterpret_cast<uintptr_t>(w) & 15u))
         return cudaErrorNotSupported;

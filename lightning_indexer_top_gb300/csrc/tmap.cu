@@ -40,6 +40,32 @@ bool encode_2d(CUtensorMap* m, const void* base, bool bf16, uint64_t cols, uint6
 
 }  // namespace
 
+// q [rows, 64 heads, 128] 16-bit: boxes {64 columns, 1 head, 128 rows}, 128-byte swizzle
+bool make_q3d_tmap(CUtensorMap* m, const void* q, bool bf16, int64_t rows) {
+    EncodeFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128, 64, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {128 * 2, 64 * 128 * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(q),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// w [rows, 64] f32: boxes of {64 heads, 128 rows}, no swizzle
+bool make_w_tmap(CUtensorMap* m, const float* w, int64_t rows) {
+    EncodeFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {64, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {64 * 4};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(w), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [rows, 128] 16-bit key cache: boxes of 64 columns x box_rows rows, 128-byte swizzle
 bool make_key_tmap(CUtensorMap* m, const void* k, bool bf16, int64_t k_row_stride, int64_t k_rows, int box_rows) {
     return encode_2d(m, k, bf16, 128, (uint64_t)k_rows, (uint64_t)k_row_stride * 2, 64, (uint32_t)box_rows);

@@ -412,3 +412,29 @@ def test_attention_mla_tc_selections_longer_than_one_split():
     for r in range(0, B, 7):
         ref = O.sparse_attention_mla(np64(q[r]), lh, idx[r, :sizes[r]].numpy(), scale, 512)
         assert np.max(np.abs(got[r] - ref)) <= 2e-2, r
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+def test_score_tensor_core_prefill_matches_oracle(dt):
+    # two sequences of 300 query rows each (not a multiple of the 128-row tile), continuing
+    # after cached prefixes of different lengths: q_pos = prefix + t
+    g = torch.Generator(device=DEV).manual_seed(73)
+    B, T, H, d = 2, 300, 64, 128
+    prefix = [700, 40]
+    n_kv = [p + T for p in prefix]
+    max_n = max(n_kv)
+    q = torch.randn(B * T, H, d, generator=g, device=DEV).to(dt)
+    w = torch.randn(B * T, H, generator=g, device=DEV) / 8
+    k = torch.randn(B * max_n, d, generator=g, device=DEV).to(dt)
+    q_pos = _i32([p + t for p in prefix for t in range(T)])
+    batch = L.Batch(_i32(n_kv), T, max_n, kv_seq_stride=max_n, q_pos=q_pos)
+    s = torch.full((B * T, max_n), 555.0, device=DEV)
+    L.idx_score(q, w, k, batch, scores=s)
+    torch.cuda.synchronize()
+    sh, kh = s.cpu().numpy(), np64(k)
+    for r in [0, 1, 127, 128, 129, 255, 299, 300, 301, 450, 599]:
+        b, t = divmod(r, T)
+        nv = prefix[b] + t + 1
+        ref = O.indexer_scores(np64(q[r]), np64(w[r]), kh[b * max_n:b * max_n + nv])
+        assert_scores_close(sh[r, :nv], ref, f"row {r}")
+        assert np.all(sh[r, nv:] == 555.0)
