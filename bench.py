@@ -47,6 +47,8 @@ WORKLOADS = {
     "decode_mla_8x8192": ((2,), {}),
     "decode_mla_64x8192": (("headline",), {"n_kv_override": 8192}),
     "long_decode_mla_ragged": ((5,), {}),
+    "prefill_mla_16384": ((3,), {}),
+    "prefill_mla_4096": ((3,), {"n_tokens_override": 4096}),
 }
 
 # DRAM bytes of the scorer per key from an ncu capture (dram__bytes_read.sum +
@@ -239,22 +241,25 @@ def main():
     step = SparseAttentionStep(wl, out_dtype=torch.bfloat16)
     stream = torch.cuda.current_stream()
 
-    # per-kernel events: score / select / attend of every timed step
+    # per-kernel events: (rotate) / score / select / attend of every timed step
     def timed_step(ev):
         ev[0].record(stream)
-        step.score()
+        if step.q_rot is not None:
+            step.rotate()
         ev[1].record(stream)
-        step.select()
+        step.score()
         ev[2].record(stream)
-        step.attend()
+        step.select()
         ev[3].record(stream)
+        step.attend()
+        ev[4].record(stream)
 
     for _ in range(max(args.warmup, 3)):
         step.run()
     torch.cuda.synchronize()
     L.idx_device_status(reset=True)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -276,9 +281,10 @@ def main():
         raise RuntimeError(f"device status {status} during the timed region")
 
     ms_total = t_start.elapsed_time(t_end)
-    ms_score = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    ms_select = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    ms_attend = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    ms_rotate = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ms_score = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    ms_select = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    ms_attend = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
     ms_step = max_over_ranks(ms_total / args.steps, dist, torch.device("cuda", local))
 
     # ---- end to end through the public API with pinned host buffers
@@ -311,17 +317,30 @@ def main():
         dist.destroy_process_group() if dist else None
         return
 
-    B = wl.B
-    n_kv_total = sum(wl.n_kv_host)
-    key_bytes = n_kv_total * wl.d * 2
-    # scorer's algorithmic bytes per launch: every key row read once, one f32 score written per
-    # key, the queries and weights read once
-    score_bytes = key_bytes + n_kv_total * 4 + B * wl.H * wl.d * 2 + B * wl.H * 4
+    B = wl.B * wl.T                       # query rows per step
     hbm, bf16, peak_kind = _peaks()
-    achieved = score_bytes / (ms_score * 1e-3) / 1e9
     src = os.path.join(ROOT, "lightning_indexer_top_gb300", "csrc", "k_score_tc.cu")
-    per_key = NCU_TRAFFIC.get(_sha(src))
-    tr = per_key * n_kv_total if per_key is not None else None
+    if wl.kind == "prefill":
+        # causal scoring: sum over rows of (visible keys) x H x d multiply-adds
+        n_kv_total = sum(min(t + 1, wl.n_kv_host[0]) for t in range(wl.T)) * wl.B
+        key_bytes = wl.k_idx.numel() * wl.k_idx.element_size()
+        flops = 2.0 * n_kv_total * wl.H * wl.d
+        roofline = {"bound": "tensor", "kernel": "idx_score (prefill, tcgen05)",
+                    "achieved": flops / (ms_score * 1e-3) / 1e12, "peak": bf16, "peak_kind": peak_kind,
+                    "unit": "TFLOP/s", "frac": flops / (ms_score * 1e-3) / 1e12 / bf16, "traffic": None,
+                    "algorithmic_flops_per_launch": flops}
+    else:
+        n_kv_total = sum(wl.n_kv_host)
+        key_bytes = n_kv_total * wl.d * 2
+        # scorer's algorithmic bytes per launch: every key row read once, one f32 score written per
+        # key, the queries and weights read once
+        score_bytes = key_bytes + n_kv_total * 4 + B * wl.H * wl.d * 2 + B * wl.H * 4
+        achieved = score_bytes / (ms_score * 1e-3) / 1e9
+        per_key = NCU_TRAFFIC.get(_sha(src))
+        roofline = {"bound": "hbm", "kernel": "idx_score (key-cache scan)", "achieved": achieved, "peak": hbm,
+                    "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
+                    "traffic": per_key * n_kv_total if per_key is not None else None,
+                    "algorithmic_bytes_per_launch": score_bytes}
     value = job_value(ws, B, ms_step)
 
     line = {
@@ -330,20 +349,20 @@ def main():
         "vs_baseline": None, "dtype": "f16/bf16 (f32 accumulate)",
         "data": "synthetic (seeded N(0,1) q/k/latent, w ~ N(0,1/64))",
         "config": {"workload": args.workload, "queries_per_gpu": B, "n_kv": max(wl.n_kv_host), "top_k": wl.top_k,
-                   "indexer": "64 heads x 128, F16 cache", "attention": "MLA 128 heads, 576/512 bf16",
+                   "indexer": "%d heads x %d, %s cache%s" % (wl.H, wl.d, str(wl.k_idx.dtype).replace("torch.", ""),
+                                                                ", Hadamard" if wl.hadamard else ""),
+                   "attention": "MLA 128 heads, 576/512 bf16",
                    "l2": "inputs larger than L2 (key cache %.2f GB, latent %.2f GB), no flush"
                          % (wl.k_idx.numel() * 2 / 1e9, wl.k_attn.numel() * 2 / 1e9)},
         "key_cache_gbs": key_bytes / ((ms_score + ms_select) * 1e-3) / 1e9,
-        "ms_per_kernel": {"score": ms_score, "topk": ms_select, "attention": ms_attend},
-        "roofline": {"bound": "hbm", "kernel": "idx_score (key-cache scan)", "achieved": achieved, "peak": hbm,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": tr, "algorithmic_bytes_per_launch": score_bytes},
+        "ms_per_kernel": {"hadamard": ms_rotate, "score": ms_score, "topk": ms_select, "attention": ms_attend},
+        "roofline": roofline,
         "e2e": {"value": job_value(ws, B, ms_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clocks,
     }
-    if not args.no_cpu_baseline and ws == 1:
+    if not args.no_cpu_baseline and ws == 1 and wl.kind == "decode":
         rows = list(range(min(args.cpu_sample, B)))
         dt, sels = cpu_oracle_queries(wl, rows)
         same = []

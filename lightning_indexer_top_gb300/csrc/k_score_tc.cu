@@ -28,6 +28,8 @@
 //               key per thread, then sum_h w_h*relu(d_h) and a coalesced store.
 // Every wait is bounded; a timeout records IDX_ERR_TIMEOUT and the CTA winds
 // down (drains its TMA loads and MMAs, frees TMEM) instead of hanging.
+#include <algorithm>
+
 #include "lidx_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -346,7 +348,14 @@ constexpr int kPStages = 3;                       // Q_h stages
 constexpr int kPQBytes = kPQ * kD * 2;            // 32 KB
 constexpr int kPKBytes = kPK * kD * 2;            // 64 KB
 constexpr int kPWBytes = kPQ * kH * 4;            // 32 KB
-constexpr int kPThreads = 320;                    // 10 warps
+#ifndef LIDX_PREFILL_EPI_WARPS
+#define LIDX_PREFILL_EPI_WARPS 8
+#endif
+constexpr int kPEpiWarps = LIDX_PREFILL_EPI_WARPS;  // a multiple of 4: each TMEM lane quarter split by keys
+constexpr int kPKW = kPK / (kPEpiWarps / 4);      // keys per epilogue warp
+static_assert(kPEpiWarps % 4 == 0 && kPKW % 32 == 0, "epilogue split");
+constexpr int kPThreads = 32 * (2 + kPEpiWarps);  // producer, MMA, epilogue
+constexpr int kPMaxQTiles = 4096;                 // (sequence, query tile) pairs enumerated in shared memory
 constexpr int kPTmemCols = 512;
 
 struct PCtl {
@@ -360,23 +369,29 @@ struct PCtl {
     int abort;
 };
 
-constexpr size_t kPSmemBytes = 1024 + kPKBytes + (size_t)kPStages * kPQBytes + kPWBytes + sizeof(PCtl);
+constexpr size_t kPSmemBytes =
+    1024 + kPKBytes + (size_t)kPStages * kPQBytes + kPWBytes + sizeof(PCtl) + (kPMaxQTiles + 1) * sizeof(int);
 
 struct PTile {
     int b, qt, kt;      // sequence, query tile, key tile
-    bool live;          // some key of the tile is visible to some row of it
 };
 
-__device__ __forceinline__ PTile ptile_of(const Geom& g, int64_t tile, int q_tiles, int k_tiles) {
+// Live tiles (some key visible to some row of the tile) are numbered with the
+// key tile fastest; pre[i] = live tiles of the (sequence, query tile) pairs
+// before pair i of this launch.  Consecutive CTAs therefore take neighbouring
+// key tiles of the same query tile, and the query rows they stream are shared
+// in L2.
+__device__ __forceinline__ PTile ptile_live(const int* pre, int n_pairs, int pair0, int q_tiles, int live) {
+    int lo = 0, hi = n_pairs;  // last pair with pre[pair] <= live
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid] <= live) lo = mid;
+        else hi = mid;
+    }
     PTile p;
-    p.kt = (int)(tile % k_tiles);
-    const int64_t bq = tile / k_tiles;
-    p.qt = (int)(bq % q_tiles);
-    p.b = (int)(bq / q_tiles);
-    // visible keys of the tile's last row bound every row of it (q_pos grows along the rows)
-    int nv = 0;
-    for (int t = p.qt * kPQ; t < min(g.T, p.qt * kPQ + kPQ); ++t) nv = max(nv, row_n_vis(g, (int64_t)p.b * g.T + t));
-    p.live = p.kt * kPK < nv;
+    p.b = (pair0 + lo) / q_tiles;
+    p.qt = (pair0 + lo) % q_tiles;
+    p.kt = live - pre[lo];
     return p;
 }
 
@@ -390,16 +405,28 @@ template <int kBF16>
 __global__ void __launch_bounds__(kPThreads, 1) score_tc_prefill_kernel(
     const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
     const __grid_constant__ CUtensorMap wmap, Geom g, float* __restrict__ scores, int64_t score_row_stride,
-    int q_tiles, int k_tiles) {
+    int q_tiles, int k_tiles, int pair0, int n_pairs) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ktile = smem;                                  // 2 x [256 rows x 128 B]
     uint8_t* qst = ktile + kPKBytes;                        // kPStages x 2 x [128 rows x 128 B]
     float* wt = reinterpret_cast<float*>(qst + (size_t)kPStages * kPQBytes);   // [128 rows][64 heads]
     PCtl& c = *reinterpret_cast<PCtl*>(reinterpret_cast<uint8_t*>(wt) + kPWBytes);
+    int* pre = reinterpret_cast<int*>(&c + 1);              // [n_pairs + 1]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n_tiles = (int64_t)g.B * q_tiles * k_tiles;
+
+    // live key tiles of each (sequence, query tile) pair: the keys visible to the
+    // pair's rows, rounded up to whole tiles (one warp per pair)
+    for (int i = warp; i < n_pairs; i += kPThreads / 32) {
+        const int b = (pair0 + i) / q_tiles, qt = (pair0 + i) % q_tiles;
+        int nv = 0;
+        for (int t = qt * kPQ + lane; t < min(g.T, qt * kPQ + kPQ); t += 32)
+            nv = max(nv, row_n_vis(g, (int64_t)b * g.T + t));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) nv = max(nv, __shfl_xor_sync(0xffffffffu, nv, o));
+        if (lane == 0) pre[i + 1] = min(k_tiles, (nv + kPK - 1) / kPK);
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kPStages; ++i) {
@@ -409,10 +436,10 @@ __global__ void __launch_bounds__(kPThreads, 1) score_tc_prefill_kernel(
         mbar_init(&c.kfull, 1);
         mbar_init(&c.kempty, 1);
         mbar_init(&c.wfull, 1);
-        mbar_init(&c.wempty, 8);
+        mbar_init(&c.wempty, kPEpiWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&c.dfull[i], 1);
-            mbar_init(&c.dempty[i], 8);
+            mbar_init(&c.dempty[i], kPEpiWarps);
         }
         mbar_init(&c.done, 1);
         c.abort = 0;
@@ -427,19 +454,36 @@ __global__ void __launch_bounds__(kPThreads, 1) score_tc_prefill_kernel(
         tmem_alloc(&c.tmem_base, kPTmemCols);
         tmem_relinquish();
     }
+    __syncthreads();
+    if (warp == 0) {
+        // inclusive scan of the per-pair counts
+        int carry = 0;
+        for (int base = 0; base < n_pairs; base += 32) {
+            const int i = base + lane;
+            int v = i < n_pairs ? pre[i + 1] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (i < n_pairs) pre[i + 1] = carry + v;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) pre[0] = 0;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = c.tmem_base;
+    const int n_live = pre[n_pairs];
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer (one lane)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0, tph = 0;
-            for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-                const PTile p = ptile_of(g, tile, q_tiles, k_tiles);
-                if (!p.live) continue;
+            for (int64_t live = blockIdx.x; live < n_live; live += gridDim.x) {
+                const PTile p = ptile_live(pre, n_pairs, pair0, q_tiles, (int)live);
                 const int32_t row0 = (int32_t)((int64_t)p.b * g.T + p.qt * kPQ);
                 const int32_t key0 = (int32_t)(seq_row0(g, p.b) + (int64_t)p.kt * kPK);
                 if (!mbar_wait(&c.kempty, tph ^ 1) || !mbar_wait(&c.wempty, tph ^ 1)) {
@@ -476,9 +520,8 @@ __global__ void __launch_bounds__(kPThreads, 1) score_tc_prefill_kernel(
             const uint32_t idesc = idesc_f16_f32(kPQ, kPK, kBF16);
             int stage = 0, buf = 0;
             uint32_t phase = 0, bph = 0, tph = 0;
-            for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-                const PTile p = ptile_of(g, tile, q_tiles, k_tiles);
-                if (!p.live) continue;
+            for (int64_t live = blockIdx.x; live < n_live; live += gridDim.x) {
+                const PTile p = ptile_live(pre, n_pairs, pair0, q_tiles, (int)live);
                 if (!mbar_wait(&c.kfull, tph)) {
                     pc_abort(c, g);
                     break;
@@ -521,23 +564,22 @@ __global__ void __launch_bounds__(kPThreads, 1) score_tc_prefill_kernel(
         __syncwarp();
     } else {
         // ---------------------------------------------------------- epilogue: 8 warps, thread = query row
-        const int ew = warp - 2;                  // 0..7
+        const int ew = warp - 2;
         const int quad = warp & 3;                // TMEM lane quarter this warp may access
-        const int half = ew >> 2;                 // which 128 keys of the tile
+        const int part = ew >> 2;                 // which kPKW keys of the tile
         const int ql = quad * 32 + lane;          // query row within the tile
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         int buf = 0;
         uint32_t bph = 0, tph = 0;
-        for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-            const PTile p = ptile_of(g, tile, q_tiles, k_tiles);
-            if (!p.live) continue;
+        for (int64_t live = blockIdx.x; live < n_live; live += gridDim.x) {
+            const PTile p = ptile_live(pre, n_pairs, pair0, q_tiles, (int)live);
             if (pc_aborted(c) || !warp_wait(&c.wfull, tph)) {
                 pc_abort(c, g);
                 break;
             }
-            float acc[128];
+            float acc[kPKW];
 #pragma unroll
-            for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+            for (int j = 0; j < kPKW; ++j) acc[j] = 0.f;
             const float* wrow = wt + ql * kH;
             bool ok = true;
             for (int h = 0; h < kH; ++h) {
@@ -548,9 +590,9 @@ __global__ void __launch_bounds__(kPThreads, 1) score_tc_prefill_kernel(
                     break;
                 }
                 tc_fence_after();
-                const uint32_t ta = tmem + lane_off + buf * kPK + half * 128;
+                const uint32_t ta = tmem + lane_off + buf * kPK + part * kPKW;
 #pragma unroll
-                for (int cb = 0; cb < 4; ++cb) {
+                for (int cb = 0; cb < kPKW / 32; ++cb) {
                     float v[32];
                     tmem_ld_32x32b_x32(ta + cb * 32, v);
                     tmem_ld_wait();
@@ -572,17 +614,17 @@ __global__ void __launch_bounds__(kPThreads, 1) score_tc_prefill_kernel(
             if (t < g.T) {
                 const int64_t r = (int64_t)p.b * g.T + t;
                 const int nv = row_n_vis(g, r);
-                const int j0 = p.kt * kPK + half * 128;
+                const int j0 = p.kt * kPK + part * kPKW;
                 float* dst = scores + r * score_row_stride + j0;
-                const int nw = min(128, nv - j0);
-                if (nw == 128 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+                const int nw = min(kPKW, nv - j0);
+                if (nw == kPKW && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
 #pragma unroll
-                    for (int j = 0; j < 128; j += 4)
+                    for (int j = 0; j < kPKW; j += 4)
                         *reinterpret_cast<float4*>(dst + j) =
                             make_float4(acc[j] + 0.f, acc[j + 1] + 0.f, acc[j + 2] + 0.f, acc[j + 3] + 0.f);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 128; ++j)
+                    for (int j = 0; j < kPKW; ++j)
                         if (j < nw) dst[j] = acc[j] + 0.f;
                 }
             }
@@ -609,19 +651,24 @@ cudaError_t launch_score_tc_prefill(const void* q, int q_dtype, const float* w, 
         return cudaErrorNotSupported;
     const int q_tiles = (g.T + kPQ - 1) / kPQ;
     const int k_tiles = (g.max_n_kv + kPK - 1) / kPK;
-    const int64_t n_tiles = (int64_t)g.B * q_tiles * k_tiles;
-    const int grid = (int)(n_tiles < sm_count() ? n_tiles : sm_count());
-    if (bf16) {
-        auto kern = score_tc_prefill_kernel<1>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
-        kern<<<grid, kPThreads, kPSmemBytes, st>>>(qm, km, wm, g, scores, score_row_stride, q_tiles, k_tiles);
-    } else {
-        auto kern = score_tc_prefill_kernel<0>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
-        kern<<<grid, kPThreads, kPSmemBytes, st>>>(qm, km, wm, g, scores, score_row_stride, q_tiles, k_tiles);
+    const int64_t pairs = (int64_t)g.B * q_tiles;
+    auto kern = bf16 ? score_tc_prefill_kernel<1> : score_tc_prefill_kernel<0>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmemBytes);
+    if (e != cudaSuccess) return e;
+    // one launch per chunk of (sequence, query tile) pairs: at most kPMaxQTiles,
+    // and few enough that the chunk's tiles are numbered in 32 bits
+    const int64_t chunk = std::min<int64_t>(kPMaxQTiles, std::max<int64_t>(1, INT32_MAX / k_tiles));
+    for (int64_t p0 = 0; p0 < pairs; p0 += chunk) {
+        const int np = (int)std::min<int64_t>(pairs - p0, chunk);
+        const int64_t max_live = (int64_t)np * k_tiles;
+        const int grid = (int)(max_live < sm_count() ? max_live : sm_count());
+        kern<<<grid, kPThreads, kPSmemBytes, st>>>(qm, km, wm, g, scores, score_row_stride, q_tiles, k_tiles, (int)p0,
+                                                   np);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
     (void)q_dtype;
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, int d, const void* k,

@@ -141,7 +141,7 @@ def make(cfg, device="cuda", *, n_kv_override=None, batch_override=None, n_token
         w = _randn((n, H), torch.float32, g, dev, std=1 / math.sqrt(H))
         qa = _randn((n, Hq, dk), torch.bfloat16, g, dev)
         lat = _randn((n, dk), torch.bfloat16, g, dev)
-        return Workload("prefill_mla_16384", "prefill", 1, n, torch.tensor([n], **i32), [n], n, top_k, H, d,
+        return Workload(f"prefill_mla_{n}", "prefill", 1, n, torch.tensor([n], **i32), [n], n, top_k, H, d,
                         q, w, k, 1 / math.sqrt(192), qa, lat, None, dv, kv_seq_stride=n,
                         q_pos=torch.arange(n, **i32), hadamard=True)
 

@@ -438,3 +438,31 @@ def test_score_tensor_core_prefill_matches_oracle(dt):
         ref = O.indexer_scores(np64(q[r]), np64(w[r]), kh[b * max_n:b * max_n + nv])
         assert_scores_close(sh[r, :nv], ref, f"row {r}")
         assert np.all(sh[r, nv:] == 555.0)
+
+
+def test_score_tensor_core_prefill_many_short_sequences():
+    # 4100 sequences of 64 query rows: more (sequence, query tile) pairs than one launch
+    # enumerates, some sequences without keys, and query positions out of order within a
+    # sequence (the visible-key bound of a tile is the largest of its rows)
+    g = torch.Generator(device=DEV).manual_seed(74)
+    B, T, H, d, max_n = 4100, 64, 64, 128, 300
+    n_kv = [(b * 37) % (max_n + 1) for b in range(B)]
+    q = torch.randn(B * T, H, d, generator=g, device=DEV).to(torch.bfloat16)
+    w = torch.randn(B * T, H, generator=g, device=DEV) / 8
+    k = torch.randn(B * max_n, d, generator=g, device=DEV).to(torch.bfloat16)
+    gc = torch.Generator().manual_seed(75)
+    q_pos = torch.cat([torch.randint(-1, max(n, 1), (T,), generator=gc) for n in n_kv]).to(torch.int32)
+    batch = L.Batch(_i32(n_kv), T, max_n, kv_seq_stride=max_n, q_pos=q_pos.to(DEV))
+    s = torch.full((B * T, max_n), 555.0, device=DEV)
+    L.idx_score(q, w, k, batch, scores=s)
+    torch.cuda.synchronize()
+    rows = [0, 63, 64 * 37 + 5] + list(range(64 * 4095, 64 * 4100, 13)) + list(range(101, B * T, 9973))
+    qp = q_pos.numpy()
+    for r in rows:
+        b = r // T
+        nv = min(int(qp[r]) + 1, n_kv[b]) if qp[r] >= 0 else 0
+        got = s[r].cpu().numpy()
+        if nv:
+            ref = O.indexer_scores(np64(q[r]), np64(w[r]), np64(k[b * max_n:b * max_n + nv]))
+            assert_scores_close(got[:nv], ref, f"row {r}")
+        assert np.all(got[nv:] == 555.0), r
