@@ -8,13 +8,13 @@
 // The output accumulator O [128 heads x 512] f32 fills all 512 TMEM columns,
 // so one work unit (query row, key split) runs on a CLUSTER OF TWO CTAs:
 //   rank 0: Q [128 x 576] bf16 lives in TMEM (288 columns) as the MMA A
-//           operand; key tiles of 64 selected rows x 576 are gathered by TMA
-//           (tile::gather4, 128-byte swizzle) into a 2-stage ring;
+//           operand; key tiles of 64 selected rows x 576 are gathered with
+//           16-byte cp.async copies (128-byte swizzle) into a 2-stage ring;
 //           S = Q K^T (M=128 heads, N=64 keys, K=576) goes to one of two TMEM
 //           buffers; four softmax warps (thread = head) turn S into
-//           P = 2^(S*scale*log2e - m) as bf16 and store P, the per-head
-//           rescale factor, row sum and max straight into rank 1's shared
-//           memory (DSMEM), then release-arrive on rank 1's barrier.
+//           P = 2^(S*scale*log2e - m) as bf16 and stage P with the per-head
+//           rescale factor, row sum and max; a sender warp bulk-copies the
+//           packet into rank 1's shared memory (DSMEM).
 //   rank 1: O lives in TMEM (512 columns); value tiles (the same rows, first
 //           512 columns) are gathered into its own ring; O += P V with P as a
 //           K-major and V as an MN-major shared-memory operand (M=128,
@@ -47,8 +47,16 @@ constexpr int kPBytes = kHq * kKeys * 2;                // P tile, bf16, 128-byt
 constexpr int kPktBytes = kPBytes + 3 * kHq * 4;        // P tile + alpha, l, m per head
 constexpr int kPktStride = 18432;                       // P tile + tail, 1024-aligned
 constexpr int kMaxKps = 4096;                           // selected keys per split, at most
-constexpr int kThreads = 288;                           // 9 warps
-constexpr int kProducerWarps = 4;                       // warps 0, 6, 7, 8
+#ifndef LIDX_MLA_WARPS
+#define LIDX_MLA_WARPS 12
+#endif
+// Random 1152-byte row gathers by cp.async are bound by the copies each warp
+// keeps in flight: one SM reaches ~22 GB/s with 4 issuing warps, ~33 GB/s with
+// 8 and ~40 GB/s with 16 (about HBM speed over all SMs), so every warp without
+// another role gathers.
+constexpr int kThreads = 32 * LIDX_MLA_WARPS;
+constexpr int kProducerWarps = LIDX_MLA_WARPS - 6;      // warps 0 and 7..
+static_assert(kProducerWarps >= 1, "warp roles");
 constexpr int kTmemCols = 512;
 constexpr int kSCol0 = 320;                             // rank 0: S buffers at 320 and 384 (Q at 0..287)
 constexpr float kRescaleLog2 = 8.f;
@@ -125,8 +133,10 @@ __device__ __forceinline__ Unit make_unit(const Geom& g, const int32_t* n_sel, i
 // the 128-byte swizzled layout the MMA descriptors read: column block
 // db = chunk/8 at db*8192, row at row*128, the 16-byte chunk at
 // ((chunk%8) ^ (row%8))*16.  A warp instruction copies 512 contiguous bytes.
-// Tile t is announced (xfull, one arrival per producer lane) once the copies of
-// tile t+1 are in flight, so two tiles' loads overlap.
+// Each producer lane hands its copies of tile t to xfull with a no-increment
+// cp.async arrival, so a tile is announced the moment its bytes have landed
+// and the producers go straight on to the next free stage.  The consumer
+// orders the landed bytes before its MMAs with a proxy fence.
 template <int kChunks>
 __device__ __forceinline__ void gather_tiles(Ctl& c, uint8_t* xtiles, const __nv_bfloat16* lat,
                                              int64_t lat_row_stride, const Unit& u, const int32_t* rows_s,
@@ -134,7 +144,6 @@ __device__ __forceinline__ void gather_tiles(Ctl& c, uint8_t* xtiles, const __nv
     const int lane = threadIdx.x & 31;
     const char* base = reinterpret_cast<const char*>(lat);
     const int64_t row_bytes = lat_row_stride * 2;
-    int issued = 0;
     for (int t = 0; t < u.n_tiles; ++t) {
         const int stage = t & 1;
         const uint32_t ph = (uint32_t)((t >> 1) & 1);
@@ -151,17 +160,10 @@ __device__ __forceinline__ void gather_tiles(Ctl& c, uint8_t* xtiles, const __nv
             const uint32_t dst = dst0 + (cc >> 3) * kBlockBytes + row * 128 + (((cc & 7) ^ (row & 7)) << 4);
             cp_async16(dst, src);
         }
-        cp_async_commit();
-        ++issued;
-        if (t > 0) {
-            cp_async_wait<1>();
-            fence_proxy_async_smem();
-            mbar_arrive(&c.xfull[(t - 1) & 1]);
-        }
+        cp_async_mbar_arrive_noinc(&c.xfull[stage]);
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (issued > 0) mbar_arrive(&c.xfull[(issued - 1) & 1]);
+    // no copy may still be writing when the CTA winds down
+    cp_async_wait_all();
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -230,7 +232,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
 
-    const int producer = warp == 0 ? 0 : (warp >= 6 ? warp - 5 : -1);   // producer index or -1
+    const int producer = warp == 0 ? 0 : (warp >= 7 ? warp - 6 : -1);   // producer index or -1
     if (rank == 0) {
         if (producer >= 0) {
             gather_tiles<kDkBlocks * 8>(c, xtiles, lat, lat_row_stride, u, rows_s, producer, g.status);
@@ -249,6 +251,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         abort_cta(c, g.status);
                         break;
                     }
+                    fence_proxy_async_smem();   // cp.async bytes (generic proxy) before the MMA reads them
                     tc_fence_after();
                     const uint32_t kb = smem_u32(xtiles + (size_t)stage * kKTileBytes);
                     const uint32_t d = tmem + kSCol0 + sb * kKeys;
@@ -262,8 +265,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(&c.done);
                 mbar_wait(&c.done, 0);
-            } else if (lane == 1) {
-                // ---------------------------------------------------- P packet sender
+            }
+            __syncwarp();
+        } else if (warp == 6) {
+            if (lane == 0) {
+                // ---------------------------------------------------- P packet sender (own warp: never
+                // held up behind the MMA issuer)
                 for (int t = 0; t < u.n_tiles; ++t) {
                     const int j = t & 1;
                     const uint32_t ph = (uint32_t)((t >> 1) & 1);
@@ -291,28 +298,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (!aborted(c)) mbar_wait(&c.pfree[t & 1], (uint32_t)((t >> 1) & 1));
             }
             __syncwarp();
-        } else {
+        } else if (warp >= 2 && warp <= 5) {
             // ---------------------------------------------------------- Q to TMEM, then softmax (thread = head)
             const int h = quad * 32 + lane;
             if (u.n_tiles > 0) {
                 const uint4* src = reinterpret_cast<const uint4*>(q + (u.r * kHq + h) * (int64_t)kDk);
-#pragma unroll 1
-                for (int cb0 = 0; cb0 < kDkBlocks; cb0 += 3) {
-                    uint4 x[24];
+                // column block cb+1 is loading while block cb goes to TMEM
+                uint4 xn[8];
 #pragma unroll
-                    for (int i = 0; i < 24; ++i) x[i] = src[cb0 * 8 + i];
+                for (int i = 0; i < 8; ++i) xn[i] = src[i];
 #pragma unroll
-                    for (int k3 = 0; k3 < 3; ++k3) {
-                        uint32_t regs[32];
+                for (int cb = 0; cb < kDkBlocks; ++cb) {
+                    uint32_t regs[32];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            regs[4 * i] = x[k3 * 8 + i].x;
-                            regs[4 * i + 1] = x[k3 * 8 + i].y;
-                            regs[4 * i + 2] = x[k3 * 8 + i].z;
-                            regs[4 * i + 3] = x[k3 * 8 + i].w;
-                        }
-                        tmem_st_32x32b_x32(tmem + lane_off + (cb0 + k3) * 32, regs);
+                    for (int i = 0; i < 8; ++i) {
+                        regs[4 * i] = xn[i].x;
+                        regs[4 * i + 1] = xn[i].y;
+                        regs[4 * i + 2] = xn[i].z;
+                        regs[4 * i + 3] = xn[i].w;
                     }
+                    if (cb + 1 < kDkBlocks) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) xn[i] = src[(cb + 1) * 8 + i];
+                    }
+                    tmem_st_32x32b_x32(tmem + lane_off + cb * 32, regs);
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -407,6 +416,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         abort_cta(c, g.status);
                         break;
                     }
+                    fence_proxy_async_smem();
                     tc_fence_after();
                     const uint32_t pb = smem_u32(pkts + j * kPktStride);
                     const uint32_t vb = smem_u32(xtiles + (size_t)stage * kKTileBytes);
@@ -428,7 +438,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mbar_wait(&c.done, 0);
             }
             __syncwarp();
-        } else {
+        } else if (warp >= 2 && warp <= 5) {
             // ---------------------------------------------------------- correction + output (thread = head)
             const int h = quad * 32 + lane;
             bool ok = true;

@@ -121,6 +121,14 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// the barrier receives one arrival (counted in its expected count) once every
+// cp.async this thread issued before has completed; the thread does not wait
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // warp-uniform wait: every lane waits, and the warp agrees on the outcome
 // (a timeout seen by any lane counts for the whole warp)
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
