@@ -15,87 +15,167 @@
 // the epilogue thread that owns a lane applies ReLU, weights and sums its 64
 // head columns with no cross-thread reduction.
 //
-// Persistent CTAs (one per SM).  The (row, 128-key tile) pairs of all query
-// rows form one flat list, split evenly over the CTAs, so ragged n_kv is
-// balanced.  Warp roles:
-//   warp 0      producer: TMA loads of key tiles (two 64-column boxes, 128-byte
-//               swizzle) into a 6-stage ring; at each new query row it also
-//               converts that row's q to the key dtype and writes it, swizzled,
-//               into one of two q buffers (the MMA's B operand).
+// Persistent CTAs (one per SM) with dynamic scheduling.  The work is split into
+// chunks of up to 8 key tiles of one query row; CTAs take chunks in order from
+// a device counter, so SMs that stream faster take more chunks (on GB300 some
+// SMs sustain ~15% less bandwidth than others, and an even static split ends
+// on the slowest).  Chunks are numbered row by row through a prefix of the
+// rows' chunk counts that the CTA builds in shared memory; above kMaxPrefixRows
+// rows a chunk is a whole row.  Warp roles:
+//   warp 0      producer (one lane): takes a chunk, publishes its descriptor
+//               (row, first tile, end tile) in a small ring, and issues the TMA
+//               loads of its key tiles (two 64-column boxes, 128-byte swizzle)
+//               into a 5-stage ring.
 //   warp 1      TMEM owner and MMA issuer (one lane): 8 tcgen05.mma per tile
 //               into one of 4 TMEM accumulators of 64 columns.
 //   warps 2-5   epilogue: tcgen05.ld of the tile's [128 x 64] accumulator, one
 //               key per thread, then sum_h w_h*relu(d_h) and a coalesced store.
+//   warp 6      q stager: converts each chunk's query row q to the key dtype
+//               with 16-byte loads and writes it, swizzled, into one of two q
+//               buffers (the MMA's B operand), a chunk ahead of the MMAs.
 // Every wait is bounded; a timeout records IDX_ERR_TIMEOUT and the CTA winds
 // down (drains its TMA loads and MMAs, frees TMEM) instead of hanging.
 #include <algorithm>
+#include <atomic>
 
 #include "lidx_internal.cuh"
 #include "sm100_ptx.cuh"
 
 namespace lidx {
+
+// chunk counters of the decode scorer: [next chunk, CTAs finished] per slot; a
+// launch uses one slot (round-robin on the host) and its last CTA zeroes it
+constexpr int kSchedSlots = 1024;
+__device__ unsigned int g_score_sched[kSchedSlots][2];
+
 namespace {
 using namespace sm100;
 
 constexpr int kTileKeys = 128;
 constexpr int kH = 64;
 constexpr int kD = 128;
-constexpr int kStages = 6;
+#ifndef LIDX_SCORE_STAGES
+#define LIDX_SCORE_STAGES 5
+#endif
+#ifndef LIDX_SCORE_CHUNK
+#define LIDX_SCORE_CHUNK 8
+#endif
+constexpr int kStages = LIDX_SCORE_STAGES;
 constexpr int kAcc = 4;
 constexpr int kTmemCols = kAcc * kH;                 // 256
 constexpr int kTileBytes = kTileKeys * kD * 2;       // 32 KB
 constexpr int kHalfBytes = kTileBytes / 2;           // one 64-column box
 constexpr int kQBytes = kH * kD * 2;                 // 16 KB
 constexpr int kQHalfBytes = kQBytes / 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
+constexpr int kChunkTiles = LIDX_SCORE_CHUNK;        // key tiles (32 KB each) per chunk
+constexpr int kRing = 4;                             // chunk descriptors in flight
+constexpr int kQBufs = 3;                            // staged q rows (one per chunk) in flight
+constexpr int kMaxPrefixRows = 2048;
+
+struct Chunk {
+    int64_t row;      // query row, -1 = no more chunks
+    int t0, t1;       // key tiles [t0, t1) of the row
+};
 
 struct Ctl {
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t tfull[kAcc];
     uint64_t tempty[kAcc];
-    uint64_t qfull[2];
-    uint64_t qempty[2];
+    uint64_t qfull[kQBufs];
+    uint64_t qempty[kQBufs];
+    uint64_t cfull[kRing];
+    uint64_t cempty[kRing];
     uint64_t done;
+    Chunk chunk[kRing];
     uint32_t tmem_base;
     int abort;
-    int64_t r_begin;     // first query row of this CTA's range
-    int t_begin;         // tile index inside that row
-    int64_t count;       // tiles in this CTA's range
+    int n_chunks;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kTileBytes + 2 * kQBytes + sizeof(Ctl);
+constexpr int kChunkReaders = 1 + 4 + 1;             // MMA lane, 4 epilogue warps, q stager
+constexpr size_t kSmemBytes =
+    1024 + (size_t)kStages * kTileBytes + kQBufs * kQBytes + sizeof(Ctl) + (2 * kMaxPrefixRows + 1) * sizeof(int);
 
 template <typename T> constexpr bool kIsBF16 = false;
 template <> constexpr bool kIsBF16<__nv_bfloat16> = true;
 
 __device__ __forceinline__ int row_tiles(int n_keys) { return (n_keys + kTileKeys - 1) / kTileKeys; }
+__device__ __forceinline__ int row_chunks(int n_keys) {
+    return (row_tiles(n_keys) + kChunkTiles - 1) / kChunkTiles;
+}
 
-// Walks the flat (row, tile) list in order, skipping rows without keys.
-struct TileCursor {
-    int64_t r;
-    int t;
-    int n_keys;
-    int n_tiles;
-    __device__ void start(const Geom& g, int64_t r0, int t0, int64_t n_rows) {
-        r = r0;
-        t = t0;
-        n_keys = r < n_rows ? row_n_vis(g, r) : 0;   // an empty share may start past the last row
-        n_tiles = row_tiles(n_keys);
+// one query row's q [64 heads x 128] -> key dtype TK in the MMA's B layout
+// (two 64-column halves, rows of 128 bytes, 16-byte chunks swizzled by row),
+// 16-byte loads and stores, the warp's 32 lanes over the 1024 chunks
+// (all loads of a batch are issued before the first conversion: two round
+// trips per row for 16-bit q, four for f32)
+template <typename TK, typename TQ>
+__device__ __forceinline__ void stage_q_row(const TQ* __restrict__ qrow, uint8_t* qdst, int lane) {
+    constexpr int kPerLane = kH * kD / 8 / 32;                   // 32 chunks of 8 elements
+    constexpr int kBatch = sizeof(TQ) == 2 ? 16 : 8;
+#pragma unroll
+    for (int b0 = 0; b0 < kPerLane; b0 += kBatch) {
+        uint4 raw[kBatch * sizeof(TQ) / 2];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int ch = (b0 + i) * 32 + lane;
+            const uint4* src = reinterpret_cast<const uint4*>(qrow + ch * 8);
+            if constexpr (sizeof(TQ) == 2) {
+                raw[i] = src[0];
+            } else {
+                raw[2 * i] = src[0];
+                raw[2 * i + 1] = src[1];
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int ch = (b0 + i) * 32 + lane;
+            const int h = ch >> 4, cc = ch & 15;
+            const int half = cc >> 3, c8 = cc & 7;
+            TK vals[8];
+            if constexpr (sizeof(TQ) == 2) {
+                const TQ* e = reinterpret_cast<const TQ*>(&raw[i]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) vals[j] = from_f32<TK>(to_f32(e[j]));
+            } else {
+                const float* e = reinterpret_cast<const float*>(&raw[2 * i]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) vals[j] = from_f32<TK>(e[j]);
+            }
+            uint8_t* dst = qdst + half * kQHalfBytes + h * 128 + ((c8 ^ (h & 7)) << 4);
+            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(vals);
+        }
     }
-    // advance one tile; returns true when the next tile starts a new row
-    __device__ bool next(const Geom& g, int64_t n_rows) {
-        if (++t < n_tiles) return false;
-        t = 0;
-        do {
-            ++r;
-            if (r >= n_rows) break;
-            n_keys = row_n_vis(g, r);
-            n_tiles = row_tiles(n_keys);
-        } while (n_tiles == 0);
-        return true;
+}
+
+// chunk number `ch` -> (row, tiles); prefix mode: pre[i] = chunks of the rows
+// before row i, nvis[i] = visible keys of row i (both in shared memory)
+__device__ __forceinline__ Chunk chunk_of(const Geom& g, const int* pre, const int* nvis, int64_t n_rows,
+                                          bool prefix, int ch, int n_chunks) {
+    Chunk d;
+    d.row = -1;
+    d.t0 = d.t1 = 0;
+    if (ch >= n_chunks) return d;
+    if (prefix) {
+        int lo = 0, hi = (int)n_rows;   // last row with pre[row] <= ch
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pre[mid] <= ch) lo = mid;
+            else hi = mid;
+        }
+        d.row = lo;
+        const int nt = row_tiles(nvis[lo]);
+        d.t0 = (ch - pre[lo]) * kChunkTiles;
+        d.t1 = min(nt, d.t0 + kChunkTiles);
+    } else {
+        d.row = ch;
+        d.t0 = 0;
+        d.t1 = row_tiles(row_n_vis(g, ch));
     }
-};
+    return d;
+}
 
 __device__ __forceinline__ void abort_cta(Ctl& c, const Geom& g) {
     *(volatile int*)&c.abort = 1;
@@ -105,18 +185,31 @@ __device__ __forceinline__ void abort_cta(Ctl& c, const Geom& g) {
 // the whole warp sees the same answer
 __device__ __forceinline__ bool warp_aborted(Ctl& c) { return __any_sync(0xffffffffu, *(volatile int*)&c.abort != 0); }
 
+// a consumer's next chunk descriptor (the whole warp waits; lane 0 releases the slot)
+__device__ __forceinline__ bool warp_next_chunk(Ctl& c, int k, Chunk& d) {
+    const int slot = k % kRing;
+    if (!warp_wait(&c.cfull[slot], (uint32_t)((k / kRing) & 1))) return false;
+    d = c.chunk[slot];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&c.cempty[slot]);
+    return true;
+}
+
 template <typename TK>
 __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
     const __grid_constant__ CUtensorMap kmap, const void* __restrict__ q, int q_dtype,
-    const float* __restrict__ w, Geom g, float* __restrict__ scores, int64_t score_row_stride) {
+    const float* __restrict__ w, Geom g, float* __restrict__ scores, int64_t score_row_stride, int sched_slot) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* tiles = smem;                                   // kStages x 32 KB, 1024-aligned
-    uint8_t* qbuf = smem + (size_t)kStages * kTileBytes;     // 2 x 16 KB, 1024-aligned
-    Ctl& c = *reinterpret_cast<Ctl*>(qbuf + 2 * kQBytes);
+    uint8_t* qbuf = smem + (size_t)kStages * kTileBytes;     // kQBufs x 16 KB, 1024-aligned
+    Ctl& c = *reinterpret_cast<Ctl*>(qbuf + kQBufs * kQBytes);
+    int* pre = reinterpret_cast<int*>(&c + 1);               // [n_rows + 1] in prefix mode
+    int* nvis = pre + kMaxPrefixRows + 1;                    // [n_rows] in prefix mode
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n_rows = (int64_t)g.B * g.T;
+    const bool prefix = n_rows <= kMaxPrefixRows;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -127,28 +220,46 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
             mbar_init(&c.tfull[i], 1);
             mbar_init(&c.tempty[i], 4);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kQBufs; ++i) {
             mbar_init(&c.qfull[i], 1);
             mbar_init(&c.qempty[i], 1);
+        }
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(&c.cfull[i], 1);
+            mbar_init(&c.cempty[i], kChunkReaders);
         }
         mbar_init(&c.done, 1);
         c.abort = 0;
         fence_mbar_init();
-        // this CTA's share of the flat tile list
-        int64_t total = 0;
-        for (int64_t r = 0; r < n_rows; ++r) total += row_tiles(row_n_vis(g, r));
-        const int64_t b0 = (int64_t)blockIdx.x * total / gridDim.x;
-        const int64_t b1 = (int64_t)(blockIdx.x + 1) * total / gridDim.x;
-        int64_t acc = 0, r = 0;
-        while (r < n_rows) {
-            const int nt = row_tiles(row_n_vis(g, r));
-            if (acc + nt > b0) break;
-            acc += nt;
-            ++r;
+    }
+    // chunks per row, then their prefix (all threads read the rows' bounds in parallel)
+    if (prefix) {
+        for (int64_t r = threadIdx.x; r < n_rows; r += kThreads) {
+            const int nv = row_n_vis(g, r);
+            nvis[r] = nv;
+            pre[r + 1] = row_chunks(nv);
         }
-        c.r_begin = r;
-        c.t_begin = (int)(b0 - acc);
-        c.count = b1 - b0;
+        __syncthreads();
+        if (warp == 0) {
+            int carry = 0;
+            for (int base = 0; base < (int)n_rows; base += 32) {
+                const int i = base + lane;
+                int v = i < n_rows ? pre[i + 1] : 0;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int u = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += u;
+                }
+                if (i < n_rows) pre[i + 1] = carry + v;
+                carry += __shfl_sync(0xffffffffu, v, 31);
+            }
+            if (lane == 0) {
+                pre[0] = 0;
+                c.n_chunks = carry;
+            }
+        }
+    } else if (threadIdx.x == 0) {
+        c.n_chunks = (int)n_rows;
     }
     if (warp == 0 && lane == 0) tma_prefetch_desc(&kmap);
     if (warp == 1) {
@@ -159,165 +270,197 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = c.tmem_base;
-    const int64_t count = c.count;
+    const int n_chunks = c.n_chunks;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        TileCursor cur;
-        cur.start(g, c.r_begin, c.t_begin, n_rows);
-        int stage = 0;
-        uint32_t phase = 0;
-        int64_t seg = -1;
-        int64_t issued = 0;
-        for (int64_t i = 0; i < count; ++i) {
-            if (warp_aborted(c)) break;
-            if (i == 0 || cur.t == 0) {
-                // new query row: stage its q (converted, swizzled) as the MMA B operand
-                ++seg;
-                const int qb = (int)(seg & 1);
-                const uint32_t qph = (uint32_t)((seg >> 1) & 1);
-                if (!warp_wait(&c.qempty[qb], qph ^ 1)) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            // the next chunk is claimed one chunk ahead, so the counter's round
+            // trip overlaps the current chunk's loads
+            int ch = (int)atomicAdd(&g_score_sched[sched_slot][0], 1u);
+            for (int k = 0;; ++k) {
+                const int slot = k % kRing;
+                if (*(volatile int*)&c.abort || !mbar_wait(&c.cempty[slot], (uint32_t)(((k / kRing) & 1) ^ 1))) {
                     abort_cta(c, g);
                     break;
                 }
-                uint8_t* qdst = qbuf + qb * kQBytes;
-                const int64_t qrow = cur.r * (int64_t)kH * kD;
-                for (int ch = lane; ch < kH * kD / 8; ch += 32) {
-                    const int h = ch >> 4, cc = ch & 15;
-                    const int half = cc >> 3, c8 = cc & 7;
-                    TK vals[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) vals[e] = from_f32<TK>(load_any(q, qrow + h * kD + cc * 8 + e, q_dtype));
-                    uint8_t* dst = qdst + half * kQHalfBytes + h * 128 + ((c8 ^ (h & 7)) << 4);
-                    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(vals);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&c.qfull[qb]);
-            }
-            if (lane == 0) {
-                if (!mbar_wait(&c.empty[stage], phase ^ 1)) {
-                    abort_cta(c, g);
-                } else {
-                    const int64_t krow = seq_row0(g, (int)(cur.r / g.T)) + (int64_t)cur.t * kTileKeys;
+                const Chunk d = chunk_of(g, pre, nvis, n_rows, prefix, ch, n_chunks);
+                c.chunk[slot] = d;
+                mbar_arrive(&c.cfull[slot]);
+                if (d.row < 0) break;
+                ch = (int)atomicAdd(&g_score_sched[sched_slot][0], 1u);
+                const int64_t krow0 = seq_row0(g, (int)(d.row / g.T));
+                bool ok = true;
+                for (int t = d.t0; t < d.t1; ++t) {
+                    if (!mbar_wait(&c.empty[stage], phase ^ 1)) {
+                        abort_cta(c, g);
+                        ok = false;
+                        break;
+                    }
+                    const int64_t krow = krow0 + (int64_t)t * kTileKeys;
                     uint8_t* dst = tiles + (size_t)stage * kTileBytes;
                     mbar_arrive_expect_tx(&c.full[stage], kTileBytes);
                     tma_load_2d(dst, &kmap, &c.full[stage], 0, (int32_t)krow);
                     tma_load_2d(dst + kHalfBytes, &kmap, &c.full[stage], 64, (int32_t)krow);
                     ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
                 }
+                if (!ok) break;
             }
-            if (warp_aborted(c)) break;
-            if (++stage == kStages) {
-                stage = 0;
-                phase ^= 1;
-            }
-            cur.next(g, n_rows);
-        }
-        // never leave the CTA with TMA writes in flight
-        if (lane == 0) {
+            // never leave the CTA with TMA writes in flight
             const int64_t n = issued < kStages ? issued : kStages;
             for (int64_t i = issued - n; i < issued; ++i)
                 mbar_wait(&c.full[i % kStages], (uint32_t)((i / kStages) & 1));
         }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_f16_f32(kTileKeys, kH, kIsBF16<TK> ? 1 : 0);
-            TileCursor cur;
-            cur.start(g, c.r_begin, c.t_begin, n_rows);
             int stage = 0, acc = 0;
             uint32_t phase = 0, aphase = 0;
-            int64_t seg = -1;
-            for (int64_t i = 0; i < count; ++i) {
-                if (*(volatile int*)&c.abort) break;
-                if (i == 0 || cur.t == 0) {
-                    ++seg;
-                    if (!mbar_wait(&c.qfull[seg & 1], (uint32_t)((seg >> 1) & 1))) {
-                        abort_cta(c, g);
-                        break;
-                    }
-                }
-                if (!mbar_wait(&c.tempty[acc], aphase ^ 1) || !mbar_wait(&c.full[stage], phase)) {
+            int64_t qseq = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int slot = k % kRing;
+                if (*(volatile int*)&c.abort || !mbar_wait(&c.cfull[slot], (uint32_t)((k / kRing) & 1))) {
                     abort_cta(c, g);
                     break;
                 }
-                tc_fence_after();
-                const uint32_t a0 = smem_u32(tiles + (size_t)stage * kTileBytes);
-                const uint32_t b0 = smem_u32(qbuf + (seg & 1) * kQBytes);
-                const uint32_t d = tmem + acc * kH;
+                const Chunk d = c.chunk[slot];
+                mbar_arrive(&c.cempty[slot]);
+                if (d.row < 0) break;
+                if (d.t1 <= d.t0) continue;
+                const int qb = (int)(qseq % kQBufs);
+                if (!mbar_wait(&c.qfull[qb], (uint32_t)((qseq / kQBufs) & 1))) {
+                    abort_cta(c, g);
+                    break;
+                }
+                const uint32_t b0 = smem_u32(qbuf + qb * kQBytes);
+                for (int t = d.t0; t < d.t1; ++t) {
+                    if (!mbar_wait(&c.tempty[acc], aphase ^ 1) || !mbar_wait(&c.full[stage], phase)) {
+                        abort_cta(c, g);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(tiles + (size_t)stage * kTileBytes);
+                    const uint32_t dt = tmem + acc * kH;
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;   // K offset inside the 128-byte row
-                    const uint64_t ad = desc_sw128_kmajor(a0 + (kk >> 2) * kHalfBytes + off, 1024);
-                    const uint64_t bd = desc_sw128_kmajor(b0 + (kk >> 2) * kQHalfBytes + off, 1024);
-                    mma_f16_ss(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t off = (kk & 3) * 32;   // K offset inside the 128-byte row
+                        const uint64_t ad = desc_sw128_kmajor(a0 + (kk >> 2) * kHalfBytes + off, 1024);
+                        const uint64_t bd = desc_sw128_kmajor(b0 + (kk >> 2) * kQHalfBytes + off, 1024);
+                        mma_f16_ss(dt, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&c.empty[stage]);
+                    mma_commit(&c.tfull[acc]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                    if (++acc == kAcc) {
+                        acc = 0;
+                        aphase ^= 1;
+                    }
                 }
-                mma_commit(&c.empty[stage]);
-                mma_commit(&c.tfull[acc]);
-                const bool last_of_row = (cur.t == cur.n_tiles - 1) || (i == count - 1);
-                if (last_of_row) mma_commit(&c.qempty[seg & 1]);
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-                if (++acc == kAcc) {
-                    acc = 0;
-                    aphase ^= 1;
-                }
-                cur.next(g, n_rows);
+                mma_commit(&c.qempty[qb]);
+                ++qseq;
             }
             // every MMA issued by this thread has completed before TMEM is freed
             mma_commit(&c.done);
             mbar_wait(&c.done, 0);
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------ epilogue
-        const int quad = warp & 3;                 // TMEM lane quarter this warp may access
-        TileCursor cur;
-        cur.start(g, c.r_begin, c.t_begin, n_rows);
-        int acc = 0;
-        uint32_t aphase = 0;
-        float wv[kH];
-        for (int64_t i = 0; i < count; ++i) {
-            if (warp_aborted(c)) break;
-            if (i == 0 || cur.t == 0) {
-                const float4* wr = reinterpret_cast<const float4*>(w + cur.r * kH);
-#pragma unroll
-                for (int h4 = 0; h4 < kH / 4; ++h4) {
-                    const float4 x = wr[h4];
-                    wv[4 * h4] = x.x;
-                    wv[4 * h4 + 1] = x.y;
-                    wv[4 * h4 + 2] = x.z;
-                    wv[4 * h4 + 3] = x.w;
-                }
-            }
-            if (!warp_wait(&c.tfull[acc], aphase)) {
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ q stager
+        int64_t qseq = 0;
+        for (int k = 0;; ++k) {
+            Chunk d;
+            if (warp_aborted(c) || !warp_next_chunk(c, k, d)) {
                 abort_cta(c, g);
                 break;
             }
-            tc_fence_after();
-            float v0[32], v1[32];
-            const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + acc * kH;
-            tmem_ld_32x32b_x32(ta, v0);
-            tmem_ld_32x32b_x32(ta + 32, v1);
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&c.tempty[acc]);
-            float s = 0.f;
-#pragma unroll
-            for (int h = 0; h < 32; ++h) s = fmaf(wv[h], fmaxf(v0[h], 0.f), s);
-#pragma unroll
-            for (int h = 0; h < 32; ++h) s = fmaf(wv[32 + h], fmaxf(v1[h], 0.f), s);
-            const int j = cur.t * kTileKeys + quad * 32 + lane;
-            if (j < cur.n_keys) scores[cur.r * score_row_stride + j] = s + 0.0f;
-            if (++acc == kAcc) {
-                acc = 0;
-                aphase ^= 1;
+            if (d.row < 0) break;
+            if (d.t1 <= d.t0) continue;
+            const int qb = (int)(qseq % kQBufs);
+            if (!warp_wait(&c.qempty[qb], (uint32_t)(((qseq / kQBufs) & 1) ^ 1))) {
+                abort_cta(c, g);
+                break;
             }
-            cur.next(g, n_rows);
+            uint8_t* qdst = qbuf + qb * kQBytes;
+            const int64_t off = d.row * (int64_t)kH * kD;
+            if (q_dtype == IDX_F32) stage_q_row<TK>(static_cast<const float*>(q) + off, qdst, lane);
+            else if (q_dtype == IDX_BF16) stage_q_row<TK>(static_cast<const __nv_bfloat16*>(q) + off, qdst, lane);
+            else stage_q_row<TK>(static_cast<const __half*>(q) + off, qdst, lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c.qfull[qb]);
+            ++qseq;
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quad = warp & 3;                 // TMEM lane quarter this warp may access
+        int acc = 0;
+        uint32_t aphase = 0;
+        float wv[kH];
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            Chunk d;
+            if (warp_aborted(c) || !warp_next_chunk(c, k, d)) {
+                abort_cta(c, g);
+                break;
+            }
+            if (d.row < 0) break;
+            if (d.t1 <= d.t0) continue;
+            const int n_keys = prefix ? nvis[d.row] : row_n_vis(g, d.row);
+            const float4* wr = reinterpret_cast<const float4*>(w + d.row * kH);
+#pragma unroll
+            for (int h4 = 0; h4 < kH / 4; ++h4) {
+                const float4 x = wr[h4];
+                wv[4 * h4] = x.x;
+                wv[4 * h4 + 1] = x.y;
+                wv[4 * h4 + 2] = x.z;
+                wv[4 * h4 + 3] = x.w;
+            }
+            for (int t = d.t0; t < d.t1; ++t) {
+                if (!warp_wait(&c.tfull[acc], aphase)) {
+                    abort_cta(c, g);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float v0[32], v1[32];
+                const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + acc * kH;
+                tmem_ld_32x32b_x32(ta, v0);
+                tmem_ld_32x32b_x32(ta + 32, v1);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c.tempty[acc]);
+                // four partial sums (a shorter dependent chain); the sum order is fixed
+                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                for (int h = 0; h < 32; h += 2) {
+                    s0 = fmaf(wv[h], fmaxf(v0[h], 0.f), s0);
+                    s1 = fmaf(wv[h + 1], fmaxf(v0[h + 1], 0.f), s1);
+                    s2 = fmaf(wv[32 + h], fmaxf(v1[h], 0.f), s2);
+                    s3 = fmaf(wv[33 + h], fmaxf(v1[h + 1], 0.f), s3);
+                }
+                const float s = (s0 + s1) + (s2 + s3);
+                const int j = t * kTileKeys + quad * 32 + lane;
+                if (j < n_keys) scores[d.row * score_row_stride + j] = s + 0.0f;
+                if (++acc == kAcc) {
+                    acc = 0;
+                    aphase ^= 1;
+                }
+            }
         }
     }
 
@@ -325,6 +468,15 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    // the last CTA to finish returns the slot's counters to zero for a later launch
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&g_score_sched[sched_slot][1], 1u) == gridDim.x - 1) {
+            atomicExch(&g_score_sched[sched_slot][0], 0u);
+            atomicExch(&g_score_sched[sched_slot][1], 0u);
+            __threadfence();
+        }
+    }
 }
 
 }  // namespace
@@ -683,24 +835,27 @@ cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, i
     }
     if (g.T != 1) return cudaErrorNotSupported;
     if ((reinterpret_cast<uintptr_t>(k) & 15u) || (k_row_stride % 8) || k_rows < 1 || k_rows > INT32_MAX ||
-        (reinterpret_cast<uintptr_t>(w) & 15u))
+        (reinterpret_cast<uintptr_t>(w) & 15u) || (reinterpret_cast<uintptr_t>(q) & 15u))
         return cudaErrorNotSupported;
     const int64_t n_rows = (int64_t)g.B * g.T;
     if (n_rows == 0 || g.max_n_kv == 0) return cudaSuccess;
     CUtensorMap map;
     const bool bf16 = k_dtype == IDX_BF16;
     if (!make_key_tmap(&map, k, bf16, k_row_stride, k_rows, kTileKeys)) return cudaErrorNotSupported;
-    const int64_t max_tiles = n_rows * ((g.max_n_kv + kTileKeys - 1) / kTileKeys);
-    const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
-    if (bf16) {
-        auto kern = score_tc_decode_kernel<__nv_bfloat16>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        kern<<<grid, kThreads, kSmemBytes, st>>>(map, q, q_dtype, w, g, scores, score_row_stride);
-    } else {
-        auto kern = score_tc_decode_kernel<__half>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        kern<<<grid, kThreads, kSmemBytes, st>>>(map, q, q_dtype, w, g, scores, score_row_stride);
-    }
+    // chunks are numbered in 32 bits
+    const int64_t chunks_per_row = ((g.max_n_kv + kTileKeys - 1) / kTileKeys + kChunkTiles - 1) / kChunkTiles;
+    const int64_t max_chunks = n_rows <= kMaxPrefixRows ? n_rows * chunks_per_row : n_rows;
+    if (max_chunks >= INT32_MAX - 2 * (int64_t)sm_count()) return cudaErrorNotSupported;
+    const int grid = (int)(max_chunks < sm_count() ? max_chunks : sm_count());
+    // one counter slot per launch, round-robin (a slot is reused only after
+    // kSchedSlots further launches; its previous launch has zeroed it by then
+    // unless that many launches are in flight at once)
+    static std::atomic<unsigned> next_slot{0};
+    const int slot = (int)(next_slot.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots);
+    auto kern = bf16 ? score_tc_decode_kernel<__nv_bfloat16> : score_tc_decode_kernel<__half>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, kSmemBytes, st>>>(map, q, q_dtype, w, g, scores, score_row_stride, slot);
     return cudaGetLastError();
 }
 

@@ -297,6 +297,50 @@ def test_score_tensor_core_one_short_row_many_idle_ctas():
     assert_scores_close(s[0].cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("B", [2047, 2500])
+def test_score_tensor_core_decode_many_rows(B):
+    # more rows than the scheduler's shared-memory prefix holds (2500: one chunk per row)
+    # and just under it (2047: chunks of 8 tiles); ragged n_kv with empty rows, one shared cache
+    g = torch.Generator(device=DEV).manual_seed(76)
+    gc = torch.Generator().manual_seed(77)
+    n_kv = torch.randint(0, 3000, (B,), generator=gc)
+    n_kv[::97] = 0
+    n_kv[5] = 2048 + 1
+    max_n = int(n_kv.max())
+    q = torch.randn(B, 64, 128, generator=g, device=DEV).to(torch.bfloat16)
+    w = torch.randn(B, 64, generator=g, device=DEV) / 8
+    k = torch.randn(max_n, 128, generator=g, device=DEV).to(torch.float16)
+    batch = L.Batch(_i32(n_kv.tolist()), 1, max_n, kv_seq_stride=0)
+    s = torch.full((B, max_n), 321.0, device=DEV)
+    L.idx_score(q, w, k, batch, scores=s)
+    torch.cuda.synchronize()
+    kh = np64(k)
+    for b in [0, 1, 5, 97, 1000, B - 2, B - 1] + list(range(3, B, 211)):
+        n = int(n_kv[b])
+        got = s[b].cpu().numpy()
+        if n:
+            ref = O.indexer_scores(np64(q[b]), np64(w[b]), kh[:n])
+            assert_scores_close(got[:n], ref, f"row {b}")
+        assert np.all(got[n:] == 321.0), b
+
+
+def test_score_tensor_core_decode_back_to_back_launches():
+    # the chunk counter of each launch returns to zero: many launches in a row give identical scores
+    g = torch.Generator(device=DEV).manual_seed(78)
+    B, n = 16, 20000
+    q = torch.randn(B, 64, 128, generator=g, device=DEV).to(torch.bfloat16)
+    w = torch.randn(B, 64, generator=g, device=DEV) / 8
+    k = torch.randn(B * n, 128, generator=g, device=DEV).to(torch.float16)
+    batch = L.Batch(_i32([n] * B), 1, n, kv_seq_stride=n)
+    first = L.idx_score(q, w, k, batch).clone()
+    for _ in range(1100):
+        s = L.idx_score(q, w, k, batch)
+    torch.cuda.synchronize()
+    assert torch.equal(first, s)
+    ref = O.indexer_scores(np64(q[3]), np64(w[3]), np64(k[3 * n:4 * n]))
+    assert_scores_close(first[3].cpu().numpy(), ref)
+
+
 # ------------------------------------------------------------------ MLA attention on the tensor cores
 
 def _mla_case(seed, B, n_kv, sizes, q_scale=1.0, sorted_sel=False):
