@@ -48,6 +48,7 @@ WORKLOADS = {
     "decode_mla_8x8192": ((2,), {}),
     "decode_mla_64x8192": (("headline",), {"n_kv_override": 8192}),
     "long_decode_mla_ragged": ((5,), {}),
+    "decode_mla_64x131072_q8": (("headline",), {"quantized_keys": True}),
     "prefill_mla_16384": ((3,), {}),
     "prefill_mla_4096": ((3,), {"n_tokens_override": 4096}),
 }
@@ -170,8 +171,12 @@ def cpu_oracle_queries(wl, rows):
     inputs = []
     for r in rows:
         row0, n = wl.row0(r), wl.n_kv_host[r]
+        if wl.k8 is not None:   # the quantized cache as it represents the keys
+            keys = O.dequantize_rows(wl.k8[row0:row0 + n].cpu().numpy(), wl.k_scale[row0:row0 + n].cpu().numpy())
+        else:
+            keys = wl.k_idx[row0:row0 + n].to("cpu", torch.float64).numpy()
         inputs.append((r, wl.q_idx[r].to("cpu", torch.float64).numpy(), wl.w[r].to("cpu", torch.float64).numpy(),
-                       wl.k_idx[row0:row0 + n].to("cpu", torch.float64).numpy(),
+                       keys,
                        wl.q_attn[r].to("cpu", torch.float64).numpy(),
                        wl.k_attn[row0:row0 + n].to("cpu", torch.float64).numpy(), n))
     t0 = time.perf_counter()
@@ -358,13 +363,15 @@ def main():
                     "algorithmic_flops_per_launch": flops}
     else:
         n_kv_total = sum(wl.n_kv_host)
-        key_bytes = n_kv_total * wl.d * 2
+        # bytes of one cached key: 2 per element (F16), or 1 per element + a 4-byte scale (int8 cache)
+        key_bytes = n_kv_total * (wl.d * 2 if wl.k8 is None else wl.d + 4)
         # scorer's algorithmic bytes per launch: every key row read once, one f32 score written per
         # key, the queries and weights read once
         score_bytes = key_bytes + n_kv_total * 4 + B * wl.H * wl.d * 2 + B * wl.H * 4
         achieved = score_bytes / (ms_score * 1e-3) / 1e9
-        per_key = NCU_TRAFFIC.get(_sha(src))
-        roofline = {"bound": "hbm", "kernel": "idx_score (key-cache scan)", "achieved": achieved, "peak": hbm,
+        per_key = NCU_TRAFFIC.get(_sha(src)) if wl.k8 is None else None
+        roofline = {"bound": "hbm", "kernel": "idx_score (key-cache scan)" if wl.k8 is None else
+                    "idx_score_q8 (int8 key-cache scan)", "achieved": achieved, "peak": hbm,
                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
                     "traffic": per_key * n_kv_total if per_key is not None else None,
                     "algorithmic_bytes_per_launch": score_bytes}
@@ -376,8 +383,9 @@ def main():
         "vs_baseline": None, "dtype": "f16/bf16 (f32 accumulate)",
         "data": "synthetic (seeded N(0,1) q/k/latent, w ~ N(0,1/64))",
         "config": {"workload": args.workload, "queries_per_gpu": B, "n_kv": max(wl.n_kv_host), "top_k": wl.top_k,
-                   "indexer": "%d heads x %d, %s cache%s" % (wl.H, wl.d, str(wl.k_idx.dtype).replace("torch.", ""),
-                                                                ", Hadamard" if wl.hadamard else ""),
+                   "indexer": "%d heads x %d, %s cache%s" % (
+                       wl.H, wl.d, "int8 + f32 row scale" if wl.k8 is not None else
+                       str(wl.k_idx.dtype).replace("torch.", ""), ", Hadamard" if wl.hadamard else ""),
                    "attention": "MLA 128 heads, 576/512 bf16",
                    "l2": "inputs larger than L2 (key cache %.2f GB, latent %.2f GB), no flush"
                          % (wl.k_idx.numel() * 2 / 1e9, wl.k_attn.numel() * 2 / 1e9)},

@@ -132,6 +132,44 @@ idx_status idx_score(const void* q, idx_dtype q_dtype, const float* w, int32_t n
                      idx_stream_t stream);
 
 /*
+ * idx_quantize_rows -- per-row symmetric 8-bit code of a key cache row, the
+ * storage format of a quantized indexer key cache ("GLM-DSA: allow for
+ * quantized indexer cache", ik_llama_opt commit log; like the q8_0 latent
+ * cache there, "a storage format only": scores use the dequantized values).
+ * For each row r, in f32 arithmetic (round to nearest even):
+ *     scale[r] = max_c |x[r, c]| / 127
+ *     q8[r, c] = clamp(rint(x[r, c] / scale[r]), -127, 127)   (0 when scale = 0)
+ * so x ~= scale[r] * q8[r, c] with |error| <= scale/2.
+ *   x          device [n_rows] rows of d elements at x + r*x_row_stride, x_dtype.
+ *   q8         device int8, row r at q8 + r*q8_row_stride (bytes).
+ *   scale      device f32 [n_rows].
+ * Errors: INVALID_ARG for NULL pointers with n_rows > 0, d < 1 or d > 1024,
+ * strides < d, or q8 / q8_row_stride not 16-byte aligned.
+ */
+idx_status idx_quantize_rows(const void* x, idx_dtype x_dtype, int64_t n_rows, int32_t d, int64_t x_row_stride,
+                             int8_t* q8, int64_t q8_row_stride, float* scale, idx_stream_t stream);
+
+/*
+ * idx_score_q8 -- idx_score over a quantized key cache (idx_quantize_rows):
+ *     s[r, j] = sum_h w[r, h] * max(0, q[r, h, :] . (scale[j] * k8[j, :]))
+ * i.e. the indexer score of the dequantized keys (ik_llama_opt commit log,
+ * "GLM-DSA: allow for quantized indexer cache"; the score itself as in
+ * idx_score).  A key row costs d + 4 bytes instead of 2d.
+ *   k8         device int8 key rows, row i at k8 + i*k_row_stride (bytes).
+ *   k_scale    device f32, k_scale[i] for cache row i (any sign).
+ *   other arguments as idx_score (block_size 0/1 only).
+ * H = 64, d = 128 decode rows (T = 1) with f16 or bf16 q run on the tensor
+ * cores: the int8 codes are widened exactly to f16 in shared memory, q is
+ * converted to f16 (exact for bf16 q inside f16's normal range), and the
+ * scale is applied per head before the ReLU.  Everything else runs on the
+ * CUDA cores.
+ */
+idx_status idx_score_q8(const void* q, idx_dtype q_dtype, const float* w, int32_t n_heads, int32_t head_dim,
+                        const int8_t* k8, int64_t k_row_stride, const float* k_scale, int64_t k_rows,
+                        idx_batch batch, int32_t block_size, float* scores, int64_t score_row_stride,
+                        void* workspace, size_t workspace_bytes, idx_stream_t stream);
+
+/*
  * idx_block_pool -- mean-pooled raw key of every complete block
  *     p[b, beta, :] = (1/C) * sum_{t=beta*C}^{beta*C+C-1} k_raw[row(b, t), :]
  * for beta < floor(n_kv[b] / C).  Blocks are cuts of the position line from
@@ -146,6 +184,32 @@ idx_status idx_score(const void* q, idx_dtype q_dtype, const float* w, int32_t n
 idx_status idx_block_pool(const void* k_raw, idx_dtype k_dtype, int64_t k_row_stride,
                           int64_t k_rows, idx_batch batch, int32_t block_size, int32_t head_dim,
                           float* pooled, int64_t pool_seq_stride, idx_stream_t stream);
+
+/*
+ * idx_block_pool_update -- incremental maintenance of a persistent pooled-key
+ * cache: only the blocks that changed are (re)pooled.  The pooled keys live
+ * across decode steps; a step appends tokens, so only blocks completed since
+ * the last pooling are new, and a sequence edit from position p on regroups
+ * the blocks from the one holding p, staling every pooled key at or after it
+ * (llama-memory-hybrid-idx.h: "The pooled keys persist in the idx cache
+ * across batches", mem_idx_stale / POS_CLEAN, get_n_kpool_new "pools to
+ * re-pool this ubatch").  For sequence b, with n_cb = floor(n_kv[b]/C):
+ *     beta0 = min(n_pooled[b], floor(stale_pos[b] / C))   clamped to [0, n_cb]
+ * and the blocks beta0 <= beta < n_cb are written exactly as idx_block_pool
+ * writes them; every other pooled row is left untouched.
+ *   n_pooled   device int32 [n_seq] or NULL (= 0): complete blocks of sequence
+ *              b whose pooled keys are current.  The caller keeps this count
+ *              (after the call it is n_cb); the library does not write it.
+ *   stale_pos  device int32 [n_seq] or NULL (= no edit): first position whose
+ *              raw key changed since those blocks were pooled; IDX_POS_CLEAN
+ *              means none, a negative value the whole sequence.
+ * Other arguments and errors as idx_block_pool.
+ */
+#define IDX_POS_CLEAN INT32_MAX
+idx_status idx_block_pool_update(const void* k_raw, idx_dtype k_dtype, int64_t k_row_stride,
+                                 int64_t k_rows, idx_batch batch, const int32_t* n_pooled,
+                                 const int32_t* stale_pos, int32_t block_size, int32_t head_dim,
+                                 float* pooled, int64_t pool_seq_stride, idx_stream_t stream);
 
 /*
  * idx_topk -- per-row selection, positions ascending.

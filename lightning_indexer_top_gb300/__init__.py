@@ -22,13 +22,15 @@ from ._build import LIB as _LIB_PATH
 from ._build import build  # noqa: F401
 
 __all__ = [
-    "Batch", "LidxError", "build", "load", "idx_hadamard", "idx_score", "idx_block_pool",
+    "Batch", "LidxError", "build", "load", "idx_hadamard", "idx_score", "idx_block_pool", "idx_block_pool_update",
+    "idx_quantize_rows", "idx_score_q8",
     "idx_topk", "sparse_attn_decode", "sparse_attn_prefill", "idx_workspace_size",
     "idx_device_status", "topk_capacity", "sparse_attn_decode_noalloc",
 ]
 
 IDX_OK, IDX_ERR_INVALID_ARG, IDX_ERR_UNSUPPORTED, IDX_ERR_CUDA, IDX_ERR_TIMEOUT, IDX_ERR_DEVICE_BOUNDS = range(6)
 IDX_F32, IDX_F16, IDX_BF16 = 0, 1, 2
+IDX_POS_CLEAN = 2**31 - 1   # stale_pos value: no edit
 IDX_OP_SCORE, IDX_OP_TOPK, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL = 0, 1, 2, 3
 
 _DTYPES = {torch.float32: IDX_F32, torch.float16: IDX_F16, torch.bfloat16: IDX_BF16}
@@ -69,6 +71,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "idx_hadamard": [P, P, I32, I64, I32, I64, P],
         "idx_score": [P, I32, P, I32, I32, P, I32, I64, I64, _Batch, I32, P, I64, P, SZ, P],
         "idx_block_pool": [P, I32, I64, I64, _Batch, I32, I32, P, I64, P],
+        "idx_block_pool_update": [P, I32, I64, I64, _Batch, P, P, I32, I32, P, I64, P],
+        "idx_quantize_rows": [P, I32, I64, I32, I64, P, I64, P, P],
+        "idx_score_q8": [P, I32, P, I32, I32, P, I64, P, I64, _Batch, I32, P, I64, P, SZ, P],
         "idx_topk": [P, I64, _Batch, I32, I32, P, I64, P, P, SZ, P],
         "sparse_attn_decode": [P, I32, I32, I32, I32, I32, P, P, I64, I64, I64, _Batch, P, I64, P, F,
                                P, I32, P, SZ, P],
@@ -203,6 +208,54 @@ def idx_block_pool(k_raw: torch.Tensor, batch: Batch, block_size: int, *, pool_s
         pooled = torch.zeros(batch.n_seq, pool_seq_stride, d, device=k_raw.device, dtype=torch.float32)
     _check(load().idx_block_pool(_ptr(k_raw), _dtype(k_raw), k_raw.stride(0), k_raw.shape[0], batch.c(),
                                  block_size, d, _ptr(pooled), pool_seq_stride, _stream(k_raw.device)))
+    return pooled
+
+
+def idx_quantize_rows(x: torch.Tensor, *, q8: Optional[torch.Tensor] = None,
+                      scale: Optional[torch.Tensor] = None):
+    """Per-row int8 codes and f32 scales of key rows [n, d]: x ~= scale[:, None] * q8."""
+    _need_cuda(x, q8, scale)
+    n, d = x.shape[0], x.shape[-1]
+    if q8 is None:
+        q8 = torch.empty(n, (d + 15) // 16 * 16, device=x.device, dtype=torch.int8)[:, :d]
+    if scale is None:
+        scale = torch.empty(n, device=x.device, dtype=torch.float32)
+    _check(load().idx_quantize_rows(_ptr(x), _dtype(x), n, d, x.stride(0), _ptr(q8), q8.stride(0), _ptr(scale),
+                                    _stream(x.device)))
+    return q8, scale
+
+
+def idx_score_q8(q: torch.Tensor, w: torch.Tensor, k8: torch.Tensor, k_scale: torch.Tensor, batch: Batch, *,
+                 scores: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Indexer scores over an int8 key cache with per-row scales (f32 [rows, keys])."""
+    _need_cuda(q, w, k8, k_scale, scores)
+    H, d = q.shape[-2], q.shape[-1]
+    rows = batch.n_rows
+    if scores is None:
+        scores = torch.empty(rows, max(batch.max_n_kv, 1), device=q.device, dtype=torch.float32)
+    _check(load().idx_score_q8(_ptr(q), _dtype(q), _ptr(w), H, d, _ptr(k8), k8.stride(0), _ptr(k_scale),
+                               k8.shape[0], batch.c(), 0, _ptr(scores), scores.stride(0), None, 0,
+                               _stream(q.device)))
+    return scores
+
+
+def idx_block_pool_update(k_raw: torch.Tensor, batch: Batch, block_size: int, pooled: torch.Tensor, *,
+                          n_pooled: Optional[torch.Tensor] = None, stale_pos: Optional[torch.Tensor] = None,
+                          pool_seq_stride: Optional[int] = None) -> torch.Tensor:
+    """(Re)pool only the blocks from min(n_pooled[b], stale_pos[b] // C) on, in place in ``pooled``.
+
+    n_pooled / stale_pos: device int32 [n_seq] or None (0 / no edit); IDX_POS_CLEAN marks no edit.
+    """
+    _need_cuda(k_raw, pooled, n_pooled, stale_pos)
+    d = k_raw.shape[-1]
+    if pool_seq_stride is None:
+        pool_seq_stride = pooled.shape[1] if pooled.dim() == 3 else max(batch.max_n_kv // block_size, 1)
+    for t in (n_pooled, stale_pos):
+        if t is not None and (t.dtype != torch.int32 or t.numel() < batch.n_seq or not t.is_contiguous()):
+            raise ValueError("n_pooled / stale_pos must be contiguous int32 with one entry per sequence")
+    _check(load().idx_block_pool_update(_ptr(k_raw), _dtype(k_raw), k_raw.stride(0), k_raw.shape[0], batch.c(),
+                                        _ptr(n_pooled), _ptr(stale_pos), block_size, d, _ptr(pooled),
+                                        pool_seq_stride, _stream(k_raw.device)))
     return pooled
 
 

@@ -211,10 +211,61 @@ idx_status idx_score(const void* q, idx_dtype q_dtype, const float* w, int32_t n
     return from_cuda(e, what);
 }
 
-idx_status idx_block_pool(const void* k_raw, idx_dtype k_dtype, int64_t k_row_stride,
-                          int64_t k_rows, idx_batch batch, int32_t block_size, int32_t head_dim,
-                          float* pooled, int64_t pool_seq_stride, idx_stream_t stream) {
-    const char* what = "idx_block_pool";
+idx_status idx_quantize_rows(const void* x, idx_dtype x_dtype, int64_t n_rows, int32_t d, int64_t x_row_stride,
+                             int8_t* q8, int64_t q8_row_stride, float* scale, idx_stream_t stream) {
+    const char* what = "idx_quantize_rows";
+    if (!valid_dtype(x_dtype)) return fail(IDX_ERR_INVALID_ARG, "%s: bad dtype", what);
+    if (n_rows < 0) return fail(IDX_ERR_INVALID_ARG, "%s: n_rows < 0", what);
+    if (d < 1 || d > 1024) return fail(IDX_ERR_INVALID_ARG, "%s: d must be in [1, 1024]", what);
+    if (x_row_stride < d || q8_row_stride < d) return fail(IDX_ERR_INVALID_ARG, "%s: row stride < d", what);
+    if (n_rows == 0) return IDX_OK;
+    if (!x || !q8 || !scale) return fail(IDX_ERR_INVALID_ARG, "%s: NULL x/q8/scale", what);
+    if (!aligned16(q8) || q8_row_stride % 16 != 0)
+        return fail(IDX_ERR_INVALID_ARG, "%s: q8 / q8_row_stride not 16-byte aligned", what);
+    return from_cuda(launch_quantize_rows(x, x_dtype, n_rows, d, x_row_stride, q8, q8_row_stride, scale,
+                                          (cudaStream_t)stream),
+                     what);
+}
+
+idx_status idx_score_q8(const void* q, idx_dtype q_dtype, const float* w, int32_t n_heads, int32_t head_dim,
+                        const int8_t* k8, int64_t k_row_stride, const float* k_scale, int64_t k_rows,
+                        idx_batch batch, int32_t block_size, float* scores, int64_t score_row_stride,
+                        void* workspace, size_t workspace_bytes, idx_stream_t stream) {
+    const char* what = "idx_score_q8";
+    (void)workspace;
+    (void)workspace_bytes;
+    idx_status s = check_batch(batch, what);
+    if (s != IDX_OK) return s;
+    if (!valid_dtype(q_dtype)) return fail(IDX_ERR_INVALID_ARG, "%s: bad dtype", what);
+    if (n_heads < 1 || n_heads > 64)
+        return fail(IDX_ERR_UNSUPPORTED, "%s: n_heads must be in [1, 64]", what);
+    if (head_dim < 1 || head_dim > 256)
+        return fail(IDX_ERR_UNSUPPORTED, "%s: head_dim must be in [1, 256]", what);
+    if (block_size < 0 || block_size > 1)
+        return fail(IDX_ERR_UNSUPPORTED, "%s: token keys only (block_size 0 or 1)", what);
+    if (k_row_stride < head_dim) return fail(IDX_ERR_INVALID_ARG, "%s: k_row_stride < head_dim", what);
+    if (k_rows < 0) return fail(IDX_ERR_INVALID_ARG, "%s: k_rows < 0", what);
+    if (score_row_stride < batch.max_n_kv)
+        return fail(IDX_ERR_INVALID_ARG, "%s: score_row_stride < keys per row", what);
+    const int64_t rows = (int64_t)batch.n_seq * batch.n_q_per_seq;
+    if (rows == 0 || batch.max_n_kv == 0) return IDX_OK;
+    if (!q || !w || !k8 || !k_scale || !scores)
+        return fail(IDX_ERR_INVALID_ARG, "%s: NULL q/w/k8/k_scale/scores", what);
+    const Geom g = make_geom(batch);
+    const cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaErrorNotSupported;
+    if (n_heads == 64 && head_dim == 128)
+        e = launch_score_tc_q8(q, q_dtype, w, k8, k_row_stride, k_scale, k_rows, g, scores, score_row_stride, st);
+    if (e == cudaErrorNotSupported)
+        e = launch_score_generic(q, q_dtype, w, n_heads, head_dim, k8, IDX_I8_ROWSCALE, k_row_stride, k_rows, g, 0,
+                                 scores, score_row_stride, st, k_scale);
+    return from_cuda(e, what);
+}
+
+static idx_status block_pool_common(const char* what, const void* k_raw, idx_dtype k_dtype, int64_t k_row_stride,
+                                    int64_t k_rows, idx_batch batch, const int32_t* n_pooled,
+                                    const int32_t* stale_pos, int32_t block_size, int32_t head_dim, float* pooled,
+                                    int64_t pool_seq_stride, idx_stream_t stream) {
     idx_status s = check_batch(batch, what);
     if (s != IDX_OK) return s;
     if (!valid_dtype(k_dtype)) return fail(IDX_ERR_INVALID_ARG, "%s: bad dtype", what);
@@ -231,9 +282,24 @@ idx_status idx_block_pool(const void* k_raw, idx_dtype k_dtype, int64_t k_row_st
     if (!k_raw || !pooled) return fail(IDX_ERR_INVALID_ARG, "%s: NULL k_raw/pooled", what);
     if (!aligned16(k_raw)) return fail(IDX_ERR_INVALID_ARG, "%s: k_raw not 16-byte aligned", what);
     const Geom g = make_geom(batch);
-    return from_cuda(launch_block_pool(k_raw, k_dtype, k_row_stride, k_rows, g, block_size, head_dim,
-                                       pooled, pool_seq_stride, (cudaStream_t)stream),
+    return from_cuda(launch_block_pool(k_raw, k_dtype, k_row_stride, k_rows, g, block_size, head_dim, pooled,
+                                       pool_seq_stride, n_pooled, stale_pos, (cudaStream_t)stream),
                      what);
+}
+
+idx_status idx_block_pool(const void* k_raw, idx_dtype k_dtype, int64_t k_row_stride,
+                          int64_t k_rows, idx_batch batch, int32_t block_size, int32_t head_dim,
+                          float* pooled, int64_t pool_seq_stride, idx_stream_t stream) {
+    return block_pool_common("idx_block_pool", k_raw, k_dtype, k_row_stride, k_rows, batch, nullptr, nullptr,
+                             block_size, head_dim, pooled, pool_seq_stride, stream);
+}
+
+idx_status idx_block_pool_update(const void* k_raw, idx_dtype k_dtype, int64_t k_row_stride,
+                                 int64_t k_rows, idx_batch batch, const int32_t* n_pooled,
+                                 const int32_t* stale_pos, int32_t block_size, int32_t head_dim,
+                                 float* pooled, int64_t pool_seq_stride, idx_stream_t stream) {
+    return block_pool_common("idx_block_pool_update", k_raw, k_dtype, k_row_stride, k_rows, batch, n_pooled,
+                             stale_pos, block_size, head_dim, pooled, pool_seq_stride, stream);
 }
 
 idx_status idx_topk(const float* scores, int64_t score_row_stride, idx_batch batch, int32_t top_k,

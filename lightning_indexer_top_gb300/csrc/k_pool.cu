@@ -5,6 +5,11 @@
 // key is the raw key's mean, before any norm or rotation (llama.cpp commit
 // c88c916636, QSA commit message; llama-memory-hybrid-idx.h, kpool_layout).
 //
+// Incremental form: per sequence only blocks beta >= beta0 are written, with
+// beta0 = min(n_pooled[b], floor(stale_pos[b]/C)) (llama-memory-hybrid-idx.h:
+// pooled keys persist across batches; an edit stales every pool at or after
+// it), so a decode step re-pools only what changed.
+//
 // One CTA of 128 threads per (block, sequence).  With 16-byte vector loads a
 // row of d elements takes TPR = d*size/16 threads, so the CTA reads
 // RP = 128/TPR rows at once; each thread sums its rows in f32 and the RP
@@ -21,15 +26,25 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) pool_kernel(const T* __restrict__ k, int64_t k_row_stride,
                                                         int64_t k_rows, Geom g, int C, int d,
                                                         float* __restrict__ pooled,
-                                                        int64_t pool_seq_stride) {
+                                                        int64_t pool_seq_stride,
+                                                        const int32_t* __restrict__ n_pooled,
+                                                        const int32_t* __restrict__ stale_pos) {
     extern __shared__ float part[];  // [RP][d]
     const int b = blockIdx.y;
     const int n_cb = seq_n_kv(g, b) / C;
+    // first block to (re)pool: after the current ones, and from the stale one on
+    int beta0 = 0;
+    if (n_pooled) beta0 = max(n_pooled[b], 0);
+    if (stale_pos) {
+        const int sp = stale_pos[b];
+        beta0 = min(beta0, sp < 0 ? 0 : sp / C);
+    }
+    beta0 = min(beta0, n_cb);
     constexpr int V = 16 / sizeof(T);
     const int tpr = d / V;              // threads per row
     const int rp = kThreads / tpr;      // rows per pass
     const int64_t row0 = seq_row0(g, b);
-    for (int beta = blockIdx.x; beta < n_cb; beta += gridDim.x) {
+    for (int beta = beta0 + (int)blockIdx.x; beta < n_cb; beta += gridDim.x) {
         const int rg = threadIdx.x / tpr, cv = threadIdx.x % tpr;
         float acc[V];
 #pragma unroll
@@ -61,7 +76,8 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(const T* __restrict__ k,
 
 template <typename T>
 cudaError_t run(const T* k, int64_t k_row_stride, int64_t k_rows, const Geom& g, int C, int d,
-                float* pooled, int64_t pool_seq_stride, cudaStream_t st) {
+                float* pooled, int64_t pool_seq_stride, const int32_t* n_pooled, const int32_t* stale_pos,
+                cudaStream_t st) {
     const int max_blocks = g.max_n_kv / C;
     if (max_blocks == 0 || g.B == 0) return cudaSuccess;
     constexpr int V = 16 / sizeof(T);
@@ -70,7 +86,7 @@ cudaError_t run(const T* k, int64_t k_row_stride, int64_t k_rows, const Geom& g,
     const size_t sm = (size_t)rp * d * sizeof(float);
     dim3 grid((unsigned)(max_blocks < 65535 ? max_blocks : 65535), (unsigned)g.B);
     pool_kernel<T><<<grid, kThreads, sm, st>>>(k, k_row_stride, k_rows, g, C, d, pooled,
-                                               pool_seq_stride);
+                                               pool_seq_stride, n_pooled, stale_pos);
     return cudaGetLastError();
 }
 
@@ -78,17 +94,17 @@ cudaError_t run(const T* k, int64_t k_row_stride, int64_t k_rows, const Geom& g,
 
 cudaError_t launch_block_pool(const void* k_raw, int k_dtype, int64_t k_row_stride, int64_t k_rows,
                               const Geom& g, int C, int d, float* pooled, int64_t pool_seq_stride,
-                              cudaStream_t st) {
+                              const int32_t* n_pooled, const int32_t* stale_pos, cudaStream_t st) {
     switch (k_dtype) {
         case IDX_F16:
             return run(static_cast<const __half*>(k_raw), k_row_stride, k_rows, g, C, d, pooled,
-                       pool_seq_stride, st);
+                       pool_seq_stride, n_pooled, stale_pos, st);
         case IDX_BF16:
             return run(static_cast<const __nv_bfloat16*>(k_raw), k_row_stride, k_rows, g, C, d,
-                       pooled, pool_seq_stride, st);
+                       pooled, pool_seq_stride, n_pooled, stale_pos, st);
         default:
             return run(static_cast<const float*>(k_raw), k_row_stride, k_rows, g, C, d, pooled,
-                       pool_seq_stride, st);
+                       pool_seq_stride, n_pooled, stale_pos, st);
     }
 }
 

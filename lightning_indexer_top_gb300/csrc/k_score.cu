@@ -23,7 +23,7 @@ template <typename TK, int HH>
 __global__ void __launch_bounds__(kTile) score_generic_kernel(
     const void* __restrict__ q, int q_dtype, const float* __restrict__ w, int H, int d,
     const TK* __restrict__ k, int64_t k_row_stride, int64_t k_rows, Geom g, int block_size,
-    float* __restrict__ scores, int64_t score_row_stride) {
+    float* __restrict__ scores, int64_t score_row_stride, const float* __restrict__ k_scale) {
     extern __shared__ float smem[];
     float* qs = smem;            // [HH][d], heads >= H zero
     float* ws = smem + HH * d;   // [HH],    heads >= H zero
@@ -68,9 +68,11 @@ __global__ void __launch_bounds__(kTile) score_generic_kernel(
                 acc[h] = a;
             }
         }
+        // quantized keys: the dot with the dequantized key is scale * (dot with the codes)
+        const float ks = k_scale ? k_scale[row] : 1.f;
         float s = 0.f;
 #pragma unroll
-        for (int h = 0; h < HH; ++h) s = fmaf(ws[h], fmaxf(acc[h], 0.f), s);
+        for (int h = 0; h < HH; ++h) s = fmaf(ws[h], fmaxf(ks * acc[h], 0.f), s);
         scores[r * score_row_stride + j] = s + 0.0f;  // -0 + +0 = +0
     }
 }
@@ -78,7 +80,7 @@ __global__ void __launch_bounds__(kTile) score_generic_kernel(
 template <typename TK>
 cudaError_t run(const void* q, int q_dtype, const float* w, int H, int d, const TK* k,
                 int64_t k_row_stride, int64_t k_rows, const Geom& g, int block_size,
-                float* scores, int64_t score_row_stride, cudaStream_t st) {
+                float* scores, int64_t score_row_stride, cudaStream_t st, const float* k_scale) {
     int max_keys = g.max_n_kv;
     if (block_size > 1) max_keys /= block_size;
     const int64_t n_rows = (int64_t)g.B * g.T;
@@ -93,7 +95,7 @@ cudaError_t run(const void* q, int q_dtype, const float* w, int H, int d, const 
         auto kern = score_generic_kernel<TK, N>;                                               \
         if (sm > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm); \
         kern<<<grid, kTile, sm, st>>>(q, q_dtype, w, H, d, k, k_row_stride, k_rows, g, block_size, \
-                                      scores, score_row_stride);                              \
+                                      scores, score_row_stride, k_scale);                     \
         break;                                                                                 \
     }
     switch (HH) {
@@ -115,17 +117,20 @@ cudaError_t run(const void* q, int q_dtype, const float* w, int H, int d, const 
 cudaError_t launch_score_generic(const void* q, int q_dtype, const float* w, int H, int d,
                                  const void* k, int k_dtype, int64_t k_row_stride, int64_t k_rows,
                                  const Geom& g, int block_size, float* scores,
-                                 int64_t score_row_stride, cudaStream_t st) {
+                                 int64_t score_row_stride, cudaStream_t st, const float* k_scale) {
     switch (k_dtype) {
         case IDX_F16:
             return run(q, q_dtype, w, H, d, static_cast<const __half*>(k), k_row_stride, k_rows, g,
-                       block_size, scores, score_row_stride, st);
+                       block_size, scores, score_row_stride, st, nullptr);
         case IDX_BF16:
             return run(q, q_dtype, w, H, d, static_cast<const __nv_bfloat16*>(k), k_row_stride,
-                       k_rows, g, block_size, scores, score_row_stride, st);
+                       k_rows, g, block_size, scores, score_row_stride, st, nullptr);
+        case IDX_I8_ROWSCALE:
+            return run(q, q_dtype, w, H, d, static_cast<const int8_t*>(k), k_row_stride, k_rows, g,
+                       block_size, scores, score_row_stride, st, k_scale);
         default:
             return run(q, q_dtype, w, H, d, static_cast<const float*>(k), k_row_stride, k_rows, g,
-                       block_size, scores, score_row_stride, st);
+                       block_size, scores, score_row_stride, st, nullptr);
     }
 }
 

@@ -37,6 +37,7 @@
 // down (drains its TMA loads and MMAs, frees TMEM) instead of hanging.
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 
 #include "lidx_internal.cuh"
 #include "sm100_ptx.cuh"
@@ -67,10 +68,23 @@ constexpr int kTileBytes = kTileKeys * kD * 2;       // 32 KB
 constexpr int kHalfBytes = kTileBytes / 2;           // one 64-column box
 constexpr int kQBytes = kH * kD * 2;                 // 16 KB
 constexpr int kQHalfBytes = kQBytes / 2;
-constexpr int kThreads = 224;
+constexpr int kThreads = 224;                        // 16-bit keys: 7 warps
+constexpr int kThreadsQ8 = 352;                      // int8 keys: + 4 converter warps
+#ifndef LIDX_Q8_RAW_STAGES
+#define LIDX_Q8_RAW_STAGES 5
+#endif
+#ifndef LIDX_Q8_CONV_STAGES
+#define LIDX_Q8_CONV_STAGES 2
+#endif
+constexpr int kRawStages = LIDX_Q8_RAW_STAGES;       // int8 keys: TMA ring of 16 KB code tiles
+constexpr int kConvStages = LIDX_Q8_CONV_STAGES;     // int8 keys: widened tiles for the MMA
+constexpr int kRawTileBytes = kTileKeys * kD;        // 16 KB
 constexpr int kChunkTiles = LIDX_SCORE_CHUNK;        // key tiles (32 KB each) per chunk
 constexpr int kRing = 4;                             // chunk descriptors in flight
-constexpr int kQBufs = 3;                            // staged q rows (one per chunk) in flight
+#ifndef LIDX_SCORE_QBUFS
+#define LIDX_SCORE_QBUFS 3
+#endif
+constexpr int kQBufs = LIDX_SCORE_QBUFS;             // staged q rows (one per chunk) in flight
 constexpr int kMaxPrefixRows = 2048;
 
 struct Chunk {
@@ -79,8 +93,10 @@ struct Chunk {
 };
 
 struct Ctl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[8];          // TMA tile landed (16-bit keys: the MMA's tiles; int8: code tiles)
+    uint64_t empty[8];
+    uint64_t afull[kConvStages];   // int8 keys: widened tile written
+    uint64_t aempty[kConvStages];  // int8 keys: widened tile read by the MMAs
     uint64_t tfull[kAcc];
     uint64_t tempty[kAcc];
     uint64_t qfull[kQBufs];
@@ -94,9 +110,17 @@ struct Ctl {
     int n_chunks;
 };
 
-constexpr int kChunkReaders = 1 + 4 + 1;             // MMA lane, 4 epilogue warps, q stager
-constexpr size_t kSmemBytes =
-    1024 + (size_t)kStages * kTileBytes + kQBufs * kQBytes + sizeof(Ctl) + (2 * kMaxPrefixRows + 1) * sizeof(int);
+static_assert(kStages <= 8 && kRawStages <= 8, "barrier arrays");
+constexpr int kChunkReaders = 1 + 4 + 1;             // MMA lane, 4 epilogue warps, q stager (+4 converters)
+template <bool Q8>
+constexpr size_t smem_bytes() {
+    return 1024 + (Q8 ? (size_t)kRawStages * kRawTileBytes + (size_t)kConvStages * kTileBytes
+                      : (size_t)kStages * kTileBytes) +
+           kQBufs * kQBytes + sizeof(Ctl) + (2 * kMaxPrefixRows + 1) * sizeof(int) +
+           (Q8 ? 4 * 8 * 32 * sizeof(float) : 0);
+}
+constexpr size_t kSmemBytes = smem_bytes<false>();
+static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448, "shared memory");
 
 template <typename T> constexpr bool kIsBF16 = false;
 template <> constexpr bool kIsBF16<__nv_bfloat16> = true;
@@ -195,26 +219,77 @@ __device__ __forceinline__ bool warp_next_chunk(Ctl& c, int k, Chunk& d) {
     return true;
 }
 
-template <typename TK>
-__global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
+// int8 codes of one 128-key tile (rows of 128 bytes, unswizzled) -> f16 in the
+// MMA's A layout (two 64-column blocks of 16 KB, rows of 128 bytes, 16-byte
+// chunks swizzled by row).  Thread t (0..127) converts key row t; it walks its
+// 8 source chunks starting at chunk t % 8 so that the 8 threads of a
+// shared-memory phase hit 8 different bank groups.
+// The widening is exact and stays on the integer/half ALUs: a code b becomes
+// the unsigned byte u = b + 128 (xor 0x80), the f16 with bit pattern 0x6400 | u
+// is 1024 + u, and subtracting 1152 leaves b (every step exact in f16).
+__device__ __forceinline__ void widen_tile_f16(const uint8_t* __restrict__ raw, uint8_t* __restrict__ dst, int t) {
+    const uint8_t* src = raw + t * 128;
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
+    uint4 row[8];                                          // all loads first: one latency per tile
+#pragma unroll
+    for (int i = 0; i < 8; ++i) row[i] = *reinterpret_cast<const uint4*>(src + ((i + t) & 7) * 16);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int cch = (i + t) & 7;                       // 16 codes: elements 16*cch .. 16*cch+15
+        const uint4 v = row[i];
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        uint32_t out[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t u = in[j] ^ 0x80808080u;
+            const uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);   // {0x64|u0, 0x64|u1}
+            const uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);   // {0x64|u2, 0x64|u3}
+            const __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), bias);
+            const __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&hi), bias);
+            out[2 * j] = *reinterpret_cast<const uint32_t*>(&a);
+            out[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+        const int blk = cch >> 2;                          // 64-element column block
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int sub = 2 * (cch & 3) + hh;             // 16-byte chunk inside the block's row
+            *reinterpret_cast<uint4*>(dst + blk * kHalfBytes + t * 128 + ((sub ^ (t & 7)) << 4)) =
+                make_uint4(out[4 * hh], out[4 * hh + 1], out[4 * hh + 2], out[4 * hh + 3]);
+        }
+    }
+}
+
+template <typename TK, bool kQ8>
+__global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decode_kernel(
     const __grid_constant__ CUtensorMap kmap, const void* __restrict__ q, int q_dtype,
-    const float* __restrict__ w, Geom g, float* __restrict__ scores, int64_t score_row_stride, int sched_slot) {
+    const float* __restrict__ w, Geom g, float* __restrict__ scores, int64_t score_row_stride, int sched_slot,
+    const float* __restrict__ k_scale) {
+    constexpr int kNT = kQ8 ? kThreadsQ8 : kThreads;
+    constexpr int kTmaStages = kQ8 ? kRawStages : kStages;   // the producer's ring
+    constexpr int kTmaBytes = kQ8 ? kRawTileBytes : kTileBytes;
+    constexpr int kAStages = kQ8 ? kConvStages : kStages;    // the MMA's A tiles
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* tiles = smem;                                   // kStages x 32 KB, 1024-aligned
-    uint8_t* qbuf = smem + (size_t)kStages * kTileBytes;     // kQBufs x 16 KB, 1024-aligned
+    uint8_t* tma_tiles = smem;                               // kTmaStages x kTmaBytes, 1024-aligned
+    uint8_t* tiles = kQ8 ? smem + (size_t)kRawStages * kRawTileBytes : smem;   // kAStages x 32 KB
+    uint8_t* qbuf = tiles + (size_t)kAStages * kTileBytes;   // kQBufs x 16 KB, 1024-aligned
     Ctl& c = *reinterpret_cast<Ctl*>(qbuf + kQBufs * kQBytes);
     int* pre = reinterpret_cast<int*>(&c + 1);               // [n_rows + 1] in prefix mode
     int* nvis = pre + kMaxPrefixRows + 1;                    // [n_rows] in prefix mode
+    float* escale = reinterpret_cast<float*>(nvis + kMaxPrefixRows);   // int8 keys: [4 warps][8 tiles][32]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n_rows = (int64_t)g.B * g.T;
     const bool prefix = n_rows <= kMaxPrefixRows;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kTmaStages; ++i) {
             mbar_init(&c.full[i], 1);
-            mbar_init(&c.empty[i], 1);
+            mbar_init(&c.empty[i], kQ8 ? 4 : 1);     // int8: freed by the 4 converter warps
+        }
+        for (int i = 0; i < kConvStages; ++i) {
+            mbar_init(&c.afull[i], 4);
+            mbar_init(&c.aempty[i], 1);
         }
         for (int i = 0; i < kAcc; ++i) {
             mbar_init(&c.tfull[i], 1);
@@ -226,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
         }
         for (int i = 0; i < kRing; ++i) {
             mbar_init(&c.cfull[i], 1);
-            mbar_init(&c.cempty[i], kChunkReaders);
+            mbar_init(&c.cempty[i], kChunkReaders + (kQ8 ? 4 : 0));
         }
         mbar_init(&c.done, 1);
         c.abort = 0;
@@ -234,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
     }
     // chunks per row, then their prefix (all threads read the rows' bounds in parallel)
     if (prefix) {
-        for (int64_t r = threadIdx.x; r < n_rows; r += kThreads) {
+        for (int64_t r = threadIdx.x; r < n_rows; r += kNT) {
             const int nv = row_n_vis(g, r);
             nvis[r] = nv;
             pre[r + 1] = row_chunks(nv);
@@ -301,12 +376,16 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
                         break;
                     }
                     const int64_t krow = krow0 + (int64_t)t * kTileKeys;
-                    uint8_t* dst = tiles + (size_t)stage * kTileBytes;
-                    mbar_arrive_expect_tx(&c.full[stage], kTileBytes);
-                    tma_load_2d(dst, &kmap, &c.full[stage], 0, (int32_t)krow);
-                    tma_load_2d(dst + kHalfBytes, &kmap, &c.full[stage], 64, (int32_t)krow);
+                    uint8_t* dst = tma_tiles + (size_t)stage * kTmaBytes;
+                    mbar_arrive_expect_tx(&c.full[stage], kTmaBytes);
+                    if constexpr (kQ8) {
+                        tma_load_2d(dst, &kmap, &c.full[stage], 0, (int32_t)krow);
+                    } else {
+                        tma_load_2d(dst, &kmap, &c.full[stage], 0, (int32_t)krow);
+                        tma_load_2d(dst + kHalfBytes, &kmap, &c.full[stage], 64, (int32_t)krow);
+                    }
                     ++issued;
-                    if (++stage == kStages) {
+                    if (++stage == kTmaStages) {
                         stage = 0;
                         phase ^= 1;
                     }
@@ -314,9 +393,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
                 if (!ok) break;
             }
             // never leave the CTA with TMA writes in flight
-            const int64_t n = issued < kStages ? issued : kStages;
+            const int64_t n = issued < kTmaStages ? issued : kTmaStages;
             for (int64_t i = issued - n; i < issued; ++i)
-                mbar_wait(&c.full[i % kStages], (uint32_t)((i / kStages) & 1));
+                mbar_wait(&c.full[i % kTmaStages], (uint32_t)((i / kTmaStages) & 1));
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -343,8 +422,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
                     break;
                 }
                 const uint32_t b0 = smem_u32(qbuf + qb * kQBytes);
+                uint64_t* a_full = kQ8 ? c.afull : c.full;
+                uint64_t* a_empty = kQ8 ? c.aempty : c.empty;
                 for (int t = d.t0; t < d.t1; ++t) {
-                    if (!mbar_wait(&c.tempty[acc], aphase ^ 1) || !mbar_wait(&c.full[stage], phase)) {
+                    if (!mbar_wait(&c.tempty[acc], aphase ^ 1) || !mbar_wait(&a_full[stage], phase)) {
                         abort_cta(c, g);
                         ok = false;
                         break;
@@ -359,9 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
                         const uint64_t bd = desc_sw128_kmajor(b0 + (kk >> 2) * kQHalfBytes + off, 1024);
                         mma_f16_ss(dt, ad, bd, idesc, kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(&c.empty[stage]);
+                    mma_commit(&a_empty[stage]);
                     mma_commit(&c.tfull[acc]);
-                    if (++stage == kStages) {
+                    if (++stage == kAStages) {
                         stage = 0;
                         phase ^= 1;
                     }
@@ -404,9 +485,47 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
             if (lane == 0) mbar_arrive(&c.qfull[qb]);
             ++qseq;
         }
+    } else if (kQ8 && warp >= 7) {
+        // ------------------------------------------------------------ converters (int8 keys)
+        const int t = threadIdx.x - 7 * 32;        // key row of the tile, 0..127
+        int rs = 0, as = 0;
+        uint32_t rph = 0, aph = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            Chunk d;
+            if (warp_aborted(c) || !warp_next_chunk(c, k, d)) {
+                abort_cta(c, g);
+                break;
+            }
+            if (d.row < 0) break;
+            for (int tt = d.t0; tt < d.t1; ++tt) {
+                if (!warp_wait(&c.full[rs], rph) || !warp_wait(&c.aempty[as], aph ^ 1)) {
+                    abort_cta(c, g);
+                    ok = false;
+                    break;
+                }
+                static_assert(!kQ8 || std::is_same<TK, __half>::value, "int8 codes are widened to f16");
+                widen_tile_f16(tma_tiles + (size_t)rs * kRawTileBytes, tiles + (size_t)as * kTileBytes, t);
+                fence_proxy_async_smem();           // generic-proxy writes before the MMA reads them
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&c.empty[rs]);
+                    mbar_arrive(&c.afull[as]);
+                }
+                if (++rs == kRawStages) {
+                    rs = 0;
+                    rph ^= 1;
+                }
+                if (++as == kConvStages) {
+                    as = 0;
+                    aph ^= 1;
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;                 // TMEM lane quarter this warp may access
+        float* esc = escale + (warp - 2) * 8 * 32;   // int8 keys: this warp's prefetched key scales
         int acc = 0;
         uint32_t aphase = 0;
         float wv[kH];
@@ -420,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
             if (d.row < 0) break;
             if (d.t1 <= d.t0) continue;
             const int n_keys = prefix ? nvis[d.row] : row_n_vis(g, d.row);
+            const int64_t krow0 = kQ8 ? seq_row0(g, (int)(d.row / g.T)) : 0;
             const float4* wr = reinterpret_cast<const float4*>(w + d.row * kH);
 #pragma unroll
             for (int h4 = 0; h4 < kH / 4; ++h4) {
@@ -429,36 +549,71 @@ __global__ void __launch_bounds__(kThreads, 1) score_tc_decode_kernel(
                 wv[4 * h4 + 2] = x.z;
                 wv[4 * h4 + 3] = x.w;
             }
-            for (int t = d.t0; t < d.t1; ++t) {
-                if (!warp_wait(&c.tfull[acc], aphase)) {
-                    abort_cta(c, g);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                float v0[32], v1[32];
-                const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + acc * kH;
-                tmem_ld_32x32b_x32(ta, v0);
-                tmem_ld_32x32b_x32(ta + 32, v1);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&c.tempty[acc]);
-                // four partial sums (a shorter dependent chain); the sum order is fixed
-                float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            // tiles in groups of 8: an int8 cache's per-key scales of a whole group are
+            // loaded at once (one memory round trip per 8 tiles, which the 4 TMEM
+            // accumulators give the MMAs slack for) and parked in this lane's own
+            // shared-memory slots
+            for (int g0 = d.t0; ok && g0 < d.t1; g0 += 8) {
+                if constexpr (kQ8) {
+                    float scs[8];
 #pragma unroll
-                for (int h = 0; h < 32; h += 2) {
-                    s0 = fmaf(wv[h], fmaxf(v0[h], 0.f), s0);
-                    s1 = fmaf(wv[h + 1], fmaxf(v0[h + 1], 0.f), s1);
-                    s2 = fmaf(wv[32 + h], fmaxf(v1[h], 0.f), s2);
-                    s3 = fmaf(wv[33 + h], fmaxf(v1[h + 1], 0.f), s3);
+                    for (int i = 0; i < 8; ++i) {
+                        const int j = (g0 + i) * kTileKeys + quad * 32 + lane;
+                        scs[i] = (g0 + i < d.t1 && j < n_keys) ? k_scale[krow0 + j] : 0.f;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) esc[i * 32 + lane] = scs[i];
                 }
-                const float s = (s0 + s1) + (s2 + s3);
-                const int j = t * kTileKeys + quad * 32 + lane;
-                if (j < n_keys) scores[d.row * score_row_stride + j] = s + 0.0f;
-                if (++acc == kAcc) {
-                    acc = 0;
-                    aphase ^= 1;
+#pragma unroll 1
+                for (int i = 0; i < 8; ++i) {
+                    const int t = g0 + i;
+                    if (t >= d.t1) break;
+                    const int j = t * kTileKeys + quad * 32 + lane;
+                    // int8 keys: the key's scale multiplies every head's dot product before the ReLU
+                    float sc = 1.f;
+                    if constexpr (kQ8) sc = esc[i * 32 + lane];
+                    if (!warp_wait(&c.tfull[acc], aphase)) {
+                        abort_cta(c, g);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    float v0[32], v1[32];
+                    const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + acc * kH;
+                    tmem_ld_32x32b_x32(ta, v0);
+                    tmem_ld_32x32b_x32(ta + 32, v1);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&c.tempty[acc]);
+                    // four partial sums (a shorter dependent chain); the sum order is fixed.
+                    // int8 keys: sum_h w_h relu(sc*D_h) = sc * sum_h w_h max(D_h, 0) for sc >= 0
+                    // and sc * sum_h w_h min(D_h, 0) for sc < 0, so the scale costs one multiply
+                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+                    if (!kQ8 || sc >= 0.f) {
+#pragma unroll
+                        for (int h = 0; h < 32; h += 2) {
+                            s0 = fmaf(wv[h], fmaxf(v0[h], 0.f), s0);
+                            s1 = fmaf(wv[h + 1], fmaxf(v0[h + 1], 0.f), s1);
+                            s2 = fmaf(wv[32 + h], fmaxf(v1[h], 0.f), s2);
+                            s3 = fmaf(wv[33 + h], fmaxf(v1[h + 1], 0.f), s3);
+                        }
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 32; h += 2) {
+                            s0 = fmaf(wv[h], fminf(v0[h], 0.f), s0);
+                            s1 = fmaf(wv[h + 1], fminf(v0[h + 1], 0.f), s1);
+                            s2 = fmaf(wv[32 + h], fminf(v1[h], 0.f), s2);
+                            s3 = fmaf(wv[33 + h], fminf(v1[h + 1], 0.f), s3);
+                        }
+                    }
+                    float s = (s0 + s1) + (s2 + s3);
+                    if constexpr (kQ8) s *= sc;
+                    if (j < n_keys) scores[d.row * score_row_stride + j] = s + 0.0f;
+                    if (++acc == kAcc) {
+                        acc = 0;
+                        aphase ^= 1;
+                    }
                 }
             }
         }
@@ -823,6 +978,47 @@ cudaError_t launch_score_tc_prefill(const void* q, int q_dtype, const float* w, 
     return cudaSuccess;
 }
 
+namespace {
+// grid of the decode scorer and the counter slot of this launch; false when the
+// chunks would not number in 32 bits
+bool decode_launch_shape(const Geom& g, int& grid, int& slot) {
+    const int64_t n_rows = (int64_t)g.B * g.T;
+    const int64_t chunks_per_row = ((g.max_n_kv + kTileKeys - 1) / kTileKeys + kChunkTiles - 1) / kChunkTiles;
+    const int64_t max_chunks = n_rows <= kMaxPrefixRows ? n_rows * chunks_per_row : n_rows;
+    if (max_chunks >= INT32_MAX - 2 * (int64_t)sm_count()) return false;
+    grid = (int)(max_chunks < sm_count() ? max_chunks : sm_count());
+    // one counter slot per launch, round-robin (a slot is reused only after
+    // kSchedSlots further launches; its previous launch has zeroed it by then
+    // unless that many launches are in flight at once)
+    static std::atomic<unsigned> next_slot{0};
+    slot = (int)(next_slot.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots);
+    return true;
+}
+}  // namespace
+
+cudaError_t launch_score_tc_q8(const void* q, int q_dtype, const float* w, const int8_t* k8, int64_t k_row_stride,
+                               const float* k_scale, int64_t k_rows, const Geom& g, float* scores,
+                               int64_t score_row_stride, cudaStream_t st) {
+    // the codes are widened to f16 exactly; q goes to f16 too (exact for f16 q, and for bf16
+    // q inside f16's normal range, as on the F16-cache path)
+    if (g.T != 1 || (q_dtype != IDX_BF16 && q_dtype != IDX_F16)) return cudaErrorNotSupported;
+    if ((reinterpret_cast<uintptr_t>(k8) & 15u) || (k_row_stride % 16) || k_rows < 1 || k_rows > INT32_MAX ||
+        (reinterpret_cast<uintptr_t>(w) & 15u) || (reinterpret_cast<uintptr_t>(q) & 15u))
+        return cudaErrorNotSupported;
+    const int64_t n_rows = (int64_t)g.B * g.T;
+    if (n_rows == 0 || g.max_n_kv == 0) return cudaSuccess;
+    CUtensorMap map;
+    if (!make_key8_tmap(&map, k8, k_row_stride, k_rows, kTileKeys)) return cudaErrorNotSupported;
+    int grid, slot;
+    if (!decode_launch_shape(g, grid, slot)) return cudaErrorNotSupported;
+    auto kern = score_tc_decode_kernel<__half, true>;
+    constexpr size_t smem = smem_bytes<true>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreadsQ8, smem, st>>>(map, q, q_dtype, w, g, scores, score_row_stride, slot, k_scale);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, int d, const void* k,
                             int k_dtype, int64_t k_row_stride, int64_t k_rows, const Geom& g, int block_size,
                             float* scores, int64_t score_row_stride, cudaStream_t st) {
@@ -842,20 +1038,12 @@ cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, i
     CUtensorMap map;
     const bool bf16 = k_dtype == IDX_BF16;
     if (!make_key_tmap(&map, k, bf16, k_row_stride, k_rows, kTileKeys)) return cudaErrorNotSupported;
-    // chunks are numbered in 32 bits
-    const int64_t chunks_per_row = ((g.max_n_kv + kTileKeys - 1) / kTileKeys + kChunkTiles - 1) / kChunkTiles;
-    const int64_t max_chunks = n_rows <= kMaxPrefixRows ? n_rows * chunks_per_row : n_rows;
-    if (max_chunks >= INT32_MAX - 2 * (int64_t)sm_count()) return cudaErrorNotSupported;
-    const int grid = (int)(max_chunks < sm_count() ? max_chunks : sm_count());
-    // one counter slot per launch, round-robin (a slot is reused only after
-    // kSchedSlots further launches; its previous launch has zeroed it by then
-    // unless that many launches are in flight at once)
-    static std::atomic<unsigned> next_slot{0};
-    const int slot = (int)(next_slot.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots);
-    auto kern = bf16 ? score_tc_decode_kernel<__nv_bfloat16> : score_tc_decode_kernel<__half>;
+    int grid, slot;
+    if (!decode_launch_shape(g, grid, slot)) return cudaErrorNotSupported;
+    auto kern = bf16 ? score_tc_decode_kernel<__nv_bfloat16, false> : score_tc_decode_kernel<__half, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kSmemBytes, st>>>(map, q, q_dtype, w, g, scores, score_row_stride, slot);
+    kern<<<grid, kThreads, kSmemBytes, st>>>(map, q, q_dtype, w, g, scores, score_row_stride, slot, nullptr);
     return cudaGetLastError();
 }
 

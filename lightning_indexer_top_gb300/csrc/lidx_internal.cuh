@@ -61,6 +61,7 @@ __device__ __forceinline__ int64_t seq_row0(const Geom& g, int b) {
 // element conversions
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(int8_t x) { return (float)x; }
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
@@ -95,10 +96,15 @@ inline size_t dtype_size(int t) { return t == IDX_F32 ? 4 : 2; }
 cudaError_t launch_hadamard(const void* x, void* y, int dtype, int64_t n_rows, int d,
                             int64_t row_stride, cudaStream_t st);
 
+// k_dtype IDX_I8_ROWSCALE: int8 key rows with per-row f32 scales k_scale
+constexpr int IDX_I8_ROWSCALE = 100;
 cudaError_t launch_score_generic(const void* q, int q_dtype, const float* w, int H, int d,
                                  const void* k, int k_dtype, int64_t k_row_stride, int64_t k_rows,
                                  const Geom& g, int block_size, float* scores,
-                                 int64_t score_row_stride, cudaStream_t st);
+                                 int64_t score_row_stride, cudaStream_t st, const float* k_scale = nullptr);
+
+cudaError_t launch_quantize_rows(const void* x, int x_dtype, int64_t n_rows, int d, int64_t x_row_stride,
+                                 int8_t* q8, int64_t q8_row_stride, float* scale, cudaStream_t st);
 
 // tensor-core scorer for H = 64, d = 128, 16-bit keys; returns cudaErrorNotSupported
 // when the shape is not one it handles (the caller then uses the generic scorer)
@@ -107,9 +113,17 @@ cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, i
                             const Geom& g, int block_size, float* scores, int64_t score_row_stride,
                             cudaStream_t st);
 
+// tensor-core decode scorer over int8 keys with per-row scales (H = 64, d = 128,
+// T = 1, 16-bit q); cudaErrorNotSupported for anything else
+cudaError_t launch_score_tc_q8(const void* q, int q_dtype, const float* w, const int8_t* k8, int64_t k_row_stride,
+                               const float* k_scale, int64_t k_rows, const Geom& g, float* scores,
+                               int64_t score_row_stride, cudaStream_t st);
+
+// n_pooled / stale_pos (device, may be NULL): pool only blocks from
+// min(n_pooled[b], stale_pos[b] / C) on (incremental maintenance)
 cudaError_t launch_block_pool(const void* k_raw, int k_dtype, int64_t k_row_stride, int64_t k_rows,
                               const Geom& g, int C, int d, float* pooled, int64_t pool_seq_stride,
-                              cudaStream_t st);
+                              const int32_t* n_pooled, const int32_t* stale_pos, cudaStream_t st);
 
 // few rows with a workspace of topk_workspace_bytes(): multi-CTA passes; else one CTA per row
 cudaError_t launch_topk(const float* scores, int64_t score_row_stride, const Geom& g, int top_k,
@@ -139,6 +153,8 @@ bool make_key_tmap(CUtensorMap* m, const void* k, bool bf16, int64_t k_row_strid
 bool make_latent_tmap(CUtensorMap* m, const void* lat, int64_t row_stride, int64_t rows);
 bool make_q3d_tmap(CUtensorMap* m, const void* q, bool bf16, int64_t rows);
 bool make_w_tmap(CUtensorMap* m, const float* w, int64_t rows);
+// [rows, 128] int8 keys: boxes of 128 bytes x box_rows rows, no swizzle
+bool make_key8_tmap(CUtensorMap* m, const int8_t* k, int64_t row_bytes, int64_t k_rows, int box_rows);
 
 // number of SMs of the current device (cached per device)
 int sm_count();

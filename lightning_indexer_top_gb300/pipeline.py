@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import torch
 
-from . import Batch, idx_block_pool, idx_hadamard, idx_score, idx_topk, idx_workspace_size, topk_capacity
+from . import Batch, idx_block_pool, idx_hadamard, idx_score, idx_score_q8, idx_topk, idx_workspace_size, topk_capacity
 from . import sparse_attn_decode, sparse_attn_prefill, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL, IDX_OP_TOPK
 from .workloads import Workload
 
@@ -62,6 +62,8 @@ class SparseAttentionStep:
             idx_block_pool(k, self.batch, wl.block_size, pool_seq_stride=self.pool_stride, pooled=self.pooled)
             kp = self.pooled.view(-1, wl.d)
             idx_score(q, wl.w, kp, self.pool_batch, block_size=wl.block_size, scores=self.scores)
+        elif wl.k8 is not None:
+            idx_score_q8(q, wl.w, wl.k8, wl.k_scale, self.batch, scores=self.scores)
         else:
             idx_score(q, wl.w, k, self.batch, scores=self.scores)
 

@@ -54,6 +54,8 @@ class Workload:
     q_pos: Optional[torch.Tensor] = None
     hadamard: bool = False
     block_size: int = 0
+    k8: Optional[torch.Tensor] = None        # int8 indexer key codes [rows, d] (quantized cache)
+    k_scale: Optional[torch.Tensor] = None   # f32 [rows] per-row scales of k8
     extra: Dict = field(default_factory=dict)
 
     def row0(self, b: int) -> int:
@@ -74,8 +76,12 @@ def _randn(shape, dtype, g, device, std=1.0):
 
 
 def make(cfg, device="cuda", *, n_kv_override=None, batch_override=None, n_tokens_override=None,
-         parity_tails=False) -> Workload:
+         parity_tails=False, quantized_keys=False) -> Workload:
     """Build configuration `cfg` (1-5 or "headline") on `device`.
+
+    quantized_keys: also store the decode indexer keys as a quantized cache
+    (int8 codes + per-row f32 scales, idx_quantize_rows of the F16 keys); the
+    workload's name gets the suffix "_q8" and the scorer reads the codes.
 
     Overrides shrink a configuration for parity tests that the oracle must
     finish quickly; they keep every other property (dtypes, heads, top_k,
@@ -129,9 +135,14 @@ def make(cfg, device="cuda", *, n_kv_override=None, batch_override=None, n_token
         qa = _randn((B, Hq, dk), torch.bfloat16, g, dev)
         lat = _randn((rows, dk), torch.bfloat16, g, dev)
         name = {2: "decode_mla_8x8192", 5: "long_decode_mla_ragged", "headline": "decode_mla_64x131072"}[cfg]
+        k8 = ks = None
+        if quantized_keys:
+            from . import idx_quantize_rows
+            k8, ks = idx_quantize_rows(k)
+            name += "_q8"
         return Workload(name, "decode", B, 1, torch.tensor(n_kv, **i32), n_kv, max_n_kv, top_k, H, d, q, w, k,
                         1 / math.sqrt(192), qa, lat, None, dv, kv_start=kv_start, kv_start_host=starts,
-                        kv_seq_stride=stride)
+                        kv_seq_stride=stride, k8=k8, k_scale=ks)
 
     if cfg == 3:
         n = n_tokens_override or 16384

@@ -23,6 +23,9 @@ from .lidx_oracle import (  # noqa: F401
     indexer_scores,
     topk_select,
     block_pool,
+    block_pool_update,
+    quantize_rows,
+    dequantize_rows,
     block_select,
     block_select_expanded,
     attention_over,

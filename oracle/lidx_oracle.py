@@ -228,6 +228,34 @@ def topk_select(scores, n_vis: int, top_k: int) -> np.ndarray:
 # S5 / S6: block-pooled indexer
 # ---------------------------------------------------------------------------
 
+def quantize_rows(x):
+    """Per-row symmetric 8-bit codes of key rows, with an f32 scale per row.
+
+    The storage format of a quantized indexer key cache ("GLM-DSA: allow for
+    quantized indexer cache", ik_llama_opt commit log; like the q8_0 latent
+    cache described there, it is "a storage format only" and the scores use
+    the dequantized values).  Reading: one scale per key row,
+        scale = max_c |x_c| / 127,   q_c = clamp(rint(x_c / scale), -127, 127)
+    taken in float32 with round-to-nearest-even (the integer decisions are made
+    in the precision the kernel makes them in); an all-zero row gets scale 0
+    and codes 0.  Returns (int8 codes, float32 scales).
+    """
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    scale = (amax / np.float32(127.0)).astype(np.float32)
+    q = np.zeros(x32.shape, dtype=np.int8)
+    nz = scale > 0
+    if np.any(nz):
+        ratio = (x32[nz] / scale[nz][:, None]).astype(np.float32)
+        q[nz] = np.clip(np.rint(ratio), -127, 127).astype(np.int8)
+    return q, scale
+
+
+def dequantize_rows(q8, scale) -> np.ndarray:
+    """Key rows as the quantized cache represents them: scale_j * q8[j, c], in float64."""
+    return np.asarray(q8, dtype=np.float64) * np.asarray(scale, dtype=np.float64)[..., None]
+
+
 def block_pool(k_raw, C: int, n_kv: int) -> np.ndarray:
     """Mean of the C raw keys of each complete block, stored as float32.
 
@@ -246,6 +274,31 @@ def block_pool(k_raw, C: int, n_kv: int) -> np.ndarray:
         return np.zeros((0, d), dtype=np.float32)
     blocks = k_raw[: n_cb * C].reshape(n_cb, C, d)
     return blocks.mean(axis=1).astype(np.float32)
+
+
+def block_pool_update(pooled_prev, k_raw, C: int, n_kv: int, n_pooled: int, stale_pos=None) -> np.ndarray:
+    """Persistent pooled keys after one maintenance step.
+
+    The pooled keys persist across batches, a batch only appends complete
+    blocks, and an edit of the sequence from position p on regroups the blocks
+    from the one holding p, so every pooled key at or after it is stale
+    (llama-memory-hybrid-idx.h: "The pooled keys persist in the idx cache
+    across batches", mem_idx_stale with POS_CLEAN, and get_n_kpool_new, the
+    pools to re-pool this ubatch).  With n_cb = floor(n_kv / C) and
+        beta0 = min(n_pooled, floor(stale_pos / C))   (a negative stale_pos: 0)
+    clamped to [0, n_cb], blocks beta0 .. n_cb-1 take the block means of the
+    current raw keys (block_pool) and every other row of pooled_prev is kept.
+    stale_pos None means no edit.  Returns a new float32 array.
+    """
+    out = np.array(pooled_prev, dtype=np.float32, copy=True)
+    n_cb = int(n_kv) // int(C)
+    beta0 = max(int(n_pooled), 0)
+    if stale_pos is not None:
+        beta0 = min(beta0, 0 if stale_pos < 0 else int(stale_pos) // int(C))
+    beta0 = min(beta0, n_cb)
+    if n_cb > beta0:
+        out[beta0:n_cb] = block_pool(k_raw, C, n_kv)[beta0:n_cb]
+    return out
 
 
 def block_select(block_scores, n_vis: int, top_k: int, C: int) -> np.ndarray:

@@ -27,7 +27,7 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for n in ("idx_score", "idx_block_pool", "idx_topk", "sparse_attn_decode", "sparse_attn_prefill",
+    for n in ("idx_score", "idx_score_q8", "idx_quantize_rows", "idx_block_pool", "idx_block_pool_update", "idx_topk", "sparse_attn_decode", "sparse_attn_prefill",
               "idx_hadamard", "idx_workspace_size", "idx_last_error", "idx_device_status"):
         assert n in names
 
@@ -63,6 +63,12 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.idx_score(None, 0, None, 4, 32, None, 0, 32, 0, bad, 0, None, 0, None, 0, None) == L.IDX_ERR_INVALID_ARG
     assert lib.idx_score(None, 0, None, 65, 32, None, 0, 32, 0, b, 0, None, 16, None, 0, None) == L.IDX_ERR_UNSUPPORTED
     assert lib.idx_block_pool(None, L.IDX_BF16, 128, 0, b, 0, 128, None, 16, None) == L.IDX_ERR_INVALID_ARG
+    assert lib.idx_block_pool_update(None, L.IDX_BF16, 128, 0, b, None, None, 0, 128, None, 16, None) == \
+        L.IDX_ERR_INVALID_ARG
+    assert lib.idx_quantize_rows(None, L.IDX_BF16, 4, 0, 128, None, 128, None, None) == L.IDX_ERR_INVALID_ARG
+    assert lib.idx_quantize_rows(None, L.IDX_BF16, 4, 128, 128, None, 120, None, None) == L.IDX_ERR_INVALID_ARG
+    assert lib.idx_score_q8(None, L.IDX_BF16, None, 64, 128, None, 128, None, 0, b, 2, None, 16, None, 0, None) == \
+        L.IDX_ERR_UNSUPPORTED
     assert lib.sparse_attn_decode(None, L.IDX_BF16, 6, 4, 128, 128, None, None, 512, 512, 0, b, None, 16, None,
                                   1.0, None, L.IDX_F32, None, 0, None) == L.IDX_ERR_INVALID_ARG
     assert b"Hq % Hkv" in lib.idx_last_error() or b"Hq" in lib.idx_last_error()

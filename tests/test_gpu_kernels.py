@@ -194,6 +194,40 @@ def test_block_pool_matches_oracle(dtype, d):
         np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-6)
 
 
+def test_block_pool_update_repools_only_new_and_stale_blocks():
+    # persistent pooled cache over three "decode steps": append, edit + append, nothing new
+    g = torch.Generator(device=DEV).manual_seed(52)
+    C, d, stride_rows, B = 64, 128, 8192, 5
+    k = torch.randn(B * stride_rows, d, generator=g, device=DEV).to(torch.bfloat16)
+    n0 = [4000, 64, 0, 8191, 130]
+    batch0 = L.Batch(_i32(n0), 1, 8191, kv_seq_stride=stride_rows)
+    pooled = torch.full((B, 128, d), 7.0, device=DEV)
+    L.idx_block_pool(k, batch0, C, pooled=pooled, pool_seq_stride=128)
+    # step: sequences grow; sequence 0 edits its keys from position 1000 on, sequence 4 from 0
+    n1 = [4100, 200, 63, 8191, 300]
+    stale = [1000, L.IDX_POS_CLEAN, L.IDX_POS_CLEAN, L.IDX_POS_CLEAN, -1]
+    k[0 * stride_rows + 1000:0 * stride_rows + 4100] = torch.randn(3100, d, generator=g, device=DEV).to(k.dtype)
+    k[4 * stride_rows:4 * stride_rows + 300] = torch.randn(300, d, generator=g, device=DEV).to(k.dtype)
+    before = pooled.clone()
+    batch1 = L.Batch(_i32(n1), 1, 8191, kv_seq_stride=stride_rows)
+    L.idx_block_pool_update(k, batch1, C, pooled, n_pooled=_i32([n // C for n in n0]), stale_pos=_i32(stale))
+    torch.cuda.synchronize()
+    kh, got, prev = np64(k), pooled.cpu().numpy(), before.cpu().numpy()
+    for b in range(B):
+        ref = O.block_pool_update(prev[b], kh[b * stride_rows:b * stride_rows + n1[b]], C, n1[b], n0[b] // C,
+                                  None if stale[b] == L.IDX_POS_CLEAN else stale[b])
+        nb = n1[b] // C
+        np.testing.assert_allclose(got[b, :nb], ref[:nb], rtol=1e-5, atol=1e-6)
+        beta0 = min(n0[b] // C, nb if stale[b] == L.IDX_POS_CLEAN else max(stale[b], 0) // C)
+        assert np.array_equal(got[b, :beta0], prev[b, :beta0]), b       # untouched bits
+        assert np.array_equal(got[b, nb:], prev[b, nb:]), b
+    # nothing new and nothing stale: a no-op
+    again = pooled.clone()
+    L.idx_block_pool_update(k, batch1, C, pooled, n_pooled=_i32([n // C for n in n1]))
+    torch.cuda.synchronize()
+    assert torch.equal(again, pooled)
+
+
 # ------------------------------------------------------------------ attention over generator-drawn index sets
 
 def _random_sel(g, n_kv, sizes, rows):
@@ -510,3 +544,83 @@ def test_score_tensor_core_prefill_many_short_sequences():
             ref = O.indexer_scores(np64(q[r]), np64(w[r]), np64(k[b * max_n:b * max_n + nv]))
             assert_scores_close(got[:nv], ref, f"row {r}")
         assert np.all(got[nv:] == 555.0), r
+
+
+# ------------------------------------------------------------------ quantized (int8 + per-row scale) key cache
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float16, 128), (torch.float32, 40)])
+def test_quantize_rows_bit_exact(dtype, d):
+    g = torch.Generator(device=DEV).manual_seed(81)
+    n = 3001
+    x = (torch.randn(n, d, generator=g, device=DEV) * torch.rand(n, 1, generator=g, device=DEV) * 10).to(dtype)
+    x[7] = 0
+    x[11, :] = 127.0
+    x[11, 1] = 2.5
+    q8, sc = L.idx_quantize_rows(x)
+    torch.cuda.synchronize()
+    rq, rs = O.quantize_rows(np64(x))
+    assert np.array_equal(sc.cpu().numpy(), rs)
+    assert np.array_equal(q8.cpu().numpy(), rq)
+
+
+def _q8_cache(g, rows, d=128):
+    k = torch.randn(rows, d, generator=g, device=DEV) * torch.rand(rows, 1, generator=g, device=DEV) * 3
+    return L.idx_quantize_rows(k)
+
+
+@pytest.mark.parametrize("qt", [torch.bfloat16, torch.float16])
+def test_score_q8_tensor_core_decode_matches_oracle(qt):
+    g = torch.Generator(device=DEV).manual_seed(82)
+    n_kv = [0, 1, 129, 8192, 300, 128, 5000, 20000]
+    starts = [0, 3, 100, 500, 9000, 9400, 9600, 15000]
+    B, H, d, rows = len(n_kv), 64, 128, 35000
+    q = torch.randn(B, H, d, generator=g, device=DEV).to(qt)
+    w = torch.randn(B, H, generator=g, device=DEV) / 8
+    k8, ks = _q8_cache(g, rows)
+    ks[9001] = -ks[9001]                     # a negative scale: relu(scale * dot) per head
+    batch = L.Batch(_i32(n_kv), 1, 20000, kv_start=_i32(starts))
+    s = torch.full((B, 20000), 777.0, device=DEV)
+    L.idx_score_q8(q, w, k8, ks, batch, scores=s)
+    torch.cuda.synchronize()
+    sh = s.cpu().numpy()
+    kd = O.dequantize_rows(k8.cpu().numpy(), ks.cpu().numpy())
+    for b, n in enumerate(n_kv):
+        ref = O.indexer_scores(np64(q[b]), np64(w[b]), kd[starts[b]:starts[b] + n])
+        assert_scores_close(sh[b, :n], ref, f"seq {b}")
+        assert np.all(sh[b, n:] == 777.0)
+
+
+def test_score_q8_generic_path_matches_oracle():
+    # 32 heads x 64 and f32 q go to the CUDA-core scorer
+    g = torch.Generator(device=DEV).manual_seed(83)
+    n_kv = [40, 700, 1]
+    B, rows = 3, 1000
+    for H, d, qt in [(32, 64, torch.bfloat16), (64, 128, torch.float32)]:
+        q = torch.randn(B, H, d, generator=g, device=DEV).to(qt)
+        w = torch.randn(B, H, generator=g, device=DEV) / 8
+        k8, ks = _q8_cache(g, rows, d)
+        batch = L.Batch(_i32(n_kv), 1, 700, kv_seq_stride=0)
+        s = L.idx_score_q8(q, w, k8, ks, batch)
+        torch.cuda.synchronize()
+        kd = O.dequantize_rows(k8.cpu().numpy(), ks.cpu().numpy())
+        for b, n in enumerate(n_kv):
+            ref = O.indexer_scores(np64(q[b]), np64(w[b]), kd[:n])
+            assert_scores_close(s[b, :n].cpu().numpy(), ref, f"H={H} seq {b}")
+
+
+def test_score_q8_selection_matches_oracle_at_128k():
+    # one row at the headline length: scores on sampled keys, then the top-2048 set
+    g = torch.Generator(device=DEV).manual_seed(84)
+    n = 131072
+    q = torch.randn(2, 64, 128, generator=g, device=DEV).to(torch.bfloat16)
+    w = torch.randn(2, 64, generator=g, device=DEV) / 8
+    k8, ks = _q8_cache(g, 2 * n)
+    batch = L.Batch(_i32([n, n]), 1, n, kv_seq_stride=n)
+    s = L.idx_score_q8(q, w, k8, ks, batch)
+    idx, ns = L.idx_topk(s, batch, 2048)
+    torch.cuda.synchronize()
+    kd = O.dequantize_rows(k8[n:].cpu().numpy(), ks[n:].cpu().numpy())
+    ref = O.indexer_scores(np64(q[1]), np64(w[1]), kd)
+    assert_scores_close(s[1].cpu().numpy(), ref, "row 1")
+    from _helpers import check_selection
+    check_selection(idx[1, :int(ns[1])].cpu().numpy(), O.topk_select(ref, n, 2048), ref, "q8 row 1")

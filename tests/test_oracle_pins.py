@@ -374,3 +374,83 @@ def test_hadamard_store_exact_on_integer_inputs():
     # an involution up to rounding: applying it twice returns the input
     y = O.hadamard_store(O.hadamard_store(x, "f32"), "f32")
     np.testing.assert_allclose(y, x, atol=1e-5)
+
+
+def test_block_pool_update_worked_example(golden):
+    g = golden["block_pool_update"]
+    prev = np.zeros((4, 1), np.float32)
+    prev[:2, 0] = g["pooled_before"]
+    k = np.array(g["k_raw_after"], float)[:, None]
+    got = O.block_pool_update(prev, k, g["C"], len(k), g["n_pooled"], g["stale_pos"])
+    np.testing.assert_array_equal(got[:3, 0], np.array(g["expected"], np.float32))
+    assert got[3, 0] == 0.0          # rows past the complete blocks are untouched
+
+
+@pytest.mark.parametrize("n_prev,n_new,stale", [(0, 100, None), (64, 100, None), (64, 100, 37), (96, 130, 95),
+                                                 (96, 96, 0), (40, 200, -1), (200, 200, None), (128, 131, 127)])
+def test_block_pool_update_equals_full_pool_after_edits(n_prev, n_new, stale):
+    # invariant: pool the old keys, edit positions >= stale, append to n_new, update
+    # -> identical to pooling the new keys from scratch; rows before beta0 keep their bits
+    rng = np.random.default_rng(n_prev * 1000 + n_new)
+    C, d = 8, 5
+    k_old = rng.standard_normal((max(n_prev, n_new), d))
+    prev = np.full((40, d), 123.0, np.float32)
+    nb_prev = n_prev // C
+    prev[:nb_prev] = O.block_pool(k_old, C, n_prev)
+    k_new = k_old.copy()
+    if stale is not None:
+        k_new[max(stale, 0):] = rng.standard_normal(k_new[max(stale, 0):].shape)
+    got = O.block_pool_update(prev, k_new, C, n_new, nb_prev, stale)
+    n_cb = n_new // C
+    np.testing.assert_array_equal(got[:n_cb], O.block_pool(k_new, C, n_new))
+    beta0 = min(nb_prev, n_cb if stale is None else (0 if stale < 0 else stale // C))
+    np.testing.assert_array_equal(got[:beta0], prev[:beta0])
+    assert np.all(got[n_cb:] == prev[n_cb:])
+
+
+def test_block_pool_update_without_stale_marker_keeps_old_blocks():
+    # an edit the caller does not report is not seen: blocks before n_pooled stay as they were
+    C, d = 4, 3
+    k = np.arange(48.0).reshape(16, d)
+    prev = O.block_pool(k, C, 16)
+    k2 = k.copy()
+    k2[0] += 100.0
+    got = O.block_pool_update(prev, k2, C, 16, 4, None)
+    np.testing.assert_array_equal(got, prev)
+    got = O.block_pool_update(prev, k2, C, 16, 4, 0)
+    np.testing.assert_array_equal(got, O.block_pool(k2, C, 16))
+
+
+def test_quantize_rows_worked_values():
+    # amax 127 -> scale exactly 1, so the codes are rint(x) with ties to even
+    x = np.array([[127.0, 2.5, 3.5, -2.5, -0.5, 126.6, -127.0, 0.49]])
+    q, s = O.quantize_rows(x)
+    assert s[0] == np.float32(1.0)
+    np.testing.assert_array_equal(q[0], np.array([127, 2, 4, -2, 0, 127, -127, 0], np.int8))
+    q, s = O.quantize_rows(np.zeros((2, 5)))
+    assert np.all(s == 0) and np.all(q == 0)
+
+
+def test_quantize_rows_invariants():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((200, 128)).astype(np.float32) * rng.uniform(1e-3, 50, (200, 1)).astype(np.float32)
+    q, s = O.quantize_rows(x)
+    assert q.dtype == np.int8 and np.all(np.abs(q.astype(int)) <= 127)
+    assert np.all(np.abs(q).max(axis=1) == 127)                   # the largest entry maps to +-127
+    err = np.abs(x.astype(np.float64) - O.dequantize_rows(q, s))
+    assert np.all(err <= s[:, None].astype(np.float64) * (0.5 + 1e-5))
+
+
+def test_scores_of_quantized_keys_within_the_dequantization_bound():
+    # |relu(a) - relu(b)| <= |a - b| and |q_h . (k - k_hat)| <= ||q_h||_1 * scale / 2
+    rng = np.random.default_rng(6)
+    H, d, n = 8, 64, 50
+    q = rng.standard_normal((H, d))
+    w = rng.standard_normal(H)
+    k = rng.standard_normal((n, d))
+    k8, sc = O.quantize_rows(k)
+    exact = O.indexer_scores(q, w, k).astype(np.float64)
+    quant = O.indexer_scores(q, w, O.dequantize_rows(k8, sc)).astype(np.float64)
+    bound = np.abs(w) @ np.abs(q).sum(axis=1) * sc.astype(np.float64) / 2
+    assert np.all(np.abs(exact - quant) <= bound + 1e-5 * np.abs(exact) + 1e-6)
+    assert np.max(np.abs(exact - quant)) > 0                       # the codes are not the keys
