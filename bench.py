@@ -49,6 +49,7 @@ WORKLOADS = {
     "decode_mla_64x8192": (("headline",), {"n_kv_override": 8192}),
     "long_decode_mla_ragged": ((5,), {}),
     "decode_mla_64x131072_q8": (("headline",), {"quantized_keys": True}),
+    "decode_mla_64x131072_paged": (("headline",), {"page_size": 64}),
     "prefill_mla_16384": ((3,), {}),
     "prefill_mla_4096": ((3,), {"n_tokens_override": 4096}),
 }
@@ -171,14 +172,15 @@ def cpu_oracle_queries(wl, rows):
     inputs = []
     for r in rows:
         row0, n = wl.row0(r), wl.n_kv_host[r]
+        rows = wl.rows_of(r, n).to(wl.k_idx.device)   # position order (through the page table if paged)
         if wl.k8 is not None:   # the quantized cache as it represents the keys
-            keys = O.dequantize_rows(wl.k8[row0:row0 + n].cpu().numpy(), wl.k_scale[row0:row0 + n].cpu().numpy())
+            keys = O.dequantize_rows(wl.k8[rows].cpu().numpy(), wl.k_scale[rows].cpu().numpy())
         else:
-            keys = wl.k_idx[row0:row0 + n].to("cpu", torch.float64).numpy()
+            keys = wl.k_idx[rows].to("cpu", torch.float64).numpy()
         inputs.append((r, wl.q_idx[r].to("cpu", torch.float64).numpy(), wl.w[r].to("cpu", torch.float64).numpy(),
                        keys,
                        wl.q_attn[r].to("cpu", torch.float64).numpy(),
-                       wl.k_attn[row0:row0 + n].to("cpu", torch.float64).numpy(), n))
+                       wl.k_attn[rows].to("cpu", torch.float64).numpy(), n))
     t0 = time.perf_counter()
     for r, q, w, k, qa, lat, n in inputs:
         s, sel, out = O.decode_pipeline_mla(q, w, k, n, wl.top_k, qa, lat, wl.scale, wl.dv)

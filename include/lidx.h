@@ -74,6 +74,21 @@ typedef enum idx_dtype {
  *                  indexer").  n_vis(r) = min(q_pos[r] + 1, n_kv[b]), >= 0.
  *   max_n_kv       host-side bound: every n_kv[b] <= max_n_kv.  It sizes the
  *                  grids; a larger n_kv[b] is clamped to it and flagged.
+ *   page_table     device int32 or NULL.  Paged caches: position j of sequence
+ *                  b lives in cache row
+ *                      page_table[b*page_table_stride + j/page_size]*page_size
+ *                      + j % page_size
+ *                  (kv_start and kv_seq_stride are then unused).  Cache cells
+ *                  need not follow positions; blocks and the causal bound stay
+ *                  cuts of the position line (llama.cpp commit c88c916636, QSA
+ *                  commit message: blocks are cuts of the position line, not of
+ *                  the cell array; ik_llama.cpp PR #2058 "UPDATE 5": several
+ *                  sequences share one cell array).  A row outside the cache is
+ *                  never read (flagged, as for kv_start).
+ *   page_table_stride  entries per sequence in page_table.
+ *   page_size      rows per page, >= 1 when page_table is given (a multiple
+ *                  of 64 keeps the tensor-core scorers; other sizes run on the
+ *                  CUDA cores).
  */
 typedef struct idx_batch {
     int32_t n_seq;
@@ -83,6 +98,9 @@ typedef struct idx_batch {
     int64_t kv_seq_stride;
     const int32_t* q_pos;
     int32_t max_n_kv;
+    const int32_t* page_table;
+    int64_t page_table_stride;
+    int32_t page_size;
 } idx_batch;
 
 /*

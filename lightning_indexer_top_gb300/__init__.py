@@ -51,6 +51,9 @@ class _Batch(ctypes.Structure):
         ("kv_seq_stride", ctypes.c_int64),
         ("q_pos", ctypes.c_void_p),
         ("max_n_kv", ctypes.c_int32),
+        ("page_table", ctypes.c_void_p),
+        ("page_table_stride", ctypes.c_int64),
+        ("page_size", ctypes.c_int32),
     ]
 
 
@@ -130,6 +133,9 @@ class Batch:
     kv_start:  optional int32 CUDA tensor [B]: cache row of position 0.
     kv_seq_stride: rows between sequences when kv_start is None.
     q_pos:     optional int32 CUDA tensor [B*T]: causal position per query row.
+    page_table: optional int32 CUDA tensor [B, pages]: physical page of each logical page
+               (position j of sequence b is cache row page_table[b, j // page_size] * page_size
+               + j % page_size); kv_start / kv_seq_stride are then unused.
     """
 
     n_kv: torch.Tensor
@@ -138,6 +144,8 @@ class Batch:
     kv_start: Optional[torch.Tensor] = None
     kv_seq_stride: int = 0
     q_pos: Optional[torch.Tensor] = None
+    page_table: Optional[torch.Tensor] = None
+    page_size: int = 0
 
     @property
     def n_seq(self) -> int:
@@ -148,11 +156,13 @@ class Batch:
         return self.n_seq * self.n_q_per_seq
 
     def c(self) -> _Batch:
-        for t in (self.n_kv, self.kv_start, self.q_pos):
+        for t in (self.n_kv, self.kv_start, self.q_pos, self.page_table):
             if t is not None and (t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous()):
                 raise ValueError("batch arrays must be contiguous int32 CUDA tensors")
+        pt_stride = self.page_table.shape[-1] if self.page_table is not None else 0
         return _Batch(self.n_seq, self.n_q_per_seq, _ptr(self.n_kv), _ptr(self.kv_start),
-                      self.kv_seq_stride, _ptr(self.q_pos), self.max_n_kv)
+                      self.kv_seq_stride, _ptr(self.q_pos), self.max_n_kv, _ptr(self.page_table), pt_stride,
+                      self.page_size if self.page_table is not None else 0)
 
 
 def topk_capacity(top_k: int, block_size: int = 0) -> int:

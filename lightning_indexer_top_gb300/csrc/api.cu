@@ -70,6 +70,11 @@ idx_status check_batch(const idx_batch& b, const char* what) {
         return fail(IDX_ERR_INVALID_ARG, "%s: kv_seq_stride < 0", what);
     if ((int64_t)b.n_seq * b.n_q_per_seq > (int64_t)INT32_MAX)
         return fail(IDX_ERR_INVALID_ARG, "%s: more than 2^31-1 query rows", what);
+    if (b.page_table) {
+        if (b.page_size < 1) return fail(IDX_ERR_INVALID_ARG, "%s: page_size < 1 with a page table", what);
+        if (b.page_table_stride < ((int64_t)b.max_n_kv + b.page_size - 1) / b.page_size)
+            return fail(IDX_ERR_INVALID_ARG, "%s: page_table_stride < pages of max_n_kv", what);
+    }
     return IDX_OK;
 }
 
@@ -82,6 +87,9 @@ Geom make_geom(const idx_batch& b) {
     g.kv_seq_stride = b.kv_seq_stride;
     g.q_pos = b.q_pos;
     g.max_n_kv = b.max_n_kv;
+    g.page_table = b.page_table;
+    g.page_table_stride = b.page_table_stride;
+    g.page_size = b.page_table ? b.page_size : 0;
     g.status = status_ptr();
     return g;
 }
@@ -188,6 +196,8 @@ idx_status idx_score(const void* q, idx_dtype q_dtype, const float* w, int32_t n
     if (head_dim < 1 || head_dim > 256)
         return fail(IDX_ERR_UNSUPPORTED, "%s: head_dim must be in [1, 256]", what);
     if (block_size < 0) return fail(IDX_ERR_INVALID_ARG, "%s: block_size < 0", what);
+    if (block_size > 1 && batch.page_table)
+        return fail(IDX_ERR_UNSUPPORTED, "%s: pooled block keys are addressed without a page table", what);
     if (k_row_stride < head_dim) return fail(IDX_ERR_INVALID_ARG, "%s: k_row_stride < head_dim", what);
     if (k_rows < 0) return fail(IDX_ERR_INVALID_ARG, "%s: k_rows < 0", what);
     const int32_t max_keys = block_size > 1 ? batch.max_n_kv / block_size : batch.max_n_kv;

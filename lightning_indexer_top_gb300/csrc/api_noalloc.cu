@@ -70,7 +70,9 @@ extern "C" idx_status sparse_attn_decode_noalloc(const void* q, idx_dtype dtype,
                                                  const int32_t* n_sel, float scale, void* out,
                                                  idx_dtype out_dtype, idx_stream_t stream) {
     if (batch.n_seq < 0 || batch.n_q_per_seq < 1 || batch.max_n_kv < 0 || (batch.n_seq > 0 && !batch.n_kv) ||
-        (!batch.kv_start && batch.kv_seq_stride < 0))
+        (!batch.kv_start && batch.kv_seq_stride < 0) ||
+        (batch.page_table && (batch.page_size < 1 || batch.page_table_stride <
+                                                       ((int64_t)batch.max_n_kv + batch.page_size - 1) / batch.page_size)))
         return record_error(IDX_ERR_INVALID_ARG, "sparse_attn_decode_noalloc: invalid batch geometry");
     if (out_dtype != IDX_F32 && out_dtype != IDX_BF16)
         return record_error(IDX_ERR_INVALID_ARG, "sparse_attn_decode_noalloc: out_dtype must be F32 or BF16");

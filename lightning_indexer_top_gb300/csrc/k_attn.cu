@@ -49,7 +49,6 @@ __global__ void __launch_bounds__(kThreads) attn_generic_kernel(
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int b = (int)(r / g.T);
     const int n_kv_b = seq_n_kv(g, b);
-    const int64_t row0 = seq_row0(g, b);
     int ns = n_sel[r];
     if (ns < 0 || ns > idx_row_stride) {
         flag(g.status, IDX_ERR_DEVICE_BOUNDS);
@@ -80,8 +79,9 @@ __global__ void __launch_bounds__(kThreads) attn_generic_kernel(
             int64_t row = -1;
             if (j < ns) {
                 const int pos = idx[r * idx_row_stride + j];
-                if (pos >= 0 && pos < n_kv_b && row0 + pos < kv_rows) {
-                    row = row0 + pos;
+                const int64_t rr = (pos >= 0 && pos < n_kv_b) ? key_row(g, b, pos) : -1;
+                if (rr >= 0 && rr < kv_rows) {
+                    row = rr;
                 } else {
                     flag(g.status, IDX_ERR_DEVICE_BOUNDS);
                 }

@@ -102,7 +102,7 @@ struct Unit {
     int64_t r;        // query row
     int k0, k1;       // selected-key range [k0, k1) of this split
     int n_tiles;
-    int64_t row0;     // cache row of position 0 of the row's sequence
+    int b;            // the row's sequence
     int n_kv;         // keys of the sequence
     int64_t fallback; // an in-bounds cache row for padding keys
 };
@@ -120,8 +120,8 @@ __device__ __forceinline__ Unit make_unit(const Geom& g, const int32_t* n_sel, i
     u.n_tiles = u.k1 > u.k0 ? (u.k1 - u.k0 + kKeys - 1) / kKeys : 0;
     const int b = (int)(u.r / g.T);
     u.n_kv = seq_n_kv(g, b);
-    u.row0 = seq_row0(g, b);
-    int64_t fb = u.row0;
+    u.b = b;
+    int64_t fb = g.page_table ? 0 : seq_row0(g, b);
     if (fb < 0) fb = 0;
     if (fb >= kv_rows) fb = kv_rows - 1;
     u.fallback = fb;
@@ -209,8 +209,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int64_t row = u.fallback;
         if (j < u.k1) {
             const int pos = idx[u.r * idx_row_stride + j];
-            const int64_t rr = u.row0 + pos;
-            if (pos >= 0 && pos < u.n_kv && rr >= 0 && rr < kv_rows) {
+            const int64_t rr = (pos >= 0 && pos < u.n_kv) ? key_row(g, u.b, pos) : -1;
+            if (rr >= 0 && rr < kv_rows) {
                 valid = true;
                 row = rr;
             } else if (rank == 0) {

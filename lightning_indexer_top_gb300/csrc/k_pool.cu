@@ -43,7 +43,6 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(const T* __restrict__ k,
     constexpr int V = 16 / sizeof(T);
     const int tpr = d / V;              // threads per row
     const int rp = kThreads / tpr;      // rows per pass
-    const int64_t row0 = seq_row0(g, b);
     for (int beta = beta0 + (int)blockIdx.x; beta < n_cb; beta += gridDim.x) {
         const int rg = threadIdx.x / tpr, cv = threadIdx.x % tpr;
         float acc[V];
@@ -51,7 +50,7 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(const T* __restrict__ k,
         for (int i = 0; i < V; ++i) acc[i] = 0.f;
         if (rg < rp) {
             for (int t = rg; t < C; t += rp) {
-                const int64_t row = row0 + (int64_t)beta * C + t;
+                const int64_t row = key_row(g, b, (int64_t)beta * C + t);
                 if (row < 0 || row >= k_rows) {
                     flag(g.status, IDX_ERR_DEVICE_BOUNDS);
                     continue;

@@ -40,11 +40,10 @@ __global__ void __launch_bounds__(kTile) score_generic_kernel(
     for (int i = threadIdx.x; i < HH; i += blockDim.x) ws[i] = (i < H) ? w[r * H + i] : 0.f;
     __syncthreads();
 
-    const int64_t row0 = seq_row0(g, b);
     for (int j0 = blockIdx.y * kTile; j0 < n_keys; j0 += gridDim.y * kTile) {
         const int j = j0 + threadIdx.x;
         if (j >= n_keys) continue;
-        const int64_t row = row0 + j;
+        const int64_t row = key_row(g, b, j);
         if (row < 0 || row >= k_rows) {
             flag(g.status, IDX_ERR_DEVICE_BOUNDS);
             continue;

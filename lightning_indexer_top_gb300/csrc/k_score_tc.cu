@@ -108,6 +108,7 @@ struct Ctl {
     uint32_t tmem_base;
     int abort;
     int n_chunks;
+    int32_t pages[16];         // paged caches: the producer's window of page-table entries
 };
 
 static_assert(kStages <= 8 && kRawStages <= 8, "barrier arrays");
@@ -263,7 +264,7 @@ template <typename TK, bool kQ8>
 __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decode_kernel(
     const __grid_constant__ CUtensorMap kmap, const void* __restrict__ q, int q_dtype,
     const float* __restrict__ w, Geom g, float* __restrict__ scores, int64_t score_row_stride, int sched_slot,
-    const float* __restrict__ k_scale) {
+    const float* __restrict__ k_scale, int64_t k_rows) {
     constexpr int kNT = kQ8 ? kThreadsQ8 : kThreads;
     constexpr int kTmaStages = kQ8 ? kRawStages : kStages;   // the producer's ring
     constexpr int kTmaBytes = kQ8 ? kRawTileBytes : kTileBytes;
@@ -356,6 +357,22 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
             // the next chunk is claimed one chunk ahead, so the counter's round
             // trip overlaps the current chunk's loads
             int ch = (int)atomicAdd(&g_score_sched[sched_slot][0], 1u);
+            // paged caches: page-table entries are read 16 at a time (one memory round trip)
+            // into a window, not one dependent load per TMA issue
+            int win_b = -1, win0 = 0;
+            auto page_of = [&](int b, int pg, int last) -> int32_t {
+                if (b != win_b || pg < win0 || pg >= win0 + 16) {
+                    win_b = b;
+                    win0 = pg;
+                    const int64_t base = (int64_t)b * g.page_table_stride;
+                    int32_t e[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) e[i] = pg + i <= last ? g.page_table[base + pg + i] : -1;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) c.pages[i] = e[i];
+                }
+                return c.pages[pg - win0];
+            };
             for (int k = 0;; ++k) {
                 const int slot = k % kRing;
                 if (*(volatile int*)&c.abort || !mbar_wait(&c.cempty[slot], (uint32_t)(((k / kRing) & 1) ^ 1))) {
@@ -367,7 +384,9 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                 mbar_arrive(&c.cfull[slot]);
                 if (d.row < 0) break;
                 ch = (int)atomicAdd(&g_score_sched[sched_slot][0], 1u);
-                const int64_t krow0 = seq_row0(g, (int)(d.row / g.T));
+                const int b_seq = (int)(d.row / g.T);
+                const int64_t krow0 = g.page_table ? 0 : seq_row0(g, b_seq);
+                const int nk = prefix ? nvis[d.row] : row_n_vis(g, d.row);
                 bool ok = true;
                 for (int t = d.t0; t < d.t1; ++t) {
                     if (!mbar_wait(&c.empty[stage], phase ^ 1)) {
@@ -375,14 +394,40 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                         ok = false;
                         break;
                     }
-                    const int64_t krow = krow0 + (int64_t)t * kTileKeys;
                     uint8_t* dst = tma_tiles + (size_t)stage * kTmaBytes;
-                    mbar_arrive_expect_tx(&c.full[stage], kTmaBytes);
-                    if constexpr (kQ8) {
-                        tma_load_2d(dst, &kmap, &c.full[stage], 0, (int32_t)krow);
+                    if (!g.page_table) {
+                        const int64_t krow = krow0 + (int64_t)t * kTileKeys;
+                        // rows past the visible keys may lie past the cache (TMA fills them with 0)
+                        const int valid = min(kTileKeys, nk - t * kTileKeys);
+                        if (krow < 0 || krow + valid > k_rows) flag(g.status, IDX_ERR_DEVICE_BOUNDS);
+                        mbar_arrive_expect_tx(&c.full[stage], kTmaBytes);
+                        if constexpr (kQ8) {
+                            tma_load_2d(dst, &kmap, &c.full[stage], 0, (int32_t)krow);
+                        } else {
+                            tma_load_2d(dst, &kmap, &c.full[stage], 0, (int32_t)krow);
+                            tma_load_2d(dst + kHalfBytes, &kmap, &c.full[stage], 64, (int32_t)krow);
+                        }
                     } else {
-                        tma_load_2d(dst, &kmap, &c.full[stage], 0, (int32_t)krow);
-                        tma_load_2d(dst + kHalfBytes, &kmap, &c.full[stage], 64, (int32_t)krow);
+                        // paged cache: two 64-key halves, each inside one page (page_size % 64 == 0);
+                        // a half past the visible keys is not loaded (its keys are never stored)
+                        const int j0 = t * kTileKeys;
+                        const int halves = j0 + 64 < nk ? 2 : 1;
+                        mbar_arrive_expect_tx(&c.full[stage], (uint32_t)(halves * (kTmaBytes / 2)));
+                        for (int hh = 0; hh < halves; ++hh) {
+                            const int jj = j0 + 64 * hh;
+                            const int pg = jj / g.page_size;
+                            const int64_t kr = (int64_t)page_of(b_seq, pg, (nk - 1) / g.page_size) * g.page_size +
+                                               (jj - pg * g.page_size);
+                            if (kr < 0 || kr + min(64, nk - (j0 + 64 * hh)) > k_rows)
+                                flag(g.status, IDX_ERR_DEVICE_BOUNDS);
+                            if constexpr (kQ8) {
+                                tma_load_2d(dst + hh * (kRawTileBytes / 2), &kmap, &c.full[stage], 0, (int32_t)kr);
+                            } else {
+                                tma_load_2d(dst + hh * (kHalfBytes / 2), &kmap, &c.full[stage], 0, (int32_t)kr);
+                                tma_load_2d(dst + kHalfBytes + hh * (kHalfBytes / 2), &kmap, &c.full[stage], 64,
+                                            (int32_t)kr);
+                            }
+                        }
                     }
                     ++issued;
                     if (++stage == kTmaStages) {
@@ -539,7 +584,8 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
             if (d.row < 0) break;
             if (d.t1 <= d.t0) continue;
             const int n_keys = prefix ? nvis[d.row] : row_n_vis(g, d.row);
-            const int64_t krow0 = kQ8 ? seq_row0(g, (int)(d.row / g.T)) : 0;
+            const int b_seq = (int)(d.row / g.T);
+            const int64_t krow0 = (kQ8 && !g.page_table) ? seq_row0(g, b_seq) : 0;
             const float4* wr = reinterpret_cast<const float4*>(w + d.row * kH);
 #pragma unroll
             for (int h4 = 0; h4 < kH / 4; ++h4) {
@@ -559,7 +605,12 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int j = (g0 + i) * kTileKeys + quad * 32 + lane;
-                        scs[i] = (g0 + i < d.t1 && j < n_keys) ? k_scale[krow0 + j] : 0.f;
+                        float v = 0.f;
+                        if (g0 + i < d.t1 && j < n_keys) {
+                            const int64_t kr = g.page_table ? key_row(g, b_seq, j) : krow0 + j;
+                            if (kr >= 0 && kr < k_rows) v = k_scale[kr];
+                        }
+                        scs[i] = v;
                     }
 #pragma unroll
                     for (int i = 0; i < 8; ++i) esc[i * 32 + lane] = scs[i];
@@ -792,14 +843,28 @@ __global__ void __launch_bounds__(kPThreads, 1) score_tc_prefill_kernel(
             for (int64_t live = blockIdx.x; live < n_live; live += gridDim.x) {
                 const PTile p = ptile_live(pre, n_pairs, pair0, q_tiles, (int)live);
                 const int32_t row0 = (int32_t)((int64_t)p.b * g.T + p.qt * kPQ);
-                const int32_t key0 = (int32_t)(seq_row0(g, p.b) + (int64_t)p.kt * kPK);
                 if (!mbar_wait(&c.kempty, tph ^ 1) || !mbar_wait(&c.wempty, tph ^ 1)) {
                     pc_abort(c, g);
                     break;
                 }
-                mbar_arrive_expect_tx(&c.kfull, kPKBytes);
-                tma_load_2d(ktile, &kmap, &c.kfull, 0, key0);
-                tma_load_2d(ktile + kPKBytes / 2, &kmap, &c.kfull, 64, key0);
+                if (!g.page_table) {
+                    const int32_t key0 = (int32_t)(seq_row0(g, p.b) + (int64_t)p.kt * kPK);
+                    mbar_arrive_expect_tx(&c.kfull, kPKBytes);
+                    tma_load_2d(ktile, &kmap, &c.kfull, 0, key0);
+                    tma_load_2d(ktile + kPKBytes / 2, &kmap, &c.kfull, 64, key0);
+                } else {
+                    // paged cache: 64-key quarters, each inside one page; quarters past the
+                    // sequence's keys are not loaded
+                    const int j0 = p.kt * kPK, nkv = seq_n_kv(g, p.b);
+                    int nq = 0;
+                    while (nq < 4 && j0 + 64 * nq < nkv) ++nq;
+                    mbar_arrive_expect_tx(&c.kfull, (uint32_t)(nq * (kPKBytes / 4)));
+                    for (int i = 0; i < nq; ++i) {
+                        const int32_t kr = (int32_t)key_row(g, p.b, j0 + 64 * i);
+                        tma_load_2d(ktile + i * (kPKBytes / 8), &kmap, &c.kfull, 0, kr);
+                        tma_load_2d(ktile + kPKBytes / 2 + i * (kPKBytes / 8), &kmap, &c.kfull, 64, kr);
+                    }
+                }
                 mbar_arrive_expect_tx(&c.wfull, kPWBytes);
                 tma_load_2d(wt, &wmap, &c.wfull, 0, row0);
                 for (int h = 0; h < kH; ++h) {
@@ -953,7 +1018,9 @@ cudaError_t launch_score_tc_prefill(const void* q, int q_dtype, const float* w, 
     if (n_rows > INT32_MAX || k_rows > INT32_MAX) return cudaErrorNotSupported;
     const bool bf16 = k_dtype == IDX_BF16;
     CUtensorMap qm, km, wm;
-    if (!make_q3d_tmap(&qm, q, bf16, n_rows) || !make_key_tmap(&km, k, bf16, k_row_stride, k_rows, kPK) ||
+    if (g.page_table && g.page_size % 64 != 0) return cudaErrorNotSupported;
+    if (!make_q3d_tmap(&qm, q, bf16, n_rows) ||
+        !make_key_tmap(&km, k, bf16, k_row_stride, k_rows, g.page_table ? 64 : kPK) ||
         !make_w_tmap(&wm, w, n_rows))
         return cudaErrorNotSupported;
     const int q_tiles = (g.T + kPQ - 1) / kPQ;
@@ -1008,14 +1075,15 @@ cudaError_t launch_score_tc_q8(const void* q, int q_dtype, const float* w, const
     const int64_t n_rows = (int64_t)g.B * g.T;
     if (n_rows == 0 || g.max_n_kv == 0) return cudaSuccess;
     CUtensorMap map;
-    if (!make_key8_tmap(&map, k8, k_row_stride, k_rows, kTileKeys)) return cudaErrorNotSupported;
+    if (g.page_table && g.page_size % 64 != 0) return cudaErrorNotSupported;
+    if (!make_key8_tmap(&map, k8, k_row_stride, k_rows, g.page_table ? 64 : kTileKeys)) return cudaErrorNotSupported;
     int grid, slot;
     if (!decode_launch_shape(g, grid, slot)) return cudaErrorNotSupported;
     auto kern = score_tc_decode_kernel<__half, true>;
     constexpr size_t smem = smem_bytes<true>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreadsQ8, smem, st>>>(map, q, q_dtype, w, g, scores, score_row_stride, slot, k_scale);
+    kern<<<grid, kThreadsQ8, smem, st>>>(map, q, q_dtype, w, g, scores, score_row_stride, slot, k_scale, k_rows);
     return cudaGetLastError();
 }
 
@@ -1037,13 +1105,14 @@ cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, i
     if (n_rows == 0 || g.max_n_kv == 0) return cudaSuccess;
     CUtensorMap map;
     const bool bf16 = k_dtype == IDX_BF16;
-    if (!make_key_tmap(&map, k, bf16, k_row_stride, k_rows, kTileKeys)) return cudaErrorNotSupported;
+    if (g.page_table && g.page_size % 64 != 0) return cudaErrorNotSupported;
+    if (!make_key_tmap(&map, k, bf16, k_row_stride, k_rows, g.page_table ? 64 : kTileKeys)) return cudaErrorNotSupported;
     int grid, slot;
     if (!decode_launch_shape(g, grid, slot)) return cudaErrorNotSupported;
     auto kern = bf16 ? score_tc_decode_kernel<__nv_bfloat16, false> : score_tc_decode_kernel<__half, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kSmemBytes, st>>>(map, q, q_dtype, w, g, scores, score_row_stride, slot, nullptr);
+    kern<<<grid, kThreads, kSmemBytes, st>>>(map, q, q_dtype, w, g, scores, score_row_stride, slot, nullptr, k_rows);
     return cudaGetLastError();
 }
 

@@ -23,6 +23,9 @@ struct Geom {
     int64_t kv_seq_stride;
     const int32_t* q_pos;
     int32_t max_n_kv;
+    const int32_t* page_table;   // paged caches (NULL: kv_start / kv_seq_stride)
+    int64_t page_table_stride;
+    int32_t page_size;
     int* status;  // device int: first fault code recorded, 0 = none
 };
 
@@ -52,9 +55,20 @@ __device__ __forceinline__ int row_n_vis(const Geom& g, int64_t r) {
     return n;
 }
 
-// cache row of position 0 of sequence b
+// cache row of position 0 of sequence b (contiguous caches)
 __device__ __forceinline__ int64_t seq_row0(const Geom& g, int b) {
     return g.kv_start ? (int64_t)g.kv_start[b] : (int64_t)b * g.kv_seq_stride;
+}
+
+// cache row of position j of sequence b: through the page table when there is
+// one; a negative page index gives a negative row, which callers reject
+__device__ __forceinline__ int64_t key_row(const Geom& g, int b, int64_t j) {
+    if (g.page_table) {
+        const int64_t pg = j / g.page_size;
+        const int32_t phys = g.page_table[(int64_t)b * g.page_table_stride + pg];
+        return (int64_t)phys * g.page_size + (j - pg * g.page_size);
+    }
+    return seq_row0(g, b) + j;
 }
 
 // ---------------------------------------------------------------------------

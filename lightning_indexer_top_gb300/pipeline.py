@@ -20,7 +20,7 @@ class SparseAttentionStep:
         self.wl = wl
         dev = wl.q_idx.device
         self.batch = Batch(wl.n_kv, wl.T, wl.max_n_kv, kv_start=wl.kv_start, kv_seq_stride=wl.kv_seq_stride,
-                           q_pos=wl.q_pos)
+                           q_pos=wl.q_pos, page_table=wl.page_table, page_size=wl.page_size)
         rows = wl.B * wl.T
         C = wl.block_size
         if C > 1:

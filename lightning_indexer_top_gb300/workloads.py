@@ -54,12 +54,22 @@ class Workload:
     q_pos: Optional[torch.Tensor] = None
     hadamard: bool = False
     block_size: int = 0
+    page_table: Optional[torch.Tensor] = None   # int32 [B, pages]: paged caches (rows of page_size)
+    page_size: int = 0
     k8: Optional[torch.Tensor] = None        # int8 indexer key codes [rows, d] (quantized cache)
     k_scale: Optional[torch.Tensor] = None   # f32 [rows] per-row scales of k8
     extra: Dict = field(default_factory=dict)
 
     def row0(self, b: int) -> int:
         return self.kv_start_host[b] if self.kv_start_host is not None else b * self.kv_seq_stride
+
+    def rows_of(self, b: int, n: int) -> torch.Tensor:
+        """Cache rows of positions 0..n-1 of sequence b (through the page table if paged)."""
+        j = torch.arange(n)
+        if self.page_table is None:
+            return self.row0(b) + j
+        pt = self.page_table[b].cpu().to(torch.int64)
+        return pt[j // self.page_size] * self.page_size + j % self.page_size
 
 
 def _gen(device, seed):
@@ -76,9 +86,12 @@ def _randn(shape, dtype, g, device, std=1.0):
 
 
 def make(cfg, device="cuda", *, n_kv_override=None, batch_override=None, n_tokens_override=None,
-         parity_tails=False, quantized_keys=False) -> Workload:
+         parity_tails=False, quantized_keys=False, page_size=0) -> Workload:
     """Build configuration `cfg` (1-5 or "headline") on `device`.
 
+    page_size: decode caches (indexer keys and latent) are stored in pages of
+    this many rows, in a seeded random page order, addressed through a page
+    table (name suffix "_paged"); 0 keeps them contiguous.
     quantized_keys: also store the decode indexer keys as a quantized cache
     (int8 codes + per-row f32 scales, idx_quantize_rows of the F16 keys); the
     workload's name gets the suffix "_q8" and the scorer reads the codes.
@@ -136,13 +149,29 @@ def make(cfg, device="cuda", *, n_kv_override=None, batch_override=None, n_token
         lat = _randn((rows, dk), torch.bfloat16, g, dev)
         name = {2: "decode_mla_8x8192", 5: "long_decode_mla_ragged", "headline": "decode_mla_64x131072"}[cfg]
         k8 = ks = None
+        table = None
+        if page_size:
+            # logical page L = b * pages + lp goes to physical page perm[L]
+            assert cfg != 5 and max_n_kv % page_size == 0, "paged workloads use equal, page-aligned sequences"
+            pages = max_n_kv // page_size
+            perm = torch.randperm(B * pages, generator=torch.Generator().manual_seed(seed)).to(dev)
+            for name_t in ("k", "lat"):
+                src = k if name_t == "k" else lat
+                dst = torch.empty_like(src)
+                dst.view(B * pages, page_size, -1)[perm] = src.view(B * pages, page_size, -1)
+                if name_t == "k":
+                    k = dst
+                else:
+                    lat = dst
+            table = perm.view(B, pages).to(torch.int32)
+            name += "_paged"
         if quantized_keys:
             from . import idx_quantize_rows
             k8, ks = idx_quantize_rows(k)
             name += "_q8"
         return Workload(name, "decode", B, 1, torch.tensor(n_kv, **i32), n_kv, max_n_kv, top_k, H, d, q, w, k,
                         1 / math.sqrt(192), qa, lat, None, dv, kv_start=kv_start, kv_start_host=starts,
-                        kv_seq_stride=stride, k8=k8, k_scale=ks)
+                        kv_seq_stride=stride, k8=k8, k_scale=ks, page_table=table, page_size=page_size)
 
     if cfg == 3:
         n = n_tokens_override or 16384

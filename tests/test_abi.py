@@ -59,6 +59,11 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert b"capacity" in lib.idx_last_error()
     # block mode capacity = floor(top_k/C)*C + C - 1
     assert lib.idx_topk(None, 16, b, 8, 4, None, 10, None, None, 0, None) == L.IDX_ERR_INVALID_ARG
+    # a page table needs page_size >= 1 and a stride covering max_n_kv
+    pg = L._Batch(1, 1, ctypes.c_void_p(16), None, 0, None, 256, ctypes.c_void_p(32), 4, 0)
+    assert lib.idx_topk(None, 256, pg, 8, 0, None, 8, None, None, 0, None) == L.IDX_ERR_INVALID_ARG
+    pg = L._Batch(1, 1, ctypes.c_void_p(16), None, 0, None, 256, ctypes.c_void_p(32), 3, 64)
+    assert lib.idx_topk(None, 256, pg, 8, 0, None, 8, None, None, 0, None) == L.IDX_ERR_INVALID_ARG
     bad = L._Batch(-1, 1, None, None, 0, None, 0)
     assert lib.idx_score(None, 0, None, 4, 32, None, 0, 32, 0, bad, 0, None, 0, None, 0, None) == L.IDX_ERR_INVALID_ARG
     assert lib.idx_score(None, 0, None, 65, 32, None, 0, 32, 0, b, 0, None, 16, None, 0, None) == L.IDX_ERR_UNSUPPORTED

@@ -51,11 +51,11 @@ def _check_mla_rows(wl, step, rows, k_rot=None, q_rot=None):
     s_gpu = step.scores
     for r in rows:
         b = r // wl.T
-        row0 = wl.row0(b)
         n_kv = wl.n_kv_host[b]
         nv = O.visible_count(n_kv, None if wl.q_pos is None else r % wl.T)
+        krows = wl.rows_of(b, nv).numpy()         # position order (through the page table if paged)
         q = np64(wl.q_idx[r]) if q_rot is None else q_rot(r)
-        s_ref = O.indexer_scores(q, np64(wl.w[r]), kh[row0:row0 + nv])
+        s_ref = O.indexer_scores(q, np64(wl.w[r]), kh[krows])
         assert_scores_close(s_gpu[r, :nv].cpu().numpy(), s_ref, f"{wl.name} row {r}")
         sel_ref = O.topk_select(s_ref, nv, wl.top_k)
         ns = int(step.n_sel[r])
@@ -64,7 +64,7 @@ def _check_mla_rows(wl, step, rows, k_rot=None, q_rot=None):
         same, jac = check_selection(sel_gpu, sel_ref, s_ref, f"{wl.name} row {r}")
         ident.append((same, jac))
         if same:
-            lat_rows = np64(lat[row0:row0 + nv])
+            lat_rows = np64(lat[torch.as_tensor(krows, device=lat.device)])
             ref = O.sparse_attention_mla(np64(wl.q_attn[r]), lat_rows, sel_ref, wl.scale, wl.dv)
             err = np.max(np.abs(np64(step.out[r]) - ref))
             assert err <= 2e-2, f"{wl.name} row {r}: attention max-abs {err}"
@@ -221,3 +221,11 @@ def test_headline_decode_64x131072_sampled_rows():
     step = _run(wl)
     ident = _check_mla_rows(wl, step, [0, 31, 63])
     _report(wl.name, ident)
+
+
+def test_paged_decode_workload_sampled_rows():
+    # the headline geometry at 8192 keys with both caches in shuffled 64-row pages
+    wl = workloads.make("headline", n_kv_override=8192, batch_override=6, page_size=64)
+    assert wl.page_table is not None and wl.name.endswith("_paged")
+    st = _run(wl)
+    _report("paged", _check_mla_rows(wl, st, [0, 3, 5]))

@@ -624,3 +624,121 @@ def test_score_q8_selection_matches_oracle_at_128k():
     assert_scores_close(s[1].cpu().numpy(), ref, "row 1")
     from _helpers import check_selection
     check_selection(idx[1, :int(ns[1])].cpu().numpy(), O.topk_select(ref, n, 2048), ref, "q8 row 1")
+
+
+# ------------------------------------------------------------------ paged caches (cell -> position maps)
+
+def _page(g, keys_per_seq, P, spare=7):
+    """Scatter per-sequence rows (lists of [n, ...] tensors) into shuffled pages of P rows.
+    Returns (paged rows, page_table [B, pages] int32 CUDA)."""
+    B = len(keys_per_seq)
+    pages = max((k.shape[0] + P - 1) // P for k in keys_per_seq)
+    n_phys = B * pages + spare
+    perm = torch.randperm(n_phys, generator=g)
+    table = perm[:B * pages].view(B, pages).to(torch.int32)
+    shape = (n_phys * P,) + tuple(keys_per_seq[0].shape[1:])
+    rows = torch.zeros(shape, dtype=keys_per_seq[0].dtype, device=DEV)
+    for b, k in enumerate(keys_per_seq):
+        for lp in range((k.shape[0] + P - 1) // P):
+            seg = k[lp * P:(lp + 1) * P]
+            ph = int(table[b, lp])
+            rows[ph * P:ph * P + seg.shape[0]] = seg
+    return rows, table.to(DEV)
+
+
+@pytest.mark.parametrize("P", [64, 256])
+def test_paged_decode_path_is_bit_identical_to_contiguous(P):
+    # scores (F16 keys and int8 keys), selection and MLA attention read the same key rows
+    # in the same order whichever way the cache is laid out
+    g = torch.Generator().manual_seed(91)
+    n_kv = [3000, 129, 64, 5000]
+    B = len(n_kv)
+    gd = torch.Generator(device=DEV).manual_seed(92)
+    keys = [torch.randn(n, 128, generator=gd, device=DEV).to(torch.float16) for n in n_kv]
+    lats = [torch.randn(n, 576, generator=gd, device=DEV).to(torch.bfloat16) for n in n_kv]
+    q = torch.randn(B, 64, 128, generator=gd, device=DEV).to(torch.bfloat16)
+    w = torch.randn(B, 64, generator=gd, device=DEV) / 8
+    qa = torch.randn(B, 128, 576, generator=gd, device=DEV).to(torch.bfloat16)
+    starts = [0]
+    for n in n_kv[:-1]:
+        starts.append(starts[-1] + n)
+    kc, lc = torch.cat(keys), torch.cat(lats)
+    contig = L.Batch(_i32(n_kv), 1, max(n_kv), kv_start=_i32(starts))
+    kp, table = _page(g, keys, P)
+    lp, table2 = _page(torch.Generator().manual_seed(91), lats, P)
+    assert torch.equal(table, table2)
+    paged = L.Batch(_i32(n_kv), 1, max(n_kv), page_table=table, page_size=P)
+    s_c = L.idx_score(q, w, kc, contig)
+    s_p = L.idx_score(q, w, kp, paged)
+    k8c, scc = L.idx_quantize_rows(kc)
+    k8p, scp = L.idx_quantize_rows(kp)
+    q8_c = L.idx_score_q8(q, w, k8c, scc, contig)
+    q8_p = L.idx_score_q8(q, w, k8p, scp, paged)
+    idx_c, ns_c = L.idx_topk(s_c, contig, 2048)
+    idx_p, ns_p = L.idx_topk(s_p, paged, 2048)
+    o_c = L.sparse_attn_decode(qa, lc, None, contig, idx_c, ns_c, 1 / math.sqrt(192), dv=512)
+    o_p = L.sparse_attn_decode(qa, lp, None, paged, idx_p, ns_p, 1 / math.sqrt(192), dv=512)
+    torch.cuda.synchronize()
+    for b, n in enumerate(n_kv):
+        assert torch.equal(s_c[b, :n], s_p[b, :n]), b
+        assert torch.equal(q8_c[b, :n], q8_p[b, :n]), b
+    assert torch.equal(idx_c, idx_p) and torch.equal(ns_c, ns_p)
+    assert torch.equal(o_c, o_p)
+    ref = O.indexer_scores(np64(q[3]), np64(w[3]), np64(keys[3]))
+    assert_scores_close(s_p[3, :n_kv[3]].cpu().numpy(), ref, "paged row 3")
+
+
+def test_paged_generic_paths_match_oracle():
+    # page size 48 (not a multiple of 64) and 32 heads: CUDA-core scorer, pool and GQA attention
+    g = torch.Generator().manual_seed(93)
+    gd = torch.Generator(device=DEV).manual_seed(94)
+    P, C = 48, 16
+    n_kv = [700, 47, 200]
+    B = len(n_kv)
+    keys = [torch.randn(n, 64, generator=gd, device=DEV).to(torch.bfloat16) for n in n_kv]
+    kv = [torch.randn(n, 2, 64, generator=gd, device=DEV).to(torch.bfloat16) for n in n_kv]
+    vv = [torch.randn(n, 2, 64, generator=gd, device=DEV).to(torch.bfloat16) for n in n_kv]
+    kp, table = _page(g, keys, P)
+    Kp, _ = _page(torch.Generator().manual_seed(93), kv, P)
+    Vp, _ = _page(torch.Generator().manual_seed(93), vv, P)
+    paged = L.Batch(_i32(n_kv), 1, max(n_kv), page_table=table, page_size=P)
+    q = torch.randn(B, 32, 64, generator=gd, device=DEV).to(torch.bfloat16)
+    w = torch.randn(B, 32, generator=gd, device=DEV) / 8
+    s = L.idx_score(q, w, kp, paged)
+    pooled = L.idx_block_pool(kp, paged, C)
+    qa = torch.randn(B, 8, 64, generator=gd, device=DEV).to(torch.bfloat16)
+    sel = torch.full((B, 64), -1, dtype=torch.int32)
+    sizes = []
+    for b, n in enumerate(n_kv):
+        m = min(n, 64)
+        sel[b, :m] = torch.randperm(n, generator=g)[:m].to(torch.int32)
+        sizes.append(m)
+    out = L.sparse_attn_decode(qa, Kp, Vp, paged, sel.to(DEV), _i32(sizes), 0.125, dv=64, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    for b, n in enumerate(n_kv):
+        ref = O.indexer_scores(np64(q[b]), np64(w[b]), np64(keys[b]))
+        assert_scores_close(s[b, :n].cpu().numpy(), ref, f"seq {b}")
+        np.testing.assert_allclose(pooled[b, :n // C].cpu().numpy(), O.block_pool(np64(keys[b]), C, n),
+                                   rtol=1e-5, atol=1e-6)
+        ro = O.sparse_attention_gqa(np64(qa[b]), np64(kv[b]), np64(vv[b]), sel[b, :sizes[b]].numpy(), 0.125)
+        assert np.max(np.abs(out[b].cpu().numpy() - ro)) <= 1e-4
+
+
+def test_paged_prefill_scores_match_contiguous():
+    # causal prefill on the tensor cores: 64-row page pieces of the 256-key tiles
+    g = torch.Generator().manual_seed(95)
+    gd = torch.Generator(device=DEV).manual_seed(96)
+    T, P = 700, 128
+    k = torch.randn(T, 128, generator=gd, device=DEV).to(torch.bfloat16)
+    q = torch.randn(T, 64, 128, generator=gd, device=DEV).to(torch.bfloat16)
+    w = torch.randn(T, 64, generator=gd, device=DEV) / 8
+    kp, table = _page(g, [k], P)
+    qp = _i32(list(range(T)))
+    contig = L.Batch(_i32([T]), T, T, kv_seq_stride=T, q_pos=qp)
+    paged = L.Batch(_i32([T]), T, T, q_pos=qp, page_table=table, page_size=P)
+    s_c = torch.full((T, T), 9.0, device=DEV)
+    s_p = torch.full((T, T), 9.0, device=DEV)
+    L.idx_score(q, w, k, contig, scores=s_c)
+    L.idx_score(q, w, kp, paged, scores=s_p)
+    torch.cuda.synchronize()
+    assert torch.equal(s_c, s_p)
