@@ -625,13 +625,22 @@ __global__ void __launch_bounds__(kMcThreads) topk_mc_bound_kernel(const float* 
     for (int i = threadIdx.x; i < 2048; i += kMcThreads) hist[i] = 0u;
     __syncthreads();
     const float* s = scores + r * score_row_stride;
-    // sample: kSampleBlocks blocks of kSampleLen consecutive scores, evenly spread
+    // sample: kSampleBlocks blocks of kSampleLen consecutive scores, evenly spread;
+    // each thread loads all of its sample keys at once (one memory round trip) and
+    // keeps them for the refinement pass
+    constexpr int kPerThread = kSampleBlocks * kSampleLen / kMcThreads;   // 32
     const int64_t span = n - kSampleLen;
-    for (int i = threadIdx.x; i < kSampleBlocks * kSampleLen; i += kMcThreads) {
+    uint32_t keys[kPerThread];
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+        const int i = threadIdx.x + k * kMcThreads;
         const int blk = i / kSampleLen, off = i % kSampleLen;
-        const int p = (int)(span * blk / (kSampleBlocks - 1)) + off;
-        atomicAdd(&hist[order_key(s[p]) >> 21], 1u);
+        int p = (int)(span * blk / (kSampleBlocks - 1)) + off;
+        p = p < 0 ? 0 : (p >= n ? n - 1 : p);   // rows shorter than one sample block
+        keys[k] = order_key(s[p]);
     }
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) atomicAdd(&hist[keys[k] >> 21], 1u);
     __syncthreads();
     // expected keys per sample above the threshold: K * samples / n; aim for twice that
     const int64_t est = ((int64_t)2 * K * kSampleBlocks * kSampleLen + n - 1) / n + 1;
@@ -641,12 +650,9 @@ __global__ void __launch_bounds__(kMcThreads) topk_mc_bound_kernel(const float* 
     const uint32_t b1 = sb[0], need2 = want - sb[1];
     for (int i = threadIdx.x; i < 2048; i += kMcThreads) hist[i] = 0u;
     __syncthreads();
-    for (int i = threadIdx.x; i < kSampleBlocks * kSampleLen; i += kMcThreads) {
-        const int blk = i / kSampleLen, off = i % kSampleLen;
-        const int p = (int)(span * blk / (kSampleBlocks - 1)) + off;
-        const uint32_t key = order_key(s[p]);
-        if ((key >> 21) == b1) atomicAdd(&hist[(key >> 10) & 2047u], 1u);
-    }
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k)
+        if ((keys[k] >> 21) == b1) atomicAdd(&hist[(keys[k] >> 10) & 2047u], 1u);
     __syncthreads();
     mc_find_bin(hist, need2, &sb[0], &sb[1], scratch);
     if (threadIdx.x == 0) L.bound[r] = (b1 << 21) | (sb[0] << 10);

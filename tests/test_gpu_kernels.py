@@ -140,6 +140,21 @@ def test_topk_bit_exact(case, top_k, path):
         assert np.all(idx_h[r, len(ref):] == -1)
 
 
+def test_topk_multi_cta_path_with_rows_shorter_than_a_sample_block():
+    # the few-long-rows path is chosen by max_n_kv; single rows in it may be tiny (n < 128)
+    g = torch.Generator().manual_seed(44)
+    n_kv = [40000, 100, 20, 129, 3]
+    n = max(n_kv)
+    scores = torch.randint(-4, 5, (len(n_kv), n), generator=g).float()
+    batch = L.Batch(_i32(n_kv), 1, n, kv_seq_stride=0)
+    for top_k in (5, 64):
+        idx, n_sel = L.idx_topk(scores.to(DEV), batch, top_k)
+        torch.cuda.synchronize()
+        for r, nv in enumerate(n_kv):
+            ref = O.topk_select(scores[r].numpy(), nv, top_k)
+            assert int(n_sel[r]) == len(ref) and idx[r, :len(ref)].tolist() == ref.tolist(), (top_k, r)
+
+
 @pytest.mark.parametrize("path", ["multi", "single"])
 def test_topk_causal_rows_and_dense_short_rows(path):
     g = torch.Generator().manual_seed(42)
