@@ -164,7 +164,6 @@ cudaError_t launch_attn_mla_tc(const void* q, const void* lat, int64_t kv_row_st
 
 // TMA tensor maps over 16-bit caches (128-byte swizzle); false if encoding fails
 bool make_key_tmap(CUtensorMap* m, const void* k, bool bf16, int64_t k_row_stride, int64_t k_rows, int box_rows);
-bool make_latent_tmap(CUtensorMap* m, const void* lat, int64_t row_stride, int64_t rows);
 bool make_q3d_tmap(CUtensorMap* m, const void* q, bool bf16, int64_t rows);
 bool make_w_tmap(CUtensorMap* m, const float* w, int64_t rows);
 // [rows, 128] int8 keys: boxes of 128 bytes x box_rows rows, no swizzle

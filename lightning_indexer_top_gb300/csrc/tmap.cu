@@ -83,9 +83,5 @@ bool make_key8_tmap(CUtensorMap* m, const int8_t* k, int64_t row_bytes, int64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows, 576] bf16 latent cache for row gathers: boxes of 64 columns x 1 row, 128-byte swizzle
-bool make_latent_tmap(CUtensorMap* m, const void* lat, int64_t row_stride, int64_t rows) {
-    return encode_2d(m, lat, true, 576, (uint64_t)rows, (uint64_t)row_stride * 2, 64, 1);
-}
 
 }  // namespace lidx
