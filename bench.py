@@ -250,9 +250,12 @@ def main():
     stream = torch.cuda.current_stream()
 
     # per-kernel events: (rotate) / score / select / attend of every timed step
+    rotates = step.q_rot is not None
+
     def timed_step(ev):
-        ev[0].record(stream)
-        if step.q_rot is not None:
+        # one event between consecutive kernels (a rotate event only when there is a rotation)
+        if rotates:
+            ev[0].record(stream)
             step.rotate()
         ev[1].record(stream)
         step.score()
@@ -289,7 +292,7 @@ def main():
         raise RuntimeError(f"device status {status} during the timed region")
 
     ms_total = t_start.elapsed_time(t_end)
-    ms_rotate = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ms_rotate = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) if rotates else 0.0
     ms_score = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     ms_select = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     ms_attend = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
