@@ -1,6 +1,6 @@
 """Comparison helpers shared by the GPU parity tests.
 
-Tolerances (from the arithmetic):
+Tolerances (derived from the arithmetic):
   * scores: |s_gpu - s_ref| <= 1e-3 * max(|s_ref|, 1e-2 * max_row |s_ref|)
     (the pages' 1e-3 relative agreement, with a floor for scores that cancel
     to near zero: f32 accumulation error scales with the row's magnitude, not
