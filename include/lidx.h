@@ -90,6 +90,9 @@ typedef enum idx_dtype {
  *                  of 64 keeps the tensor-core scorers; other sizes run on the
  *                  CUDA cores).
  */
+/* top_k = -1 selects this (see idx_topk) */
+#define IDX_DEFAULT_TOP_K 2048
+
 typedef struct idx_batch {
     int32_t n_seq;
     int32_t n_q_per_seq;
@@ -231,6 +234,10 @@ idx_status idx_block_pool_update(const void* k_raw, idx_dtype k_dtype, int64_t k
 
 /*
  * idx_topk -- per-row selection, positions ascending.
+ * top_k = -1 means the model's configured indexer top_k ("GLM-DSA: convert
+ *   sparse-attention control from env vars to CLI args": dsa_top_k default -1
+ *   == the model's indexer_top_k), IDX_DEFAULT_TOP_K = 2048 for the models the
+ *   pages run; idx_workspace_size maps -1 the same way.
  * Token mode (block_size 0 or 1): K = min(top_k, n_vis(r)) positions with
  *   the largest scores; equal scores: the lower position wins; -0 == +0.
  *   ("ggml_top_k(min(top_k, n_tokens))", ik_llama.cpp PR #2058.)

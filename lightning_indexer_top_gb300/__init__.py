@@ -165,8 +165,13 @@ class Batch:
                       self.page_size if self.page_table is not None else 0)
 
 
+IDX_DEFAULT_TOP_K = 2048   # top_k = -1: the model's configured indexer top_k
+
+
 def topk_capacity(top_k: int, block_size: int = 0) -> int:
-    """Row capacity idx_topk writes: top_k, or floor(top_k/C)*C + C - 1 in block mode."""
+    """Row capacity idx_topk writes: top_k, or floor(top_k/C)*C + C - 1 in block mode (-1: the default)."""
+    if top_k == -1:
+        top_k = IDX_DEFAULT_TOP_K
     if block_size > 1:
         return (top_k // block_size) * block_size + block_size - 1
     return top_k

@@ -318,7 +318,8 @@ idx_status idx_topk(const float* scores, int64_t score_row_stride, idx_batch bat
     const char* what = "idx_topk";
     idx_status s = check_batch(batch, what);
     if (s != IDX_OK) return s;
-    if (top_k < 1) return fail(IDX_ERR_INVALID_ARG, "%s: top_k < 1", what);
+    if (top_k == -1) top_k = IDX_DEFAULT_TOP_K;   // the model's configured indexer top_k
+    if (top_k < 1) return fail(IDX_ERR_INVALID_ARG, "%s: top_k < 1 (or -1 for the default)", what);
     if (block_size < 0) return fail(IDX_ERR_INVALID_ARG, "%s: block_size < 0", what);
     const bool blocks = block_size > 1;
     const int64_t cap = blocks ? (int64_t)(top_k / block_size) * block_size + block_size - 1 : top_k;
@@ -364,6 +365,7 @@ idx_status sparse_attn_prefill(const void* q, idx_dtype dtype, int32_t n_q_heads
 size_t idx_workspace_size(int32_t op, int64_t n_rows, int32_t max_n_kv, int32_t top_k,
                           int32_t n_q_heads, int32_t dv) {
     (void)max_n_kv;
+    if (top_k == -1) top_k = IDX_DEFAULT_TOP_K;
     if (n_rows <= 0 || top_k <= 0) return 0;
     if ((op == IDX_OP_ATTN_DECODE || op == IDX_OP_ATTN_PREFILL) && n_q_heads == 128 && dv == 512)
         return mla_workspace_bytes(n_rows, top_k);

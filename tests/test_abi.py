@@ -93,3 +93,11 @@ def test_empty_batch_is_a_no_op(lib):
 
 def test_workspace_size_is_pure_host(lib):
     assert lib.idx_workspace_size(99, -5, -1, 0, 0, 0) == 0
+
+
+def test_default_top_k_minus_one(lib):
+    # -1 is the model's configured indexer top_k (2048) for sizing as for selection
+    for rows in (8, 64, 1000):
+        assert lib.idx_workspace_size(L.IDX_OP_TOPK, rows, 131072, -1, 0, 0) == \
+            lib.idx_workspace_size(L.IDX_OP_TOPK, rows, 131072, 2048, 0, 0)
+    assert L.topk_capacity(-1) == 2048

@@ -140,6 +140,16 @@ def test_topk_bit_exact(case, top_k, path):
         assert np.all(idx_h[r, len(ref):] == -1)
 
 
+def test_topk_default_minus_one_equals_2048():
+    g = torch.Generator().manual_seed(45)
+    scores = torch.randn(3, 40000, generator=g).to(DEV)
+    batch = L.Batch(_i32([40000, 3000, 1000]), 1, 40000, kv_seq_stride=0)
+    a, na = L.idx_topk(scores, batch, -1)
+    b, nb = L.idx_topk(scores, batch, 2048)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(na, nb)
+
+
 def test_topk_multi_cta_path_with_rows_shorter_than_a_sample_block():
     # the few-long-rows path is chosen by max_n_kv; single rows in it may be tiny (n < 128)
     g = torch.Generator().manual_seed(44)
