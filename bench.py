@@ -168,13 +168,15 @@ def cpu_oracle_queries(wl, rows):
     import numpy as np
     import torch
     import oracle as O
+    import lightning_indexer_top_gb300 as L
     sels = {}
     inputs = []
     for r in rows:
         row0, n = wl.row0(r), wl.n_kv_host[r]
         rows = wl.rows_of(r, n).to(wl.k_idx.device)   # position order (through the page table if paged)
         if wl.k8 is not None:   # the quantized cache as it represents the keys
-            keys = O.dequantize_rows(wl.k8[rows].cpu().numpy(), wl.k_scale[rows].cpu().numpy())
+            sc = wl.k_scale[rows] if wl.k_scale is not None else L.inline_scales(wl.k8[rows], wl.d)
+            keys = O.dequantize_rows(wl.k8[rows][:, :wl.d].cpu().numpy(), sc.cpu().numpy())
         else:
             keys = wl.k_idx[rows].to("cpu", torch.float64).numpy()
         inputs.append((r, wl.q_idx[r].to("cpu", torch.float64).numpy(), wl.w[r].to("cpu", torch.float64).numpy(),
@@ -368,7 +370,8 @@ def main():
                     "algorithmic_flops_per_launch": flops}
     else:
         n_kv_total = sum(wl.n_kv_host)
-        # bytes of one cached key: 2 per element (F16), or 1 per element + a 4-byte scale (int8 cache)
+        # bytes of one cached key: 2 per element (F16), or 1 per element + a 4-byte scale (int8 cache;
+        # the inline layout's 12 bytes of row padding are not counted)
         key_bytes = n_kv_total * (wl.d * 2 if wl.k8 is None else wl.d + 4)
         # scorer's algorithmic bytes per launch: every key row read once, one f32 score written per
         # key, the queries and weights read once

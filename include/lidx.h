@@ -163,7 +163,9 @@ idx_status idx_score(const void* q, idx_dtype q_dtype, const float* w, int32_t n
  * so x ~= scale[r] * q8[r, c] with |error| <= scale/2.
  *   x          device [n_rows] rows of d elements at x + r*x_row_stride, x_dtype.
  *   q8         device int8, row r at q8 + r*q8_row_stride (bytes).
- *   scale      device f32 [n_rows].
+ *   scale      device f32 [n_rows], or NULL: each row's scale is stored inline
+ *              in bytes d .. d+3 of its code row (d % 4 == 0, q8_row_stride
+ *              >= d + 4; for d = 128 a 144-byte row keeps TMA alignment).
  * Errors: INVALID_ARG for NULL pointers with n_rows > 0, d < 1 or d > 1024,
  * strides < d, or q8 / q8_row_stride not 16-byte aligned.
  */
@@ -177,7 +179,9 @@ idx_status idx_quantize_rows(const void* x, idx_dtype x_dtype, int64_t n_rows, i
  * "GLM-DSA: allow for quantized indexer cache"; the score itself as in
  * idx_score).  A key row costs d + 4 bytes instead of 2d.
  *   k8         device int8 key rows, row i at k8 + i*k_row_stride (bytes).
- *   k_scale    device f32, k_scale[i] for cache row i (any sign).
+ *   k_scale    device f32, k_scale[i] for cache row i (any sign), or NULL for
+ *              inline scales (bytes head_dim .. head_dim+3 of each row, as
+ *              idx_quantize_rows writes them with scale NULL).
  *   other arguments as idx_score (block_size 0/1 only).
  * H = 64, d = 128 decode rows (T = 1) with f16 or bf16 q run on the tensor
  * cores: the int8 codes are widened exactly to f16 in shared memory, q is

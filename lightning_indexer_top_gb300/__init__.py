@@ -23,7 +23,7 @@ from ._build import build  # noqa: F401
 
 __all__ = [
     "Batch", "LidxError", "build", "load", "idx_hadamard", "idx_score", "idx_block_pool", "idx_block_pool_update",
-    "idx_quantize_rows", "idx_score_q8",
+    "idx_quantize_rows", "idx_score_q8", "inline_scales",
     "idx_topk", "sparse_attn_decode", "sparse_attn_prefill", "idx_workspace_size",
     "idx_device_status", "topk_capacity", "sparse_attn_decode_noalloc",
 ]
@@ -227,10 +227,19 @@ def idx_block_pool(k_raw: torch.Tensor, batch: Batch, block_size: int, *, pool_s
 
 
 def idx_quantize_rows(x: torch.Tensor, *, q8: Optional[torch.Tensor] = None,
-                      scale: Optional[torch.Tensor] = None):
-    """Per-row int8 codes and f32 scales of key rows [n, d]: x ~= scale[:, None] * q8."""
+                      scale: Optional[torch.Tensor] = None, inline_scale: bool = False):
+    """Per-row int8 codes and f32 scales of key rows [n, d]: x ~= scale[:, None] * q8.
+
+    inline_scale: each row's scale is stored in bytes d .. d+3 of its code row (rows of
+    ceil((d + 4) / 16) * 16 bytes); returns (rows [n, that width] int8, None)."""
     _need_cuda(x, q8, scale)
     n, d = x.shape[0], x.shape[-1]
+    if inline_scale:
+        if q8 is None:
+            q8 = torch.empty(n, (d + 4 + 15) // 16 * 16, device=x.device, dtype=torch.int8)
+        _check(load().idx_quantize_rows(_ptr(x), _dtype(x), n, d, x.stride(0), _ptr(q8), q8.stride(0), None,
+                                        _stream(x.device)))
+        return q8, None
     if q8 is None:
         q8 = torch.empty(n, (d + 15) // 16 * 16, device=x.device, dtype=torch.int8)[:, :d]
     if scale is None:
@@ -240,9 +249,15 @@ def idx_quantize_rows(x: torch.Tensor, *, q8: Optional[torch.Tensor] = None,
     return q8, scale
 
 
-def idx_score_q8(q: torch.Tensor, w: torch.Tensor, k8: torch.Tensor, k_scale: torch.Tensor, batch: Batch, *,
-                 scores: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Indexer scores over an int8 key cache with per-row scales (f32 [rows, keys])."""
+def inline_scales(rows: torch.Tensor, d: int) -> torch.Tensor:
+    """The f32 scales stored inline (bytes d .. d+3) in int8 code rows written with inline_scale."""
+    return rows[:, d:d + 4].contiguous().view(torch.float32).view(-1)
+
+
+def idx_score_q8(q: torch.Tensor, w: torch.Tensor, k8: torch.Tensor, k_scale: Optional[torch.Tensor],
+                 batch: Batch, *, scores: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Indexer scores over an int8 key cache with per-row scales (f32 [rows, keys]);
+    k_scale None: the scales are inline in the rows (idx_quantize_rows(..., inline_scale=True))."""
     _need_cuda(q, w, k8, k_scale, scores)
     H, d = q.shape[-2], q.shape[-1]
     rows = batch.n_rows

@@ -229,9 +229,11 @@ idx_status idx_quantize_rows(const void* x, idx_dtype x_dtype, int64_t n_rows, i
     if (d < 1 || d > 1024) return fail(IDX_ERR_INVALID_ARG, "%s: d must be in [1, 1024]", what);
     if (x_row_stride < d || q8_row_stride < d) return fail(IDX_ERR_INVALID_ARG, "%s: row stride < d", what);
     if (n_rows == 0) return IDX_OK;
-    if (!x || !q8 || !scale) return fail(IDX_ERR_INVALID_ARG, "%s: NULL x/q8/scale", what);
+    if (!x || !q8) return fail(IDX_ERR_INVALID_ARG, "%s: NULL x/q8", what);
     if (!aligned16(q8) || q8_row_stride % 16 != 0)
         return fail(IDX_ERR_INVALID_ARG, "%s: q8 / q8_row_stride not 16-byte aligned", what);
+    if (!scale && (d % 4 != 0 || q8_row_stride < d + 4))
+        return fail(IDX_ERR_INVALID_ARG, "%s: inline scales need d %% 4 == 0 and q8_row_stride >= d + 4", what);
     return from_cuda(launch_quantize_rows(x, x_dtype, n_rows, d, x_row_stride, q8, q8_row_stride, scale,
                                           (cudaStream_t)stream),
                      what);
@@ -259,8 +261,10 @@ idx_status idx_score_q8(const void* q, idx_dtype q_dtype, const float* w, int32_
         return fail(IDX_ERR_INVALID_ARG, "%s: score_row_stride < keys per row", what);
     const int64_t rows = (int64_t)batch.n_seq * batch.n_q_per_seq;
     if (rows == 0 || batch.max_n_kv == 0) return IDX_OK;
-    if (!q || !w || !k8 || !k_scale || !scores)
-        return fail(IDX_ERR_INVALID_ARG, "%s: NULL q/w/k8/k_scale/scores", what);
+    if (!q || !w || !k8 || !scores) return fail(IDX_ERR_INVALID_ARG, "%s: NULL q/w/k8/scores", what);
+    if (!k_scale && (head_dim % 4 != 0 || k_row_stride < head_dim + 4 || k_row_stride % 4 != 0))
+        return fail(IDX_ERR_INVALID_ARG, "%s: inline scales need head_dim %% 4 == 0 and a row stride >= head_dim + 4",
+                    what);
     const Geom g = make_geom(batch);
     const cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = cudaErrorNotSupported;

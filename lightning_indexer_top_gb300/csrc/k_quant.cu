@@ -3,7 +3,9 @@
 // commit log):
 //     scale[r] = max_c |x[r, c]| / 127,   q8[r, c] = clamp(rint(x[r, c] / scale[r]), -127, 127)
 // in f32 with IEEE round-to-nearest-even division (so a CPU in f32 takes the
-// same integer decisions).  One warp per row; a cache-write op, off the scan.
+// same integer decisions).  The scale goes to its own array, or (scale NULL)
+// into bytes d .. d+3 of the code row.  One warp per row; a cache-write op,
+// off the scan.
 #include "lidx_internal.cuh"
 
 namespace lidx {
@@ -30,7 +32,10 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_rows_kernel(const T* __r
         if (s > 0.f) v = fminf(fmaxf(rintf(__fdiv_rn(to_f32(xr[c]), s)), -127.f), 127.f);
         qr[c] = (int8_t)(int)v;
     }
-    if (lane == 0) scale[r] = s;
+    if (lane == 0) {
+        if (scale) scale[r] = s;
+        else *reinterpret_cast<float*>(qr + d) = s;   // inline: the row's bytes d .. d+3
+    }
 }
 
 }  // namespace

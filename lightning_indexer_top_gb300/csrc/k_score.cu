@@ -68,7 +68,9 @@ __global__ void __launch_bounds__(kTile) score_generic_kernel(
             }
         }
         // quantized keys: the dot with the dequantized key is scale * (dot with the codes)
-        const float ks = k_scale ? k_scale[row] : 1.f;
+        float ks = 1.f;
+        if constexpr (sizeof(TK) == 1)   // int8 codes: scale array, or inline after the row's d codes
+            ks = k_scale ? k_scale[row] : *reinterpret_cast<const float*>(kr + d);
         float s = 0.f;
 #pragma unroll
         for (int h = 0; h < HH; ++h) s = fmaf(ws[h], fmaxf(ks * acc[h], 0.f), s);
@@ -121,6 +123,7 @@ cudaError_t launch_score_generic(const void* q, int q_dtype, const float* w, int
         case IDX_F16:
             return run(q, q_dtype, w, H, d, static_cast<const __half*>(k), k_row_stride, k_rows, g,
                        block_size, scores, score_row_stride, st, nullptr);
+        // (k_scale NULL with int8 keys: the scale is stored inline after each row's codes)
         case IDX_BF16:
             return run(q, q_dtype, w, H, d, static_cast<const __nv_bfloat16*>(k), k_row_stride,
                        k_rows, g, block_size, scores, score_row_stride, st, nullptr);

@@ -78,7 +78,9 @@ constexpr int kThreadsQ8 = 352;                      // int8 keys: + 4 converter
 #endif
 constexpr int kRawStages = LIDX_Q8_RAW_STAGES;       // int8 keys: TMA ring of 16 KB code tiles
 constexpr int kConvStages = LIDX_Q8_CONV_STAGES;     // int8 keys: widened tiles for the MMA
-constexpr int kRawTileBytes = kTileKeys * kD;        // 16 KB
+constexpr int kRawPitchInline = kD + 16;             // int8 rows with their scale inline: 128 codes + f32 + pad
+constexpr int kRawTileBytes = kTileKeys * kRawPitchInline;   // 18 KB stage (16 KB used without inline scales)
+constexpr int kSRing = 8;                            // int8 keys, inline scales: tiles of scales in flight
 constexpr int kChunkTiles = LIDX_SCORE_CHUNK;        // key tiles (32 KB each) per chunk
 constexpr int kRing = 4;                             // chunk descriptors in flight
 #ifndef LIDX_SCORE_QBUFS
@@ -97,6 +99,8 @@ struct Ctl {
     uint64_t empty[8];
     uint64_t afull[kConvStages];   // int8 keys: widened tile written
     uint64_t aempty[kConvStages];  // int8 keys: widened tile read by the MMAs
+    uint64_t sfull[kSRing];        // int8 keys, inline scales: a tile's scales staged by the converters
+    uint64_t sempty[kSRing];       // ... and read by the epilogue
     uint64_t tfull[kAcc];
     uint64_t tempty[kAcc];
     uint64_t qfull[kQBufs];
@@ -118,7 +122,7 @@ constexpr size_t smem_bytes() {
     return 1024 + (Q8 ? (size_t)kRawStages * kRawTileBytes + (size_t)kConvStages * kTileBytes
                       : (size_t)kStages * kTileBytes) +
            kQBufs * kQBytes + sizeof(Ctl) + (2 * kMaxPrefixRows + 1) * sizeof(int) +
-           (Q8 ? 4 * 8 * 32 * sizeof(float) : 0);
+           (Q8 ? kSRing * kTileKeys * sizeof(float) : 0);
 }
 constexpr size_t kSmemBytes = smem_bytes<false>();
 static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448, "shared memory");
@@ -228,15 +232,19 @@ __device__ __forceinline__ bool warp_next_chunk(Ctl& c, int k, Chunk& d) {
 // The widening is exact and stays on the integer/half ALUs: a code b becomes
 // the unsigned byte u = b + 128 (xor 0x80), the f16 with bit pattern 0x6400 | u
 // is 1024 + u, and subtracting 1152 leaves b (every step exact in f16).
-__device__ __forceinline__ void widen_tile_f16(const uint8_t* __restrict__ raw, uint8_t* __restrict__ dst, int t) {
-    const uint8_t* src = raw + t * 128;
+// With inline scales the rows are 144 bytes apart, which already spreads 8
+// consecutive rows over 8 bank groups, so the chunks are walked in order.
+__device__ __forceinline__ void widen_tile_f16(const uint8_t* __restrict__ raw, uint8_t* __restrict__ dst, int t,
+                                               bool inline_scale) {
+    const uint8_t* src = raw + t * (inline_scale ? kRawPitchInline : 128);
+    const int rot = inline_scale ? 0 : t;
     const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
     uint4 row[8];                                          // all loads first: one latency per tile
 #pragma unroll
-    for (int i = 0; i < 8; ++i) row[i] = *reinterpret_cast<const uint4*>(src + ((i + t) & 7) * 16);
+    for (int i = 0; i < 8; ++i) row[i] = *reinterpret_cast<const uint4*>(src + ((i + rot) & 7) * 16);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int cch = (i + t) & 7;                       // 16 codes: elements 16*cch .. 16*cch+15
+        const int cch = (i + rot) & 7;                     // 16 codes: elements 16*cch .. 16*cch+15
         const uint4 v = row[i];
         const uint32_t in[4] = {v.x, v.y, v.z, v.w};
         uint32_t out[8];
@@ -267,7 +275,10 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
     const float* __restrict__ k_scale, int64_t k_rows) {
     constexpr int kNT = kQ8 ? kThreadsQ8 : kThreads;
     constexpr int kTmaStages = kQ8 ? kRawStages : kStages;   // the producer's ring
-    constexpr int kTmaBytes = kQ8 ? kRawTileBytes : kTileBytes;
+    constexpr int kTmaStride = kQ8 ? kRawTileBytes : kTileBytes;
+    // int8 keys without a scale array carry each row's scale in bytes 128..131 of the row
+    const bool inline_scale = kQ8 && k_scale == nullptr;
+    const int kTmaBytes = kQ8 ? kTileKeys * (inline_scale ? kRawPitchInline : 128) : kTileBytes;
     constexpr int kAStages = kQ8 ? kConvStages : kStages;    // the MMA's A tiles
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -277,7 +288,8 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
     Ctl& c = *reinterpret_cast<Ctl*>(qbuf + kQBufs * kQBytes);
     int* pre = reinterpret_cast<int*>(&c + 1);               // [n_rows + 1] in prefix mode
     int* nvis = pre + kMaxPrefixRows + 1;                    // [n_rows] in prefix mode
-    float* escale = reinterpret_cast<float*>(nvis + kMaxPrefixRows);   // int8 keys: [4 warps][8 tiles][32]
+    float* escale = reinterpret_cast<float*>(nvis + kMaxPrefixRows);   // int8 keys: [4 warps][8 tiles][32],
+                                                                       // or with inline scales [kSRing][128]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n_rows = (int64_t)g.B * g.T;
@@ -291,6 +303,10 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
         for (int i = 0; i < kConvStages; ++i) {
             mbar_init(&c.afull[i], 4);
             mbar_init(&c.aempty[i], 1);
+        }
+        for (int i = 0; i < kSRing; ++i) {
+            mbar_init(&c.sfull[i], 4);
+            mbar_init(&c.sempty[i], 4);
         }
         for (int i = 0; i < kAcc; ++i) {
             mbar_init(&c.tfull[i], 1);
@@ -394,7 +410,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                         ok = false;
                         break;
                     }
-                    uint8_t* dst = tma_tiles + (size_t)stage * kTmaBytes;
+                    uint8_t* dst = tma_tiles + (size_t)stage * kTmaStride;
                     if (!g.page_table) {
                         const int64_t krow = krow0 + (int64_t)t * kTileKeys;
                         // rows past the visible keys may lie past the cache (TMA fills them with 0)
@@ -421,7 +437,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                             if (kr < 0 || kr + min(64, nk - (j0 + 64 * hh)) > k_rows)
                                 flag(g.status, IDX_ERR_DEVICE_BOUNDS);
                             if constexpr (kQ8) {
-                                tma_load_2d(dst + hh * (kRawTileBytes / 2), &kmap, &c.full[stage], 0, (int32_t)kr);
+                                tma_load_2d(dst + hh * (kTmaBytes / 2), &kmap, &c.full[stage], 0, (int32_t)kr);
                             } else {
                                 tma_load_2d(dst + hh * (kHalfBytes / 2), &kmap, &c.full[stage], 0, (int32_t)kr);
                                 tma_load_2d(dst + kHalfBytes + hh * (kHalfBytes / 2), &kmap, &c.full[stage], 64,
@@ -532,9 +548,10 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
         }
     } else if (kQ8 && warp >= 7) {
         // ------------------------------------------------------------ converters (int8 keys)
+        // with inline scales they also hand each row's scale to the epilogue (ring of kSRing tiles)
         const int t = threadIdx.x - 7 * 32;        // key row of the tile, 0..127
-        int rs = 0, as = 0;
-        uint32_t rph = 0, aph = 0;
+        int rs = 0, as = 0, ss = 0;
+        uint32_t rph = 0, aph = 0, sph = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
             Chunk d;
@@ -544,18 +561,27 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
             }
             if (d.row < 0) break;
             for (int tt = d.t0; tt < d.t1; ++tt) {
-                if (!warp_wait(&c.full[rs], rph) || !warp_wait(&c.aempty[as], aph ^ 1)) {
+                if (!warp_wait(&c.full[rs], rph) || !warp_wait(&c.aempty[as], aph ^ 1) ||
+                    (inline_scale && !warp_wait(&c.sempty[ss], sph ^ 1))) {
                     abort_cta(c, g);
                     ok = false;
                     break;
                 }
                 static_assert(!kQ8 || std::is_same<TK, __half>::value, "int8 codes are widened to f16");
-                widen_tile_f16(tma_tiles + (size_t)rs * kRawTileBytes, tiles + (size_t)as * kTileBytes, t);
+                const uint8_t* raw = tma_tiles + (size_t)rs * kRawTileBytes;
+                widen_tile_f16(raw, tiles + (size_t)as * kTileBytes, t, inline_scale);
+                if (inline_scale)
+                    escale[ss * kTileKeys + t] = *reinterpret_cast<const float*>(raw + t * kRawPitchInline + kD);
                 fence_proxy_async_smem();           // generic-proxy writes before the MMA reads them
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&c.empty[rs]);
                     mbar_arrive(&c.afull[as]);
+                    if (inline_scale) mbar_arrive(&c.sfull[ss]);
+                }
+                if (inline_scale && ++ss == kSRing) {
+                    ss = 0;
+                    sph ^= 1;
                 }
                 if (++rs == kRawStages) {
                     rs = 0;
@@ -571,6 +597,8 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;                 // TMEM lane quarter this warp may access
         float* esc = escale + (warp - 2) * 8 * 32;   // int8 keys: this warp's prefetched key scales
+        int ss = 0;                                // inline scales: ring slot of the next tile
+        uint32_t sph = 0;
         int acc = 0;
         uint32_t aphase = 0;
         float wv[kH];
@@ -600,7 +628,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
             // accumulators give the MMAs slack for) and parked in this lane's own
             // shared-memory slots
             for (int g0 = d.t0; ok && g0 < d.t1; g0 += 8) {
-                if constexpr (kQ8) {
+                if (kQ8 && !inline_scale) {
                     float scs[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
@@ -622,7 +650,24 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                     const int j = t * kTileKeys + quad * 32 + lane;
                     // int8 keys: the key's scale multiplies every head's dot product before the ReLU
                     float sc = 1.f;
-                    if constexpr (kQ8) sc = esc[i * 32 + lane];
+                    if constexpr (kQ8) {
+                        if (!inline_scale) {
+                            sc = esc[i * 32 + lane];
+                        } else {
+                            if (!warp_wait(&c.sfull[ss], sph)) {
+                                abort_cta(c, g);
+                                ok = false;
+                                break;
+                            }
+                            sc = j < n_keys ? escale[ss * kTileKeys + quad * 32 + lane] : 0.f;
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&c.sempty[ss]);
+                            if (++ss == kSRing) {
+                                ss = 0;
+                                sph ^= 1;
+                            }
+                        }
+                    }
                     if (!warp_wait(&c.tfull[acc], aphase)) {
                         abort_cta(c, g);
                         ok = false;
@@ -1070,13 +1115,15 @@ cudaError_t launch_score_tc_q8(const void* q, int q_dtype, const float* w, const
     // q inside f16's normal range, as on the F16-cache path)
     if (g.T != 1 || (q_dtype != IDX_BF16 && q_dtype != IDX_F16)) return cudaErrorNotSupported;
     if ((reinterpret_cast<uintptr_t>(k8) & 15u) || (k_row_stride % 16) || k_rows < 1 || k_rows > INT32_MAX ||
-        (reinterpret_cast<uintptr_t>(w) & 15u) || (reinterpret_cast<uintptr_t>(q) & 15u))
+        (reinterpret_cast<uintptr_t>(w) & 15u) || (reinterpret_cast<uintptr_t>(q) & 15u) ||
+        (!k_scale && k_row_stride < kRawPitchInline))
         return cudaErrorNotSupported;
     const int64_t n_rows = (int64_t)g.B * g.T;
     if (n_rows == 0 || g.max_n_kv == 0) return cudaSuccess;
     CUtensorMap map;
     if (g.page_table && g.page_size % 64 != 0) return cudaErrorNotSupported;
-    if (!make_key8_tmap(&map, k8, k_row_stride, k_rows, g.page_table ? 64 : kTileKeys)) return cudaErrorNotSupported;
+    if (!make_key8_tmap(&map, k8, k_row_stride, k_rows, g.page_table ? 64 : kTileKeys, k_scale ? 128 : kRawPitchInline))
+        return cudaErrorNotSupported;
     int grid, slot;
     if (!decode_launch_shape(g, grid, slot)) return cudaErrorNotSupported;
     auto kern = score_tc_decode_kernel<__half, true>;

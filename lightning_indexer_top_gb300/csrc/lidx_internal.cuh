@@ -128,7 +128,8 @@ cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, i
                             cudaStream_t st);
 
 // tensor-core decode scorer over int8 keys with per-row scales (H = 64, d = 128,
-// T = 1, 16-bit q); cudaErrorNotSupported for anything else
+// T = 1, 16-bit q); k_scale NULL: each row's f32 scale sits in its bytes 128..131
+// (row stride >= 144); cudaErrorNotSupported for anything else
 cudaError_t launch_score_tc_q8(const void* q, int q_dtype, const float* w, const int8_t* k8, int64_t k_row_stride,
                                const float* k_scale, int64_t k_rows, const Geom& g, float* scores,
                                int64_t score_row_stride, cudaStream_t st);
@@ -166,8 +167,10 @@ cudaError_t launch_attn_mla_tc(const void* q, const void* lat, int64_t kv_row_st
 bool make_key_tmap(CUtensorMap* m, const void* k, bool bf16, int64_t k_row_stride, int64_t k_rows, int box_rows);
 bool make_q3d_tmap(CUtensorMap* m, const void* q, bool bf16, int64_t rows);
 bool make_w_tmap(CUtensorMap* m, const float* w, int64_t rows);
-// [rows, 128] int8 keys: boxes of 128 bytes x box_rows rows, no swizzle
-bool make_key8_tmap(CUtensorMap* m, const int8_t* k, int64_t row_bytes, int64_t k_rows, int box_rows);
+// [rows, payload] int8 keys (128 codes, or 144 bytes with the scale inline): boxes of
+// payload bytes x box_rows rows, no swizzle
+bool make_key8_tmap(CUtensorMap* m, const int8_t* k, int64_t row_bytes, int64_t k_rows, int box_rows,
+                    int payload);
 
 // number of SMs of the current device (cached per device)
 int sm_count();

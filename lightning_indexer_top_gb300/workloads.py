@@ -56,8 +56,8 @@ class Workload:
     block_size: int = 0
     page_table: Optional[torch.Tensor] = None   # int32 [B, pages]: paged caches (rows of page_size)
     page_size: int = 0
-    k8: Optional[torch.Tensor] = None        # int8 indexer key codes [rows, d] (quantized cache)
-    k_scale: Optional[torch.Tensor] = None   # f32 [rows] per-row scales of k8
+    k8: Optional[torch.Tensor] = None        # int8 indexer key codes [rows, >= d] (quantized cache)
+    k_scale: Optional[torch.Tensor] = None   # f32 [rows] per-row scales of k8 (None: inline in the rows)
     extra: Dict = field(default_factory=dict)
 
     def row0(self, b: int) -> int:
@@ -166,6 +166,7 @@ def make(cfg, device="cuda", *, n_kv_override=None, batch_override=None, n_token
             table = perm.view(B, pages).to(torch.int32)
             name += "_paged"
         if quantized_keys:
+            # 128-byte code rows and a separate f32 scale array (the faster of the two layouts)
             from . import idx_quantize_rows
             k8, ks = idx_quantize_rows(k)
             name += "_q8"

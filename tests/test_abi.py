@@ -72,6 +72,9 @@ def test_host_validation_rejects_bad_arguments(lib):
         L.IDX_ERR_INVALID_ARG
     assert lib.idx_quantize_rows(None, L.IDX_BF16, 4, 0, 128, None, 128, None, None) == L.IDX_ERR_INVALID_ARG
     assert lib.idx_quantize_rows(None, L.IDX_BF16, 4, 128, 128, None, 120, None, None) == L.IDX_ERR_INVALID_ARG
+    # inline scales need room for the scale after the codes
+    assert lib.idx_quantize_rows(ctypes.c_void_p(16), L.IDX_BF16, 4, 128, 128, ctypes.c_void_p(256), 128, None,
+                                 None) == L.IDX_ERR_INVALID_ARG
     assert lib.idx_score_q8(None, L.IDX_BF16, None, 64, 128, None, 128, None, 0, b, 2, None, 16, None, 0, None) == \
         L.IDX_ERR_UNSUPPORTED
     assert lib.sparse_attn_decode(None, L.IDX_BF16, 6, 4, 128, 128, None, None, 512, 512, 0, b, None, 16, None,

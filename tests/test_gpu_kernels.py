@@ -699,6 +699,10 @@ def test_paged_decode_path_is_bit_identical_to_contiguous(P):
     k8p, scp = L.idx_quantize_rows(kp)
     q8_c = L.idx_score_q8(q, w, k8c, scc, contig)
     q8_p = L.idx_score_q8(q, w, k8p, scp, paged)
+    rc, _ = L.idx_quantize_rows(kc, inline_scale=True)
+    rp, _ = L.idx_quantize_rows(kp, inline_scale=True)
+    qi_c = L.idx_score_q8(q, w, rc, None, contig)
+    qi_p = L.idx_score_q8(q, w, rp, None, paged)
     idx_c, ns_c = L.idx_topk(s_c, contig, 2048)
     idx_p, ns_p = L.idx_topk(s_p, paged, 2048)
     o_c = L.sparse_attn_decode(qa, lc, None, contig, idx_c, ns_c, 1 / math.sqrt(192), dv=512)
@@ -707,6 +711,7 @@ def test_paged_decode_path_is_bit_identical_to_contiguous(P):
     for b, n in enumerate(n_kv):
         assert torch.equal(s_c[b, :n], s_p[b, :n]), b
         assert torch.equal(q8_c[b, :n], q8_p[b, :n]), b
+        assert torch.equal(qi_c[b, :n], qi_p[b, :n]) and torch.equal(qi_c[b, :n], q8_c[b, :n]), b
     assert torch.equal(idx_c, idx_p) and torch.equal(ns_c, ns_p)
     assert torch.equal(o_c, o_p)
     ref = O.indexer_scores(np64(q[3]), np64(w[3]), np64(keys[3]))
@@ -767,3 +772,35 @@ def test_paged_prefill_scores_match_contiguous():
     L.idx_score(q, w, kp, paged, scores=s_p)
     torch.cuda.synchronize()
     assert torch.equal(s_c, s_p)
+
+
+def test_quantize_and_score_with_inline_scales():
+    # rows of 144 bytes: 128 codes, the f32 scale in bytes 128..131; the same codes and scales as
+    # the separate layout, and scores of the dequantized keys (tensor-core and CUDA-core paths)
+    g = torch.Generator(device=DEV).manual_seed(86)
+    n = 9000
+    k = torch.randn(n, 128, generator=g, device=DEV) * torch.rand(n, 1, generator=g, device=DEV) * 3
+    rows, none = L.idx_quantize_rows(k, inline_scale=True)
+    assert none is None and rows.stride(0) == 144
+    k8s, scs = L.idx_quantize_rows(k)
+    torch.cuda.synchronize()
+    assert torch.equal(rows[:, :128], k8s) and torch.equal(L.inline_scales(rows, 128), scs)
+    n_kv = [0, 1, 300, 8192, 500]
+    starts = [0, 1, 10, 400, 8500]
+    B = len(n_kv)
+    q = torch.randn(B, 64, 128, generator=g, device=DEV).to(torch.bfloat16)
+    w = torch.randn(B, 64, generator=g, device=DEV) / 8
+    batch = L.Batch(_i32(n_kv), 1, 8192, kv_start=_i32(starts))
+    s_in = torch.full((B, 8192), 5.0, device=DEV)
+    L.idx_score_q8(q, w, rows, None, batch, scores=s_in)
+    s_sep = L.idx_score_q8(q, w, k8s, scs, batch)
+    qf = q.float()   # f32 q: the CUDA-core path with inline scales
+    s_gen = L.idx_score_q8(qf, w, rows, None, batch)
+    torch.cuda.synchronize()
+    kd = O.dequantize_rows(k8s.cpu().numpy(), scs.cpu().numpy())
+    for b, nk in enumerate(n_kv):
+        assert torch.equal(s_in[b, :nk], s_sep[b, :nk]), b
+        assert np.all(s_in[b, nk:].cpu().numpy() == 5.0)
+        ref = O.indexer_scores(np64(q[b]), np64(w[b]), kd[starts[b]:starts[b] + nk])
+        assert_scores_close(s_in[b, :nk].cpu().numpy(), ref, f"inline seq {b}")
+        assert_scores_close(s_gen[b, :nk].cpu().numpy(), ref, f"inline generic seq {b}")
