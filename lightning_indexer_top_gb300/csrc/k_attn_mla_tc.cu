@@ -42,11 +42,21 @@ constexpr int kDkBlocks = kDk / 64;                     // 9 column blocks of 12
 constexpr int kDvBlocks = kDv / 64;                     // 8
 constexpr int kBlockBytes = kKeys * 128;                // one column block of a tile
 constexpr int kKTileBytes = kDkBlocks * kBlockBytes;    // 73728
-constexpr int kStages = 2;
+constexpr int kVTileBytes = kDvBlocks * kBlockBytes;    // 65536
+constexpr int kStagesK = 3;                             // rank 0: key tiles in flight
+constexpr int kStagesV = 2;                             // rank 1: value tiles in flight
 constexpr int kPBytes = kHq * kKeys * 2;                // P tile, bf16, 128-byte swizzle K-major
 constexpr int kPktBytes = kPBytes + 3 * kHq * 4;        // P tile + alpha, l, m per head
 constexpr int kPktStride = 18432;                       // P tile + tail, 1024-aligned
-constexpr int kMaxKps = 4096;                           // selected keys per split, at most
+constexpr int kMaxKps = 2048;                           // selected keys per split, at most
+// Shared memory, per rank (the two CTAs share one launch size):
+//   rank 0: [0, 3 x 72 KB) key-tile ring
+//   rank 1: [0, 2 x 64 KB) value-tile ring, then the two P packet slots that
+//           rank 0 writes directly
+//   both:   from kTailOff the staged cache rows, the validity bits, barriers
+constexpr int kPktOff = kStagesV * kVTileBytes;
+constexpr int kTailOff = kStagesK * kKTileBytes;
+static_assert(kPktOff + 2 * kPktStride <= kTailOff, "rank 1 layout");
 #ifndef LIDX_MLA_WARPS
 #define LIDX_MLA_WARPS 12
 #endif
@@ -55,7 +65,7 @@ constexpr int kMaxKps = 4096;                           // selected keys per spl
 // 8 and ~40 GB/s with 16 (about HBM speed over all SMs), so every warp without
 // another role gathers.
 constexpr int kThreads = 32 * LIDX_MLA_WARPS;
-constexpr int kProducerWarps = LIDX_MLA_WARPS - 6;      // warps 0 and 7..
+constexpr int kProducerWarps = LIDX_MLA_WARPS - 5;      // warps 0 and 6..
 static_assert(kProducerWarps >= 1, "warp roles");
 constexpr int kTmemCols = 512;
 constexpr int kSCol0 = 320;                             // rank 0: S buffers at 320 and 384 (Q at 0..287)
@@ -69,15 +79,13 @@ struct PktTail {
 static_assert(kPBytes + sizeof(PktTail) <= kPktStride, "packet layout");
 
 struct Ctl {
-    uint64_t xfull[kStages];   // gathered tile landed (32 producer lanes arrive)
-    uint64_t xempty[kStages];  // tile consumed by the MMAs
+    uint64_t xfull[kStagesK];  // gathered tile landed (every producer lane arrives)
+    uint64_t xempty[kStagesK]; // tile consumed by the MMAs
     uint64_t sfull[2];         // rank 0: S accumulator written
     uint64_t sempty[2];        // rank 0: S read by the softmax warps
     uint64_t qready;           // rank 0: Q stored in TMEM
-    uint64_t staged[2];        // rank 0: P packet j written to the staging slot
-    uint64_t stfree[2];        // rank 0: staging slot j read by its bulk copy
     uint64_t pfree[2];         // rank 0: rank 1's packet slot j consumed by its MMAs
-    uint64_t pfull[2];         // rank 1: packet j arrived
+    uint64_t pfull[2];         // rank 1: packet j landed (rank 0 posts its byte count, its stores complete it)
     uint64_t cdone[2];         // rank 1: O corrected for packet j
     uint64_t pvdone[2];        // rank 1: PV MMAs that read packet j completed
     uint64_t done;
@@ -85,8 +93,8 @@ struct Ctl {
     int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kKTileBytes + 2 * kPktStride + kMaxKps * 4 +
-                              kMaxKps / 8 + sizeof(Ctl);
+constexpr size_t kSmemBytes = 1024 + (size_t)kTailOff + kMaxKps * 4 + kMaxKps / 8 + sizeof(Ctl);
+static_assert(kSmemBytes <= 232448, "shared memory");
 
 __device__ __forceinline__ void abort_cta(Ctl& c, int* status) {
     *(volatile int*)&c.abort = 1;
@@ -137,7 +145,7 @@ __device__ __forceinline__ Unit make_unit(const Geom& g, const int32_t* n_sel, i
 // cp.async arrival, so a tile is announced the moment its bytes have landed
 // and the producers go straight on to the next free stage.  The consumer
 // orders the landed bytes before its MMAs with a proxy fence.
-template <int kChunks>
+template <int kChunks, int kNStages, int kStageBytes>
 __device__ __forceinline__ void gather_tiles(Ctl& c, uint8_t* xtiles, const __nv_bfloat16* lat,
                                              int64_t lat_row_stride, const Unit& u, const int32_t* rows_s,
                                              int p, int* status) {
@@ -145,13 +153,13 @@ __device__ __forceinline__ void gather_tiles(Ctl& c, uint8_t* xtiles, const __nv
     const char* base = reinterpret_cast<const char*>(lat);
     const int64_t row_bytes = lat_row_stride * 2;
     for (int t = 0; t < u.n_tiles; ++t) {
-        const int stage = t & 1;
-        const uint32_t ph = (uint32_t)((t >> 1) & 1);
+        const int stage = t % kNStages;
+        const uint32_t ph = (uint32_t)((t / kNStages) & 1);
         if (warp_aborted(c) || !warp_wait(&c.xempty[stage], ph ^ 1)) {
             abort_cta(c, status);
             break;
         }
-        const uint32_t dst0 = smem_u32(xtiles + (size_t)stage * kKTileBytes);
+        const uint32_t dst0 = smem_u32(xtiles + (size_t)stage * kStageBytes);
         const int32_t* rr = rows_s + t * kKeys;
 #pragma unroll 4
         for (int i = p * 32 + lane; i < kKeys * kChunks; i += 32 * kProducerWarps) {
@@ -175,8 +183,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* xtiles = smem;                                         // K tiles (rank 0) / V tiles (rank 1)
-    uint8_t* pkts = smem + (size_t)kStages * kKTileBytes;           // P staging (rank 0) / P received (rank 1)
-    int32_t* rows_s = reinterpret_cast<int32_t*>(pkts + 2 * kPktStride);   // cache row of each selected key
+    uint8_t* pkts = smem + kPktOff;                                 // rank 1: P packets (rank 0 writes them)
+    int32_t* rows_s = reinterpret_cast<int32_t*>(smem + kTailOff);         // cache row of each selected key
     uint32_t* vmask = reinterpret_cast<uint32_t*>(rows_s + kMaxKps);       // bit = key index is valid
     Ctl& c = *reinterpret_cast<Ctl*>(vmask + kMaxKps / 32);
 
@@ -185,13 +193,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const Unit u = make_unit(g, n_sel, idx_row_stride, kv_rows, splits, kps);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStagesK; ++i) {
             mbar_init(&c.xfull[i], 32 * kProducerWarps);
             mbar_init(&c.xempty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&c.sfull[i], 1);
             mbar_init(&c.sempty[i], 4);
-            mbar_init(&c.staged[i], 4);
-            mbar_init(&c.stfree[i], 1);
             mbar_init(&c.pfree[i], 1);
             mbar_init(&c.pfull[i], 1);
             mbar_init(&c.cdone[i], 4);
@@ -202,40 +210,92 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         c.abort = 0;
         fence_mbar_init();
     }
-    // the split's selected keys -> cache rows + validity bits, 32 keys per warp step
-    for (int wd = warp; wd < u.n_tiles * (kKeys / 32); wd += kThreads / 32) {
-        const int j = u.k0 + wd * 32 + lane;
-        bool valid = false;
-        int64_t row = u.fallback;
-        if (j < u.k1) {
-            const int pos = idx[u.r * idx_row_stride + j];
-            const int64_t rr = (pos >= 0 && pos < u.n_kv) ? key_row(g, u.b, pos) : -1;
-            if (rr >= 0 && rr < kv_rows) {
-                valid = true;
-                row = rr;
-            } else if (rank == 0) {
-                flag(g.status, IDX_ERR_DEVICE_BOUNDS);
-            }
-        }
-        rows_s[wd * 32 + lane] = (int32_t)row;
-        const uint32_t bits = __ballot_sync(0xffffffffu, valid);
-        if (lane == 0) vmask[wd] = bits;
-    }
     if (warp == 1) {
         tmem_alloc(&c.tmem_base, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
-    cluster_sync();  // barriers of both CTAs initialised, indices staged, TMEM allocated
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = c.tmem_base;
     const int quad = warp & 3;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
 
-    const int producer = warp == 0 ? 0 : (warp >= 7 ? warp - 6 : -1);   // producer index or -1
+    // Rank 0's softmax warps put Q into TMEM while the other warps turn the
+    // split's selected keys into cache rows + validity bits (32 keys per warp
+    // step, the index loads of a warp issued together).
+    if (rank == 0 && warp >= 2 && warp <= 5) {
+        const int h = quad * 32 + lane;
+        if (u.n_tiles > 0) {
+            const uint4* src = reinterpret_cast<const uint4*>(q + (u.r * kHq + h) * (int64_t)kDk);
+            // column block cb+1 is loading while block cb goes to TMEM
+            uint4 xn[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xn[i] = src[i];
+#pragma unroll
+            for (int cb = 0; cb < kDkBlocks; ++cb) {
+                uint32_t regs[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    regs[4 * i] = xn[i].x;
+                    regs[4 * i + 1] = xn[i].y;
+                    regs[4 * i + 2] = xn[i].z;
+                    regs[4 * i + 3] = xn[i].w;
+                }
+                if (cb + 1 < kDkBlocks) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) xn[i] = src[(cb + 1) * 8 + i];
+                }
+                tmem_st_32x32b_x32(tmem + lane_off + cb * 32, regs);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c.qready);
+        }
+    } else {
+        const int n_st = rank == 0 ? kThreads / 32 - 4 : kThreads / 32;
+        const int si = rank == 0 && warp > 5 ? warp - 4 : warp;
+        const int n_words = u.n_tiles * (kKeys / 32);
+        constexpr int kBatch = 8;
+        for (int w0 = si; w0 < n_words; w0 += kBatch * n_st) {
+            int pos[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int j = u.k0 + (w0 + k * n_st) * 32 + lane;
+                pos[k] = (w0 + k * n_st < n_words && j < u.k1) ? idx[u.r * idx_row_stride + j] : -1;
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int wd = w0 + k * n_st;
+                if (wd >= n_words) break;
+                const int j = u.k0 + wd * 32 + lane;
+                bool valid = false;
+                int64_t row = u.fallback;
+                if (j < u.k1) {
+                    const int64_t rr = (pos[k] >= 0 && pos[k] < u.n_kv) ? key_row(g, u.b, pos[k]) : -1;
+                    if (rr >= 0 && rr < kv_rows) {
+                        valid = true;
+                        row = rr;
+                    } else if (rank == 0) {
+                        flag(g.status, IDX_ERR_DEVICE_BOUNDS);
+                    }
+                }
+                rows_s[wd * 32 + lane] = (int32_t)row;
+                const uint32_t bits = __ballot_sync(0xffffffffu, valid);
+                if (lane == 0) vmask[wd] = bits;
+            }
+        }
+    }
+    tc_fence_before();
+    cluster_sync();  // barriers of both CTAs initialised, indices staged
+    tc_fence_after();
+
+    const int producer = warp == 0 ? 0 : (warp >= 6 ? warp - 5 : -1);   // producer index or -1
     if (rank == 0) {
         if (producer >= 0) {
-            gather_tiles<kDkBlocks * 8>(c, xtiles, lat, lat_row_stride, u, rows_s, producer, g.status);
+            gather_tiles<kDkBlocks * 8, kStagesK, kKTileBytes>(c, xtiles, lat, lat_row_stride, u, rows_s, producer,
+                                                               g.status);
         } else if (warp == 1) {
             if (lane == 0) {
                 // ---------------------------------------------------- S = Q K^T issuer
@@ -244,10 +304,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!ok) abort_cta(c, g.status);
                 tc_fence_after();
                 for (int t = 0; ok && t < u.n_tiles; ++t) {
-                    const int stage = t & 1, sb = t & 1;
-                    const uint32_t ph = (uint32_t)((t >> 1) & 1);
+                    const int stage = t % kStagesK, sb = t & 1;
                     if (aborted(c)) break;
-                    if (!mbar_wait(&c.xfull[stage], ph) || !mbar_wait(&c.sempty[sb], ph ^ 1)) {
+                    if (!mbar_wait(&c.xfull[stage], (uint32_t)((t / kStagesK) & 1)) ||
+                        !mbar_wait(&c.sempty[sb], (uint32_t)((t >> 1) & 1) ^ 1)) {
                         abort_cta(c, g.status);
                         break;
                     }
@@ -267,67 +327,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mbar_wait(&c.done, 0);
             }
             __syncwarp();
-        } else if (warp == 6) {
-            if (lane == 0) {
-                // ---------------------------------------------------- P packet sender (own warp: never
-                // held up behind the MMA issuer)
-                for (int t = 0; t < u.n_tiles; ++t) {
-                    const int j = t & 1;
-                    const uint32_t ph = (uint32_t)((t >> 1) & 1);
-                    if (aborted(c)) break;
-                    if (!mbar_wait(&c.staged[j], ph) || !mbar_wait(&c.pfree[j], ph ^ 1)) {
-                        abort_cta(c, g.status);
-                        break;
-                    }
-                    uint8_t* slot = pkts + j * kPktStride;
-                    const uint32_t rbar = mapa(&c.pfull[j], 1);
-                    mbar_arrive_expect_tx_remote(rbar, kPktBytes);
-                    bulk_copy_s2cluster(mapa(slot, 1), slot, kPktBytes, rbar);
-                    bulk_commit();
-                    // the previous packet's copy has read its staging slot: release it
-                    if (t > 0) {
-                        bulk_wait_read<1>();
-                        mbar_arrive(&c.stfree[(t - 1) & 1]);
-                    }
-                }
-                bulk_wait_read<0>();
-                if (u.n_tiles > 0 && !aborted(c)) mbar_arrive(&c.stfree[(u.n_tiles - 1) & 1]);
-                // rank 1's last arrivals on pfree land before this CTA may leave
-                const int n = min(u.n_tiles, 2);
-                for (int t = u.n_tiles - n; t < u.n_tiles; ++t)
-                    if (!aborted(c)) mbar_wait(&c.pfree[t & 1], (uint32_t)((t >> 1) & 1));
-            }
-            __syncwarp();
         } else if (warp >= 2 && warp <= 5) {
-            // ---------------------------------------------------------- Q to TMEM, then softmax (thread = head)
+            // ---------------------------------------------------------- softmax (thread = head); P goes
+            // straight into rank 1's packet slot by asynchronous stores that complete its barrier
             const int h = quad * 32 + lane;
-            if (u.n_tiles > 0) {
-                const uint4* src = reinterpret_cast<const uint4*>(q + (u.r * kHq + h) * (int64_t)kDk);
-                // column block cb+1 is loading while block cb goes to TMEM
-                uint4 xn[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) xn[i] = src[i];
-#pragma unroll
-                for (int cb = 0; cb < kDkBlocks; ++cb) {
-                    uint32_t regs[32];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        regs[4 * i] = xn[i].x;
-                        regs[4 * i + 1] = xn[i].y;
-                        regs[4 * i + 2] = xn[i].z;
-                        regs[4 * i + 3] = xn[i].w;
-                    }
-                    if (cb + 1 < kDkBlocks) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) xn[i] = src[(cb + 1) * 8 + i];
-                    }
-                    tmem_st_32x32b_x32(tmem + lane_off + cb * 32, regs);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&c.qready);
-            }
             float m_used = 0.f, lsum = 0.f;
             bool has_m = false;
             for (int t = 0; t < u.n_tiles; ++t) {
@@ -382,44 +385,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 lsum += psum;
 
-                // staging slot j is free once the copy of tile t-2 has read it
-                if (!warp_wait(&c.stfree[j], ph ^ 1)) {
+                // rank 1's slot j is free once its MMAs of tile t-2 have completed
+                if (!warp_wait(&c.pfree[j], ph ^ 1)) {
                     abort_cta(c, g.status);
                     break;
                 }
-                uint8_t* slot = pkts + j * kPktStride;
-                uint8_t* rowp = slot + (h >> 3) * 1024 + (h & 7) * 128;
+                const uint32_t slot = mapa(pkts + j * kPktStride, 1);
+                const uint32_t rbar = mapa(&c.pfull[j], 1);
+                if (h == 0) mbar_arrive_expect_tx_remote(rbar, kPktBytes);
+                const uint32_t rowp = slot + (uint32_t)((h >> 3) * 1024 + (h & 7) * 128);
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch)
-                    *reinterpret_cast<uint4*>(rowp + ((ch ^ (h & 7)) << 4)) =
-                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-                PktTail& tail = *reinterpret_cast<PktTail*>(slot + kPBytes);
-                tail.alpha[h] = alpha;
-                tail.l[h] = lsum;
-                tail.m[h] = m_used;
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&c.staged[j]);
+                    st_async_v4(rowp + ((ch ^ (h & 7)) << 4),
+                                make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]), rbar);
+                const uint32_t tail = slot + kPBytes + (uint32_t)h * 4;
+                st_async_f32(tail + offsetof(PktTail, alpha), alpha, rbar);
+                st_async_f32(tail + offsetof(PktTail, l), lsum, rbar);
+                st_async_f32(tail + offsetof(PktTail, m), m_used, rbar);
             }
+            // rank 1's last arrivals on pfree land before this CTA may leave
+            const int n = min(u.n_tiles, 2);
+            for (int t = u.n_tiles - n; t < u.n_tiles; ++t)
+                if (!warp_aborted(c)) warp_wait(&c.pfree[t & 1], (uint32_t)((t >> 1) & 1));
         }
     } else {
         if (producer >= 0) {
-            gather_tiles<kDvBlocks * 8>(c, xtiles, lat, lat_row_stride, u, rows_s, producer, g.status);
+            gather_tiles<kDvBlocks * 8, kStagesV, kVTileBytes>(c, xtiles, lat, lat_row_stride, u, rows_s, producer,
+                                                               g.status);
         } else if (warp == 1) {
             if (lane == 0) {
                 const uint32_t idesc = idesc_f16_f32_major(kHq, 256, 1, 0, 1);
                 for (int t = 0; t < u.n_tiles; ++t) {
-                    const int stage = t & 1, j = t & 1;
+                    const int stage = t % kStagesV, j = t & 1;
                     const uint32_t ph = (uint32_t)((t >> 1) & 1);
                     if (aborted(c)) break;
-                    if (!mbar_wait(&c.xfull[stage], ph) || !mbar_wait(&c.cdone[j], ph)) {
+                    if (!mbar_wait(&c.xfull[stage], (uint32_t)((t / kStagesV) & 1)) || !mbar_wait(&c.cdone[j], ph)) {
                         abort_cta(c, g.status);
                         break;
                     }
                     fence_proxy_async_smem();
                     tc_fence_after();
                     const uint32_t pb = smem_u32(pkts + j * kPktStride);
-                    const uint32_t vb = smem_u32(xtiles + (size_t)stage * kKTileBytes);
+                    const uint32_t vb = smem_u32(xtiles + (size_t)stage * kVTileBytes);
 #pragma unroll
                     for (int ks = 0; ks < kKeys / 16; ++ks) {
                         const uint64_t ad = desc_sw128_kmajor(pb + ks * 32, 1024);

@@ -293,6 +293,22 @@ __device__ __forceinline__ uint32_t mapa(const void* p, uint32_t rank) {
     return r;
 }
 
+// asynchronous stores into another CTA's shared memory (addresses from mapa):
+// the issuing thread does not wait; the bytes complete transactions on the
+// destination CTA's mbarrier once they have landed
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     addr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar_cluster)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+                 "r"(__float_as_uint(v)), "r"(bar_cluster)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t bar_cluster, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(bar_cluster),
                  "r"(bytes)
