@@ -190,7 +190,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     const uint32_t rank = cluster_ctarank();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Unit u = make_unit(g, n_sel, idx_row_stride, kv_rows, splits, kps);
+    pdl_trigger();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStagesK; ++i) {
@@ -221,13 +221,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
 
-    // Rank 0's softmax warps put Q into TMEM while the other warps turn the
-    // split's selected keys into cache rows + validity bits (32 keys per warp
-    // step, the index loads of a warp issued together).
-    if (rank == 0 && warp >= 2 && warp <= 5) {
+    // Rank 0's softmax warps put Q into TMEM (Q is an input no other kernel
+    // writes, so this overlaps the end of the previous kernel) while the other
+    // warps, once the previous kernel's selection is visible, turn the split's
+    // selected keys into cache rows + validity bits (32 keys per warp step, the
+    // index loads of a warp issued together).
+    const bool q_warp = rank == 0 && warp >= 2 && warp <= 5;
+    if (q_warp) {
         const int h = quad * 32 + lane;
-        if (u.n_tiles > 0) {
-            const uint4* src = reinterpret_cast<const uint4*>(q + (u.r * kHq + h) * (int64_t)kDk);
+        {
+            const int64_t qrow = (int64_t)(blockIdx.x >> 1) / splits;
+            const uint4* src = reinterpret_cast<const uint4*>(q + (qrow * kHq + h) * (int64_t)kDk);
             // column block cb+1 is loading while block cb goes to TMEM
             uint4 xn[8];
 #pragma unroll
@@ -253,7 +257,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&c.qready);
         }
-    } else {
+    }
+    pdl_wait();
+    const Unit u = make_unit(g, n_sel, idx_row_stride, kv_rows, splits, kps);
+    if (!q_warp) {
         const int n_st = rank == 0 ? kThreads / 32 - 4 : kThreads / 32;
         const int si = rank == 0 && warp > 5 ? warp - 4 : warp;
         const int n_words = u.n_tiles * (kKeys / 32);
@@ -565,6 +572,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restrict__ part_o,
                                                           const float* __restrict__ part_ml, int splits,
                                                           void* __restrict__ out, int out_dtype) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t r = blockIdx.x;
     const int h = blockIdx.y;
     const int c0 = threadIdx.x * 4;
@@ -660,13 +669,13 @@ cudaError_t launch_attn_mla_tc(const void* q, const void* lat, int64_t kv_row_st
     if (grid > INT32_MAX) return cudaErrorNotSupported;
     cudaFuncSetAttribute(mla_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     const float scale_log2 = scale * 1.4426950408889634f;
-    mla_attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, st>>>(
-        static_cast<const __nv_bfloat16*>(lat), kv_row_stride, static_cast<const __nv_bfloat16*>(q), g, idx,
-        idx_row_stride, n_sel, kv_rows, scale_log2, splits, (int)kps64, out, out_dtype, part_o, part_ml);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(mla_attn_tc_kernel, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st,
+                               static_cast<const __nv_bfloat16*>(lat), kv_row_stride,
+                               static_cast<const __nv_bfloat16*>(q), g, idx, idx_row_stride, n_sel, kv_rows,
+                               scale_log2, splits, (int)kps64, out, out_dtype, part_o, part_ml);
     if (e != cudaSuccess || splits == 1) return e;
-    mla_combine_kernel<<<dim3((unsigned)n_rows, kHq), 128, 0, st>>>(part_o, part_ml, splits, out, out_dtype);
-    return cudaGetLastError();
+    return launch_pdl(mla_combine_kernel, dim3((unsigned)n_rows, kHq), dim3(128), 0, st,
+                      static_cast<const float*>(part_o), static_cast<const float*>(part_ml), splits, out, out_dtype);
 }
 
 }  // namespace lidx

@@ -294,6 +294,8 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n_rows = (int64_t)g.B * g.T;
     const bool prefix = n_rows <= kMaxPrefixRows;
+    pdl_trigger();
+    pdl_wait();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kTmaStages; ++i) {
@@ -1130,8 +1132,8 @@ cudaError_t launch_score_tc_q8(const void* q, int q_dtype, const float* w, const
     constexpr size_t smem = smem_bytes<true>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreadsQ8, smem, st>>>(map, q, q_dtype, w, g, scores, score_row_stride, slot, k_scale, k_rows);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreadsQ8), smem, st, map, q, q_dtype, w, g, scores, score_row_stride,
+                      slot, k_scale, k_rows);
 }
 
 cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, int d, const void* k,
@@ -1159,8 +1161,8 @@ cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, i
     auto kern = bf16 ? score_tc_decode_kernel<__nv_bfloat16, false> : score_tc_decode_kernel<__half, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kSmemBytes, st>>>(map, q, q_dtype, w, g, scores, score_row_stride, slot, nullptr, k_rows);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, st, map, q, q_dtype, w, g, scores,
+                      score_row_stride, slot, static_cast<const float*>(nullptr), k_rows);
 }
 
 }  // namespace lidx

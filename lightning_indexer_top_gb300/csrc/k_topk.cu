@@ -375,6 +375,8 @@ __global__ void __launch_bounds__(kMapThreads, 1) topk_map_kernel(const float* _
                                                                   int32_t* __restrict__ n_sel) {
     extern __shared__ __align__(16) unsigned char map_raw[];
     MapShared& sh = *reinterpret_cast<MapShared*>(map_raw);
+    pdl_trigger();
+    pdl_wait();
     const int64_t r = blockIdx.x;
     const int n = row_n_vis(g, r);
     const int K = min(top_k, n);
@@ -617,6 +619,8 @@ __global__ void __launch_bounds__(kMcThreads) topk_mc_bound_kernel(const float* 
     __shared__ uint32_t hist[2048];
     __shared__ uint32_t scratch[kMcThreads / 32];
     __shared__ uint32_t sb[2];
+    pdl_trigger();
+    pdl_wait();
     const int64_t r = blockIdx.x;
     const int n = row_n_vis(g, r);
     const int K = min(top_k, n);
@@ -663,6 +667,8 @@ __global__ void __launch_bounds__(kMcThreads) topk_mc_filter_kernel(const float*
                                                                     McLayout L) {
     __shared__ uint64_t buf[kMcLocal];
     __shared__ uint32_t nbuf, base;
+    pdl_trigger();
+    pdl_wait();
     const int64_t r = blockIdx.y;
     const int n = row_n_vis(g, r);
     const int K = min(top_k, n);
@@ -721,6 +727,8 @@ __global__ void __launch_bounds__(kMapThreads, 1) topk_mc_finish_kernel(const fl
     extern __shared__ __align__(16) unsigned char map_raw[];
     MapShared& sh = *reinterpret_cast<MapShared*>(map_raw);
     GenShared<kMapThreads>& gsh = *reinterpret_cast<GenShared<kMapThreads>*>(map_raw);
+    pdl_trigger();
+    pdl_wait();
     const int64_t r = blockIdx.x;
     const int n = row_n_vis(g, r);
     const int K = min(top_k, n);
@@ -806,20 +814,23 @@ cudaError_t launch_topk(const float* scores, int64_t score_row_stride, const Geo
         // few long rows: spread the passes over the rows' chunks
         const McLayout L = mc_layout(ws, n_rows);
         const int chunks = (g.max_n_kv + kMcChunk - 1) / kMcChunk;
-        topk_mc_bound_kernel<<<(unsigned)n_rows, kMcThreads, 0, st>>>(scores, score_row_stride, g, top_k, L);
+        cudaError_t e = launch_pdl(topk_mc_bound_kernel, dim3((unsigned)n_rows), dim3(kMcThreads), 0, st, scores,
+                                   score_row_stride, g, top_k, L);
+        if (e != cudaSuccess) return e;
         if (chunks > 0) {
-            dim3 grid((unsigned)chunks, (unsigned)n_rows);
-            topk_mc_filter_kernel<<<grid, kMcThreads, 0, st>>>(scores, score_row_stride, g, top_k, L);
+            e = launch_pdl(topk_mc_filter_kernel, dim3((unsigned)chunks, (unsigned)n_rows), dim3(kMcThreads), 0, st,
+                           scores, score_row_stride, g, top_k, L);
+            if (e != cudaSuccess) return e;
         }
         const size_t sm = sizeof(MapShared);
         cudaFuncSetAttribute(topk_mc_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        topk_mc_finish_kernel<<<(unsigned)n_rows, kMapThreads, sm, st>>>(scores, score_row_stride, g, top_k, L, idx,
-                                                                         idx_row_stride, n_sel);
+        return launch_pdl(topk_mc_finish_kernel, dim3((unsigned)n_rows), dim3(kMapThreads), sm, st, scores,
+                          score_row_stride, g, top_k, L, idx, idx_row_stride, n_sel);
     } else {
         const size_t sm = sizeof(MapShared);
         cudaFuncSetAttribute(topk_map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        topk_map_kernel<<<(unsigned)n_rows, kMapThreads, sm, st>>>(scores, score_row_stride, g, top_k, idx,
-                                                                   idx_row_stride, n_sel);
+        return launch_pdl(topk_map_kernel, dim3((unsigned)n_rows), dim3(kMapThreads), sm, st, scores,
+                          score_row_stride, g, top_k, idx, idx_row_stride, n_sel);
     }
     return cudaGetLastError();
 }

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "lidx.h"
 
 namespace lidx {
@@ -28,6 +30,17 @@ struct Geom {
     int32_t page_size;
     int* status;  // device int: first fault code recorded, 0 = none
 };
+
+// Programmatic dependent launch along the decode chain (scorer -> top-k ->
+// attention -> next step's scorer).  Each kernel of the chain lets the next
+// one launch as soon as all of its CTAs have started (pdl_trigger), and every
+// CTA waits for the previous grid to complete, its writes visible
+// (pdl_wait), before it reads or writes anything another kernel produces or
+// consumes.  Completion therefore stays transitive along the chain; only
+// launch latency and work on pure inputs overlap.  Launched without the
+// attribute, both instructions are no-ops.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void flag(int* status, int code) {
     if (status) atomicCAS(status, 0, code);
@@ -174,6 +187,23 @@ bool make_key8_tmap(CUtensorMap* m, const int8_t* k, int64_t row_bytes, int64_t 
 
 // number of SMs of the current device (cached per device)
 int sm_count();
+
+// launch with programmatic stream serialisation (see pdl_trigger / pdl_wait)
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // set idx_last_error() for the calling thread and return s
 idx_status record_error(idx_status s, const char* msg);
