@@ -59,7 +59,7 @@ WORKLOADS = {
 # the keys it scans), keyed by the SHA-256 of the kernel source it was taken on.  A
 # source change makes the figure stale and the bench reports traffic = null.
 NCU_TRAFFIC = {
-    "58eb46cf034ea00bce5658a18b76f7cb72cf2707fc1be8e9747eddaa221f2946": (268665088 + 5505536) / (8 * 131072),
+    "109a2ab854e599c02be3faceedad79793cb25341a97c6a27b1054b6145e15260": (268644864 + 5571584) / (8 * 131072),
 }
 
 
