@@ -112,7 +112,6 @@ struct Ctl {
     uint32_t tmem_base;
     int abort;
     int n_chunks;
-    int32_t pages[16];         // paged caches: the producer's window of page-table entries
 };
 
 static_assert(kStages <= 8 && kRawStages <= 8, "barrier arrays");
@@ -368,52 +367,50 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int64_t issued = 0;
-            // the next chunk is claimed one chunk ahead, so the counter's round
-            // trip overlaps the current chunk's loads
-            int ch = (int)atomicAdd(&g_score_sched[sched_slot][0], 1u);
-            // paged caches: page-table entries are read 16 at a time (one memory round trip)
-            // into a window, not one dependent load per TMA issue
-            int win_b = -1, win0 = 0;
-            auto page_of = [&](int b, int pg, int last) -> int32_t {
-                if (b != win_b || pg < win0 || pg >= win0 + 16) {
-                    win_b = b;
-                    win0 = pg;
-                    const int64_t base = (int64_t)b * g.page_table_stride;
-                    int32_t e[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) e[i] = pg + i <= last ? g.page_table[base + pg + i] : -1;
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) c.pages[i] = e[i];
-                }
-                return c.pages[pg - win0];
-            };
-            for (int k = 0;; ++k) {
-                const int slot = k % kRing;
+        // Lane 0 claims chunks, waits for free stages and issues the TMA loads.
+        // For paged caches the whole warp first resolves the chunk's key rows
+        // through the page table, one 64-key half per lane, so lane 0's per-tile
+        // work stays as short as in the contiguous case.
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t issued = 0;
+        // the next chunk is claimed one chunk ahead, so the counter's round
+        // trip overlaps the current chunk's loads
+        int ch = 0;
+        if (lane == 0) ch = (int)atomicAdd(&g_score_sched[sched_slot][0], 1u);
+        for (int k = 0;; ++k) {
+            const int slot = k % kRing;
+            int go = 1;
+            if (lane == 0) {
                 if (*(volatile int*)&c.abort || !mbar_wait(&c.cempty[slot], (uint32_t)(((k / kRing) & 1) ^ 1))) {
                     abort_cta(c, g);
-                    break;
+                    go = 0;
+                } else {
+                    const Chunk d = chunk_of(g, pre, nvis, n_rows, prefix, ch, n_chunks);
+                    c.chunk[slot] = d;
+                    mbar_arrive(&c.cfull[slot]);
+                    if (d.row < 0)
+                        go = 0;
+                    else
+                        ch = (int)atomicAdd(&g_score_sched[sched_slot][0], 1u);
                 }
-                const Chunk d = chunk_of(g, pre, nvis, n_rows, prefix, ch, n_chunks);
-                c.chunk[slot] = d;
-                mbar_arrive(&c.cfull[slot]);
-                if (d.row < 0) break;
-                ch = (int)atomicAdd(&g_score_sched[sched_slot][0], 1u);
-                const int b_seq = (int)(d.row / g.T);
-                const int64_t krow0 = g.page_table ? 0 : seq_row0(g, b_seq);
-                const int nk = prefix ? nvis[d.row] : row_n_vis(g, d.row);
-                bool ok = true;
-                for (int t = d.t0; t < d.t1; ++t) {
-                    if (!mbar_wait(&c.empty[stage], phase ^ 1)) {
-                        abort_cta(c, g);
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* dst = tma_tiles + (size_t)stage * kTmaStride;
-                    if (!g.page_table) {
+            }
+            __syncwarp();
+            if (!__shfl_sync(0xffffffffu, go, 0)) break;
+            const Chunk d = c.chunk[slot];
+            const int b_seq = (int)(d.row / g.T);
+            const int nk = prefix ? nvis[d.row] : row_n_vis(g, d.row);
+            int ok = 1;
+            if (!g.page_table) {
+                if (lane == 0) {
+                    const int64_t krow0 = seq_row0(g, b_seq);
+                    for (int t = d.t0; t < d.t1; ++t) {
+                        if (!mbar_wait(&c.empty[stage], phase ^ 1)) {
+                            abort_cta(c, g);
+                            ok = 0;
+                            break;
+                        }
+                        uint8_t* dst = tma_tiles + (size_t)stage * kTmaStride;
                         const int64_t krow = krow0 + (int64_t)t * kTileKeys;
                         // rows past the visible keys may lie past the cache (TMA fills them with 0)
                         const int valid = min(kTileKeys, nk - t * kTileKeys);
@@ -425,37 +422,67 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                             tma_load_2d(dst, &kmap, &c.full[stage], 0, (int32_t)krow);
                             tma_load_2d(dst + kHalfBytes, &kmap, &c.full[stage], 64, (int32_t)krow);
                         }
-                    } else {
-                        // paged cache: two 64-key halves, each inside one page (page_size % 64 == 0);
-                        // a half past the visible keys is not loaded (its keys are never stored)
-                        const int j0 = t * kTileKeys;
-                        const int halves = j0 + 64 < nk ? 2 : 1;
-                        mbar_arrive_expect_tx(&c.full[stage], (uint32_t)(halves * (kTmaBytes / 2)));
-                        for (int hh = 0; hh < halves; ++hh) {
-                            const int jj = j0 + 64 * hh;
-                            const int pg = jj / g.page_size;
-                            const int64_t kr = (int64_t)page_of(b_seq, pg, (nk - 1) / g.page_size) * g.page_size +
-                                               (jj - pg * g.page_size);
-                            if (kr < 0 || kr + min(64, nk - (j0 + 64 * hh)) > k_rows)
-                                flag(g.status, IDX_ERR_DEVICE_BOUNDS);
-                            if constexpr (kQ8) {
-                                tma_load_2d(dst + hh * (kTmaBytes / 2), &kmap, &c.full[stage], 0, (int32_t)kr);
-                            } else {
-                                tma_load_2d(dst + hh * (kHalfBytes / 2), &kmap, &c.full[stage], 0, (int32_t)kr);
-                                tma_load_2d(dst + kHalfBytes + hh * (kHalfBytes / 2), &kmap, &c.full[stage], 64,
-                                            (int32_t)kr);
-                            }
+                        ++issued;
+                        if (++stage == kTmaStages) {
+                            stage = 0;
+                            phase ^= 1;
                         }
                     }
-                    ++issued;
-                    if (++stage == kTmaStages) {
-                        stage = 0;
-                        phase ^= 1;
+                }
+            } else {
+                // paged cache: two 64-key halves per tile, each inside one page
+                // (page_size % 64 == 0); a half past the visible keys is not
+                // loaded (its keys are never stored).  16 tiles = 32 halves per pass.
+                for (int tg = d.t0; ok && tg < d.t1; tg += 16) {
+                    const int tn = min(16, d.t1 - tg);
+                    const int jj = tg * kTileKeys + 64 * lane;
+                    int64_t kr = 0;
+                    if (lane < 2 * tn && jj < nk) {
+                        const int pg = jj / g.page_size;
+                        kr = (int64_t)g.page_table[(int64_t)b_seq * g.page_table_stride + pg] * g.page_size +
+                             (jj - pg * g.page_size);
+                        if (kr < 0 || kr + min(64, nk - jj) > k_rows) flag(g.status, IDX_ERR_DEVICE_BOUNDS);
+                    }
+                    for (int i = 0; i < tn; ++i) {
+                        const int64_t kr0 = __shfl_sync(0xffffffffu, kr, 2 * i);
+                        const int64_t kr1 = __shfl_sync(0xffffffffu, kr, 2 * i + 1);
+                        if (lane == 0) {
+                            if (!mbar_wait(&c.empty[stage], phase ^ 1)) {
+                                abort_cta(c, g);
+                                ok = 0;
+                            } else {
+                                uint8_t* dst = tma_tiles + (size_t)stage * kTmaStride;
+                                const int j0 = (tg + i) * kTileKeys;
+                                const int halves = j0 + 64 < nk ? 2 : 1;
+                                mbar_arrive_expect_tx(&c.full[stage], (uint32_t)(halves * (kTmaBytes / 2)));
+                                for (int hh = 0; hh < halves; ++hh) {
+                                    const int32_t kr_h = (int32_t)(hh ? kr1 : kr0);
+                                    if constexpr (kQ8) {
+                                        tma_load_2d(dst + hh * (kTmaBytes / 2), &kmap, &c.full[stage], 0, kr_h);
+                                    } else {
+                                        tma_load_2d(dst + hh * (kHalfBytes / 2), &kmap, &c.full[stage], 0, kr_h);
+                                        tma_load_2d(dst + kHalfBytes + hh * (kHalfBytes / 2), &kmap, &c.full[stage],
+                                                    64, kr_h);
+                                    }
+                                }
+                                ++issued;
+                                if (++stage == kTmaStages) {
+                                    stage = 0;
+                                    phase ^= 1;
+                                }
+                            }
+                        }
+                        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                            ok = 0;
+                            break;
+                        }
                     }
                 }
-                if (!ok) break;
             }
-            // never leave the CTA with TMA writes in flight
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        }
+        // never leave the CTA with TMA writes in flight
+        if (lane == 0) {
             const int64_t n = issued < kTmaStages ? issued : kTmaStages;
             for (int64_t i = issued - n; i < issued; ++i)
                 mbar_wait(&c.full[i % kTmaStages], (uint32_t)((i / kTmaStages) & 1));
