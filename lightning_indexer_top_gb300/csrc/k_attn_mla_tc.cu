@@ -9,24 +9,26 @@
 // so one work unit (query row, key split) runs on a CLUSTER OF TWO CTAs:
 //   rank 0: Q [128 x 576] bf16 lives in TMEM (288 columns) as the MMA A
 //           operand; key tiles of 64 selected rows x 576 are gathered with
-//           16-byte cp.async copies (128-byte swizzle) into a 2-stage ring;
+//           16-byte cp.async copies (128-byte swizzle) into a 3-stage ring;
 //           S = Q K^T (M=128 heads, N=64 keys, K=576) goes to one of two TMEM
 //           buffers; four softmax warps (thread = head) turn S into
-//           P = 2^(S*scale*log2e - m) as bf16 and stage P with the per-head
-//           rescale factor, row sum and max; a sender warp bulk-copies the
-//           packet into rank 1's shared memory (DSMEM).
+//           P = 2^(S*scale*log2e - m) as bf16 and write P, the per-head
+//           rescale factor, row sum and max straight into rank 1's packet
+//           slot with st.async stores that complete the slot's barrier there.
 //   rank 1: O lives in TMEM (512 columns); value tiles (the same rows, first
-//           512 columns) are gathered into its own ring; O += P V with P as a
-//           K-major and V as an MN-major shared-memory operand (M=128,
+//           512 columns) are gathered into its own 2-stage ring; O += P V with
+//           P as a K-major and V as an MN-major shared-memory operand (M=128,
 //           N=256 x 2, K=16 x 4).  Four correction warps rescale their heads'
 //           O rows when rank 0 raised a row maximum by more than 2^8 (rare
 //           after the first tiles, so P stays <= 2^8 otherwise) and finally
 //           write O / l, or the unnormalised partial (O, m, l) of a key split.
 // Each CTA first turns its slice of the index list into cache rows and a
-// validity bitmask in shared memory; padding and invalid indices gather a
-// valid row and get p = 0.  Key splits (few query rows) are merged by a small
-// combine kernel.  Every wait is bounded; a timeout records IDX_ERR_TIMEOUT
-// and the cluster winds down.
+// validity bitmask in shared memory (rank 0 meanwhile puts Q into TMEM);
+// padding and invalid indices gather a valid row and get p = 0.  Key splits
+// (few query rows) are merged by a small combine kernel.  Both kernels take
+// part in the decode launch chain (pdl_trigger / pdl_wait): everything up to
+// the Q load runs while the previous kernel drains.  Every wait is bounded; a
+// timeout records IDX_ERR_TIMEOUT and the cluster winds down.
 #include "lidx_internal.cuh"
 #include "sm100_ptx.cuh"
 

@@ -315,22 +315,5 @@ __device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t bar_cluste
                  : "memory");
 }
 
-// bulk copy from this CTA's shared memory into another CTA's, completing
-// `bytes` of transactions on that CTA's mbarrier
-__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst_cluster, const void* src, uint32_t bytes,
-                                                    uint32_t bar_cluster) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst_cluster), "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
 }  // namespace sm100
 }  // namespace lidx
