@@ -229,3 +229,46 @@ def test_paged_decode_workload_sampled_rows():
     assert wl.page_table is not None and wl.name.endswith("_paged")
     st = _run(wl)
     _report("paged", _check_mla_rows(wl, st, [0, 3, 5]))
+
+
+@pytest.mark.parametrize("make_args", [(("headline",), {"batch_override": 16, "n_kv_override": 65536}), ((2,), {})],
+                         ids=["16x65536", "8x8192"])
+def test_decode_chain_back_to_back_equals_synchronised_steps(make_args):
+    # The decode kernels chain with programmatic dependent launch: each kernel may start while its
+    # predecessor drains and must wait for it before touching its outputs. Alternating two query sets
+    # makes any read of a stale buffer visible: back-to-back steps, never synchronised, must give exactly
+    # the selections and outputs of steps synchronised after every call.
+    args, kw = make_args
+    wl = workloads.make(*args, **kw)
+    st = SparseAttentionStep(wl)
+    sets = {
+        "a": (wl.q_idx.clone(), wl.w.clone(), wl.q_attn.clone()),
+        "b": (wl.q_idx.flip(0).clone(), wl.w.flip(0).clone(), wl.q_attn.flip(0).clone()),
+    }
+
+    def load(name):
+        q, w, qa = sets[name]
+        wl.q_idx.copy_(q)
+        wl.w.copy_(w)
+        wl.q_attn.copy_(qa)
+
+    ref = {}
+    for name in "ab":
+        load(name)
+        torch.cuda.synchronize()
+        for call in (st.score, st.select, st.attend):
+            call()
+            torch.cuda.synchronize()
+        ref[name] = (st.n_sel.clone(), st.idx.clone(), st.out.clone())
+    assert not torch.equal(ref["a"][1], ref["b"][1])
+    got = []
+    for i in range(6):
+        name = "ab"[i % 2]
+        load(name)
+        st.run()
+        got.append((name, st.n_sel.clone(), st.idx.clone(), st.out.clone()))
+    torch.cuda.synchronize()
+    assert L.idx_device_status(reset=True) == 0
+    for name, n_sel, idx, out in got:
+        assert torch.equal(n_sel, ref[name][0]) and torch.equal(idx, ref[name][1]), name
+        assert torch.equal(out, ref[name][2]), name
