@@ -13,8 +13,9 @@
 // Costs and rules:
 //  - The array is kScratchBytes (20,000,768 bytes = 76 key-split units of
 //    128 heads x (512 + 2) floats): enough for every split count the
-//    attention chooses on a 152-SM GB300.  Every GPU that loads the library
-//    holds it until the process exits.
+//    attention chooses on a 152-SM GB300 when each row selects at most 2048
+//    keys (rows with more keys are always split, rows x splits units).
+//    Every GPU that loads the library holds it until the process exits.
 //  - A call whose key-split partials would not fit is rejected with
 //    IDX_ERR_INVALID_ARG before anything is launched.
 //  - All calls share the one array, and it keeps the contents of the last
