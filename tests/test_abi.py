@@ -104,3 +104,24 @@ def test_default_top_k_minus_one(lib):
         assert lib.idx_workspace_size(L.IDX_OP_TOPK, rows, 131072, -1, 0, 0) == \
             lib.idx_workspace_size(L.IDX_OP_TOPK, rows, 131072, 2048, 0, 0)
     assert L.topk_capacity(-1) == 2048
+
+
+def test_mla_attention_workspace_follows_the_split_policy(lib):
+    # Host policy of the MLA attention (no GPU needed; without one the library assumes GB300's 152 SMs):
+    # few rows spread their selection over key splits until the 76 two-CTA clusters are covered (at least
+    # 256 keys per split); a split never holds more than 2048 selected keys; one split needs no workspace,
+    # otherwise every (row, split) keeps 128 heads x (512 + 2) f32 partials.
+    def expected(rows, cap):
+        clusters = 152 // 2
+        min_s = -(-cap // 2048) if cap > 2048 else 1
+        s = min(clusters // rows, -(-cap // 256)) if rows < clusters else 1
+        s = max(s, min_s, 1)
+        return 0 if s <= 1 else rows * s * 128 * 514 * 4
+    for rows, cap in ((64, 2048), (8, 2048), (1, 2048), (75, 2048), (76, 2048), (1000, 2048), (100, 4096),
+                      (8, 4096), (1, 100000), (300, 6000), (3, 300)):
+        got = lib.idx_workspace_size(L.IDX_OP_ATTN_DECODE, rows, 131072, cap, 128, 512)
+        assert got == expected(rows, cap), (rows, cap, got)
+        assert lib.idx_workspace_size(L.IDX_OP_ATTN_PREFILL, rows, 131072, cap, 128, 512) == got
+    # the headline (64 rows x 2048) needs none; 8 rows split 8 ways
+    assert lib.idx_workspace_size(L.IDX_OP_ATTN_DECODE, 64, 131072, 2048, 128, 512) == 0
+    assert lib.idx_workspace_size(L.IDX_OP_ATTN_DECODE, 8, 8192, 2048, 128, 512) == 8 * 8 * 128 * 514 * 4
