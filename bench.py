@@ -198,7 +198,8 @@ def run_reference(args):
     import torch
     from lightning_indexer_top_gb300 import workloads
     wl = workloads.make("headline", device="cpu", batch_override=1)
-    for _ in range(args.warmup):
+    warmup = max(args.warmup, 3)
+    for _ in range(warmup):
         cpu_oracle_queries(wl, [0])
     t = 0.0
     for _ in range(args.steps):
@@ -206,7 +207,7 @@ def run_reference(args):
         t += dt
     v = args.steps / t
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "steps": args.steps, "warmup": warmup, "ms_per_step": 1e3 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) inputs)",
             "config": {"workload": WORKLOAD, "sample": "1 query of the workload per step",
