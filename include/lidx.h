@@ -310,10 +310,13 @@ idx_status sparse_attn_prefill(const void* q, idx_dtype dtype, int32_t n_q_heads
  *   20,000,768 bytes that belongs to the library (held by every GPU that
  *   loads it until the process exits).
  *   Supported: dtype BF16, n_q_heads 128, n_kv_heads 1, dk 576, dv 512,
- *   16-byte aligned q/k/out, kv_row_stride % 8 == 0 (else UNSUPPORTED).
- *   The array covers every split of rows selecting at most 2048 keys; a
- *   call whose partials would not fit (many rows selecting more) returns
- *   INVALID_ARG without launching anything.  The array is shared by all calls and keeps
+ *   16-byte aligned q/k/out, kv_row_stride % 8 == 0 (else UNSUPPORTED);
+ *   kv_row_stride < 576 (overlapping, zero or negative) is INVALID_ARG.
+ *   On a device with at most 152 SMs (a GB300) the array covers every
+ *   split of rows selecting at most 2048 keys; a call whose partials would
+ *   not fit (rows selecting more keys, or a device with more SMs, where the
+ *   split policy may use more units) returns INVALID_ARG without launching
+ *   anything.  The array is shared by all calls and keeps
  *   the last call's contents (nothing in it must start at zero); calls whose
  *   work overlaps on the GPU race on it and must be serialised by the caller.
  *   The first call on each device, with that device current, looks up the

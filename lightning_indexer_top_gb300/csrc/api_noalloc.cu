@@ -13,8 +13,11 @@
 // Costs and rules:
 //  - The array is kScratchBytes (20,000,768 bytes = 76 key-split units of
 //    128 heads x (512 + 2) floats): enough for every split count the
-//    attention chooses on a 152-SM GB300 when each row selects at most 2048
-//    keys (rows with more keys are always split, rows x splits units).
+//    attention chooses on a device with at most 152 SMs (a GB300) when each
+//    row selects at most 2048 keys.  The split policy reads the SM count at
+//    run time and uses at most SMs/2 units for such rows, so a device with
+//    more SMs, or rows selecting more keys (always split, rows x splits
+//    units), can need more: such calls are rejected, never truncated.
 //    Every GPU that loads the library holds it until the process exits.
 //  - A call whose key-split partials would not fit is rejected with
 //    IDX_ERR_INVALID_ARG before anything is launched.
@@ -85,6 +88,11 @@ extern "C" idx_status sparse_attn_decode_noalloc(const void* q, idx_dtype dtype,
     if (rows == 0) return IDX_OK;
     if (!q || !k || !idx || !n_sel || !out)
         return record_error(IDX_ERR_INVALID_ARG, "sparse_attn_decode_noalloc: NULL q/k/idx/n_sel/out");
+    // the same row-stride rule as sparse_attn_decode: a latent row must not
+    // overlap the next one (this also rules out zero and negative strides)
+    if (n_kv_heads < 1 || dk < 1 || kv_row_stride < (int64_t)n_kv_heads * dk)
+        return record_error(IDX_ERR_INVALID_ARG, "sparse_attn_decode_noalloc: kv_row_stride < Hkv*dk");
+    if (kv_rows < 0) return record_error(IDX_ERR_INVALID_ARG, "sparse_attn_decode_noalloc: kv_rows < 0");
     if (!mla_tc_supported(dtype, n_q_heads, n_kv_heads, dk, dv, k, nullptr, kv_row_stride, kv_rows, q, out))
         return record_error(IDX_ERR_UNSUPPORTED,
                             "sparse_attn_decode_noalloc: serves only bf16 MLA latent attention with 128 query "
@@ -93,7 +101,8 @@ extern "C" idx_status sparse_attn_decode_noalloc(const void* q, idx_dtype dtype,
     if (need > kScratchBytes)
         return record_error(IDX_ERR_INVALID_ARG,
                             "sparse_attn_decode_noalloc: the key-split partials of this call exceed the "
-                            "20,000,768-byte static scratch array; use sparse_attn_decode with a workspace");
+                            "20,000,768-byte static scratch array (sized for devices with at most 152 SMs "
+                            "and rows selecting at most 2048 keys); use sparse_attn_decode with a workspace");
     void* scratch = nullptr;
     if (need > 0) {
         const idx_status s = scratch_ptr(&scratch);
