@@ -113,40 +113,6 @@ def hadamard_rotate(x, store: str | None = None) -> np.ndarray:
     return y
 
 
-def hadamard_store(x, store: str) -> np.ndarray:
-    """The rotated rows as the cache stores them: H x computed in float32, then
-    rounded once to ``store`` ("bf16", "f16" or "f32"); returned widened to
-    float64.
-
-    The pages compute the rotation inside the f32 compute graph and copy the
-    result into the F16 key cache (ik_llama.cpp PR #2058, commit
-    "decode-correct via persistent indexer-K cache": the batch's rotated keys
-    are written to kr_l; later "use builtin Hadamard").  Rounding to the cache
-    dtype is a quantisation decided by floating point, so it is decided here in
-    that same f32 precision: the Walsh-Hadamard butterflies in natural order
-    (stage h = 1, 2, 4, ...: (a, b) -> (a + b, a - b) for each pair e, e + h
-    with e & h == 0), each add rounded to float32, then one float32 multiply by
-    float32(1/sqrt(d)), then one rounding to the storage type.  Pinned against
-    the exact rotation :func:`hadamard_rotate`.
-    """
-    x = np.asarray(x, dtype=np.float64)
-    d = x.shape[-1]
-    if d < 1 or d & (d - 1):
-        raise ValueError("Hadamard order must be a power of two")
-    v = x.astype(np.float32).reshape(-1, d).copy()
-    h = 1
-    while h < d:
-        v = v.reshape(-1, d // (2 * h), 2, h)
-        a = v[:, :, 0, :].copy()
-        b = v[:, :, 1, :].copy()
-        v[:, :, 0, :] = a + b
-        v[:, :, 1, :] = a - b
-        v = v.reshape(-1, d)
-        h *= 2
-    v = v * np.float32(1.0 / math.sqrt(d))
-    return round_to_storage(v.astype(np.float64), store).reshape(x.shape)
-
-
 # ---------------------------------------------------------------------------
 # S3: visibility
 # ---------------------------------------------------------------------------

@@ -1,9 +1,11 @@
-"""Pins of the CPU oracle against what the pages and the mathematics fix.
+"""Pins of the CPU oracles against what the pages and the mathematics fix.
 
 Each test ties an oracle function to something other than its own code: a
 hand-worked example (tests/golden), a closed form, a library routine that
 computes the same thing by another method, brute-force enumeration on tiny
-inputs, or an invariant the pages state.  All run on the CPU.
+inputs, or an invariant the pages state.  Every pin runs against both
+oracles -- the numpy one and the C++ one -- through the fixture ``O``; the last
+tests also hold the two against each other.  All run on the CPU.
 """
 
 import itertools
@@ -14,7 +16,13 @@ import pytest
 import scipy.linalg
 import torch
 
-import oracle as O
+import oracle
+import oracle.cpp
+
+
+@pytest.fixture(params=["numpy", "cpp"])
+def O(request):
+    return oracle if request.param == "numpy" else oracle.cpp
 
 
 def _lnfix(x):
@@ -23,7 +31,7 @@ def _lnfix(x):
 
 # ---------------------------------------------------------------- rounding
 
-def test_round_f16_matches_numpy_half():
+def test_round_f16_matches_numpy_half(O):
     rng = np.random.default_rng(1)
     x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-6, 5, 20000),
                         [0.0, -0.0, 65504.0, 65519.0, 65520.0, 6.1e-5, 5.96e-8, 2.98e-8, 2.99e-8]])
@@ -32,7 +40,7 @@ def test_round_f16_matches_numpy_half():
     np.testing.assert_array_equal(ours, ref)
 
 
-def test_round_bf16_matches_torch_for_float32_values():
+def test_round_bf16_matches_torch_for_float32_values(O):
     # for values exact in float32, torch's float32 -> bfloat16 cast is a single RNE rounding
     g = torch.Generator().manual_seed(2)
     x = (torch.randn(50000, generator=g) * torch.exp(torch.randn(50000, generator=g) * 8)).float()
@@ -41,7 +49,7 @@ def test_round_bf16_matches_torch_for_float32_values():
     np.testing.assert_array_equal(ours, ref)
 
 
-def test_round_ties_to_even_closed_form():
+def test_round_ties_to_even_closed_form(O):
     # bf16 spacing at 1 is 2**-7: 1 + 2**-8 is a tie -> 1 (even); 1 + 3*2**-8 -> 1 + 2**-6
     assert O.round_to_storage([1 + 2 ** -8], "bf16")[0] == 1.0
     assert O.round_to_storage([1 + 3 * 2 ** -8], "bf16")[0] == 1 + 2 ** -6
@@ -54,11 +62,11 @@ def test_round_ties_to_even_closed_form():
 # ---------------------------------------------------------------- Hadamard
 
 @pytest.mark.parametrize("d", [1, 2, 8, 32, 128])
-def test_hadamard_matrix_equals_scipy(d):
+def test_hadamard_matrix_equals_scipy(O, d):
     np.testing.assert_allclose(O.hadamard_matrix(d), scipy.linalg.hadamard(d) / math.sqrt(d), rtol=0, atol=1e-15)
 
 
-def test_hadamard_matrix_closed_form_entries():
+def test_hadamard_matrix_closed_form_entries(O):
     d = 128
     h = O.hadamard_matrix(d)
     i, j = np.meshgrid(np.arange(d), np.arange(d), indexing="ij")
@@ -66,7 +74,7 @@ def test_hadamard_matrix_closed_form_entries():
     np.testing.assert_array_equal(h * math.sqrt(d), sign)
 
 
-def test_hadamard_orthonormal_symmetric():
+def test_hadamard_orthonormal_symmetric(O):
     h = O.hadamard_matrix(128)
     np.testing.assert_allclose(h @ h, np.eye(128), atol=1e-13)
     np.testing.assert_array_equal(h, h.T)
@@ -85,7 +93,7 @@ def _fwht(v):
     return np.array(v) / math.sqrt(len(v))
 
 
-def test_hadamard_rotate_equals_butterfly_fwht():
+def test_hadamard_rotate_equals_butterfly_fwht(O):
     rng = np.random.default_rng(3)
     x = rng.standard_normal((5, 128))
     y = O.hadamard_rotate(x)
@@ -96,7 +104,7 @@ def test_hadamard_rotate_equals_butterfly_fwht():
     np.testing.assert_allclose(O.hadamard_rotate(e0), np.full(128, 1 / math.sqrt(128)), atol=1e-15)
 
 
-def test_hadamard_round_trip_and_score_invariance():
+def test_hadamard_round_trip_and_score_invariance(O):
     rng = np.random.default_rng(4)
     q = rng.standard_normal((8, 128)); k = rng.standard_normal((300, 128)); w = rng.standard_normal(8)
     np.testing.assert_allclose(O.hadamard_rotate(O.hadamard_rotate(q)), q, atol=1e-12)
@@ -105,7 +113,7 @@ def test_hadamard_round_trip_and_score_invariance():
     np.testing.assert_allclose(s1, s0, rtol=1e-6, atol=1e-6)
 
 
-def test_hadamard_store_rounds_once():
+def test_hadamard_store_rounds_once(O):
     rng = np.random.default_rng(5)
     x = O.round_to_storage(rng.standard_normal((4, 128)), "bf16")
     y = O.hadamard_rotate(x, store="bf16")
@@ -114,14 +122,14 @@ def test_hadamard_store_rounds_once():
 
 # ---------------------------------------------------------------- score
 
-def test_score_worked_example(golden):
+def test_score_worked_example(O, golden):
     g = golden["score"]
     s = O.indexer_scores(np.array(g["q"], float), np.array(g["w"]), np.array(g["k"], float))
     assert s.dtype == np.float32
     np.testing.assert_array_equal(s, np.array(g["expected"], np.float32))
 
 
-def test_score_closed_form_unit_query():
+def test_score_closed_form_unit_query(O):
     # one head, weight 1, q = e_c  ->  score_j = relu(k_jc)
     rng = np.random.default_rng(6)
     k = rng.standard_normal((50, 16))
@@ -130,7 +138,7 @@ def test_score_closed_form_unit_query():
         np.testing.assert_array_equal(O.indexer_scores(q, [1.0], k), np.maximum(k[:, c], 0).astype(np.float32))
 
 
-def test_score_relu_before_head_sum_and_homogeneity():
+def test_score_relu_before_head_sum_and_homogeneity(O):
     rng = np.random.default_rng(7)
     q = rng.standard_normal((4, 8)); k = rng.standard_normal((40, 8)); w = rng.uniform(0.1, 1, 4)
     s = O.indexer_scores(q, w, k).astype(np.float64)
@@ -151,7 +159,7 @@ def test_score_relu_before_head_sum_and_homogeneity():
 
 # ---------------------------------------------------------------- top-k
 
-def test_topk_worked_example(golden):
+def test_topk_worked_example(O, golden):
     g = golden["topk"]
     for c in g["cases"]:
         got = O.topk_select(np.array(g["scores"], np.float32), c["n_vis"], c["top_k"])
@@ -170,7 +178,7 @@ def _valid_topk_sets(s, k):
     return out
 
 
-def test_topk_brute_force_enumeration_with_ties():
+def test_topk_brute_force_enumeration_with_ties(O):
     rng = np.random.default_rng(8)
     for trial in range(300):
         n = int(rng.integers(1, 10))
@@ -183,7 +191,7 @@ def test_topk_brute_force_enumeration_with_ties():
         assert O.topk_select(s, n_vis, k).tolist() == sets[0]
 
 
-def test_topk_equals_python_stable_sort():
+def test_topk_equals_python_stable_sort(O):
     rng = np.random.default_rng(9)
     for _ in range(20):
         n = int(rng.integers(1, 3000))
@@ -193,20 +201,20 @@ def test_topk_equals_python_stable_sort():
         assert O.topk_select(s, n, k).tolist() == ref
 
 
-def test_topk_negative_zero_ties_with_zero():
+def test_topk_negative_zero_ties_with_zero(O):
     s = np.array([-0.0, 0.0, -0.0, 1.0], np.float32)
     assert O.topk_select(s, 4, 2).tolist() == [0, 3]
 
 
 # ---------------------------------------------------------------- blocks
 
-def test_block_pool_worked_example(golden):
+def test_block_pool_worked_example(O, golden):
     g = golden["block_pool"]
     got = O.block_pool(np.array(g["k_raw"], float), g["C"], len(g["k_raw"]))
     np.testing.assert_array_equal(got, np.array(g["expected"], np.float32))
 
 
-def test_block_pool_closed_forms():
+def test_block_pool_closed_forms(O):
     # C = 1: pooled keys are the keys; a linear ramp pools to the block midpoint
     rng = np.random.default_rng(10)
     k = O.round_to_storage(rng.standard_normal((33, 4)), "f32")
@@ -216,7 +224,7 @@ def test_block_pool_closed_forms():
     assert O.block_pool(t, 8, 7).shape == (0, 3)
 
 
-def test_block_select_worked_example(golden):
+def test_block_select_worked_example(O, golden):
     g = golden["block_select"]
     for c in g["cases"]:
         got = O.block_select(np.array(c["block_scores"], np.float32), c["n_vis"], g["top_k"], g["C"])
@@ -225,7 +233,7 @@ def test_block_select_worked_example(golden):
         assert got2.tolist() == c["expected"], c
 
 
-def test_block_selection_equals_expansion_and_whole_blocks():
+def test_block_selection_equals_expansion_and_whole_blocks(O):
     rng = np.random.default_rng(11)
     for _ in range(400):
         C = int(rng.choice([1, 2, 3, 4, 8]))
@@ -245,7 +253,7 @@ def test_block_selection_equals_expansion_and_whole_blocks():
         assert len(body) == min(top_k // C, n_cb) * C
 
 
-def test_block_dense_threshold_both_sides():
+def test_block_dense_threshold_both_sides(O):
     rng = np.random.default_rng(12)
     for C in (2, 4, 64):
         for top_k in (C, 4 * C, 32 * C):
@@ -257,7 +265,7 @@ def test_block_dense_threshold_both_sides():
             assert len(O.block_select(bs, n, top_k, C)) == top_k
 
 
-def test_block_select_brute_force_blocks():
+def test_block_select_brute_force_blocks(O):
     rng = np.random.default_rng(13)
     for _ in range(200):
         C = int(rng.integers(1, 4)); n_vis = int(rng.integers(1, 16)); top_k = int(rng.integers(1, 12))
@@ -272,7 +280,7 @@ def test_block_select_brute_force_blocks():
 
 # ---------------------------------------------------------------- attention
 
-def test_attention_worked_examples(golden):
+def test_attention_worked_examples(O, golden):
     g = golden["attention"]["gqa"]
     out = O.attention_over(np.array(g["q"], float), np.array(_lnfix(g["K"])), np.array(g["V"], float), g["scale"])
     np.testing.assert_allclose(out, g["expected"], rtol=1e-14)
@@ -281,7 +289,7 @@ def test_attention_worked_examples(golden):
     np.testing.assert_allclose(out, m["expected"], rtol=1e-14)
 
 
-def test_dense_attention_equals_torch_sdpa_causal_gqa():
+def test_dense_attention_equals_torch_sdpa_causal_gqa(O):
     # library routine: scaled_dot_product_attention in float64 with a causal mask
     g = torch.Generator().manual_seed(14)
     T, Hq, Hkv, dk, dv = 24, 8, 2, 16, 12
@@ -298,7 +306,7 @@ def test_dense_attention_equals_torch_sdpa_causal_gqa():
         np.testing.assert_allclose(out, ref[t].numpy(), rtol=1e-12, atol=1e-12)
 
 
-def test_attention_closed_forms():
+def test_attention_closed_forms(O):
     rng = np.random.default_rng(15)
     K = rng.standard_normal((10, 2, 8)); V = rng.standard_normal((10, 2, 5))
     q = rng.standard_normal((4, 8))
@@ -315,7 +323,7 @@ def test_attention_closed_forms():
     np.testing.assert_allclose(out[1], lat[[0, 5], :16].mean(0), rtol=1e-13)
 
 
-def test_sparse_equals_dense_when_topk_covers_visible():
+def test_sparse_equals_dense_when_topk_covers_visible(O):
     # exact no-op when top_k >= visible keys (ik_llama.cpp PR #2058 validation)
     rng = np.random.default_rng(16)
     n, H, d = 40, 4, 16
@@ -327,7 +335,7 @@ def test_sparse_equals_dense_when_topk_covers_visible():
         np.testing.assert_array_equal(out, O.dense_attention_mla(qa, lat, n_vis, 0.2, dv=16))
 
 
-def test_visible_count():
+def test_visible_count(O):
     assert O.visible_count(100, None) == 100
     assert O.visible_count(100, 0) == 1
     assert O.visible_count(100, 99) == 100
@@ -335,7 +343,7 @@ def test_visible_count():
     assert O.visible_count(100, -1) == 0
 
 
-def test_attention_large_logits_limit():
+def test_attention_large_logits_limit(O):
     # logits of order 1e4: softmax is the one-hot of the largest logit, so o = v of that key
     rng = np.random.default_rng(17)
     K = rng.standard_normal((6, 1, 4)); V = rng.standard_normal((6, 1, 3))
@@ -346,37 +354,7 @@ def test_attention_large_logits_limit():
     np.testing.assert_allclose(out[0], V[best, 0], rtol=1e-9, atol=1e-12)
 
 
-def test_hadamard_store_close_to_exact_rotation():
-    # the f32 butterflies land within one storage ulp (+ the f32 error bound) of the exact
-    # rotation rounded once, and agree with it on almost every element
-    rng = np.random.default_rng(18)
-    for fmt, p in (("bf16", 8), ("f16", 11)):
-        x = O.round_to_storage(rng.standard_normal((400, 128)), fmt)
-        got = O.hadamard_store(x, fmt)
-        exact = O.hadamard_rotate(x)
-        ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(exact), 1e-30))) - (p - 1))
-        f32_bound = 8 * 2.0 ** -24 * np.abs(x).sum(axis=1, keepdims=True) / math.sqrt(128)
-        assert np.all(np.abs(got - exact) <= ulp + f32_bound)
-        assert np.mean(got == O.round_to_storage(exact, fmt)) > 0.995
-    # f32 storage: the f32 result itself, close to the exact rotation
-    x = rng.standard_normal((10, 64))
-    np.testing.assert_allclose(O.hadamard_store(x, "f32"), O.hadamard_rotate(x.astype(np.float32)), rtol=0, atol=1e-5)
-
-
-def test_hadamard_store_exact_on_integer_inputs():
-    # small integers: every butterfly is exact in f32, so only the final scale and rounding remain
-    rng = np.random.default_rng(19)
-    x = rng.integers(-8, 9, (20, 32)).astype(float)
-    sums = O.hadamard_rotate(x) * math.sqrt(32)          # integer Walsh sums
-    np.testing.assert_allclose(sums, np.round(sums), atol=1e-9)
-    expect = O.round_to_storage((np.round(sums).astype(np.float32) * np.float32(1 / math.sqrt(32))).astype(np.float64), "bf16")
-    np.testing.assert_array_equal(O.hadamard_store(x, "bf16"), expect)
-    # an involution up to rounding: applying it twice returns the input
-    y = O.hadamard_store(O.hadamard_store(x, "f32"), "f32")
-    np.testing.assert_allclose(y, x, atol=1e-5)
-
-
-def test_block_pool_update_worked_example(golden):
+def test_block_pool_update_worked_example(O, golden):
     g = golden["block_pool_update"]
     prev = np.zeros((4, 1), np.float32)
     prev[:2, 0] = g["pooled_before"]
@@ -388,7 +366,7 @@ def test_block_pool_update_worked_example(golden):
 
 @pytest.mark.parametrize("n_prev,n_new,stale", [(0, 100, None), (64, 100, None), (64, 100, 37), (96, 130, 95),
                                                  (96, 96, 0), (40, 200, -1), (200, 200, None), (128, 131, 127)])
-def test_block_pool_update_equals_full_pool_after_edits(n_prev, n_new, stale):
+def test_block_pool_update_equals_full_pool_after_edits(O, n_prev, n_new, stale):
     # invariant: pool the old keys, edit positions >= stale, append to n_new, update
     # -> identical to pooling the new keys from scratch; rows before beta0 keep their bits
     rng = np.random.default_rng(n_prev * 1000 + n_new)
@@ -408,7 +386,7 @@ def test_block_pool_update_equals_full_pool_after_edits(n_prev, n_new, stale):
     assert np.all(got[n_cb:] == prev[n_cb:])
 
 
-def test_block_pool_update_without_stale_marker_keeps_old_blocks():
+def test_block_pool_update_without_stale_marker_keeps_old_blocks(O):
     # an edit the caller does not report is not seen: blocks before n_pooled stay as they were
     C, d = 4, 3
     k = np.arange(48.0).reshape(16, d)
@@ -421,7 +399,7 @@ def test_block_pool_update_without_stale_marker_keeps_old_blocks():
     np.testing.assert_array_equal(got, O.block_pool(k2, C, 16))
 
 
-def test_quantize_rows_worked_values():
+def test_quantize_rows_worked_values(O):
     # amax 127 -> scale exactly 1, so the codes are rint(x) with ties to even
     x = np.array([[127.0, 2.5, 3.5, -2.5, -0.5, 126.6, -127.0, 0.49]])
     q, s = O.quantize_rows(x)
@@ -431,7 +409,7 @@ def test_quantize_rows_worked_values():
     assert np.all(s == 0) and np.all(q == 0)
 
 
-def test_quantize_rows_invariants():
+def test_quantize_rows_invariants(O):
     rng = np.random.default_rng(5)
     x = rng.standard_normal((200, 128)).astype(np.float32) * rng.uniform(1e-3, 50, (200, 1)).astype(np.float32)
     q, s = O.quantize_rows(x)
@@ -441,7 +419,7 @@ def test_quantize_rows_invariants():
     assert np.all(err <= s[:, None].astype(np.float64) * (0.5 + 1e-5))
 
 
-def test_scores_of_quantized_keys_within_the_dequantization_bound():
+def test_scores_of_quantized_keys_within_the_dequantization_bound(O):
     # |relu(a) - relu(b)| <= |a - b| and |q_h . (k - k_hat)| <= ||q_h||_1 * scale / 2
     rng = np.random.default_rng(6)
     H, d, n = 8, 64, 50
@@ -454,3 +432,88 @@ def test_scores_of_quantized_keys_within_the_dequantization_bound():
     bound = np.abs(w) @ np.abs(q).sum(axis=1) * sc.astype(np.float64) / 2
     assert np.all(np.abs(exact - quant) <= bound + 1e-5 * np.abs(exact) + 1e-6)
     assert np.max(np.abs(exact - quant)) > 0                       # the codes are not the keys
+
+
+def test_dequantize_negative_scale_worked_example(O, golden):
+    g = golden["quantized_keys"]
+    k = O.dequantize_rows(np.array(g["codes"], np.int8), np.array(g["scale"], np.float32))
+    np.testing.assert_array_equal(k, np.array(g["dequantized"]))
+    s = O.indexer_scores(np.array(g["q"], float), np.array(g["w"]), k)
+    np.testing.assert_array_equal(s, np.array(g["expected_scores"], np.float32))
+    if hasattr(O, "scores_batch"):
+        # the batch form reads the int8 codes and their scales as stored
+        s8 = O.scores_batch(np.array(g["q"], float)[None], np.array(g["w"])[None], np.array(g["codes"], np.int8),
+                            [0], [2], k_scale=np.array(g["scale"], np.float32))
+        np.testing.assert_array_equal(s8[0], np.array(g["expected_scores"], np.float32))
+
+
+# ---------------------------------------------------------------- the two oracles against each other
+
+def _f32_ulp(x):
+    return np.spacing(np.abs(np.asarray(x, np.float32))).astype(np.float64)
+
+
+def test_oracles_agree_on_scores_and_selection():
+    # independent implementations (numpy matmuls vs C++ loops): the same double values up to summation
+    # order, so the f32 scores differ by at most one rounding step; on the same scores the selections,
+    # both block forms and the pooled keys are identical
+    rng = np.random.default_rng(20)
+    cpp = oracle.cpp
+    for n, H, d in ((1, 1, 1), (37, 4, 32), (700, 64, 128)):
+        q = rng.standard_normal((H, d)); w = rng.standard_normal(H) / 8; k = rng.standard_normal((n, d))
+        a, b = oracle.indexer_scores(q, w, k), cpp.indexer_scores(q, w, k)
+        assert np.all(np.abs(a.astype(np.float64) - b) <= _f32_ulp(a))
+        for top_k in (1, 5, 64, 2048):
+            assert oracle.topk_select(a, n, top_k).tolist() == cpp.topk_select(a, n, top_k).tolist()
+    for C in (1, 3, 64):
+        kr = rng.standard_normal((300, 16))
+        pa, pb = oracle.block_pool(kr, C, 300), cpp.block_pool(kr, C, 300)
+        assert np.all(np.abs(pa.astype(np.float64) - pb) <= _f32_ulp(pa))
+        bs = rng.integers(-3, 4, 300 // C).astype(np.float32)
+        for n_vis in (0, C - 1, 150, 300):
+            for top_k in (C, 7 * C, 2048):
+                assert oracle.block_select(bs, n_vis, top_k, C).tolist() == cpp.block_select(bs, n_vis, top_k, C).tolist()
+    x = rng.standard_normal((50, 128)).astype(np.float32) * 3
+    qa, sa = oracle.quantize_rows(x)
+    qb, sb = cpp.quantize_rows(x)
+    np.testing.assert_array_equal(qa, qb)
+    np.testing.assert_array_equal(sa, sb)
+
+
+def test_oracles_agree_on_attention_and_hadamard():
+    rng = np.random.default_rng(21)
+    cpp = oracle.cpp
+    q = rng.standard_normal((16, 40)); lat = rng.standard_normal((90, 40)); sel = rng.permutation(90)[:33]
+    np.testing.assert_allclose(cpp.sparse_attention_mla(q, lat, sel, 0.3, dv=32),
+                               oracle.sparse_attention_mla(q, lat, sel, 0.3, dv=32), rtol=1e-12, atol=1e-13)
+    K = rng.standard_normal((50, 4, 24)); V = rng.standard_normal((50, 4, 20)); qg = rng.standard_normal((8, 24))
+    np.testing.assert_allclose(cpp.sparse_attention_gqa(qg, K, V, sel[sel < 50], 0.2),
+                               oracle.sparse_attention_gqa(qg, K, V, sel[sel < 50], 0.2), rtol=1e-12, atol=1e-13)
+    x = rng.standard_normal((20, 128))
+    np.testing.assert_allclose(cpp.hadamard_rotate(x), oracle.hadamard_rotate(x), rtol=0, atol=1e-13)
+
+
+def test_cpp_batch_forms_read_storage_types_exactly():
+    # the batch functions read f16 / bf16 / int8 caches as stored: the same as widening first
+    rng = np.random.default_rng(22)
+    cpp = oracle.cpp
+    R, H, d, n = 3, 8, 32, 200
+    q = torch.randn(R, H, d, dtype=torch.float64).to(torch.bfloat16)
+    w = rng.standard_normal((R, H))
+    k = torch.randn(n, d, dtype=torch.float64).to(torch.float16)
+    n_vis = [200, 17, 0]
+    s = cpp.scores_batch(q, w, k, [0, 5, 0], n_vis)
+    for r in range(R):
+        ref = cpp.indexer_scores(q[r].double().numpy(), w[r], k.double().numpy()[[0, 5, 0][r]:][:n_vis[r]])
+        np.testing.assert_array_equal(s[r, :n_vis[r]], ref)
+    k8, sc = cpp.quantize_rows(k.double().numpy())
+    s8 = cpp.scores_batch(q, w, k8, [0, 0, 0], [200, 200, 200], k_scale=sc)
+    np.testing.assert_array_equal(s8[1], cpp.indexer_scores(q[1].double().numpy(), w[1], cpp.dequantize_rows(k8, sc)))
+    lat = torch.randn(n, 40, dtype=torch.float64).to(torch.bfloat16)
+    idx = np.array([[3, 9, 150], [0, 1, -1]])
+    qa = torch.randn(2, 4, 40, dtype=torch.float64).to(torch.bfloat16)
+    out = cpp.attention_batch(qa, lat, None, [0, 10], idx, [3, 2], 0.25, 1, dv=32)
+    np.testing.assert_array_equal(out[0], cpp.sparse_attention_mla(qa[0].double().numpy(), lat.double().numpy(),
+                                                                   [3, 9, 150], 0.25, dv=32))
+    np.testing.assert_array_equal(out[1], cpp.sparse_attention_mla(qa[1].double().numpy(), lat.double().numpy()[10:],
+                                                                   [0, 1], 0.25, dv=32))
