@@ -10,14 +10,20 @@ from __future__ import annotations
 
 import torch
 
-from . import Batch, idx_block_pool, idx_hadamard, idx_score, idx_score_q8, idx_topk, idx_workspace_size, topk_capacity
+from . import Batch, idx_block_pool, idx_block_pool_update, idx_hadamard, idx_score, idx_score_q8, idx_topk, idx_workspace_size, topk_capacity
 from . import sparse_attn_decode, sparse_attn_prefill, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL, IDX_OP_TOPK
 from .workloads import Workload
 
 
 class SparseAttentionStep:
-    def __init__(self, wl: Workload, out_dtype=None):
+    """pool: block-pooled workloads only.  "full" pools every complete block in every step;
+    "update" keeps the pooled keys across steps (pooled once at construction) and each step
+    re-pools only the newest complete block of every sequence, as a decode step does when
+    its token has just completed a block (idx_block_pool_update)."""
+
+    def __init__(self, wl: Workload, out_dtype=None, pool: str = "full"):
         self.wl = wl
+        self.pool_mode = pool
         dev = wl.q_idx.device
         self.batch = Batch(wl.n_kv, wl.T, wl.max_n_kv, kv_start=wl.kv_start, kv_seq_stride=wl.kv_seq_stride,
                            q_pos=wl.q_pos, page_table=wl.page_table, page_size=wl.page_size)
@@ -28,6 +34,9 @@ class SparseAttentionStep:
             self.pooled = torch.zeros(wl.B, self.pool_stride, wl.d, device=dev, dtype=torch.float32)
             self.pool_batch = Batch(wl.n_kv, wl.T, wl.max_n_kv, kv_seq_stride=self.pool_stride, q_pos=wl.q_pos)
             n_keys = self.pool_stride
+            if pool == "update":
+                self.n_pooled = torch.clamp(wl.n_kv // C - 1, min=0).to(torch.int32).contiguous()
+                idx_block_pool(wl.k_idx, self.batch, C, pool_seq_stride=self.pool_stride, pooled=self.pooled)
         else:
             n_keys = max(wl.max_n_kv, 1)
         self.scores = torch.empty(rows, n_keys, device=dev, dtype=torch.float32)
@@ -59,7 +68,11 @@ class SparseAttentionStep:
         q = wl.q_idx if self.q_rot is None else self.q_rot
         k = wl.k_idx if self.k_rot is None else self.k_rot
         if wl.block_size > 1:
-            idx_block_pool(k, self.batch, wl.block_size, pool_seq_stride=self.pool_stride, pooled=self.pooled)
+            if self.pool_mode == "update":
+                idx_block_pool_update(k, self.batch, wl.block_size, self.pooled, n_pooled=self.n_pooled,
+                                      pool_seq_stride=self.pool_stride)
+            else:
+                idx_block_pool(k, self.batch, wl.block_size, pool_seq_stride=self.pool_stride, pooled=self.pooled)
             kp = self.pooled.view(-1, wl.d)
             idx_score(q, wl.w, kp, self.pool_batch, block_size=wl.block_size, scores=self.scores)
         elif wl.k8 is not None:

@@ -1,8 +1,13 @@
 """End-to-end parity on the five synthetic configurations and the headline
 decode workload: the whole path (Hadamard -> score -> select -> attend) runs
-on the GPU exactly as the bench launches it; the oracle recomputes sampled
-rows from the same inputs.  Reports the identical-set rate and the mean
-Jaccard of the selections (the pages' comparison metric)."""
+on the GPU exactly as the bench launches it; the C++ oracle recomputes every
+row (configuration 3: rows 0-2100, which include every exactly dense row, and
+every 16th row after them) from the same inputs, read as stored.
+
+A GPU selection that differs from the oracle's by a legal near-tie swap is a
+valid result too; its attention output is then checked against the oracle's
+attention over that same (validated) selection.  Reports the identical-set
+rate and the mean Jaccard of the selections (the pages' comparison metric)."""
 
 import math
 
@@ -11,6 +16,7 @@ import pytest
 import torch
 
 import oracle as O
+import oracle.cpp as C
 import lightning_indexer_top_gb300 as L
 from lightning_indexer_top_gb300 import workloads
 from lightning_indexer_top_gb300.pipeline import SparseAttentionStep
@@ -39,35 +45,60 @@ def _run(wl):
 def _report(name, ident):
     rate = float(np.mean([i for i, _ in ident]))
     jac = float(np.mean([j for _, j in ident]))
-    print(f"\n[{name}] identical-set rate {rate:.3f}  mean Jaccard {jac:.5f}  over {len(ident)} rows")
+    print(f"\n[{name}] identical-set rate {rate:.4f}  mean Jaccard {jac:.6f}  over {len(ident)} rows")
     return rate
 
 
-def _check_mla_rows(wl, step, rows, k_rot=None, q_rot=None):
-    """Verify sampled rows of an MLA workload (decode or causal prefill)."""
-    ident = []
-    kh = np64(wl.k_idx) if k_rot is None else k_rot
-    lat = wl.k_attn
-    s_gpu = step.scores
-    for r in rows:
-        b = r // wl.T
-        n_kv = wl.n_kv_host[b]
-        nv = O.visible_count(n_kv, None if wl.q_pos is None else r % wl.T)
-        krows = wl.rows_of(b, nv).numpy()         # position order (through the page table if paged)
-        q = np64(wl.q_idx[r]) if q_rot is None else q_rot(r)
-        s_ref = O.indexer_scores(q, np64(wl.w[r]), kh[krows])
-        assert_scores_close(s_gpu[r, :nv].cpu().numpy(), s_ref, f"{wl.name} row {r}")
-        sel_ref = O.topk_select(s_ref, nv, wl.top_k)
-        ns = int(step.n_sel[r])
-        sel_gpu = sorted_unique(step.idx[r].cpu().numpy(), ns)
-        assert all(x == -1 for x in step.idx[r, ns:].tolist())
-        same, jac = check_selection(sel_gpu, sel_ref, s_ref, f"{wl.name} row {r}")
+def _seq_arrays(wl, t, seqs):
+    """Host copy of cache `t` in its storage type, and the cache row of position 0 of each sequence.
+    Paged caches are gathered into position order, one sequence after another."""
+    if wl.page_table is None:
+        return t.cpu(), {b: wl.row0(b) for b in seqs}
+    parts, off, pos = [], {}, 0
+    for b in seqs:
+        rows = wl.rows_of(b, wl.n_kv_host[b]).to(t.device)
+        parts.append(t[rows].cpu())
+        off[b] = pos
+        pos += wl.n_kv_host[b]
+    return torch.cat(parts), off
+
+
+def _check_mla_rows(wl, step, rows, rotate=False):
+    """Check rows of an MLA workload (decode or causal prefill) against the C++ oracle: scores
+    (1e-3 rule), selections (identical or legal near-tie swaps), attention (2e-2 max-abs, bf16 out)."""
+    rows = [int(r) for r in rows]
+    seqs = sorted({r // wl.T for r in rows})
+    keys, koff = _seq_arrays(wl, wl.k_idx, seqs)
+    lat, loff = _seq_arrays(wl, wl.k_attn, seqs)
+    sel_rows = torch.as_tensor(rows)
+    q = wl.q_idx.cpu()[sel_rows]
+    if rotate:
+        # the cache holds rotated keys; q is rotated on its way in (both rounded once to bf16)
+        keys = C.hadamard_rotate(np64(keys), store="bf16")
+        q = C.hadamard_rotate(np64(q), store="bf16")
+    n_vis = [C.visible_count(wl.n_kv_host[r // wl.T], None if wl.q_pos is None else r % wl.T) for r in rows]
+    s_ref = C.scores_batch(q, np64(wl.w.cpu()[sel_rows]), keys, [koff[r // wl.T] for r in rows], n_vis)
+    idx_ref, ns_ref = C.topk_batch(s_ref, n_vis, wl.top_k)
+    s_gpu = step.scores.cpu()[sel_rows].numpy()
+    idx_gpu = step.idx.cpu()[sel_rows].numpy()
+    ns_gpu = step.n_sel.cpu()[sel_rows].numpy()
+    ident, attend = [], np.full((len(rows), wl.top_k), -1, np.int64)
+    for i, r in enumerate(rows):
+        nv = n_vis[i]
+        assert_scores_close(s_gpu[i, :nv], s_ref[i, :nv], f"{wl.name} row {r}")
+        ns = int(ns_gpu[i])
+        sel_gpu = sorted_unique(idx_gpu[i], ns)
+        assert np.all(idx_gpu[i, ns:] == -1)
+        sel_ref = idx_ref[i, :ns_ref[i]].tolist()
+        same, jac = check_selection(sel_gpu, sel_ref, s_ref[i, :nv], f"{wl.name} row {r}")
         ident.append((same, jac))
-        if same:
-            lat_rows = np64(lat[torch.as_tensor(krows, device=lat.device)])
-            ref = O.sparse_attention_mla(np64(wl.q_attn[r]), lat_rows, sel_ref, wl.scale, wl.dv)
-            err = np.max(np.abs(np64(step.out[r]) - ref))
-            assert err <= 2e-2, f"{wl.name} row {r}: attention max-abs {err}"
+        # the oracle attends over its own selection, or over the GPU's once it is shown to be legal
+        chosen = sel_ref if same else sel_gpu
+        attend[i, :len(chosen)] = chosen
+    ref = C.attention_batch(wl.q_attn.cpu()[sel_rows], lat, None, [loff[r // wl.T] for r in rows], attend,
+                            ns_gpu, wl.scale, 1, dv=wl.dv)
+    err = np.max(np.abs(np64(step.out.cpu()[sel_rows]) - ref), axis=(1, 2))
+    assert np.all(err <= 2e-2), f"{wl.name}: attention max-abs {err.max()} at row {rows[int(err.argmax())]}"
     return ident
 
 
@@ -90,17 +121,16 @@ def test_config1_tiny_prefill_fp32_all_rows():
             assert sel_gpu == list(range(nv))          # exactly dense below the budget
             dense = O.dense_attention_gqa(np64(wl.q_attn[t]), Kh, Vh, nv, wl.scale)
             assert np.max(np.abs(np64(step.out[t]) - dense)) <= 1e-4
-        if same:
-            ref = O.sparse_attention_gqa(np64(wl.q_attn[t]), Kh, Vh, sel_ref, wl.scale)
-            assert np.max(np.abs(np64(step.out[t]) - ref)) <= 1e-4, t
-    assert _report(wl.name, ident) > 0.9
+        # the oracle's own selection, or the GPU's once it is shown to be a legal near-tie swap
+        ref = O.sparse_attention_gqa(np64(wl.q_attn[t]), Kh, Vh, sel_ref if same else sel_gpu, wl.scale)
+        assert np.max(np.abs(np64(step.out[t]) - ref)) <= 1e-4, t
+    _report(wl.name, ident)
 
 
 def test_config2_decode_mla_all_rows():
     wl = workloads.make(2)
     step = _run(wl)
-    ident = _check_mla_rows(wl, step, range(wl.B))
-    assert _report(wl.name, ident) >= 0.5
+    _report(wl.name, _check_mla_rows(wl, step, range(wl.B)))
 
 
 def test_config2_batched_equals_each_sequence_alone():
@@ -122,17 +152,14 @@ def test_config2_batched_equals_each_sequence_alone():
         assert torch.equal(st.out[0], full.out[b])
 
 
-def test_config3_prefill_sampled_rows():
+def test_config3_prefill_stratified_rows():
     wl = workloads.make(3)
     step = _run(wl)
-    # the oracle rotates the keys once (the cache holds rotated keys) and each sampled q row
-    k_rot = O.hadamard_store(np64(wl.k_idx), "bf16")
-    rows = [0, 1, 777, 2046, 2047, 2048, 2049, 5000, 9999, 16383]
-    ident = _check_mla_rows(wl, step, rows, k_rot=k_rot,
-                            q_rot=lambda r: O.hadamard_store(np64(wl.q_idx[r]), "bf16"))
-    for r in rows[:5]:   # rows below the budget are exactly dense
+    # every row up to 2100 (all the exactly dense rows and the first ones past the budget), then every 16th
+    rows = list(range(0, 2101)) + list(range(2101, wl.T, 16)) + [wl.T - 1]
+    _report(wl.name, _check_mla_rows(wl, step, sorted(set(rows)), rotate=True))
+    for r in range(2048):   # rows below the budget are exactly dense
         assert int(step.n_sel[r]) == r + 1
-    _report(wl.name, ident)
 
 
 def test_prefill_chunking_over_query_rows_is_bit_identical():
@@ -182,10 +209,9 @@ def test_config4_block_decode_all_rows_with_tails():
         assert len([t for t in sel_gpu if t < n_cb * C]) == len(gb) * C      # whole blocks
         same, jac = check_selection(gb, rb, bs_ref, f"seq {b}")
         ident.append((same, jac))
-        if same:
-            ref = O.sparse_attention_gqa(np64(wl.q_attn[b]), np64(Kh[row0:row0 + n]), np64(Vh[row0:row0 + n]),
-                                         sel_ref, wl.scale)
-            assert np.max(np.abs(np64(step.out[b]) - ref)) <= 2e-2, b
+        ref = O.sparse_attention_gqa(np64(wl.q_attn[b]), np64(Kh[row0:row0 + n]), np64(Vh[row0:row0 + n]),
+                                     sel_ref if same else sel_gpu, wl.scale)
+        assert np.max(np.abs(np64(step.out[b]) - ref)) <= 2e-2, b
     _report(wl.name, ident)
 
 
@@ -207,28 +233,24 @@ def test_config4_dense_threshold():
     assert np.max(np.abs(np64(step.out[0]) - dense)) <= 2e-2
 
 
-def test_config5_long_ragged_decode_sampled_rows():
+def test_config5_long_ragged_decode_all_rows():
     wl = workloads.make(5)
     step = _run(wl)
-    order = np.argsort(wl.n_kv_host)
-    rows = [int(order[0]), int(order[len(order) // 2]), int(order[-1]), 7]
-    ident = _check_mla_rows(wl, step, rows)
-    _report(wl.name, ident)
+    _report(wl.name, _check_mla_rows(wl, step, range(wl.B)))
 
 
-def test_headline_decode_64x131072_sampled_rows():
+def test_headline_decode_64x131072_all_rows():
     wl = workloads.make("headline")
     step = _run(wl)
-    ident = _check_mla_rows(wl, step, [0, 31, 63])
-    _report(wl.name, ident)
+    _report(wl.name, _check_mla_rows(wl, step, range(wl.B)))
 
 
-def test_paged_decode_workload_sampled_rows():
+def test_paged_decode_workload_all_rows():
     # the headline geometry at 8192 keys with both caches in shuffled 64-row pages
     wl = workloads.make("headline", n_kv_override=8192, batch_override=6, page_size=64)
     assert wl.page_table is not None and wl.name.endswith("_paged")
     st = _run(wl)
-    _report("paged", _check_mla_rows(wl, st, [0, 3, 5]))
+    _report("paged", _check_mla_rows(wl, st, range(wl.B)))
 
 
 @pytest.mark.parametrize("make_args", [(("headline",), {"batch_override": 16, "n_kv_override": 65536}), ((2,), {})],

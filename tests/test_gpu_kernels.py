@@ -32,15 +32,30 @@ def _i32(x):
 
 # ------------------------------------------------------------------ Hadamard
 
+_STORE_BITS = {torch.float32: (24, -126), torch.float16: (11, -14), torch.bfloat16: (8, -126)}
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
 @pytest.mark.parametrize("d", [32, 64, 128, 256])
 def test_hadamard_matches_oracle(dtype, d):
-    # the stored rotation is decided in f32 on both sides: bit-exact
+    # The oracle's value is the exact rotation (rounded once to the storage type for the agreement
+    # rate).  The kernel rotates in f32 and rounds once, so it may differ from the exact value by the
+    # f32 error of a d-point transform -- log2(d) butterfly stages and the 1/sqrt(d) scaling, each
+    # within 2^-24 of sum|x|/sqrt(d) -- plus half a storage ulp for the final rounding.
     g = torch.Generator(device=DEV).manual_seed(11 + d)
     x = torch.randn(1003, d, generator=g, device=DEV).to(dtype)
     y = L.idx_hadamard(x, torch.empty_like(x))
-    ref = O.hadamard_store(np64(x), FMT[dtype])
-    np.testing.assert_array_equal(np64(y), ref)
+    xh, got = np64(x), np64(y)
+    exact = O.hadamard_rotate(xh)
+    p, emin = _STORE_BITS[dtype]
+    f32_err = (math.log2(d) + 3) * 2.0 ** -24 * np.abs(xh).sum(axis=1, keepdims=True) / math.sqrt(d)
+    mag = np.abs(exact) + f32_err
+    ulp = np.exp2(np.maximum(np.floor(np.log2(np.maximum(mag, 1e-300))), emin) - (p - 1))
+    assert np.all(np.abs(got - exact) <= 0.5 * ulp + f32_err)
+    agree = float(np.mean(got == O.round_to_storage(exact, FMT[dtype])))
+    print(f"\n[hadamard {FMT[dtype]} d={d}] equal to the exact rotation rounded once: {agree:.5f}")
+    if dtype != torch.float32:
+        assert agree > 0.99
     # in place gives the same bits
     x2 = x.clone()
     L.idx_hadamard(x2)
