@@ -133,16 +133,18 @@ void oracle_hadamard_matrix(int d, double* h) {
         for (int j = 0; j < d; ++j) h[(int64_t)i * d + j] = (__builtin_popcount((unsigned)(i & j)) & 1) ? -inv : inv;
 }
 
-// y_r = H_d x_r for each row, in double, then rounded once to store_fmt (F64: no rounding)
+// y_r = H_d x_r = (sum_j (-1)^popcount(i & j) x_r[j]) / sqrt(d) for each row: the +-1 sums in
+// double (exact for stored 16-bit values, so an exactly cancelling sum stays 0), then one
+// division, then rounded once to store_fmt (F64: no rounding)
 void oracle_hadamard(const double* x, int64_t n_rows, int d, int store_fmt, double* y) {
-    std::vector<double> h((size_t)d * d);
-    oracle_hadamard_matrix(d, h.data());
+    const double sqrt_d = std::sqrt((double)d);
 #pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n_rows; ++r) {
         for (int i = 0; i < d; ++i) {
             double acc = 0.0;
-            for (int j = 0; j < d; ++j) acc += h[(size_t)i * d + j] * x[r * d + j];
-            y[r * d + i] = round_storage(acc, store_fmt);
+            for (int j = 0; j < d; ++j)
+                acc += (__builtin_popcount((unsigned)(i & j)) & 1) ? -x[r * d + j] : x[r * d + j];
+            y[r * d + i] = round_storage(acc / sqrt_d, store_fmt);
         }
     }
 }

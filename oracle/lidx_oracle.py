@@ -101,13 +101,18 @@ def hadamard_rotate(x, store: str | None = None) -> np.ndarray:
     """Rotate every length-d row (last axis) of ``x`` by H_d: y = H x.
 
     ``store`` names the storage dtype the rotated rows are written back in
-    ("bf16", "f16", "f32"); the rotation is done in float64 and rounded once.
+    ("bf16", "f16", "f32"); the rotation is done in float64 -- the +-1 sums
+    first, then one division by sqrt(d) -- and rounded once.
     Score invariance: (Hq).(Hk) = q.k because H is orthonormal (ik_llama.cpp
     PR #2058, commit "Add GLM-5.2/DeepSeek-V3.2 DSA lightning indexer",
     simplifications list)."""
     x = np.asarray(x, dtype=np.float64)
-    h = hadamard_matrix(x.shape[-1])
-    y = x @ h.T                                   # row vector form of H x
+    d = x.shape[-1]
+    signs = hadamard_matrix(d) * math.sqrt(d)      # the +-1 Sylvester matrix (entries exact)
+    signs = np.round(signs)
+    # H x = (S x) / sqrt(d): the +-1 sums of stored values are exact in double, so an exactly
+    # cancelling sum stays exactly 0; then one division
+    y = (x @ signs.T) / math.sqrt(d)
     if store is not None:
         y = round_to_storage(y, store)
     return y

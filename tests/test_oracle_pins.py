@@ -113,6 +113,28 @@ def test_hadamard_round_trip_and_score_invariance(O):
     np.testing.assert_allclose(s1, s0, rtol=1e-6, atol=1e-6)
 
 
+def test_hadamard_exact_cancellation_gives_zero(O):
+    # H x = (S x) / sqrt(d) with S the +-1 Sylvester matrix: x = e_0 + e_1 gives (1 + (-1)^(i&1)) / sqrt(d),
+    # exactly 0 at every odd i and exactly 2/sqrt(d) at every even i, also after rounding
+    for d in (32, 64, 128):
+        x = np.zeros(d); x[0] = x[1] = 1.0
+        y = O.hadamard_rotate(x)
+        assert np.all(y[1::2] == 0.0)
+        np.testing.assert_allclose(y[0::2], 2 / math.sqrt(d), rtol=1e-15)
+        assert np.all(O.hadamard_rotate(x, store="bf16")[1::2] == 0.0)
+
+
+def test_hadamard_cancelling_bf16_row_worked_example(O, golden):
+    g = golden["hadamard_cancel"]
+    x = np.array(g["x"])
+    assert np.all(O.round_to_storage(x, "bf16") == x)         # the inputs are stored bf16 values
+    signs = np.array([(-1) ** bin(g["index"] & j).count("1") for j in range(g["d"])])
+    assert float(np.sum(signs * x)) == 0.0                    # the signed sum cancels exactly
+    y = O.hadamard_rotate(x[None])[0]
+    assert y[g["index"]] == g["expected"]
+    assert O.hadamard_rotate(x[None], store="bf16")[0][g["index"]] == g["expected"]
+
+
 def test_hadamard_store_rounds_once(O):
     rng = np.random.default_rng(5)
     x = O.round_to_storage(rng.standard_normal((4, 128)), "bf16")
