@@ -115,8 +115,10 @@ typedef struct idx_batch {
  *   x, y       device [n_rows] rows of d elements, row r at x + r*row_stride
  *              (y likewise).  y may equal x (in place); other overlap is
  *              not allowed.
- *   dtype      storage type of x and y; the rotation runs in f32 and is
- *              rounded once (nearest even) to dtype.
+ *   dtype      storage type of x and y; y is the exact rotation rounded
+ *              once (nearest even) to dtype (16-bit types: f32 butterflies
+ *              with a certified error bound, the few elements the bound
+ *              cannot decide recomputed in f64; f32: computed in f64).
  *   d          32, 64, 128 or 256.
  * Errors: INVALID_ARG for x or y NULL with n_rows > 0, n_rows < 0,
  * unsupported d, row_stride < d, or x, y not 16-byte aligned or

@@ -133,7 +133,7 @@ idx_status attn_common(const char* what, const void* q, idx_dtype dtype, int32_t
     }
     return from_cuda(launch_attn_generic(q, dtype, Hq, Hkv, dk, dv, k, v, kv_row_stride,
                                          v_row_stride, kv_rows, g, idx, idx_row_stride, n_sel,
-                                         scale, out, out_dtype, st),
+                                         scale, out, out_dtype, ws, ws_bytes, st),
                      what);
 }
 
@@ -371,8 +371,12 @@ size_t idx_workspace_size(int32_t op, int64_t n_rows, int32_t max_n_kv, int32_t 
     (void)max_n_kv;
     if (top_k == -1) top_k = IDX_DEFAULT_TOP_K;
     if (n_rows <= 0 || top_k <= 0) return 0;
-    if ((op == IDX_OP_ATTN_DECODE || op == IDX_OP_ATTN_PREFILL) && n_q_heads == 128 && dv == 512)
-        return mla_workspace_bytes(n_rows, top_k);
+    if (op == IDX_OP_ATTN_DECODE || op == IDX_OP_ATTN_PREFILL) {
+        // 128 heads x 512: the tensor-core MLA path's split partials (if such a call runs on the CUDA
+        // cores instead, it uses as many key splits as this fits); otherwise the CUDA-core path's
+        if (n_q_heads == 128 && dv == 512) return mla_workspace_bytes(n_rows, top_k);
+        return generic_attn_workspace_bytes(n_rows, top_k, n_q_heads, dv);
+    }
     if (op == IDX_OP_TOPK) return topk_workspace_bytes(n_rows, top_k);
     return 0;
 }

@@ -8,9 +8,14 @@
 // per token, and the value is its first dv columns ("openpangu: MLA-latent KV
 // cache", same log).
 //
-// Grid (query rows, kv heads x head chunks).  A CTA of 4 warps serves one
-// query row, one kv head and HC = 4*HPW of its query heads.  Per tile of 32
-// selected keys it gathers the K (and V) rows into shared memory as f32;
+// Grid (query rows, kv heads x head chunks, key splits).  A CTA of 4 warps
+// serves one query row, one kv head, HC = 4*HPW of its query heads and one
+// split of the row's selected keys.  When the rows are few (a decode batch),
+// the selection is split so that the CTAs cover the SMs; each split writes
+// its unnormalised output with its running max and sum, and a combine kernel
+// merges the splits (rescaling each by exp(m_s - max)).  Per tile of 32
+// selected keys a CTA gathers the K (and V) rows into shared memory as f32
+// (16-byte loads when rows and head slices are 16-byte aligned);
 // warp w then owns heads w, w+4, ...: lane l computes the logit of key l,
 // the warp keeps a running max and sum (online softmax), and each lane
 // accumulates dv/32 output columns.  Unselected lanes and invalid indices
@@ -27,12 +32,56 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kKeys = 32;
 
+// eight consecutive elements as f32 from a 16-byte aligned address
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&f)[8]) {
+    if constexpr (sizeof(T) == 4) {
+        const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    } else {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
+        const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = to_f32(e[i]);
+    }
+}
+
+// rows [dst_row0 ..) of a tile: element c of key `key` at dst[key * pitch + c]
+template <typename T>
+__device__ __forceinline__ void gather_tile(float* dst, int pitch, const T* __restrict__ src, int64_t row_stride,
+                                            int64_t col0, int width, const int64_t* rows_s, bool vec) {
+    if (vec) {
+        const int w8 = width >> 3;
+        for (int e = threadIdx.x; e < kKeys * w8; e += kThreads) {
+            const int key = e / w8, c = (e % w8) * 8;
+            const int64_t row = rows_s[key];
+            float f[8];
+            if (row >= 0) {
+                load8(src + row * row_stride + col0 + c, f);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dst[key * pitch + c + i] = f[i];
+        }
+    } else {
+        for (int e = threadIdx.x; e < kKeys * width; e += kThreads) {
+            const int key = e / width, c = e % width;
+            const int64_t row = rows_s[key];
+            dst[key * pitch + c] = row >= 0 ? to_f32(src[row * row_stride + col0 + c]) : 0.f;
+        }
+    }
+}
+
 template <typename T, int HPW, int DVL>
 __global__ void __launch_bounds__(kThreads) attn_generic_kernel(
     const T* __restrict__ q, int Hq, int Hkv, int dk, int dv, const T* __restrict__ k,
     const T* __restrict__ v, int64_t kv_row_stride, int64_t v_row_stride, int64_t kv_rows, Geom g,
     const int32_t* __restrict__ idx, int64_t idx_row_stride, const int32_t* __restrict__ n_sel,
-    float scale, void* __restrict__ out, int out_dtype, int n_chunks) {
+    float scale, void* __restrict__ out, int out_dtype, int n_chunks, bool vec, int splits, int kps,
+    float* __restrict__ part_o, float* __restrict__ part_ml) {
     constexpr int HC = 4 * HPW;
     extern __shared__ __align__(16) unsigned char sm_raw[];
     int64_t* rows_s = reinterpret_cast<int64_t*>(sm_raw);            // [kKeys] cache rows, -1 invalid
@@ -72,12 +121,14 @@ __global__ void __launch_bounds__(kThreads) attn_generic_kernel(
         for (int i = 0; i < DVL; ++i) o[hh][i] = 0.f;
     }
 
-    for (int t0 = 0; t0 < ns; t0 += kKeys) {
+    const int split = blockIdx.z;
+    const int t_end = min(ns, (split + 1) * kps);
+    for (int t0 = split * kps; t0 < t_end; t0 += kKeys) {
         __syncthreads();  // previous tile fully consumed (and qs written, first time)
         if (threadIdx.x < kKeys) {
             const int j = t0 + threadIdx.x;
             int64_t row = -1;
-            if (j < ns) {
+            if (j < t_end) {
                 const int pos = idx[r * idx_row_stride + j];
                 const int64_t rr = (pos >= 0 && pos < n_kv_b) ? key_row(g, b, pos) : -1;
                 if (rr >= 0 && rr < kv_rows) {
@@ -89,18 +140,8 @@ __global__ void __launch_bounds__(kThreads) attn_generic_kernel(
             rows_s[threadIdx.x] = row;
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < kKeys * dk; e += kThreads) {
-            const int key = e / dk, c = e % dk;
-            const int64_t row = rows_s[key];
-            ks[key * (dk + 1) + c] = row >= 0 ? to_f32(k[row * kv_row_stride + (int64_t)gkv * dk + c]) : 0.f;
-        }
-        if (v) {
-            for (int e = threadIdx.x; e < kKeys * dv; e += kThreads) {
-                const int key = e / dv, c = e % dv;
-                const int64_t row = rows_s[key];
-                vs[key * dv + c] = row >= 0 ? to_f32(v[row * v_row_stride + (int64_t)gkv * dv + c]) : 0.f;
-            }
-        }
+        gather_tile(ks, dk + 1, k, kv_row_stride, (int64_t)gkv * dk, dk, rows_s, vec);
+        if (v) gather_tile(vs, dv, v, v_row_stride, (int64_t)gkv * dv, dv, rows_s, vec);
         __syncthreads();
 
         const bool valid = rows_s[lane] >= 0;
@@ -141,6 +182,25 @@ __global__ void __launch_bounds__(kThreads) attn_generic_kernel(
         }
     }
 
+    if (splits > 1) {
+        // this split's unnormalised output, running max and sum (l = 0: no valid key)
+#pragma unroll
+        for (int hh = 0; hh < HPW; ++hh) {
+            const int hl = warp + 4 * hh;
+            if (hl >= n_heads) continue;
+            const int64_t u = (r * splits + split) * (int64_t)Hq + h_base + hl;
+#pragma unroll
+            for (int i = 0; i < DVL; ++i) {
+                const int c = lane + 32 * i;
+                if (c < dv) part_o[u * dv + c] = o[hh][i];
+            }
+            if (lane == 0) {
+                part_ml[2 * u] = has_m[hh] ? m_run[hh] : 0.f;
+                part_ml[2 * u + 1] = l_run[hh];
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int hh = 0; hh < HPW; ++hh) {
         const int hl = warp + 4 * hh;
@@ -160,14 +220,64 @@ __global__ void __launch_bounds__(kThreads) attn_generic_kernel(
     }
 }
 
+// merges the key splits of one (row, head): o = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s
+__global__ void __launch_bounds__(128) attn_generic_combine_kernel(const float* __restrict__ part_o,
+                                                                   const float* __restrict__ part_ml, int splits,
+                                                                   int Hq, int dv, void* __restrict__ out,
+                                                                   int out_dtype) {
+    const int64_t r = blockIdx.x;
+    const int h = blockIdx.y;
+    float M = 0.f;
+    bool any = false;
+    for (int s = 0; s < splits; ++s) {
+        const int64_t u = (r * splits + s) * (int64_t)Hq + h;
+        if (part_ml[2 * u + 1] > 0.f) {
+            M = any ? fmaxf(M, part_ml[2 * u]) : part_ml[2 * u];
+            any = true;
+        }
+    }
+    float den = 0.f;
+    for (int s = 0; s < splits; ++s) {
+        const int64_t u = (r * splits + s) * (int64_t)Hq + h;
+        const float l = part_ml[2 * u + 1];
+        if (l > 0.f) den += expf(part_ml[2 * u] - M) * l;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int c = threadIdx.x; c < dv; c += blockDim.x) {
+        float acc = 0.f;
+        for (int s = 0; s < splits; ++s) {
+            const int64_t u = (r * splits + s) * (int64_t)Hq + h;
+            const float l = part_ml[2 * u + 1];
+            if (l > 0.f) acc += expf(part_ml[2 * u] - M) * part_o[u * dv + c];
+        }
+        const int64_t o = (r * Hq + h) * (int64_t)dv + c;
+        if (out_dtype == IDX_BF16)
+            static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(acc * inv);
+        else
+            static_cast<float*>(out)[o] = acc * inv;
+    }
+}
+
 template <typename T, int HPW>
 cudaError_t run_dv(const T* q, int Hq, int Hkv, int dk, int dv, const T* k, const T* v,
                    int64_t kv_row_stride, int64_t v_row_stride, int64_t kv_rows, const Geom& g,
                    const int32_t* idx, int64_t idx_row_stride, const int32_t* n_sel, float scale,
-                   void* out, int out_dtype, int n_chunks, cudaStream_t st) {
+                   void* out, int out_dtype, int n_chunks, void* ws, size_t ws_bytes, cudaStream_t st) {
     constexpr int HC = 4 * HPW;
     const int64_t n_rows = (int64_t)g.B * g.T;
-    dim3 grid((unsigned)n_rows, (unsigned)(Hkv * n_chunks));
+    const size_t per_split = (size_t)n_rows * Hq * (dv + 2) * sizeof(float);
+    int splits = generic_attn_splits(n_rows, idx_row_stride);
+    if (splits > 1 && (!ws || (reinterpret_cast<uintptr_t>(ws) & 15u))) splits = 1;
+    if (splits > 1 && (size_t)splits * per_split > ws_bytes) splits = (int)(ws_bytes / per_split);
+    if (splits < 1) splits = 1;
+    const int kps = (int)(((idx_row_stride + splits - 1) / splits + kKeys - 1) / kKeys * kKeys);
+    float* part_o = splits > 1 ? static_cast<float*>(ws) : nullptr;
+    float* part_ml = splits > 1 ? part_o + (size_t)n_rows * splits * Hq * dv : nullptr;
+    const size_t ts = sizeof(T);
+    const bool vec = dk % 8 == 0 && dv % 8 == 0 && !(reinterpret_cast<uintptr_t>(k) & 15u) &&
+                     !(reinterpret_cast<uintptr_t>(v) & 15u) && (kv_row_stride * ts) % 16 == 0 &&
+                     (!v || (v_row_stride * ts) % 16 == 0) && (dk * ts) % 16 == 0 && (dv * ts) % 16 == 0;
+    dim3 grid((unsigned)n_rows, (unsigned)(Hkv * n_chunks), (unsigned)splits);
     size_t sm = (size_t)(HC * dk + kKeys * (dk + 1) + (v ? kKeys * dv : 0)) * sizeof(float) +
                 kKeys * sizeof(int64_t);
     const int dvl = (dv + 31) / 32;
@@ -177,7 +287,11 @@ cudaError_t run_dv(const T* q, int Hq, int Hkv, int dk, int dv, const T* k, cons
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);       \
         kern<<<grid, kThreads, sm, st>>>(q, Hq, Hkv, dk, dv, k, v, kv_row_stride, v_row_stride, \
                                          kv_rows, g, idx, idx_row_stride, n_sel, scale, out,    \
-                                         out_dtype, n_chunks);                                  \
+                                         out_dtype, n_chunks, vec, splits, kps, part_o, part_ml); \
+        cudaError_t e = cudaGetLastError();                                                     \
+        if (e != cudaSuccess || splits == 1) return e;                                          \
+        attn_generic_combine_kernel<<<dim3((unsigned)n_rows, (unsigned)Hq), 128, 0, st>>>(      \
+            part_o, part_ml, splits, Hq, dv, out, out_dtype);                                   \
         return cudaGetLastError();                                                              \
     }
     LIDX_ATTN_CASE(1)
@@ -193,40 +307,60 @@ template <typename T>
 cudaError_t run(const T* q, int Hq, int Hkv, int dk, int dv, const T* k, const T* v,
                 int64_t kv_row_stride, int64_t v_row_stride, int64_t kv_rows, const Geom& g,
                 const int32_t* idx, int64_t idx_row_stride, const int32_t* n_sel, float scale,
-                void* out, int out_dtype, cudaStream_t st) {
+                void* out, int out_dtype, void* ws, size_t ws_bytes, cudaStream_t st) {
     const int G = Hq / Hkv;
     if ((int64_t)g.B * g.T == 0) return cudaSuccess;
     if (G <= 4)
         return run_dv<T, 1>(q, Hq, Hkv, dk, dv, k, v, kv_row_stride, v_row_stride, kv_rows, g, idx,
-                            idx_row_stride, n_sel, scale, out, out_dtype, 1, st);
+                            idx_row_stride, n_sel, scale, out, out_dtype, 1, ws, ws_bytes, st);
     if (G <= 8)
         return run_dv<T, 2>(q, Hq, Hkv, dk, dv, k, v, kv_row_stride, v_row_stride, kv_rows, g, idx,
-                            idx_row_stride, n_sel, scale, out, out_dtype, 1, st);
+                            idx_row_stride, n_sel, scale, out, out_dtype, 1, ws, ws_bytes, st);
     return run_dv<T, 4>(q, Hq, Hkv, dk, dv, k, v, kv_row_stride, v_row_stride, kv_rows, g, idx,
-                        idx_row_stride, n_sel, scale, out, out_dtype, (G + 15) / 16, st);
+                        idx_row_stride, n_sel, scale, out, out_dtype, (G + 15) / 16, ws, ws_bytes, st);
 }
 
 }  // namespace
+
+// key splits per (row, kv head) for few rows: enough CTAs to cover the SMs twice, at least 128
+// selected keys per split; many rows need none
+int generic_attn_splits(int64_t n_rows, int64_t cap) {
+    if (n_rows <= 0) return 1;
+    int sms = sm_count();
+    if (sms < 2) sms = 152;
+    int64_t s = 2 * (int64_t)sms / n_rows;
+    const int64_t by_keys = (cap + 127) / 128;
+    if (s > by_keys) s = by_keys;
+    if (s > 64) s = 64;
+    return s < 1 ? 1 : (int)s;
+}
+
+size_t generic_attn_workspace_bytes(int64_t n_rows, int64_t cap, int Hq, int dv) {
+    const int s = generic_attn_splits(n_rows, cap);
+    if (s <= 1 || Hq < 1 || dv < 1) return 0;
+    return (size_t)n_rows * s * Hq * (dv + 2) * sizeof(float);
+}
 
 cudaError_t launch_attn_generic(const void* q, int dtype, int Hq, int Hkv, int dk, int dv,
                                 const void* k, const void* v, int64_t kv_row_stride,
                                 int64_t v_row_stride, int64_t kv_rows, const Geom& g,
                                 const int32_t* idx, int64_t idx_row_stride, const int32_t* n_sel,
-                                float scale, void* out, int out_dtype, cudaStream_t st) {
+                                float scale, void* out, int out_dtype, void* ws, size_t ws_bytes,
+                                cudaStream_t st) {
     switch (dtype) {
         case IDX_F16:
             return run(static_cast<const __half*>(q), Hq, Hkv, dk, dv, static_cast<const __half*>(k),
                        static_cast<const __half*>(v), kv_row_stride, v_row_stride, kv_rows, g, idx,
-                       idx_row_stride, n_sel, scale, out, out_dtype, st);
+                       idx_row_stride, n_sel, scale, out, out_dtype, ws, ws_bytes, st);
         case IDX_BF16:
             return run(static_cast<const __nv_bfloat16*>(q), Hq, Hkv, dk, dv,
                        static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
                        kv_row_stride, v_row_stride, kv_rows, g, idx, idx_row_stride, n_sel, scale,
-                       out, out_dtype, st);
+                       out, out_dtype, ws, ws_bytes, st);
         default:
             return run(static_cast<const float*>(q), Hq, Hkv, dk, dv, static_cast<const float*>(k),
                        static_cast<const float*>(v), kv_row_stride, v_row_stride, kv_rows, g, idx,
-                       idx_row_stride, n_sel, scale, out, out_dtype, st);
+                       idx_row_stride, n_sel, scale, out, out_dtype, ws, ws_bytes, st);
     }
 }
 

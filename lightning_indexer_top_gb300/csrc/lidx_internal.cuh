@@ -159,11 +159,17 @@ cudaError_t launch_topk(const float* scores, int64_t score_row_stride, const Geo
                         size_t ws_bytes, cudaStream_t st);
 size_t topk_workspace_bytes(int64_t n_rows, int top_k);
 
+// CUDA-core attention (any head counts and widths); with few rows the selected keys are split
+// over CTAs, and the partials need generic_attn_workspace_bytes() of the workspace (without it,
+// or with less, fewer splits are used)
+int generic_attn_splits(int64_t n_rows, int64_t cap);
+size_t generic_attn_workspace_bytes(int64_t n_rows, int64_t cap, int Hq, int dv);
 cudaError_t launch_attn_generic(const void* q, int dtype, int Hq, int Hkv, int dk, int dv,
                                 const void* k, const void* v, int64_t kv_row_stride,
                                 int64_t v_row_stride, int64_t kv_rows, const Geom& g,
                                 const int32_t* idx, int64_t idx_row_stride, const int32_t* n_sel,
-                                float scale, void* out, int out_dtype, cudaStream_t st);
+                                float scale, void* out, int out_dtype, void* ws, size_t ws_bytes,
+                                cudaStream_t st);
 
 // tcgen05 sparse MLA attention (128 heads, 576/512 bf16 latent); the caller
 // checks mla_tc_supported() first; splits > 1 needs mla_workspace_bytes()

@@ -38,24 +38,27 @@ _STORE_BITS = {torch.float32: (24, -126), torch.float16: (11, -14), torch.bfloat
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
 @pytest.mark.parametrize("d", [32, 64, 128, 256])
 def test_hadamard_matches_oracle(dtype, d):
-    # The oracle's value is the exact rotation (rounded once to the storage type for the agreement
-    # rate).  The kernel rotates in f32 and rounds once, so it may differ from the exact value by the
-    # f32 error of a d-point transform -- log2(d) butterfly stages and the 1/sqrt(d) scaling, each
-    # within 2^-24 of sum|x|/sqrt(d) -- plus half a storage ulp for the final rounding.
+    # The stored rotation is the exact rotation rounded once: bit-exact against the oracle for 16-bit
+    # storage.  For f32 storage the kernel's f64 rotation can, in rare near-midpoint cases, round
+    # differently from the oracle's own f64 sum, so it is held to half an f32 ulp of the exact value
+    # (plus the f64 error) and must agree on all but a tiny fraction of elements.
     g = torch.Generator(device=DEV).manual_seed(11 + d)
     x = torch.randn(1003, d, generator=g, device=DEV).to(dtype)
+    x[0] = 0
+    x[1, ::3] = 1e-3    # many equal magnitudes: exact ties at the rounding midpoints for d = 64, 256
     y = L.idx_hadamard(x, torch.empty_like(x))
     xh, got = np64(x), np64(y)
-    exact = O.hadamard_rotate(xh)
-    p, emin = _STORE_BITS[dtype]
-    f32_err = (math.log2(d) + 3) * 2.0 ** -24 * np.abs(xh).sum(axis=1, keepdims=True) / math.sqrt(d)
-    mag = np.abs(exact) + f32_err
-    ulp = np.exp2(np.maximum(np.floor(np.log2(np.maximum(mag, 1e-300))), emin) - (p - 1))
-    assert np.all(np.abs(got - exact) <= 0.5 * ulp + f32_err)
-    agree = float(np.mean(got == O.round_to_storage(exact, FMT[dtype])))
-    print(f"\n[hadamard {FMT[dtype]} d={d}] equal to the exact rotation rounded once: {agree:.5f}")
+    ref = O.hadamard_rotate(xh, store=FMT[dtype])
     if dtype != torch.float32:
-        assert agree > 0.99
+        np.testing.assert_array_equal(got, ref)
+    else:
+        exact = O.hadamard_rotate(xh)
+        p, emin = _STORE_BITS[dtype]
+        ulp = np.exp2(np.maximum(np.floor(np.log2(np.maximum(np.abs(exact), 1e-300))), emin) - (p - 1))
+        assert np.all(np.abs(got - exact) <= 0.5 * ulp + 1e-12 * np.abs(xh).sum(axis=1, keepdims=True))
+        agree = float(np.mean(got == ref))
+        print(f"\n[hadamard f32 d={d}] equal to the exact rotation rounded once: {agree:.6f}")
+        assert agree > 0.9999
     # in place gives the same bits
     x2 = x.clone()
     L.idx_hadamard(x2)
@@ -299,6 +302,35 @@ def test_attention_gqa_matches_oracle(dtype, out_dtype):
         ref = O.sparse_attention_gqa(np64(q[r]), Kh[r * n_kv:(r + 1) * n_kv], Vh[r * n_kv:(r + 1) * n_kv], sel,
                                      1 / math.sqrt(dh))
         assert np.max(np.abs(got[r] - ref)) <= tol, r
+
+
+def test_attention_gqa_key_splits_and_fallback_without_workspace():
+    # few rows: the selected keys are split over CTAs and merged; with too small a workspace the call
+    # falls back to one split per row; both agree with the oracle (and with each other closely)
+    g = torch.Generator().manual_seed(63)
+    B, Hq, Hkv, dh, n_kv = 4, 32, 4, 128, 5000
+    sizes = [2111, 700, 129, 0]
+    q = torch.randn(B, Hq, dh, generator=g).to(torch.bfloat16)
+    K = torch.randn(B * n_kv, Hkv, dh, generator=g).to(torch.bfloat16)
+    V = torch.randn(B * n_kv, Hkv, dh, generator=g).to(torch.bfloat16)
+    idx = _random_sel(g, n_kv, sizes, B)
+    batch = L.Batch(_i32([n_kv] * B), 1, n_kv, kv_seq_stride=n_kv)
+    need = L.idx_workspace_size(L.IDX_OP_ATTN_DECODE, B, n_kv, idx.shape[1], Hq, dh)
+    assert need > 0
+    args = (q.to(DEV), K.to(DEV), V.to(DEV), batch, idx.to(DEV), _i32(sizes), 1 / math.sqrt(dh))
+    split = L.sparse_attn_decode(*args, out_dtype=torch.float32)
+    single = L.sparse_attn_decode(*args, out_dtype=torch.float32,
+                                  workspace=torch.empty(16, device=DEV, dtype=torch.uint8))
+    torch.cuda.synchronize()
+    Kh, Vh = np64(K), np64(V)
+    for r in range(B):
+        if sizes[r] == 0:
+            assert torch.all(split[r] == 0) and torch.all(single[r] == 0)
+            continue
+        ref = O.sparse_attention_gqa(np64(q[r]), Kh[r * n_kv:(r + 1) * n_kv], Vh[r * n_kv:(r + 1) * n_kv],
+                                     idx[r, :sizes[r]].numpy(), 1 / math.sqrt(dh))
+        assert np.max(np.abs(np64(split[r]) - ref)) <= 1e-4, r
+        assert np.max(np.abs(np64(single[r]) - ref)) <= 1e-4, r
 
 
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
