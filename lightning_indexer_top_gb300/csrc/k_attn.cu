@@ -15,7 +15,8 @@
 // its unnormalised output with its running max and sum, and a combine kernel
 // merges the splits (rescaling each by exp(m_s - max)).  Per tile of 32
 // selected keys a CTA gathers the K (and V) rows into shared memory as f32
-// (16-byte loads when rows and head slices are 16-byte aligned);
+// (16-byte loads, all of a tile's in flight at once, when rows and head
+// slices are 16-byte aligned);
 // warp w then owns heads w, w+4, ...: lane l computes the logit of key l,
 // the warp keeps a running max and sum (online softmax), and each lane
 // accumulates dv/32 output columns.  Unselected lanes and invalid indices
@@ -32,45 +33,81 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kKeys = 32;
 
-// eight consecutive elements as f32 from a 16-byte aligned address
+// eight consecutive elements (16-byte aligned source) as they are stored, and widened to f32
 template <typename T>
-__device__ __forceinline__ void load8(const T* p, float (&f)[8]) {
-    if constexpr (sizeof(T) == 4) {
-        const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-    } else {
-        const uint4 u = *reinterpret_cast<const uint4*>(p);
-        const T* e = reinterpret_cast<const T*>(&u);
+struct Raw8 {
+    uint4 u[sizeof(T) / 2];
+};
+
+template <typename T>
+__device__ __forceinline__ Raw8<T> load_raw8(const T* p) {
+    Raw8<T> r;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = to_f32(e[i]);
-    }
+    for (int i = 0; i < (int)(sizeof(T) / 2); ++i) r.u[i] = reinterpret_cast<const uint4*>(p)[i];
+    return r;
 }
 
-// rows [dst_row0 ..) of a tile: element c of key `key` at dst[key * pitch + c]
 template <typename T>
-__device__ __forceinline__ void gather_tile(float* dst, int pitch, const T* __restrict__ src, int64_t row_stride,
-                                            int64_t col0, int width, const int64_t* rows_s, bool vec) {
-    if (vec) {
-        const int w8 = width >> 3;
-        for (int e = threadIdx.x; e < kKeys * w8; e += kThreads) {
-            const int key = e / w8, c = (e % w8) * 8;
-            const int64_t row = rows_s[key];
-            float f[8];
-            if (row >= 0) {
-                load8(src + row * row_stride + col0 + c, f);
-            } else {
+__device__ __forceinline__ void store_f32(const Raw8<T>& r, float* dst) {
+    const T* e = reinterpret_cast<const T*>(r.u);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) f[i] = 0.f;
+    for (int i = 0; i < 8; ++i) dst[i] = to_f32(e[i]);
+}
+
+// The K rows (dk elements from column kc0 of each row) and, with v, the V rows (dv elements from
+// column vc0) of one tile of kKeys keys, widened into shared memory: key `key` at ks[key * (dk + 1)]
+// and vs[key * dv].  Invalid keys (rows_s < 0) give zeros.  With `vec` every 16-byte piece of a
+// tile is loaded before any is stored, up to kBatch per thread, so a tile costs one memory round
+// trip rather than one per piece.
+template <typename T>
+__device__ __forceinline__ void gather_kv_tile(float* ks, float* vs, const T* __restrict__ k, const T* __restrict__ v,
+                                               int64_t k_stride, int64_t v_stride, int64_t kc0, int64_t vc0, int dk,
+                                               int dv, const int64_t* rows_s, bool vec) {
+    if (vec) {
+        constexpr int kBatch = 8;
+        const int wk = dk >> 3, wv = v ? dv >> 3 : 0;
+        const int nk = kKeys * wk, total = nk + kKeys * wv;
+        for (int e0 = threadIdx.x; e0 < total; e0 += kThreads * kBatch) {
+            Raw8<T> r[kBatch];
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+                const int e = e0 + b * kThreads;
+                if (e < total) {
+                    const bool isk = e < nk;
+                    const int ee = isk ? e : e - nk, w = isk ? wk : wv;
+                    const int key = ee / w, c = (ee % w) * 8;
+                    const int64_t row = rows_s[key];
+                    if (row >= 0) {
+                        r[b] = isk ? load_raw8(k + row * k_stride + kc0 + c) : load_raw8(v + row * v_stride + vc0 + c);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < (int)(sizeof(T) / 2); ++i) r[b].u[i] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dst[key * pitch + c + i] = f[i];
+            for (int b = 0; b < kBatch; ++b) {
+                const int e = e0 + b * kThreads;
+                if (e < total) {
+                    const bool isk = e < nk;
+                    const int ee = isk ? e : e - nk, w = isk ? wk : wv;
+                    const int key = ee / w, c = (ee % w) * 8;
+                    store_f32(r[b], isk ? ks + key * (dk + 1) + c : vs + key * dv + c);
+                }
+            }
         }
     } else {
-        for (int e = threadIdx.x; e < kKeys * width; e += kThreads) {
-            const int key = e / width, c = e % width;
+        for (int e = threadIdx.x; e < kKeys * dk; e += kThreads) {
+            const int key = e / dk, c = e % dk;
             const int64_t row = rows_s[key];
-            dst[key * pitch + c] = row >= 0 ? to_f32(src[row * row_stride + col0 + c]) : 0.f;
+            ks[key * (dk + 1) + c] = row >= 0 ? to_f32(k[row * k_stride + kc0 + c]) : 0.f;
+        }
+        if (v) {
+            for (int e = threadIdx.x; e < kKeys * dv; e += kThreads) {
+                const int key = e / dv, c = e % dv;
+                const int64_t row = rows_s[key];
+                vs[key * dv + c] = row >= 0 ? to_f32(v[row * v_stride + vc0 + c]) : 0.f;
+            }
         }
     }
 }
@@ -140,8 +177,8 @@ __global__ void __launch_bounds__(kThreads) attn_generic_kernel(
             rows_s[threadIdx.x] = row;
         }
         __syncthreads();
-        gather_tile(ks, dk + 1, k, kv_row_stride, (int64_t)gkv * dk, dk, rows_s, vec);
-        if (v) gather_tile(vs, dv, v, v_row_stride, (int64_t)gkv * dv, dv, rows_s, vec);
+        gather_kv_tile(ks, vs, k, v, kv_row_stride, v_row_stride, (int64_t)gkv * dk, (int64_t)gkv * dv, dk, dv,
+                       rows_s, vec);
         __syncthreads();
 
         const bool valid = rows_s[lane] >= 0;
