@@ -256,10 +256,17 @@ def rooflines(wl, step, ms, hbm, bf16, peak_kind):
         n_keys = sum(wl.n_kv_host)
         per_key = wl.d * 2 if wl.k8 is None else wl.d + 4
         nbytes = n_keys * (per_key + 4) + B * wl.H * (wl.d * q_bytes + 4)
-        r["score"] = hbm_line("idx_score (key-cache scan)" if wl.k8 is None else "idx_score_q8 (int8 key-cache scan)",
-                              nbytes, ms["score"])
+        if step.fused:
+            # one call: the scan (with the histogram epilogue) and the two select kernels; the bytes are
+            # the scan's (keys read, scores written, q and w read) plus the selection written
+            r["score"] = hbm_line("idx_score_topk (key-cache scan + histogram select)",
+                                  nbytes + sum(n_sel) * 4, ms["score"] + ms["topk"])
+        else:
+            r["score"] = hbm_line("idx_score (key-cache scan)" if wl.k8 is None else
+                                  "idx_score_q8 (int8 key-cache scan)", nbytes, ms["score"])
     n_scores = sum(n_vis) if C <= 1 else sum(n // C for n in n_vis)
-    r["topk"] = hbm_line("idx_topk", n_scores * 4 + sum(n_sel) * 4, ms["topk"])
+    if not getattr(step, "fused", False):
+        r["topk"] = hbm_line("idx_topk", n_scores * 4 + sum(n_sel) * 4, ms["topk"])
     Hq, dk = wl.q_attn.shape[1], wl.q_attn.shape[-1]
     if wl.v_attn is None:
         nbytes = sum(n_sel) * dk * 2 + B * Hq * (dk * 2 + wl.dv * out_bytes)

@@ -264,6 +264,32 @@ idx_status idx_topk(const float* scores, int64_t score_row_stride, idx_batch bat
                     idx_stream_t stream);
 
 /*
+ * idx_score_topk -- the fused indexer + selection: idx_score (token keys)
+ * followed by idx_topk, with the same results, in one call (ik_llama_opt
+ * commit log, "Route DSA indexer selection through ggml_indexer_topk": the
+ * selection of the lightning indexer as one op, with no per-head score
+ * tensor).  Decode rows (n_q_per_seq 1) with H = 64, d = 128 16-bit keys and
+ * fewer than 2 x SMs rows run fused: the tensor-core scorer also counts each
+ * row's scores into a 2048-bin histogram of their order key's top 11 bits,
+ * which fixes the bin of the top_k-th score exactly, so the select only
+ * ranks the keys of that one bin.  Other shapes run idx_score + idx_topk.
+ *   Arguments as idx_score (block_size 0) and idx_topk (token mode); scores
+ *   are written as idx_score writes them.
+ *   workspace  idx_workspace_size(IDX_OP_SCORE_TOPK, ...) bytes, 16-byte
+ *              aligned; with less (or NULL) the call runs unfused.
+ * The fused scorer zeroes its histograms itself behind a bounded barrier
+ * across its CTAs (one per SM); if that barrier times out (the device was
+ * shared with work that held SMs for seconds) IDX_ERR_TIMEOUT is recorded in
+ * the device status and the select falls back to ranking every score, so the
+ * result stays exact.
+ */
+idx_status idx_score_topk(const void* q, idx_dtype q_dtype, const float* w, int32_t n_heads, int32_t head_dim,
+                          const void* k, idx_dtype k_dtype, int64_t k_row_stride, int64_t k_rows, idx_batch batch,
+                          int32_t top_k, float* scores, int64_t score_row_stride, int32_t* idx,
+                          int64_t idx_row_stride, int32_t* n_sel, void* workspace, size_t workspace_bytes,
+                          idx_stream_t stream);
+
+/*
  * sparse_attn_decode / sparse_attn_prefill -- softmax attention of each
  * query row over only its selected keys:
  *     l[h, j] = scale * q[r, h, :] . K[j, g(h), :],  p = softmax_j(l),
@@ -331,7 +357,7 @@ idx_status sparse_attn_decode_noalloc(const void* q, idx_dtype dtype, int32_t n_
                                       idx_dtype out_dtype, idx_stream_t stream);
 
 /* Operation selectors for idx_workspace_size. */
-enum { IDX_OP_SCORE = 0, IDX_OP_TOPK = 1, IDX_OP_ATTN_DECODE = 2, IDX_OP_ATTN_PREFILL = 3 };
+enum { IDX_OP_SCORE = 0, IDX_OP_TOPK = 1, IDX_OP_ATTN_DECODE = 2, IDX_OP_ATTN_PREFILL = 3, IDX_OP_SCORE_TOPK = 4 };
 
 /*
  * idx_workspace_size -- bytes of device workspace an operation needs for the

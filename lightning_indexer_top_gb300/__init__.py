@@ -31,7 +31,7 @@ __all__ = [
 IDX_OK, IDX_ERR_INVALID_ARG, IDX_ERR_UNSUPPORTED, IDX_ERR_CUDA, IDX_ERR_TIMEOUT, IDX_ERR_DEVICE_BOUNDS = range(6)
 IDX_F32, IDX_F16, IDX_BF16 = 0, 1, 2
 IDX_POS_CLEAN = 2**31 - 1   # stale_pos value: no edit
-IDX_OP_SCORE, IDX_OP_TOPK, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL = 0, 1, 2, 3
+IDX_OP_SCORE, IDX_OP_TOPK, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL, IDX_OP_SCORE_TOPK = 0, 1, 2, 3, 4
 
 _DTYPES = {torch.float32: IDX_F32, torch.float16: IDX_F16, torch.bfloat16: IDX_BF16}
 
@@ -78,6 +78,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "idx_quantize_rows": [P, I32, I64, I32, I64, P, I64, P, P],
         "idx_score_q8": [P, I32, P, I32, I32, P, I64, P, I64, _Batch, I32, P, I64, P, SZ, P],
         "idx_topk": [P, I64, _Batch, I32, I32, P, I64, P, P, SZ, P],
+        "idx_score_topk": [P, I32, P, I32, I32, P, I32, I64, I64, _Batch, I32, P, I64, P, I64, P, P, SZ, P],
         "sparse_attn_decode": [P, I32, I32, I32, I32, I32, P, P, I64, I64, I64, _Batch, P, I64, P, F,
                                P, I32, P, SZ, P],
         "sparse_attn_prefill": [P, I32, I32, I32, I32, I32, P, P, I64, I64, I64, _Batch, P, I64, P, F,
@@ -351,6 +352,33 @@ def sparse_attn_prefill(q, k, v, batch, idx, n_sel, scale, *, out=None, out_dtyp
     """Same function as sparse_attn_decode, tuned for many query rows."""
     return _attn("sparse_attn_prefill", q, k, v, batch, idx, n_sel, scale, out, out_dtype, workspace,
                  n_kv_heads, dv)
+
+
+def idx_score_topk(q: torch.Tensor, w: torch.Tensor, k: torch.Tensor, batch: Batch, top_k: int, *,
+                   scores: Optional[torch.Tensor] = None, idx: Optional[torch.Tensor] = None,
+                   n_sel: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """The fused indexer + selection (token keys): (scores, idx, n_sel) exactly as idx_score followed
+    by idx_topk would give them."""
+    _need_cuda(q, w, k, scores, idx, n_sel, workspace)
+    rows, H, d = q.shape
+    assert rows == batch.n_rows and w.shape == (rows, H) and w.dtype == torch.float32
+    assert q.is_contiguous() and w.is_contiguous() and k.stride(-1) == 1
+    kk = 2048 if top_k == -1 else top_k
+    if scores is None:
+        scores = torch.empty(rows, max(batch.max_n_kv, 1), device=q.device, dtype=torch.float32)
+    if idx is None:
+        idx = torch.empty(rows, kk, device=q.device, dtype=torch.int32)
+    if n_sel is None:
+        n_sel = torch.empty(rows, device=q.device, dtype=torch.int32)
+    if workspace is None:
+        need = idx_workspace_size(IDX_OP_SCORE_TOPK, rows, batch.max_n_kv, top_k)
+        if need:
+            workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().idx_score_topk(_ptr(q), _dtype(q), _ptr(w), H, d, _ptr(k), _dtype(k), k.stride(0), k.shape[0],
+                                 batch.c(), top_k, _ptr(scores), scores.stride(0), _ptr(idx), idx.stride(0),
+                                 _ptr(n_sel), _ptr(workspace), ws_bytes, _stream(q.device)))
+    return scores, idx, n_sel
 
 
 def sparse_attn_decode_noalloc(q, latent, batch, idx, n_sel, scale, *, out=None, out_dtype=torch.bfloat16):

@@ -344,6 +344,53 @@ idx_status idx_topk(const float* scores, int64_t score_row_stride, idx_batch bat
                      what);
 }
 
+idx_status idx_score_topk(const void* q, idx_dtype q_dtype, const float* w, int32_t n_heads, int32_t head_dim,
+                          const void* k, idx_dtype k_dtype, int64_t k_row_stride, int64_t k_rows, idx_batch batch,
+                          int32_t top_k, float* scores, int64_t score_row_stride, int32_t* idx,
+                          int64_t idx_row_stride, int32_t* n_sel, void* workspace, size_t workspace_bytes,
+                          idx_stream_t stream) {
+    const char* what = "idx_score_topk";
+    idx_status s = check_batch(batch, what);
+    if (s != IDX_OK) return s;
+    if (top_k == -1) top_k = IDX_DEFAULT_TOP_K;   // the model's configured indexer top_k
+    if (top_k < 1) return fail(IDX_ERR_INVALID_ARG, "%s: top_k < 1 (or -1 for the default)", what);
+    if (!valid_dtype(q_dtype) || !valid_dtype(k_dtype)) return fail(IDX_ERR_INVALID_ARG, "%s: bad dtype", what);
+    if (n_heads < 1 || n_heads > 64) return fail(IDX_ERR_UNSUPPORTED, "%s: n_heads must be in [1, 64]", what);
+    if (head_dim < 1 || head_dim > 256) return fail(IDX_ERR_UNSUPPORTED, "%s: head_dim must be in [1, 256]", what);
+    if (k_row_stride < head_dim) return fail(IDX_ERR_INVALID_ARG, "%s: k_row_stride < head_dim", what);
+    if (k_rows < 0) return fail(IDX_ERR_INVALID_ARG, "%s: k_rows < 0", what);
+    if (score_row_stride < batch.max_n_kv)
+        return fail(IDX_ERR_INVALID_ARG, "%s: score_row_stride < keys per row", what);
+    if (idx_row_stride < top_k) return fail(IDX_ERR_INVALID_ARG, "%s: idx_row_stride < top_k", what);
+    if (workspace && !aligned16(workspace))
+        return fail(IDX_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", what);
+    const int64_t rows = (int64_t)batch.n_seq * batch.n_q_per_seq;
+    if (rows == 0) return IDX_OK;
+    if (!q || !w || !k || !scores || !idx) return fail(IDX_ERR_INVALID_ARG, "%s: NULL q/w/k/scores/idx", what);
+    const cudaStream_t st = (cudaStream_t)stream;
+    // fused: decode rows on the tensor-core scorer, few enough for the multi-CTA select
+    const bool q_exact = q_dtype == k_dtype || (q_dtype == IDX_BF16 && k_dtype == IDX_F16);
+    if (n_heads == 64 && head_dim == 128 && k_dtype != IDX_F32 && q_exact && batch.n_q_per_seq == 1 &&
+        batch.max_n_kv > 0 && rows < 2 * (int64_t)sm_count() && workspace &&
+        workspace_bytes >= topk_fused_workspace_bytes(rows)) {
+        const Geom g = make_geom(batch);
+        cudaError_t e = launch_score_tc(q, q_dtype, w, n_heads, head_dim, k, k_dtype, k_row_stride, k_rows, g, 0,
+                                        scores, score_row_stride, st, topk_fused_hist(workspace),
+                                        topk_fused_counters(workspace, rows), (int)rows);
+        if (e == cudaSuccess)
+            return from_cuda(launch_topk_fused(scores, score_row_stride, g, top_k, idx, idx_row_stride, n_sel,
+                                               workspace, st),
+                             what);
+        if (e != cudaErrorNotSupported) return from_cuda(e, what);
+    }
+    // otherwise the two calls, with the same results
+    s = idx_score(q, q_dtype, w, n_heads, head_dim, k, k_dtype, k_row_stride, k_rows, batch, 0, scores,
+                  score_row_stride, nullptr, 0, stream);
+    if (s != IDX_OK) return s;
+    return idx_topk(scores, score_row_stride, batch, top_k, 0, idx, idx_row_stride, n_sel, workspace,
+                    workspace_bytes, stream);
+}
+
 idx_status sparse_attn_decode(const void* q, idx_dtype dtype, int32_t n_q_heads, int32_t n_kv_heads,
                               int32_t dk, int32_t dv, const void* k, const void* v,
                               int64_t kv_row_stride, int64_t v_row_stride, int64_t kv_rows,
@@ -378,6 +425,11 @@ size_t idx_workspace_size(int32_t op, int64_t n_rows, int32_t max_n_kv, int32_t 
         return generic_attn_workspace_bytes(n_rows, top_k, n_q_heads, dv);
     }
     if (op == IDX_OP_TOPK) return topk_workspace_bytes(n_rows, top_k);
+    if (op == IDX_OP_SCORE_TOPK) {
+        int sms = sm_count();
+        if (sms < 2) sms = 152;
+        return n_rows < 2 * (int64_t)sms ? topk_fused_workspace_bytes(n_rows) : topk_workspace_bytes(n_rows, top_k);
+    }
     return 0;
 }
 

@@ -178,8 +178,8 @@ __device__ __forceinline__ void gather_tiles(Ctl& c, uint8_t* xtiles, const __nv
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_attn_tc_kernel(const __nv_bfloat16* __restrict__ lat, int64_t lat_row_stride,
-                       const __nv_bfloat16* __restrict__ q, Geom g, const int32_t* __restrict__ idx,
-                       int64_t idx_row_stride, const int32_t* __restrict__ n_sel, int64_t kv_rows,
+                       const __nv_bfloat16* __restrict__ q, Geom g, const int32_t* idx,
+                       int64_t idx_row_stride, const int32_t* n_sel, int64_t kv_rows,
                        float scale_log2, int splits, int kps, void* __restrict__ out, int out_dtype,
                        float* __restrict__ part_o, float* __restrict__ part_ml) {
     extern __shared__ uint8_t smem_raw[];
@@ -571,8 +571,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // Merge key splits: out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s over splits with l_s > 0.
-__global__ void __launch_bounds__(128) mla_combine_kernel(const float* __restrict__ part_o,
-                                                          const float* __restrict__ part_ml, int splits,
+__global__ void __launch_bounds__(128) mla_combine_kernel(const float* part_o,
+                                                          const float* part_ml, int splits,
                                                           void* __restrict__ out, int out_dtype) {
     pdl_trigger();
     pdl_wait();

@@ -33,6 +33,15 @@
 //   warp 6      q stager: converts each chunk's query row q to the key dtype
 //               with 16-byte loads and writes it, swizzled, into one of two q
 //               buffers (the MMA's B operand), a chunk ahead of the MMAs.
+// With a histogram buffer (the fused score + top-k), the epilogue also counts
+// every score of a row into a 2048-bin histogram of its order key's top 11
+// bits: each warp folds equal bins (match_any) and adds them to global memory
+// with fire-and-forget atomics.  The launch zeroes the histograms itself: each
+// CTA clears a slice in its prologue and counts itself on the slot's third
+// counter, and the epilogue adds nothing before every CTA has (a grid barrier,
+// safe because the persistent CTAs, one per SM, are all resident once the
+// previous kernel has drained; the wait is bounded, and a timeout leaves the
+// histogram incomplete, which the select detects and bypasses).
 // Every wait is bounded; a timeout records IDX_ERR_TIMEOUT and the CTA winds
 // down (drains its TMA loads and MMAs, frees TMEM) instead of hanging.
 #include <algorithm>
@@ -44,10 +53,11 @@
 
 namespace lidx {
 
-// chunk counters of the decode scorer: [next chunk, CTAs finished] per slot; a
-// launch uses one slot (round-robin on the host) and its last CTA zeroes it
+// chunk counters of the decode scorer: [next chunk, CTAs finished, CTAs whose
+// histogram slice is zeroed] per slot; a launch uses one slot (round-robin on
+// the host) and its last CTA zeroes it
 constexpr int kSchedSlots = 1024;
-__device__ unsigned int g_score_sched[kSchedSlots][2];
+__device__ unsigned int g_score_sched[kSchedSlots][3];
 
 namespace {
 using namespace sm100;
@@ -271,7 +281,8 @@ template <typename TK, bool kQ8>
 __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decode_kernel(
     const __grid_constant__ CUtensorMap kmap, const void* __restrict__ q, int q_dtype,
     const float* __restrict__ w, Geom g, float* __restrict__ scores, int64_t score_row_stride, int sched_slot,
-    const float* __restrict__ k_scale, int64_t k_rows) {
+    const float* __restrict__ k_scale, int64_t k_rows, uint32_t* __restrict__ hist, uint32_t* __restrict__ zero2,
+    int n_zero2) {
     constexpr int kNT = kQ8 ? kThreadsQ8 : kThreads;
     constexpr int kTmaStages = kQ8 ? kRawStages : kStages;   // the producer's ring
     constexpr int kTmaStride = kQ8 ? kRawTileBytes : kTileBytes;
@@ -359,9 +370,24 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
         tmem_alloc(&c.tmem_base, kTmemCols);
         tmem_relinquish();
     }
+    if (hist) {
+        // this CTA's slice of the histograms (rows x 2048 counts, 16-byte stores), and the
+        // select's per-row counters
+        const int64_t n4 = n_rows * 512;
+        const int64_t per = (n4 + gridDim.x - 1) / gridDim.x;
+        const int64_t a = (int64_t)blockIdx.x * per, e = min(n4, a + per);
+        uint4* h4 = reinterpret_cast<uint4*>(hist);
+        for (int64_t i = a + threadIdx.x; i < e; i += kNT) h4[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (blockIdx.x == 0)
+            for (int i = threadIdx.x; i < n_zero2; i += kNT) zero2[i] = 0u;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (hist && threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(&g_score_sched[sched_slot][2], 1u);
+    }
     const uint32_t tmem = c.tmem_base;
     const int n_chunks = c.n_chunks;
 
@@ -632,6 +658,16 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
         uint32_t aphase = 0;
         float wv[kH];
         bool ok = true;
+        // fused top-k: no count is added before every CTA has zeroed its histogram slice
+        bool use_hist = hist != nullptr;
+        if (use_hist) {
+            int ready = 1;
+            if (lane == 0) ready = wait_counter(&g_score_sched[sched_slot][2], gridDim.x) ? 1 : 0;
+            if (!__shfl_sync(0xffffffffu, ready, 0)) {
+                flag(g.status, IDX_ERR_TIMEOUT);
+                use_hist = false;
+            }
+        }
         for (int k = 0; ok; ++k) {
             Chunk d;
             if (warp_aborted(c) || !warp_next_chunk(c, k, d)) {
@@ -734,7 +770,15 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                     }
                     float s = (s0 + s1) + (s2 + s3);
                     if constexpr (kQ8) s *= sc;
-                    if (j < n_keys) scores[d.row * score_row_stride + j] = s + 0.0f;
+                    s += 0.0f;   // -0 + +0 = +0
+                    if (j < n_keys) scores[d.row * score_row_stride + j] = s;
+                    if (use_hist) {
+                        // equal bins of the warp folded into one atomic add
+                        const uint32_t bin = j < n_keys ? order_key(s) >> 21 : 0xffffffffu;
+                        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+                        if (j < n_keys && lane == __ffs(peers) - 1)
+                            atomicAdd(&hist[d.row * 2048 + bin], (uint32_t)__popc(peers));
+                    }
                     if (++acc == kAcc) {
                         acc = 0;
                         aphase ^= 1;
@@ -754,6 +798,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
         if (atomicAdd(&g_score_sched[sched_slot][1], 1u) == gridDim.x - 1) {
             atomicExch(&g_score_sched[sched_slot][0], 0u);
             atomicExch(&g_score_sched[sched_slot][1], 0u);
+            atomicExch(&g_score_sched[sched_slot][2], 0u);
             __threadfence();
         }
     }
@@ -1160,13 +1205,15 @@ cudaError_t launch_score_tc_q8(const void* q, int q_dtype, const float* w, const
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kThreadsQ8), smem, st, map, q, q_dtype, w, g, scores, score_row_stride,
-                      slot, k_scale, k_rows);
+                      slot, k_scale, k_rows, static_cast<uint32_t*>(nullptr), static_cast<uint32_t*>(nullptr), 0);
 }
 
 cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, int d, const void* k,
                             int k_dtype, int64_t k_row_stride, int64_t k_rows, const Geom& g, int block_size,
-                            float* scores, int64_t score_row_stride, cudaStream_t st) {
+                            float* scores, int64_t score_row_stride, cudaStream_t st, uint32_t* hist,
+                            uint32_t* zero2, int n_zero2) {
     if (H != kH || d != kD || k_dtype == IDX_F32 || block_size > 1) return cudaErrorNotSupported;
+    if (hist && g.T != 1) return cudaErrorNotSupported;   // the histogram epilogue is the decode scorer's
     if (g.T >= 64) {
         // many query rows per sequence: query tiles on the tensor cores (same-type operands)
         if (q_dtype != k_dtype || (reinterpret_cast<uintptr_t>(q) & 15u) || (k_row_stride % 8)) return cudaErrorNotSupported;
@@ -1189,7 +1236,7 @@ cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, i
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, st, map, q, q_dtype, w, g, scores,
-                      score_row_stride, slot, static_cast<const float*>(nullptr), k_rows);
+                      score_row_stride, slot, static_cast<const float*>(nullptr), k_rows, hist, zero2, n_zero2);
 }
 
 }  // namespace lidx

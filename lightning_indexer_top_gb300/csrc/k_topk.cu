@@ -72,7 +72,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, GenShared<NT>& s
 // the bin (of `bits` bits at `shift`) that holds the `need`-th largest key and
 // the number of matching keys in higher bins.
 template <int NT>
-__device__ __forceinline__ void radix_round(const float* __restrict__ s, int n, uint32_t prefix,
+__device__ __forceinline__ void radix_round(const float* s, int n, uint32_t prefix,
                                             uint32_t mask, int shift, int bits, uint32_t need,
                                             GenShared<NT>& sh) {
     const int nbins = 1 << bits;
@@ -149,8 +149,8 @@ __device__ __forceinline__ void radix_round(const float* __restrict__ s, int n, 
 
 // The general selection of one row by a CTA of NT threads.
 template <bool kBlocks, int NT>
-__device__ __forceinline__ void select_row(const float* __restrict__ s, int n_vis, int top_k, int C,
-                                           int32_t* __restrict__ out, int32_t* n_sel_row, GenShared<NT>& sh) {
+__device__ __forceinline__ void select_row(const float* s, int n_vis, int top_k, int C,
+                                           int32_t* out, int32_t* n_sel_row, GenShared<NT>& sh) {
     constexpr int kChunk = NT * kPer;
     // n = candidates (tokens or complete blocks), K = how many of them to take
     const int n = kBlocks ? n_vis / C : n_vis;
@@ -244,11 +244,11 @@ __device__ __forceinline__ void select_row(const float* __restrict__ s, int n_vi
 }
 
 template <bool kBlocks>
-__global__ void __launch_bounds__(kThreads) topk_kernel(const float* __restrict__ scores,
+__global__ void __launch_bounds__(kThreads) topk_kernel(const float* scores,
                                                         int64_t score_row_stride, Geom g, int top_k,
-                                                        int C, int32_t* __restrict__ idx,
+                                                        int C, int32_t* idx,
                                                         int64_t idx_row_stride,
-                                                        int32_t* __restrict__ n_sel) {
+                                                        int32_t* n_sel) {
     __shared__ GenShared<kThreads> sh;
     const int64_t r = blockIdx.x;
     select_row<kBlocks, kThreads>(scores + r * score_row_stride, row_n_vis(g, r), top_k, C,
@@ -369,10 +369,10 @@ __device__ __forceinline__ void map_cand_hist(MapShared& sh, uint32_t n_cand, ui
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kMapThreads, 1) topk_map_kernel(const float* __restrict__ scores,
+__global__ void __launch_bounds__(kMapThreads, 1) topk_map_kernel(const float* scores,
                                                                   int64_t score_row_stride, Geom g, int top_k,
-                                                                  int32_t* __restrict__ idx, int64_t idx_row_stride,
-                                                                  int32_t* __restrict__ n_sel) {
+                                                                  int32_t* idx, int64_t idx_row_stride,
+                                                                  int32_t* n_sel) {
     extern __shared__ __align__(16) unsigned char map_raw[];
     MapShared& sh = *reinterpret_cast<MapShared*>(map_raw);
     pdl_trigger();
@@ -584,7 +584,7 @@ __host__ __device__ inline McLayout mc_layout(void* ws, int64_t rows) {
 }
 
 // threshold bin of row r from its histogram: bin holding the K-th largest key
-__device__ __forceinline__ void mc_find_bin(const uint32_t* __restrict__ h, uint32_t K, uint32_t* bin_out,
+__device__ __forceinline__ void mc_find_bin(const uint32_t* h, uint32_t K, uint32_t* bin_out,
                                             uint32_t* above_out, uint32_t* scratch) {
     // thread t owns bins [2047 - 8t - 7, 2047 - 8t], walked from the top
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -613,7 +613,7 @@ __device__ __forceinline__ void mc_find_bin(const uint32_t* __restrict__ h, uint
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kMcThreads) topk_mc_bound_kernel(const float* __restrict__ scores,
+__global__ void __launch_bounds__(kMcThreads) topk_mc_bound_kernel(const float* scores,
                                                                    int64_t score_row_stride, Geom g, int top_k,
                                                                    McLayout L) {
     __shared__ uint32_t hist[2048];
@@ -662,23 +662,14 @@ __global__ void __launch_bounds__(kMcThreads) topk_mc_bound_kernel(const float* 
     if (threadIdx.x == 0) L.bound[r] = (b1 << 21) | (sb[0] << 10);
 }
 
-__global__ void __launch_bounds__(kMcThreads) topk_mc_filter_kernel(const float* __restrict__ scores,
-                                                                    int64_t score_row_stride, Geom g, int top_k,
-                                                                    McLayout L) {
-    __shared__ uint64_t buf[kMcLocal];
-    __shared__ uint32_t nbuf, base;
-    pdl_trigger();
-    pdl_wait();
-    const int64_t r = blockIdx.y;
-    const int n = row_n_vis(g, r);
-    const int K = min(top_k, n);
-    const int c0 = blockIdx.x * kMcChunk;
-    if (K == n || c0 >= n) return;
-    const uint32_t lo = L.bound[r];
+// append every position j in [c0, c1) of row r whose order key is >= lo to the row's candidate
+// list (key << 32 | position): warp-aggregated slots in a shared buffer, one global reservation
+// per CTA for the buffer, straight to the list when the buffer is full
+__device__ __forceinline__ void mc_filter_range(const float* s, int c0, int c1, uint32_t lo,
+                                                const McLayout& L, int64_t r, uint64_t* buf, uint32_t& nbuf,
+                                                uint32_t& base) {
     if (threadIdx.x == 0) nbuf = 0u;
     __syncthreads();
-    const float* s = scores + r * score_row_stride;
-    const int c1 = min(n, c0 + kMcChunk);
     const int lane = threadIdx.x & 31;
     uint32_t* cnt = L.cnt + r;
     uint64_t* cand = L.cand + r * (int64_t)kMcCandCap;
@@ -719,11 +710,64 @@ __global__ void __launch_bounds__(kMcThreads) topk_mc_filter_kernel(const float*
         if (base + i < (uint32_t)kMcCandCap) cand[base + i] = buf[i];
 }
 
-__global__ void __launch_bounds__(kMapThreads, 1) topk_mc_finish_kernel(const float* __restrict__ scores,
+__global__ void __launch_bounds__(kMcThreads) topk_mc_filter_kernel(const float* scores,
+                                                                    int64_t score_row_stride, Geom g, int top_k,
+                                                                    McLayout L) {
+    __shared__ uint64_t buf[kMcLocal];
+    __shared__ uint32_t nbuf, base;
+    pdl_trigger();
+    pdl_wait();
+    const int64_t r = blockIdx.y;
+    const int n = row_n_vis(g, r);
+    const int K = min(top_k, n);
+    const int c0 = blockIdx.x * kMcChunk;
+    if (K == n || c0 >= n) return;
+    mc_filter_range(scores + r * score_row_stride, c0, min(n, c0 + kMcChunk), L.bound[r], L, r, buf, nbuf, base);
+}
+
+// Fused path: the scorer left an exact histogram of each row's order keys by their top 11 bits.
+// The bin b* holding the K-th largest key follows from it directly: every key in a higher bin is
+// selected, and only the keys of b* remain to be ranked, so the filter keeps the keys with bin
+// >= b* (exactly above + hist[b*] of them) and the finish kernel resolves b*.  A histogram whose
+// total is not the row's key count (its launch could not count, see the scorer) sets the bound to
+// 0: every key becomes a candidate, the list overflows, and the finish takes the general path.
+__global__ void __launch_bounds__(kMcThreads) topk_hist_filter_kernel(const float* scores,
+                                                                      int64_t score_row_stride, Geom g, int top_k,
+                                                                      McLayout L, const uint32_t* hist,
+                                                                      int chunk) {
+    __shared__ uint64_t buf[kMcLocal];
+    __shared__ uint32_t nbuf, base;
+    __shared__ uint32_t scratch[kMcThreads / 32];
+    __shared__ uint32_t sb[3];
+    pdl_trigger();
+    pdl_wait();
+    const int64_t r = blockIdx.y;
+    const int n = row_n_vis(g, r);
+    const int K = min(top_k, n);
+    const int c0 = blockIdx.x * chunk;
+    if (K == n || c0 >= n) return;
+    const uint32_t* h = hist + r * 2048;
+    if (threadIdx.x == 0) {
+        sb[0] = 0u;
+        sb[2] = 0u;
+    }
+    __syncthreads();
+    uint32_t part = 0;
+    for (int i = threadIdx.x; i < 2048; i += kMcThreads) part += h[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&sb[2], part);
+    mc_find_bin(h, (uint32_t)K, &sb[0], &sb[1], scratch);
+    const uint32_t lo = sb[2] == (uint32_t)n ? sb[0] << 21 : 0u;
+    if (blockIdx.x == 0 && threadIdx.x == 0) L.bound[r] = lo;
+    mc_filter_range(scores + r * score_row_stride, c0, min(n, c0 + chunk), lo, L, r, buf, nbuf, base);
+}
+
+__global__ void __launch_bounds__(kMapThreads, 1) topk_mc_finish_kernel(const float* scores,
                                                                        int64_t score_row_stride, Geom g, int top_k,
-                                                                       McLayout L, int32_t* __restrict__ idx,
+                                                                       McLayout L, int32_t* idx,
                                                                        int64_t idx_row_stride,
-                                                                       int32_t* __restrict__ n_sel) {
+                                                                       int32_t* n_sel) {
     extern __shared__ __align__(16) unsigned char map_raw[];
     MapShared& sh = *reinterpret_cast<MapShared*>(map_raw);
     GenShared<kMapThreads>& gsh = *reinterpret_cast<GenShared<kMapThreads>*>(map_raw);
@@ -833,6 +877,41 @@ cudaError_t launch_topk(const float* scores, int64_t score_row_stride, const Geo
                           score_row_stride, g, top_k, idx, idx_row_stride, n_sel);
     }
     return cudaGetLastError();
+}
+
+size_t topk_fused_workspace_bytes(int64_t n_rows) {
+    if (n_rows <= 0) return 0;
+    return (size_t)n_rows * 2048 * sizeof(uint32_t) + mc_bytes(n_rows);
+}
+
+// the fused workspace: [rows][2048] histogram counts, then the candidate lists of the multi-CTA path
+uint32_t* topk_fused_hist(void* ws) { return static_cast<uint32_t*>(ws); }
+uint32_t* topk_fused_counters(void* ws, int64_t n_rows) {
+    return mc_layout(static_cast<char*>(ws) + (size_t)n_rows * 2048 * sizeof(uint32_t), n_rows).cnt;
+}
+
+cudaError_t launch_topk_fused(const float* scores, int64_t score_row_stride, const Geom& g, int top_k, int32_t* idx,
+                              int64_t idx_row_stride, int32_t* n_sel, void* ws, cudaStream_t st) {
+    const int64_t n_rows = (int64_t)g.B * g.T;
+    if (n_rows == 0) return cudaSuccess;
+    const uint32_t* hist = static_cast<const uint32_t*>(ws);
+    const McLayout L = mc_layout(static_cast<char*>(ws) + (size_t)n_rows * 2048 * sizeof(uint32_t), n_rows);
+    // filter chunks: about two CTAs per SM over the whole batch, 2048 to 32768 scores each
+    int sms = sm_count();
+    if (sms < 2) sms = 152;
+    int64_t chunk = ((int64_t)n_rows * g.max_n_kv + 2 * sms - 1) / (2 * sms);
+    chunk = (chunk + 2047) / 2048 * 2048;
+    chunk = chunk < 2048 ? 2048 : (chunk > 32768 ? 32768 : chunk);
+    const int64_t chunks = (g.max_n_kv + chunk - 1) / chunk;
+    if (chunks > 0) {
+        cudaError_t e = launch_pdl(topk_hist_filter_kernel, dim3((unsigned)chunks, (unsigned)n_rows), dim3(kMcThreads),
+                                   0, st, scores, score_row_stride, g, top_k, L, hist, (int)chunk);
+        if (e != cudaSuccess) return e;
+    }
+    const size_t sm = sizeof(MapShared);
+    cudaFuncSetAttribute(topk_mc_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    return launch_pdl(topk_mc_finish_kernel, dim3((unsigned)n_rows), dim3(kMapThreads), sm, st, scores,
+                      score_row_stride, g, top_k, L, idx, idx_row_stride, n_sel);
 }
 
 size_t topk_workspace_bytes(int64_t n_rows, int top_k) {

@@ -57,6 +57,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return true;
 }
 
+// wait until the global counter *p reaches `target` (acquire); false on timeout
+__device__ __forceinline__ bool wait_counter(const unsigned int* p, unsigned int target) {
+    const long long t0 = clock64();
+    for (;;) {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target) return true;
+        if (clock64() - t0 > kWaitCycles) return false;
+        __nanosleep(64);
+    }
+}
+
 // wait with cluster-scope acquire: for phases completed by release-arrivals of
 // another CTA of the cluster (data that CTA stored into this CTA's memory)
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {

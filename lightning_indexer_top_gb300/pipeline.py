@@ -11,6 +11,7 @@ from __future__ import annotations
 import torch
 
 from . import Batch, idx_block_pool, idx_block_pool_update, idx_hadamard, idx_score, idx_score_q8, idx_topk, idx_workspace_size, topk_capacity
+from . import idx_score_topk, IDX_OP_SCORE_TOPK
 from . import sparse_attn_decode, sparse_attn_prefill, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL, IDX_OP_TOPK
 from .workloads import Workload
 
@@ -21,7 +22,7 @@ class SparseAttentionStep:
     re-pools only the newest complete block of every sequence, as a decode step does when
     its token has just completed a block (idx_block_pool_update)."""
 
-    def __init__(self, wl: Workload, out_dtype=None, pool: str = "full"):
+    def __init__(self, wl: Workload, out_dtype=None, pool: str = "full", fused: bool = True):
         self.wl = wl
         self.pool_mode = pool
         dev = wl.q_idx.device
@@ -43,7 +44,10 @@ class SparseAttentionStep:
         cap = topk_capacity(wl.top_k, C)
         self.idx = torch.empty(rows, cap, device=dev, dtype=torch.int32)
         self.n_sel = torch.empty(rows, device=dev, dtype=torch.int32)
-        tws = idx_workspace_size(IDX_OP_TOPK, rows, wl.max_n_kv, wl.top_k) if C <= 1 else 0
+        # decode rows over token keys in a 16-bit cache: scoring and selection in one fused call
+        self.fused = fused and C <= 1 and wl.k8 is None and wl.T == 1 and wl.H == 64 and wl.d == 128
+        op = IDX_OP_SCORE_TOPK if self.fused else IDX_OP_TOPK
+        tws = idx_workspace_size(op, rows, wl.max_n_kv, wl.top_k) if C <= 1 else 0
         self.topk_ws = torch.empty(tws, device=dev, dtype=torch.uint8) if tws else None
         if out_dtype is None:   # f32 in -> f32 out, 16-bit in -> bf16 out
             out_dtype = torch.float32 if wl.q_attn.dtype == torch.float32 else torch.bfloat16
@@ -77,10 +81,15 @@ class SparseAttentionStep:
             idx_score(q, wl.w, kp, self.pool_batch, block_size=wl.block_size, scores=self.scores)
         elif wl.k8 is not None:
             idx_score_q8(q, wl.w, wl.k8, wl.k_scale, self.batch, scores=self.scores)
+        elif self.fused:
+            idx_score_topk(q, wl.w, k, self.batch, wl.top_k, scores=self.scores, idx=self.idx, n_sel=self.n_sel,
+                           workspace=self.topk_ws)
         else:
             idx_score(q, wl.w, k, self.batch, scores=self.scores)
 
     def select(self):
+        if self.fused:
+            return   # selected by the fused call in score()
         idx_topk(self.scores, self.batch, self.wl.top_k, block_size=self.wl.block_size, idx=self.idx,
                  n_sel=self.n_sel, workspace=self.topk_ws)
 
@@ -104,8 +113,10 @@ class SparseAttentionStep:
     def launches_per_step(self) -> int:
         """Kernels one run() enqueues (library launches only)."""
         n = 3 + (1 if self.attn_ws is not None else 0)   # score, select, attend (+ split combine)
-        if self.topk_ws is not None:
-            n += 2                              # multi-CTA select: histogram, filter, finish
+        if self.fused:
+            n += 1                              # fused select: filter, finish
+        elif self.topk_ws is not None:
+            n += 2                              # multi-CTA select: bound, filter, finish
         if self.q_rot is not None:
             n += 2                              # two Hadamard rotations
         if self.wl.block_size > 1:

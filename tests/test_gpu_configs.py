@@ -294,3 +294,24 @@ def test_decode_chain_back_to_back_equals_synchronised_steps(make_args):
     for name, n_sel, idx, out in got:
         assert torch.equal(n_sel, ref[name][0]) and torch.equal(idx, ref[name][1]), name
         assert torch.equal(out, ref[name][2]), name
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused_select", "separate_select"])
+def test_first_step_reads_the_selection_it_waits_for(fused):
+    # A fresh step whose selection buffers hold sentinels: the attention, launched while the select
+    # may still run (programmatic dependent launch), must read the selection that select writes,
+    # not the sentinels: the step's output equals attention re-run after a full synchronisation.
+    wl = workloads.make(5, batch_override=16)
+    for _ in range(3):
+        st = SparseAttentionStep(wl, fused=fused)
+        st.idx.fill_(-7)
+        st.n_sel.fill_(-7)
+        st.out.zero_()
+        torch.cuda.synchronize()
+        st.run()
+        torch.cuda.synchronize()
+        first = st.out.clone()
+        st.attend()
+        torch.cuda.synchronize()
+        assert torch.equal(first, st.out)
+    assert L.idx_device_status(reset=True) == 0

@@ -158,6 +158,65 @@ def test_topk_bit_exact(case, top_k, path):
         assert np.all(idx_h[r, len(ref):] == -1)
 
 
+def _fused_case(name):
+    """(q bf16 [B,64,128], w f32 [B,64], F16 key cache, n_kv per row, top_k) for the fused score + top-k."""
+    g = torch.Generator().manual_seed(91)
+    if name == "ragged":
+        n_kv = [65536, 3000, 2048, 2049, 0, 1, 40000, 131072]
+    elif name == "short_rows":
+        n_kv = [8192] * 8
+    else:   # "ties": every key row repeated 4 times, so each score appears 4 times (ties across the cut)
+        n_kv = [20000, 65536, 4096]
+    B, n = len(n_kv), max(n_kv)
+    q = torch.randn(B, 64, 128, generator=g).to(torch.bfloat16)
+    w = torch.randn(B, 64, generator=g) / 8
+    k = torch.randn(B * n, 128, generator=g).to(torch.float16)
+    if name == "ties":
+        k = k.view(B, n, 128)[:, : n // 4].unsqueeze(2).expand(B, n // 4, 4, 128).reshape(B * n, 128).contiguous()
+    return q, w, k, n_kv, 2048
+
+
+@pytest.mark.parametrize("name", ["ragged", "short_rows", "ties"])
+def test_fused_score_topk_equals_score_then_topk(name):
+    # the histogram-driven select gives exactly what idx_score + idx_topk give, and what the
+    # oracle's stable selection gives on the same f32 scores
+    q, w, k, n_kv, top_k = _fused_case(name)
+    B, n = len(n_kv), max(n_kv)
+    batch = L.Batch(_i32(n_kv), 1, n, kv_seq_stride=n)
+    qd, wd, kd = q.to(DEV), w.to(DEV), k.to(DEV)
+    assert L.idx_workspace_size(L.IDX_OP_SCORE_TOPK, B, n, top_k) > 0
+    s1, idx1, ns1 = L.idx_score_topk(qd, wd, kd, batch, top_k)
+    s2 = L.idx_score(qd, wd, kd, batch)
+    idx2, ns2 = L.idx_topk(s2, batch, top_k)
+    torch.cuda.synchronize()
+    assert L.idx_device_status(reset=True) == 0
+    for r in range(B):
+        assert torch.equal(s1[r, :n_kv[r]], s2[r, :n_kv[r]]), r
+    assert torch.equal(ns1, ns2) and torch.equal(idx1, idx2)
+    sh = s1.cpu().numpy()
+    for r in range(B):
+        ref = O.topk_select(sh[r], n_kv[r], top_k)
+        assert int(ns1[r]) == len(ref) and idx1[r, :len(ref)].tolist() == ref.tolist(), r
+
+
+def test_fused_score_topk_back_to_back_launches():
+    # each fused launch zeroes its own histograms: repeated calls on alternating inputs give the
+    # same selections as isolated calls
+    q, w, k, n_kv, top_k = _fused_case("ragged")
+    B, n = len(n_kv), max(n_kv)
+    batch = L.Batch(_i32(n_kv), 1, n, kv_seq_stride=n)
+    qd, wd, kd = q.to(DEV), w.to(DEV), k.to(DEV)
+    q2 = qd.flip(0).contiguous()
+    ws = torch.empty(L.idx_workspace_size(L.IDX_OP_SCORE_TOPK, B, n, top_k), device=DEV, dtype=torch.uint8)
+    ref = [L.idx_score_topk(x, wd, kd, batch, top_k, workspace=ws)[1].clone() for x in (qd, q2)]
+    torch.cuda.synchronize()
+    outs = [L.idx_score_topk(x, wd, kd, batch, top_k, workspace=ws)[1].clone() for x in (qd, q2, qd, q2, qd)]
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        assert torch.equal(o, ref[i % 2]), i
+    assert L.idx_device_status(reset=True) == 0
+
+
 def test_topk_default_minus_one_equals_2048():
     g = torch.Generator().manual_seed(45)
     scores = torch.randn(3, 40000, generator=g).to(DEV)
