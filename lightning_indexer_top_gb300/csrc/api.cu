@@ -371,12 +371,12 @@ idx_status idx_score_topk(const void* q, idx_dtype q_dtype, const float* w, int3
     // fused: decode rows on the tensor-core scorer, few enough for the multi-CTA select
     const bool q_exact = q_dtype == k_dtype || (q_dtype == IDX_BF16 && k_dtype == IDX_F16);
     if (n_heads == 64 && head_dim == 128 && k_dtype != IDX_F32 && q_exact && batch.n_q_per_seq == 1 &&
-        batch.max_n_kv > 0 && rows < 2 * (int64_t)sm_count() && workspace &&
+        batch.max_n_kv > 0 && rows < 2 * (int64_t)sm_count() && rows <= 1024 && workspace &&
         workspace_bytes >= topk_fused_workspace_bytes(rows)) {
         const Geom g = make_geom(batch);
+        const FusedArrays fa = topk_fused_arrays(workspace, rows);
         cudaError_t e = launch_score_tc(q, q_dtype, w, n_heads, head_dim, k, k_dtype, k_row_stride, k_rows, g, 0,
-                                        scores, score_row_stride, st, topk_fused_hist(workspace),
-                                        topk_fused_counters(workspace, rows), (int)rows);
+                                        scores, score_row_stride, st, fa.hist, fa.cnt);
         if (e == cudaSuccess)
             return from_cuda(launch_topk_fused(scores, score_row_stride, g, top_k, idx, idx_row_stride, n_sel,
                                                workspace, st),

@@ -35,8 +35,11 @@
 //               buffers (the MMA's B operand), a chunk ahead of the MMAs.
 // With a histogram buffer (the fused score + top-k), the epilogue also counts
 // every score of a row into a 2048-bin histogram of its order key's top 11
-// bits: each warp folds equal bins (match_any) and adds them to global memory
-// with fire-and-forget atomics.  The launch zeroes the histograms itself: each
+// bits: each warp folds equal bins (match_any) into a shared-memory histogram
+// of the chunk (two counts of 16 bits per word, two buffers used in turn), and
+// when all four epilogue warps have finished the chunk (an mbarrier), each
+// flushes its quarter of the nonzero bins to the row's global histogram with
+// atomic adds and clears them.  The launch zeroes the histograms itself: each
 // CTA clears a slice in its prologue and counts itself on the slot's third
 // counter, and the epilogue adds nothing before every CTA has (a grid barrier,
 // safe because the persistent CTAs, one per SM, are all resident once the
@@ -61,6 +64,12 @@ __device__ unsigned int g_score_sched[kSchedSlots][3];
 
 namespace {
 using namespace sm100;
+
+// the fused select's inputs the decode scorer produces (all NULL: plain scoring)
+struct HistOut {
+    uint32_t* hist;       // [rows][2048] counts of the order keys' top 11 bits
+    uint32_t* cnt;        // [rows] candidate counters of the select, zeroed here
+};
 
 constexpr int kTileKeys = 128;
 constexpr int kH = 64;
@@ -97,7 +106,8 @@ constexpr int kRing = 4;                             // chunk descriptors in fli
 #define LIDX_SCORE_QBUFS 3
 #endif
 constexpr int kQBufs = LIDX_SCORE_QBUFS;             // staged q rows (one per chunk) in flight
-constexpr int kMaxPrefixRows = 2048;
+constexpr int kMaxPrefixRows = 1024;
+constexpr int kHistWords = 1024;                     // 2048 bins, two 16-bit counts per word
 
 struct Chunk {
     int64_t row;      // query row, -1 = no more chunks
@@ -118,6 +128,7 @@ struct Ctl {
     uint64_t cfull[kRing];
     uint64_t cempty[kRing];
     uint64_t done;
+    uint64_t hdone[2];             // fused top-k: the 4 epilogue warps finished adding a chunk's counts
     Chunk chunk[kRing];
     uint32_t tmem_base;
     int abort;
@@ -131,7 +142,7 @@ constexpr size_t smem_bytes() {
     return 1024 + (Q8 ? (size_t)kRawStages * kRawTileBytes + (size_t)kConvStages * kTileBytes
                       : (size_t)kStages * kTileBytes) +
            kQBufs * kQBytes + sizeof(Ctl) + (2 * kMaxPrefixRows + 1) * sizeof(int) +
-           (Q8 ? kSRing * kTileKeys * sizeof(float) : 0);
+           (Q8 ? kSRing * kTileKeys * sizeof(float) : 2 * kHistWords * sizeof(uint32_t));
 }
 constexpr size_t kSmemBytes = smem_bytes<false>();
 static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448, "shared memory");
@@ -281,8 +292,8 @@ template <typename TK, bool kQ8>
 __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decode_kernel(
     const __grid_constant__ CUtensorMap kmap, const void* __restrict__ q, int q_dtype,
     const float* __restrict__ w, Geom g, float* __restrict__ scores, int64_t score_row_stride, int sched_slot,
-    const float* __restrict__ k_scale, int64_t k_rows, uint32_t* __restrict__ hist, uint32_t* __restrict__ zero2,
-    int n_zero2) {
+    const float* __restrict__ k_scale, int64_t k_rows, HistOut ho) {
+    uint32_t* hist = ho.hist;
     constexpr int kNT = kQ8 ? kThreadsQ8 : kThreads;
     constexpr int kTmaStages = kQ8 ? kRawStages : kStages;   // the producer's ring
     constexpr int kTmaStride = kQ8 ? kRawTileBytes : kTileBytes;
@@ -300,6 +311,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
     int* nvis = pre + kMaxPrefixRows + 1;                    // [n_rows] in prefix mode
     float* escale = reinterpret_cast<float*>(nvis + kMaxPrefixRows);   // int8 keys: [4 warps][8 tiles][32],
                                                                        // or with inline scales [kSRing][128]
+    uint32_t* shist = reinterpret_cast<uint32_t*>(nvis + kMaxPrefixRows);   // 16-bit keys: 2 x kHistWords
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n_rows = (int64_t)g.B * g.T;
@@ -333,6 +345,8 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
             mbar_init(&c.cempty[i], kChunkReaders + (kQ8 ? 4 : 0));
         }
         mbar_init(&c.done, 1);
+        mbar_init(&c.hdone[0], 4);
+        mbar_init(&c.hdone[1], 4);
         c.abort = 0;
         fence_mbar_init();
     }
@@ -370,6 +384,8 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
         tmem_alloc(&c.tmem_base, kTmemCols);
         tmem_relinquish();
     }
+    if (!kQ8 && hist)
+        for (int i = threadIdx.x; i < 2 * kHistWords; i += kNT) shist[i] = 0u;
     if (hist) {
         // this CTA's slice of the histograms (rows x 2048 counts, 16-byte stores), and the
         // select's per-row counters
@@ -379,7 +395,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
         uint4* h4 = reinterpret_cast<uint4*>(hist);
         for (int64_t i = a + threadIdx.x; i < e; i += kNT) h4[i] = make_uint4(0u, 0u, 0u, 0u);
         if (blockIdx.x == 0)
-            for (int i = threadIdx.x; i < n_zero2; i += kNT) zero2[i] = 0u;
+            for (int64_t i = threadIdx.x; i < n_rows; i += kNT) ho.cnt[i] = 0u;
     }
     tc_fence_before();
     __syncthreads();
@@ -400,6 +416,9 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
         int stage = 0;
         uint32_t phase = 0;
         int64_t issued = 0;
+        // key tiles are read once: tag them evict-first in L2, so that the scores this launch
+        // writes (which the fused select reads back) are not pushed out by the stream of keys
+        const uint64_t kpol = l2_evict_first_policy();
         // the next chunk is claimed one chunk ahead, so the counter's round
         // trip overlaps the current chunk's loads
         int ch = 0;
@@ -443,10 +462,10 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                         if (krow < 0 || krow + valid > k_rows) flag(g.status, IDX_ERR_DEVICE_BOUNDS);
                         mbar_arrive_expect_tx(&c.full[stage], kTmaBytes);
                         if constexpr (kQ8) {
-                            tma_load_2d(dst, &kmap, &c.full[stage], 0, (int32_t)krow);
+                            tma_load_2d_hint(dst, &kmap, &c.full[stage], 0, (int32_t)krow, kpol);
                         } else {
-                            tma_load_2d(dst, &kmap, &c.full[stage], 0, (int32_t)krow);
-                            tma_load_2d(dst + kHalfBytes, &kmap, &c.full[stage], 64, (int32_t)krow);
+                            tma_load_2d_hint(dst, &kmap, &c.full[stage], 0, (int32_t)krow, kpol);
+                            tma_load_2d_hint(dst + kHalfBytes, &kmap, &c.full[stage], 64, (int32_t)krow, kpol);
                         }
                         ++issued;
                         if (++stage == kTmaStages) {
@@ -484,11 +503,11 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                                 for (int hh = 0; hh < halves; ++hh) {
                                     const int32_t kr_h = (int32_t)(hh ? kr1 : kr0);
                                     if constexpr (kQ8) {
-                                        tma_load_2d(dst + hh * (kTmaBytes / 2), &kmap, &c.full[stage], 0, kr_h);
+                                        tma_load_2d_hint(dst + hh * (kTmaBytes / 2), &kmap, &c.full[stage], 0, kr_h, kpol);
                                     } else {
-                                        tma_load_2d(dst + hh * (kHalfBytes / 2), &kmap, &c.full[stage], 0, kr_h);
-                                        tma_load_2d(dst + kHalfBytes + hh * (kHalfBytes / 2), &kmap, &c.full[stage],
-                                                    64, kr_h);
+                                        tma_load_2d_hint(dst + hh * (kHalfBytes / 2), &kmap, &c.full[stage], 0, kr_h, kpol);
+                                        tma_load_2d_hint(dst + kHalfBytes + hh * (kHalfBytes / 2), &kmap,
+                                                         &c.full[stage], 64, kr_h, kpol);
                                     }
                                 }
                                 ++issued;
@@ -660,6 +679,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
         bool ok = true;
         // fused top-k: no count is added before every CTA has zeroed its histogram slice
         bool use_hist = hist != nullptr;
+        int64_t hchunk = 0;                        // non-empty chunks this epilogue has finished
         if (use_hist) {
             int ready = 1;
             if (lane == 0) ready = wait_counter(&g_score_sched[sched_slot][2], gridDim.x) ? 1 : 0;
@@ -688,6 +708,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                 wv[4 * h4 + 2] = x.z;
                 wv[4 * h4 + 3] = x.w;
             }
+            const int hb = (int)(hchunk & 1);      // shared histogram buffer of this chunk
             // tiles in groups of 8: an int8 cache's per-key scales of a whole group are
             // loaded at once (one memory round trip per 8 tiles, which the 4 TMEM
             // accumulators give the MMAs slack for) and parked in this lane's own
@@ -772,18 +793,44 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                     if constexpr (kQ8) s *= sc;
                     s += 0.0f;   // -0 + +0 = +0
                     if (j < n_keys) scores[d.row * score_row_stride + j] = s;
-                    if (use_hist) {
-                        // equal bins of the warp folded into one atomic add
-                        const uint32_t bin = j < n_keys ? order_key(s) >> 21 : 0xffffffffu;
-                        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-                        if (j < n_keys && lane == __ffs(peers) - 1)
-                            atomicAdd(&hist[d.row * 2048 + bin], (uint32_t)__popc(peers));
+                    if constexpr (!kQ8) {
+                        if (use_hist) {
+                            // equal bins of the warp folded into one shared-memory add (16-bit halves)
+                            const uint32_t bin = j < n_keys ? order_key(s) >> 21 : 0xffffffffu;
+                            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+                            if (j < n_keys && lane == __ffs(peers) - 1)
+                                atomicAdd(&shist[hb * kHistWords + (bin >> 1)], (uint32_t)__popc(peers) << ((bin & 1) * 16));
+                        }
                     }
                     if (++acc == kAcc) {
                         acc = 0;
                         aphase ^= 1;
                     }
                 }
+            }
+            if constexpr (!kQ8) {
+                if (use_hist && ok) {
+                    // all four epilogue warps have added this chunk's counts: this warp flushes
+                    // its quarter of the buffer's nonzero bins and clears them
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&c.hdone[hb]);
+                    if (!warp_wait(&c.hdone[hb], (uint32_t)((hchunk >> 1) & 1))) {
+                        abort_cta(c, g);
+                        ok = false;
+                    } else {
+                        uint32_t* hw = shist + hb * kHistWords;
+                        uint32_t* grow = hist + d.row * 2048;
+                        for (int i = quad * (kHistWords / 4) + lane; i < (quad + 1) * (kHistWords / 4); i += 32) {
+                            const uint32_t v = hw[i];
+                            if (v) {
+                                hw[i] = 0u;
+                                if (v & 0xffffu) atomicAdd(&grow[2 * i], v & 0xffffu);
+                                if (v >> 16) atomicAdd(&grow[2 * i + 1], v >> 16);
+                            }
+                        }
+                    }
+                }
+                ++hchunk;
             }
         }
     }
@@ -1205,13 +1252,13 @@ cudaError_t launch_score_tc_q8(const void* q, int q_dtype, const float* w, const
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kThreadsQ8), smem, st, map, q, q_dtype, w, g, scores, score_row_stride,
-                      slot, k_scale, k_rows, static_cast<uint32_t*>(nullptr), static_cast<uint32_t*>(nullptr), 0);
+                      slot, k_scale, k_rows, HistOut{nullptr, nullptr});
 }
 
 cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, int d, const void* k,
                             int k_dtype, int64_t k_row_stride, int64_t k_rows, const Geom& g, int block_size,
                             float* scores, int64_t score_row_stride, cudaStream_t st, uint32_t* hist,
-                            uint32_t* zero2, int n_zero2) {
+                            uint32_t* cnt) {
     if (H != kH || d != kD || k_dtype == IDX_F32 || block_size > 1) return cudaErrorNotSupported;
     if (hist && g.T != 1) return cudaErrorNotSupported;   // the histogram epilogue is the decode scorer's
     if (g.T >= 64) {
@@ -1236,7 +1283,8 @@ cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, i
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, st, map, q, q_dtype, w, g, scores,
-                      score_row_stride, slot, static_cast<const float*>(nullptr), k_rows, hist, zero2, n_zero2);
+                      score_row_stride, slot, static_cast<const float*>(nullptr), k_rows,
+                      HistOut{hist, cnt});
 }
 
 }  // namespace lidx

@@ -289,6 +289,7 @@ struct MapShared {
     uint32_t cand_n;
     uint32_t bin, above;
     int overflow;
+    uint32_t total;
 };
 
 // exclusive prefix sums of (a, b) over the CTA
@@ -372,7 +373,7 @@ __device__ __forceinline__ void map_cand_hist(MapShared& sh, uint32_t n_cand, ui
 __global__ void __launch_bounds__(kMapThreads, 1) topk_map_kernel(const float* scores,
                                                                   int64_t score_row_stride, Geom g, int top_k,
                                                                   int32_t* idx, int64_t idx_row_stride,
-                                                                  int32_t* n_sel) {
+                                                                  int32_t* n_sel, const uint32_t* hist) {
     extern __shared__ __align__(16) unsigned char map_raw[];
     MapShared& sh = *reinterpret_cast<MapShared*>(map_raw);
     pdl_trigger();
@@ -395,12 +396,31 @@ __global__ void __launch_bounds__(kMapThreads, 1) topk_map_kernel(const float* s
         sh.sel[i] = 0u;
         sh.eq[i] = 0u;
     }
-    for (int i = threadIdx.x; i < 2048; i += kMapThreads) sh.hist[i] = 0u;
+    // the fused path brings the row's histogram from the scorer (pass 1 is then skipped, unless the
+    // histogram is not exact: its total must be the row's key count)
+    uint32_t hpart = 0;
+    for (int i = threadIdx.x; i < 2048; i += kMapThreads) {
+        const uint32_t v = hist ? hist[r * 2048 + i] : 0u;
+        sh.hist[i] = v;
+        hpart += v;
+    }
     if (threadIdx.x == 0) {
         sh.cand_n = 0u;
         sh.overflow = 0;
+        sh.total = 0u;
     }
     __syncthreads();
+    if (hist) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) hpart += __shfl_xor_sync(0xffffffffu, hpart, o);
+        if (lane == 0 && hpart) atomicAdd(&sh.total, hpart);
+        __syncthreads();
+    }
+    const bool have_hist = hist && sh.total == (uint32_t)n;
+    if (hist && !have_hist) {
+        for (int i = threadIdx.x; i < 2048; i += kMapThreads) sh.hist[i] = 0u;
+        __syncthreads();
+    }
 
     const bool vec = (reinterpret_cast<uintptr_t>(s) & 15u) == 0;
     const int n4 = vec ? n >> 2 : 0;
@@ -415,7 +435,7 @@ __global__ void __launch_bounds__(kMapThreads, 1) topk_map_kernel(const float* s
         const uint32_t peers = __match_any_sync(0xffffffffu, bin);
         if (in && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[bin], (uint32_t)__popc(peers));
     };
-    for (int i0 = threadIdx.x; i0 < lim; i0 += step) {
+    for (int i0 = threadIdx.x; !have_hist && i0 < lim; i0 += step) {
         float4 v[kBatch];
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
@@ -431,7 +451,7 @@ __global__ void __launch_bounds__(kMapThreads, 1) topk_map_kernel(const float* s
             hcount(order_key(v[b].w), in);
         }
     }
-    for (int j0 = (n4 << 2); j0 < n; j0 += kMapThreads) {   // the unaligned rest, whole warps at a time
+    for (int j0 = (n4 << 2); !have_hist && j0 < n; j0 += kMapThreads) {   // the unaligned rest, whole warps
         const int j = j0 + threadIdx.x;
         const bool in = j < n;
         hcount(in ? order_key(s[j]) : 0u, in);
@@ -725,20 +745,18 @@ __global__ void __launch_bounds__(kMcThreads) topk_mc_filter_kernel(const float*
     mc_filter_range(scores + r * score_row_stride, c0, min(n, c0 + kMcChunk), L.bound[r], L, r, buf, nbuf, base);
 }
 
-// Fused path: the scorer left an exact histogram of each row's order keys by their top 11 bits.
-// The bin b* holding the K-th largest key follows from it directly: every key in a higher bin is
-// selected, and only the keys of b* remain to be ranked, so the filter keeps the keys with bin
-// >= b* (exactly above + hist[b*] of them) and the finish kernel resolves b*.  A histogram whose
-// total is not the row's key count (its launch could not count, see the scorer) sets the bound to
-// 0: every key becomes a candidate, the list overflows, and the finish takes the general path.
+// Fused path: the scorer counted each row's order keys by their top 11 bits, and the bound kernel
+// derived from that exact histogram the bin b* holding the K-th largest key, with the count above
+// it (L.bound[r] = b* << 21 | above).  Every key in a higher bin is selected and only the keys of b*
+// remain to be ranked, so the filter keeps the keys with bin >= b* (above + hist[b*] of them) and
+// the finish kernel resolves b*.  A bound of ~0 (the histogram was not exact: its launch could not
+// count, see the scorer) makes every key a candidate; the list overflows and the finish takes the
+// general path.
 __global__ void __launch_bounds__(kMcThreads) topk_hist_filter_kernel(const float* scores,
                                                                       int64_t score_row_stride, Geom g, int top_k,
-                                                                      McLayout L, const uint32_t* hist,
-                                                                      int chunk) {
+                                                                      McLayout L, int chunk) {
     __shared__ uint64_t buf[kMcLocal];
     __shared__ uint32_t nbuf, base;
-    __shared__ uint32_t scratch[kMcThreads / 32];
-    __shared__ uint32_t sb[3];
     pdl_trigger();
     pdl_wait();
     const int64_t r = blockIdx.y;
@@ -746,28 +764,69 @@ __global__ void __launch_bounds__(kMcThreads) topk_hist_filter_kernel(const floa
     const int K = min(top_k, n);
     const int c0 = blockIdx.x * chunk;
     if (K == n || c0 >= n) return;
-    const uint32_t* h = hist + r * 2048;
-    if (threadIdx.x == 0) {
-        sb[0] = 0u;
-        sb[2] = 0u;
+    const uint32_t b = L.bound[r];
+    const uint32_t lo = b == 0xffffffffu ? 0u : (b & 0xffe00000u);
+    const float* s = scores + r * score_row_stride;
+    const int c1 = min(n, c0 + chunk);
+    if (((reinterpret_cast<uintptr_t>(s) | (uint32_t)c0) & 15u) != 0) {
+        mc_filter_range(s, c0, c1, lo, L, r, buf, nbuf, base);
+        return;
+    }
+    // 16-byte loads: thread t takes the float4s t, t + 256, ... of the chunk, all issued at once
+    if (threadIdx.x == 0) nbuf = 0u;
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    uint32_t* cnt = L.cnt + r;
+    uint64_t* cand = L.cand + r * (int64_t)kMcCandCap;
+    constexpr int kV = 4;                     // float4s per thread per pass
+    for (int j0 = c0; j0 < c1; j0 += kMcThreads * 4 * kV) {
+        float4 v[kV];
+#pragma unroll
+        for (int b = 0; b < kV; ++b) {
+            const int j = j0 + (b * kMcThreads + threadIdx.x) * 4;
+            v[b] = j + 3 < c1 ? *reinterpret_cast<const float4*>(s + j)
+                              : make_float4(j < c1 ? s[j] : 0.f, j + 1 < c1 ? s[j + 1] : 0.f,
+                                            j + 2 < c1 ? s[j + 2] : 0.f, 0.f);
+        }
+#pragma unroll
+        for (int b = 0; b < kV; ++b) {
+            const float e[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = j0 + (b * kMcThreads + threadIdx.x) * 4 + q;
+                const uint32_t key = order_key(e[q]);
+                const bool hit = j < c1 && key >= lo;
+                const uint32_t m = __ballot_sync(0xffffffffu, hit);
+                if (m) {
+                    uint32_t at = 0;
+                    if (lane == __ffs(m) - 1) at = atomicAdd(&nbuf, (uint32_t)__popc(m));
+                    at = __shfl_sync(0xffffffffu, at, __ffs(m) - 1) + __popc(m & ((1u << lane) - 1u));
+                    if (hit) {
+                        const uint64_t kp = ((uint64_t)key << 32) | (uint32_t)j;
+                        if (at < (uint32_t)kMcLocal) {
+                            buf[at] = kp;
+                        } else {
+                            const uint32_t slot = atomicAdd(cnt, 1u);
+                            if (slot < (uint32_t)kMcCandCap) cand[slot] = kp;
+                        }
+                    }
+                }
+            }
+        }
     }
     __syncthreads();
-    uint32_t part = 0;
-    for (int i = threadIdx.x; i < 2048; i += kMcThreads) part += h[i];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-    if ((threadIdx.x & 31) == 0) atomicAdd(&sb[2], part);
-    mc_find_bin(h, (uint32_t)K, &sb[0], &sb[1], scratch);
-    const uint32_t lo = sb[2] == (uint32_t)n ? sb[0] << 21 : 0u;
-    if (blockIdx.x == 0 && threadIdx.x == 0) L.bound[r] = lo;
-    mc_filter_range(scores + r * score_row_stride, c0, min(n, c0 + chunk), lo, L, r, buf, nbuf, base);
+    const uint32_t nb = min(nbuf, (uint32_t)kMcLocal);
+    if (threadIdx.x == 0) base = nb ? atomicAdd(cnt, nb) : 0u;
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < nb; i += kMcThreads)
+        if (base + i < (uint32_t)kMcCandCap) cand[base + i] = buf[i];
 }
 
 __global__ void __launch_bounds__(kMapThreads, 1) topk_mc_finish_kernel(const float* scores,
                                                                        int64_t score_row_stride, Geom g, int top_k,
                                                                        McLayout L, int32_t* idx,
                                                                        int64_t idx_row_stride,
-                                                                       int32_t* n_sel) {
+                                                                       int32_t* n_sel, int known_bin) {
     extern __shared__ __align__(16) unsigned char map_raw[];
     MapShared& sh = *reinterpret_cast<MapShared*>(map_raw);
     GenShared<kMapThreads>& gsh = *reinterpret_cast<GenShared<kMapThreads>*>(map_raw);
@@ -795,12 +854,23 @@ __global__ void __launch_bounds__(kMapThreads, 1) topk_mc_finish_kernel(const fl
         sh.cand_pos[i] = (int32_t)(uint32_t)kp;
     }
     __syncthreads();
-    // exact top K among the candidates: three radix rounds over the full keys
+    // exact top K among the candidates: three radix rounds over the full keys; on the fused path
+    // the first round's bin and the count above it are known from the row's histogram
     uint32_t need = (uint32_t)K, prefix = 0u, mask = 0u;
     const int shifts[3] = {21, 10, 0};
     const int bitsv[3] = {11, 11, 10};
+    int round0 = 0;
+    if (known_bin) {
+        const uint32_t b = L.bound[r];
+        if (b != 0xffffffffu) {
+            prefix = b & 0xffe00000u;
+            mask = 0xffe00000u;
+            need -= b & 0x1fffffu;
+            round0 = 1;
+        }
+    }
 #pragma unroll 1
-    for (int round = 0; round < 3; ++round) {
+    for (int round = round0; round < 3; ++round) {
         map_cand_hist(sh, n_cand, prefix, mask, shifts[round], bitsv[round]);
         map_find_bin(1 << bitsv[round], need, sh);
         prefix |= sh.bin << shifts[round];
@@ -869,49 +939,116 @@ cudaError_t launch_topk(const float* scores, int64_t score_row_stride, const Geo
         const size_t sm = sizeof(MapShared);
         cudaFuncSetAttribute(topk_mc_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         return launch_pdl(topk_mc_finish_kernel, dim3((unsigned)n_rows), dim3(kMapThreads), sm, st, scores,
-                          score_row_stride, g, top_k, L, idx, idx_row_stride, n_sel);
+                          score_row_stride, g, top_k, L, idx, idx_row_stride, n_sel, 0);
     } else {
         const size_t sm = sizeof(MapShared);
         cudaFuncSetAttribute(topk_map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         return launch_pdl(topk_map_kernel, dim3((unsigned)n_rows), dim3(kMapThreads), sm, st, scores,
-                          score_row_stride, g, top_k, idx, idx_row_stride, n_sel);
+                          score_row_stride, g, top_k, idx, idx_row_stride, n_sel,
+                          static_cast<const uint32_t*>(nullptr));
     }
     return cudaGetLastError();
 }
 
+// the fused workspace: [rows][2048] histogram counts, then the candidate lists, bounds and
+// candidate counters of the multi-CTA path (mc_layout)
 size_t topk_fused_workspace_bytes(int64_t n_rows) {
     if (n_rows <= 0) return 0;
     return (size_t)n_rows * 2048 * sizeof(uint32_t) + mc_bytes(n_rows);
 }
 
-// the fused workspace: [rows][2048] histogram counts, then the candidate lists of the multi-CTA path
-uint32_t* topk_fused_hist(void* ws) { return static_cast<uint32_t*>(ws); }
-uint32_t* topk_fused_counters(void* ws, int64_t n_rows) {
-    return mc_layout(static_cast<char*>(ws) + (size_t)n_rows * 2048 * sizeof(uint32_t), n_rows).cnt;
+static McLayout fused_mc(void* ws, int64_t n_rows) {
+    return mc_layout(static_cast<char*>(ws) + (size_t)n_rows * 2048 * sizeof(uint32_t), n_rows);
 }
+
+FusedArrays topk_fused_arrays(void* ws, int64_t n_rows) {
+    FusedArrays a;
+    a.hist = static_cast<uint32_t*>(ws);
+    a.cnt = fused_mc(ws, n_rows).cnt;
+    return a;
+}
+
+// One CTA per row: from the row's exact histogram of order-key top-11-bit bins, the bin b* that
+// holds the K-th largest key and the count above it: L.bound[r] = b* << 21 | above (K <= 2^21).
+// A histogram whose total is not the row's key count (its launch could not count, see the scorer)
+// gives ~0.  256 threads, 8 bins each, walked from the top.
+__global__ void __launch_bounds__(kMcThreads) topk_hist_bound_kernel(const uint32_t* hist, Geom g, int top_k,
+                                                                     McLayout L) {
+    __shared__ uint32_t scratch[kMcThreads / 32];
+    __shared__ uint32_t sb[3];
+    pdl_trigger();
+    pdl_wait();
+    const int64_t r = blockIdx.x;
+    const int n = row_n_vis(g, r);
+    const int K = min(top_k, n);
+    if (K == n) return;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    // thread t owns bins [2047 - 8t - 7, 2047 - 8t]
+    const uint4* h4 = reinterpret_cast<const uint4*>(hist + r * 2048 + 2040 - 8 * threadIdx.x);
+    const uint4 lo4 = h4[0], hi4 = h4[1];
+    const uint32_t bins[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};   // from the top
+    uint32_t local = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) local += bins[i];
+    uint32_t x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[wid] = x;
+    if (threadIdx.x == 0) sb[0] = 0xffffffffu;
+    __syncthreads();
+    uint32_t before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kMcThreads / 32; ++w) {
+        before += w < wid ? scratch[w] : 0u;
+        total += scratch[w];
+    }
+    uint32_t c = before + x - local;
+    if (total == (uint32_t)n) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (c < (uint32_t)K && (uint32_t)K <= c + bins[i]) sb[0] = ((uint32_t)(2047 - 8 * threadIdx.x - i) << 21) | c;
+            c += bins[i];
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) L.bound[r] = sb[0];
+}
+
+// Rows up to kFusedMapMax keys: one CTA per row (topk_map_kernel seeded with the row's histogram:
+// one pass over the scores, which the scorer left in L2, marks the keys above the threshold bin
+// and collects that bin's keys, ranked in shared memory).  Longer rows: the bound kernel, then
+// the filter over all SMs, then the finish (one SM streaming a 131072-key row is slower than the
+// two extra launches).
+constexpr int kFusedMapMax = 16384;
 
 cudaError_t launch_topk_fused(const float* scores, int64_t score_row_stride, const Geom& g, int top_k, int32_t* idx,
                               int64_t idx_row_stride, int32_t* n_sel, void* ws, cudaStream_t st) {
     const int64_t n_rows = (int64_t)g.B * g.T;
     if (n_rows == 0) return cudaSuccess;
-    const uint32_t* hist = static_cast<const uint32_t*>(ws);
-    const McLayout L = mc_layout(static_cast<char*>(ws) + (size_t)n_rows * 2048 * sizeof(uint32_t), n_rows);
-    // filter chunks: about two CTAs per SM over the whole batch, 2048 to 32768 scores each
-    int sms = sm_count();
-    if (sms < 2) sms = 152;
-    int64_t chunk = ((int64_t)n_rows * g.max_n_kv + 2 * sms - 1) / (2 * sms);
-    chunk = (chunk + 2047) / 2048 * 2048;
-    chunk = chunk < 2048 ? 2048 : (chunk > 32768 ? 32768 : chunk);
-    const int64_t chunks = (g.max_n_kv + chunk - 1) / chunk;
-    if (chunks > 0) {
-        cudaError_t e = launch_pdl(topk_hist_filter_kernel, dim3((unsigned)chunks, (unsigned)n_rows), dim3(kMcThreads),
-                                   0, st, scores, score_row_stride, g, top_k, L, hist, (int)chunk);
-        if (e != cudaSuccess) return e;
-    }
     const size_t sm = sizeof(MapShared);
+    if (g.max_n_kv <= kFusedMapMax) {
+        cudaFuncSetAttribute(topk_map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        return launch_pdl(topk_map_kernel, dim3((unsigned)n_rows), dim3(kMapThreads), sm, st, scores,
+                          score_row_stride, g, top_k, idx, idx_row_stride, n_sel, static_cast<const uint32_t*>(ws));
+    }
+    const McLayout L = fused_mc(ws, n_rows);
+    cudaError_t e = launch_pdl(topk_hist_bound_kernel, dim3((unsigned)n_rows), dim3(kMcThreads), 0, st,
+                               static_cast<const uint32_t*>(ws), g, top_k, L);
+    if (e != cudaSuccess) return e;
+    // filter chunks of 8192 scores (two passes of four 16-byte loads per thread), longer when a
+    // batch would need more than 2048 CTAs
+    int64_t chunk = 8192;
+    while ((g.max_n_kv + chunk - 1) / chunk * n_rows > 2048 && chunk < (1 << 20)) chunk *= 2;
+    const int64_t chunks = (g.max_n_kv + chunk - 1) / chunk;
+    e = launch_pdl(topk_hist_filter_kernel, dim3((unsigned)chunks, (unsigned)n_rows), dim3(kMcThreads), 0, st,
+                   scores, score_row_stride, g, top_k, L, (int)chunk);
+    if (e != cudaSuccess) return e;
     cudaFuncSetAttribute(topk_mc_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     return launch_pdl(topk_mc_finish_kernel, dim3((unsigned)n_rows), dim3(kMapThreads), sm, st, scores,
-                      score_row_stride, g, top_k, L, idx, idx_row_stride, n_sel);
+                      score_row_stride, g, top_k, L, idx, idx_row_stride, n_sel, 1);
 }
 
 size_t topk_workspace_bytes(int64_t n_rows, int top_k) {

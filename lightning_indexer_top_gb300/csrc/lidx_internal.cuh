@@ -141,13 +141,12 @@ cudaError_t launch_quantize_rows(const void* x, int x_dtype, int64_t n_rows, int
 
 // tensor-core scorer for H = 64, d = 128, 16-bit keys; returns cudaErrorNotSupported
 // when the shape is not one it handles (the caller then uses the generic scorer)
-// hist (decode rows only, T = 1): also count each row's scores into hist[row][2048] by the top
-// 11 bits of their order key; the launch zeroes hist and zero2[0 .. n_zero2) first
+// hist (decode rows only, T = 1, at most 1024 rows): also count each row's scores into
+// hist[row][2048] by the top 11 bits of their order key; the launch zeroes hist and cnt[rows]
 cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, int d,
                             const void* k, int k_dtype, int64_t k_row_stride, int64_t k_rows,
                             const Geom& g, int block_size, float* scores, int64_t score_row_stride,
-                            cudaStream_t st, uint32_t* hist = nullptr, uint32_t* zero2 = nullptr,
-                            int n_zero2 = 0);
+                            cudaStream_t st, uint32_t* hist = nullptr, uint32_t* cnt = nullptr);
 
 // tensor-core decode scorer over int8 keys with per-row scales (H = 64, d = 128,
 // T = 1, 16-bit q); k_scale NULL: each row's f32 scale sits in its bytes 128..131
@@ -171,8 +170,12 @@ size_t topk_workspace_bytes(int64_t n_rows, int top_k);
 // fused score + top-k: the scorer counts each row's scores into the workspace's histograms (and
 // zeroes the select's counters); the select reads them (filter + finish kernels)
 size_t topk_fused_workspace_bytes(int64_t n_rows);
-uint32_t* topk_fused_hist(void* ws);
-uint32_t* topk_fused_counters(void* ws, int64_t n_rows);
+// the fused workspace's arrays the scorer writes: histograms, candidate counters
+struct FusedArrays {
+    uint32_t* hist;
+    uint32_t* cnt;
+};
+FusedArrays topk_fused_arrays(void* ws, int64_t n_rows);
 cudaError_t launch_topk_fused(const float* scores, int64_t score_row_stride, const Geom& g, int top_k, int32_t* idx,
                               int64_t idx_row_stride, int32_t* n_sel, void* ws, cudaStream_t st);
 

@@ -114,7 +114,8 @@ class SparseAttentionStep:
         """Kernels one run() enqueues (library launches only)."""
         n = 3 + (1 if self.attn_ws is not None else 0)   # score, select, attend (+ split combine)
         if self.fused:
-            n += 1                              # fused select: filter, finish
+            # fused select: one kernel for rows up to 16384 keys, else bound, filter, finish
+            n += 0 if self.wl.max_n_kv <= 16384 else 2
         elif self.topk_ws is not None:
             n += 2                              # multi-CTA select: bound, filter, finish
         if self.q_rot is not None:

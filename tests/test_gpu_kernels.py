@@ -165,6 +165,8 @@ def _fused_case(name):
         n_kv = [65536, 3000, 2048, 2049, 0, 1, 40000, 131072]
     elif name == "short_rows":
         n_kv = [8192] * 8
+    elif name == "short_ragged":
+        n_kv = [16384, 5000, 2048, 2049, 0, 1, 9000, 12000]
     else:   # "ties": every key row repeated 4 times, so each score appears 4 times (ties across the cut)
         n_kv = [20000, 65536, 4096]
     B, n = len(n_kv), max(n_kv)
@@ -176,7 +178,7 @@ def _fused_case(name):
     return q, w, k, n_kv, 2048
 
 
-@pytest.mark.parametrize("name", ["ragged", "short_rows", "ties"])
+@pytest.mark.parametrize("name", ["ragged", "short_rows", "short_ragged", "ties"])
 def test_fused_score_topk_equals_score_then_topk(name):
     # the histogram-driven select gives exactly what idx_score + idx_topk give, and what the
     # oracle's stable selection gives on the same f32 scores
