@@ -100,7 +100,7 @@ constexpr int kConvStages = LIDX_Q8_CONV_STAGES;     // int8 keys: widened tiles
 constexpr int kRawPitchInline = kD + 16;             // int8 rows with their scale inline: 128 codes + f32 + pad
 constexpr int kRawTileBytes = kTileKeys * kRawPitchInline;   // 18 KB stage (16 KB used without inline scales)
 constexpr int kSRing = 8;                            // int8 keys, inline scales: tiles of scales in flight
-constexpr int kChunkTiles = LIDX_SCORE_CHUNK;        // key tiles (32 KB each) per chunk
+constexpr int kChunkTiles = LIDX_SCORE_CHUNK;        // key tiles (32 KB each) per chunk, at most
 constexpr int kRing = 4;                             // chunk descriptors in flight
 #ifndef LIDX_SCORE_QBUFS
 #define LIDX_SCORE_QBUFS 3
@@ -151,8 +151,8 @@ template <typename T> constexpr bool kIsBF16 = false;
 template <> constexpr bool kIsBF16<__nv_bfloat16> = true;
 
 __device__ __forceinline__ int row_tiles(int n_keys) { return (n_keys + kTileKeys - 1) / kTileKeys; }
-__device__ __forceinline__ int row_chunks(int n_keys) {
-    return (row_tiles(n_keys) + kChunkTiles - 1) / kChunkTiles;
+__device__ __forceinline__ int row_chunks(int n_keys, int ct) {
+    return (row_tiles(n_keys) + ct - 1) / ct;
 }
 
 // one query row's q [64 heads x 128] -> key dtype TK in the MMA's B layout
@@ -202,7 +202,7 @@ __device__ __forceinline__ void stage_q_row(const TQ* __restrict__ qrow, uint8_t
 // chunk number `ch` -> (row, tiles); prefix mode: pre[i] = chunks of the rows
 // before row i, nvis[i] = visible keys of row i (both in shared memory)
 __device__ __forceinline__ Chunk chunk_of(const Geom& g, const int* pre, const int* nvis, int64_t n_rows,
-                                          bool prefix, int ch, int n_chunks) {
+                                          bool prefix, int ch, int n_chunks, int ct) {
     Chunk d;
     d.row = -1;
     d.t0 = d.t1 = 0;
@@ -216,8 +216,8 @@ __device__ __forceinline__ Chunk chunk_of(const Geom& g, const int* pre, const i
         }
         d.row = lo;
         const int nt = row_tiles(nvis[lo]);
-        d.t0 = (ch - pre[lo]) * kChunkTiles;
-        d.t1 = min(nt, d.t0 + kChunkTiles);
+        d.t0 = (ch - pre[lo]) * ct;
+        d.t1 = min(nt, d.t0 + ct);
     } else {
         d.row = ch;
         d.t0 = 0;
@@ -292,7 +292,7 @@ template <typename TK, bool kQ8>
 __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decode_kernel(
     const __grid_constant__ CUtensorMap kmap, const void* __restrict__ q, int q_dtype,
     const float* __restrict__ w, Geom g, float* __restrict__ scores, int64_t score_row_stride, int sched_slot,
-    const float* __restrict__ k_scale, int64_t k_rows, HistOut ho) {
+    const float* __restrict__ k_scale, int64_t k_rows, HistOut ho, int chunk_tiles) {
     uint32_t* hist = ho.hist;
     constexpr int kNT = kQ8 ? kThreadsQ8 : kThreads;
     constexpr int kTmaStages = kQ8 ? kRawStages : kStages;   // the producer's ring
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
         for (int64_t r = threadIdx.x; r < n_rows; r += kNT) {
             const int nv = row_n_vis(g, r);
             nvis[r] = nv;
-            pre[r + 1] = row_chunks(nv);
+            pre[r + 1] = row_chunks(nv, chunk_tiles);
         }
         __syncthreads();
         if (warp == 0) {
@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                     abort_cta(c, g);
                     go = 0;
                 } else {
-                    const Chunk d = chunk_of(g, pre, nvis, n_rows, prefix, ch, n_chunks);
+                    const Chunk d = chunk_of(g, pre, nvis, n_rows, prefix, ch, n_chunks, chunk_tiles);
                     c.chunk[slot] = d;
                     mbar_arrive(&c.cfull[slot]);
                     if (d.row < 0)
@@ -1212,11 +1212,17 @@ cudaError_t launch_score_tc_prefill(const void* q, int q_dtype, const float* w, 
 }
 
 namespace {
-// grid of the decode scorer and the counter slot of this launch; false when the
-// chunks would not number in 32 bits
-bool decode_launch_shape(const Geom& g, int& grid, int& slot) {
+// grid of the decode scorer, the key tiles per chunk and the counter slot of this launch; false
+// when the chunks would not number in 32 bits.  Chunks are kChunkTiles tiles, or fewer (down to 2)
+// when a small batch would otherwise leave SMs idle: about four chunks per SM.
+bool decode_launch_shape(const Geom& g, int& grid, int& ct, int& slot) {
     const int64_t n_rows = (int64_t)g.B * g.T;
-    const int64_t chunks_per_row = ((g.max_n_kv + kTileKeys - 1) / kTileKeys + kChunkTiles - 1) / kChunkTiles;
+    const int64_t tiles_per_row = (g.max_n_kv + kTileKeys - 1) / kTileKeys;
+    ct = kChunkTiles;
+    if (n_rows <= kMaxPrefixRows) {
+        while (ct > 2 && n_rows * ((tiles_per_row + ct - 1) / ct) < 4 * (int64_t)sm_count()) ct >>= 1;
+    }
+    const int64_t chunks_per_row = (tiles_per_row + ct - 1) / ct;
     const int64_t max_chunks = n_rows <= kMaxPrefixRows ? n_rows * chunks_per_row : n_rows;
     if (max_chunks >= INT32_MAX - 2 * (int64_t)sm_count()) return false;
     grid = (int)(max_chunks < sm_count() ? max_chunks : sm_count());
@@ -1245,14 +1251,14 @@ cudaError_t launch_score_tc_q8(const void* q, int q_dtype, const float* w, const
     if (g.page_table && g.page_size % 64 != 0) return cudaErrorNotSupported;
     if (!make_key8_tmap(&map, k8, k_row_stride, k_rows, g.page_table ? 64 : kTileKeys, k_scale ? 128 : kRawPitchInline))
         return cudaErrorNotSupported;
-    int grid, slot;
-    if (!decode_launch_shape(g, grid, slot)) return cudaErrorNotSupported;
+    int grid, ct, slot;
+    if (!decode_launch_shape(g, grid, ct, slot)) return cudaErrorNotSupported;
     auto kern = score_tc_decode_kernel<__half, true>;
     constexpr size_t smem = smem_bytes<true>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kThreadsQ8), smem, st, map, q, q_dtype, w, g, scores, score_row_stride,
-                      slot, k_scale, k_rows, HistOut{nullptr, nullptr});
+                      slot, k_scale, k_rows, HistOut{nullptr, nullptr}, ct);
 }
 
 cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, int d, const void* k,
@@ -1277,14 +1283,14 @@ cudaError_t launch_score_tc(const void* q, int q_dtype, const float* w, int H, i
     const bool bf16 = k_dtype == IDX_BF16;
     if (g.page_table && g.page_size % 64 != 0) return cudaErrorNotSupported;
     if (!make_key_tmap(&map, k, bf16, k_row_stride, k_rows, g.page_table ? 64 : kTileKeys)) return cudaErrorNotSupported;
-    int grid, slot;
-    if (!decode_launch_shape(g, grid, slot)) return cudaErrorNotSupported;
+    int grid, ct, slot;
+    if (!decode_launch_shape(g, grid, ct, slot)) return cudaErrorNotSupported;
     auto kern = bf16 ? score_tc_decode_kernel<__nv_bfloat16, false> : score_tc_decode_kernel<__half, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemBytes, st, map, q, q_dtype, w, g, scores,
                       score_row_stride, slot, static_cast<const float*>(nullptr), k_rows,
-                      HistOut{hist, cnt});
+                      HistOut{hist, cnt}, ct);
 }
 
 }  // namespace lidx
