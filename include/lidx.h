@@ -47,7 +47,9 @@ typedef enum idx_status {
     IDX_ERR_UNSUPPORTED = 2,
     IDX_ERR_CUDA = 3,
     IDX_ERR_TIMEOUT = 4,      /* device status only: a bounded wait ran out */
-    IDX_ERR_DEVICE_BOUNDS = 5 /* device status only: an out-of-range index or row was skipped */
+    IDX_ERR_DEVICE_BOUNDS = 5, /* device status only: an out-of-range index or row was skipped */
+    IDX_ERR_INEXACT = 6        /* device status only: a query value overflowed the type the scorer
+                                  converts it to (bf16 q of magnitude >= 65520 against F16 keys) */
 } idx_status;
 
 typedef enum idx_dtype {
@@ -145,8 +147,15 @@ idx_status idx_hadamard(const void* x, void* y, idx_dtype dtype, int64_t n_rows,
  *   scores     f32, row r at scores + r*score_row_stride; entries j of
  *              visible keys are written, the rest of the row is untouched.
  *   workspace  may be NULL when idx_workspace_size(IDX_OP_SCORE, ...) is 0.
- * Supported: q_dtype, k_dtype in {F32, F16, BF16}, H <= 128, d <= 256 and
- * H*d <= 16384.  H = 64, d = 128 with F16/BF16 keys runs on the tensor cores.
+ * Supported: q_dtype, k_dtype in {F32, F16, BF16}, H <= 64, d <= 256 and
+ * H*d <= 16384.  H = 64, d = 128 with F16/BF16 keys runs on the tensor cores
+ * when q converts exactly to the key type: the same type, or bf16 q with F16
+ * keys (bf16's 8-bit significand fits f16's 11 bits).  A bf16 q element of
+ * magnitude >= 65520 does not fit f16's range: it is staged as +-inf and
+ * IDX_ERR_INEXACT is recorded in the device status; elements below f16's
+ * normal range (2^-14) keep their f16 rounding, an error of at most 2^-25
+ * each.  Every other combination (f32 q, f16 q with BF16 keys) runs on the
+ * CUDA cores in f32 with q as given.
  */
 idx_status idx_score(const void* q, idx_dtype q_dtype, const float* w, int32_t n_heads,
                      int32_t head_dim, const void* k, idx_dtype k_dtype, int64_t k_row_stride,
@@ -187,9 +196,9 @@ idx_status idx_quantize_rows(const void* x, idx_dtype x_dtype, int64_t n_rows, i
  *   other arguments as idx_score (block_size 0/1 only).
  * H = 64, d = 128 decode rows (T = 1) with f16 or bf16 q run on the tensor
  * cores: the int8 codes are widened exactly to f16 in shared memory, q is
- * converted to f16 (exact for bf16 q inside f16's normal range), and the
- * scale is applied per head before the ReLU.  Everything else runs on the
- * CUDA cores.
+ * converted to f16 (exact for bf16 q inside f16's normal range; beyond it
+ * IDX_ERR_INEXACT is recorded, as for idx_score), and the scale is applied
+ * per head before the ReLU.  Everything else runs on the CUDA cores.
  */
 idx_status idx_score_q8(const void* q, idx_dtype q_dtype, const float* w, int32_t n_heads, int32_t head_dim,
                         const int8_t* k8, int64_t k_row_stride, const float* k_scale, int64_t k_rows,

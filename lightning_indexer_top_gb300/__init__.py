@@ -28,7 +28,7 @@ __all__ = [
     "idx_device_status", "topk_capacity", "sparse_attn_decode_noalloc",
 ]
 
-IDX_OK, IDX_ERR_INVALID_ARG, IDX_ERR_UNSUPPORTED, IDX_ERR_CUDA, IDX_ERR_TIMEOUT, IDX_ERR_DEVICE_BOUNDS = range(6)
+IDX_OK, IDX_ERR_INVALID_ARG, IDX_ERR_UNSUPPORTED, IDX_ERR_CUDA, IDX_ERR_TIMEOUT, IDX_ERR_DEVICE_BOUNDS, IDX_ERR_INEXACT = range(7)
 IDX_F32, IDX_F16, IDX_BF16 = 0, 1, 2
 IDX_POS_CLEAN = 2**31 - 1   # stale_pos value: no edit
 IDX_OP_SCORE, IDX_OP_TOPK, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL, IDX_OP_SCORE_TOPK = 0, 1, 2, 3, 4

@@ -160,8 +160,12 @@ __device__ __forceinline__ int row_chunks(int n_keys, int ct) {
 // 16-byte loads and stores, the warp's 32 lanes over the 1024 chunks
 // (all loads of a batch are issued before the first conversion: two round
 // trips per row for 16-bit q, four for f32)
+// Returns true if a value overflowed the key type (a bf16 q element of magnitude >= 65520 staged
+// as f16 becomes +-inf); below f16's normal range values keep their f16 rounding (an error of at
+// most 2^-25 per element).
 template <typename TK, typename TQ>
-__device__ __forceinline__ void stage_q_row(const TQ* __restrict__ qrow, uint8_t* qdst, int lane) {
+__device__ __forceinline__ bool stage_q_row(const TQ* __restrict__ qrow, uint8_t* qdst, int lane) {
+    bool overflow = false;
     constexpr int kPerLane = kH * kD / 8 / 32;                   // 32 chunks of 8 elements
     constexpr int kBatch = sizeof(TQ) == 2 ? 16 : 8;
 #pragma unroll
@@ -187,7 +191,11 @@ __device__ __forceinline__ void stage_q_row(const TQ* __restrict__ qrow, uint8_t
             if constexpr (sizeof(TQ) == 2) {
                 const TQ* e = reinterpret_cast<const TQ*>(&raw[i]);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) vals[j] = from_f32<TK>(to_f32(e[j]));
+                for (int j = 0; j < 8; ++j) {
+                    const float x = to_f32(e[j]);
+                    vals[j] = from_f32<TK>(x);
+                    if constexpr (std::is_same<TK, __half>::value) overflow |= fabsf(x) >= 65520.f;
+                }
             } else {
                 const float* e = reinterpret_cast<const float*>(&raw[2 * i]);
 #pragma unroll
@@ -197,6 +205,7 @@ __device__ __forceinline__ void stage_q_row(const TQ* __restrict__ qrow, uint8_t
             *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(vals);
         }
     }
+    return overflow;
 }
 
 // chunk number `ch` -> (row, tiles); prefix mode: pre[i] = chunks of the rows
@@ -612,9 +621,11 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
             }
             uint8_t* qdst = qbuf + qb * kQBytes;
             const int64_t off = d.row * (int64_t)kH * kD;
-            if (q_dtype == IDX_F32) stage_q_row<TK>(static_cast<const float*>(q) + off, qdst, lane);
-            else if (q_dtype == IDX_BF16) stage_q_row<TK>(static_cast<const __nv_bfloat16*>(q) + off, qdst, lane);
-            else stage_q_row<TK>(static_cast<const __half*>(q) + off, qdst, lane);
+            bool ovf;
+            if (q_dtype == IDX_F32) ovf = stage_q_row<TK>(static_cast<const float*>(q) + off, qdst, lane);
+            else if (q_dtype == IDX_BF16) ovf = stage_q_row<TK>(static_cast<const __nv_bfloat16*>(q) + off, qdst, lane);
+            else ovf = stage_q_row<TK>(static_cast<const __half*>(q) + off, qdst, lane);
+            if (__any_sync(0xffffffffu, ovf) && lane == 0) flag(g.status, IDX_ERR_INEXACT);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&c.qfull[qb]);

@@ -452,6 +452,35 @@ def test_score_tensor_core_decode_matches_oracle(qt, kt):
         assert np.all(sh[b, n:] == 777.0)
 
 
+def test_score_q_beyond_f16_range_is_flagged_and_f32_q_stays_exact():
+    # bf16 q against F16 keys runs on the tensor cores with q staged as f16: exact inside f16's
+    # range; an element beyond it (here 1e5 -> 99840 in bf16) cannot be staged and is flagged
+    g = torch.Generator(device=DEV).manual_seed(77)
+    n = 4096
+    q = torch.randn(2, 64, 128, generator=g, device=DEV).to(torch.bfloat16)
+    w = torch.randn(2, 64, generator=g, device=DEV) / 8
+    k = torch.randn(2 * n, 128, generator=g, device=DEV).to(torch.float16)
+    batch = L.Batch(_i32([n, n]), 1, n, kv_seq_stride=n)
+    assert L.idx_device_status(reset=True) == 0
+    s = L.idx_score(q, w, k, batch)
+    torch.cuda.synchronize()
+    assert L.idx_device_status(reset=True) == 0
+    assert_scores_close(s[0].cpu().numpy(), O.indexer_scores(np64(q[0]), np64(w[0]), np64(k[:n])), "in range")
+    q[1, 3, 7] = 1e5
+    L.idx_score(q, w, k, batch, scores=s)
+    torch.cuda.synchronize()
+    assert L.idx_device_status(reset=True) == L.IDX_ERR_INEXACT
+    # f32 q of wide dynamic range (1e-8 .. 1e6 scales per head): the CUDA-core path keeps it in f32
+    scale = torch.logspace(-8, 6, 64, device=DEV)[None, :, None]
+    q32 = torch.randn(2, 64, 128, generator=g, device=DEV) * scale
+    s32 = L.idx_score(q32, w, k, batch)
+    torch.cuda.synchronize()
+    assert L.idx_device_status(reset=True) == 0
+    for r in range(2):
+        assert_scores_close(s32[r].cpu().numpy(), O.indexer_scores(np64(q32[r]), np64(w[r]), np64(k[r * n:(r + 1) * n])),
+                            f"f32 row {r}")
+
+
 def test_score_tensor_core_one_short_row_many_idle_ctas():
     # far fewer tiles than SMs: most CTAs get an empty share
     g = torch.Generator(device=DEV).manual_seed(72)
