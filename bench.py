@@ -48,6 +48,7 @@ WORKLOAD = "decode_mla_64x131072"
 WORKLOADS = {
     "decode_mla_64x131072": (("headline",), {}, {}),
     "decode_mla_8x131072": (("headline",), {"batch_override": 8}, {}),
+    "decode_mla_16x131072": (("headline",), {"batch_override": 16}, {}),
     "decode_mla_8x8192": ((2,), {}, {}),
     "decode_mla_64x8192": (("headline",), {"n_kv_override": 8192}, {}),
     "long_decode_mla_ragged": ((5,), {}, {}),
@@ -584,7 +585,9 @@ def main():
                    "indexer": "%d heads x %d, %s cache%s" % (
                        wl.H, wl.d, "int8 + f32 row scale" if wl.k8 is not None else
                        str(wl.k_idx.dtype).replace("torch.", ""), ", Hadamard" if wl.hadamard else ""),
-                   "attention": "MLA 128 heads, 576/512 bf16",
+                   "attention": ("MLA %d heads, %d/%d bf16" % (wl.q_attn.shape[1], wl.k_attn.shape[-1], wl.dv)
+                                 if wl.v_attn is None else "GQA %d q / %d kv heads, %d/%d bf16" % (
+                                     wl.q_attn.shape[1], wl.k_attn.shape[1], wl.k_attn.shape[-1], wl.dv)),
                    "l2": "inputs larger than L2 (key cache %.2f GB, latent %.2f GB), no flush"
                          % (wl.k_idx.numel() * 2 / 1e9, wl.k_attn.numel() * 2 / 1e9)},
         "timing": {"windows": len(windows), "steps_per_window": args.steps,

@@ -33,56 +33,34 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kKeys = 32;
 
-// eight consecutive elements (16-byte aligned source) as they are stored, and widened to f32
-template <typename T>
-struct Raw8 {
-    uint4 u[sizeof(T) / 2];
-};
-
-template <typename T>
-__device__ __forceinline__ Raw8<T> load_raw8(const T* p) {
-    Raw8<T> r;
-#pragma unroll
-    for (int i = 0; i < (int)(sizeof(T) / 2); ++i) r.u[i] = reinterpret_cast<const uint4*>(p)[i];
-    return r;
-}
-
-template <typename T>
-__device__ __forceinline__ void store_f32(const Raw8<T>& r, float* dst) {
-    const T* e = reinterpret_cast<const T*>(r.u);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) dst[i] = to_f32(e[i]);
-}
-
 // The K rows (dk elements from column kc0 of each row) and, with v, the V rows (dv elements from
-// column vc0) of one tile of kKeys keys, widened into shared memory: key `key` at ks[key * (dk + 1)]
-// and vs[key * dv].  Invalid keys (rows_s < 0) give zeros.  With `vec` every 16-byte piece of a
-// tile is loaded before any is stored, up to kBatch per thread, so a tile costs one memory round
-// trip rather than one per piece.
+// column vc0) of one tile of kKeys keys, copied as stored into shared memory: key `key` at
+// ks[key * kp] and vs[key * vp].  Invalid keys (rows_s < 0) give zeros.  With `vec` each thread
+// moves 16-byte pieces, all of a tile's loads issued before any store (one memory round trip per
+// tile); otherwise element by element.
 template <typename T>
-__device__ __forceinline__ void gather_kv_tile(float* ks, float* vs, const T* __restrict__ k, const T* __restrict__ v,
+__device__ __forceinline__ void gather_kv_tile(T* ks, T* vs, const T* __restrict__ k, const T* __restrict__ v,
                                                int64_t k_stride, int64_t v_stride, int64_t kc0, int64_t vc0, int dk,
-                                               int dv, const int64_t* rows_s, bool vec) {
+                                               int dv, int kp, int vp, const int64_t* rows_s, bool vec) {
     if (vec) {
+        constexpr int E = 16 / sizeof(T);      // elements per 16-byte piece
         constexpr int kBatch = 8;
-        const int wk = dk >> 3, wv = v ? dv >> 3 : 0;
+        const int wk = dk / E, wv = v ? dv / E : 0;
         const int nk = kKeys * wk, total = nk + kKeys * wv;
         for (int e0 = threadIdx.x; e0 < total; e0 += kThreads * kBatch) {
-            Raw8<T> r[kBatch];
+            uint4 r[kBatch];
 #pragma unroll
             for (int b = 0; b < kBatch; ++b) {
                 const int e = e0 + b * kThreads;
+                r[b] = make_uint4(0u, 0u, 0u, 0u);
                 if (e < total) {
                     const bool isk = e < nk;
                     const int ee = isk ? e : e - nk, w = isk ? wk : wv;
-                    const int key = ee / w, c = (ee % w) * 8;
+                    const int key = ee / w, c = (ee % w) * E;
                     const int64_t row = rows_s[key];
-                    if (row >= 0) {
-                        r[b] = isk ? load_raw8(k + row * k_stride + kc0 + c) : load_raw8(v + row * v_stride + vc0 + c);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < (int)(sizeof(T) / 2); ++i) r[b].u[i] = make_uint4(0u, 0u, 0u, 0u);
-                    }
+                    if (row >= 0)
+                        r[b] = isk ? *reinterpret_cast<const uint4*>(k + row * k_stride + kc0 + c)
+                                   : *reinterpret_cast<const uint4*>(v + row * v_stride + vc0 + c);
                 }
             }
 #pragma unroll
@@ -91,8 +69,8 @@ __device__ __forceinline__ void gather_kv_tile(float* ks, float* vs, const T* __
                 if (e < total) {
                     const bool isk = e < nk;
                     const int ee = isk ? e : e - nk, w = isk ? wk : wv;
-                    const int key = ee / w, c = (ee % w) * 8;
-                    store_f32(r[b], isk ? ks + key * (dk + 1) + c : vs + key * dv + c);
+                    const int key = ee / w, c = (ee % w) * E;
+                    *reinterpret_cast<uint4*>(isk ? ks + key * kp + c : vs + key * vp + c) = r[b];
                 }
             }
         }
@@ -100,31 +78,67 @@ __device__ __forceinline__ void gather_kv_tile(float* ks, float* vs, const T* __
         for (int e = threadIdx.x; e < kKeys * dk; e += kThreads) {
             const int key = e / dk, c = e % dk;
             const int64_t row = rows_s[key];
-            ks[key * (dk + 1) + c] = row >= 0 ? to_f32(k[row * k_stride + kc0 + c]) : 0.f;
+            ks[key * kp + c] = row >= 0 ? k[row * k_stride + kc0 + c] : from_f32<T>(0.f);
         }
         if (v) {
             for (int e = threadIdx.x; e < kKeys * dv; e += kThreads) {
                 const int key = e / dv, c = e % dv;
                 const int64_t row = rows_s[key];
-                vs[key * dv + c] = row >= 0 ? to_f32(v[row * v_stride + vc0 + c]) : 0.f;
+                vs[key * vp + c] = row >= 0 ? v[row * v_stride + vc0 + c] : from_f32<T>(0.f);
             }
         }
     }
 }
 
-template <typename T, int HPW, int DVL>
-__global__ void __launch_bounds__(kThreads) attn_generic_kernel(
+// eight consecutive shared-memory elements (16-byte aligned) widened to f32
+template <typename T>
+__device__ __forceinline__ void lds8(const T* p, float (&f)[8]) {
+    if constexpr (sizeof(T) == 4) {
+        const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    } else {
+        const uint4 u = *reinterpret_cast<const uint4*>(p);
+        const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = to_f32(e[i]);
+    }
+}
+
+// two consecutive shared-memory elements (aligned to two elements) widened to f32
+template <typename T>
+__device__ __forceinline__ void lds2(const T* p, float& x, float& y) {
+    if constexpr (sizeof(T) == 4) {
+        const float2 a = *reinterpret_cast<const float2*>(p);
+        x = a.x;
+        y = a.y;
+    } else {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+        const T* e = reinterpret_cast<const T*>(&u);
+        x = to_f32(e[0]);
+        y = to_f32(e[1]);
+    }
+}
+
+template <typename T, int HPW, int DV2>
+__global__ void __launch_bounds__(kThreads, 4) attn_generic_kernel(
     const T* __restrict__ q, int Hq, int Hkv, int dk, int dv, const T* __restrict__ k,
     const T* __restrict__ v, int64_t kv_row_stride, int64_t v_row_stride, int64_t kv_rows, Geom g,
-    const int32_t* __restrict__ idx, int64_t idx_row_stride, const int32_t* __restrict__ n_sel,
+    const int32_t* idx, int64_t idx_row_stride, const int32_t* n_sel,
     float scale, void* __restrict__ out, int out_dtype, int n_chunks, bool vec, int splits, int kps,
     float* __restrict__ part_o, float* __restrict__ part_ml) {
     constexpr int HC = 4 * HPW;
     extern __shared__ __align__(16) unsigned char sm_raw[];
-    int64_t* rows_s = reinterpret_cast<int64_t*>(sm_raw);            // [kKeys] cache rows, -1 invalid
-    float* qs = reinterpret_cast<float*>(sm_raw + kKeys * sizeof(int64_t));  // [HC][dk], pre-scaled
-    float* ks = qs + HC * dk;                    // [kKeys][dk+1]
-    float* vs = ks + kKeys * (dk + 1);           // [kKeys][dv] (GQA only)
+    // q as f32, rows of qp = dk rounded up to 8 (zero padding); K and V tiles as stored, K rows of
+    // kp = qp + 16 bytes (16-byte aligned; the extra step spreads the 32 lanes' row reads over the
+    // bank groups), V rows of vp elements (16-byte aligned)
+    const int qp = (dk + 7) & ~7;
+    const int kp = qp + 16 / (int)sizeof(T);
+    const int vp = (dv + 15 / (int)sizeof(T)) / (16 / (int)sizeof(T)) * (16 / (int)sizeof(T));
+    int64_t* rows_s = reinterpret_cast<int64_t*>(sm_raw);                     // [kKeys] cache rows, -1 invalid
+    float* qs = reinterpret_cast<float*>(sm_raw + kKeys * sizeof(int64_t));   // [HC][qp], pre-scaled
+    T* ks = reinterpret_cast<T*>(qs + HC * qp);                               // [kKeys][kp]
+    T* vs = ks + kKeys * kp;                                                  // [kKeys][vp] (GQA only)
 
     const int64_t r = blockIdx.x;
     const int gkv = blockIdx.y / n_chunks;       // kv head
@@ -141,12 +155,14 @@ __global__ void __launch_bounds__(kThreads) attn_generic_kernel(
         ns = ns < 0 ? 0 : (int)idx_row_stride;
     }
 
-    for (int i = threadIdx.x; i < HC * dk; i += kThreads) {
-        const int hl = i / dk, c = i % dk;
-        qs[i] = hl < n_heads ? scale * to_f32(q[(r * Hq + h_base + hl) * (int64_t)dk + c]) : 0.f;
+    for (int i = threadIdx.x; i < HC * qp; i += kThreads) {
+        const int hl = i / qp, c = i % qp;
+        qs[i] = (hl < n_heads && c < dk) ? scale * to_f32(q[(r * Hq + h_base + hl) * (int64_t)dk + c]) : 0.f;
     }
+    // the K padding columns [dk, kp) are read (against zero q) and must hold finite values
+    for (int i = threadIdx.x; i < kKeys * kp; i += kThreads) ks[i] = from_f32<T>(0.f);
 
-    float o[HPW][DVL];
+    float o[HPW][2 * DV2];
     float m_run[HPW], l_run[HPW];
     bool has_m[HPW];
 #pragma unroll
@@ -155,13 +171,13 @@ __global__ void __launch_bounds__(kThreads) attn_generic_kernel(
         l_run[hh] = 0.f;
         has_m[hh] = false;
 #pragma unroll
-        for (int i = 0; i < DVL; ++i) o[hh][i] = 0.f;
+        for (int i = 0; i < 2 * DV2; ++i) o[hh][i] = 0.f;
     }
 
     const int split = blockIdx.z;
     const int t_end = min(ns, (split + 1) * kps);
     for (int t0 = split * kps; t0 < t_end; t0 += kKeys) {
-        __syncthreads();  // previous tile fully consumed (and qs written, first time)
+        __syncthreads();  // previous tile fully consumed (and qs / padding written, first time)
         if (threadIdx.x < kKeys) {
             const int j = t0 + threadIdx.x;
             int64_t row = -1;
@@ -177,45 +193,84 @@ __global__ void __launch_bounds__(kThreads) attn_generic_kernel(
             rows_s[threadIdx.x] = row;
         }
         __syncthreads();
-        gather_kv_tile(ks, vs, k, v, kv_row_stride, v_row_stride, (int64_t)gkv * dk, (int64_t)gkv * dv, dk, dv,
-                       rows_s, vec);
+        gather_kv_tile(ks, vs, k, v, kv_row_stride, v_row_stride, (int64_t)gkv * dk, (int64_t)gkv * dv, dk, dv, kp,
+                       vp, rows_s, vec);
         __syncthreads();
 
         const bool valid = rows_s[lane] >= 0;
-        const float* vrow_base = v ? vs : ks;
-        const int vstride = v ? dv : dk + 1;
+        if (__ballot_sync(0xffffffffu, valid) == 0u) continue;  // whole tile invalid (block-uniform)
+        const T* vrow_base = v ? vs : ks;
+        const int vstride = v ? vp : kp;
+        // logits of this lane's key for the warp's heads: one 16-byte read of the key row per 8
+        // dimensions, shared by the heads
+        float logit[HPW];
+#pragma unroll
+        for (int hh = 0; hh < HPW; ++hh) logit[hh] = 0.f;
+        const T* kr = ks + lane * kp;
+        for (int c = 0; c < qp; c += 8) {
+            float kv8[8];
+            lds8(kr + c, kv8);
+#pragma unroll
+            for (int hh = 0; hh < HPW; ++hh) {
+                const int hl = warp + 4 * hh;
+                if (hl >= n_heads) continue;   // warp-uniform
+                const float4 qa = *reinterpret_cast<const float4*>(qs + hl * qp + c);
+                const float4 qb = *reinterpret_cast<const float4*>(qs + hl * qp + c + 4);
+                float a = logit[hh];
+                a = fmaf(qa.x, kv8[0], a);
+                a = fmaf(qa.y, kv8[1], a);
+                a = fmaf(qa.z, kv8[2], a);
+                a = fmaf(qa.w, kv8[3], a);
+                a = fmaf(qb.x, kv8[4], a);
+                a = fmaf(qb.y, kv8[5], a);
+                a = fmaf(qb.z, kv8[6], a);
+                a = fmaf(qb.w, kv8[7], a);
+                logit[hh] = a;
+            }
+        }
+        float p[HPW];
 #pragma unroll
         for (int hh = 0; hh < HPW; ++hh) {
             const int hl = warp + 4 * hh;
+            p[hh] = 0.f;
             if (hl >= n_heads) continue;  // warp-uniform
-            const float* qh = qs + hl * dk;
-            const float* kr = ks + lane * (dk + 1);
-            float logit = 0.f;
-            for (int c = 0; c < dk; ++c) logit = fmaf(qh[c], kr[c], logit);
-            float tmax = valid ? logit : -FLT_MAX;
+            float tmax = valid ? logit[hh] : -FLT_MAX;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-            if (__ballot_sync(0xffffffffu, valid) == 0u) continue;  // whole tile invalid
             const float m_new = has_m[hh] ? fmaxf(m_run[hh], tmax) : tmax;
             const float corr = has_m[hh] ? expf(m_run[hh] - m_new) : 0.f;
-            const float p = valid ? expf(logit - m_new) : 0.f;
-            float psum = p;
+            p[hh] = valid ? expf(logit[hh] - m_new) : 0.f;
+            float psum = p[hh];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
             l_run[hh] = l_run[hh] * corr + psum;
 #pragma unroll
-            for (int i = 0; i < DVL; ++i) o[hh][i] *= corr;
-            for (int key = 0; key < kKeys; ++key) {
-                const float pk = __shfl_sync(0xffffffffu, p, key);
-                const float* vr = vrow_base + key * vstride;
-#pragma unroll
-                for (int i = 0; i < DVL; ++i) {
-                    const int c = lane + 32 * i;
-                    if (c < dv) o[hh][i] = fmaf(pk, vr[c], o[hh][i]);
-                }
-            }
+            for (int i = 0; i < 2 * DV2; ++i) o[hh][i] *= corr;
             m_run[hh] = m_new;
             has_m[hh] = true;
+        }
+        // o += p V: lane owns the column pairs 2*lane + 64*i; each pair is read once for all heads
+        for (int key = 0; key < kKeys; ++key) {
+            float pk[HPW];
+#pragma unroll
+            for (int hh = 0; hh < HPW; ++hh) pk[hh] = __shfl_sync(0xffffffffu, p[hh], key);
+            const T* vr = vrow_base + key * vstride;
+#pragma unroll
+            for (int i = 0; i < DV2; ++i) {
+                const int c = 2 * lane + 64 * i;
+                if (c >= dv) continue;
+                float x, y = 0.f;
+                if (c + 1 < dv) {
+                    lds2(vr + c, x, y);
+                } else {
+                    x = to_f32(vr[c]);
+                }
+#pragma unroll
+                for (int hh = 0; hh < HPW; ++hh) {
+                    o[hh][2 * i] = fmaf(pk[hh], x, o[hh][2 * i]);
+                    o[hh][2 * i + 1] = fmaf(pk[hh], y, o[hh][2 * i + 1]);
+                }
+            }
         }
     }
 
@@ -227,9 +282,10 @@ __global__ void __launch_bounds__(kThreads) attn_generic_kernel(
             if (hl >= n_heads) continue;
             const int64_t u = (r * splits + split) * (int64_t)Hq + h_base + hl;
 #pragma unroll
-            for (int i = 0; i < DVL; ++i) {
-                const int c = lane + 32 * i;
-                if (c < dv) part_o[u * dv + c] = o[hh][i];
+            for (int i = 0; i < DV2; ++i) {
+                const int c = 2 * lane + 64 * i;
+                if (c < dv) part_o[u * dv + c] = o[hh][2 * i];
+                if (c + 1 < dv) part_o[u * dv + c + 1] = o[hh][2 * i + 1];
             }
             if (lane == 0) {
                 part_ml[2 * u] = has_m[hh] ? m_run[hh] : 0.f;
@@ -245,14 +301,17 @@ __global__ void __launch_bounds__(kThreads) attn_generic_kernel(
         const float inv = l_run[hh] > 0.f ? 1.f / l_run[hh] : 0.f;
         const int64_t base = (r * Hq + h_base + hl) * (int64_t)dv;
 #pragma unroll
-        for (int i = 0; i < DVL; ++i) {
-            const int c = lane + 32 * i;
-            if (c >= dv) continue;
-            const float val = o[hh][i] * inv;
-            if (out_dtype == IDX_BF16)
-                static_cast<__nv_bfloat16*>(out)[base + c] = __float2bfloat16_rn(val);
-            else
-                static_cast<float*>(out)[base + c] = val;
+        for (int i = 0; i < DV2; ++i) {
+            const int c = 2 * lane + 64 * i;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                if (c + e >= dv) continue;
+                const float val = o[hh][2 * i + e] * inv;
+                if (out_dtype == IDX_BF16)
+                    static_cast<__nv_bfloat16*>(out)[base + c + e] = __float2bfloat16_rn(val);
+                else
+                    static_cast<float*>(out)[base + c + e] = val;
+            }
         }
     }
 }
@@ -315,11 +374,14 @@ cudaError_t run_dv(const T* q, int Hq, int Hkv, int dk, int dv, const T* k, cons
                      !(reinterpret_cast<uintptr_t>(v) & 15u) && (kv_row_stride * ts) % 16 == 0 &&
                      (!v || (v_row_stride * ts) % 16 == 0) && (dk * ts) % 16 == 0 && (dv * ts) % 16 == 0;
     dim3 grid((unsigned)n_rows, (unsigned)(Hkv * n_chunks), (unsigned)splits);
-    size_t sm = (size_t)(HC * dk + kKeys * (dk + 1) + (v ? kKeys * dv : 0)) * sizeof(float) +
+    const int qp = (dk + 7) & ~7;
+    const int el = 16 / (int)sizeof(T);
+    const int kp = qp + el, vp = (dv + el - 1) / el * el;
+    size_t sm = (size_t)HC * qp * sizeof(float) + (size_t)kKeys * (kp + (v ? vp : 0)) * sizeof(T) +
                 kKeys * sizeof(int64_t);
-    const int dvl = (dv + 31) / 32;
+    const int dv2 = (dv + 63) / 64;   // column pairs per lane
 #define LIDX_ATTN_CASE(N)                                                                       \
-    if (dvl <= N) {                                                                             \
+    if (dv2 <= N) {                                                                             \
         auto kern = attn_generic_kernel<T, HPW, N>;                                             \
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);       \
         kern<<<grid, kThreads, sm, st>>>(q, Hq, Hkv, dk, dv, k, v, kv_row_stride, v_row_stride, \
@@ -335,7 +397,6 @@ cudaError_t run_dv(const T* q, int Hq, int Hkv, int dk, int dv, const T* k, cons
     LIDX_ATTN_CASE(2)
     LIDX_ATTN_CASE(4)
     LIDX_ATTN_CASE(8)
-    LIDX_ATTN_CASE(16)
 #undef LIDX_ATTN_CASE
     return cudaErrorNotSupported;
 }

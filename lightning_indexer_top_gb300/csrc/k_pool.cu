@@ -83,7 +83,16 @@ cudaError_t run(const T* k, int64_t k_row_stride, int64_t k_rows, const Geom& g,
     const int tpr = d / V;
     const int rp = kThreads / tpr;
     const size_t sm = (size_t)rp * d * sizeof(float);
-    dim3 grid((unsigned)(max_blocks < 65535 ? max_blocks : 65535), (unsigned)g.B);
+    // a full pooling covers every block; an update usually re-pools few blocks per sequence, so a
+    // few CTAs per sequence stride over them (most of a full-size grid would only exit)
+    int gx = max_blocks < 65535 ? max_blocks : 65535;
+    if (n_pooled || stale_pos) {
+        int sms = sm_count();
+        if (sms < 2) sms = 152;
+        const int want = (2 * sms + g.B - 1) / g.B;
+        if (gx > want) gx = want;
+    }
+    dim3 grid((unsigned)gx, (unsigned)g.B);
     pool_kernel<T><<<grid, kThreads, sm, st>>>(k, k_row_stride, k_rows, g, C, d, pooled,
                                                pool_seq_stride, n_pooled, stale_pos);
     return cudaGetLastError();

@@ -11,7 +11,9 @@
 // that key row in chunks of 8 elements and keeps one f32 accumulator per
 // head in registers.  The head count is rounded up to a power of two (a
 // template parameter, so the accumulators stay in registers) and the padding
-// heads get q = 0, w = 0.
+// heads get q = 0, w = 0.  Pooled block keys (few per row) with 16 or more
+// heads take score_split_kernel instead: four threads per key, each over a
+// quarter of the heads.
 #include "lidx_internal.cuh"
 
 namespace lidx {
@@ -78,6 +80,82 @@ __global__ void __launch_bounds__(kTile) score_generic_kernel(
     }
 }
 
+// Few keys per row and many heads (the pooled block keys of a decode step): four threads per key,
+// each summing HH/4 heads, so a row's keys spread over 4x the threads; the four partial head sums
+// of a key are added by shuffles.  q sits in shared memory head-fastest ([d][HH]), so a thread
+// reads its heads' values at one dimension with 16-byte loads and the four head groups of a warp
+// hit different banks; key rows are read with 16-byte loads (the four threads of a key share the
+// lines in L1).  Grid (query rows, tiles of 32 keys).
+constexpr int kSplitKeys = 32;
+
+template <typename TK, int HH>
+__global__ void __launch_bounds__(128) score_split_kernel(
+    const void* __restrict__ q, int q_dtype, const float* __restrict__ w, int H, int d,
+    const TK* __restrict__ k, int64_t k_row_stride, int64_t k_rows, Geom g, int block_size,
+    float* __restrict__ scores, int64_t score_row_stride, bool vec) {
+    constexpr int HG = HH / 4;   // heads per thread
+    extern __shared__ __align__(16) float smem[];
+    float* qs = smem;            // [d][HH], heads >= H zero
+    float* ws = smem + HH * d;   // [HH]
+    const int64_t r = blockIdx.x;
+    const int b = (int)(r / g.T);
+    int n_keys = row_n_vis(g, r);
+    if (block_size > 1) n_keys /= block_size;
+    if ((int)blockIdx.y * kSplitKeys >= n_keys) return;
+    for (int i = threadIdx.x; i < HH * d; i += blockDim.x) {
+        const int h = i % HH, c = i / HH;
+        qs[i] = h < H ? load_any(q, (r * H + h) * (int64_t)d + c, q_dtype) : 0.f;
+    }
+    for (int i = threadIdx.x; i < HH; i += blockDim.x) ws[i] = (i < H) ? w[r * H + i] : 0.f;
+    __syncthreads();
+    const int hg = threadIdx.x & 3;
+    const int j = blockIdx.y * kSplitKeys + (threadIdx.x >> 2);
+    bool valid = j < n_keys;
+    int64_t row = 0;
+    if (valid) {
+        row = key_row(g, b, j);
+        if (row < 0 || row >= k_rows) {
+            flag(g.status, IDX_ERR_DEVICE_BOUNDS);
+            valid = false;
+        }
+    }
+    float part = 0.f;
+    if (valid) {
+        const TK* kr = k + row * k_row_stride;
+        float acc[HG];
+#pragma unroll
+        for (int h = 0; h < HG; ++h) acc[h] = 0.f;
+        for (int c0 = 0; c0 < d; c0 += 4) {
+            float kv[4];
+            if (vec && sizeof(TK) == 4 && c0 + 4 <= d) {
+                const float4 x = *reinterpret_cast<const float4*>(kr + c0);
+                kv[0] = x.x; kv[1] = x.y; kv[2] = x.z; kv[3] = x.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) kv[i] = (c0 + i < d) ? to_f32(kr[c0 + i]) : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (c0 + i >= d) break;
+                const float4* qc = reinterpret_cast<const float4*>(qs + (c0 + i) * HH + hg * HG);
+#pragma unroll
+                for (int h4 = 0; h4 < HG / 4; ++h4) {
+                    const float4 qq = qc[h4];
+                    acc[4 * h4] = fmaf(qq.x, kv[i], acc[4 * h4]);
+                    acc[4 * h4 + 1] = fmaf(qq.y, kv[i], acc[4 * h4 + 1]);
+                    acc[4 * h4 + 2] = fmaf(qq.z, kv[i], acc[4 * h4 + 2]);
+                    acc[4 * h4 + 3] = fmaf(qq.w, kv[i], acc[4 * h4 + 3]);
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < HG; ++h) part = fmaf(ws[hg * HG + h], fmaxf(acc[h], 0.f), part);
+    }
+    part += __shfl_xor_sync(0xffffffffu, part, 1);
+    part += __shfl_xor_sync(0xffffffffu, part, 2);
+    if (valid && hg == 0) scores[r * score_row_stride + j] = part + 0.0f;
+}
+
 template <typename TK>
 cudaError_t run(const void* q, int q_dtype, const float* w, int H, int d, const TK* k,
                 int64_t k_row_stride, int64_t k_rows, const Geom& g, int block_size,
@@ -86,11 +164,21 @@ cudaError_t run(const void* q, int q_dtype, const float* w, int H, int d, const 
     if (block_size > 1) max_keys /= block_size;
     const int64_t n_rows = (int64_t)g.B * g.T;
     if (max_keys <= 0 || n_rows == 0) return cudaSuccess;
-    const int tiles = (max_keys + kTile - 1) / kTile;
-    dim3 grid((unsigned)n_rows, (unsigned)(tiles < 65535 ? tiles : 65535));
     int HH = 1;
     while (HH < H) HH <<= 1;
     size_t sm = (size_t)(HH * d + HH) * sizeof(float);
+    // pooled block keys with many heads: four threads per key
+    if (block_size > 1 && HH >= 16 && sizeof(TK) != 1 && max_keys <= 65535 * kSplitKeys) {
+        dim3 sgrid((unsigned)n_rows, (unsigned)((max_keys + kSplitKeys - 1) / kSplitKeys));
+        auto kern = HH == 16 ? score_split_kernel<TK, 16> : (HH == 32 ? score_split_kernel<TK, 32> : score_split_kernel<TK, 64>);
+        if (sm > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        const bool vec = !(reinterpret_cast<uintptr_t>(k) & 15u) && (k_row_stride * (int64_t)sizeof(TK)) % 16 == 0;
+        kern<<<sgrid, 128, sm, st>>>(q, q_dtype, w, H, d, k, k_row_stride, k_rows, g, block_size, scores,
+                                      score_row_stride, vec);
+        return cudaGetLastError();
+    }
+    const int tiles = (max_keys + kTile - 1) / kTile;
+    dim3 grid((unsigned)n_rows, (unsigned)(tiles < 65535 ? tiles : 65535));
 #define LIDX_SCORE_CASE(N)                                                                     \
     case N: {                                                                                  \
         auto kern = score_generic_kernel<TK, N>;                                               \

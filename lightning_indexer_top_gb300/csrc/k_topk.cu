@@ -256,6 +256,95 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* scores,
 }
 
 // ---------------------------------------------------------------------------
+// Block mode with at most kRankMax complete blocks per row (the pooled keys of
+// a decode step): one CTA per row sorts the blocks in shared memory by the
+// composite key (order key, then the complement of the block index), so that
+// a larger composite is a better block and equal scores order the lower block
+// first, with a bitonic network; the first K are kept and expanded in
+// ascending block order to their C member positions, then the tail.  The same
+// selection as select_row<true> (the lower block index wins ties, -0 == +0).
+// ---------------------------------------------------------------------------
+constexpr int kRankMax = 1024;
+constexpr int kRankThreads = 1024;
+
+__global__ void __launch_bounds__(kRankThreads) topk_block_rank_kernel(const float* scores, int64_t score_row_stride,
+                                                                      Geom g, int top_k, int C, int32_t* idx,
+                                                                      int64_t idx_row_stride, int32_t* n_sel) {
+    __shared__ uint64_t comp_s[kRankMax];
+    __shared__ uint32_t sel_s[kRankMax / 32];
+    __shared__ uint32_t pre_s[kRankMax / 32];
+    __shared__ int32_t blk_s[kRankMax];
+    const int64_t r = blockIdx.x;
+    const int n_vis = row_n_vis(g, r);
+    const int n = n_vis / C;
+    const int K = min(top_k / C, n);
+    const int cap = (top_k / C) * C + C - 1;
+    const int tail0 = n * C;
+    const int n_out = K * C + (n_vis - tail0);
+    const float* s = scores + r * score_row_stride;
+    int32_t* out = idx + r * idx_row_stride;
+    const int nw = (n + 31) >> 5;
+    int n_pad = 2;
+    while (n_pad < n) n_pad <<= 1;
+    for (int i = threadIdx.x; i < n_pad; i += kRankThreads)
+        comp_s[i] = i < n ? ((uint64_t)order_key(s[i]) << 32) | (uint32_t)(0xffffffffu - (uint32_t)i) : 0ull;
+    for (int i = threadIdx.x; i < nw; i += kRankThreads) sel_s[i] = 0u;
+    __syncthreads();
+    if (K == n) {
+        for (int i = threadIdx.x; i < n_vis; i += kRankThreads) out[i] = i;
+    } else {
+        if (K > 0) {
+            // bitonic sort, descending: pair (i, i + stride) in a run of `size` goes down if i's run is
+            // an even one, up otherwise
+            for (int size = 2; size <= n_pad; size <<= 1) {
+                for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                    for (int t = threadIdx.x; t < n_pad / 2; t += kRankThreads) {
+                        const int i = 2 * stride * (t / stride) + (t % stride), j = i + stride;
+                        const uint64_t a = comp_s[i], c = comp_s[j];
+                        const bool down = (i & size) == 0;
+                        if (down ? (a < c) : (a > c)) {
+                            comp_s[i] = c;
+                            comp_s[j] = a;
+                        }
+                    }
+                    __syncthreads();
+                }
+            }
+            for (int i = threadIdx.x; i < K; i += kRankThreads) {
+                const int bidx = (int)(0xffffffffu - (uint32_t)comp_s[i]);
+                atomicOr(&sel_s[bidx >> 5], 1u << (bidx & 31));
+            }
+            __syncthreads();
+            if (threadIdx.x < 32) {   // exclusive prefix of selected blocks per 32-block word
+                uint32_t carry = 0;
+                for (int w0 = 0; w0 < nw; w0 += 32) {
+                    const int w = w0 + threadIdx.x;
+                    const uint32_t c = w < nw ? (uint32_t)__popc(sel_s[w]) : 0u;
+                    uint32_t x = c;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                        if ((int)threadIdx.x >= o) x += y;
+                    }
+                    if (w < nw) pre_s[w] = carry + x - c;
+                    carry += __shfl_sync(0xffffffffu, x, 31);
+                }
+            }
+            __syncthreads();
+            for (int b = threadIdx.x; b < n; b += kRankThreads) {
+                const uint32_t word = sel_s[b >> 5];
+                if ((word >> (b & 31)) & 1u) blk_s[pre_s[b >> 5] + __popc(word & ((1u << (b & 31)) - 1u))] = b;
+            }
+            __syncthreads();
+            for (int o = threadIdx.x; o < K * C; o += kRankThreads) out[o] = blk_s[o / C] * C + o % C;
+        }
+        for (int i = threadIdx.x; i < n_vis - tail0; i += kRankThreads) out[K * C + i] = tail0 + i;
+    }
+    for (int i = n_out + threadIdx.x; i < cap; i += kRankThreads) out[i] = -1;
+    if (n_sel && threadIdx.x == 0) n_sel[r] = n_out;
+}
+
+// ---------------------------------------------------------------------------
 // Token-mode selection for rows of up to kMapMax candidates, touching the
 // scores in one pass after the histogram:
 //   1. histogram of the top 11 key bits -> the bin B1 holding the K-th
@@ -772,7 +861,8 @@ __global__ void __launch_bounds__(kMcThreads) topk_hist_filter_kernel(const floa
         mc_filter_range(s, c0, c1, lo, L, r, buf, nbuf, base);
         return;
     }
-    // 16-byte loads: thread t takes the float4s t, t + 256, ... of the chunk, all issued at once
+    // 16-byte loads: thread t takes the float4s t, t + 256, ... of the chunk, all issued at once; each
+    // thread marks its hits in a bit mask, one warp scan places them, one shared atomic per warp
     if (threadIdx.x == 0) nbuf = 0u;
     __syncthreads();
     const int lane = threadIdx.x & 31;
@@ -788,30 +878,42 @@ __global__ void __launch_bounds__(kMcThreads) topk_hist_filter_kernel(const floa
                               : make_float4(j < c1 ? s[j] : 0.f, j + 1 < c1 ? s[j + 1] : 0.f,
                                             j + 2 < c1 ? s[j + 2] : 0.f, 0.f);
         }
+        uint32_t keys[4 * kV];
+        uint32_t hits = 0;
 #pragma unroll
         for (int b = 0; b < kV; ++b) {
             const float e[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int j = j0 + (b * kMcThreads + threadIdx.x) * 4 + q;
-                const uint32_t key = order_key(e[q]);
-                const bool hit = j < c1 && key >= lo;
-                const uint32_t m = __ballot_sync(0xffffffffu, hit);
-                if (m) {
-                    uint32_t at = 0;
-                    if (lane == __ffs(m) - 1) at = atomicAdd(&nbuf, (uint32_t)__popc(m));
-                    at = __shfl_sync(0xffffffffu, at, __ffs(m) - 1) + __popc(m & ((1u << lane) - 1u));
-                    if (hit) {
-                        const uint64_t kp = ((uint64_t)key << 32) | (uint32_t)j;
-                        if (at < (uint32_t)kMcLocal) {
-                            buf[at] = kp;
-                        } else {
-                            const uint32_t slot = atomicAdd(cnt, 1u);
-                            if (slot < (uint32_t)kMcCandCap) cand[slot] = kp;
-                        }
-                    }
-                }
+                keys[4 * b + q] = order_key(e[q]);
+                hits |= (uint32_t)(j < c1 && keys[4 * b + q] >= lo) << (4 * b + q);
             }
+        }
+        const uint32_t nh = __popc(hits);
+        uint32_t incl = nh;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
+        uint32_t wbase = 0;
+        if (lane == 31 && wtot) wbase = atomicAdd(&nbuf, wtot);
+        wbase = __shfl_sync(0xffffffffu, wbase, 31);
+        uint32_t at = wbase + incl - nh;
+        while (hits) {
+            const int q = __ffs(hits) - 1;
+            hits &= hits - 1;
+            const int j = j0 + ((q >> 2) * kMcThreads + threadIdx.x) * 4 + (q & 3);
+            const uint64_t kp = ((uint64_t)keys[q] << 32) | (uint32_t)j;
+            if (at < (uint32_t)kMcLocal) {
+                buf[at] = kp;
+            } else {
+                const uint32_t slot = atomicAdd(cnt, 1u);
+                if (slot < (uint32_t)kMcCandCap) cand[slot] = kp;
+            }
+            ++at;
         }
     }
     __syncthreads();
@@ -922,8 +1024,12 @@ cudaError_t launch_topk(const float* scores, int64_t score_row_stride, const Geo
     const int64_t n_rows = (int64_t)g.B * g.T;
     if (n_rows == 0) return cudaSuccess;
     if (block_size > 1) {
-        topk_kernel<true><<<(unsigned)n_rows, kThreads, 0, st>>>(scores, score_row_stride, g, top_k,
-                                                                 block_size, idx, idx_row_stride, n_sel);
+        if (g.max_n_kv / block_size <= kRankMax)
+            topk_block_rank_kernel<<<(unsigned)n_rows, kRankThreads, 0, st>>>(scores, score_row_stride, g, top_k,
+                                                                             block_size, idx, idx_row_stride, n_sel);
+        else
+            topk_kernel<true><<<(unsigned)n_rows, kThreads, 0, st>>>(scores, score_row_stride, g, top_k,
+                                                                     block_size, idx, idx_row_stride, n_sel);
     } else if (ws && ws_bytes >= mc_bytes(n_rows) && n_rows < 2 * sm_count() && g.max_n_kv >= 4 * kMcChunk) {
         // few long rows: spread the passes over the rows' chunks
         const McLayout L = mc_layout(ws, n_rows);

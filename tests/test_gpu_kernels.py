@@ -93,16 +93,22 @@ def test_score_generic_matches_oracle(H, d, qt, kt):
         assert np.all(sh[r, nv:] == 12345.0), "entries past the visible keys must be untouched"
 
 
-def test_score_block_mode_counts_complete_blocks():
-    g = torch.Generator(device=DEV).manual_seed(31)
-    C, H, d = 4, 8, 128
+@pytest.mark.parametrize("H", [8, 16, 32, 64])
+def test_score_block_mode_counts_complete_blocks(H):
+    # H >= 16 takes the split-head pooled-key scorer, H = 8 the one-key-per-thread scorer
+    g = torch.Generator(device=DEV).manual_seed(31 + H)
+    C, d = 4, 128
     n_kv = [37, 4, 3, 64]
     B = len(n_kv)
     stride = 16
     pooled = torch.randn(B * stride, d, generator=g, device=DEV)
+    if H == 32:   # more blocks than one 64-key tile of the split scorer
+        n_kv = [37, 4, 3, 64 * 4 * 3 + 9]
+        stride = 200
+        pooled = torch.randn(B * stride, d, generator=g, device=DEV)
     q = torch.randn(B, H, d, generator=g, device=DEV).to(torch.bfloat16)
     w = torch.randn(B, H, generator=g, device=DEV)
-    batch = L.Batch(_i32(n_kv), 1, 64, kv_seq_stride=stride)
+    batch = L.Batch(_i32(n_kv), 1, max(n_kv), kv_seq_stride=stride)
     s = torch.full((B, stride), -7.0, device=DEV)
     L.idx_score(q, w, pooled, batch, block_size=C, scores=s)
     torch.cuda.synchronize()
@@ -260,9 +266,13 @@ def test_topk_causal_rows_and_dense_short_rows(path):
 
 
 @pytest.mark.parametrize("C,top_k", [(64, 2048), (4, 10), (3, 2), (8, 8)])
-def test_topk_block_mode_bit_exact(C, top_k):
+@pytest.mark.parametrize("many_blocks", [False, True], ids=["rank_select", "radix_select"])
+def test_topk_block_mode_bit_exact(C, top_k, many_blocks):
+    # rows of at most 1024 complete blocks take the rank-based select, longer ones the radix select
     g = torch.Generator().manual_seed(43 + C)
     n_vis = [top_k + C - 1, top_k + C, 0, 1, C - 1, 5 * top_k + 3, 40 * C + 17, 2 * C]
+    if many_blocks:
+        n_vis.append(1100 * C + 5)
     B = len(n_vis)
     nb_max = max(n_vis) // C + 1
     bscores = torch.randint(-2, 3, (B, nb_max), generator=g).float()
