@@ -172,38 +172,45 @@ KERNELS = ("hadamard", "score", "topk", "attention")
 
 def time_step(step, stream, steps: int, warmup: int, min_ms: float = 0.0, sampler=None):
     """Warm-up, then windows of `steps` steps until at least `min_ms` of timed work (one window at
-    least).  Each window is bracketed by synchronisation and timed with CUDA events on `stream`; one
-    event between consecutive kernels gives per-kernel times.  Returns the window step times, the
-    per-kernel medians over all timed steps and the host time span of the timed windows."""
+    least).  Each window is bracketed by synchronisation and timed with two CUDA events on `stream`
+    around its steps, which run back to back as a serving loop runs them (nothing is recorded
+    between the kernels, so launches chained on the device stay chained).  One more window of
+    `steps` steps with an event between consecutive calls gives the per-kernel times.  Returns the
+    window step times, the per-kernel medians and the host time span of the step-time windows."""
     import torch
     rotates = step.q_rot is not None
     calls = (step.rotate if rotates else None, step.score, step.select, step.attend)
     for _ in range(max(warmup, 3)):
         step.run()
     torch.cuda.synchronize()
-    windows, per_kernel = [], {k: [] for k in KERNELS}
+    windows = []
     t_host0 = time.perf_counter()
     spent = 0.0
     while not windows or spent < min_ms:
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
         w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         w0.record(stream)
-        for i in range(steps):
-            for j, call in enumerate(calls):
-                evs[i][j].record(stream)
-                if call is not None:
-                    call()
-            evs[i][4].record(stream)
+        for _ in range(steps):
+            step.run()
         w1.record(stream)
         torch.cuda.synchronize()
         ms = w0.elapsed_time(w1)
         windows.append(ms / steps)
         spent += ms
-        for e in evs:
-            for j, k in enumerate(KERNELS):
-                per_kernel[k].append(e[j].elapsed_time(e[j + 1]))
     t_host1 = time.perf_counter()
+    per_kernel = {k: [] for k in KERNELS}
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        for j, call in enumerate(calls):
+            evs[i][j].record(stream)
+            if call is not None:
+                call()
+        evs[i][4].record(stream)
+    torch.cuda.synchronize()
+    for e in evs:
+        for j, k in enumerate(KERNELS):
+            per_kernel[k].append(e[j].elapsed_time(e[j + 1]))
     med = {k: statistics.median(v) for k, v in per_kernel.items()}
     if not rotates:
         med["hadamard"] = 0.0
@@ -246,6 +253,18 @@ def rooflines(wl, step, ms, hbm, bf16, peak_kind):
         return {"bound": "tensor", "kernel": kernel, "achieved": a, "peak": bf16, "peak_kind": peak_kind,
                 "unit": "TFLOP/s", "frac": a / bf16, "algorithmic_flops_per_launch": flops, "ms": t_ms}
 
+    if getattr(step, "one_launch", False):
+        # the whole step in one kernel: the scan's bytes (keys, scores, q, w), the selection written,
+        # and the attention's (gathered latent rows, q, out)
+        n_keys = sum(wl.n_kv_host)
+        dk = wl.q_attn.shape[-1]
+        nbytes = (n_keys * (wl.d * 2 + 4) + B * wl.H * (wl.d * q_bytes + 4) + sum(n_sel) * 4 +
+                  sum(n_sel) * dk * 2 + B * wl.q_attn.shape[1] * (dk * 2 + wl.dv * out_bytes))
+        t = ms["score"] + ms["topk"] + ms["attention"]
+        r["step"] = hbm_line("sparse_decode_step (score + top-k + MLA attention, one launch)", nbytes, t)
+        r["step"]["tensor_frac"] = (2.0 * n_keys * wl.H * wl.d + 2.0 * sum(n_sel) * wl.q_attn.shape[1] *
+                                    (dk + wl.dv)) / (t * 1e-3) / 1e12 / bf16
+        return r, "step"
     if wl.kind == "prefill":
         r["score"] = tensor_line("idx_score (prefill, tcgen05)", 2.0 * sum(n_vis) * wl.H * wl.d, ms["score"])
     elif C > 1:
@@ -592,7 +611,8 @@ def main():
                          % (wl.k_idx.numel() * 2 / 1e9, wl.k_attn.numel() * 2 / 1e9)},
         "timing": {"windows": len(windows), "steps_per_window": args.steps,
                    "ms_per_step_median": statistics.median(windows), "ms_per_step_min": min(windows),
-                   "ms_per_step_max": max(windows), "per_kernel": "median over every timed step"},
+                   "ms_per_step_max": max(windows),
+                   "per_kernel": "medians over one extra window with an event between consecutive calls"},
         "key_cache_gbs": key_bytes / ((ms["score"] + ms["topk"]) * 1e-3) / 1e9,
         "key_cache_frac": key_bytes / ((ms["score"] + ms["topk"]) * 1e-3) / 1e9 / hbm,
         "ms_per_kernel": ms,

@@ -365,8 +365,63 @@ idx_status sparse_attn_decode_noalloc(const void* q, idx_dtype dtype, int32_t n_
                                       int64_t idx_row_stride, const int32_t* n_sel, float scale, void* out,
                                       idx_dtype out_dtype, idx_stream_t stream);
 
+/*
+ * sparse_decode_step -- one decode step of the sparse attention: the
+ * indexer's scores and top-k selection (idx_score_topk) followed by the
+ * attention over the selected keys (sparse_attn_decode), with the results of
+ * those two calls (scores, idx, n_sel and out are all written).  The pages'
+ * fused indexer + top-k ("Route DSA indexer selection through
+ * ggml_indexer_topk") feeding the gathered decode ("Gather OpenPangu DSA
+ * decode reads", ik_llama_opt commit log).
+ *   Indexer arguments as idx_score_topk; attention arguments as
+ *   sparse_attn_decode (q_attn with attn_dtype, n_q_heads, n_kv_heads, dk,
+ *   dv, k_attn, v_attn, strides and kv_rows).
+ *   workspace  idx_workspace_size(IDX_OP_DECODE_STEP, n_rows, max_n_kv,
+ *              top_k, n_q_heads, dv) bytes, 16-byte aligned.
+ * Few short decode rows run as ONE launch (a grid of 2-CTA clusters resident
+ * at once: each CTA scores a share of the key tiles, the CTA finishing a row
+ * selects it, each cluster then attends one (row, key split) unit, and the
+ * splits are merged after a grid barrier): n_q_per_seq 1, at most 32 rows,
+ * max_n_kv <= 16384, the indexer at 64 heads x 128 with 16-bit keys (q of
+ * the keys' type, or BF16 q with F16 keys), the 128-head MLA latent
+ * attention (BF16, dk 576, dv 512, v_attn NULL), 16-byte aligned tensors,
+ * and rows x key splits no more than the clusters the device holds at once.
+ * The scores, the selection and (with the same key splits) the output are
+ * bit for bit those of the two calls.  Anything else runs the two calls.
+ * The fused launch waits on flags other CTAs of the same launch raise (all
+ * bounded, ~2 s; a timeout records IDX_ERR_TIMEOUT in the device status).
+ * Its flags and counters use one of 256 slots of a library-owned device
+ * array, taken round-robin per call; more than 256 fused calls in flight on
+ * one device at once (across streams) would share a slot and must not run.
+ */
+idx_status sparse_decode_step(const void* q, idx_dtype q_dtype, const float* w, int32_t n_heads, int32_t head_dim,
+                              const void* k, idx_dtype k_dtype, int64_t k_row_stride, int64_t k_rows,
+                              idx_batch batch, int32_t top_k, float* scores, int64_t score_row_stride, int32_t* idx,
+                              int64_t idx_row_stride, int32_t* n_sel, const void* q_attn, idx_dtype attn_dtype,
+                              int32_t n_q_heads, int32_t n_kv_heads, int32_t dk, int32_t dv, const void* k_attn,
+                              const void* v_attn, int64_t kv_row_stride, int64_t v_row_stride, int64_t kv_rows,
+                              float scale, void* out, idx_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                              idx_stream_t stream);
+
+/*
+ * sparse_decode_step_fused -- 1 when a sparse_decode_step call with these
+ * sizes runs as one launch on the current device (given the supported
+ * dtypes, head counts, alignment and a workspace of
+ * idx_workspace_size(IDX_OP_DECODE_STEP, ...) bytes), else 0.  Host only;
+ * the first call per device queries how many clusters the device holds.
+ */
+int32_t sparse_decode_step_fused(int64_t n_rows, int32_t n_q_per_seq, int32_t max_n_kv, int32_t top_k,
+                                 int64_t idx_row_stride);
+
 /* Operation selectors for idx_workspace_size. */
-enum { IDX_OP_SCORE = 0, IDX_OP_TOPK = 1, IDX_OP_ATTN_DECODE = 2, IDX_OP_ATTN_PREFILL = 3, IDX_OP_SCORE_TOPK = 4 };
+enum {
+    IDX_OP_SCORE = 0,
+    IDX_OP_TOPK = 1,
+    IDX_OP_ATTN_DECODE = 2,
+    IDX_OP_ATTN_PREFILL = 3,
+    IDX_OP_SCORE_TOPK = 4,
+    IDX_OP_DECODE_STEP = 5
+};
 
 /*
  * idx_workspace_size -- bytes of device workspace an operation needs for the

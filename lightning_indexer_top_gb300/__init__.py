@@ -25,13 +25,13 @@ __all__ = [
     "Batch", "LidxError", "build", "load", "idx_hadamard", "idx_score", "idx_block_pool", "idx_block_pool_update",
     "idx_quantize_rows", "idx_score_q8", "inline_scales",
     "idx_topk", "sparse_attn_decode", "sparse_attn_prefill", "idx_workspace_size",
-    "idx_device_status", "topk_capacity", "sparse_attn_decode_noalloc",
+    "idx_device_status", "topk_capacity", "sparse_attn_decode_noalloc", "idx_score_topk", "sparse_decode_step", "sparse_decode_step_fused",
 ]
 
 IDX_OK, IDX_ERR_INVALID_ARG, IDX_ERR_UNSUPPORTED, IDX_ERR_CUDA, IDX_ERR_TIMEOUT, IDX_ERR_DEVICE_BOUNDS, IDX_ERR_INEXACT = range(7)
 IDX_F32, IDX_F16, IDX_BF16 = 0, 1, 2
 IDX_POS_CLEAN = 2**31 - 1   # stale_pos value: no edit
-IDX_OP_SCORE, IDX_OP_TOPK, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL, IDX_OP_SCORE_TOPK = 0, 1, 2, 3, 4
+IDX_OP_SCORE, IDX_OP_TOPK, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL, IDX_OP_SCORE_TOPK, IDX_OP_DECODE_STEP = 0, 1, 2, 3, 4, 5
 
 _DTYPES = {torch.float32: IDX_F32, torch.float16: IDX_F16, torch.bfloat16: IDX_BF16}
 
@@ -84,7 +84,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "sparse_attn_prefill": [P, I32, I32, I32, I32, I32, P, P, I64, I64, I64, _Batch, P, I64, P, F,
                                 P, I32, P, SZ, P],
         "sparse_attn_decode_noalloc": [P, I32, I32, I32, I32, I32, P, I64, I64, _Batch, P, I64, P, F, P, I32, P],
+        "sparse_decode_step": [P, I32, P, I32, I32, P, I32, I64, I64, _Batch, I32, P, I64, P, I64, P,
+                               P, I32, I32, I32, I32, I32, P, P, I64, I64, I64, F, P, I32, P, SZ, P],
         "idx_workspace_size": [I32, I64, I32, I32, I32, I32],
+        "sparse_decode_step_fused": [I64, I32, I32, I32, I64],
         "idx_last_error": [],
         "idx_device_status": [I32],
     }
@@ -379,6 +382,52 @@ def idx_score_topk(q: torch.Tensor, w: torch.Tensor, k: torch.Tensor, batch: Bat
                                  batch.c(), top_k, _ptr(scores), scores.stride(0), _ptr(idx), idx.stride(0),
                                  _ptr(n_sel), _ptr(workspace), ws_bytes, _stream(q.device)))
     return scores, idx, n_sel
+
+
+def sparse_decode_step(q: torch.Tensor, w: torch.Tensor, k: torch.Tensor, batch: Batch, top_k: int,
+                       q_attn: torch.Tensor, k_attn: torch.Tensor, v_attn: Optional[torch.Tensor], scale: float, *,
+                       dv: Optional[int] = None, scores: Optional[torch.Tensor] = None,
+                       idx: Optional[torch.Tensor] = None, n_sel: Optional[torch.Tensor] = None,
+                       out: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                       workspace: Optional[torch.Tensor] = None):
+    """One decode step: idx_score_topk then sparse_attn_decode (one launch for few short rows).
+    Returns (scores, idx, n_sel, out)."""
+    _need_cuda(q, w, k, q_attn, k_attn, v_attn, scores, idx, n_sel, out, workspace)
+    rows, H, d = q.shape
+    assert rows == batch.n_rows and w.shape == (rows, H) and w.dtype == torch.float32
+    assert q.is_contiguous() and w.is_contiguous() and k.stride(-1) == 1 and q_attn.is_contiguous()
+    _, Hq, dk = q_attn.shape
+    if v_attn is None:
+        hkv, dv = 1, (dv if dv is not None else 512)
+        v_row_stride = 0
+    else:
+        hkv, dv = k_attn.shape[1], v_attn.shape[-1]
+        v_row_stride = v_attn.stride(0)
+    kk = 2048 if top_k == -1 else top_k
+    if scores is None:
+        scores = torch.empty(rows, max(batch.max_n_kv, 1), device=q.device, dtype=torch.float32)
+    if idx is None:
+        idx = torch.empty(rows, kk, device=q.device, dtype=torch.int32)
+    if n_sel is None:
+        n_sel = torch.empty(rows, device=q.device, dtype=torch.int32)
+    if out is None:
+        out = torch.empty(rows, Hq, dv, device=q.device, dtype=out_dtype)
+    if workspace is None:
+        need = idx_workspace_size(IDX_OP_DECODE_STEP, rows, batch.max_n_kv, top_k, Hq, dv)
+        if need:
+            workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().sparse_decode_step(_ptr(q), _dtype(q), _ptr(w), H, d, _ptr(k), _dtype(k), k.stride(0), k.shape[0],
+                                     batch.c(), top_k, _ptr(scores), scores.stride(0), _ptr(idx), idx.stride(0),
+                                     _ptr(n_sel), _ptr(q_attn), _dtype(q_attn), Hq, hkv, dk, dv, _ptr(k_attn),
+                                     _ptr(v_attn), k_attn.stride(0), v_row_stride, k_attn.shape[0], float(scale),
+                                     _ptr(out), _dtype(out), _ptr(workspace), ws_bytes, _stream(q.device)))
+    return scores, idx, n_sel, out
+
+
+def sparse_decode_step_fused(n_rows: int, n_q_per_seq: int, max_n_kv: int, top_k: int, idx_row_stride: int) -> bool:
+    """Whether sparse_decode_step runs as one launch for these sizes on the current device."""
+    return bool(load().sparse_decode_step_fused(n_rows, n_q_per_seq, max_n_kv, top_k, idx_row_stride))
 
 
 def sparse_attn_decode_noalloc(q, latent, batch, idx, n_sel, scale, *, out=None, out_dtype=torch.bfloat16):

@@ -413,6 +413,86 @@ idx_status sparse_attn_prefill(const void* q, idx_dtype dtype, int32_t n_q_heads
                        scale, out, out_dtype, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
+idx_status sparse_decode_step(const void* q, idx_dtype q_dtype, const float* w, int32_t n_heads, int32_t head_dim,
+                              const void* k, idx_dtype k_dtype, int64_t k_row_stride, int64_t k_rows,
+                              idx_batch batch, int32_t top_k, float* scores, int64_t score_row_stride, int32_t* idx,
+                              int64_t idx_row_stride, int32_t* n_sel, const void* q_attn, idx_dtype attn_dtype,
+                              int32_t n_q_heads, int32_t n_kv_heads, int32_t dk, int32_t dv, const void* k_attn,
+                              const void* v_attn, int64_t kv_row_stride, int64_t v_row_stride, int64_t kv_rows,
+                              float scale, void* out, idx_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                              idx_stream_t stream) {
+    const char* what = "sparse_decode_step";
+    idx_status s = check_batch(batch, what);
+    if (s != IDX_OK) return s;
+    if (top_k == -1) top_k = IDX_DEFAULT_TOP_K;
+    if (top_k < 1) return fail(IDX_ERR_INVALID_ARG, "%s: top_k < 1 (or -1 for the default)", what);
+    if (!valid_dtype(q_dtype) || !valid_dtype(k_dtype) || !valid_dtype(attn_dtype))
+        return fail(IDX_ERR_INVALID_ARG, "%s: bad dtype", what);
+    if (out_dtype != IDX_F32 && out_dtype != IDX_BF16)
+        return fail(IDX_ERR_INVALID_ARG, "%s: out_dtype must be F32 or BF16", what);
+    if (n_heads < 1 || n_heads > 64) return fail(IDX_ERR_UNSUPPORTED, "%s: n_heads must be in [1, 64]", what);
+    if (head_dim < 1 || head_dim > 256) return fail(IDX_ERR_UNSUPPORTED, "%s: head_dim must be in [1, 256]", what);
+    if (k_row_stride < head_dim) return fail(IDX_ERR_INVALID_ARG, "%s: k_row_stride < head_dim", what);
+    if (k_rows < 0 || kv_rows < 0) return fail(IDX_ERR_INVALID_ARG, "%s: k_rows or kv_rows < 0", what);
+    if (score_row_stride < batch.max_n_kv)
+        return fail(IDX_ERR_INVALID_ARG, "%s: score_row_stride < keys per row", what);
+    if (idx_row_stride < top_k) return fail(IDX_ERR_INVALID_ARG, "%s: idx_row_stride < top_k", what);
+    if (n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads != 0)
+        return fail(IDX_ERR_INVALID_ARG, "%s: need Hq, Hkv >= 1 and Hq %% Hkv == 0", what);
+    if (dk < 1 || dk > 576 || dv < 1 || dv > 512)
+        return fail(IDX_ERR_INVALID_ARG, "%s: need 1 <= dk <= 576 and 1 <= dv <= 512", what);
+    if (!v_attn && (n_kv_heads != 1 || dv > dk))
+        return fail(IDX_ERR_INVALID_ARG, "%s: latent form (v == NULL) needs Hkv == 1, dv <= dk", what);
+    if (kv_row_stride < (int64_t)n_kv_heads * dk) return fail(IDX_ERR_INVALID_ARG, "%s: kv_row_stride < Hkv*dk", what);
+    if (v_attn && v_row_stride < (int64_t)n_kv_heads * dv)
+        return fail(IDX_ERR_INVALID_ARG, "%s: v_row_stride < Hkv*dv", what);
+    if (!std::isfinite(scale)) return fail(IDX_ERR_INVALID_ARG, "%s: scale not finite", what);
+    if (workspace && !aligned16(workspace))
+        return fail(IDX_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", what);
+    const int64_t rows = (int64_t)batch.n_seq * batch.n_q_per_seq;
+    if (rows == 0) return IDX_OK;
+    if (!q || !w || !k || !scores || !idx || !n_sel || !q_attn || !k_attn || !out)
+        return fail(IDX_ERR_INVALID_ARG, "%s: NULL q/w/k/scores/idx/n_sel/q_attn/k_attn/out", what);
+    const cudaStream_t st = (cudaStream_t)stream;
+    // one launch for few short decode rows with the 128-head MLA attention
+    const bool q_exact = q_dtype == k_dtype || (q_dtype == IDX_BF16 && k_dtype == IDX_F16);
+    if (n_heads == 64 && head_dim == 128 && k_dtype != IDX_F32 && q_exact && batch.n_q_per_seq == 1 &&
+        aligned16(q) && aligned16(k) && (k_row_stride * 2) % 16 == 0 && batch.max_n_kv > 0 &&
+        mla_tc_supported(attn_dtype, n_q_heads, n_kv_heads, dk, dv, k_attn, v_attn, kv_row_stride, kv_rows, q_attn,
+                         out) &&
+        fused_decode_fits(rows, batch.max_n_kv, top_k, idx_row_stride)) {
+        const size_t need = fused_decode_workspace_bytes(rows, idx_row_stride);
+        if (workspace && workspace_bytes >= need) {
+            const Geom g = make_geom(batch);
+            const cudaError_t e = launch_decode_fused(q, q_dtype, w, k, k_dtype, k_row_stride, k_rows, g, top_k, scores,
+                                                      score_row_stride, idx, idx_row_stride, n_sel, k_attn,
+                                                      kv_row_stride, kv_rows, q_attn, scale, out, out_dtype, workspace,
+                                                      workspace_bytes, st);
+            if (e == cudaSuccess) return IDX_OK;
+            // a grid the device cannot hold at once (or a shape the launch declines) runs unfused
+            if (e != cudaErrorNotSupported && e != cudaErrorCooperativeLaunchTooLarge)
+                return from_cuda(e, what);
+            cudaGetLastError();
+        }
+    }
+    // otherwise the two calls, with the same results
+    s = idx_score_topk(q, q_dtype, w, n_heads, head_dim, k, k_dtype, k_row_stride, k_rows, batch, top_k, scores,
+                       score_row_stride, idx, idx_row_stride, n_sel, workspace, workspace_bytes, stream);
+    if (s != IDX_OK) return s;
+    return sparse_attn_decode(q_attn, attn_dtype, n_q_heads, n_kv_heads, dk, dv, k_attn, v_attn, kv_row_stride,
+                              v_row_stride, kv_rows, batch, idx, idx_row_stride, n_sel, scale, out, out_dtype,
+                              workspace, workspace_bytes, stream);
+}
+
+int32_t sparse_decode_step_fused(int64_t n_rows, int32_t n_q_per_seq, int32_t max_n_kv, int32_t top_k,
+                                 int64_t idx_row_stride) {
+    if (top_k == -1) top_k = IDX_DEFAULT_TOP_K;
+    return n_q_per_seq == 1 && max_n_kv > 0 && top_k >= 1 && idx_row_stride >= top_k &&
+                   fused_decode_fits(n_rows, max_n_kv, top_k, idx_row_stride)
+               ? 1
+               : 0;
+}
+
 size_t idx_workspace_size(int32_t op, int64_t n_rows, int32_t max_n_kv, int32_t top_k,
                           int32_t n_q_heads, int32_t dv) {
     (void)max_n_kv;
@@ -425,6 +505,14 @@ size_t idx_workspace_size(int32_t op, int64_t n_rows, int32_t max_n_kv, int32_t 
         return generic_attn_workspace_bytes(n_rows, top_k, n_q_heads, dv);
     }
     if (op == IDX_OP_TOPK) return topk_workspace_bytes(n_rows, top_k);
+    if (op == IDX_OP_DECODE_STEP) {
+        // the larger of the two calls' (they run one after the other on the same buffer); the
+        // fused launch needs the attention's split partials only
+        const size_t a = idx_workspace_size(IDX_OP_SCORE_TOPK, n_rows, max_n_kv, top_k, 0, 0);
+        const size_t b = idx_workspace_size(IDX_OP_ATTN_DECODE, n_rows, max_n_kv, top_k, n_q_heads, dv);
+        const size_t c = n_q_heads == 128 && dv == 512 && n_rows <= 32 ? fused_decode_workspace_bytes(n_rows, top_k) : 0;
+        return a > b ? (a > c ? a : c) : (b > c ? b : c);
+    }
     if (op == IDX_OP_SCORE_TOPK) {
         int sms = sm_count();
         if (sms < 2) sms = 152;

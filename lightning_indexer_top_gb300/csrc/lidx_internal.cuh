@@ -202,6 +202,17 @@ cudaError_t launch_attn_mla_tc(const void* q, const void* lat, int64_t kv_row_st
                                float scale, void* out, int out_dtype, void* ws, size_t ws_bytes,
                                cudaStream_t st);
 
+// fused decode step (scores + top-k + MLA attention in one cooperative launch) for few short
+// decode rows: whether a batch fits, its workspace, the launch (cudaErrorNotSupported when the
+// device cannot hold the grid at once)
+bool fused_decode_fits(int64_t n_rows, int max_n_kv, int top_k, int64_t idx_row_stride);
+size_t fused_decode_workspace_bytes(int64_t n_rows, int64_t idx_row_stride);
+cudaError_t launch_decode_fused(const void* qi, int qi_dtype, const float* w, const void* k, int k_dtype,
+                                int64_t k_row_stride, int64_t k_rows, const Geom& g, int top_k, float* scores,
+                                int64_t score_row_stride, int32_t* idx, int64_t idx_row_stride, int32_t* n_sel,
+                                const void* lat, int64_t lat_row_stride, int64_t kv_rows, const void* qa, float scale,
+                                void* out, int out_dtype, void* ws, size_t ws_bytes, cudaStream_t st);
+
 // TMA tensor maps over 16-bit caches (128-byte swizzle); false if encoding fails
 bool make_key_tmap(CUtensorMap* m, const void* k, bool bf16, int64_t k_row_stride, int64_t k_rows, int box_rows);
 bool make_q3d_tmap(CUtensorMap* m, const void* q, bool bf16, int64_t rows);

@@ -11,7 +11,7 @@ from __future__ import annotations
 import torch
 
 from . import Batch, idx_block_pool, idx_block_pool_update, idx_hadamard, idx_score, idx_score_q8, idx_topk, idx_workspace_size, topk_capacity
-from . import idx_score_topk, IDX_OP_SCORE_TOPK
+from . import idx_score_topk, IDX_OP_SCORE_TOPK, sparse_decode_step, sparse_decode_step_fused, IDX_OP_DECODE_STEP
 from . import sparse_attn_decode, sparse_attn_prefill, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL, IDX_OP_TOPK
 from .workloads import Workload
 
@@ -22,7 +22,8 @@ class SparseAttentionStep:
     re-pools only the newest complete block of every sequence, as a decode step does when
     its token has just completed a block (idx_block_pool_update)."""
 
-    def __init__(self, wl: Workload, out_dtype=None, pool: str = "full", fused: bool = True):
+    def __init__(self, wl: Workload, out_dtype=None, pool: str = "full", fused: bool = True,
+                 one_call: bool = True):
         self.wl = wl
         self.pool_mode = pool
         dev = wl.q_idx.device
@@ -56,6 +57,15 @@ class SparseAttentionStep:
         ws = idx_workspace_size(op, rows, wl.max_n_kv, cap, wl.q_attn.shape[1], wl.dv)
         self.attn_ws = torch.empty(max(ws, 16), device=dev, dtype=torch.uint8) if ws else None
         self.attn = sparse_attn_prefill if wl.kind == "prefill" else sparse_attn_decode
+        # MLA decode over few short rows: the whole step as one call (sparse_decode_step), one launch
+        self.one_call = (one_call and self.fused and wl.kind == "decode" and wl.v_attn is None and
+                         wl.q_attn.shape[1] == 128 and not wl.hadamard and
+                         sparse_decode_step_fused(rows, wl.T, wl.max_n_kv, wl.top_k, cap))
+        self.one_launch = self.one_call
+        self.step_ws = None
+        if self.one_call:
+            sws = idx_workspace_size(IDX_OP_DECODE_STEP, rows, wl.max_n_kv, wl.top_k, 128, wl.dv)
+            self.step_ws = torch.empty(sws, device=dev, dtype=torch.uint8) if sws else None
         self.q_rot = None
         self.k_rot = None
         if wl.hadamard:
@@ -81,6 +91,10 @@ class SparseAttentionStep:
             idx_score(q, wl.w, kp, self.pool_batch, block_size=wl.block_size, scores=self.scores)
         elif wl.k8 is not None:
             idx_score_q8(q, wl.w, wl.k8, wl.k_scale, self.batch, scores=self.scores)
+        elif self.one_call:
+            sparse_decode_step(q, wl.w, k, self.batch, wl.top_k, wl.q_attn, wl.k_attn, None, wl.scale, dv=wl.dv,
+                               scores=self.scores, idx=self.idx, n_sel=self.n_sel, out=self.out,
+                               workspace=self.step_ws)
         elif self.fused:
             idx_score_topk(q, wl.w, k, self.batch, wl.top_k, scores=self.scores, idx=self.idx, n_sel=self.n_sel,
                            workspace=self.topk_ws)
@@ -95,6 +109,8 @@ class SparseAttentionStep:
 
     def attend(self):
         wl = self.wl
+        if self.one_call:
+            return   # attended by the one call in score()
         if wl.v_attn is None:
             self.attn(wl.q_attn, wl.k_attn, None, self.batch, self.idx, self.n_sel, wl.scale, out=self.out,
                       workspace=self.attn_ws, dv=wl.dv)
@@ -112,6 +128,8 @@ class SparseAttentionStep:
 
     def launches_per_step(self) -> int:
         """Kernels one run() enqueues (library launches only)."""
+        if self.one_launch:
+            return 1
         n = 3 + (1 if self.attn_ws is not None else 0)   # score, select, attend (+ split combine)
         if self.fused:
             # fused select: one kernel for rows up to 16384 keys, else bound, filter, finish

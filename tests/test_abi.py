@@ -22,13 +22,14 @@ def lib():
 def _declared_functions():
     src = open(os.path.join(ROOT, "include", "lidx.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:idx_status|size_t|const char\*)\s+(\w+)\s*\(", src, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:idx_status|size_t|int32_t|const char\*)\s+(\w+)\s*\(", src, flags=re.M)))
 
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("idx_score", "idx_score_q8", "idx_quantize_rows", "idx_block_pool", "idx_block_pool_update", "idx_topk", "sparse_attn_decode", "sparse_attn_prefill",
-              "idx_hadamard", "idx_workspace_size", "idx_last_error", "idx_device_status"):
+              "idx_hadamard", "idx_workspace_size", "idx_last_error", "idx_device_status", "idx_score_topk",
+              "sparse_decode_step", "sparse_decode_step_fused", "sparse_attn_decode_noalloc"):
         assert n in names
 
 
@@ -125,3 +126,53 @@ def test_mla_attention_workspace_follows_the_split_policy(lib):
     # the headline (64 rows x 2048) needs none; 8 rows split 8 ways
     assert lib.idx_workspace_size(L.IDX_OP_ATTN_DECODE, 64, 131072, 2048, 128, 512) == 0
     assert lib.idx_workspace_size(L.IDX_OP_ATTN_DECODE, 8, 8192, 2048, 128, 512) == 8 * 8 * 128 * 514 * 4
+
+
+def _step(lib, b, *, top_k=8, idx_stride=8, score_stride=16, out_dtype=L.IDX_BF16, hq=128, hkv=1, dk=576,
+          dv=512, kv_stride=576, ptr=16, scale=1.0):
+    p = ctypes.c_void_p(ptr) if ptr else None
+    return lib.sparse_decode_step(p, L.IDX_BF16, p, 64, 128, p, L.IDX_F16, 128, 16, b, top_k, p, score_stride, p,
+                                  idx_stride, p, p, L.IDX_BF16, hq, hkv, dk, dv, p, None, kv_stride, 0, 16,
+                                  scale, p, out_dtype, None, 0, None)
+
+
+def test_decode_step_host_validation(lib):
+    # every rejection happens on the host, before anything is launched
+    b = _batch()
+    assert _step(lib, b, top_k=0) == L.IDX_ERR_INVALID_ARG
+    assert b"top_k" in lib.idx_last_error()
+    assert _step(lib, b, idx_stride=4) == L.IDX_ERR_INVALID_ARG
+    assert b"idx_row_stride" in lib.idx_last_error()
+    assert _step(lib, b, score_stride=8) == L.IDX_ERR_INVALID_ARG
+    assert b"score_row_stride" in lib.idx_last_error()
+    assert _step(lib, b, out_dtype=L.IDX_F16) == L.IDX_ERR_INVALID_ARG
+    assert _step(lib, b, hq=6, hkv=4) == L.IDX_ERR_INVALID_ARG
+    assert _step(lib, b, hkv=2) == L.IDX_ERR_INVALID_ARG          # latent form needs one kv head
+    assert _step(lib, b, kv_stride=512) == L.IDX_ERR_INVALID_ARG
+    assert b"kv_row_stride" in lib.idx_last_error()
+    assert _step(lib, b, scale=float("inf")) == L.IDX_ERR_INVALID_ARG
+    assert _step(lib, b, ptr=0) == L.IDX_ERR_INVALID_ARG
+    assert b"NULL" in lib.idx_last_error()
+    assert _step(lib, L._Batch(0, 1, None, None, 0, None, 0), ptr=0) == L.IDX_OK
+    assert _step(lib, L._Batch(-1, 1, None, None, 0, None, 0)) == L.IDX_ERR_INVALID_ARG
+
+
+def test_decode_step_workspace_covers_both_calls(lib):
+    # the step's workspace serves the indexer's fused select and then the attention's key splits
+    for rows, n_kv in ((8, 8192), (64, 131072), (1, 4096), (300, 65536)):
+        a = lib.idx_workspace_size(L.IDX_OP_SCORE_TOPK, rows, n_kv, 2048, 0, 0)
+        b = lib.idx_workspace_size(L.IDX_OP_ATTN_DECODE, rows, n_kv, 2048, 128, 512)
+        got = lib.idx_workspace_size(L.IDX_OP_DECODE_STEP, rows, n_kv, 2048, 128, 512)
+        assert got >= max(a, b)
+        if rows <= 32:   # the one-launch step also keeps each row's 2048-bin score histogram
+            assert got >= (-(-b // 16) * 16) + rows * 2048 * 4
+
+
+def test_decode_step_fused_plan_is_host_only(lib):
+    # only one query row per sequence, at most 32 rows, at most 16384 keys, and an index row that holds top_k
+    assert lib.sparse_decode_step_fused(8, 2, 8192, 2048, 2048) == 0
+    assert lib.sparse_decode_step_fused(33, 1, 8192, 2048, 2048) == 0
+    assert lib.sparse_decode_step_fused(8, 1, 16385, 2048, 2048) == 0
+    assert lib.sparse_decode_step_fused(8, 1, 8192, 2048, 1024) == 0
+    assert lib.sparse_decode_step_fused(8, 1, 0, 2048, 2048) == 0
+    assert lib.sparse_decode_step_fused(8, 1, 8192, 2048, 2048) in (0, 1)   # 0 without a device
