@@ -131,6 +131,12 @@ idx_status attn_common(const char* what, const void* q, idx_dtype dtype, int32_t
                                             out, out_dtype, ws, ws_bytes, st),
                          what);
     }
+    if (gqa_tc_supported(dtype, Hq, Hkv, dk, dv, k, v, kv_row_stride, v_row_stride, q)) {
+        const cudaError_t e = launch_attn_gqa_tc(q, dtype, Hq, Hkv, k, v, kv_row_stride, v_row_stride, kv_rows, g, idx,
+                                                 idx_row_stride, n_sel, scale, out, out_dtype, ws,
+                                                 ws ? ws_bytes : 0, st);
+        if (e != cudaErrorNotSupported) return from_cuda(e, what);
+    }
     return from_cuda(launch_attn_generic(q, dtype, Hq, Hkv, dk, dv, k, v, kv_row_stride,
                                          v_row_stride, kv_rows, g, idx, idx_row_stride, n_sel,
                                          scale, out, out_dtype, ws, ws_bytes, st),

@@ -433,6 +433,13 @@ int generic_attn_splits(int64_t n_rows, int64_t cap) {
     return s < 1 ? 1 : (int)s;
 }
 
+cudaError_t launch_attn_generic_combine(const float* part_o, const float* part_ml, int splits, int64_t n_rows, int Hq,
+                                        int dv, void* out, int out_dtype, cudaStream_t st) {
+    attn_generic_combine_kernel<<<dim3((unsigned)n_rows, (unsigned)Hq), 128, 0, st>>>(part_o, part_ml, splits, Hq, dv,
+                                                                                      out, out_dtype);
+    return cudaGetLastError();
+}
+
 size_t generic_attn_workspace_bytes(int64_t n_rows, int64_t cap, int Hq, int dv) {
     const int s = generic_attn_splits(n_rows, cap);
     if (s <= 1 || Hq < 1 || dv < 1) return 0;

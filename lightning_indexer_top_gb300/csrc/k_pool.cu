@@ -13,8 +13,9 @@
 // One CTA of 128 threads per (block, sequence).  With 16-byte vector loads a
 // row of d elements takes TPR = d*size/16 threads, so the CTA reads
 // RP = 128/TPR rows at once; each thread sums its rows in f32 and the RP
-// partial sums are added in shared memory.  A pure HBM stream: each raw key
-// byte is read once and 1/C of it is written (as f32).
+// partial sums are added in shared memory; a thread's loads of 8 rows are in
+// flight together.  A pure HBM stream: each raw key byte is read once and 1/C
+// of it is written (as f32).
 #include "lidx_internal.cuh"
 
 namespace lidx {
@@ -49,16 +50,29 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(const T* __restrict__ k,
 #pragma unroll
         for (int i = 0; i < V; ++i) acc[i] = 0.f;
         if (rg < rp) {
-            for (int t = rg; t < C; t += rp) {
-                const int64_t row = key_row(g, b, (int64_t)beta * C + t);
-                if (row < 0 || row >= k_rows) {
-                    flag(g.status, IDX_ERR_DEVICE_BOUNDS);
-                    continue;
-                }
-                const uint4 raw = *reinterpret_cast<const uint4*>(k + row * k_row_stride + cv * V);
-                const T* e = reinterpret_cast<const T*>(&raw);
+            // kBatch rows' loads in flight at once, then their sums in row order
+            constexpr int kBatch = 8;
+            for (int t0 = rg; t0 < C; t0 += kBatch * rp) {
+                uint4 raw[kBatch];
 #pragma unroll
-                for (int i = 0; i < V; ++i) acc[i] += to_f32(e[i]);
+                for (int u = 0; u < kBatch; ++u) {
+                    raw[u] = make_uint4(0u, 0u, 0u, 0u);
+                    const int t = t0 + u * rp;
+                    if (t < C) {
+                        const int64_t row = key_row(g, b, (int64_t)beta * C + t);
+                        if (row < 0 || row >= k_rows)
+                            flag(g.status, IDX_ERR_DEVICE_BOUNDS);
+                        else
+                            raw[u] = *reinterpret_cast<const uint4*>(k + row * k_row_stride + cv * V);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u) {
+                    if (t0 + u * rp >= C) break;
+                    const T* e = reinterpret_cast<const T*>(&raw[u]);
+#pragma unroll
+                    for (int i = 0; i < V; ++i) acc[i] += to_f32(e[i]);
+                }
             }
 #pragma unroll
             for (int i = 0; i < V; ++i) part[rg * d + cv * V + i] = acc[i];

@@ -294,22 +294,30 @@ __global__ void __launch_bounds__(kRankThreads) topk_block_rank_kernel(const flo
         for (int i = threadIdx.x; i < n_vis; i += kRankThreads) out[i] = i;
     } else {
         if (K > 0) {
-            // bitonic sort, descending: pair (i, i + stride) in a run of `size` goes down if i's run is
-            // an even one, up otherwise
+            // bitonic sort, descending, one element per thread: the pair (i, i ^ stride) of a run of
+            // `size` keeps the larger value at the lower index when the run is an even one (the
+            // smaller otherwise); partners closer than a warp trade by shuffles, farther ones
+            // through shared memory
+            const int i = threadIdx.x;
+            uint64_t val = i < n_pad ? comp_s[i] : 0ull;
             for (int size = 2; size <= n_pad; size <<= 1) {
                 for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                    for (int t = threadIdx.x; t < n_pad / 2; t += kRankThreads) {
-                        const int i = 2 * stride * (t / stride) + (t % stride), j = i + stride;
-                        const uint64_t a = comp_s[i], c = comp_s[j];
-                        const bool down = (i & size) == 0;
-                        if (down ? (a < c) : (a > c)) {
-                            comp_s[i] = c;
-                            comp_s[j] = a;
-                        }
+                    uint64_t other;
+                    if (stride >= 32) {
+                        __syncthreads();
+                        comp_s[i] = val;
+                        __syncthreads();
+                        other = comp_s[i ^ stride];
+                    } else {
+                        other = __shfl_xor_sync(0xffffffffu, val, stride);
                     }
-                    __syncthreads();
+                    const bool lower = (i & stride) == 0, down = (i & size) == 0;
+                    val = (lower == down) ? (val > other ? val : other) : (val < other ? val : other);
                 }
             }
+            __syncthreads();
+            comp_s[i] = val;
+            __syncthreads();
             for (int i = threadIdx.x; i < K; i += kRankThreads) {
                 const int bidx = (int)(0xffffffffu - (uint32_t)comp_s[i]);
                 atomicOr(&sel_s[bidx >> 5], 1u << (bidx & 31));

@@ -191,6 +191,21 @@ cudaError_t launch_attn_generic(const void* q, int dtype, int Hq, int Hkv, int d
                                 float scale, void* out, int out_dtype, void* ws, size_t ws_bytes,
                                 cudaStream_t st);
 
+// merge of the CUDA-core layout's key-split partials ([row, split, head] x dv, then (m, l) in
+// natural-log units)
+cudaError_t launch_attn_generic_combine(const float* part_o, const float* part_ml, int splits, int64_t n_rows, int Hq,
+                                        int dv, void* out, int out_dtype, cudaStream_t st);
+
+// tcgen05 sparse GQA attention (16-bit K/V, dk = dv = 128, at most 16 query heads per kv head);
+// splits write the CUDA-core layout's partials into ws (fewer splits when it is smaller);
+// cudaErrorNotSupported when the selection needs more splits than the workspace holds
+bool gqa_tc_supported(int dtype, int Hq, int Hkv, int dk, int dv, const void* k, const void* v,
+                      int64_t kv_row_stride, int64_t v_row_stride, const void* q);
+cudaError_t launch_attn_gqa_tc(const void* q, int dtype, int Hq, int Hkv, const void* k, const void* v,
+                               int64_t kv_row_stride, int64_t v_row_stride, int64_t kv_rows, const Geom& g,
+                               const int32_t* idx, int64_t idx_row_stride, const int32_t* n_sel, float scale,
+                               void* out, int out_dtype, void* ws, size_t ws_bytes, cudaStream_t st);
+
 // tcgen05 sparse MLA attention (128 heads, 576/512 bf16 latent); the caller
 // checks mla_tc_supported() first; splits > 1 needs mla_workspace_bytes()
 bool mla_tc_supported(int dtype, int Hq, int Hkv, int dk, int dv, const void* k, const void* v,

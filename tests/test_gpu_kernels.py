@@ -376,8 +376,9 @@ def test_attention_gqa_matches_oracle(dtype, out_dtype):
 
 
 def test_attention_gqa_key_splits_and_fallback_without_workspace():
-    # few rows: the selected keys are split over CTAs and merged; with too small a workspace the call
-    # falls back to one split per row; both agree with the oracle (and with each other closely)
+    # few rows: the selected keys are split over CTAs and merged (tensor cores, P rounded to bf16 for
+    # the PV product: the bf16 rule); with too small a workspace for the splits the call runs one split
+    # per row on the CUDA cores (f32 throughout: 1e-4); both agree with the oracle
     g = torch.Generator().manual_seed(63)
     B, Hq, Hkv, dh, n_kv = 4, 32, 4, 128, 5000
     sizes = [2111, 700, 129, 0]
@@ -400,8 +401,51 @@ def test_attention_gqa_key_splits_and_fallback_without_workspace():
             continue
         ref = O.sparse_attention_gqa(np64(q[r]), Kh[r * n_kv:(r + 1) * n_kv], Vh[r * n_kv:(r + 1) * n_kv],
                                      idx[r, :sizes[r]].numpy(), 1 / math.sqrt(dh))
-        assert np.max(np.abs(np64(split[r]) - ref)) <= 1e-4, r
+        assert np.max(np.abs(np64(split[r]) - ref)) <= 2e-2, r
         assert np.max(np.abs(np64(single[r]) - ref)) <= 1e-4, r
+
+
+@pytest.mark.parametrize("dtype,G,B", [(torch.bfloat16, 8, 16), (torch.float16, 8, 3), (torch.bfloat16, 16, 2),
+                                       (torch.float16, 1, 2)])
+def test_attention_gqa_tensor_cores_block_selections(dtype, G, B):
+    # the block-pooled decode's shape: selections of whole 64-key blocks plus a ragged tail, dk = dv = 128,
+    # G query heads per kv head; rows with an empty selection, one key, a dense row and an invalid index
+    g = torch.Generator().manual_seed(64 + G)
+    Hkv, dh, n_kv, C = 4, 128, 6000, 64
+    Hq = G * Hkv
+    q = torch.randn(B, Hq, dh, generator=g).to(dtype)
+    K = torch.randn(B * n_kv, Hkv, dh, generator=g).to(dtype)
+    V = torch.randn(B * n_kv, Hkv, dh, generator=g).to(dtype)
+    cap = 2048 + C - 1
+    idx = torch.full((B, cap), -1, dtype=torch.int32)
+    sizes = []
+    for r in range(B):
+        kind = r % 4
+        if kind == 0:      # 32 random whole blocks and the tail of the sequence
+            blocks = torch.randperm(n_kv // C, generator=g)[:32].sort().values
+            sel = torch.cat([(blocks[:, None] * C + torch.arange(C)).reshape(-1), torch.arange(n_kv - 37, n_kv)])
+        elif kind == 1:    # one key
+            sel = torch.tensor([int(torch.randint(n_kv, (1,), generator=g))])
+        elif kind == 2:    # every key of a short prefix (dense)
+            sel = torch.arange(700)
+        else:              # nothing
+            sel = torch.tensor([], dtype=torch.int64)
+        idx[r, :len(sel)] = sel.to(torch.int32)
+        sizes.append(len(sel))
+    batch = L.Batch(_i32([n_kv] * B), 1, n_kv, kv_seq_stride=n_kv)
+    args = (q.to(DEV), K.to(DEV), V.to(DEV), batch, idx.to(DEV), _i32(sizes), 1 / math.sqrt(dh))
+    for out_dtype in (torch.bfloat16, torch.float32):
+        out = L.sparse_attn_decode(*args, out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        assert L.idx_device_status(reset=True) == 0
+        Kh, Vh = np64(K), np64(V)
+        for r in range(B):
+            if sizes[r] == 0:
+                assert torch.all(out[r] == 0)
+                continue
+            ref = O.sparse_attention_gqa(np64(q[r]), Kh[r * n_kv:(r + 1) * n_kv], Vh[r * n_kv:(r + 1) * n_kv],
+                                         idx[r, :sizes[r]].numpy(), 1 / math.sqrt(dh))
+            assert np.max(np.abs(np64(out[r]) - ref)) <= 2e-2, (r, out_dtype)
 
 
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
