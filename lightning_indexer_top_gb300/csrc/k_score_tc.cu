@@ -83,6 +83,7 @@ constexpr int kD = 128;
 constexpr int kStages = LIDX_SCORE_STAGES;
 constexpr int kAcc = 4;
 constexpr int kTmemCols = kAcc * kH;                 // 256
+constexpr int kTmemColsQ8 = 512;                     // int8 keys: + the widened A tiles (64 columns each) at 256
 constexpr int kTileBytes = kTileKeys * kD * 2;       // 32 KB
 constexpr int kHalfBytes = kTileBytes / 2;           // one 64-column box
 constexpr int kQBytes = kH * kD * 2;                 // 16 KB
@@ -90,13 +91,13 @@ constexpr int kQHalfBytes = kQBytes / 2;
 constexpr int kThreads = 224;                        // 16-bit keys: 7 warps
 constexpr int kThreadsQ8 = 352;                      // int8 keys: + 4 converter warps
 #ifndef LIDX_Q8_RAW_STAGES
-#define LIDX_Q8_RAW_STAGES 5
+#define LIDX_Q8_RAW_STAGES 8
 #endif
 #ifndef LIDX_Q8_CONV_STAGES
 #define LIDX_Q8_CONV_STAGES 2
 #endif
 constexpr int kRawStages = LIDX_Q8_RAW_STAGES;       // int8 keys: TMA ring of 16 KB code tiles
-constexpr int kConvStages = LIDX_Q8_CONV_STAGES;     // int8 keys: widened tiles for the MMA
+constexpr int kConvStages = LIDX_Q8_CONV_STAGES;     // int8 keys: widened tiles for the MMA (in TMEM)
 constexpr int kRawPitchInline = kD + 16;             // int8 rows with their scale inline: 128 codes + f32 + pad
 constexpr int kRawTileBytes = kTileKeys * kRawPitchInline;   // 18 KB stage (16 KB used without inline scales)
 constexpr int kSRing = 8;                            // int8 keys, inline scales: tiles of scales in flight
@@ -139,8 +140,7 @@ static_assert(kStages <= 8 && kRawStages <= 8, "barrier arrays");
 constexpr int kChunkReaders = 1 + 4 + 1;             // MMA lane, 4 epilogue warps, q stager (+4 converters)
 template <bool Q8>
 constexpr size_t smem_bytes() {
-    return 1024 + (Q8 ? (size_t)kRawStages * kRawTileBytes + (size_t)kConvStages * kTileBytes
-                      : (size_t)kStages * kTileBytes) +
+    return 1024 + (Q8 ? (size_t)kRawStages * kRawTileBytes : (size_t)kStages * kTileBytes) +
            kQBufs * kQBytes + sizeof(Ctl) + (2 * kMaxPrefixRows + 1) * sizeof(int) +
            (Q8 ? kSRing * kTileKeys * sizeof(float) : 2 * kHistWords * sizeof(uint32_t));
 }
@@ -253,30 +253,30 @@ __device__ __forceinline__ bool warp_next_chunk(Ctl& c, int k, Chunk& d) {
     return true;
 }
 
-// int8 codes of one 128-key tile (rows of 128 bytes, unswizzled) -> f16 in the
-// MMA's A layout (two 64-column blocks of 16 KB, rows of 128 bytes, 16-byte
-// chunks swizzled by row).  Thread t (0..127) converts key row t; it walks its
-// 8 source chunks starting at chunk t % 8 so that the 8 threads of a
-// shared-memory phase hit 8 different bank groups.
+// int8 codes of key row t of a 128-key tile -> f16, written into TMEM lane t as
+// the MMA's A operand (column c holds elements 2c and 2c+1).  Thread t of the
+// four converter warps owns TMEM lane t.  The TMA lands the code rows in the
+// 128-byte swizzle (chunk i of row t at (i ^ (t % 8)) * 16), so the 8 threads
+// of a shared-memory phase hit 8 different bank groups.
 // The widening is exact and stays on the integer/half ALUs: a code b becomes
 // the unsigned byte u = b + 128 (xor 0x80), the f16 with bit pattern 0x6400 | u
 // is 1024 + u, and subtracting 1152 leaves b (every step exact in f16).
-// With inline scales the rows are 144 bytes apart, which already spreads 8
-// consecutive rows over 8 bank groups, so the chunks are walked in order.
-__device__ __forceinline__ void widen_tile_f16(const uint8_t* __restrict__ raw, uint8_t* __restrict__ dst, int t,
+// With inline scales the rows are 144 bytes apart (no swizzle), which already
+// spreads 8 consecutive rows over 8 bank groups.
+__device__ __forceinline__ void widen_row_tmem(const uint8_t* __restrict__ raw, uint32_t taddr, int t,
                                                bool inline_scale) {
+    // row t's 128 codes (eight 16-byte chunks; in the 128-byte swizzle of the TMA box unless the
+    // rows carry their scale inline, whose 144-byte pitch already spreads the lanes over the banks)
     const uint8_t* src = raw + t * (inline_scale ? kRawPitchInline : 128);
-    const int rot = inline_scale ? 0 : t;
+    const int sw = inline_scale ? 0 : (t & 7);
     const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
     uint4 row[8];                                          // all loads first: one latency per tile
 #pragma unroll
-    for (int i = 0; i < 8; ++i) row[i] = *reinterpret_cast<const uint4*>(src + ((i + rot) & 7) * 16);
+    for (int i = 0; i < 8; ++i) row[i] = *reinterpret_cast<const uint4*>(src + ((i ^ sw) << 4));
+    uint32_t out[64];                                      // column c = elements 2c, 2c+1
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int cch = (i + rot) & 7;                     // 16 codes: elements 16*cch .. 16*cch+15
-        const uint4 v = row[i];
-        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[8];
+        const uint32_t in[4] = {row[i].x, row[i].y, row[i].z, row[i].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint32_t u = in[j] ^ 0x80808080u;
@@ -284,17 +284,13 @@ __device__ __forceinline__ void widen_tile_f16(const uint8_t* __restrict__ raw, 
             const uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);   // {0x64|u2, 0x64|u3}
             const __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo), bias);
             const __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&hi), bias);
-            out[2 * j] = *reinterpret_cast<const uint32_t*>(&a);
-            out[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-        const int blk = cch >> 2;                          // 64-element column block
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int sub = 2 * (cch & 3) + hh;             // 16-byte chunk inside the block's row
-            *reinterpret_cast<uint4*>(dst + blk * kHalfBytes + t * 128 + ((sub ^ (t & 7)) << 4)) =
-                make_uint4(out[4 * hh], out[4 * hh + 1], out[4 * hh + 2], out[4 * hh + 3]);
+            out[8 * i + 2 * j] = *reinterpret_cast<const uint32_t*>(&a);
+            out[8 * i + 2 * j + 1] = *reinterpret_cast<const uint32_t*>(&b);
         }
     }
+    tmem_st_32x32b_x32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(out));
+    tmem_st_32x32b_x32(taddr + 32, *reinterpret_cast<const uint32_t(*)[32]>(out + 32));
+    tmem_st_wait();
 }
 
 template <typename TK, bool kQ8>
@@ -313,8 +309,9 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* tma_tiles = smem;                               // kTmaStages x kTmaBytes, 1024-aligned
-    uint8_t* tiles = kQ8 ? smem + (size_t)kRawStages * kRawTileBytes : smem;   // kAStages x 32 KB
-    uint8_t* qbuf = tiles + (size_t)kAStages * kTileBytes;   // kQBufs x 16 KB, 1024-aligned
+    uint8_t* tiles = smem;                                   // 16-bit keys: kStages x 32 KB
+    uint8_t* qbuf = kQ8 ? smem + (size_t)kRawStages * kRawTileBytes
+                        : tiles + (size_t)kStages * kTileBytes;   // kQBufs x 16 KB, 1024-aligned
     Ctl& c = *reinterpret_cast<Ctl*>(qbuf + kQBufs * kQBytes);
     int* pre = reinterpret_cast<int*>(&c + 1);               // [n_rows + 1] in prefix mode
     int* nvis = pre + kMaxPrefixRows + 1;                    // [n_rows] in prefix mode
@@ -390,7 +387,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
     }
     if (warp == 0 && lane == 0) tma_prefetch_desc(&kmap);
     if (warp == 1) {
-        tmem_alloc(&c.tmem_base, kTmemCols);
+        tmem_alloc(&c.tmem_base, kQ8 ? kTmemColsQ8 : kTmemCols);
         tmem_relinquish();
     }
     if (!kQ8 && hist)
@@ -575,14 +572,25 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(tiles + (size_t)stage * kTileBytes);
                     const uint32_t dt = tmem + acc * kH;
+                    if constexpr (kQ8) {
+                        // A = the widened key tile in TMEM (lane = key, two f16 per column)
+                        const uint32_t at = tmem + kAcc * kH + stage * (kD / 2);
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {
-                        const uint32_t off = (kk & 3) * 32;   // K offset inside the 128-byte row
-                        const uint64_t ad = desc_sw128_kmajor(a0 + (kk >> 2) * kHalfBytes + off, 1024);
-                        const uint64_t bd = desc_sw128_kmajor(b0 + (kk >> 2) * kQHalfBytes + off, 1024);
-                        mma_f16_ss(dt, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < kD / 16; ++kk) {
+                            const uint32_t off = (kk & 3) * 32;
+                            const uint64_t bd = desc_sw128_kmajor(b0 + (kk >> 2) * kQHalfBytes + off, 1024);
+                            mma_f16_ts(dt, at + kk * 8, bd, idesc, kk > 0 ? 1u : 0u);
+                        }
+                    } else {
+                        const uint32_t a0 = smem_u32(tiles + (size_t)stage * kTileBytes);
+#pragma unroll
+                        for (int kk = 0; kk < kD / 16; ++kk) {
+                            const uint32_t off = (kk & 3) * 32;   // K offset inside the 128-byte row
+                            const uint64_t ad = desc_sw128_kmajor(a0 + (kk >> 2) * kHalfBytes + off, 1024);
+                            const uint64_t bd = desc_sw128_kmajor(b0 + (kk >> 2) * kQHalfBytes + off, 1024);
+                            mma_f16_ss(dt, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                        }
                     }
                     mma_commit(&a_empty[stage]);
                     mma_commit(&c.tfull[acc]);
@@ -634,7 +642,9 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
     } else if (kQ8 && warp >= 7) {
         // ------------------------------------------------------------ converters (int8 keys)
         // with inline scales they also hand each row's scale to the epilogue (ring of kSRing tiles)
-        const int t = threadIdx.x - 7 * 32;        // key row of the tile, 0..127
+        // key row of the tile = the TMEM lane this warp may write (lane quarter = warp % 4)
+        const int t = (warp & 3) * 32 + lane;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         int rs = 0, as = 0, ss = 0;
         uint32_t rph = 0, aph = 0, sph = 0;
         bool ok = true;
@@ -654,10 +664,10 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
                 }
                 static_assert(!kQ8 || std::is_same<TK, __half>::value, "int8 codes are widened to f16");
                 const uint8_t* raw = tma_tiles + (size_t)rs * kRawTileBytes;
-                widen_tile_f16(raw, tiles + (size_t)as * kTileBytes, t, inline_scale);
+                widen_row_tmem(raw, tmem + lane_off + kAcc * kH + as * (kD / 2), t, inline_scale);
                 if (inline_scale)
                     escale[ss * kTileKeys + t] = *reinterpret_cast<const float*>(raw + t * kRawPitchInline + kD);
-                fence_proxy_async_smem();           // generic-proxy writes before the MMA reads them
+                tc_fence_before();                  // the TMEM stores before the MMA reads them
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&c.empty[rs]);
@@ -721,24 +731,27 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
             }
             const int hb = (int)(hchunk & 1);      // shared histogram buffer of this chunk
             // tiles in groups of 8: an int8 cache's per-key scales of a whole group are
-            // loaded at once (one memory round trip per 8 tiles, which the 4 TMEM
-            // accumulators give the MMAs slack for) and parked in this lane's own
-            // shared-memory slots
+            // loaded at once, the next group's while this one is processed, and parked in
+            // this lane's own shared-memory slots
+            float scn[8];
+            auto load_scales = [&](int g0) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int j = (g0 + i) * kTileKeys + quad * 32 + lane;
+                    float v = 0.f;
+                    if (g0 + i < d.t1 && j < n_keys) {
+                        const int64_t kr = g.page_table ? key_row(g, b_seq, j) : krow0 + j;
+                        if (kr >= 0 && kr < k_rows) v = k_scale[kr];
+                    }
+                    scn[i] = v;
+                }
+            };
+            if (kQ8 && !inline_scale) load_scales(d.t0);
             for (int g0 = d.t0; ok && g0 < d.t1; g0 += 8) {
                 if (kQ8 && !inline_scale) {
-                    float scs[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int j = (g0 + i) * kTileKeys + quad * 32 + lane;
-                        float v = 0.f;
-                        if (g0 + i < d.t1 && j < n_keys) {
-                            const int64_t kr = g.page_table ? key_row(g, b_seq, j) : krow0 + j;
-                            if (kr >= 0 && kr < k_rows) v = k_scale[kr];
-                        }
-                        scs[i] = v;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) esc[i * 32 + lane] = scs[i];
+                    for (int i = 0; i < 8; ++i) esc[i * 32 + lane] = scn[i];
+                    if (g0 + 8 < d.t1) load_scales(g0 + 8);
                 }
 #pragma unroll 1
                 for (int i = 0; i < 8; ++i) {
@@ -849,7 +862,7 @@ __global__ void __launch_bounds__(kQ8 ? kThreadsQ8 : kThreads, 1) score_tc_decod
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc(tmem, kQ8 ? kTmemColsQ8 : kTmemCols);
     // the last CTA to finish returns the slot's counters to zero for a later launch
     if (threadIdx.x == 0) {
         __threadfence();
@@ -1226,10 +1239,10 @@ namespace {
 // grid of the decode scorer, the key tiles per chunk and the counter slot of this launch; false
 // when the chunks would not number in 32 bits.  Chunks are kChunkTiles tiles, or fewer (down to 2)
 // when a small batch would otherwise leave SMs idle: about four chunks per SM.
-bool decode_launch_shape(const Geom& g, int& grid, int& ct, int& slot) {
+bool decode_launch_shape(const Geom& g, int& grid, int& ct, int& slot, int max_ct = kChunkTiles) {
     const int64_t n_rows = (int64_t)g.B * g.T;
     const int64_t tiles_per_row = (g.max_n_kv + kTileKeys - 1) / kTileKeys;
-    ct = kChunkTiles;
+    ct = max_ct;
     if (n_rows <= kMaxPrefixRows) {
         while (ct > 2 && n_rows * ((tiles_per_row + ct - 1) / ct) < 4 * (int64_t)sm_count()) ct >>= 1;
     }
@@ -1260,10 +1273,13 @@ cudaError_t launch_score_tc_q8(const void* q, int q_dtype, const float* w, const
     if (n_rows == 0 || g.max_n_kv == 0) return cudaSuccess;
     CUtensorMap map;
     if (g.page_table && g.page_size % 64 != 0) return cudaErrorNotSupported;
-    if (!make_key8_tmap(&map, k8, k_row_stride, k_rows, g.page_table ? 64 : kTileKeys, k_scale ? 128 : kRawPitchInline))
+    if (!make_key8_tmap(&map, k8, k_row_stride, k_rows, g.page_table ? 64 : kTileKeys, k_scale ? 128 : kRawPitchInline,
+                        k_scale != nullptr))
         return cudaErrorNotSupported;
     int grid, ct, slot;
-    if (!decode_launch_shape(g, grid, ct, slot)) return cudaErrorNotSupported;
+    // int8 keys: chunks of up to 32 tiles of 16 KB (the epilogue pays a row's weights and a group's
+    // first scales once per chunk)
+    if (!decode_launch_shape(g, grid, ct, slot, 4 * kChunkTiles)) return cudaErrorNotSupported;
     auto kern = score_tc_decode_kernel<__half, true>;
     constexpr size_t smem = smem_bytes<true>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

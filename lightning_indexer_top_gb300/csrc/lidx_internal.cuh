@@ -233,9 +233,9 @@ bool make_key_tmap(CUtensorMap* m, const void* k, bool bf16, int64_t k_row_strid
 bool make_q3d_tmap(CUtensorMap* m, const void* q, bool bf16, int64_t rows);
 bool make_w_tmap(CUtensorMap* m, const float* w, int64_t rows);
 // [rows, payload] int8 keys (128 codes, or 144 bytes with the scale inline): boxes of
-// payload bytes x box_rows rows, no swizzle
+// payload bytes x box_rows rows, unswizzled or (128-byte rows) in the 128-byte swizzle
 bool make_key8_tmap(CUtensorMap* m, const int8_t* k, int64_t row_bytes, int64_t k_rows, int box_rows,
-                    int payload);
+                    int payload, bool swizzle128 = false);
 
 // number of SMs of the current device (cached per device)
 int sm_count();

@@ -72,7 +72,7 @@ bool make_key_tmap(CUtensorMap* m, const void* k, bool bf16, int64_t k_row_strid
 }
 
 bool make_key8_tmap(CUtensorMap* m, const int8_t* k, int64_t row_bytes, int64_t k_rows, int box_rows,
-                    int payload) {
+                    int payload, bool swizzle128) {
     EncodeFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)payload, (cuuint64_t)k_rows};
@@ -80,8 +80,8 @@ bool make_key8_tmap(CUtensorMap* m, const int8_t* k, int64_t row_bytes, int64_t 
     cuuint32_t box[2] = {(cuuint32_t)payload, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(k), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 
