@@ -64,10 +64,12 @@ CONFIG_LINES = ["decode_mla_8x8192", "prefill_mla_16384", "block_decode_gqa_16x3
 
 # DRAM bytes of the decode scorer per key from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum of one launch over 8 rows x 131072 keys, scaled to a launch by the keys
-# it scans), keyed by the SHA-256 of the kernel source it was taken on.  A source change makes
-# the figure stale and the bench reports traffic = null.
+# it scans), keyed by the SHA-256 of the kernel source it was taken on and the indexer cache (F16
+# rows or int8 codes + scale).  A source change makes the figure stale and the bench reports
+# traffic = null.
 NCU_TRAFFIC = {
-    "0d21b06a7972f2fe6cdd46e62cb9fcda8286991492e6ba4afc02edcf9a1a2c99": (268662784 + 4346112) / (8 * 131072),
+    ("be41d910d0faeb047ff57344c2b357cd8742db8d6dd9e7413861b008c6d82c37", "f16"): (268662784 + 4388352) / (8 * 131072),
+    ("be41d910d0faeb047ff57344c2b357cd8742db8d6dd9e7413861b008c6d82c37", "q8"): (138649344 + 3528960) / (8 * 131072),
 }
 
 
@@ -260,7 +262,7 @@ def rooflines(wl, step, ms, hbm, bf16, peak_kind):
         dk = wl.q_attn.shape[-1]
         nbytes = (n_keys * (wl.d * 2 + 4) + B * wl.H * (wl.d * q_bytes + 4) + sum(n_sel) * 4 +
                   sum(n_sel) * dk * 2 + B * wl.q_attn.shape[1] * (dk * 2 + wl.dv * out_bytes))
-        t = ms["score"] + ms["topk"] + ms["attention"]
+        t = ms["score"]   # the one call (select and attend are empty in this pipeline)
         r["step"] = hbm_line("sparse_decode_step (score + top-k + MLA attention, one launch)", nbytes, t)
         r["step"]["tensor_frac"] = (2.0 * n_keys * wl.H * wl.d + 2.0 * sum(n_sel) * wl.q_attn.shape[1] *
                                     (dk + wl.dv)) / (t * 1e-3) / 1e12 / bf16
@@ -300,7 +302,10 @@ def rooflines(wl, step, ms, hbm, bf16, peak_kind):
     else:
         Hkv = wl.k_attn.shape[1]
         nbytes = sum(n_sel) * Hkv * (dk + wl.dv) * 2 + B * Hq * (dk + wl.dv) * 2
-        r["attention"] = hbm_line("sparse_attn_decode (GQA, CUDA cores)", nbytes, ms["attention"])
+        tc = (str(wl.k_attn.dtype) in ("torch.float16", "torch.bfloat16") and dk == 128 and wl.dv == 128
+              and Hq % Hkv == 0 and Hq // Hkv <= 16)
+        r["attention"] = hbm_line("sparse_attn_decode (GQA, %s)" % ("tcgen05" if tc else "CUDA cores"), nbytes,
+                                  ms["attention"])
     if wl.hadamard:
         nbytes = 2 * (wl.q_idx.numel() + wl.k_idx.numel()) * wl.q_idx.element_size()
         r["hadamard"] = hbm_line("idx_hadamard (q and k)", nbytes, ms["hadamard"])
@@ -589,8 +594,8 @@ def main():
     rl, dom = rooflines(wl, step, ms, hbm, bf16, peak_kind)
     roofline = dict(rl[dom])
     src = os.path.join(ROOT, "lightning_indexer_top_gb300", "csrc", "k_score_tc.cu")
-    per_key = NCU_TRAFFIC.get(_sha(src)) if (dom == "score" and wl.k8 is None and wl.kind == "decode"
-                                              and wl.block_size <= 1) else None
+    per_key = (NCU_TRAFFIC.get((_sha(src), "f16" if wl.k8 is None else "q8"))
+               if (dom == "score" and wl.kind == "decode" and wl.block_size <= 1) else None)
     roofline["traffic"] = per_key * sum(wl.n_kv_host) if per_key is not None else None
     key_bytes = sum(wl.n_kv_host) * (wl.d * 2 if wl.k8 is None else wl.d + 4)
     value = job_value(ws, B, ms_step)
