@@ -73,7 +73,7 @@ static_assert(kPktOff + 2 * kPktStride <= kTailOff, "rank 1 layout");
 // another role gathers.
 constexpr int kThreads = 32 * LIDX_MLA_WARPS;
 constexpr int kProducerWarps = LIDX_MLA_WARPS - 5;      // warps 0 and 6..
-static_assert(kProducerWarps >= 1, "warp roles");
+static_assert(kProducerWarps >= 1 && LIDX_MLA_WARPS % 4 == 0, "warp roles; whole TMEM lane quarters");
 constexpr int kTmemCols = 512;
 constexpr int kSCol0 = 320;                             // rank 0: S buffers at 320 and 384 (Q at 0..287)
 constexpr float kRescaleLog2 = 8.f;
@@ -268,6 +268,7 @@ __device__ __forceinline__ void mla_stage_rows(const MlaSmem& sm, uint32_t rank,
     const int n_st = rank == 0 ? kThreads / 32 - 4 : kThreads / 32;
     const int si = rank == 0 && warp > 5 ? warp - 4 : warp;
     const int n_words = u.n_tiles * (kKeys / 32);
+    const int64_t row0 = g.page_table ? 0 : seq_row0(g, u.b);   // contiguous caches: read once
     constexpr int kBatch = 8;
     for (int w0 = si; w0 < n_words; w0 += kBatch * n_st) {
         int pos[kBatch];
@@ -284,7 +285,8 @@ __device__ __forceinline__ void mla_stage_rows(const MlaSmem& sm, uint32_t rank,
             bool valid = false;
             int64_t row = u.fallback;
             if (j < u.k1) {
-                const int64_t rr = (pos[k] >= 0 && pos[k] < u.n_kv) ? key_row(g, u.b, pos[k]) : -1;
+                const int64_t rr = (pos[k] >= 0 && pos[k] < u.n_kv)
+                                       ? (g.page_table ? key_row(g, u.b, pos[k]) : row0 + pos[k]) : -1;
                 if (rr >= 0 && rr < kv_rows) {
                     valid = true;
                     row = rr;
@@ -468,15 +470,13 @@ __device__ __forceinline__ void mla_run(const MlaSmem& sm, uint32_t tmem, uint32
             }
             __syncwarp();
         } else if (warp >= 2 && warp <= 5) {
-            // ---------------------------------------------------------- correction + output (thread = head)
+            // ---------------------------------------------------------- O correction (thread = head)
             const int h = quad * 32 + lane;
-            bool ok = true;
             for (int t = 0; t < u.n_tiles; ++t) {
                 const int j = t & 1;
                 const uint32_t ph = (uint32_t)((t >> 1) & 1);
                 if (warp_aborted(c) || !warp_wait_cluster(&c.pfull[j], ph)) {
                     abort_cta(c, g.status);
-                    ok = false;
                     break;
                 }
                 const PktTail& tail = *reinterpret_cast<const PktTail*>(pkts + j * kPktStride + kPBytes);
@@ -485,7 +485,6 @@ __device__ __forceinline__ void mla_run(const MlaSmem& sm, uint32_t tmem, uint32
                     const int tp = t - 1;
                     if (!warp_wait(&c.pvdone[tp & 1], (uint32_t)((tp >> 1) & 1))) {
                         abort_cta(c, g.status);
-                        ok = false;
                         break;
                     }
                     tc_fence_after();
@@ -504,71 +503,78 @@ __device__ __forceinline__ void mla_run(const MlaSmem& sm, uint32_t tmem, uint32
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&c.cdone[j]);
             }
-            float lsum = 0.f, mrow = 0.f;
-            const bool have = ok && u.n_tiles > 0;
-            if (have) {
-                const int tl = u.n_tiles - 1;
-                if (!warp_wait(&c.pvdone[tl & 1], (uint32_t)((tl >> 1) & 1))) {
-                    abort_cta(c, g.status);
+        }
+        // ------------------------------------------------------------------ output: every warp, three
+        // per TMEM lane quarter (thread = head), warp w taking the quarter's column blocks w/4, w/4 + 3, ...
+        const int h = quad * 32 + lane;
+        const int part = warp >> 2;
+        float lsum = 0.f, mrow = 0.f;
+        const bool have = u.n_tiles > 0 && !warp_aborted(c);
+        if (have) {
+            const int tl = u.n_tiles - 1;
+            if (!warp_wait(&c.pvdone[tl & 1], (uint32_t)((tl >> 1) & 1))) {
+                abort_cta(c, g.status);
+            } else {
+                tc_fence_after();
+                const PktTail& tail = *reinterpret_cast<const PktTail*>(pkts + (tl & 1) * kPktStride + kPBytes);
+                lsum = tail.l[h];
+                mrow = tail.m[h];
+            }
+        }
+        const bool read_o = have && !warp_aborted(c);
+        if (splits == 1) {
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            const int64_t base = (u.r * kHq + h) * (int64_t)kDv;
+            for (int cb = part; cb < kDv / 32; cb += kThreads / 128) {
+                float v[32];
+                if (read_o) {
+                    tmem_ld_32x32b_x32(tmem + lane_off + cb * 32, v);
+                    tmem_ld_wait();
                 } else {
-                    tc_fence_after();
-                    const PktTail& tail = *reinterpret_cast<const PktTail*>(pkts + (tl & 1) * kPktStride + kPBytes);
-                    lsum = tail.l[h];
-                    mrow = tail.m[h];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                }
+                if (out_dtype == IDX_BF16) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + base + cb * 32);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint4 pk;
+                        __nv_bfloat162 a0 = __floats2bfloat162_rn(v[8 * q4] * inv, v[8 * q4 + 1] * inv);
+                        __nv_bfloat162 a1 = __floats2bfloat162_rn(v[8 * q4 + 2] * inv, v[8 * q4 + 3] * inv);
+                        __nv_bfloat162 a2 = __floats2bfloat162_rn(v[8 * q4 + 4] * inv, v[8 * q4 + 5] * inv);
+                        __nv_bfloat162 a3 = __floats2bfloat162_rn(v[8 * q4 + 6] * inv, v[8 * q4 + 7] * inv);
+                        pk.x = *reinterpret_cast<uint32_t*>(&a0);
+                        pk.y = *reinterpret_cast<uint32_t*>(&a1);
+                        pk.z = *reinterpret_cast<uint32_t*>(&a2);
+                        pk.w = *reinterpret_cast<uint32_t*>(&a3);
+                        dst[q4] = pk;
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + base + cb * 32);
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        dst[q4] = make_float4(v[4 * q4] * inv, v[4 * q4 + 1] * inv, v[4 * q4 + 2] * inv,
+                                              v[4 * q4 + 3] * inv);
                 }
             }
-            const bool read_o = have && !warp_aborted(c);
-            if (splits == 1) {
-                const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-                const int64_t base = (u.r * kHq + h) * (int64_t)kDv;
-                for (int cb = 0; cb < kDv / 32; ++cb) {
-                    float v[32];
-                    if (read_o) {
-                        tmem_ld_32x32b_x32(tmem + lane_off + cb * 32, v);
-                        tmem_ld_wait();
-                    } else {
+        } else {
+            // partial O as [unit][column / 4][head][4]: for each 4 columns the warp's 32 heads are
+            // 512 contiguous bytes (one 16-byte store per head, coalesced across the warp)
+            float4* po = reinterpret_cast<float4*>(part_o + unit * (int64_t)kDv * kHq) + h;
+            for (int cb = part; cb < kDv / 32; cb += kThreads / 128) {
+                float v[32];
+                if (read_o) {
+                    tmem_ld_32x32b_x32(tmem + lane_off + cb * 32, v);
+                    tmem_ld_wait();
+                } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0.f;
-                    }
-                    if (out_dtype == IDX_BF16) {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + base + cb * 32);
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint4 pk;
-                            __nv_bfloat162 a0 = __floats2bfloat162_rn(v[8 * q4] * inv, v[8 * q4 + 1] * inv);
-                            __nv_bfloat162 a1 = __floats2bfloat162_rn(v[8 * q4 + 2] * inv, v[8 * q4 + 3] * inv);
-                            __nv_bfloat162 a2 = __floats2bfloat162_rn(v[8 * q4 + 4] * inv, v[8 * q4 + 5] * inv);
-                            __nv_bfloat162 a3 = __floats2bfloat162_rn(v[8 * q4 + 6] * inv, v[8 * q4 + 7] * inv);
-                            pk.x = *reinterpret_cast<uint32_t*>(&a0);
-                            pk.y = *reinterpret_cast<uint32_t*>(&a1);
-                            pk.z = *reinterpret_cast<uint32_t*>(&a2);
-                            pk.w = *reinterpret_cast<uint32_t*>(&a3);
-                            dst[q4] = pk;
-                        }
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + base + cb * 32);
-#pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4)
-                            dst[q4] = make_float4(v[4 * q4] * inv, v[4 * q4 + 1] * inv, v[4 * q4 + 2] * inv,
-                                                  v[4 * q4 + 3] * inv);
-                    }
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
                 }
-            } else {
-                // partial O as [unit][column][head]: for each column the warp's 32 heads are 128
-                // contiguous bytes (one store per column, coalesced across the warp)
-                float* po = part_o + unit * (int64_t)kDv * kHq + h;
-                for (int cb = 0; cb < kDv / 32; ++cb) {
-                    float v[32];
-                    if (read_o) {
-                        tmem_ld_32x32b_x32(tmem + lane_off + cb * 32, v);
-                        tmem_ld_wait();
-                    } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0.f;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) po[(int64_t)(cb * 32 + i) * kHq] = v[i];
-                }
+                for (int q4 = 0; q4 < 8; ++q4)
+                    po[(int64_t)(cb * 8 + q4) * kHq] = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+            }
+            if (part == 0) {
                 part_ml[(unit * kHq + h) * 2] = mrow;
                 part_ml[(unit * kHq + h) * 2 + 1] = read_o ? lsum : 0.f;
             }

@@ -58,7 +58,8 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* part_o,
                                                           void* __restrict__ out, int out_dtype) {
     pdl_trigger();
     pdl_wait();
-    // block (row, 4 columns), thread = head: the partials ([unit][column][head]) are read coalesced
+    // block (row, 4 columns), thread = head: the partials ([unit][column / 4][head][4]) are read
+    // coalesced, 16 bytes per head and split
     const int64_t r = blockIdx.x;
     const int c0 = blockIdx.y * 4;
     const int h = threadIdx.x;
@@ -81,9 +82,11 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const float* part_o,
             if (!(l > 0.f)) continue;
             const float wgt = exp2f(part_ml[(u * kHq + h) * 2] - M);
             den += wgt * l;
-            const float* o = part_o + (u * kDv + c0) * (int64_t)kHq + h;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] += wgt * o[i * kHq];
+            const float4 o = reinterpret_cast<const float4*>(part_o + u * (int64_t)kDv * kHq)[(c0 / 4) * kHq + h];
+            acc[0] += wgt * o.x;
+            acc[1] += wgt * o.y;
+            acc[2] += wgt * o.z;
+            acc[3] += wgt * o.w;
         }
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;

@@ -39,6 +39,7 @@
 // are then unspecified but every access stays in bounds), so the grid always
 // completes.
 #include <atomic>
+#include <cstring>
 #include <type_traits>
 
 #include "attn_mla_tc.cuh"
@@ -81,6 +82,9 @@ static_assert(2 * kThreads >= kFGroups, "two 32-key groups per thread cover a ro
 // after the attention unit's control block
 struct FCtl {
     uint64_t mma[2];               // phase 1: MMAs into accumulator a completed
+    uint64_t kfull[kFStages];      // phase 1: stage's key tile landed (tensor-map loads)
+    uint64_t accfree[2];           // phase 1: the epilogue warps have read accumulator a
+    int tdone[kFStages];           // phase 1: epilogue warps done with the stage's tile
     int n_pend;                    // rows this CTA completed (to select)
     int pend[kFusedMaxRows];
     int pre[kFusedMaxRows + 1];    // score tiles of the rows before row r
@@ -348,7 +352,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
     int64_t k_rows, Geom g, int top_k, float* scores, int64_t score_row_stride, int32_t* idx, int64_t idx_row_stride,
     int32_t* n_sel, const __nv_bfloat16* __restrict__ lat, int64_t lat_row_stride, int64_t kv_rows,
     const __nv_bfloat16* __restrict__ qa, float scale_log2, int splits, int kps, void* out, int out_dtype,
-    float* part_o, float* part_ml, uint32_t* ghist, int slot) {
+    float* part_o, float* part_ml, uint32_t* ghist, int slot, const __grid_constant__ CUtensorMap kmap,
+    int use_tma) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const MlaSmem sm = mla_smem(smem);
@@ -400,6 +405,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
             mla_init(c);
             mbar_init(&f.mma[0], 1);
             mbar_init(&f.mma[1], 1);
+            for (int i = 0; i < kFStages; ++i) mbar_init(&f.kfull[i], 1);
+            mbar_init(&f.accfree[0], 4);
+            mbar_init(&f.accfree[1], 4);
             fence_mbar_init();
         }
     }
@@ -429,9 +437,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
     const int G = (int)gridDim.x;
     const int my_n = total > (int)blockIdx.x ? (total - 1 - (int)blockIdx.x) / G + 1 : 0;
     const uint32_t acc_col0 = rank == 0 ? kFAccCol0 : kFAccCol1;
+    // row and tile of this CTA's i-th tile; `r` carries the row of an earlier call (tiles are
+    // visited in increasing order, so the search only moves forward)
     auto tile_row = [&](int i, int& r, int& t) {
         const int gt = (int)blockIdx.x + i * G;
-        r = 0;
         while (r + 1 < n_rows && f.pre[r + 1] <= gt) ++r;
         t = gt - f.pre[r];
     };
@@ -439,12 +448,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
     // the epilogue warps add to the histograms only once every CTA has zeroed its slice (checked
     // before a warp's first add, so the wait overlaps the first tiles' loads)
     int hist_state = 0;   // 0 not yet checked, 1 zeroed everywhere, -1 gave up waiting
+    int r_ld = 0, r_q = 0, r_ep = 0, r_pub = 0;   // running rows of the loops over this CTA's tiles
     for (int i0 = 0; i0 < my_n; i0 += kFStages) {
         const int nb = min(kFStages, my_n - i0);
-        // every tile of the batch: key rows by 16-byte copies (zero-filled past the allocation)...
-        for (int bt = 0; bt < nb; ++bt) {
-            int r, t;
-            tile_row(i0 + bt, r, t);
+        // every tile of the batch: the key rows of a contiguous cache by two tensor-map boxes of
+        // 64 columns x 128 rows (zero-filled past the allocation), of a paged one by 16-byte copies...
+        if (use_tma) {
+            if (threadIdx.x == 0) {
+                for (int bt = 0; bt < nb; ++bt) {
+                    int t;
+                    tile_row(i0 + bt, r_ld, t);
+                    const int r = r_ld;
+                    const int64_t krow = seq_row0(g, r) + (int64_t)t * kFK;
+                    if (krow < 0 || krow + min(f.nvis[r] - t * kFK, kFK) > k_rows)
+                        flag(g.status, IDX_ERR_DEVICE_BOUNDS);
+                    uint8_t* dst = smem + bt * kFStage;
+                    mbar_arrive_expect_tx(&f.kfull[bt], (uint32_t)(2 * kFKHalf));
+                    tma_load_2d(dst, &kmap, &f.kfull[bt], 0, (int32_t)krow);
+                    tma_load_2d(dst + kFKHalf, &kmap, &f.kfull[bt], 64, (int32_t)krow);
+                }
+            }
+        } else for (int bt = 0; bt < nb; ++bt) {
+            int t;
+            tile_row(i0 + bt, r_ld, t);
+            const int r = r_ld;
             const int nv = f.nvis[r];
             const uint32_t base = smem_u32(smem + bt * kFStage);
             const int64_t row0 = g.page_table ? 0 : seq_row0(g, r);   // read once per tile
@@ -470,8 +497,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
 #pragma unroll
             for (int bt = 0; bt < kFStages; ++bt) {
                 if (bt >= nb) break;
-                int r, t;
-                tile_row(i0 + bt, r, t);
+                int t;
+                tile_row(i0 + bt, r_q, t);
+                const int r = r_q;
 #pragma unroll
                 for (int k = 0; k < kPer; ++k) {
                     const int ch = threadIdx.x + k * kThreads;
@@ -517,42 +545,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
         }
         cp_async_wait_group<0>();
         fence_proxy_async_smem();   // this thread's copies and q stores before the MMAs read them
+        if (threadIdx.x < kFStages) f.tdone[threadIdx.x] = 0;
         __syncthreads();
-        // tile bt's MMAs go to accumulator (i0 + bt) & 1; tile bt+1's are issued before tile bt's
-        // epilogue, whose accumulator the other one is
-        auto issue = [&](int bt) {
-            const int k = i0 + bt;
-            const uint32_t a0 = smem_u32(smem + bt * kFStage), b0 = a0 + 2 * kFKHalf;
-            tc_fence_after();
+        // Roles within the batch, with no CTA barrier per tile: warp 1 issues tile bt's MMAs into
+        // accumulator k & 1 (k = i0 + bt) once its keys have landed and the epilogue of tile k-2
+        // has read that accumulator; warps 4..7 run the epilogues; warp 2 publishes each finished
+        // tile to its row's counter (the selector starts when a row's last tile is counted).
+        if (warp == 1) {
+            if (lane == 0) {
+                for (int bt = 0; bt < nb; ++bt) {
+                    const int k = i0 + bt;
+                    if (use_tma && !mbar_wait(&f.kfull[bt], (uint32_t)((i0 / kFStages) & 1)))
+                        flag(g.status, IDX_ERR_TIMEOUT);
+                    if (k >= 2 && !mbar_wait(&f.accfree[k & 1], (uint32_t)(((k - 2) >> 1) & 1)))
+                        flag(g.status, IDX_ERR_TIMEOUT);
+                    const uint32_t a0 = smem_u32(smem + bt * kFStage), b0 = a0 + 2 * kFKHalf;
+                    tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < kFD / 16; ++kk) {
-                const uint32_t off = (kk & 3) * 32;
-                const uint64_t ad = desc_sw128_kmajor(a0 + (kk >> 2) * kFKHalf + off, 1024);
-                const uint64_t bd = desc_sw128_kmajor(b0 + (kk >> 2) * kFQHalf + off, 1024);
-                mma_f16_ss(tmem + acc_col0 + (k & 1) * kFH, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < kFD / 16; ++kk) {
+                        const uint32_t off = (kk & 3) * 32;
+                        const uint64_t ad = desc_sw128_kmajor(a0 + (kk >> 2) * kFKHalf + off, 1024);
+                        const uint64_t bd = desc_sw128_kmajor(b0 + (kk >> 2) * kFQHalf + off, 1024);
+                        mma_f16_ss(tmem + acc_col0 + (k & 1) * kFH, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&f.mma[k & 1]);
+                }
             }
-            mma_commit(&f.mma[k & 1]);
-        };
-        if (warp == 1 && lane == 0) issue(0);
-        for (int bt = 0; bt < nb; ++bt) {
-            const int k = i0 + bt;
-            int r, t;
-            tile_row(k, r, t);
-            if (warp == 1 && lane == 0 && bt + 1 < nb) issue(bt + 1);
-            if (warp >= 4 && warp < 8) {
+            __syncwarp();
+        } else if (warp >= 4 && warp < 8) {
+            for (int bt = 0; bt < nb; ++bt) {
+                const int k = i0 + bt;
+                int t;
+                tile_row(k, r_ep, t);
+                const int r = r_ep;
                 // epilogue (thread = key = TMEM lane): sum_h w_h relu(D_h) in idx_score's order
                 const int quad = warp & 3;
                 const int j = t * kFK + quad * 32 + lane;
                 const int nv = f.nvis[r];
-                if (!warp_wait(&f.mma[k & 1], (uint32_t)((k >> 1) & 1))) {
-                    if (lane == 0) flag(g.status, IDX_ERR_TIMEOUT);
-                } else {
+                const bool ok = warp_wait(&f.mma[k & 1], (uint32_t)((k >> 1) & 1));
+                float v0[32], v1[32];
+                if (ok) {
                     tc_fence_after();
-                    float v0[32], v1[32];
                     const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + acc_col0 + (k & 1) * kFH;
                     tmem_ld_32x32b_x32(ta, v0);
                     tmem_ld_32x32b_x32(ta + 32, v1);
                     tmem_ld_wait();
+                } else if (lane == 0) {
+                    flag(g.status, IDX_ERR_TIMEOUT);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&f.accfree[k & 1]);   // the accumulator may be reused
+                if (ok) {
                     const float* wv = reinterpret_cast<const float*>(smem + kFWOff) + bt * kFH;
                     float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
@@ -571,23 +615,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
                         hist_state = __shfl_sync(0xffffffffu, ready, 0) ? 1 : -1;
                         if (hist_state < 0 && lane == 0) flag(g.status, IDX_ERR_TIMEOUT);
                     }
-                    if (hist_state > 0) {
-                        // equal bins of the warp folded into one add
-                        const uint32_t bin = j < nv ? order_key(sc) >> 21 : 0xffffffffu;
-                        const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-                        if (j < nv && lane == __ffs(peers) - 1)
-                            atomicAdd(&ghist[(int64_t)r * 2048 + bin], (uint32_t)__popc(peers));
-                    }
+                    if (hist_state > 0 && j < nv) atomicAdd(&ghist[(int64_t)r * 2048 + (order_key(sc) >> 21)], 1u);
+                }
+                __syncwarp();
+                if (lane == 0) {   // the warp's scores and counts before its count of the tile
+                    __threadfence_block();
+                    atomicAdd(&f.tdone[bt], 1);
                 }
             }
-            tc_fence_before();
-            __syncthreads();   // scores and counts written, accumulator k & 1 free
-            if (threadIdx.x == 0) {   // the row's selector starts as soon as its last tile is counted
-                __threadfence();
-                atomicAdd(&row_cnt[r], 1u);
+        } else if (warp == 2) {
+            if (lane == 0) {
+                for (int bt = 0; bt < nb; ++bt) {
+                    int t;
+                    tile_row(i0 + bt, r_pub, t);
+                    const int r = r_pub;
+                    const long long c0 = clock64();
+                    while (*reinterpret_cast<volatile int*>(&f.tdone[bt]) < 4) {
+                        if (clock64() - c0 > kWaitCycles) {
+                            flag(g.status, IDX_ERR_TIMEOUT);
+                            break;
+                        }
+                    }
+                    __threadfence();   // the epilogue warps' scores and counts, then the count
+                    atomicAdd(&row_cnt[r], 1u);
+                }
             }
+            __syncwarp();
         }
-        __syncthreads();   // the batch's stages free
+        tc_fence_before();
+        __syncthreads();   // the batch's stages and both accumulators free
+        tc_fence_after();
     }
     // (a row whose counts are incomplete - a CTA that gave up waiting for the zeroing - has a
     // histogram total below its key count, and its select counts the keys itself)
@@ -634,60 +691,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
             __threadfence();
         }
         __syncthreads();
-        // work item (row, 4 columns), thread = head (the combine kernel's layout and arithmetic)
+        // work item (row, 4 columns), thread = head (the combine kernel's layout and arithmetic); a
+        // thread group takes two items at a time, all of their loads issued together
         const int grp = threadIdx.x >> 7, h = threadIdx.x & 127;
         const int64_t items = (int64_t)n_rows * (kDv / 4);
-        for (int64_t p = (int64_t)blockIdx.x * (kThreads / 128) + grp; p < items;
-             p += (int64_t)gridDim.x * (kThreads / 128)) {
-            const int64_t r = p / (kDv / 4);
-            const int c0 = (int)(p % (kDv / 4)) * 4;
-            // the (m, l) and the 4 columns of every split, loads issued together
-            float ml_m[kFMaxSplits], ml_l[kFMaxSplits], o[kFMaxSplits][4];
+        const int64_t gs = (int64_t)gridDim.x * (kThreads / 128);   // thread groups in the grid
+        for (int64_t p0 = (int64_t)blockIdx.x * (kThreads / 128) + grp; p0 < items; p0 += 2 * gs) {
+            float ml_m[2][kFMaxSplits], ml_l[2][kFMaxSplits];
+            float4 o[2][kFMaxSplits];
 #pragma unroll
-            for (int s = 0; s < kFMaxSplits; ++s) {
-                ml_m[s] = 0.f;
-                ml_l[s] = 0.f;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) o[s][i] = 0.f;
-                if (s < splits) {
-                    const int64_t un = r * splits + s;
-                    ml_m[s] = __ldcg(part_ml + (un * kHq + h) * 2);
-                    ml_l[s] = __ldcg(part_ml + (un * kHq + h) * 2 + 1);
-                    const float* src = part_o + (un * kDv + c0) * (int64_t)kHq + h;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) o[s][i] = __ldcg(src + i * kHq);
-                }
-            }
-            float M = -3.0e38f;
-            bool any = false;
-#pragma unroll
-            for (int s = 0; s < kFMaxSplits; ++s) {
-                if (s < splits && ml_l[s] > 0.f) {
-                    M = fmaxf(M, ml_m[s]);
-                    any = true;
-                }
-            }
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            float den = 0.f;
-            if (any) {
+            for (int k = 0; k < 2; ++k) {
+                const int64_t p = p0 + k * gs;
+                const int64_t r = p / (kDv / 4);
+                const int c4 = (int)(p % (kDv / 4));
 #pragma unroll
                 for (int s = 0; s < kFMaxSplits; ++s) {
-                    if (s >= splits || !(ml_l[s] > 0.f)) continue;
-                    const float wgt = exp2f(ml_m[s] - M);
-                    den += wgt * ml_l[s];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[i] += wgt * o[s][i];
+                    ml_m[k][s] = 0.f;
+                    ml_l[k][s] = 0.f;
+                    o[k][s] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (p < items && s < splits) {
+                        const int64_t un = r * splits + s;
+                        ml_m[k][s] = __ldcg(part_ml + (un * kHq + h) * 2);
+                        ml_l[k][s] = __ldcg(part_ml + (un * kHq + h) * 2 + 1);
+                        o[k][s] = __ldcg(reinterpret_cast<const float4*>(part_o + un * (int64_t)kDv * kHq) +
+                                         (int64_t)c4 * kHq + h);
+                    }
                 }
             }
-            const float inv = den > 0.f ? 1.f / den : 0.f;
-            const int64_t base = (r * kHq + h) * (int64_t)kDv + c0;
-            if (out_dtype == IDX_BF16) {
-                __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out) + base;
-                *reinterpret_cast<__nv_bfloat162*>(ob) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-                *reinterpret_cast<__nv_bfloat162*>(ob + 2) = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
-            } else {
-                *reinterpret_cast<float4*>(static_cast<float*>(out) + base) =
-                    make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int64_t p = p0 + k * gs;
+                if (p >= items) continue;
+                const int64_t r = p / (kDv / 4);
+                const int c0 = (int)(p % (kDv / 4)) * 4;
+                float M = -3.0e38f;
+                bool any = false;
+#pragma unroll
+                for (int s = 0; s < kFMaxSplits; ++s) {
+                    if (s < splits && ml_l[k][s] > 0.f) {
+                        M = fmaxf(M, ml_m[k][s]);
+                        any = true;
+                    }
+                }
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                float den = 0.f;
+                if (any) {
+#pragma unroll
+                    for (int s = 0; s < kFMaxSplits; ++s) {
+                        if (s >= splits || !(ml_l[k][s] > 0.f)) continue;
+                        const float wgt = exp2f(ml_m[k][s] - M);
+                        den += wgt * ml_l[k][s];
+                        acc[0] += wgt * o[k][s].x;
+                        acc[1] += wgt * o[k][s].y;
+                        acc[2] += wgt * o[k][s].z;
+                        acc[3] += wgt * o[k][s].w;
+                    }
+                }
+                const float inv = den > 0.f ? 1.f / den : 0.f;
+                const int64_t base = (r * kHq + h) * (int64_t)kDv + c0;
+                if (out_dtype == IDX_BF16) {
+                    __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out) + base;
+                    *reinterpret_cast<__nv_bfloat162*>(ob) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+                    *reinterpret_cast<__nv_bfloat162*>(ob + 2) = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+                } else {
+                    *reinterpret_cast<float4*>(static_cast<float*>(out) + base) =
+                        make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+                }
             }
         }
     }
@@ -731,11 +800,16 @@ cudaError_t launch_fused_t(const void* qi, const float* w, const void* k, int64_
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const float scale_log2 = scale * 1.4426950408889634f;
+    // contiguous caches: key tiles by tensor-map loads (rows addressable by a 32-bit coordinate)
+    CUtensorMap kmap;
+    memset(&kmap, 0, sizeof(kmap));
+    const int use_tma = !g.page_table && k_rows < (int64_t)INT32_MAX &&
+                        make_key_tmap(&kmap, k, std::is_same<TK, __nv_bfloat16>::value, k_row_stride, k_rows, kFK);
     return cudaLaunchKernelEx(&cfg, kern, static_cast<const TQ*>(qi), w, static_cast<const TK*>(k), k_row_stride,
                               k_rows, g, top_k, scores, score_row_stride, idx, idx_row_stride, n_sel,
                               static_cast<const __nv_bfloat16*>(lat), lat_row_stride, kv_rows,
                               static_cast<const __nv_bfloat16*>(qa), scale_log2, splits, kps, out, out_dtype, part_o,
-                              part_ml, ghist, slot);
+                              part_ml, ghist, slot, kmap, use_tma);
 }
 
 }  // namespace
