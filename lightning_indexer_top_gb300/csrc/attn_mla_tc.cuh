@@ -72,8 +72,12 @@ static_assert(kPktOff + 2 * kPktStride <= kTailOff, "rank 1 layout");
 // 8 and ~40 GB/s with 16 (about HBM speed over all SMs), so every warp without
 // another role gathers.
 constexpr int kThreads = 32 * LIDX_MLA_WARPS;
-constexpr int kProducerWarps = LIDX_MLA_WARPS - 5;      // warps 0 and 6..
-static_assert(kProducerWarps >= 1 && LIDX_MLA_WARPS % 4 == 0, "warp roles; whole TMEM lane quarters");
+// Warp roles: 1 issues the MMAs, 2..5 (one per TMEM lane quarter) run the softmax (rank 0) or the
+// O correction (rank 1), 0 and 6.. gather, except warp 9, which shares warp 1's scheduler: a busy
+// third warp there slows the MMA issue (the tensor pipe then idles between instructions).
+constexpr int kProducerWarps = LIDX_MLA_WARPS - 6;      // warps 0, 6..8, 10..
+static_assert(kProducerWarps >= 1 && LIDX_MLA_WARPS >= 10 && LIDX_MLA_WARPS % 4 == 0,
+              "warp roles; whole TMEM lane quarters");
 constexpr int kTmemCols = 512;
 constexpr int kSCol0 = 320;                             // rank 0: S buffers at 320 and 384 (Q at 0..287)
 constexpr float kRescaleLog2 = 8.f;
@@ -167,12 +171,17 @@ __device__ __forceinline__ void gather_tiles(Ctl& c, uint8_t* xtiles, const __nv
         }
         const uint32_t dst0 = smem_u32(xtiles + (size_t)stage * kStageBytes);
         const int32_t* rr = rows_s + t * kKeys;
-#pragma unroll 4
-        for (int i = p * 32 + lane; i < kKeys * kChunks; i += 32 * kProducerWarps) {
-            const int row = i / kChunks, cc = i - row * kChunks;
-            const char* src = base + (int64_t)rr[row] * row_bytes + cc * 16;
-            const uint32_t dst = dst0 + (cc >> 3) * kBlockBytes + row * 128 + (((cc & 7) ^ (row & 7)) << 4);
-            cp_async16(dst, src);
+        // warp p copies rows p, p + kProducerWarps, ...; lane l the 16-byte chunks l, l + 32, l + 64 of
+        // each (a warp instruction covers 512 contiguous bytes of a row; the swizzle XORs bits 4-6)
+#pragma unroll 2
+        for (int row = p; row < kKeys; row += kProducerWarps) {
+            const char* src = base + (int64_t)rr[row] * row_bytes;
+            const uint32_t rb = dst0 + row * 128, x = (uint32_t)(row & 7) << 4;
+#pragma unroll
+            for (int k = 0; k < (kChunks + 31) / 32; ++k) {
+                const int cc = lane + 32 * k;
+                if (cc < kChunks) cp_async16(rb + ((uint32_t)((cc >> 3) * kBlockBytes + ((cc & 7) << 4)) ^ x), src + cc * 16);
+            }
         }
         cp_async_mbar_arrive_noinc(&c.xfull[stage]);
     }
@@ -315,7 +324,7 @@ __device__ __forceinline__ void mla_run(const MlaSmem& sm, uint32_t tmem, uint32
     const int32_t* rows_s = sm.rows_s;
     const uint32_t* vmask = sm.vmask;
     Ctl& c = *sm.c;
-    const int producer = warp == 0 ? 0 : (warp >= 6 ? warp - 5 : -1);   // producer index or -1
+    const int producer = warp == 0 ? 0 : (warp >= 6 && warp != 9 ? warp - (warp > 9 ? 6 : 5) : -1);   // index or -1
     if (rank == 0) {
         if (producer >= 0) {
             gather_tiles<kDkBlocks * 8, kStagesK, kKTileBytes>(c, xtiles, lat, lat_row_stride, u, rows_s, producer,
@@ -374,13 +383,27 @@ __device__ __forceinline__ void mla_run(const MlaSmem& sm, uint32_t tmem, uint32
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&c.sempty[sb]);
 
+                // the tile's largest scaled logit: for a full tile and a positive scale, the scaled
+                // largest logit (the same value: rounding a product by a positive factor is monotone)
+                const bool full = (ma & mb) == 0xffffffffu;
                 float mt = -3.0e38f;
+                if (full && scale_log2 > 0.f) {
+                    float a0 = fmaxf(s0[0], s0[1]), a1 = fmaxf(s0[2], s0[3]);
+                    float a2 = fmaxf(s1[0], s1[1]), a3 = fmaxf(s1[2], s1[3]);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    s0[i] *= scale_log2;
-                    s1[i] *= scale_log2;
-                    if ((ma >> i) & 1u) mt = fmaxf(mt, s0[i]);
-                    if ((mb >> i) & 1u) mt = fmaxf(mt, s1[i]);
+                    for (int i = 4; i < 32; i += 4) {
+                        a0 = fmaxf(a0, fmaxf(s0[i], s0[i + 1]));
+                        a1 = fmaxf(a1, fmaxf(s0[i + 2], s0[i + 3]));
+                        a2 = fmaxf(a2, fmaxf(s1[i], s1[i + 1]));
+                        a3 = fmaxf(a3, fmaxf(s1[i + 2], s1[i + 3]));
+                    }
+                    mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * scale_log2;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        if ((ma >> i) & 1u) mt = fmaxf(mt, s0[i] * scale_log2);
+                        if ((mb >> i) & 1u) mt = fmaxf(mt, s1[i] * scale_log2);
+                    }
                 }
                 float alpha = 1.f;
                 if ((ma | mb) != 0u) {
@@ -393,14 +416,21 @@ __device__ __forceinline__ void mla_run(const MlaSmem& sm, uint32_t tmem, uint32
                         m_used = mt;
                     }
                 }
+                // p = 2^(s * scale_log2 - m) with one rounding of the exponent's argument (FMA)
                 uint32_t pk[32];
                 float psum = 0.f;
+                const float nm = -m_used;
+                const uint32_t ka = full ? 0xffffffffu : ma, kb = full ? 0xffffffffu : mb;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ((ma >> (2 * i)) & 1u) ? ex2_approx(s0[2 * i] - m_used) : 0.f;
-                    const float p1 = ((ma >> (2 * i + 1)) & 1u) ? ex2_approx(s0[2 * i + 1] - m_used) : 0.f;
-                    const float p2 = ((mb >> (2 * i)) & 1u) ? ex2_approx(s1[2 * i] - m_used) : 0.f;
-                    const float p3 = ((mb >> (2 * i + 1)) & 1u) ? ex2_approx(s1[2 * i + 1] - m_used) : 0.f;
+                    const float e0 = ex2_approx(fmaf(s0[2 * i], scale_log2, nm));
+                    const float e1 = ex2_approx(fmaf(s0[2 * i + 1], scale_log2, nm));
+                    const float e2 = ex2_approx(fmaf(s1[2 * i], scale_log2, nm));
+                    const float e3 = ex2_approx(fmaf(s1[2 * i + 1], scale_log2, nm));
+                    const float p0 = ((ka >> (2 * i)) & 1u) ? e0 : 0.f;
+                    const float p1 = ((ka >> (2 * i + 1)) & 1u) ? e1 : 0.f;
+                    const float p2 = ((kb >> (2 * i)) & 1u) ? e2 : 0.f;
+                    const float p3 = ((kb >> (2 * i + 1)) & 1u) ? e3 : 0.f;
                     psum += (p0 + p1) + (p2 + p3);
                     const __nv_bfloat162 a = __floats2bfloat162_rn(p0, p1);
                     const __nv_bfloat162 bb = __floats2bfloat162_rn(p2, p3);
@@ -511,8 +541,11 @@ __device__ __forceinline__ void mla_run(const MlaSmem& sm, uint32_t tmem, uint32
         float lsum = 0.f, mrow = 0.f;
         const bool have = u.n_tiles > 0 && !warp_aborted(c);
         if (have) {
+            // every PV MMA of the unit completed: `done` completes once per unit, so a warp that
+            // arrives here early (a producer) cannot mistake an older phase for it, as it could
+            // with the per-packet barriers
             const int tl = u.n_tiles - 1;
-            if (!warp_wait(&c.pvdone[tl & 1], (uint32_t)((tl >> 1) & 1))) {
+            if (!warp_wait(&c.done, 0u)) {
                 abort_cta(c, g.status);
             } else {
                 tc_fence_after();
