@@ -842,18 +842,57 @@ __global__ void __launch_bounds__(kMcThreads) topk_mc_filter_kernel(const float*
     mc_filter_range(scores + r * score_row_stride, c0, min(n, c0 + kMcChunk), L.bound[r], L, r, buf, nbuf, base);
 }
 
-// Fused path: the scorer counted each row's order keys by their top 11 bits, and the bound kernel
-// derived from that exact histogram the bin b* holding the K-th largest key, with the count above
-// it (L.bound[r] = b* << 21 | above).  Every key in a higher bin is selected and only the keys of b*
+// Fused path: the scorer counted each row's order keys by their top 11 bits; each filter CTA derives
+// from that exact histogram the bin b* holding the K-th largest key, with the count above it
+// (L.bound[r] = b* << 21 | above, recorded by the row's first CTA for the finish kernel).  Every key in a higher bin is selected and only the keys of b*
 // remain to be ranked, so the filter keeps the keys with bin >= b* (above + hist[b*] of them) and
 // the finish kernel resolves b*.  A bound of ~0 (the histogram was not exact: its launch could not
 // count, see the scorer) makes every key a candidate; the list overflows and the finish takes the
 // general path.
+// the bound of row r from its histogram (as topk_hist_bound computes it) to every thread of a
+// kMcThreads CTA: thread t owns bins [2047 - 8t - 7, 2047 - 8t]
+__device__ __forceinline__ uint32_t hist_bound(const uint32_t* hrow, int n, int K, uint32_t* scratch, uint32_t* sb) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const uint4* h4 = reinterpret_cast<const uint4*>(hrow + 2040 - 8 * threadIdx.x);
+    const uint4 lo4 = h4[0], hi4 = h4[1];
+    const uint32_t bins[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};   // from the top
+    uint32_t local = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) local += bins[i];
+    uint32_t x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[wid] = x;
+    if (threadIdx.x == 0) *sb = 0xffffffffu;
+    __syncthreads();
+    uint32_t before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kMcThreads / 32; ++w) {
+        before += w < wid ? scratch[w] : 0u;
+        total += scratch[w];
+    }
+    uint32_t c = before + x - local;
+    if (total == (uint32_t)n) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (c < (uint32_t)K && (uint32_t)K <= c + bins[i]) *sb = ((uint32_t)(2047 - 8 * threadIdx.x - i) << 21) | c;
+            c += bins[i];
+        }
+    }
+    __syncthreads();
+    return *sb;
+}
+
 __global__ void __launch_bounds__(kMcThreads) topk_hist_filter_kernel(const float* scores,
-                                                                      int64_t score_row_stride, Geom g, int top_k,
+                                                                      int64_t score_row_stride,
+                                                                      const uint32_t* hist, Geom g, int top_k,
                                                                       McLayout L, int chunk) {
     __shared__ uint64_t buf[kMcLocal];
     __shared__ uint32_t nbuf, base;
+    __shared__ uint32_t scratch[kMcThreads / 32], sbound;
     pdl_trigger();
     pdl_wait();
     const int64_t r = blockIdx.y;
@@ -861,30 +900,44 @@ __global__ void __launch_bounds__(kMcThreads) topk_hist_filter_kernel(const floa
     const int K = min(top_k, n);
     const int c0 = blockIdx.x * chunk;
     if (K == n || c0 >= n) return;
-    const uint32_t b = L.bound[r];
-    const uint32_t lo = b == 0xffffffffu ? 0u : (b & 0xffe00000u);
     const float* s = scores + r * score_row_stride;
     const int c1 = min(n, c0 + chunk);
-    if (((reinterpret_cast<uintptr_t>(s) | (uint32_t)c0) & 15u) != 0) {
+    const bool aligned = ((reinterpret_cast<uintptr_t>(s) | (uint32_t)c0) & 15u) == 0;
+    // the first pass's 16-byte loads are issued before the row's bound is derived from its histogram
+    // (every CTA of the row derives it; the first records it for the finish kernel)
+    constexpr int kV = 4;                     // float4s per thread per pass
+    float4 v[kV];
+    if (aligned) {
+#pragma unroll
+        for (int b = 0; b < kV; ++b) {
+            const int j = c0 + (b * kMcThreads + threadIdx.x) * 4;
+            v[b] = j + 3 < c1 ? *reinterpret_cast<const float4*>(s + j)
+                              : make_float4(j < c1 ? s[j] : 0.f, j + 1 < c1 ? s[j + 1] : 0.f,
+                                            j + 2 < c1 ? s[j + 2] : 0.f, 0.f);
+        }
+    }
+    if (threadIdx.x == 0) nbuf = 0u;
+    const uint32_t b = hist_bound(hist + r * 2048, n, K, scratch, &sbound);   // (synchronises)
+    if (blockIdx.x == 0 && threadIdx.x == 0) L.bound[r] = b;
+    const uint32_t lo = b == 0xffffffffu ? 0u : (b & 0xffe00000u);
+    if (!aligned) {
         mc_filter_range(s, c0, c1, lo, L, r, buf, nbuf, base);
         return;
     }
     // 16-byte loads: thread t takes the float4s t, t + 256, ... of the chunk, all issued at once; each
     // thread marks its hits in a bit mask, one warp scan places them, one shared atomic per warp
-    if (threadIdx.x == 0) nbuf = 0u;
-    __syncthreads();
     const int lane = threadIdx.x & 31;
     uint32_t* cnt = L.cnt + r;
     uint64_t* cand = L.cand + r * (int64_t)kMcCandCap;
-    constexpr int kV = 4;                     // float4s per thread per pass
     for (int j0 = c0; j0 < c1; j0 += kMcThreads * 4 * kV) {
-        float4 v[kV];
+        if (j0 > c0) {
 #pragma unroll
-        for (int b = 0; b < kV; ++b) {
-            const int j = j0 + (b * kMcThreads + threadIdx.x) * 4;
-            v[b] = j + 3 < c1 ? *reinterpret_cast<const float4*>(s + j)
-                              : make_float4(j < c1 ? s[j] : 0.f, j + 1 < c1 ? s[j + 1] : 0.f,
-                                            j + 2 < c1 ? s[j + 2] : 0.f, 0.f);
+            for (int b = 0; b < kV; ++b) {
+                const int j = j0 + (b * kMcThreads + threadIdx.x) * 4;
+                v[b] = j + 3 < c1 ? *reinterpret_cast<const float4*>(s + j)
+                                  : make_float4(j < c1 ? s[j] : 0.f, j + 1 < c1 ? s[j + 1] : 0.f,
+                                                j + 2 < c1 ? s[j + 2] : 0.f, 0.f);
+            }
         }
         uint32_t keys[4 * kV];
         uint32_t hits = 0;
@@ -1082,59 +1135,10 @@ FusedArrays topk_fused_arrays(void* ws, int64_t n_rows) {
     return a;
 }
 
-// One CTA per row: from the row's exact histogram of order-key top-11-bit bins, the bin b* that
-// holds the K-th largest key and the count above it: L.bound[r] = b* << 21 | above (K <= 2^21).
-// A histogram whose total is not the row's key count (its launch could not count, see the scorer)
-// gives ~0.  256 threads, 8 bins each, walked from the top.
-__global__ void __launch_bounds__(kMcThreads) topk_hist_bound_kernel(const uint32_t* hist, Geom g, int top_k,
-                                                                     McLayout L) {
-    __shared__ uint32_t scratch[kMcThreads / 32];
-    __shared__ uint32_t sb[3];
-    pdl_trigger();
-    pdl_wait();
-    const int64_t r = blockIdx.x;
-    const int n = row_n_vis(g, r);
-    const int K = min(top_k, n);
-    if (K == n) return;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    // thread t owns bins [2047 - 8t - 7, 2047 - 8t]
-    const uint4* h4 = reinterpret_cast<const uint4*>(hist + r * 2048 + 2040 - 8 * threadIdx.x);
-    const uint4 lo4 = h4[0], hi4 = h4[1];
-    const uint32_t bins[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};   // from the top
-    uint32_t local = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) local += bins[i];
-    uint32_t x = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) scratch[wid] = x;
-    if (threadIdx.x == 0) sb[0] = 0xffffffffu;
-    __syncthreads();
-    uint32_t before = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < kMcThreads / 32; ++w) {
-        before += w < wid ? scratch[w] : 0u;
-        total += scratch[w];
-    }
-    uint32_t c = before + x - local;
-    if (total == (uint32_t)n) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if (c < (uint32_t)K && (uint32_t)K <= c + bins[i]) sb[0] = ((uint32_t)(2047 - 8 * threadIdx.x - i) << 21) | c;
-            c += bins[i];
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) L.bound[r] = sb[0];
-}
-
 // Rows up to kFusedMapMax keys: one CTA per row (topk_map_kernel seeded with the row's histogram:
 // one pass over the scores, which the scorer left in L2, marks the keys above the threshold bin
-// and collects that bin's keys, ranked in shared memory).  Longer rows: the bound kernel, then
-// the filter over all SMs, then the finish (one SM streaming a 131072-key row is slower than the
+// and collects that bin's keys, ranked in shared memory).  Longer rows: the filter over all SMs
+// (each CTA derives the row's bound from the histogram first), then the finish (one SM streaming a 131072-key row is slower than the
 // two extra launches).
 constexpr int kFusedMapMax = 16384;
 
@@ -1149,16 +1153,14 @@ cudaError_t launch_topk_fused(const float* scores, int64_t score_row_stride, con
                           score_row_stride, g, top_k, idx, idx_row_stride, n_sel, static_cast<const uint32_t*>(ws));
     }
     const McLayout L = fused_mc(ws, n_rows);
-    cudaError_t e = launch_pdl(topk_hist_bound_kernel, dim3((unsigned)n_rows), dim3(kMcThreads), 0, st,
-                               static_cast<const uint32_t*>(ws), g, top_k, L);
-    if (e != cudaSuccess) return e;
     // filter chunks of 8192 scores (two passes of four 16-byte loads per thread), longer when a
     // batch would need more than 2048 CTAs
     int64_t chunk = 8192;
     while ((g.max_n_kv + chunk - 1) / chunk * n_rows > 2048 && chunk < (1 << 20)) chunk *= 2;
     const int64_t chunks = (g.max_n_kv + chunk - 1) / chunk;
-    e = launch_pdl(topk_hist_filter_kernel, dim3((unsigned)chunks, (unsigned)n_rows), dim3(kMcThreads), 0, st,
-                   scores, score_row_stride, g, top_k, L, (int)chunk);
+    cudaError_t e = launch_pdl(topk_hist_filter_kernel, dim3((unsigned)chunks, (unsigned)n_rows), dim3(kMcThreads),
+                               0, st, scores, score_row_stride, static_cast<const uint32_t*>(ws), g, top_k, L,
+                               (int)chunk);
     if (e != cudaSuccess) return e;
     cudaFuncSetAttribute(topk_mc_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     return launch_pdl(topk_mc_finish_kernel, dim3((unsigned)n_rows), dim3(kMapThreads), sm, st, scores,
