@@ -43,6 +43,7 @@
 #include <type_traits>
 
 #include "attn_mla_tc.cuh"
+#include "select_row.cuh"
 
 namespace lidx {
 
@@ -63,21 +64,13 @@ constexpr int kFKHalf = kFK * 128;                // one 64-column block of a ke
 constexpr int kFQHalf = kFH * 128;                // one 64-column block of q (8 KB)
 constexpr int kFStage = 2 * kFKHalf + 2 * kFQHalf;   // 48 KB
 constexpr int kFStages = 4;                       // score tiles in flight per CTA
-constexpr int kFSelMax = 16384;                   // keys a row may have
 constexpr int kFMaxSplits = 8;                    // key splits the merge handles
 constexpr int kFWOff = kFStages * kFStage;        // weights of the stages [kFStages][64]
-constexpr int kFSelOff = 0;                       // select (after phase 1): order keys [kFSelMax]
-constexpr int kFHistOff = kFSelOff + kFSelMax * 4;   // select: histograms of the three rounds [2048 + 2048 + 1024]
-constexpr int kFGroups = kFSelMax / 32;              // select: 32-key groups of a row
-constexpr int kFBitsOff = kFHistOff + 5120 * 4;      // select: per group, the selected and the equal keys' bits
-constexpr int kFSelScratch = kFBitsOff + 2 * kFGroups * 4;   // select: scan and bin-search slots [6][32]
 // score accumulators (two, used in turn): rank 0 in its S columns (Q at 0..287; S is used only in
 // phase 3), rank 1 in its O columns (written only in phase 3)
 constexpr uint32_t kFAccCol0 = 384;
 constexpr uint32_t kFAccCol1 = 0;
-constexpr int kWarpsF = kThreads / 32;
-static_assert(kFSelScratch + 6 * 32 * 4 <= kFWOff, "select scratch inside the score stages");
-static_assert(2 * kThreads >= kFGroups, "two 32-key groups per thread cover a row");
+static_assert(sel::kBytes <= kFWOff, "the selection's shared memory inside the score stages");
 
 // after the attention unit's control block
 struct FCtl {
@@ -102,248 +95,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// exclusive prefix of v over the CTA (kThreads threads) and the total.  `slot` (2 x kWarps words)
-// must not be used by another scan or bin search before the next CTA barrier after this one.
-__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* slot, uint32_t* total) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    __syncwarp();   // shuffles of a reconverged warp (a diverged one pays for every shuffle)
-    uint32_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) slot[wid] = x;
-    __syncthreads();
-    if (wid == 0) {
-        uint32_t u = lane < kWarpsF ? slot[lane] : 0u;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, u, o);
-            if (lane >= o) u += y;
-        }
-        if (lane < kWarpsF) slot[kWarpsF + lane] = u;
-    }
-    __syncthreads();
-    *total = slot[2 * kWarpsF - 1];
-    return (wid > 0 ? slot[kWarpsF + wid - 1] : 0u) + x - v;
-}
-
-// bin of a histogram (NB bins) holding the need-th largest counted key, the count in higher bins,
-// and the histogram's total, to every thread (bin and count unspecified when need > total).
-// Thread t < NB/8 sums the 8 bins NB-8(t+1) .. NB-8t-1 (higher bins to lower threads); warp scans
-// and the warps' totals give each thread the count in its bins and all higher ones, and the one
-// thread whose bins hold the need-th key walks them.  `slot` (kWarps + 3 words) as for block_scan.
-template <int NB>
-__device__ __forceinline__ void find_bin(const uint32_t* hist, uint32_t need, uint32_t* slot, uint32_t* bin,
-                                         uint32_t* above, uint32_t* total) {
-    constexpr int nt = NB / 8, nw = nt / 32;
-    static_assert(nt % 32 == 0 && nt <= kThreads && nw <= kWarpsF, "whole warps, 8 bins per thread");
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    uint32_t h[8], c = 0, x = 0;
-    if (threadIdx.x < nt) {
-        const uint4* h4 = reinterpret_cast<const uint4*>(hist + NB - 8 * (threadIdx.x + 1));
-        const uint4 a0 = h4[0], a1 = h4[1];
-        h[0] = a0.x; h[1] = a0.y; h[2] = a0.z; h[3] = a0.w;
-        h[4] = a1.x; h[5] = a1.y; h[6] = a1.z; h[7] = a1.w;
-        c = ((h[0] + h[1]) + (h[2] + h[3])) + ((h[4] + h[5]) + (h[6] + h[7]));
-        __syncwarp();
-        x = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) slot[wid] = x;
-    }
-    __syncthreads();
-    if (threadIdx.x < nt) {
-        uint32_t off = 0, tot = 0;
-#pragma unroll
-        for (int w = 0; w < nw; ++w) {
-            const uint32_t t = slot[w];
-            off += w < wid ? t : 0u;
-            tot += t;
-        }
-        x += off;   // keys in this thread's bins and all higher bins
-        if (x - c < need && x >= need) {
-            uint32_t cc = x - c;
-            int b = NB - 8 * (int)threadIdx.x - 8;
-#pragma unroll
-            for (int i = 7; i >= 0; --i) {
-                if (cc + h[i] >= need) {
-                    b = NB - 8 * (int)threadIdx.x - 8 + i;
-                    break;
-                }
-                cc += h[i];
-            }
-            slot[kWarpsF] = (uint32_t)b;
-            slot[kWarpsF + 1] = cc;
-        }
-        if (threadIdx.x == 0) slot[kWarpsF + 2] = tot;
-    }
-    __syncthreads();
-    *bin = slot[kWarpsF];
-    *above = slot[kWarpsF + 1];
-    *total = slot[kWarpsF + 2];
-}
-
-// Phase 2: the top_k positions of row r (scores complete in global memory) in ascending order,
-// the lowest positions first among equal scores (-0 == +0), -1 padding up to top_k; n_sel[r].
-// ghist: the row's histogram of the order keys' top 11 bits (NULL: counted here).
-// Three radix rounds (11, 11, 10 bits) find the top_k-th order key T: the first from the
-// histogram (its bin found while the row's scores are in flight), the others counting only the
-// keys in the previous round's bin.  Position i of the row is handled by thread i mod kThreads, so
-// a warp holds the 32 keys of one group in each batch entry, one ballot gives the group's
-// selection bits, and the output is written from those bits.
-__device__ void select_row_fused(const float* s, int n, int top_k, const uint32_t* ghist, int32_t* out,
-                                 int32_t* n_sel_r, uint8_t* smem) {
-    uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kFSelOff);
-    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kFHistOff);
-    uint32_t* hist2 = hist + 2048;
-    uint32_t* hist3 = hist + 4096;
-    uint32_t* selw = reinterpret_cast<uint32_t*>(smem + kFBitsOff);
-    uint32_t* eqw = selw + kFGroups;
-    uint32_t* scratch = reinterpret_cast<uint32_t*>(smem + kFSelScratch);   // 6 slots of 32 words
-    const int K = min(top_k, n);
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    if (K == n) {
-        for (int i = threadIdx.x; i < n; i += kThreads) out[i] = i;
-    } else {
-        constexpr int kB = 24;                          // positions per thread and batch
-        constexpr int kStride = kB * kThreads;          // 9216 positions (288 groups) per batch
-        constexpr int kHB = (2048 + kThreads - 1) / kThreads;
-        // the histogram and the first batch of scores in flight together
-        uint32_t hv[kHB];
-#pragma unroll
-        for (int u = 0; u < kHB; ++u) {
-            const int i = threadIdx.x + u * kThreads;
-            hv[u] = (ghist && i < 2048) ? __ldcg(ghist + i) : 0u;
-        }
-        float v[kB];
-#pragma unroll
-        for (int u = 0; u < kB; ++u) {
-            const int i = threadIdx.x + u * kThreads;
-            v[u] = i < n ? __ldcg(s + i) : 0.f;
-        }
-        for (int i = threadIdx.x; i < 3072; i += kThreads) hist2[i] = 0u;   // rounds 2 and 3
-#pragma unroll
-        for (int u = 0; u < kHB; ++u) {
-            const int i = threadIdx.x + u * kThreads;
-            if (i < 2048) hist[i] = hv[u];
-        }
-        __syncthreads();
-        // round 1 from the scorer's histogram when it counts exactly this row's keys
-        uint32_t need = (uint32_t)K, bin, above, total;
-        find_bin<2048>(hist, need, scratch + 32, &bin, &above, &total);
-        const bool have = total == (uint32_t)n;
-        // order keys to shared memory; the first round's bin counted for round 2
-        for (int b0 = 0; b0 < n; b0 += kStride) {
-            if (b0 > 0) {
-#pragma unroll
-                for (int u = 0; u < kB; ++u) {
-                    const int i = b0 + threadIdx.x + u * kThreads;
-                    v[u] = i < n ? __ldcg(s + i) : 0.f;
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int i = b0 + threadIdx.x + u * kThreads;
-                const uint32_t key = order_key(v[u]);
-                if (i < n) keys[i] = key;
-                if (have && i < n && (key >> 21) == bin) atomicAdd(&hist2[(key >> 10) & 2047u], 1u);
-            }
-        }
-        __syncthreads();
-        if (!have) {
-            // the scorer's counts are incomplete: count here
-            for (int i = threadIdx.x; i < 2048; i += kThreads) hist[i] = 0u;
-            __syncthreads();
-            for (int i = threadIdx.x; i < n; i += kThreads) atomicAdd(&hist[keys[i] >> 21], 1u);
-            __syncthreads();
-            find_bin<2048>(hist, need, scratch + 32, &bin, &above, &total);
-            for (int i = threadIdx.x; i < n; i += kThreads) {
-                const uint32_t key = keys[i];
-                if ((key >> 21) == bin) atomicAdd(&hist2[(key >> 10) & 2047u], 1u);
-            }
-            __syncthreads();
-        }
-        need -= above;
-        const uint32_t p1 = bin;                        // top 11 bits of T
-        find_bin<2048>(hist2, need, scratch + 64, &bin, &above, &total);
-        need -= above;
-        const uint32_t p2 = (p1 << 11) | bin;           // top 22 bits of T
-        for (int b0 = 0; b0 < n; b0 += kStride) {
-            uint32_t kk[kB];
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int i = b0 + threadIdx.x + u * kThreads;
-                kk[u] = i < n ? keys[i] : 0u;
-            }
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const bool ok = b0 + (int)threadIdx.x + u * kThreads < n;
-                if (ok && (kk[u] >> 10) == p2) atomicAdd(&hist3[kk[u] & 1023u], 1u);
-            }
-        }
-        __syncthreads();
-        find_bin<1024>(hist3, need, scratch + 96, &bin, &above, &total);
-        need -= above;                                  // keys equal to T to take (the lowest positions)
-        const uint32_t T = (p2 << 10) | bin;
-        const bool all_eq = need == hist3[bin];         // (uniform) every key equal to T is taken
-        // selection bits of each 32-key group: entry u of warp w in the batch at b0 is group
-        // b0/32 + w + 12u; lane u of the warp keeps that group's bits and stores them
-        for (int b0 = 0; b0 < n; b0 += kStride) {
-            uint32_t kk[kB];
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const int i = b0 + threadIdx.x + u * kThreads;
-                kk[u] = i < n ? keys[i] : 0u;
-            }
-            __syncwarp();
-            uint32_t my_sel = 0u, my_eq = 0u;
-#pragma unroll
-            for (int u = 0; u < kB; ++u) {
-                const bool ok = b0 + (int)threadIdx.x + u * kThreads < n;
-                const uint32_t gt = __ballot_sync(0xffffffffu, ok && kk[u] > T);
-                const uint32_t eq = __ballot_sync(0xffffffffu, ok && kk[u] == T);
-                my_sel = lane == u ? (all_eq ? (gt | eq) : gt) : my_sel;
-                my_eq = lane == u ? eq : my_eq;
-            }
-            const int grp = (b0 >> 5) + wid + lane * (kThreads / 32);
-            if (lane < kB && grp < kFGroups) {
-                selw[grp] = my_sel;
-                eqw[grp] = my_eq;
-            }
-        }
-        const int groups = (n + 31) >> 5;
-        const int ga = 2 * threadIdx.x, gb = ga + 1;    // this thread's two groups, in position order
-        __syncthreads();
-        if (!all_eq) {
-            // ties at T: only the lowest `need` positions among the keys equal to T
-            const uint32_t ea = ga < groups ? eqw[ga] : 0u, eb = gb < groups ? eqw[gb] : 0u;
-            uint32_t tot;
-            const uint32_t before = block_scan((uint32_t)(__popc(ea) + __popc(eb)), scratch + 128, &tot);
-            uint32_t left = before >= need ? 0u : need - before;
-            uint32_t ta = 0u, tb = 0u;
-            for (uint32_t w = ea; w && left; w &= w - 1u, --left) ta |= w & (0u - w);
-            for (uint32_t w = eb; w && left; w &= w - 1u, --left) tb |= w & (0u - w);
-            if (ga < groups) selw[ga] |= ta;
-            if (gb < groups) selw[gb] |= tb;
-            __syncthreads();
-        }
-        // ordered write-out: each thread the set bits of its two groups
-        const uint32_t sa = ga < groups ? selw[ga] : 0u, sb = gb < groups ? selw[gb] : 0u;
-        uint32_t tot;
-        uint32_t pos = block_scan((uint32_t)(__popc(sa) + __popc(sb)), scratch + 160, &tot);
-        for (uint32_t w = sa; w; w &= w - 1u) out[pos++] = ga * 32 + (__ffs(w) - 1);
-        for (uint32_t w = sb; w; w &= w - 1u) out[pos++] = gb * 32 + (__ffs(w) - 1);
-    }
-    for (int i = K + threadIdx.x; i < top_k; i += kThreads) out[i] = -1;
-    if (threadIdx.x == 0) *n_sel_r = K;
-    __syncthreads();
 }
 
 template <typename TK, typename TQ>
@@ -656,8 +407,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
             flag(g.status, IDX_ERR_TIMEOUT);
         __syncthreads();
         __threadfence();   // the other CTAs' scores and counts of row r (their counts were seen above)
-        select_row_fused(scores + (int64_t)r * score_row_stride, f.nvis[r], top_k, ghist + (int64_t)r * 2048,
-                         idx + (int64_t)r * idx_row_stride, n_sel + r, smem);
+        sel::select_row<kThreads>(scores + (int64_t)r * score_row_stride, f.nvis[r], top_k,
+                                  ghist + (int64_t)r * 2048, idx + (int64_t)r * idx_row_stride, n_sel + r, smem);
         if (threadIdx.x == 0) {
             __threadfence();
             atomicExch(&row_flag[r], 1u);
@@ -841,7 +592,7 @@ size_t fused_decode_workspace_bytes(int64_t n_rows, int64_t idx_row_stride) {
 
 // whether the fused decode kernel takes this batch: decode rows, few and short enough
 bool fused_decode_fits(int64_t n_rows, int max_n_kv, int top_k, int64_t idx_row_stride) {
-    if (n_rows < 1 || n_rows > kFusedMaxRows || max_n_kv > kFSelMax || idx_row_stride > kMaxKps) return false;
+    if (n_rows < 1 || n_rows > kFusedMaxRows || max_n_kv > sel::kMaxKeys || idx_row_stride > kMaxKps) return false;
     const int clusters = fused_decode_clusters();
     const int splits = mla_splits(n_rows, idx_row_stride);
     return clusters > 0 && splits <= kFMaxSplits && n_rows * (int64_t)splits <= clusters && top_k >= 1;

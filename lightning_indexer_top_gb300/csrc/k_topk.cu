@@ -24,6 +24,7 @@
 // Rows with K == n_vis (every visible key kept, e.g. the first top_k rows of a
 // causal prefill) skip the select and write 0..n_vis-1.
 #include "lidx_internal.cuh"
+#include "select_row.cuh"
 
 namespace lidx {
 namespace {
@@ -1077,6 +1078,22 @@ __global__ void __launch_bounds__(kMapThreads, 1) topk_mc_finish_kernel(const fl
     if (threadIdx.x == 0 && n_sel) n_sel[r] = K;
 }
 
+// Many rows of at most sel::kMaxKeys scores (a causal prefill): one CTA of kRowThreads per row, the
+// row's order keys in shared memory (two CTAs per SM), three radix rounds and an ordered write-out
+// from per-group selection bits (select_row.cuh).
+constexpr int kRowThreads = 384;
+
+__global__ void __launch_bounds__(kRowThreads) topk_rows_kernel(const float* scores, int64_t score_row_stride,
+                                                               Geom g, int top_k, int32_t* idx,
+                                                               int64_t idx_row_stride, int32_t* n_sel) {
+    extern __shared__ __align__(16) uint8_t rows_smem[];
+    pdl_trigger();
+    pdl_wait();
+    const int64_t r = blockIdx.x;
+    sel::select_row<kRowThreads>(scores + r * score_row_stride, row_n_vis(g, r), top_k, nullptr,
+                                 idx + r * idx_row_stride, n_sel ? n_sel + r : nullptr, rows_smem);
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const float* scores, int64_t score_row_stride, const Geom& g, int top_k,
@@ -1107,6 +1124,11 @@ cudaError_t launch_topk(const float* scores, int64_t score_row_stride, const Geo
         cudaFuncSetAttribute(topk_mc_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         return launch_pdl(topk_mc_finish_kernel, dim3((unsigned)n_rows), dim3(kMapThreads), sm, st, scores,
                           score_row_stride, g, top_k, L, idx, idx_row_stride, n_sel, 0);
+    } else if (g.max_n_kv <= sel::kMaxKeys && n_rows >= 2 * sm_count()) {
+        // many short rows: a lighter CTA per row, two per SM
+        cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sel::kBytes);
+        return launch_pdl(topk_rows_kernel, dim3((unsigned)n_rows), dim3(kRowThreads), (size_t)sel::kBytes, st,
+                          scores, score_row_stride, g, top_k, idx, idx_row_stride, n_sel);
     } else {
         const size_t sm = sizeof(MapShared);
         cudaFuncSetAttribute(topk_map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
