@@ -225,6 +225,32 @@ def test_fused_score_topk_back_to_back_launches():
     assert L.idx_device_status(reset=True) == 0
 
 
+@pytest.mark.parametrize("top_k", [1, 700, 2048])
+def test_topk_many_short_rows_bit_exact(top_k):
+    # >= 2 rows per SM and <= 16384 keys per row: the one-CTA-per-row kernel of the causal prefill.
+    # Rows mix ties (small integers, signed zeros, one constant row), normal scores, ragged lengths
+    # from 0 to 16384 (both sides of 9216, where the kernel loads a second batch) and dense rows.
+    g = torch.Generator().manual_seed(47)
+    rows, n = 320, 16384
+    scores = torch.randn(rows, n, generator=g)
+    scores[0::5] = torch.randint(-3, 4, (len(range(0, rows, 5)), n), generator=g).float()
+    z = torch.randint(0, 2, (len(range(1, rows, 7)), n), generator=g).float()
+    z[z == 0] = -0.0
+    scores[1::7] = z
+    scores[2] = 0.0
+    n_kv = [(n - 53 * r) % (n + 1) for r in range(rows)]
+    n_kv[3], n_kv[4], n_kv[5], n_kv[6] = 0, 1, top_k, top_k + 1
+    batch = L.Batch(_i32(n_kv), 1, n, kv_seq_stride=0)
+    idx, n_sel = L.idx_topk(scores.to(DEV), batch, top_k)
+    torch.cuda.synchronize()
+    idx_h, ns_h = idx.cpu().numpy(), n_sel.cpu().numpy()
+    for r in range(rows):
+        ref = O.topk_select(scores[r].numpy(), n_kv[r], top_k)
+        assert ns_h[r] == len(ref), f"row {r}"
+        assert idx_h[r, :len(ref)].tolist() == ref.tolist(), f"row {r}"
+        assert np.all(idx_h[r, len(ref):] == -1), f"row {r}"
+
+
 def test_topk_default_minus_one_equals_2048():
     g = torch.Generator().manual_seed(45)
     scores = torch.randn(3, 40000, generator=g).to(DEV)
