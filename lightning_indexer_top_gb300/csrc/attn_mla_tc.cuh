@@ -94,7 +94,8 @@ struct Ctl {
     uint64_t xempty[kStagesK]; // tile consumed by the MMAs
     uint64_t sfull[2];         // rank 0: S accumulator written
     uint64_t sempty[2];        // rank 0: S read by the softmax warps
-    uint64_t qready;           // rank 0: Q stored in TMEM
+    uint64_t qready;           // rank 0: Q stored in TMEM (its shared-memory staging free again)
+    uint64_t qbulk;            // rank 0: Q's rows landed in shared memory
     uint64_t pfree[2];         // rank 0: rank 1's packet slot j consumed by its MMAs
     uint64_t pfull[2];         // rank 1: packet j landed (rank 0 posts its byte count, its stores complete it)
     uint64_t cdone[2];         // rank 1: O corrected for packet j
@@ -223,36 +224,40 @@ __device__ __forceinline__ void mla_init(Ctl& c) {
         mbar_init(&c.pvdone[i], 1);
     }
     mbar_init(&c.qready, 4);
+    mbar_init(&c.qbulk, 1);
     mbar_init(&c.done, 1);
     c.abort = 0;
     fence_mbar_init();
 }
 
-// rank 0, warps 2..5 (thread = head): Q of query row qrow into TMEM columns
-// 0..287 (the QK^T MMA's A operand), then an arrival on qready
-__device__ __forceinline__ void mla_load_q(Ctl& c, uint32_t tmem, const __nv_bfloat16* __restrict__ q, int64_t qrow) {
+// rank 0, warps 2..5 (thread = head): Q of query row qrow into TMEM columns 0..287 (the QK^T MMA's A
+// operand), then an arrival on qready.  Each thread bulk-copies its head's row (1152 contiguous bytes)
+// into the key ring, not yet in use, at a pitch of kQPitch bytes (rows 4 banks apart, so a warp's
+// 16-byte reads of its 32 rows do not collide), and moves it to TMEM a column block at a time.  The
+// key producers start only after qready (the staging area is their first stages).
+constexpr int kQPitch = kDk * 2 + 16;
+static_assert(kHq * kQPitch <= kStagesK * kKTileBytes, "Q staging inside the key ring");
+__device__ __forceinline__ void mla_load_q(Ctl& c, uint8_t* xtiles, uint32_t tmem, const __nv_bfloat16* __restrict__ q,
+                                           int64_t qrow) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quad = warp & 3;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const int h = quad * 32 + lane;
-    const uint4* src = reinterpret_cast<const uint4*>(q + (qrow * kHq + h) * (int64_t)kDk);
-    // column block cb+1 is loading while block cb goes to TMEM
-    uint4 xn[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) xn[i] = src[i];
+    uint8_t* row = xtiles + h * kQPitch;
+    if (warp == 2 && lane == 0) mbar_arrive_expect_tx(&c.qbulk, kHq * kDk * 2);
+    bulk_load(row, q + (qrow * kHq + h) * (int64_t)kDk, kDk * 2, &c.qbulk);
+    const bool ok = warp_wait(&c.qbulk, 0);
+    const uint4* src = reinterpret_cast<const uint4*>(row);
 #pragma unroll
     for (int cb = 0; cb < kDkBlocks; ++cb) {
         uint32_t regs[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            regs[4 * i] = xn[i].x;
-            regs[4 * i + 1] = xn[i].y;
-            regs[4 * i + 2] = xn[i].z;
-            regs[4 * i + 3] = xn[i].w;
-        }
-        if (cb + 1 < kDkBlocks) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) xn[i] = src[(cb + 1) * 8 + i];
+            const uint4 x = ok ? src[cb * 8 + i] : make_uint4(0u, 0u, 0u, 0u);
+            regs[4 * i] = x.x;
+            regs[4 * i + 1] = x.y;
+            regs[4 * i + 2] = x.z;
+            regs[4 * i + 3] = x.w;
         }
         tmem_st_32x32b_x32(tmem + lane_off + cb * 32, regs);
     }
@@ -327,6 +332,8 @@ __device__ __forceinline__ void mla_run(const MlaSmem& sm, uint32_t tmem, uint32
     const int producer = warp == 0 ? 0 : (warp >= 6 && warp != 9 ? warp - (warp > 9 ? 6 : 5) : -1);   // index or -1
     if (rank == 0) {
         if (producer >= 0) {
+            // Q's staging area is the ring's first stages: gather once Q is in TMEM
+            if (u.n_tiles > 0 && !warp_wait(&c.qready, 0)) abort_cta(c, g.status);
             gather_tiles<kDkBlocks * 8, kStagesK, kKTileBytes>(c, xtiles, lat, lat_row_stride, u, rows_s, producer,
                                                                g.status);
         } else if (warp == 1) {

@@ -36,7 +36,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // warps, once the previous kernel's selection is visible, stage the
     // split's selected keys.
     const bool q_warp = mla_q_warp(rank);
-    if (q_warp) mla_load_q(c, tmem, q, unit / splits);
+    if (q_warp) mla_load_q(c, sm.xtiles, tmem, q, unit / splits);
     pdl_wait();
     const Unit u = make_unit(unit, g, n_sel, idx_row_stride, kv_rows, splits, kps);
     if (!q_warp) mla_stage_rows(sm, rank, u, g, idx, idx_row_stride, kv_rows);

@@ -419,7 +419,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) decode_
     if (cid < n_units) {
         const int r = (int)(cid / splits);
         // rank 0 puts the unit's Q into TMEM while thread 0 waits for the row's selection
-        if (mla_q_warp(rank)) mla_load_q(c, tmem, qa, r);
+        if (mla_q_warp(rank)) mla_load_q(c, sm.xtiles, tmem, qa, r);
         if (threadIdx.x == 0) f.flag_ok = wait_counter(&row_flag[r], 1u) ? 1 : 0;
         __syncthreads();
         if (!f.flag_ok && threadIdx.x == 0) flag(g.status, IDX_ERR_TIMEOUT);
