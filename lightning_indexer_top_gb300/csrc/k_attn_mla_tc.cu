@@ -6,19 +6,22 @@ namespace lidx {
 namespace {
 using namespace sm100;
 
+// A persistent grid of 2-CTA clusters: cluster c runs the units c, c + C, c + 2C, ... (C clusters),
+// keeping its TMEM and re-initialising its barriers between units (every phase of the last unit has
+// completed and no remote arrival is pending once both CTAs passed the unit's closing cluster barrier).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_attn_tc_kernel(const __nv_bfloat16* __restrict__ lat, int64_t lat_row_stride,
                        const __nv_bfloat16* __restrict__ q, Geom g, const int32_t* idx,
                        int64_t idx_row_stride, const int32_t* n_sel, int64_t kv_rows,
                        float scale_log2, int splits, int kps, void* __restrict__ out, int out_dtype,
-                       float* __restrict__ part_o, float* __restrict__ part_ml) {
+                       float* __restrict__ part_o, float* __restrict__ part_ml, int64_t n_units) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const MlaSmem sm = mla_smem(smem);
     Ctl& c = *sm.c;
     const uint32_t rank = cluster_ctarank();
     const int warp = threadIdx.x >> 5;
-    const int64_t unit = blockIdx.x >> 1;
+    const int64_t n_clusters = gridDim.x >> 1;
     pdl_trigger();
 
     if (threadIdx.x == 0) mla_init(c);
@@ -31,24 +34,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = c.tmem_base;
 
-    // Rank 0's softmax warps put Q into TMEM (Q is an input no other kernel
-    // writes, so this overlaps the end of the previous kernel) while the other
-    // warps, once the previous kernel's selection is visible, stage the
-    // split's selected keys.
     const bool q_warp = mla_q_warp(rank);
-    if (q_warp) mla_load_q(c, sm.xtiles, tmem, q, unit / splits);
-    pdl_wait();
-    const Unit u = make_unit(unit, g, n_sel, idx_row_stride, kv_rows, splits, kps);
-    if (!q_warp) mla_stage_rows(sm, rank, u, g, idx, idx_row_stride, kv_rows);
-    tc_fence_before();
-    cluster_sync();  // barriers of both CTAs initialised, indices staged
-    tc_fence_after();
-    mla_run(sm, tmem, rank, u, unit, lat, lat_row_stride, g, scale_log2, splits, out, out_dtype, part_o, part_ml);
-
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();  // no cross-CTA traffic may target a CTA that has left
-    tc_fence_after();
+    for (int64_t unit = blockIdx.x >> 1; unit < n_units; unit += n_clusters) {
+        const bool first = unit == (int64_t)(blockIdx.x >> 1);
+        if (!first) {
+            if (threadIdx.x == 0) mla_init(c);
+            __syncthreads();
+        }
+        // Rank 0's softmax warps put Q into TMEM (Q is an input no other kernel writes, so for the
+        // first unit this overlaps the end of the previous kernel) while the other warps, once the
+        // previous kernel's selection is visible, stage the split's selected keys.
+        if (q_warp) mla_load_q(c, sm.xtiles, tmem, q, unit / splits);
+        if (first) pdl_wait();
+        const Unit u = make_unit(unit, g, n_sel, idx_row_stride, kv_rows, splits, kps);
+        if (!q_warp) mla_stage_rows(sm, rank, u, g, idx, idx_row_stride, kv_rows);
+        tc_fence_before();
+        cluster_sync();  // barriers of both CTAs initialised, indices staged
+        tc_fence_after();
+        mla_run(sm, tmem, rank, u, unit, lat, lat_row_stride, g, scale_log2, splits, out, out_dtype, part_o, part_ml);
+        tc_fence_before();
+        __syncthreads();
+        cluster_sync();  // no cross-CTA traffic of this unit is in flight
+        tc_fence_after();
+    }
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -127,6 +135,26 @@ size_t mla_workspace_bytes(int64_t n_rows, int64_t cap) {
     return (size_t)n_rows * s * kHq * (kDv + 2) * sizeof(float);
 }
 
+// clusters of the attention kernel that can be resident at once (0: unknown)
+int64_t mla_clusters() {
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev]) return cache[dev] > 0 ? cache[dev] : 0;
+    cudaFuncSetAttribute(mla_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, mla_attn_tc_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    cache[dev] = n > 0 ? n : -1;
+    return n > 0 ? n : 0;
+}
+
 bool mla_tc_supported(int dtype, int Hq, int Hkv, int dk, int dv, const void* k, const void* v,
                       int64_t kv_row_stride, int64_t kv_rows, const void* q, const void* out) {
     return dtype == IDX_BF16 && !v && Hq == kHq && Hkv == 1 && dk == kDk && dv == kDv &&
@@ -151,14 +179,15 @@ cudaError_t launch_attn_mla_tc(const void* q, const void* lat, int64_t kv_row_st
         part_o = static_cast<float*>(ws);
         part_ml = part_o + (size_t)n_rows * splits * kHq * kDv;
     }
-    const int64_t grid = 2 * n_rows * splits;
-    if (grid > INT32_MAX) return cudaErrorNotSupported;
+    const int64_t n_units = n_rows * splits;
     cudaFuncSetAttribute(mla_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    const int64_t resident = mla_clusters();
+    const int64_t clusters = resident > 0 && resident < n_units ? resident : n_units;
     const float scale_log2 = scale * 1.4426950408889634f;
-    cudaError_t e = launch_pdl(mla_attn_tc_kernel, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st,
+    cudaError_t e = launch_pdl(mla_attn_tc_kernel, dim3((unsigned)(2 * clusters)), dim3(kThreads), kSmemBytes, st,
                                static_cast<const __nv_bfloat16*>(lat), kv_row_stride,
                                static_cast<const __nv_bfloat16*>(q), g, idx, idx_row_stride, n_sel, kv_rows,
-                               scale_log2, splits, (int)kps64, out, out_dtype, part_o, part_ml);
+                               scale_log2, splits, (int)kps64, out, out_dtype, part_o, part_ml, n_units);
     if (e != cudaSuccess || splits == 1) return e;
     return launch_pdl(mla_combine_kernel, dim3((unsigned)n_rows, kDv / 4), dim3(kHq), 0, st,
                       static_cast<const float*>(part_o), static_cast<const float*>(part_ml), splits, out, out_dtype);
