@@ -317,12 +317,13 @@ __global__ void __launch_bounds__(kThreads, 4) attn_generic_kernel(
 }
 
 // merges the key splits of one (row, head): o = sum_s e^(m_s - M) o_s / sum_s e^(m_s - M) l_s
-__global__ void __launch_bounds__(128) attn_generic_combine_kernel(const float* __restrict__ part_o,
-                                                                   const float* __restrict__ part_ml, int splits,
-                                                                   int Hq, int dv, void* __restrict__ out,
+__global__ void __launch_bounds__(128) attn_generic_combine_kernel(const float* part_o, const float* part_ml,
+                                                                   int splits, int Hq, int dv, void* __restrict__ out,
                                                                    int out_dtype) {
     const int64_t r = blockIdx.x;
     const int h = blockIdx.y;
+    pdl_trigger();
+    pdl_wait();
     float M = 0.f;
     bool any = false;
     for (int s = 0; s < splits; ++s) {
@@ -389,9 +390,7 @@ cudaError_t run_dv(const T* q, int Hq, int Hkv, int dk, int dv, const T* k, cons
                                          out_dtype, n_chunks, vec, splits, kps, part_o, part_ml); \
         cudaError_t e = cudaGetLastError();                                                     \
         if (e != cudaSuccess || splits == 1) return e;                                          \
-        attn_generic_combine_kernel<<<dim3((unsigned)n_rows, (unsigned)Hq), 128, 0, st>>>(      \
-            part_o, part_ml, splits, Hq, dv, out, out_dtype);                                   \
-        return cudaGetLastError();                                                              \
+        return launch_attn_generic_combine(part_o, part_ml, splits, n_rows, Hq, dv, out, out_dtype, st); \
     }
     LIDX_ATTN_CASE(1)
     LIDX_ATTN_CASE(2)
@@ -435,9 +434,8 @@ int generic_attn_splits(int64_t n_rows, int64_t cap) {
 
 cudaError_t launch_attn_generic_combine(const float* part_o, const float* part_ml, int splits, int64_t n_rows, int Hq,
                                         int dv, void* out, int out_dtype, cudaStream_t st) {
-    attn_generic_combine_kernel<<<dim3((unsigned)n_rows, (unsigned)Hq), 128, 0, st>>>(part_o, part_ml, splits, Hq, dv,
-                                                                                      out, out_dtype);
-    return cudaGetLastError();
+    return launch_pdl(attn_generic_combine_kernel, dim3((unsigned)n_rows, (unsigned)Hq), dim3(128), 0, st, part_o,
+                      part_ml, splits, Hq, dv, out, out_dtype);
 }
 
 size_t generic_attn_workspace_bytes(int64_t n_rows, int64_t cap, int Hq, int dv) {

@@ -55,9 +55,11 @@ struct Ctl {
     uint64_t sempty[2];
     uint64_t pready[2];
     uint64_t pvdone[2];
-    uint64_t rfull[2];            // the four softmax warps' maxima of a tile are in red[t & 1]
+    uint64_t rfull[2];            // the four softmax warps' flags of a tile are in over[t & 1]
+    uint64_t mfull;               // ... and, when some flag is set, their maxima in red[t & 1]
     uint64_t lfull;               // ... and their row sums in lred
     uint64_t done;
+    uint8_t over[2][4];           // per warp: a key of the tile lifts a head past the rescale margin
     float red[2][4][kN];          // per-warp maxima of a tile (two tiles in turn)
     float lred[4][kN];            // per-warp row sums at the end
     uint32_t tmem_base;
@@ -120,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_gqa_tc_kernel(
             mbar_init(&c.pvdone[i], 1);
             mbar_init(&c.rfull[i], 4);
         }
+        mbar_init(&c.mfull, 4);
         mbar_init(&c.lfull, 4);
         mbar_init(&c.done, 1);
         c.abort = 0;
@@ -267,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_gqa_tc_kernel(
             l_part[h] = 0.f;
         }
         bool has_m = false, ok = true;
+        uint32_t n_exch = 0;
         for (int t = 0; t < n_tiles; ++t) {
             const int j = t & 1;
             const uint32_t ph = (uint32_t)((t >> 1) & 1);
@@ -281,30 +285,52 @@ __global__ void __launch_bounds__(kThreads, 1) attn_gqa_tc_kernel(
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&c.sempty[j]);
-            const bool valid = (vmask[t * 4 + quad] >> lane) & 1u;
-            const bool any_valid = (vmask[t * 4] | vmask[t * 4 + 1] | vmask[t * 4 + 2] | vmask[t * 4 + 3]) != 0u;
-            // the tile's maximum per head over its 128 keys: warp maxima, exchanged through shared memory
+            const uint4 vm = *reinterpret_cast<const uint4*>(vmask + t * 4);
+            const uint32_t vq = quad == 0 ? vm.x : quad == 1 ? vm.y : quad == 2 ? vm.z : vm.w;
+            const bool valid = (vq >> lane) & 1u;
+            const bool any_valid = (vm.x | vm.y | vm.z | vm.w) != 0u;
+            // The running maximum of a head moves only when a key of the tile exceeds it by more than the
+            // rescale margin.  Each warp first says whether one of its keys does (one vote); the maxima of
+            // the tile are exchanged only then, and for the first tile with a valid key.
+            bool over = false;
 #pragma unroll
             for (int h = 0; h < kN; ++h) {
                 sv[h] *= scale_log2;
-                if (h >= G) continue;   // (uniform)
-                float x = valid ? sv[h] : -3.0e38f;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-                if (lane == 0) c.red[j][quad][h] = x;
+                if (h < G && valid && sv[h] > m_used[h] + kRescaleLog2) over = true;
             }
+            const bool w_over = __any_sync(0xffffffffu, over);
+            if (lane == 0) c.over[j][quad] = w_over ? 1 : 0;
             __syncwarp();
             if (lane == 0) mbar_arrive(&c.rfull[j]);
             if (!warp_wait(&c.rfull[j], ph)) {
                 ok = false;
                 break;
             }
+            const bool exch = any_valid && (!has_m || *reinterpret_cast<volatile uint32_t*>(c.over[j]) != 0u);
+            if (exch) {
+                // the tile's maximum per head over its 128 keys: warp maxima, exchanged through shared memory
+#pragma unroll
+                for (int h = 0; h < kN; ++h) {
+                    if (h >= G) continue;   // (uniform)
+                    float x = valid ? sv[h] : -3.0e38f;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+                    if (lane == 0) c.red[j][quad][h] = x;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c.mfull);
+                if (!warp_wait(&c.mfull, n_exch & 1u)) {
+                    ok = false;
+                    break;
+                }
+                ++n_exch;
+            }
             float alpha[kN];
             bool resc = false;
 #pragma unroll
             for (int h = 0; h < kN; ++h) {
                 alpha[h] = 1.f;
-                if (h >= G || !any_valid) continue;
+                if (h >= G || !exch) continue;
                 const float tmax = fmaxf(fmaxf(c.red[j][0][h], c.red[j][1][h]), fmaxf(c.red[j][2][h], c.red[j][3][h]));
                 if (!has_m) {
                     m_used[h] = tmax;

@@ -24,7 +24,7 @@ namespace {
 constexpr int kThreads = 128;
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads) pool_kernel(const T* __restrict__ k, int64_t k_row_stride,
+__global__ void __launch_bounds__(kThreads) pool_kernel(const T* k, int64_t k_row_stride,
                                                         int64_t k_rows, Geom g, int C, int d,
                                                         float* __restrict__ pooled,
                                                         int64_t pool_seq_stride,
@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(const T* __restrict__ k,
                                                         const int32_t* __restrict__ stale_pos) {
     extern __shared__ float part[];  // [RP][d]
     const int b = blockIdx.y;
+    pdl_trigger();
+    pdl_wait();
     const int n_cb = seq_n_kv(g, b) / C;
     // first block to (re)pool: after the current ones, and from the stale one on
     int beta0 = 0;
@@ -107,9 +109,8 @@ cudaError_t run(const T* k, int64_t k_row_stride, int64_t k_rows, const Geom& g,
         if (gx > want) gx = want;
     }
     dim3 grid((unsigned)gx, (unsigned)g.B);
-    pool_kernel<T><<<grid, kThreads, sm, st>>>(k, k_row_stride, k_rows, g, C, d, pooled,
-                                               pool_seq_stride, n_pooled, stale_pos);
-    return cudaGetLastError();
+    return launch_pdl(pool_kernel<T>, grid, dim3(kThreads), sm, st, k, k_row_stride, k_rows, g, C, d, pooled,
+                      pool_seq_stride, n_pooled, stale_pos);
 }
 
 }  // namespace

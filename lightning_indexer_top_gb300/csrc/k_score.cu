@@ -23,10 +23,12 @@ constexpr int kTile = 128;
 
 template <typename TK, int HH>
 __global__ void __launch_bounds__(kTile) score_generic_kernel(
-    const void* __restrict__ q, int q_dtype, const float* __restrict__ w, int H, int d,
-    const TK* __restrict__ k, int64_t k_row_stride, int64_t k_rows, Geom g, int block_size,
-    float* __restrict__ scores, int64_t score_row_stride, const float* __restrict__ k_scale) {
+    const void* q, int q_dtype, const float* __restrict__ w, int H, int d,
+    const TK* k, int64_t k_row_stride, int64_t k_rows, Geom g, int block_size,
+    float* __restrict__ scores, int64_t score_row_stride, const float* k_scale) {
     extern __shared__ float smem[];
+    pdl_trigger();
+    pdl_wait();
     float* qs = smem;            // [HH][d], heads >= H zero
     float* ws = smem + HH * d;   // [HH],    heads >= H zero
 
@@ -90,10 +92,12 @@ constexpr int kSplitKeys = 32;
 
 template <typename TK, int HH>
 __global__ void __launch_bounds__(128) score_split_kernel(
-    const void* __restrict__ q, int q_dtype, const float* __restrict__ w, int H, int d,
-    const TK* __restrict__ k, int64_t k_row_stride, int64_t k_rows, Geom g, int block_size,
+    const void* q, int q_dtype, const float* __restrict__ w, int H, int d,
+    const TK* k, int64_t k_row_stride, int64_t k_rows, Geom g, int block_size,
     float* __restrict__ scores, int64_t score_row_stride, bool vec) {
     constexpr int HG = HH / 4;   // heads per thread
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ __align__(16) float smem[];
     float* qs = smem;            // [d][HH], heads >= H zero
     float* ws = smem + HH * d;   // [HH]
@@ -209,9 +213,8 @@ cudaError_t run(const void* q, int q_dtype, const float* w, int H, int d, const 
         auto kern = HH == 16 ? score_split_kernel<TK, 16> : (HH == 32 ? score_split_kernel<TK, 32> : score_split_kernel<TK, 64>);
         if (sm > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         const bool vec = !(reinterpret_cast<uintptr_t>(k) & 15u) && (k_row_stride * (int64_t)sizeof(TK)) % 16 == 0;
-        kern<<<sgrid, 128, sm, st>>>(q, q_dtype, w, H, d, k, k_row_stride, k_rows, g, block_size, scores,
-                                      score_row_stride, vec);
-        return cudaGetLastError();
+        return launch_pdl(kern, sgrid, dim3(128), sm, st, q, q_dtype, w, H, d, k, k_row_stride, k_rows, g,
+                          block_size, scores, score_row_stride, vec);
     }
     const int tiles = (max_keys + kTile - 1) / kTile;
     dim3 grid((unsigned)n_rows, (unsigned)(tiles < 65535 ? tiles : 65535));
@@ -219,9 +222,8 @@ cudaError_t run(const void* q, int q_dtype, const float* w, int H, int d, const 
     case N: {                                                                                  \
         auto kern = score_generic_kernel<TK, N>;                                               \
         if (sm > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm); \
-        kern<<<grid, kTile, sm, st>>>(q, q_dtype, w, H, d, k, k_row_stride, k_rows, g, block_size, \
-                                      scores, score_row_stride, k_scale);                     \
-        break;                                                                                 \
+        return launch_pdl(kern, grid, dim3(kTile), sm, st, q, q_dtype, w, H, d, k, k_row_stride, \
+                          k_rows, g, block_size, scores, score_row_stride, k_scale);           \
     }
     switch (HH) {
         LIDX_SCORE_CASE(1)

@@ -252,6 +252,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* scores,
                                                         int32_t* n_sel) {
     __shared__ GenShared<kThreads> sh;
     const int64_t r = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();
     select_row<kBlocks, kThreads>(scores + r * score_row_stride, row_n_vis(g, r), top_k, C,
                                   idx + r * idx_row_stride, n_sel ? n_sel + r : nullptr, sh);
 }
@@ -276,6 +278,8 @@ __global__ void __launch_bounds__(kRankThreads) topk_block_rank_kernel(const flo
     __shared__ uint32_t pre_s[kRankMax / 32];
     __shared__ int32_t blk_s[kRankMax];
     const int64_t r = blockIdx.x;
+    pdl_trigger();
+    pdl_wait();
     const int n_vis = row_n_vis(g, r);
     const int n = n_vis / C;
     const int K = min(top_k / C, n);
@@ -1103,11 +1107,10 @@ cudaError_t launch_topk(const float* scores, int64_t score_row_stride, const Geo
     if (n_rows == 0) return cudaSuccess;
     if (block_size > 1) {
         if (g.max_n_kv / block_size <= kRankMax)
-            topk_block_rank_kernel<<<(unsigned)n_rows, kRankThreads, 0, st>>>(scores, score_row_stride, g, top_k,
-                                                                             block_size, idx, idx_row_stride, n_sel);
-        else
-            topk_kernel<true><<<(unsigned)n_rows, kThreads, 0, st>>>(scores, score_row_stride, g, top_k,
-                                                                     block_size, idx, idx_row_stride, n_sel);
+            return launch_pdl(topk_block_rank_kernel, dim3((unsigned)n_rows), dim3(kRankThreads), 0, st, scores,
+                              score_row_stride, g, top_k, block_size, idx, idx_row_stride, n_sel);
+        return launch_pdl(topk_kernel<true>, dim3((unsigned)n_rows), dim3(kThreads), 0, st, scores, score_row_stride,
+                          g, top_k, block_size, idx, idx_row_stride, n_sel);
     } else if (ws && ws_bytes >= mc_bytes(n_rows) && n_rows < 2 * sm_count() && g.max_n_kv >= 4 * kMcChunk) {
         // few long rows: spread the passes over the rows' chunks
         const McLayout L = mc_layout(ws, n_rows);
