@@ -173,18 +173,22 @@ def _fused_case(name):
         n_kv = [8192] * 8
     elif name == "short_ragged":
         n_kv = [16384, 5000, 2048, 2049, 0, 1, 9000, 12000]
+    elif name == "flat":      # one key row everywhere: every score of a row ties, the lowest positions win
+        n_kv = [40000, 131072, 2049]
     else:   # "ties": every key row repeated 4 times, so each score appears 4 times (ties across the cut)
         n_kv = [20000, 65536, 4096]
     B, n = len(n_kv), max(n_kv)
     q = torch.randn(B, 64, 128, generator=g).to(torch.bfloat16)
     w = torch.randn(B, 64, generator=g) / 8
     k = torch.randn(B * n, 128, generator=g).to(torch.float16)
+    if name == "flat":
+        k = k[:1].expand(B * n, 128).contiguous()
     if name == "ties":
         k = k.view(B, n, 128)[:, : n // 4].unsqueeze(2).expand(B, n // 4, 4, 128).reshape(B * n, 128).contiguous()
     return q, w, k, n_kv, 2048
 
 
-@pytest.mark.parametrize("name", ["ragged", "short_rows", "short_ragged", "ties"])
+@pytest.mark.parametrize("name", ["ragged", "short_rows", "short_ragged", "ties", "flat"])
 def test_fused_score_topk_equals_score_then_topk(name):
     # the histogram-driven select gives exactly what idx_score + idx_topk give, and what the
     # oracle's stable selection gives on the same f32 scores
@@ -205,6 +209,9 @@ def test_fused_score_topk_equals_score_then_topk(name):
     for r in range(B):
         ref = O.topk_select(sh[r], n_kv[r], top_k)
         assert int(ns1[r]) == len(ref) and idx1[r, :len(ref)].tolist() == ref.tolist(), r
+    if name == "flat":
+        for r in range(B):
+            assert idx1[r, :top_k].tolist() == list(range(top_k)), r
 
 
 def test_fused_score_topk_back_to_back_launches():
