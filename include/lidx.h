@@ -273,6 +273,36 @@ idx_status idx_topk(const float* scores, int64_t score_row_stride, idx_batch bat
                     idx_stream_t stream);
 
 /*
+ * idx_block_score_topk -- the indexer of a block-pooled decode step in one
+ * call: idx_block_pool_update (raw keys -> the persistent pooled-key cache),
+ * idx_score over the pooled keys (block_size C) and idx_topk in block mode,
+ * with their results bit for bit (llama.cpp commit c88c916636, QSA commit
+ * message: block keys are the mean of the block's raw keys, a query keeps its
+ * best floor(top_k/C) complete blocks and the tail; the pooled keys persist
+ * across decode steps, llama-memory-hybrid-idx.h).  Decode rows
+ * (n_q_per_seq 1) with 9 to 64 heads and at most 1024 blocks per row run as
+ * one launch (a cluster of CTAs per row: each re-pools and scores its share of
+ * the row's blocks, the first ranks them); other shapes run the three calls.
+ *   q, w, n_heads, head_dim   as idx_score; k_raw, k_dtype, k_row_stride,
+ *              k_rows, batch  the raw key cache as idx_block_pool_update reads
+ *              it (batch also gives n_kv, q_pos and n_q_per_seq of the rows);
+ *   n_pooled, stale_pos, block_size, pooled, pool_seq_stride  as
+ *              idx_block_pool_update (pooled is updated in place and scored
+ *              from: block beta of sequence b at pooled + (b*pool_seq_stride +
+ *              beta)*head_dim);
+ *   top_k, scores, score_row_stride, idx, idx_row_stride, n_sel  as idx_score
+ *              (block scores, floor(max_n_kv / C) per row) and idx_topk in
+ *              block mode.
+ * Errors: those of the three calls.
+ */
+idx_status idx_block_score_topk(const void* q, idx_dtype q_dtype, const float* w, int32_t n_heads, int32_t head_dim,
+                                const void* k_raw, idx_dtype k_dtype, int64_t k_row_stride, int64_t k_rows,
+                                idx_batch batch, const int32_t* n_pooled, const int32_t* stale_pos,
+                                int32_t block_size, float* pooled, int64_t pool_seq_stride, int32_t top_k,
+                                float* scores, int64_t score_row_stride, int32_t* idx, int64_t idx_row_stride,
+                                int32_t* n_sel, idx_stream_t stream);
+
+/*
  * idx_score_topk -- the fused indexer + selection: idx_score (token keys)
  * followed by idx_topk, with the same results, in one call (ik_llama_opt
  * commit log, "Route DSA indexer selection through ggml_indexer_topk": the

@@ -25,7 +25,7 @@ __all__ = [
     "Batch", "LidxError", "build", "load", "idx_hadamard", "idx_score", "idx_block_pool", "idx_block_pool_update",
     "idx_quantize_rows", "idx_score_q8", "inline_scales",
     "idx_topk", "sparse_attn_decode", "sparse_attn_prefill", "idx_workspace_size",
-    "idx_device_status", "topk_capacity", "sparse_attn_decode_noalloc", "idx_score_topk", "sparse_decode_step", "sparse_decode_step_fused",
+    "idx_device_status", "topk_capacity", "sparse_attn_decode_noalloc", "idx_score_topk", "idx_block_score_topk", "sparse_decode_step", "sparse_decode_step_fused",
 ]
 
 IDX_OK, IDX_ERR_INVALID_ARG, IDX_ERR_UNSUPPORTED, IDX_ERR_CUDA, IDX_ERR_TIMEOUT, IDX_ERR_DEVICE_BOUNDS, IDX_ERR_INEXACT = range(7)
@@ -79,6 +79,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "idx_score_q8": [P, I32, P, I32, I32, P, I64, P, I64, _Batch, I32, P, I64, P, SZ, P],
         "idx_topk": [P, I64, _Batch, I32, I32, P, I64, P, P, SZ, P],
         "idx_score_topk": [P, I32, P, I32, I32, P, I32, I64, I64, _Batch, I32, P, I64, P, I64, P, P, SZ, P],
+        "idx_block_score_topk": [P, I32, P, I32, I32, P, I32, I64, I64, _Batch, P, P, I32, P, I64, I32, P, I64, P,
+                                 I64, P, P],
         "sparse_attn_decode": [P, I32, I32, I32, I32, I32, P, P, I64, I64, I64, _Batch, P, I64, P, F,
                                P, I32, P, SZ, P],
         "sparse_attn_prefill": [P, I32, I32, I32, I32, I32, P, P, I64, I64, I64, _Batch, P, I64, P, F,
@@ -355,6 +357,38 @@ def sparse_attn_prefill(q, k, v, batch, idx, n_sel, scale, *, out=None, out_dtyp
     """Same function as sparse_attn_decode, tuned for many query rows."""
     return _attn("sparse_attn_prefill", q, k, v, batch, idx, n_sel, scale, out, out_dtype, workspace,
                  n_kv_heads, dv)
+
+
+def idx_block_score_topk(q: torch.Tensor, w: torch.Tensor, k_raw: torch.Tensor, batch: Batch, block_size: int,
+                         pooled: torch.Tensor, top_k: int, *, n_pooled: Optional[torch.Tensor] = None,
+                         stale_pos: Optional[torch.Tensor] = None, pool_seq_stride: Optional[int] = None,
+                         scores: Optional[torch.Tensor] = None, idx: Optional[torch.Tensor] = None,
+                         n_sel: Optional[torch.Tensor] = None):
+    """The indexer of a block-pooled decode step in one call: (scores, idx, n_sel) exactly as
+    idx_block_pool_update + idx_score over ``pooled`` + idx_topk in block mode give them; ``pooled``
+    is updated in place."""
+    _need_cuda(q, w, k_raw, pooled, n_pooled, stale_pos, scores, idx, n_sel)
+    rows, H, d = q.shape
+    assert rows == batch.n_rows and w.shape == (rows, H) and w.dtype == torch.float32
+    assert q.is_contiguous() and w.is_contiguous() and k_raw.stride(-1) == 1
+    assert pooled.dtype == torch.float32 and pooled.is_contiguous()
+    if pool_seq_stride is None:
+        pool_seq_stride = pooled.shape[1] if pooled.dim() == 3 else max(batch.max_n_kv // block_size, 1)
+    for t in (n_pooled, stale_pos):
+        if t is not None and (t.dtype != torch.int32 or t.numel() < batch.n_seq or not t.is_contiguous()):
+            raise ValueError("n_pooled / stale_pos must be contiguous int32 with one entry per sequence")
+    kk = 2048 if top_k == -1 else top_k
+    if scores is None:
+        scores = torch.empty(rows, max(batch.max_n_kv // block_size, 1), device=q.device, dtype=torch.float32)
+    if idx is None:
+        idx = torch.empty(rows, topk_capacity(kk, block_size), device=q.device, dtype=torch.int32)
+    if n_sel is None:
+        n_sel = torch.empty(rows, device=q.device, dtype=torch.int32)
+    _check(load().idx_block_score_topk(_ptr(q), _dtype(q), _ptr(w), H, d, _ptr(k_raw), _dtype(k_raw), k_raw.stride(0),
+                                       k_raw.shape[0], batch.c(), _ptr(n_pooled), _ptr(stale_pos), block_size,
+                                       _ptr(pooled), pool_seq_stride, top_k, _ptr(scores), scores.stride(0), _ptr(idx),
+                                       idx.stride(0), _ptr(n_sel), _stream(q.device)))
+    return scores, idx, n_sel
 
 
 def idx_score_topk(q: torch.Tensor, w: torch.Tensor, k: torch.Tensor, batch: Batch, top_k: int, *,

@@ -350,6 +350,50 @@ idx_status idx_topk(const float* scores, int64_t score_row_stride, idx_batch bat
                      what);
 }
 
+idx_status idx_block_score_topk(const void* q, idx_dtype q_dtype, const float* w, int32_t n_heads, int32_t head_dim,
+                                const void* k_raw, idx_dtype k_dtype, int64_t k_row_stride, int64_t k_rows,
+                                idx_batch batch, const int32_t* n_pooled, const int32_t* stale_pos,
+                                int32_t block_size, float* pooled, int64_t pool_seq_stride, int32_t top_k,
+                                float* scores, int64_t score_row_stride, int32_t* idx, int64_t idx_row_stride,
+                                int32_t* n_sel, idx_stream_t stream) {
+    const char* what = "idx_block_score_topk";
+    if (top_k == -1) top_k = IDX_DEFAULT_TOP_K;   // the model's configured indexer top_k
+    // the pooled keys are addressed by pool_seq_stride alone (as idx_score addresses them)
+    idx_batch pb = batch;
+    pb.kv_start = nullptr;
+    pb.kv_seq_stride = pool_seq_stride;
+    pb.page_table = nullptr;
+    pb.page_table_stride = 0;
+    pb.page_size = 0;
+    // one launch when every argument is valid for the three calls and the shape fits it
+    const int64_t rows = (int64_t)batch.n_seq * batch.n_q_per_seq;
+    const int64_t row_bytes = (int64_t)head_dim * (valid_dtype(k_dtype) ? dtype_size(k_dtype) : 0);
+    const bool ok = check_batch(batch, what) == IDX_OK && valid_dtype(q_dtype) && valid_dtype(k_dtype) &&
+                    top_k >= 1 && block_size > 1 && n_heads >= 1 && n_heads <= 64 && head_dim >= 1 &&
+                    head_dim <= 256 && row_bytes % 16 == 0 && row_bytes <= 2048 && k_row_stride >= head_dim &&
+                    (k_row_stride * (int64_t)dtype_size(k_dtype)) % 16 == 0 && k_rows >= 0 &&
+                    pool_seq_stride >= batch.max_n_kv / block_size &&
+                    score_row_stride >= batch.max_n_kv / block_size &&
+                    idx_row_stride >= (int64_t)(top_k / block_size) * block_size + block_size - 1 && rows > 0 &&
+                    q && w && k_raw && aligned16(k_raw) && pooled && scores && idx;
+    if (ok) {
+        cudaError_t e = launch_block_score_topk(q, q_dtype, w, n_heads, head_dim, k_raw, k_dtype, k_row_stride, k_rows,
+                                                make_geom(batch), block_size, n_pooled, stale_pos, pooled,
+                                                pool_seq_stride, top_k, scores, score_row_stride, idx, idx_row_stride,
+                                                n_sel, (cudaStream_t)stream);
+        if (e != cudaErrorNotSupported) return from_cuda(e, what);
+    }
+    // otherwise the three calls, with the same results (and their argument errors)
+    idx_status s = idx_block_pool_update(k_raw, k_dtype, k_row_stride, k_rows, batch, n_pooled, stale_pos, block_size,
+                                         head_dim, pooled, pool_seq_stride, stream);
+    if (s != IDX_OK) return s;
+    s = idx_score(q, q_dtype, w, n_heads, head_dim, pooled, IDX_F32, head_dim,
+                  (int64_t)batch.n_seq * pool_seq_stride, pb, block_size, scores, score_row_stride, nullptr, 0, stream);
+    if (s != IDX_OK) return s;
+    return idx_topk(scores, score_row_stride, batch, top_k, block_size, idx, idx_row_stride, n_sel, nullptr, 0,
+                    stream);
+}
+
 idx_status idx_score_topk(const void* q, idx_dtype q_dtype, const float* w, int32_t n_heads, int32_t head_dim,
                           const void* k, idx_dtype k_dtype, int64_t k_row_stride, int64_t k_rows, idx_batch batch,
                           int32_t top_k, float* scores, int64_t score_row_stride, int32_t* idx,

@@ -10,18 +10,16 @@
 // pooled keys persist across batches; an edit stales every pool at or after
 // it), so a decode step re-pools only what changed.
 //
-// One CTA of 128 threads per (block, sequence).  With 16-byte vector loads a
-// row of d elements takes TPR = d*size/16 threads, so the CTA reads
-// RP = 128/TPR rows at once; each thread sums its rows in f32 and the RP
-// partial sums are added in shared memory; a thread's loads of 8 rows are in
-// flight together.  A pure HBM stream: each raw key byte is read once and 1/C
-// of it is written (as f32).
-#include "lidx_internal.cuh"
+// One CTA of 128 threads per (block, sequence), striding over the blocks to
+// (re)pool; the arithmetic of a block is blk::pool_block (block_ops.cuh), which
+// the one-launch idx_block_score_topk shares.  A pure HBM stream: each raw key
+// byte is read once and 1/C of it is written (as f32).
+#include "block_ops.cuh"
 
 namespace lidx {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = blk::kPoolThreads;
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) pool_kernel(const T* k, int64_t k_row_stride,
@@ -35,58 +33,10 @@ __global__ void __launch_bounds__(kThreads) pool_kernel(const T* k, int64_t k_ro
     pdl_trigger();
     pdl_wait();
     const int n_cb = seq_n_kv(g, b) / C;
-    // first block to (re)pool: after the current ones, and from the stale one on
-    int beta0 = 0;
-    if (n_pooled) beta0 = max(n_pooled[b], 0);
-    if (stale_pos) {
-        const int sp = stale_pos[b];
-        beta0 = min(beta0, sp < 0 ? 0 : sp / C);
-    }
-    beta0 = min(beta0, n_cb);
-    constexpr int V = 16 / sizeof(T);
-    const int tpr = d / V;              // threads per row
-    const int rp = kThreads / tpr;      // rows per pass
-    for (int beta = beta0 + (int)blockIdx.x; beta < n_cb; beta += gridDim.x) {
-        const int rg = threadIdx.x / tpr, cv = threadIdx.x % tpr;
-        float acc[V];
-#pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] = 0.f;
-        if (rg < rp) {
-            // kBatch rows' loads in flight at once, then their sums in row order
-            constexpr int kBatch = 8;
-            for (int t0 = rg; t0 < C; t0 += kBatch * rp) {
-                uint4 raw[kBatch];
-#pragma unroll
-                for (int u = 0; u < kBatch; ++u) {
-                    raw[u] = make_uint4(0u, 0u, 0u, 0u);
-                    const int t = t0 + u * rp;
-                    if (t < C) {
-                        const int64_t row = key_row(g, b, (int64_t)beta * C + t);
-                        if (row < 0 || row >= k_rows)
-                            flag(g.status, IDX_ERR_DEVICE_BOUNDS);
-                        else
-                            raw[u] = *reinterpret_cast<const uint4*>(k + row * k_row_stride + cv * V);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kBatch; ++u) {
-                    if (t0 + u * rp >= C) break;
-                    const T* e = reinterpret_cast<const T*>(&raw[u]);
-#pragma unroll
-                    for (int i = 0; i < V; ++i) acc[i] += to_f32(e[i]);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < V; ++i) part[rg * d + cv * V + i] = acc[i];
-        }
-        __syncthreads();
-        for (int c = threadIdx.x; c < d; c += kThreads) {
-            float sum = 0.f;
-            for (int i = 0; i < rp; ++i) sum += part[i * d + c];
-            pooled[((int64_t)b * pool_seq_stride + beta) * d + c] = sum / (float)C;
-        }
-        __syncthreads();
-    }
+    const int beta0 = blk::pool_first_block(n_pooled, stale_pos, b, C, n_cb);
+    for (int beta = beta0 + (int)blockIdx.x; beta < n_cb; beta += gridDim.x)
+        blk::pool_block(k, k_row_stride, k_rows, g, C, d, b, beta, part,
+                        pooled + ((int64_t)b * pool_seq_stride + beta) * d);
 }
 
 template <typename T>

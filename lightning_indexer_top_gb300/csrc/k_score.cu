@@ -14,7 +14,7 @@
 // heads get q = 0, w = 0.  Pooled block keys (few per row) with 16 or more
 // heads take score_split_kernel instead: four threads per key, each over a
 // quarter of the heads.
-#include "lidx_internal.cuh"
+#include "block_ops.cuh"
 
 namespace lidx {
 namespace {
@@ -95,7 +95,6 @@ __global__ void __launch_bounds__(128) score_split_kernel(
     const void* q, int q_dtype, const float* __restrict__ w, int H, int d,
     const TK* k, int64_t k_row_stride, int64_t k_rows, Geom g, int block_size,
     float* __restrict__ scores, int64_t score_row_stride, bool vec) {
-    constexpr int HG = HH / 4;   // heads per thread
     pdl_trigger();
     pdl_wait();
     extern __shared__ __align__(16) float smem[];
@@ -106,39 +105,7 @@ __global__ void __launch_bounds__(128) score_split_kernel(
     int n_keys = row_n_vis(g, r);
     if (block_size > 1) n_keys /= block_size;
     if ((int)blockIdx.y * kSplitKeys >= n_keys) return;
-    if (q_dtype != IDX_F32 && d % 8 == 0 && !(reinterpret_cast<uintptr_t>(q) & 15u)) {
-        // 16-bit q: 8 elements per 16-byte load, a thread's loads issued together
-        constexpr int kQB = 8;
-        const int n8 = HH * d / 8;
-        for (int i0 = threadIdx.x; i0 < n8; i0 += kQB * blockDim.x) {
-            uint4 raw[kQB];
-#pragma unroll
-            for (int u = 0; u < kQB; ++u) {
-                const int i = i0 + u * blockDim.x;
-                const int h = (i * 8) / d, c = (i * 8) % d;
-                raw[u] = (i < n8 && h < H)
-                             ? *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(q) + (r * H + h) * (int64_t)d + c)
-                             : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int u = 0; u < kQB; ++u) {
-                const int i = i0 + u * blockDim.x;
-                if (i >= n8) break;
-                const int h = (i * 8) / d, c = (i * 8) % d;
-                const uint16_t* e = reinterpret_cast<const uint16_t*>(&raw[u]);
-#pragma unroll
-                for (int x = 0; x < 8; ++x)
-                    qs[(c + x) * HH + h] = q_dtype == IDX_BF16 ? __bfloat162float(__ushort_as_bfloat16(e[x]))
-                                                               : __half2float(__ushort_as_half(e[x]));
-            }
-        }
-    } else {
-        for (int i = threadIdx.x; i < HH * d; i += blockDim.x) {
-            const int h = i % HH, c = i / HH;
-            qs[i] = h < H ? load_any(q, (r * H + h) * (int64_t)d + c, q_dtype) : 0.f;
-        }
-    }
-    for (int i = threadIdx.x; i < HH; i += blockDim.x) ws[i] = (i < H) ? w[r * H + i] : 0.f;
+    blk::load_q_split<HH>(q, q_dtype, w, H, d, r, qs, ws);
     __syncthreads();
     const int hg = threadIdx.x & 3;
     const int j = blockIdx.y * kSplitKeys + (threadIdx.x >> 2);
@@ -151,49 +118,8 @@ __global__ void __launch_bounds__(128) score_split_kernel(
             valid = false;
         }
     }
-    float part = 0.f;
-    if (valid) {
-        const TK* kr = k + row * k_row_stride;
-        float acc[HG];
-#pragma unroll
-        for (int h = 0; h < HG; ++h) acc[h] = 0.f;
-        // 32 dimensions of the key row in flight at a time (8 loads of 4), then their products
-        constexpr int kKB = 32;
-        for (int c00 = 0; c00 < d; c00 += kKB) {
-            float kv[kKB];
-            if (vec && sizeof(TK) == 4 && c00 + kKB <= d) {
-#pragma unroll
-                for (int u = 0; u < kKB / 4; ++u) {
-                    const float4 x = *reinterpret_cast<const float4*>(kr + c00 + 4 * u);
-                    kv[4 * u] = x.x;
-                    kv[4 * u + 1] = x.y;
-                    kv[4 * u + 2] = x.z;
-                    kv[4 * u + 3] = x.w;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < kKB; ++i) kv[i] = (c00 + i < d) ? to_f32(kr[c00 + i]) : 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < kKB; ++i) {
-                if (c00 + i >= d) break;
-                const float4* qc = reinterpret_cast<const float4*>(qs + (c00 + i) * HH + hg * HG);
-#pragma unroll
-                for (int h4 = 0; h4 < HG / 4; ++h4) {
-                    const float4 qq = qc[h4];
-                    acc[4 * h4] = fmaf(qq.x, kv[i], acc[4 * h4]);
-                    acc[4 * h4 + 1] = fmaf(qq.y, kv[i], acc[4 * h4 + 1]);
-                    acc[4 * h4 + 2] = fmaf(qq.z, kv[i], acc[4 * h4 + 2]);
-                    acc[4 * h4 + 3] = fmaf(qq.w, kv[i], acc[4 * h4 + 3]);
-                }
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < HG; ++h) part = fmaf(ws[hg * HG + h], fmaxf(acc[h], 0.f), part);
-    }
-    part += __shfl_xor_sync(0xffffffffu, part, 1);
-    part += __shfl_xor_sync(0xffffffffu, part, 2);
-    if (valid && hg == 0) scores[r * score_row_stride + j] = part + 0.0f;
+    const float part = blk::score_split_sum(valid ? blk::score_split_part<TK, HH>(qs, ws, k + row * k_row_stride, d, hg, vec) : 0.f);
+    if (valid && hg == 0) scores[r * score_row_stride + j] = part;
 }
 
 template <typename TK>

@@ -24,6 +24,7 @@
 // Rows with K == n_vis (every visible key kept, e.g. the first top_k rows of a
 // causal prefill) skip the select and write 0..n_vis-1.
 #include "lidx_internal.cuh"
+#include "block_ops.cuh"
 #include "select_row.cuh"
 
 namespace lidx {
@@ -258,103 +259,17 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const float* scores,
                                   idx + r * idx_row_stride, n_sel ? n_sel + r : nullptr, sh);
 }
 
-// ---------------------------------------------------------------------------
-// Block mode with at most kRankMax complete blocks per row (the pooled keys of
-// a decode step): one CTA per row sorts the blocks in shared memory by the
-// composite key (order key, then the complement of the block index), so that
-// a larger composite is a better block and equal scores order the lower block
-// first, with a bitonic network; the first K are kept and expanded in
-// ascending block order to their C member positions, then the tail.  The same
-// selection as select_row<true> (the lower block index wins ties, -0 == +0).
-// ---------------------------------------------------------------------------
-constexpr int kRankMax = 1024;
-constexpr int kRankThreads = 1024;
-
-__global__ void __launch_bounds__(kRankThreads) topk_block_rank_kernel(const float* scores, int64_t score_row_stride,
-                                                                      Geom g, int top_k, int C, int32_t* idx,
-                                                                      int64_t idx_row_stride, int32_t* n_sel) {
-    __shared__ uint64_t comp_s[kRankMax];
-    __shared__ uint32_t sel_s[kRankMax / 32];
-    __shared__ uint32_t pre_s[kRankMax / 32];
-    __shared__ int32_t blk_s[kRankMax];
+// Block mode with at most blk::kRankMax complete blocks per row: one CTA per row (blk::block_rank_row).
+__global__ void __launch_bounds__(blk::kRankThreads) topk_block_rank_kernel(const float* scores,
+                                                                           int64_t score_row_stride, Geom g,
+                                                                           int top_k, int C, int32_t* idx,
+                                                                           int64_t idx_row_stride, int32_t* n_sel) {
+    __shared__ blk::RankShared rs;
     const int64_t r = blockIdx.x;
     pdl_trigger();
     pdl_wait();
-    const int n_vis = row_n_vis(g, r);
-    const int n = n_vis / C;
-    const int K = min(top_k / C, n);
-    const int cap = (top_k / C) * C + C - 1;
-    const int tail0 = n * C;
-    const int n_out = K * C + (n_vis - tail0);
-    const float* s = scores + r * score_row_stride;
-    int32_t* out = idx + r * idx_row_stride;
-    const int nw = (n + 31) >> 5;
-    int n_pad = 2;
-    while (n_pad < n) n_pad <<= 1;
-    for (int i = threadIdx.x; i < n_pad; i += kRankThreads)
-        comp_s[i] = i < n ? ((uint64_t)order_key(s[i]) << 32) | (uint32_t)(0xffffffffu - (uint32_t)i) : 0ull;
-    for (int i = threadIdx.x; i < nw; i += kRankThreads) sel_s[i] = 0u;
-    __syncthreads();
-    if (K == n) {
-        for (int i = threadIdx.x; i < n_vis; i += kRankThreads) out[i] = i;
-    } else {
-        if (K > 0) {
-            // bitonic sort, descending, one element per thread: the pair (i, i ^ stride) of a run of
-            // `size` keeps the larger value at the lower index when the run is an even one (the
-            // smaller otherwise); partners closer than a warp trade by shuffles, farther ones
-            // through shared memory
-            const int i = threadIdx.x;
-            uint64_t val = i < n_pad ? comp_s[i] : 0ull;
-            for (int size = 2; size <= n_pad; size <<= 1) {
-                for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                    uint64_t other;
-                    if (stride >= 32) {
-                        __syncthreads();
-                        comp_s[i] = val;
-                        __syncthreads();
-                        other = comp_s[i ^ stride];
-                    } else {
-                        other = __shfl_xor_sync(0xffffffffu, val, stride);
-                    }
-                    const bool lower = (i & stride) == 0, down = (i & size) == 0;
-                    val = (lower == down) ? (val > other ? val : other) : (val < other ? val : other);
-                }
-            }
-            __syncthreads();
-            comp_s[i] = val;
-            __syncthreads();
-            for (int i = threadIdx.x; i < K; i += kRankThreads) {
-                const int bidx = (int)(0xffffffffu - (uint32_t)comp_s[i]);
-                atomicOr(&sel_s[bidx >> 5], 1u << (bidx & 31));
-            }
-            __syncthreads();
-            if (threadIdx.x < 32) {   // exclusive prefix of selected blocks per 32-block word
-                uint32_t carry = 0;
-                for (int w0 = 0; w0 < nw; w0 += 32) {
-                    const int w = w0 + threadIdx.x;
-                    const uint32_t c = w < nw ? (uint32_t)__popc(sel_s[w]) : 0u;
-                    uint32_t x = c;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-                        if ((int)threadIdx.x >= o) x += y;
-                    }
-                    if (w < nw) pre_s[w] = carry + x - c;
-                    carry += __shfl_sync(0xffffffffu, x, 31);
-                }
-            }
-            __syncthreads();
-            for (int b = threadIdx.x; b < n; b += kRankThreads) {
-                const uint32_t word = sel_s[b >> 5];
-                if ((word >> (b & 31)) & 1u) blk_s[pre_s[b >> 5] + __popc(word & ((1u << (b & 31)) - 1u))] = b;
-            }
-            __syncthreads();
-            for (int o = threadIdx.x; o < K * C; o += kRankThreads) out[o] = blk_s[o / C] * C + o % C;
-        }
-        for (int i = threadIdx.x; i < n_vis - tail0; i += kRankThreads) out[K * C + i] = tail0 + i;
-    }
-    for (int i = n_out + threadIdx.x; i < cap; i += kRankThreads) out[i] = -1;
-    if (n_sel && threadIdx.x == 0) n_sel[r] = n_out;
+    blk::block_rank_row<blk::kRankThreads>(scores + r * score_row_stride, row_n_vis(g, r), top_k, C, idx + r * idx_row_stride,
+                        n_sel ? n_sel + r : nullptr, rs);
 }
 
 // ---------------------------------------------------------------------------
@@ -1106,8 +1021,8 @@ cudaError_t launch_topk(const float* scores, int64_t score_row_stride, const Geo
     const int64_t n_rows = (int64_t)g.B * g.T;
     if (n_rows == 0) return cudaSuccess;
     if (block_size > 1) {
-        if (g.max_n_kv / block_size <= kRankMax)
-            return launch_pdl(topk_block_rank_kernel, dim3((unsigned)n_rows), dim3(kRankThreads), 0, st, scores,
+        if (g.max_n_kv / block_size <= blk::kRankMax)
+            return launch_pdl(topk_block_rank_kernel, dim3((unsigned)n_rows), dim3(blk::kRankThreads), 0, st, scores,
                               score_row_stride, g, top_k, block_size, idx, idx_row_stride, n_sel);
         return launch_pdl(topk_kernel<true>, dim3((unsigned)n_rows), dim3(kThreads), 0, st, scores, score_row_stride,
                           g, top_k, block_size, idx, idx_row_stride, n_sel);

@@ -161,6 +161,14 @@ cudaError_t launch_block_pool(const void* k_raw, int k_dtype, int64_t k_row_stri
                               const Geom& g, int C, int d, float* pooled, int64_t pool_seq_stride,
                               const int32_t* n_pooled, const int32_t* stale_pos, cudaStream_t st);
 
+// pool update + pooled-key scores + block selection in one launch (k_block_select.cu);
+// cudaErrorNotSupported for shapes it does not take
+cudaError_t launch_block_score_topk(const void* q, int q_dtype, const float* w, int H, int d, const void* k_raw,
+                                    int k_dtype, int64_t k_row_stride, int64_t k_rows, const Geom& g, int C,
+                                    const int32_t* n_pooled, const int32_t* stale_pos, float* pooled,
+                                    int64_t pool_seq_stride, int top_k, float* scores, int64_t score_row_stride,
+                                    int32_t* idx, int64_t idx_row_stride, int32_t* n_sel, cudaStream_t st);
+
 // few rows with a workspace of topk_workspace_bytes(): multi-CTA passes; else one CTA per row
 cudaError_t launch_topk(const float* scores, int64_t score_row_stride, const Geom& g, int top_k,
                         int block_size, int32_t* idx, int64_t idx_row_stride, int32_t* n_sel, void* ws,

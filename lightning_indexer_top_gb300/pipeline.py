@@ -10,8 +10,8 @@ from __future__ import annotations
 
 import torch
 
-from . import Batch, idx_block_pool, idx_block_pool_update, idx_hadamard, idx_score, idx_score_q8, idx_topk, idx_workspace_size, topk_capacity
-from . import idx_score_topk, IDX_OP_SCORE_TOPK, sparse_decode_step, sparse_decode_step_fused, IDX_OP_DECODE_STEP
+from . import Batch, idx_block_pool, idx_hadamard, idx_score, idx_score_q8, idx_topk, idx_workspace_size, topk_capacity
+from . import idx_block_score_topk, idx_score_topk, IDX_OP_SCORE_TOPK, sparse_decode_step, sparse_decode_step_fused, IDX_OP_DECODE_STEP
 from . import sparse_attn_decode, sparse_attn_prefill, IDX_OP_ATTN_DECODE, IDX_OP_ATTN_PREFILL, IDX_OP_TOPK
 from .workloads import Workload
 
@@ -82,13 +82,11 @@ class SparseAttentionStep:
         q = wl.q_idx if self.q_rot is None else self.q_rot
         k = wl.k_idx if self.k_rot is None else self.k_rot
         if wl.block_size > 1:
-            if self.pool_mode == "update":
-                idx_block_pool_update(k, self.batch, wl.block_size, self.pooled, n_pooled=self.n_pooled,
-                                      pool_seq_stride=self.pool_stride)
-            else:
-                idx_block_pool(k, self.batch, wl.block_size, pool_seq_stride=self.pool_stride, pooled=self.pooled)
-            kp = self.pooled.view(-1, wl.d)
-            idx_score(q, wl.w, kp, self.pool_batch, block_size=wl.block_size, scores=self.scores)
+            # pool update (or a full pooling), pooled-key scores and block selection in one call
+            n_pooled = self.n_pooled if self.pool_mode == "update" else None
+            idx_block_score_topk(q, wl.w, k, self.batch, wl.block_size, self.pooled, wl.top_k, n_pooled=n_pooled,
+                                 pool_seq_stride=self.pool_stride, scores=self.scores, idx=self.idx,
+                                 n_sel=self.n_sel)
         elif wl.k8 is not None:
             idx_score_q8(q, wl.w, wl.k8, wl.k_scale, self.batch, scores=self.scores)
         elif self.one_call:
@@ -102,7 +100,7 @@ class SparseAttentionStep:
             idx_score(q, wl.w, k, self.batch, scores=self.scores)
 
     def select(self):
-        if self.fused:
+        if self.fused or self.wl.block_size > 1:
             return   # selected by the fused call in score()
         idx_topk(self.scores, self.batch, self.wl.top_k, block_size=self.wl.block_size, idx=self.idx,
                  n_sel=self.n_sel, workspace=self.topk_ws)
@@ -131,6 +129,12 @@ class SparseAttentionStep:
         if self.one_launch:
             return 1
         n = 3 + (1 if self.attn_ws is not None else 0)   # score, select, attend (+ split combine)
+        wl = self.wl
+        if wl.block_size > 1:
+            # pool update + pooled-key scores + block select: one launch for decode rows of 9-64 heads and
+            # at most 1024 blocks, else three
+            one = wl.T == 1 and 9 <= wl.H <= 64 and wl.max_n_kv // wl.block_size <= 1024
+            return (1 if one else 3) + n - 2 + (2 if self.q_rot is not None else 0)
         if self.fused:
             # fused select: one kernel for rows up to 16384 keys, else bound, filter, finish
             n += 0 if self.wl.max_n_kv <= 16384 else 2
@@ -138,6 +142,4 @@ class SparseAttentionStep:
             n += 2                              # multi-CTA select: bound, filter, finish
         if self.q_rot is not None:
             n += 2                              # two Hadamard rotations
-        if self.wl.block_size > 1:
-            n += 1                              # block pool
         return n

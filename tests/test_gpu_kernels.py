@@ -1028,3 +1028,69 @@ def test_quantize_and_score_with_inline_scales():
         ref = O.indexer_scores(np64(q[b]), np64(w[b]), kd[starts[b]:starts[b] + nk])
         assert_scores_close(s_in[b, :nk].cpu().numpy(), ref, f"inline seq {b}")
         assert_scores_close(s_gen[b, :nk].cpu().numpy(), ref, f"inline generic seq {b}")
+
+
+def _block_step_case(name):
+    """(q, w, raw keys, n_kv, H, mode, stale) for the one-call block-pooled indexer."""
+    g = torch.Generator().manual_seed(1234)
+    H, kdt, mode, stale = 32, torch.bfloat16, "update", None
+    n_kv = [32768 - 4 * s for s in range(16)]
+    if name == "ragged_full":          # blocks of one key row short, empty rows, dense rows, a full pooling
+        n_kv, mode = [20000, 63, 0, 64, 2111, 2112, 2175, 32768], "full"
+    elif name == "stale_f16_64heads":  # edits re-pool from the stale block on
+        H, kdt, stale = 64, torch.float16, [100, 2 ** 31 - 1, 0, 30000, 5000, -1, 64, 32767]
+        n_kv = [32768, 32000, 20000, 32768, 8000, 4096, 128, 32768]
+    elif name == "f32_12heads":
+        H, kdt = 12, torch.float32
+    elif name == "8heads_three_calls":  # below the one launch's head range: the three calls inside
+        H = 8
+    elif name == "rows_200":           # more rows than SMs: one CTA per row
+        n_kv = [4096 - 8 * (s % 7) for s in range(200)]
+    B, n = len(n_kv), max(n_kv)
+    q = torch.randn(B, H, 128, generator=g).to(torch.bfloat16)
+    w = torch.randn(B, H, generator=g) / math.sqrt(H)
+    k = torch.randn(B * n, 128, generator=g).to(kdt)
+    return q, w, k, n_kv, H, mode, stale
+
+
+@pytest.mark.parametrize("name", ["decode16", "ragged_full", "stale_f16_64heads", "f32_12heads",
+                                  "8heads_three_calls", "rows_200"])
+def test_block_score_topk_equals_the_three_calls(name):
+    # pool update + pooled-key score + block select in one call: the pooled cache, the block scores
+    # and the selection bit for bit those of idx_block_pool_update, idx_score and idx_topk
+    q, w, k, n_kv, H, mode, stale = _block_step_case(name)
+    B, n, C, top_k = len(n_kv), max(n_kv), 64, 2048
+    ps = n // C
+    batch = L.Batch(_i32(n_kv), 1, n, kv_seq_stride=n)
+    pool_batch = L.Batch(_i32(n_kv), 1, n, kv_seq_stride=ps)
+    qd, wd, kd = q.to(DEV), w.to(DEV), k.to(DEV)
+    pooled0 = L.idx_block_pool(kd, batch, C, pool_seq_stride=ps)
+    n_cb = [x // C for x in n_kv]
+    n_pooled = stale_pos = None
+    if mode == "update":
+        n_pooled = _i32([max(c - 1, 0) for c in n_cb] if stale is None else n_cb)
+        first = [max(c - 1, 0) for c in n_cb] if stale is None else \
+            [min(c, 0 if s < 0 else s // C) for c, s in zip(n_cb, stale)]
+        for b in range(B):   # what must be re-pooled holds garbage before the call
+            pooled0[b, first[b]:n_cb[b]] = 1e6
+        if stale is not None:
+            stale_pos = _i32(stale)
+    else:
+        pooled0.fill_(1e6)
+    pooled_ref, pooled_one = pooled0.clone(), pooled0.clone()
+    L.idx_block_pool_update(kd, batch, C, pooled_ref, n_pooled=n_pooled, stale_pos=stale_pos, pool_seq_stride=ps)
+    s_ref = L.idx_score(qd, wd, pooled_ref.view(-1, 128), pool_batch, block_size=C)
+    i_ref, ns_ref = L.idx_topk(s_ref, batch, top_k, block_size=C)
+    s_one, i_one, ns_one = L.idx_block_score_topk(qd, wd, kd, batch, C, pooled_one, top_k, n_pooled=n_pooled,
+                                                  stale_pos=stale_pos, pool_seq_stride=ps)
+    torch.cuda.synchronize()
+    assert L.idx_device_status(reset=True) == 0
+    assert torch.equal(pooled_ref, pooled_one)
+    for r in range(B):
+        assert torch.equal(s_ref[r, :n_cb[r]], s_one[r, :n_cb[r]]), r
+    assert torch.equal(ns_ref, ns_one) and torch.equal(i_ref, i_one)
+    # and the selection is the oracle's block selection of those scores
+    sh = s_one.cpu().numpy()
+    for r in range(0, B, max(1, B // 8)):
+        ref = O.block_select(sh[r, :n_cb[r]], n_kv[r], top_k, C)
+        assert int(ns_one[r]) == len(ref) and i_one[r, :len(ref)].tolist() == list(ref), r
