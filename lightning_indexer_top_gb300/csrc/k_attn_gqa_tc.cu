@@ -62,6 +62,8 @@ struct Ctl {
     uint8_t over[2][4];           // per warp: a key of the tile lifts a head past the rescale margin
     float red[2][4][kN];          // per-warp maxima of a tile (two tiles in turn)
     float lred[4][kN];            // per-warp row sums at the end
+    float xo[kN][kD];             // split pairs, rank 0: rank 1's unnormalised output ...
+    float xml[kN][2];             // ... and its maximum (natural-log units) and sum per head
     uint32_t tmem_base;
     int abort;
 };
@@ -84,7 +86,14 @@ template <> __device__ __forceinline__ uint16_t to_bits<__nv_bfloat16>(float x) 
 }
 template <> __device__ __forceinline__ uint16_t to_bits<__half>(float x) { return __half_as_ushort(__float2half_rn(x)); }
 
-template <typename T>
+// the two key splits of a (row, kv head) as a cluster pair: rank 1 hands its unnormalised output,
+// maximum and sum to rank 0 over DSMEM and rank 0 merges them (the combine's arithmetic)
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+template <typename T, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) attn_gqa_tc_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, int64_t kv_row_stride,
     int64_t v_row_stride, int64_t kv_rows, Geom g, const int32_t* idx, int64_t idx_row_stride, const int32_t* n_sel,
@@ -101,6 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_gqa_tc_kernel(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t unit = blockIdx.x;
     const int split = (int)(unit % splits);
+    if (kPair) cluster_arrive_relaxed();   // (phase 0: this CTA has started)
     const int64_t rg = unit / splits;
     const int gkv = (int)(rg % Hkv);
     const int64_t r = rg / Hkv;
@@ -205,6 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_gqa_tc_kernel(
             cp_async_mbar_arrive_noinc(&c.xfull[stage]);
         }
         cp_async_wait_all();
+        if (kPair) {
+            cluster_wait();
+            cluster_sync();
+        }
     } else if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------------------------ MMA issuer
@@ -258,6 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_gqa_tc_kernel(
             mbar_wait(&c.done, 0);
         }
         __syncwarp();
+        if (kPair) {
+            cluster_wait();
+            cluster_sync();
+        }
     } else {
         // ------------------------------------------------------------------ softmax (thread = key)
         const int quad = warp & 3;
@@ -407,9 +425,52 @@ __global__ void __launch_bounds__(kThreads, 1) attn_gqa_tc_kernel(
         } else {
             have = false;
         }
+        if (kPair) {
+            cluster_wait();   // (phase 0: both CTAs have started)
+            if (split == 1) {
+#pragma unroll
+                for (int h = 0; h < kN; ++h) {
+                    if (h >= G) continue;
+                    const float l = have ? (c.lred[0][h] + c.lred[1][h]) + (c.lred[2][h] + c.lred[3][h]) : 0.f;
+                    st_cluster_f32(mapa(&c.xo[h][kk], 0), o[h]);
+                    if (kk == 0) {
+                        st_cluster_f32(mapa(&c.xml[h][0], 0), m_used[h] * 0.6931471805599453f);
+                        st_cluster_f32(mapa(&c.xml[h][1], 0), l);
+                    }
+                }
+            }
+            cluster_sync();   // (phase 1: rank 1's output is in rank 0's shared memory)
+            if (split == 0) {
+#pragma unroll
+                for (int h = 0; h < kN; ++h) {
+                    if (h >= G) continue;
+                    const float l0 = have ? (c.lred[0][h] + c.lred[1][h]) + (c.lred[2][h] + c.lred[3][h]) : 0.f;
+                    const float m0 = m_used[h] * 0.6931471805599453f;
+                    const float m1 = c.xml[h][0], l1 = c.xml[h][1];
+                    float M = 0.f;
+                    bool any = false;
+                    if (l0 > 0.f) {
+                        M = m0;
+                        any = true;
+                    }
+                    if (l1 > 0.f) M = any ? fmaxf(M, m1) : m1;
+                    float den = 0.f, acc = 0.f;
+                    if (l0 > 0.f) den += expf(m0 - M) * l0;
+                    if (l1 > 0.f) den += expf(m1 - M) * l1;
+                    const float inv = den > 0.f ? 1.f / den : 0.f;
+                    if (l0 > 0.f) acc += expf(m0 - M) * o[h];
+                    if (l1 > 0.f) acc += expf(m1 - M) * c.xo[h][kk];
+                    const int64_t dst = (r * Hq + h0 + h) * (int64_t)kD + kk;
+                    if (out_dtype == IDX_BF16)
+                        static_cast<__nv_bfloat16*>(out)[dst] = __float2bfloat16_rn(acc * inv);
+                    else
+                        static_cast<float*>(out)[dst] = acc * inv;
+                }
+            }
+        }
 #pragma unroll
         for (int h = 0; h < kN; ++h) {
-            if (h >= G) continue;
+            if (h >= G || kPair) continue;
             const float l = have ? (c.lred[0][h] + c.lred[1][h]) + (c.lred[2][h] + c.lred[3][h]) : 0.f;
             if (splits == 1) {
                 const float val = l > 0.f ? o[h] / l : 0.f;
@@ -459,6 +520,37 @@ int gqa_tc_splits(int64_t units, int64_t cap) {
     return s < 1 ? 1 : (int)s;
 }
 
+namespace {
+
+// the kernel with programmatic stream serialisation, as 2-CTA clusters when kPair
+template <typename T, bool kPair>
+cudaError_t launch_gqa(int64_t grid, const void* q, const void* k, const void* v, int64_t kv_row_stride,
+                       int64_t v_row_stride, int64_t kv_rows, const Geom& g, const int32_t* idx, int64_t idx_row_stride,
+                       const int32_t* n_sel, int Hq, int Hkv, float scale_log2, int splits, int kps, void* out,
+                       int out_dtype, float* part_o, float* part_ml, cudaStream_t st) {
+    auto kern = attn_gqa_tc_kernel<T, kPair>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = kPair ? 2 : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = kPair ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<const T*>(q), static_cast<const T*>(k),
+                              static_cast<const T*>(v), kv_row_stride, v_row_stride, kv_rows, g, idx, idx_row_stride,
+                              n_sel, Hq, Hkv, scale_log2, splits, kps, out, out_dtype, part_o, part_ml);
+}
+
+}  // namespace
+
 cudaError_t launch_attn_gqa_tc(const void* q, int dtype, int Hq, int Hkv, const void* k, const void* v,
                                int64_t kv_row_stride, int64_t v_row_stride, int64_t kv_rows, const Geom& g,
                                const int32_t* idx, int64_t idx_row_stride, const int32_t* n_sel, float scale,
@@ -478,26 +570,27 @@ cudaError_t launch_attn_gqa_tc(const void* q, int dtype, int Hq, int Hkv, const 
     if (kps > kMaxKps) return cudaErrorNotSupported;
     const int64_t grid = n_rows * Hkv * splits;
     if (grid > INT32_MAX) return cudaErrorNotSupported;
-    float* part_o = splits > 1 ? static_cast<float*>(ws) : nullptr;
-    float* part_ml = splits > 1 ? part_o + (size_t)n_rows * splits * Hq * kD : nullptr;
+    // two splits: a 2-CTA cluster per (row, kv head) merges them itself; more: partials + combine
+    const bool pair = splits == 2;
+    float* part_o = splits > 2 ? static_cast<float*>(ws) : nullptr;
+    float* part_ml = splits > 2 ? part_o + (size_t)n_rows * splits * Hq * kD : nullptr;
     const float scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e;
-    if (dtype == IDX_BF16) {
-        auto kern = attn_gqa_tc_kernel<__nv_bfloat16>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        e = launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st,
-                       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-                       static_cast<const __nv_bfloat16*>(v), kv_row_stride, v_row_stride, kv_rows, g, idx,
-                       idx_row_stride, n_sel, Hq, Hkv, scale_log2, splits, kps, out, out_dtype, part_o, part_ml);
-    } else {
-        auto kern = attn_gqa_tc_kernel<__half>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        e = launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, st, static_cast<const __half*>(q),
-                       static_cast<const __half*>(k), static_cast<const __half*>(v), kv_row_stride, v_row_stride,
-                       kv_rows, g, idx, idx_row_stride, n_sel, Hq, Hkv, scale_log2, splits, kps, out, out_dtype,
-                       part_o, part_ml);
-    }
-    if (e != cudaSuccess || splits == 1) return e;
+    if (dtype == IDX_BF16)
+        e = pair ? launch_gqa<__nv_bfloat16, true>(grid, q, k, v, kv_row_stride, v_row_stride, kv_rows, g, idx,
+                                                   idx_row_stride, n_sel, Hq, Hkv, scale_log2, splits, kps, out,
+                                                   out_dtype, part_o, part_ml, st)
+                 : launch_gqa<__nv_bfloat16, false>(grid, q, k, v, kv_row_stride, v_row_stride, kv_rows, g, idx,
+                                                    idx_row_stride, n_sel, Hq, Hkv, scale_log2, splits, kps, out,
+                                                    out_dtype, part_o, part_ml, st);
+    else
+        e = pair ? launch_gqa<__half, true>(grid, q, k, v, kv_row_stride, v_row_stride, kv_rows, g, idx,
+                                            idx_row_stride, n_sel, Hq, Hkv, scale_log2, splits, kps, out, out_dtype,
+                                            part_o, part_ml, st)
+                 : launch_gqa<__half, false>(grid, q, k, v, kv_row_stride, v_row_stride, kv_rows, g, idx,
+                                             idx_row_stride, n_sel, Hq, Hkv, scale_log2, splits, kps, out, out_dtype,
+                                             part_o, part_ml, st);
+    if (e != cudaSuccess || splits <= 2) return e;
     return launch_attn_generic_combine(part_o, part_ml, splits, n_rows, Hq, kD, out, out_dtype, st);
 }
 

@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_topk_kernel(
             valid ? blk::score_split_part<float, HH>(qs, ws, prow + (int64_t)j * d, d, hg, vec) : 0.f);
         if (valid && hg == 0) {
             scores[r * score_row_stride + j] = v;
-            asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(sc0 + 4u * (uint32_t)j), "f"(v) : "memory");
+            sm100::st_cluster_f32(sc0 + 4u * (uint32_t)j, v);
         }
     }
     // 3. rank 0 selects once every CTA's scores are in its shared memory

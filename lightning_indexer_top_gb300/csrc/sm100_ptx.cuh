@@ -369,6 +369,11 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint4 v, uint32_t bar
                  : "memory");
 }
 
+// a plain 32-bit store into another CTA's shared memory (address from mapa)
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar_cluster) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
                  "r"(__float_as_uint(v)), "r"(bar_cluster)

@@ -124,16 +124,34 @@ class SparseAttentionStep:
         self.attend()
         return self.out
 
+    def _gqa_split_pair(self) -> bool:
+        """Whether the tensor-core GQA attention runs its rows' keys as two splits, which a 2-CTA
+        cluster merges itself (no combine launch): the library's split rule for that kernel."""
+        wl = self.wl
+        if wl.v_attn is None or wl.dv != 128 or wl.q_attn.shape[2] != 128 or wl.q_attn.dtype == torch.float32:
+            return False
+        rows, hq, hkv = wl.B * wl.T, wl.q_attn.shape[1], wl.v_attn.shape[1]
+        if hq % hkv or hq // hkv > 16:
+            return False
+        cap = self.idx.shape[1]
+        sms = torch.cuda.get_device_properties(self.idx.device).multi_processor_count
+        s = max(min(sms // max(rows * hkv, 1), -(-cap // 256)), -(-cap // 2048), 1)
+        if s > 1:
+            fit = (self.attn_ws.numel() if self.attn_ws is not None else 0) // (rows * hq * 130 * 4)
+            s = min(s, fit) if fit > 1 else 1
+        return s == 2
+
     def launches_per_step(self) -> int:
         """Kernels one run() enqueues (library launches only)."""
         if self.one_launch:
             return 1
-        n = 3 + (1 if self.attn_ws is not None else 0)   # score, select, attend (+ split combine)
         wl = self.wl
+        combine = 1 if self.attn_ws is not None and not self._gqa_split_pair() else 0
+        n = 3 + combine   # score, select, attend (+ split combine)
         if wl.block_size > 1:
             # pool update + pooled-key scores + block select: one launch for decode rows of 9-64 heads and
-            # at most 1024 blocks, else three
-            one = wl.T == 1 and 9 <= wl.H <= 64 and wl.max_n_kv // wl.block_size <= 1024
+            # at most 512 blocks, else three
+            one = wl.T == 1 and 9 <= wl.H <= 64 and wl.max_n_kv // wl.block_size <= 512
             return (1 if one else 3) + n - 2 + (2 if self.q_rot is not None else 0)
         if self.fused:
             # fused select: one kernel for rows up to 16384 keys, else bound, filter, finish
