@@ -178,6 +178,69 @@ __device__ __forceinline__ float score_split_part(const float* qs, const float* 
     return part;
 }
 
+// score_split_part for two keys at once (kr0, kr1), each with exactly its arithmetic (the same fmaf
+// chain per key and head, in dimension order): the q values read from shared memory serve both keys
+template <typename TK, int HH>
+__device__ __forceinline__ void score_split_part2(const float* qs, const float* ws, const TK* kr0, const TK* kr1,
+                                                  int d, int hg, bool vec, float& part0, float& part1) {
+    constexpr int HG = HH / 4;
+    float a0[HG], a1[HG];
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+        a0[h] = 0.f;
+        a1[h] = 0.f;
+    }
+    constexpr int kKB = 16;
+    for (int c00 = 0; c00 < d; c00 += kKB) {
+        float k0[kKB], k1[kKB];
+        if (vec && sizeof(TK) == 4 && c00 + kKB <= d) {
+#pragma unroll
+            for (int u = 0; u < kKB / 4; ++u) {
+                const float4 x = *reinterpret_cast<const float4*>(kr0 + c00 + 4 * u);
+                const float4 y = *reinterpret_cast<const float4*>(kr1 + c00 + 4 * u);
+                k0[4 * u] = x.x;
+                k0[4 * u + 1] = x.y;
+                k0[4 * u + 2] = x.z;
+                k0[4 * u + 3] = x.w;
+                k1[4 * u] = y.x;
+                k1[4 * u + 1] = y.y;
+                k1[4 * u + 2] = y.z;
+                k1[4 * u + 3] = y.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kKB; ++i) {
+                k0[i] = (c00 + i < d) ? to_f32(kr0[c00 + i]) : 0.f;
+                k1[i] = (c00 + i < d) ? to_f32(kr1[c00 + i]) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kKB; ++i) {
+            if (c00 + i >= d) break;
+            const float4* qc = reinterpret_cast<const float4*>(qs + (c00 + i) * HH + hg * HG);
+#pragma unroll
+            for (int h4 = 0; h4 < HG / 4; ++h4) {
+                const float4 qq = qc[h4];
+                a0[4 * h4] = fmaf(qq.x, k0[i], a0[4 * h4]);
+                a0[4 * h4 + 1] = fmaf(qq.y, k0[i], a0[4 * h4 + 1]);
+                a0[4 * h4 + 2] = fmaf(qq.z, k0[i], a0[4 * h4 + 2]);
+                a0[4 * h4 + 3] = fmaf(qq.w, k0[i], a0[4 * h4 + 3]);
+                a1[4 * h4] = fmaf(qq.x, k1[i], a1[4 * h4]);
+                a1[4 * h4 + 1] = fmaf(qq.y, k1[i], a1[4 * h4 + 1]);
+                a1[4 * h4 + 2] = fmaf(qq.z, k1[i], a1[4 * h4 + 2]);
+                a1[4 * h4 + 3] = fmaf(qq.w, k1[i], a1[4 * h4 + 3]);
+            }
+        }
+    }
+    part0 = 0.f;
+    part1 = 0.f;
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+        part0 = fmaf(ws[hg * HG + h], fmaxf(a0[h], 0.f), part0);
+        part1 = fmaf(ws[hg * HG + h], fmaxf(a1[h], 0.f), part1);
+    }
+}
+
 // the four partials of a key (lanes 4i..4i+3), added; every lane of the warp must call it
 __device__ __forceinline__ float score_split_sum(float part) {
     part += __shfl_xor_sync(0xffffffffu, part, 1);

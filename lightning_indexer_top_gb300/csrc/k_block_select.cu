@@ -12,7 +12,7 @@
 // two up to 8 whose clusters are all resident at once.  CTA q of a row owns the row's blocks
 // [q*per, (q+1)*per): it re-pools those at or after the sequence's first
 // stale block (writing the pooled cache as the update does), scores its
-// blocks four threads per block key and writes each score both to the scores
+// blocks (four threads per block key, two keys per thread) and writes each score both to the scores
 // output and into rank 0's shared memory; after a cluster barrier rank 0 ranks
 // the row's blocks and writes the selection.  Decode rows only (one query row
 // per sequence: the pooled cache is per sequence, so rows of one sequence
@@ -37,8 +37,9 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_topk_kernel(
     float* qs = smem;                  // [d][HH], heads >= H zero
     float* ws = qs + HH * d;           // [HH]
     float* part = ws + HH;             // pool partial sums
-    float* sc = part + kPartFloats;    // rank 0: the row's block scores
+    float* sc = part + kPartFloats;    // the row's block scores (every CTA of the cluster)
     __shared__ blk::RankShared rs;
+    __shared__ uint32_t cnts[kMaxCl];
     pdl_trigger();
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");   // this CTA has started
     pdl_wait();
@@ -61,22 +62,96 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_topk_kernel(
     blk::load_q_split<HH>(q, q_dtype, w, H, d, r, qs, ws);
     __syncthreads();
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");   // rank 0's shared memory is live
-    const uint32_t sc0 = sm100::mapa(sc, 0);
+    uint32_t scq[kMaxCl];   // sc in each CTA of the cluster
+#pragma unroll
+    for (int q2 = 0; q2 < kMaxCl; ++q2) scq[q2] = q2 < (int)cl ? sm100::mapa(sc, (uint32_t)q2) : 0u;
     const int je = min(j1, n_cb);
-    for (int jb = j0; jb < je; jb += kThreads / 4) {
-        const int j = jb + (int)(threadIdx.x >> 2), hg = threadIdx.x & 3;
-        const bool valid = j < je;
-        const float v = blk::score_split_sum(
-            valid ? blk::score_split_part<float, HH>(qs, ws, prow + (int64_t)j * d, d, hg, vec) : 0.f);
-        if (valid && hg == 0) {
-            scores[r * score_row_stride + j] = v;
-            sm100::st_cluster_f32(sc0 + 4u * (uint32_t)j, v);
+    // two keys per thread (keys i and i + half of a pass of up to kThreads/2 keys): the q values a
+    // thread reads serve both
+    for (int jb = j0; jb < je; jb += kThreads / 2) {
+        const int nk = min(kThreads / 2, je - jb), half = (nk + 1) >> 1;
+        const int i = (int)(threadIdx.x >> 2), hg = threadIdx.x & 3;
+        const int ja = jb + i, jc = jb + half + i;
+        const bool va = i < half, vc = va && half + i < nk;
+        float pa = 0.f, pc = 0.f;
+        if (va)
+            blk::score_split_part2<float, HH>(qs, ws, prow + (int64_t)ja * d, prow + (int64_t)(vc ? jc : ja) * d, d,
+                                              hg, vec, pa, pc);
+        pa = blk::score_split_sum(pa);
+        pc = blk::score_split_sum(pc);
+        if (hg == 0) {
+            if (va) scores[r * score_row_stride + ja] = pa;
+            if (vc) scores[r * score_row_stride + jc] = pc;
+#pragma unroll
+            for (int q2 = 0; q2 < kMaxCl; ++q2) {
+                if (q2 >= (int)cl) break;
+                if (va) sm100::st_cluster_f32(scq[q2] + 4u * (uint32_t)ja, pa);
+                if (vc) sm100::st_cluster_f32(scq[q2] + 4u * (uint32_t)jc, pc);
+            }
         }
     }
-    // 3. rank 0 selects once every CTA's scores are in its shared memory
+    // 3. every CTA holds all the row's block scores: it ranks its own blocks against all of them by
+    //    the composite key (order key, then the complement of the block index: a larger composite is
+    //    a better block, equal scores put the lower block first); block j is kept when fewer than K
+    //    composites exceed its own (the same selection as blk::block_rank_row)
     sm100::cluster_sync();
-    if (rank != 0) return;
-    blk::block_rank_row<kThreads>(sc, n_vis, top_k, C, idx + r * idx_row_stride, n_sel ? n_sel + r : nullptr, rs);
+    const int K = min(top_k / C, n_cb);
+    for (int i = threadIdx.x; i < n_cb; i += kThreads)
+        rs.comp[i] = ((uint64_t)order_key(sc[i]) << 32) | (uint32_t)(0xffffffffu - (uint32_t)i);
+    for (int i = threadIdx.x; i < blk::kRankMax / 32; i += kThreads) rs.sel[i] = 0u;
+    __syncthreads();
+    for (int jb = j0; jb < je; jb += kThreads / 4) {   // four threads per block, each a quarter of the keys
+        const int j = jb + (int)(threadIdx.x >> 2), pt = threadIdx.x & 3;
+        uint32_t above = 0;
+        if (j < je) {
+            const uint64_t cj = rs.comp[j];
+            for (int i = pt; i < n_cb; i += 4) above += rs.comp[i] > cj ? 1u : 0u;
+        }
+        above += __shfl_xor_sync(0xffffffffu, above, 1);
+        above += __shfl_xor_sync(0xffffffffu, above, 2);
+        if (j < je && pt == 0 && above < (uint32_t)K) atomicOr(&rs.sel[(j - j0) >> 5], 1u << ((j - j0) & 31));
+    }
+    __syncthreads();
+    // this CTA's kept blocks in ascending order (a scan of the selection words), their count to every CTA
+    const int nw = (max(je - j0, 0) + 31) >> 5;
+    if (threadIdx.x < 32) {
+        uint32_t carry = 0;
+        for (int w0 = 0; w0 < nw; w0 += 32) {
+            const int w = w0 + (int)threadIdx.x;
+            const uint32_t c = w < nw ? (uint32_t)__popc(rs.sel[w]) : 0u;
+            uint32_t x = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                if ((int)threadIdx.x >= o) x += y;
+            }
+            if (w < nw) rs.pre[w] = carry + x - c;
+            carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (threadIdx.x < cl) sm100::st_cluster_f32(sm100::mapa(&cnts[rank], threadIdx.x), __uint_as_float(carry));
+    }
+    __syncthreads();
+    for (int j = j0 + (int)threadIdx.x; j < je; j += kThreads) {
+        const uint32_t word = rs.sel[(j - j0) >> 5];
+        if ((word >> ((j - j0) & 31)) & 1u)
+            rs.blk[rs.pre[(j - j0) >> 5] + __popc(word & ((1u << ((j - j0) & 31)) - 1u))] = j;
+    }
+    sm100::cluster_sync();   // (every CTA's count is in every CTA)
+    uint32_t base = 0, mine = cnts[rank];
+    for (uint32_t q2 = 0; q2 < rank; ++q2) base += cnts[q2];
+    int32_t* out = idx + r * idx_row_stride;
+    for (int e = threadIdx.x; e < (int)mine * C; e += kThreads) {
+        const int p = e / C, t = e - p * C;
+        out[(int64_t)(base + p) * C + t] = rs.blk[p] * C + t;
+    }
+    if (rank == cl - 1) {
+        // the tail tokens after the kept blocks, the padding, the count
+        const int tail0 = n_cb * C, n_out = K * C + (n_vis - tail0);
+        const int cap = (top_k / C) * C + C - 1;
+        for (int i = threadIdx.x; i < n_vis - tail0; i += kThreads) out[K * C + i] = tail0 + i;
+        for (int i = n_out + threadIdx.x; i < cap; i += kThreads) out[i] = -1;
+        if (threadIdx.x == 0 && n_sel) n_sel[r] = n_out;
+    }
 }
 
 template <typename T, int HH>
