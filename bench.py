@@ -272,9 +272,11 @@ def rooflines(wl, step, ms, hbm, bf16, peak_kind):
     elif C > 1:
         n_cb = sum(n // C for n in wl.n_kv_host)
         nbytes = n_cb * (wl.d * 4 + 4) + B * wl.H * (wl.d * q_bytes + 4)
-        # the step also re-pools the newest block of every sequence (idx_block_pool_update)
-        nbytes += wl.B * (C * wl.d * wl.k_idx.element_size() + wl.d * 4)
-        r["score"] = hbm_line("idx_block_pool_update + idx_score (pooled keys)", nbytes, ms["score"])
+        # the step also re-pools the newest block of every sequence and writes the selection; one call
+        # (idx_block_score_topk: pool update + pooled-key scores + block select)
+        nbytes += wl.B * (C * wl.d * wl.k_idx.element_size() + wl.d * 4) + sum(n_sel) * 4
+        r["score"] = hbm_line("idx_block_score_topk (pool update + pooled-key scores + block select, one launch)",
+                              nbytes, ms["score"] + ms["topk"])
     else:
         n_keys = sum(wl.n_kv_host)
         per_key = wl.d * 2 if wl.k8 is None else wl.d + 4
@@ -288,7 +290,7 @@ def rooflines(wl, step, ms, hbm, bf16, peak_kind):
             r["score"] = hbm_line("idx_score (key-cache scan)" if wl.k8 is None else
                                   "idx_score_q8 (int8 key-cache scan)", nbytes, ms["score"])
     n_scores = sum(n_vis) if C <= 1 else sum(n // C for n in n_vis)
-    if not getattr(step, "fused", False):
+    if not getattr(step, "fused", False) and C <= 1:
         r["topk"] = hbm_line("idx_topk", n_scores * 4 + sum(n_sel) * 4, ms["topk"])
     Hq, dk = wl.q_attn.shape[1], wl.q_attn.shape[-1]
     if wl.v_attn is None:
