@@ -1046,6 +1046,8 @@ def _block_step_case(name):
         H = 8
     elif name == "rows_200":           # more rows than SMs: one CTA per row
         n_kv = [4096 - 8 * (s % 7) for s in range(200)]
+    elif name == "paged_raw":          # the raw keys in shuffled pages of 64 rows
+        n_kv = [5000, 32768, 64, 20000]
     B, n = len(n_kv), max(n_kv)
     q = torch.randn(B, H, 128, generator=g).to(torch.bfloat16)
     w = torch.randn(B, H, generator=g) / math.sqrt(H)
@@ -1054,7 +1056,7 @@ def _block_step_case(name):
 
 
 @pytest.mark.parametrize("name", ["decode16", "ragged_full", "stale_f16_64heads", "f32_12heads",
-                                  "8heads_three_calls", "rows_200"])
+                                  "8heads_three_calls", "rows_200", "paged_raw"])
 def test_block_score_topk_equals_the_three_calls(name):
     # pool update + pooled-key score + block select in one call: the pooled cache, the block scores
     # and the selection bit for bit those of idx_block_pool_update, idx_score and idx_topk
@@ -1064,6 +1066,9 @@ def test_block_score_topk_equals_the_three_calls(name):
     batch = L.Batch(_i32(n_kv), 1, n, kv_seq_stride=n)
     pool_batch = L.Batch(_i32(n_kv), 1, n, kv_seq_stride=ps)
     qd, wd, kd = q.to(DEV), w.to(DEV), k.to(DEV)
+    if name == "paged_raw":
+        kd, table = _page(torch.Generator().manual_seed(5), [kd[b * n:b * n + n_kv[b]] for b in range(B)], 64)
+        batch = L.Batch(_i32(n_kv), 1, n, page_table=table, page_size=64)
     pooled0 = L.idx_block_pool(kd, batch, C, pool_seq_stride=ps)
     n_cb = [x // C for x in n_kv]
     n_pooled = stale_pos = None
