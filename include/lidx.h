@@ -280,7 +280,7 @@ idx_status idx_topk(const float* scores, int64_t score_row_stride, idx_batch bat
  * message: block keys are the mean of the block's raw keys, a query keeps its
  * best floor(top_k/C) complete blocks and the tail; the pooled keys persist
  * across decode steps, llama-memory-hybrid-idx.h).  Decode rows
- * (n_q_per_seq 1) with 9 to 64 heads and at most 512 blocks per row run as
+ * (n_q_per_seq 1) with 9 to 64 heads and at most 1024 blocks per row run as
  * one launch (a cluster of CTAs per row: each re-pools and scores its share of
  * the row's blocks, the first ranks them); other shapes run the three calls.
  *   q, w, n_heads, head_dim   as idx_score; k_raw, k_dtype, k_row_stride,

@@ -23,7 +23,7 @@
 namespace lidx {
 namespace {
 
-constexpr int kThreads = 512;   // the block rank's CTA size: rows of at most 512 blocks
+constexpr int kThreads = 512;
 constexpr int kMaxCl = 8;
 constexpr int kPartFloats = 1024;             // pool partial sums: (128 / (d*size/16)) * d = 2048 / size
 
@@ -218,8 +218,8 @@ cudaError_t launch_block_score_topk(const void* q, int q_dtype, const float* w, 
                                     int64_t pool_seq_stride, int top_k, float* scores, int64_t score_row_stride,
                                     int32_t* idx, int64_t idx_row_stride, int32_t* n_sel, cudaStream_t st) {
     // the pooled-key scorer's split path (H in [9, 64]: 16 to 64 padded heads), one query row per
-    // sequence, at most 512 blocks per row, d within the shared-memory plan
-    if (g.T != 1 || C < 2 || H < 9 || H > 64 || d < 1 || d > 256 || g.max_n_kv / C > kThreads ||
+    // sequence, at most blk::kRankMax blocks per row, d within the shared-memory plan
+    if (g.T != 1 || C < 2 || H < 9 || H > 64 || d < 1 || d > 256 || g.max_n_kv / C > blk::kRankMax ||
         g.max_n_kv / C < 1 || g.B < 1)
         return cudaErrorNotSupported;
     switch (k_dtype) {

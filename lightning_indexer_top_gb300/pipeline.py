@@ -150,8 +150,8 @@ class SparseAttentionStep:
         n = 3 + combine   # score, select, attend (+ split combine)
         if wl.block_size > 1:
             # pool update + pooled-key scores + block select: one launch for decode rows of 9-64 heads and
-            # at most 512 blocks, else three
-            one = wl.T == 1 and 9 <= wl.H <= 64 and wl.max_n_kv // wl.block_size <= 512
+            # at most 1024 blocks, else three
+            one = wl.T == 1 and 9 <= wl.H <= 64 and wl.max_n_kv // wl.block_size <= 1024
             return (1 if one else 3) + n - 2 + (2 if self.q_rot is not None else 0)
         if self.fused:
             # fused select: one kernel for rows up to 16384 keys, else bound, filter, finish

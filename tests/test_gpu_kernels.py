@@ -1036,7 +1036,7 @@ def _block_step_case(name):
     H, kdt, mode, stale = 32, torch.bfloat16, "update", None
     n_kv = [32768 - 4 * s for s in range(16)]
     if name == "ragged_full":          # blocks of one key row short, empty rows, dense rows, a full pooling
-        n_kv, mode = [20000, 63, 0, 64, 2111, 2112, 2175, 32768], "full"
+        n_kv, mode = [20000, 63, 0, 64, 2111, 2112, 2175, 65536], "full"
     elif name == "stale_f16_64heads":  # edits re-pool from the stale block on
         H, kdt, stale = 64, torch.float16, [100, 2 ** 31 - 1, 0, 30000, 5000, -1, 64, 32767]
         n_kv = [32768, 32000, 20000, 32768, 8000, 4096, 128, 32768]
