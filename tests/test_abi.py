@@ -29,7 +29,7 @@ def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("idx_score", "idx_score_q8", "idx_quantize_rows", "idx_block_pool", "idx_block_pool_update", "idx_topk", "sparse_attn_decode", "sparse_attn_prefill",
               "idx_hadamard", "idx_workspace_size", "idx_last_error", "idx_device_status", "idx_score_topk",
-              "sparse_decode_step", "sparse_decode_step_fused", "sparse_attn_decode_noalloc"):
+              "sparse_decode_step", "sparse_decode_step_fused", "sparse_attn_decode_noalloc", "idx_block_score_topk"):
         assert n in names
 
 
@@ -86,6 +86,30 @@ def test_host_validation_rejects_bad_arguments(lib):
                                   1.0, None, L.IDX_F32, None, 0, None) == L.IDX_ERR_INVALID_ARG
     assert lib.sparse_attn_decode(None, L.IDX_BF16, 8, 1, 576, 512, None, None, 576, 0, 0, b, None, 16, None,
                                   float("nan"), None, L.IDX_F32, None, 0, None) == L.IDX_ERR_INVALID_ARG
+
+
+def test_block_score_topk_host_validation(lib):
+    # the one-call block indexer reports the three calls' argument errors, found on the host before any
+    # launch: block_size < 1 and a pooled stride below max_n_kv / C (the pool's checks, made first)
+    b = _batch()
+    args = dict(q=None, q_dtype=L.IDX_BF16, w=None, H=32, d=128, k=None, k_dtype=L.IDX_BF16, ks=128, kr=0, b=b,
+                n_pooled=None, stale=None, C=64, pooled=None, ps=16, top_k=2048, scores=None, ss=16, idx=None,
+                istride=2048 + 63, n_sel=None, stream=None)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.idx_block_score_topk(a["q"], a["q_dtype"], a["w"], a["H"], a["d"], a["k"], a["k_dtype"], a["ks"],
+                                        a["kr"], a["b"], a["n_pooled"], a["stale"], a["C"], a["pooled"], a["ps"],
+                                        a["top_k"], a["scores"], a["ss"], a["idx"], a["istride"], a["n_sel"],
+                                        a["stream"])
+    assert call(C=0) == L.IDX_ERR_INVALID_ARG
+    assert b"block_size" in lib.idx_last_error()
+    wide = L._Batch(1, 1, ctypes.c_void_p(16), None, 4096, None, 4096)
+    assert call(b=wide, ps=8) == L.IDX_ERR_INVALID_ARG
+    assert b"pool_seq_stride" in lib.idx_last_error()
+    assert call(k_dtype=7) == L.IDX_ERR_INVALID_ARG
+    # an empty batch is a no-op
+    assert call(b=L._Batch(0, 1, None, None, 0, None, 0)) == L.IDX_OK
 
 
 def test_empty_batch_is_a_no_op(lib):
