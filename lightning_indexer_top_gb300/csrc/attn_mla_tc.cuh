@@ -575,7 +575,11 @@ __device__ __forceinline__ void mla_run(const MlaSmem& sm, uint32_t tmem, uint32
                     for (int i = 0; i < 32; ++i) v[i] = 0.f;
                 }
                 if (out_dtype == IDX_BF16) {
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + base + cb * 32);
+                    // the warp's 32 heads x 32 columns pass through shared memory (the value-tile ring is
+                    // idle once every PV MMA completed; rows of 80 bytes, conflict-free 16-byte stores), so
+                    // that each store instruction writes eight heads' 64-byte row segments whole instead
+                    // of 32 scattered 16-byte pieces
+                    uint8_t* tw = xtiles + warp * (32 * 80);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint4 pk;
@@ -587,8 +591,17 @@ __device__ __forceinline__ void mla_run(const MlaSmem& sm, uint32_t tmem, uint32
                         pk.y = *reinterpret_cast<uint32_t*>(&a1);
                         pk.z = *reinterpret_cast<uint32_t*>(&a2);
                         pk.w = *reinterpret_cast<uint32_t*>(&a3);
-                        dst[q4] = pk;
+                        *reinterpret_cast<uint4*>(tw + lane * 80 + q4 * 16) = pk;
                     }
+                    __syncwarp();
+                    __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out) + (u.r * kHq + quad * 32) * (int64_t)kDv + cb * 32;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int rr = 8 * j + (lane >> 2), ch = lane & 3;
+                        *reinterpret_cast<uint4*>(ob + (int64_t)rr * kDv + ch * 8) =
+                            *reinterpret_cast<const uint4*>(tw + rr * 80 + ch * 16);
+                    }
+                    __syncwarp();
                 } else {
                     float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + base + cb * 32);
 #pragma unroll
