@@ -177,15 +177,27 @@ cudaError_t launch_t(const void* q, int q_dtype, const float* w, int H, int d, c
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     // the most CTAs per row (a power of two, at most kMaxCl, at least 32 blocks each) whose clusters
-    // are all resident at once
+    // are all resident at once (the occupancy query runs once per shape and device)
+    static thread_local int64_t memo_rows = -1;
+    static thread_local int memo_blocks = -1, memo_dev = -1, memo_cl = 1;
+    int dev = 0;
+    cudaGetDevice(&dev);
     int cl = kMaxCl;
-    while (cl > 1 && max_blocks < cl * 32) cl >>= 1;
-    for (; cl > 1; cl >>= 1) {
-        attr[0].val.clusterDim.x = (unsigned)cl;
-        cfg.gridDim = dim3((unsigned)(n_rows * cl));
-        cfg.numAttrs = 1;
-        int active = 0;
-        if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) == cudaSuccess && active >= n_rows) break;
+    if (memo_rows == n_rows && memo_blocks == max_blocks && memo_dev == dev) {
+        cl = memo_cl;
+    } else {
+        while (cl > 1 && max_blocks < cl * 32) cl >>= 1;
+        for (; cl > 1; cl >>= 1) {
+            attr[0].val.clusterDim.x = (unsigned)cl;
+            cfg.gridDim = dim3((unsigned)(n_rows * cl));
+            cfg.numAttrs = 1;
+            int active = 0;
+            if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) == cudaSuccess && active >= n_rows) break;
+        }
+        memo_rows = n_rows;
+        memo_blocks = max_blocks;
+        memo_dev = dev;
+        memo_cl = cl;
     }
     attr[0].val.clusterDim.x = (unsigned)cl;
     cfg.gridDim = dim3((unsigned)(n_rows * cl));
