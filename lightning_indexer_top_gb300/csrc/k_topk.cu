@@ -954,6 +954,41 @@ __global__ void __launch_bounds__(kMapThreads, 1) topk_mc_finish_kernel(const fl
     }
 #pragma unroll 1
     for (int round = round0; round < 3; ++round) {
+        if (round == 2 && sh.hist[sh.bin] <= 64u) {
+            // the last round sees only the keys sharing T's top 22 bits (the previous round's bin
+            // count, at most 64 here): T is the need-th largest of them, found by ranking them
+            // directly - the same T and count above it as the 1024-bin histogram gives
+            uint32_t* small = sh.hist;
+            __syncthreads();   // (every thread has read the bin count)
+            if (threadIdx.x == 0) sh.cand_n = 0u;
+            __syncthreads();
+            for (uint32_t i = threadIdx.x; i < n_cand; i += kMapThreads) {
+                const uint32_t key = sh.cand_key[i];
+                if ((key & mask) == prefix) {
+                    const uint32_t slot = atomicAdd(&sh.cand_n, 1u);
+                    if (slot < 64u) small[slot] = key;
+                }
+            }
+            __syncthreads();
+            const uint32_t m = min(sh.cand_n, 64u);
+            if (threadIdx.x < m) {
+                const uint32_t key = small[threadIdx.x];
+                uint32_t gt = 0, ge = 0;
+                for (uint32_t j = 0; j < m; ++j) {
+                    gt += small[j] > key ? 1u : 0u;
+                    ge += small[j] >= key ? 1u : 0u;
+                }
+                if (gt < need && need <= ge) {   // (keys equal to T all write the same values)
+                    sh.bin = key & 1023u;
+                    sh.above = gt;
+                }
+            }
+            __syncthreads();
+            prefix |= sh.bin;
+            mask = 0xffffffffu;
+            need -= sh.above;
+            break;
+        }
         map_cand_hist(sh, n_cand, prefix, mask, shifts[round], bitsv[round]);
         map_find_bin(1 << bitsv[round], need, sh);
         prefix |= sh.bin << shifts[round];
