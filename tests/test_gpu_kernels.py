@@ -1099,3 +1099,27 @@ def test_block_score_topk_equals_the_three_calls(name):
     for r in range(0, B, max(1, B // 8)):
         ref = O.block_select(sh[r, :n_cb[r]], n_kv[r], top_k, C)
         assert int(ns_one[r]) == len(ref) and i_one[r, :len(ref)].tolist() == list(ref), r
+
+
+@pytest.mark.parametrize("planted", [0, 150])
+def test_topk_long_rows_threshold_ties(planted):
+    # few long rows (the multi-CTA select: sampled bound, filter, finish): the finish ranks the keys that
+    # share the threshold's top 22 bits directly when they are few, and by a histogram when many are
+    # equal (planted copies of the top_k-th score)
+    g = torch.Generator().manual_seed(4242 + planted)
+    rows, n, top_k = 4, 131072, 2048
+    s = torch.randn(rows, n, generator=g)
+    if planted:
+        for r in range(rows):
+            t = torch.sort(s[r], descending=True).values[top_k - 1]
+            pos = torch.randperm(n, generator=g)[:planted]
+            s[r, pos] = t
+    n_kv = [n, n - 1000, n - 77, n]
+    batch = L.Batch(_i32(n_kv), 1, n, kv_seq_stride=0)
+    ws = torch.empty(L.idx_workspace_size(L.IDX_OP_TOPK, rows, n, top_k), device=DEV, dtype=torch.uint8)
+    idx, n_sel = L.idx_topk(s.to(DEV), batch, top_k, workspace=ws)
+    torch.cuda.synchronize()
+    assert L.idx_device_status(reset=True) == 0
+    for r in range(rows):
+        ref = O.topk_select(s[r].numpy(), n_kv[r], top_k)
+        assert int(n_sel[r]) == len(ref) and idx[r, :len(ref)].cpu().tolist() == ref.tolist(), r
