@@ -925,18 +925,6 @@ __global__ void __launch_bounds__(kMapThreads, 1) topk_mc_finish_kernel(const fl
         select_row<false, kMapThreads>(s, n, top_k, 1, out, n_sel ? n_sel + r : nullptr, gsh);
         return;
     }
-    const int nwords = (n + 31) >> 5;
-    for (int i = threadIdx.x; i < nwords; i += kMapThreads) {
-        sh.sel[i] = 0u;
-        sh.eq[i] = 0u;
-    }
-    const uint64_t* cand = L.cand + r * (int64_t)kMcCandCap;
-    for (uint32_t i = threadIdx.x; i < n_cand; i += kMapThreads) {
-        const uint64_t kp = cand[i];
-        sh.cand_key[i] = (uint32_t)(kp >> 32);
-        sh.cand_pos[i] = (int32_t)(uint32_t)kp;
-    }
-    __syncthreads();
     // exact top K among the candidates: three radix rounds over the full keys; on the fused path
     // the first round's bin and the count above it are known from the row's histogram
     uint32_t need = (uint32_t)K, prefix = 0u, mask = 0u;
@@ -951,6 +939,31 @@ __global__ void __launch_bounds__(kMapThreads, 1) topk_mc_finish_kernel(const fl
             need -= b & 0x1fffffu;
             round0 = 1;
         }
+    }
+    const int nwords = (n + 31) >> 5;
+    for (int i = threadIdx.x; i < nwords; i += kMapThreads) {
+        sh.sel[i] = 0u;
+        sh.eq[i] = 0u;
+    }
+    // with the first bin known, the next round's histogram is counted while the candidates load
+    if (round0 == 1)
+        for (int i = threadIdx.x; i < 2048; i += kMapThreads) sh.hist[i] = 0u;
+    __syncthreads();
+    const uint64_t* cand = L.cand + r * (int64_t)kMcCandCap;
+    for (uint32_t i = threadIdx.x; i < n_cand; i += kMapThreads) {
+        const uint64_t kp = cand[i];
+        const uint32_t key = (uint32_t)(kp >> 32);
+        sh.cand_key[i] = key;
+        sh.cand_pos[i] = (int32_t)(uint32_t)kp;
+        if (round0 == 1 && (key & mask) == prefix) atomicAdd(&sh.hist[(key >> 10) & 2047u], 1u);
+    }
+    __syncthreads();
+    if (round0 == 1) {
+        map_find_bin(2048, need, sh);
+        prefix |= sh.bin << 10;
+        mask |= 2047u << 10;
+        need -= sh.above;
+        round0 = 2;
     }
 #pragma unroll 1
     for (int round = round0; round < 3; ++round) {
