@@ -806,7 +806,8 @@ __device__ __forceinline__ uint32_t hist_bound(const uint32_t* hrow, int n, int 
     return *sb;
 }
 
-__global__ void __launch_bounds__(kMcThreads) topk_hist_filter_kernel(const float* scores,
+// (at most 40 registers: six CTAs per SM, so a batch's 1024 chunk CTAs take fewer waves)
+__global__ void __launch_bounds__(kMcThreads, 6) topk_hist_filter_kernel(const float* scores,
                                                                       int64_t score_row_stride,
                                                                       const uint32_t* hist, Geom g, int top_k,
                                                                       McLayout L, int chunk) {
